@@ -1,0 +1,255 @@
+/*
+ * q4w.h -- C ABI of the q4_0 weight-only int4 decode kernels (GB300, sm_103a).
+ *
+ * One shared library, libq4w.so.  Plain pointers and sizes only; no C++ types
+ * or exceptions cross this boundary.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Every array argument is DEVICE memory owned by the caller, unless
+ *   the argument's comment says "host".  The library allocates nothing and
+ *   frees nothing in any call; scratch space comes from the caller through a
+ *   (workspace pointer, size) pair sized by q4_workspace_bytes().
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   Work is enqueued asynchronously; nothing is synchronised.  Results are
+ *   ready when the stream reaches that point.
+ * Device.  Calls run on the current CUDA device, which must be compute
+ *   capability 10.3 (GB300); anything else returns Q4_ERR_ARCH.
+ * Errors.  Each call returns a q4_status.  Argument checks happen before any
+ *   launch, so a non-zero status from a check means nothing was enqueued.
+ *   q4_last_error() returns a thread-local message naming the offending
+ *   argument; q4_status_string() names the code.
+ * Alignment.  Every device pointer must be 16-byte aligned (Q4_ERR_ALIGN).
+ *
+ * q4_0 weight layout ("the ggml q4_0 grid", per-block-32 symmetric int4; see
+ * "visible-cx/gemma-4-E2B-CoreAI", Provenance, and "Gemma 4 E2B (text
+ * decoder) - Core AI", QAT weights), planar, row-major, for a matrix of N
+ * rows and K columns (K a multiple of 32):
+ *   codes  uint8  [N][K/2]   byte j of a row holds column 2j in its low nibble
+ *                            and column 2j+1 in its high nibble (low nibble
+ *                            first, "Gemma-4 E2B mobile mixed-bit QAT weights",
+ *                            the decode recipe);
+ *   scales uint16 [N][K/32]  IEEE fp16 bit patterns, one per 32-column block.
+ *   The weight value is scale * (code - 8): unsigned code minus midpoint
+ *   ("Gemma-4 E2B mobile mixed-bit QAT weights", P6 DONE; the affine form
+ *   scale*code - 8*scale of its receiving-end design).
+ * Activations named *_f16 are uint16 arrays of IEEE fp16 bit patterns.
+ */
+#ifndef Q4W_H_
+#define Q4W_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* q4_stream_t; /* same handle as cudaStream_t */
+
+typedef enum q4_status {
+  Q4_OK = 0,
+  Q4_ERR_NULL = 1,        /* a required pointer is NULL */
+  Q4_ERR_SHAPE = 2,       /* a size is out of range or inconsistent */
+  Q4_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned */
+  Q4_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than required */
+  Q4_ERR_ARCH = 5,        /* the current device is not compute capability 10.3 */
+  Q4_ERR_CUDA = 6,        /* a CUDA runtime call failed (message has the CUDA error) */
+  Q4_ERR_TIMEOUT = 7,     /* a bounded device-side wait ran out */
+  Q4_ERR_DEVICE = 8       /* a device-side check failed (see the entry point) */
+} q4_status;
+
+/* Operation ids for q4_workspace_bytes(). */
+typedef enum q4_op {
+  Q4_OP_GEMV = 0,
+  Q4_OP_GEMM_CHUNK = 1,
+  Q4_OP_PLE = 2,
+  Q4_OP_LMHEAD = 3,
+  Q4_OP_DECODE_PASS = 4
+} q4_op;
+
+/* ---------------------------------------------------------------------- */
+/* Quantise (setup, not part of a decode step).                            */
+/* ---------------------------------------------------------------------- */
+/* q4_quantize: fp32 W [N][K] -> q4_0 codes [N][K/2] + fp16 scales [N][K/32].
+ * Per 32-column block: m = the element of largest |w| (the first one in
+ * column order on ties); d = m / -8 in fp32 (exact); code = clamp(round(w/d)
+ * + 8, 0, 15) with an IEEE fp32 quotient and rounding half away from zero;
+ * the stored scale is d rounded to fp16 (nearest-even).  An all-zero block
+ * stores scale +0 and codes 8.  Source: "visible-cx/gemma-4-E2B-CoreAI",
+ * Provenance (int4 per-block-32, q4_0 grid; rounding happens at export);
+ * "Gemma 4 E2B (text decoder) - Core AI", QAT weights (per-block-32 absmax
+ * symmetric int4; --lin-sym is the literal grid).
+ *   N >= 1, K >= 32, K % 32 == 0.
+ *   err: optional device int32; set to 1 if a block had a non-finite weight
+ *   or a scale beyond the fp16 range (those blocks are stored as zero).  The
+ *   word is only ever set, never cleared, by the kernel.              */
+int q4_quantize(const float* W, int N, int K, uint8_t* codes, uint16_t* scales,
+                int32_t* err, q4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* S=1 decode GEMV ("main", one token per call).                           */
+/* ---------------------------------------------------------------------- */
+/* q4_gemv: y[b][n] = sum_k scale[n][k/32] * (code[n][k] - 8) * x[b][k],
+ * fp32 accumulation, for b < batch.  Source: "visible-cx/gemma-4-E2B-CoreAI",
+ * Provenance (main = S=1 decode); "Gemma-4 E2B mobile mixed-bit QAT weights",
+ * the S=4 verify ("weights read once for 4 rows") for batch > 1.
+ *   codes/scales: q4_0 matrix [N][K]; x_f16: [batch][K]; y: f32 [batch][N].
+ *   1 <= batch <= 8; N >= 1; K % 32 == 0, 32 <= K <= 32768.
+ *   Deterministic: the same inputs give the same bits on every call.
+ *   ws/ws_bytes: unused (may be NULL/0).                                    */
+int q4_gemv(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16,
+            float* y, int N, int K, int batch, void* ws, size_t ws_bytes,
+            q4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* S=64 chunked-prefill GEMM ("prefill", static query width 64).           */
+/* ---------------------------------------------------------------------- */
+/* q4_gemm_chunk: Y[t][n] = sum_k bf16(scale*(code-8))[n][k] * bf16(x[t][k]),
+ * fp32 accumulation on the tensor cores.  Both tiles are rounded to bf16
+ * (nearest-even) before the products.  Source: "visible-cx/gemma-4-E2B-
+ * CoreAI", Provenance and Performance (prefill serves full-width 64-token
+ * chunks only; the remainder goes through main).
+ *   X_f16: [M][K] with M == 64; Y: f32 [M][N]; codes/scales [N][K].
+ *   N % 128 == 0, K % 64 == 0, 64 <= K <= 32768.
+ *   ws/ws_bytes: unused (may be NULL/0).                                   */
+int q4_gemm_chunk(const uint8_t* codes, const uint16_t* scales, const uint16_t* X_f16,
+                  float* Y, int M, int N, int K, void* ws, size_t ws_bytes,
+                  q4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Per-Layer-Embedding gather + projection.                                */
+/* ---------------------------------------------------------------------- */
+/* ple_gather_project: for each of S tokens t with id v = ids[t]:
+ *   g[t][j]   = (float(table[v][j]) * row_scale[v]) * embed_scale   (fp32)
+ *   p[t][j]   = sum_d proj[j][d] * float(hidden[t][d])             (fp32)
+ *   n[t][c*ld+i] = p[t][c*ld+i] * rsqrt(mean_i p[t][c*ld+i]^2 + eps) * norm_w[i]
+ *   out[t][j] = n[t][j] + g[t][j]                                  (f32)
+ * for j < L*ld, chunks c < L.  Source: "visible-cx/gemma-4-E2B-CoreAI", The
+ * PLE gather-table sidecar (int8 table [V][8960] + per-row f32 scale, x16.0,
+ * proj.f32 [8960][1536], proj_norm.f32 [256]); "Gemma-4 E2B mobile mixed-bit
+ * QAT weights", P2 DONE (35 layer-major blocks of 256 concatenated on axis 1).
+ *   ids: int32 [S]; table: int8 [V][L*ld]; row_scale: f32 [V];
+ *   proj: f32 [L*ld][D]; hidden_f16: [S][D]; norm_w: f32 [ld];
+ *   out: f32 [S][L*ld]; gathered_opt: int8 [S][L*ld] copy of the table rows,
+ *   or NULL.  1 <= S <= 4096; ld == 256; 1 <= L <= 256; D % 32 == 0,
+ *   32 <= D <= 32768; V >= 1.  An id outside [0, V) writes zeros for that
+ *   token and sets the optional device int32 *err to 1 (never cleared by
+ *   the kernel).                                                          */
+int ple_gather_project(const int32_t* ids, int S, const int8_t* table,
+                       const float* row_scale, int V, int L, int ld, float embed_scale,
+                       const float* proj, const uint16_t* hidden_f16, int D,
+                       const float* norm_w, float eps, float* out, int8_t* gathered_opt,
+                       int32_t* err, q4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* LM head + softcap + argmax.                                             */
+/* ---------------------------------------------------------------------- */
+/* lmhead_softcap_argmax: for each batch row b:
+ *   z[n] = sum_k scale[n][k/32]*(code[n][k]-8)*h[b][k]   (fp32)
+ *   s[n] = tanh(z[n] / cap) * cap
+ *   idx[b] = argmax_n s[n] (lowest index among equal z), top1[b] = s[idx],
+ *   top2[b] = the largest s over the other rows.
+ * The logits are not read back unless logits_opt is given.  Source: "Gemma 4
+ * E2B (text decoder) - Core AI", Signature features (final logit softcap
+ * tanh(z/30)*30) and What it took (fused head with a two-level in-kernel
+ * argmax, no logit readback).
+ *   h_f16: [b][K]; idx int32 [b]; top1, top2 f32 [b];
+ *   logits_opt: f32 [b][V] softcapped logits, or NULL.
+ *   1 <= b <= 8; V >= 2; K % 32 == 0, 32 <= K <= 32768; cap > 0.
+ *   ws: q4_workspace_bytes(Q4_OP_LMHEAD, V, K, b) bytes; its contents on
+ *   entry do not matter.  Calls that share one ws must not overlap.       */
+int lmhead_softcap_argmax(const uint8_t* codes, const uint16_t* scales,
+                          const uint16_t* h_f16, int b, int V, int K, float cap,
+                          int32_t* idx, float* top1, float* top2, float* logits_opt,
+                          void* ws, size_t ws_bytes, q4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Decode weight pass over a stack of layers (S=1).                        */
+/* ---------------------------------------------------------------------- */
+typedef struct q4_matrix {
+  const uint8_t* codes;    /* device, [rows][cols/2] */
+  const uint16_t* scales;  /* device, [rows][cols/32] */
+} q4_matrix;
+
+typedef struct q4_layer {
+  int q_rows;      /* rows of W_q = cols of W_o (e.g. 2048 or 4096) */
+  int kv_rows;     /* rows of W_k and W_v; 0 when the layer shares K/V */
+  int mlp_rows;    /* rows of W_gate and W_up = cols of W_down */
+  q4_matrix q, k, v, o, gate, up, down;   /* k, v ignored when kv_rows == 0 */
+} q4_layer;
+
+/* q4_decode_pass: the weight pass of one decode step over n_layers layers,
+ * hidden size H.  Per layer, with RMSNorm(v) = v * rsqrt(mean(v^2) + eps):
+ *   a = f16(RMSNorm(h));  q = W_q a;  k = W_k a;  v = W_v a;
+ *   o = W_o f16(q);       b = f16(RMSNorm(o));
+ *   g = W_gate b;  u = W_up b;  m = f16(gelu_tanh(g) * u);
+ *   h' = f16(RMSNorm(W_down m))
+ * with fp32 accumulation and fp32 gelu_tanh(x) = 0.5x(1+tanh(sqrt(2/pi)(x +
+ * 0.044715x^3))).  k and v are computed (into the workspace) and not used.
+ * Sources: "Gemma 4 E2B (text decoder) - Core AI", Signature features (35
+ * layers, dual head_dim, KV-sharing, double-wide MLP, RMSNorm weight applied
+ * directly); "Gemma-4 E2B mobile mixed-bit QAT weights", the decode recipe
+ * and P2 progress (shapes) and Speed (fused gate/up with an fp32 tanh GELU).
+ * The exact stage order is this library's synthetic weight-pass workload.
+ *   layers: HOST array of n_layers descriptors (read during the call only);
+ *   h0_f16, h_out_f16: device [H]; 1 <= n_layers <= 256; H % 32 == 0;
+ *   q_rows, mlp_rows % 32 == 0 and in [32, 32768]; kv_rows >= 0.
+ *   ws: q4_workspace_bytes(Q4_OP_DECODE_PASS, H, max(q_rows + 2 kv_rows),
+ *   max(mlp_rows)) bytes.  Every stage is one kernel launch on `stream`
+ *   (programmatic dependent launch between stages); the sequence can be
+ *   captured into a CUDA graph.                                            */
+int q4_decode_pass(const q4_layer* layers, int n_layers, int H, const uint16_t* h0_f16,
+                   uint16_t* h_out_f16, float eps, void* ws, size_t ws_bytes,
+                   q4_stream_t stream);
+
+/* Prologue of one decode-pass stage, exposed for stage tests. */
+typedef enum q4_stage_in {
+  Q4_IN_F16 = 0,          /* x = in (fp16) */
+  Q4_IN_RMS_F16 = 1,      /* x = f16(RMSNorm(in fp16)) */
+  Q4_IN_RMS_F32 = 2,      /* x = f16(RMSNorm(in f32)) */
+  Q4_IN_RMS2_F32 = 3      /* x = f16(RMSNorm(f16(RMSNorm(in f32)))) */
+} q4_stage_in;
+
+/* q4_gemv_stage: one stage of q4_decode_pass as a standalone call, with the
+ * same kernel and launch shape the pass uses.  Up to three q4 matrices with
+ * the same K are applied to one input vector:
+ *   x = prologue(in) per `in_mode`;  y_i = W_i x  (fp32).
+ * pair == 0: matrix i writes out32[i] (f32 [rows_i], may be NULL) and
+ *            out16[i] (fp16 [rows_i], may be NULL).
+ * pair == 1: exactly two matrices (gate, up) with rows_0 == rows_1; writes
+ *            m = f16(gelu_tanh(y_0) * y_1) to out16[0], and y_0 / y_1 to
+ *            out32[0] / out32[1] when those are non-NULL.
+ *   in: device [K] fp16 (Q4_IN_F16, Q4_IN_RMS_F16) or f32 (the others).
+ *   1 <= nmat <= 3; rows_i >= 1; K % 32 == 0, 32 <= K <= 32768.
+ *   Source: as q4_decode_pass.                                             */
+int q4_gemv_stage(const q4_matrix* mats /* host [nmat] */, const int* rows /* host [nmat] */,
+                  int nmat, int K, const void* in, int in_mode, float eps, int pair,
+                  float* const* out32 /* host [nmat] */, uint16_t* const* out16 /* host [nmat] */,
+                  q4_stream_t stream);
+
+/* q4_rmsnorm_f16: out = f16(RMSNorm(in f32 [H])), the last step of the pass.
+ * Source: "Gemma 4 E2B (text decoder) - Core AI", Signature features. */
+int q4_rmsnorm_f16(const float* in, int H, float eps, uint16_t* out_f16, q4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Helpers.                                                                */
+/* ---------------------------------------------------------------------- */
+/* Bytes of workspace an operation needs (0 = none).  Arguments per op:
+ *   Q4_OP_GEMV (N, K, batch), Q4_OP_GEMM_CHUNK (N, K, 64), Q4_OP_PLE (S, D, L),
+ *   Q4_OP_LMHEAD (V, K, b), Q4_OP_DECODE_PASS (H, max q+2kv rows, max mlp).
+ * Depends on the current device's SM count for Q4_OP_LMHEAD; returns 0 when
+ * the current device cannot be queried.                                   */
+size_t q4_workspace_bytes(int op, int a, int b, int c);
+
+const char* q4_status_string(int status);
+const char* q4_last_error(void);   /* thread-local; "" when no error yet */
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int q4_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* Q4W_H_ */

@@ -1,0 +1,307 @@
+// LM head fused with the logit softcap and a two-level argmax.
+//
+// "Gemma 4 E2B (text decoder) - Core AI": the final logits are softcapped as
+// tanh(z/30)*30 (Signature features) and the head is fused with a two-level
+// in-kernel argmax so that no logits are read back (What it took).  tanh is
+// increasing, so the argmax and the runner-up are selected on z and only the
+// two winners are softcapped; the full softcapped logits are written only
+// when the caller asks for them.
+//
+// Level 1: every lane group keeps the top two (z, row) of the rows it
+// computes; the CTA merges them into one partial per batch row in the
+// workspace.  Level 2: the CTA that takes the last ticket of an atomic
+// counter merges all partials (no CTA waits for another).
+#include <climits>
+
+#include "q4w_device.cuh"
+#include "q4w_internal.cuh"
+
+namespace q4w {
+
+struct Top2 {
+  float v1, v2;
+  int i1, i2;
+};
+
+__device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
+  return a > b || (a == b && ia < ib);
+}
+__device__ __forceinline__ void top2_init(Top2& t) {
+  t.v1 = t.v2 = -INFINITY;
+  t.i1 = t.i2 = INT_MAX;
+}
+__device__ __forceinline__ void top2_insert(Top2& t, float v, int i) {
+  if (better(v, i, t.v1, t.i1)) {
+    t.v2 = t.v1;
+    t.i2 = t.i1;
+    t.v1 = v;
+    t.i1 = i;
+  } else if (better(v, i, t.v2, t.i2)) {
+    t.v2 = v;
+    t.i2 = i;
+  }
+}
+__device__ __forceinline__ void top2_merge(Top2& t, const Top2& o) {
+  top2_insert(t, o.v1, o.i1);
+  top2_insert(t, o.v2, o.i2);
+}
+
+constexpr int kMaxBatch = 8;
+constexpr size_t kTicketBytes = 256;
+
+__device__ __forceinline__ Top2 load_cg(const Top2* p) {
+  Top2 t;
+  t.v1 = __ldcg(&p->v1);
+  t.v2 = __ldcg(&p->v2);
+  t.i1 = __ldcg(&p->i1);
+  t.i2 = __ldcg(&p->i2);
+  return t;
+}
+
+// Second level: runs in the CTA that finishes last.
+__device__ void head_finish(const Top2* partials, unsigned* ticket, int B, float cap, int32_t* idx,
+                            float* top1, float* top2) {
+  __shared__ bool last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (threadIdx.x < B) {
+    const int b = threadIdx.x;
+    Top2 t;
+    top2_init(t);
+    for (int c = 0; c < (int)gridDim.x; ++c) top2_merge(t, load_cg(partials + (size_t)c * kMaxBatch + b));
+    idx[b] = t.i1;
+    top1[b] = cap * tanhf(t.v1 / cap);
+    top2[b] = cap * tanhf(t.v2 / cap);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *ticket = 0u;
+}
+
+// b == 1: lane groups own R rows each, like the decode GEMV stages.
+template <int LPR, int R>
+__global__ void __launch_bounds__(kThreads) head_rows_kernel(const uint8_t* __restrict__ codes,
+                                                            const __half* __restrict__ scales,
+                                                            const __half* __restrict__ h, int V, int K,
+                                                            float cap, float* __restrict__ logits,
+                                                            Top2* partials, unsigned* ticket,
+                                                            int32_t* idx, float* top1, float* top2,
+                                                            int tasks) {
+  extern __shared__ float4 dyn_smem4[];
+  float* xs = reinterpret_cast<float*>(dyn_smem4);
+  __shared__ Top2 st[kThreads];
+  const int nb = K >> 5;
+  for (int k = threadIdx.x; k < K; k += kThreads) xs_store(xs, k, __half2float(h[k]));
+  __syncthreads();
+  xs_biases(xs, nb);
+  __syncthreads();
+
+  constexpr int G = 32 / LPR;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane / LPR, li = lane % LPR;
+  const size_t row_bytes = (size_t)(K >> 1);
+  Top2 best;
+  top2_init(best);
+
+  for (int task = blockIdx.x * kWarps + warp; task < tasks; task += gridDim.x * kWarps) {
+    const int rbase = (task * G + g) * R;
+    float acc[R];
+    bool ok[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      acc[r] = 0.f;
+      ok[r] = rbase + r < V;
+    }
+#pragma unroll 2
+    for (int j = li; j < nb; j += LPR) {
+      uint4 c[R];
+      float d[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (ok[r]) {
+          c[r] = ld_stream16(codes + (size_t)(rbase + r) * row_bytes + 16 * j);
+          d[r] = ld_scale(scales + (size_t)(rbase + r) * nb + j);
+        } else {
+          c[r] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+          d[r] = 0.f;
+        }
+      }
+      float4 xv[8];
+      float bias;
+      load_xblock(xs, j, xv, bias);
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[r] = fmaf(d[r], q4_block_dot(c[r], xv, bias), acc[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int o = LPR / 2; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+    if (li == 0) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (!ok[r]) continue;
+        top2_insert(best, acc[r], rbase + r);
+        if (logits) logits[rbase + r] = cap * tanhf(acc[r] / cap);
+      }
+    }
+  }
+  st[threadIdx.x] = best;   // non-leaders hold the empty state
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Top2 t;
+    top2_init(t);
+    for (int i = 0; i < kThreads; ++i) top2_merge(t, st[i]);
+    partials[(size_t)blockIdx.x * kMaxBatch] = t;
+  }
+  head_finish(partials, ticket, 1, cap, idx, top1, top2);
+}
+
+// b >= 2: one warp per row, lane group g serves batch rows g, g+G, ...
+template <int LPR>
+__global__ void __launch_bounds__(kThreads) head_batched_kernel(const uint8_t* __restrict__ codes,
+                                                               const __half* __restrict__ scales,
+                                                               const __half* __restrict__ h, int B,
+                                                               int V, int K, float cap,
+                                                               float* __restrict__ logits,
+                                                               Top2* partials, unsigned* ticket,
+                                                               int32_t* idx, float* top1,
+                                                               float* top2) {
+  extern __shared__ float4 dyn_smem4[];
+  float* xs = reinterpret_cast<float*>(dyn_smem4);
+  __shared__ Top2 st[kWarps][kMaxBatch];
+  const int nb = K >> 5;
+  const int xstride = nb * kXStride;
+  for (int i = threadIdx.x; i < B * K; i += kThreads) {
+    const int b = i / K, k = i - b * K;
+    xs_store(xs + b * xstride, k, __half2float(h[i]));
+  }
+  __syncthreads();
+  for (int b = 0; b < B; ++b) xs_biases(xs + b * xstride, nb);
+  __syncthreads();
+
+  constexpr int G = 32 / LPR;
+  constexpr int T = (kMaxBatch + G - 1) / G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane / LPR, li = lane % LPR;
+  const size_t row_bytes = (size_t)(K >> 1);
+  Top2 best[T];
+#pragma unroll
+  for (int t = 0; t < T; ++t) top2_init(best[t]);
+
+  for (int row = blockIdx.x * kWarps + warp; row < V; row += gridDim.x * kWarps) {
+    const uint8_t* cp = codes + (size_t)row * row_bytes;
+    const __half* sp = scales + (size_t)row * nb;
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      if (t * G >= B) break;   // uniform across the warp
+      const int b = g + G * t;
+      const bool okb = b < B;
+      float acc = 0.f;
+      for (int j = li; j < nb; j += LPR) {
+        const uint4 c = ld_stream16(cp + 16 * j);
+        const float d = ld_scale(sp + j);
+        float4 xv[8];
+        float bias;
+        load_xblock(xs + (okb ? b : 0) * xstride, j, xv, bias);
+        acc = fmaf(d, q4_block_dot(c, xv, bias), acc);
+      }
+#pragma unroll
+      for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (li == 0 && okb) {
+        top2_insert(best[t], acc, row);
+        if (logits) logits[(size_t)b * V + row] = cap * tanhf(acc / cap);
+      }
+    }
+  }
+  if (li == 0) {
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      const int b = g + G * t;
+      if (b < B) st[warp][b] = best[t];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < B) {
+    Top2 t;
+    top2_init(t);
+    for (int w = 0; w < kWarps; ++w) top2_merge(t, st[w][threadIdx.x]);
+    partials[(size_t)blockIdx.x * kMaxBatch + threadIdx.x] = t;
+  }
+  head_finish(partials, ticket, B, cap, idx, top1, top2);
+}
+
+static int lpr_for(int nb) {
+  int l = 32;
+  while (l > 1 && nb % l) l >>= 1;
+  return l;
+}
+
+static int head_grid(const DeviceInfo& dev) { return 2 * dev.sms; }
+
+size_t lmhead_ws_bytes(int V, int K, int b, const DeviceInfo& dev) {
+  (void)V;
+  (void)K;
+  (void)b;
+  return kTicketBytes + (size_t)head_grid(dev) * kMaxBatch * sizeof(Top2);
+}
+
+template <int LPR>
+static cudaError_t launch_head_t(const uint8_t* codes, const __half* scales, const __half* h, int B,
+                                 int V, int K, float cap, int32_t* idx, float* top1, float* top2,
+                                 float* logits, Top2* partials, unsigned* ticket, const DeviceInfo& dev,
+                                 cudaStream_t s) {
+  const int nb = K >> 5;
+  int grid = head_grid(dev);
+  if (B == 1) {
+    constexpr int G = 32 / LPR;
+    constexpr int R = 4;
+    const int tasks = (V + G * R - 1) / (G * R);
+    const int need = (tasks + kWarps - 1) / kWarps;
+    if (grid > need) grid = need;
+    const size_t smem = (size_t)nb * kXStride * sizeof(float);
+    auto k = head_rows_kernel<LPR, R>;
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    k<<<grid, kThreads, smem, s>>>(codes, scales, h, V, K, cap, logits, partials, ticket, idx, top1,
+                                   top2, tasks);
+  } else {
+    const int need = (V + kWarps - 1) / kWarps;
+    if (grid > need) grid = need;
+    const size_t smem = (size_t)B * nb * kXStride * sizeof(float);
+    auto k = head_batched_kernel<LPR>;
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    k<<<grid, kThreads, smem, s>>>(codes, scales, h, B, V, K, cap, logits, partials, ticket, idx, top1,
+                                   top2);
+  }
+  return cudaGetLastError();
+}
+
+int launch_lmhead(const uint8_t* codes, const __half* scales, const __half* h, int b, int V, int K,
+                  float cap, int32_t* idx, float* top1, float* top2, float* logits, void* ws,
+                  const DeviceInfo& dev, cudaStream_t s) {
+  if ((size_t)b * (K >> 5) * kXStride * sizeof(float) > (size_t)200 * 1024)
+    return fail(Q4_ERR_SHAPE, "lmhead: batch %d x K %d does not fit in shared memory", b, K);
+  unsigned* ticket = reinterpret_cast<unsigned*>(ws);
+  Top2* partials = reinterpret_cast<Top2*>(reinterpret_cast<char*>(ws) + kTicketBytes);
+  cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return cuda_fail(e, "lmhead ticket reset");
+  switch (lpr_for(K >> 5)) {
+    case 32: e = launch_head_t<32>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+    case 16: e = launch_head_t<16>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+    case 8: e = launch_head_t<8>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+    case 4: e = launch_head_t<4>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+    case 2: e = launch_head_t<2>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+    default: e = launch_head_t<1>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+  }
+  return e == cudaSuccess ? Q4_OK : cuda_fail(e, "lmhead launch");
+}
+
+}  // namespace q4w

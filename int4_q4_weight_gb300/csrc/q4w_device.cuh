@@ -1,0 +1,141 @@
+// Device-side building blocks shared by the q4_0 GEMV-shaped kernels.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace q4w {
+
+constexpr int kThreads = 256;          // threads per CTA of the GEMV-shaped kernels
+constexpr int kWarps = kThreads / 32;
+constexpr int kXStride = 36;           // floats per 32-column block of x in shared memory:
+                                       // 32 values, the block bias, 3 pad (144 B keeps
+                                       // 8 lanes reading 8 blocks free of bank conflicts)
+
+// ------------------------------------------------------------ PDL hooks ---
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// --------------------------------------------------------------- loads ---
+// 16-byte streaming load of weight codes: read once, keep out of L1.
+__device__ __forceinline__ uint4 ld_stream16(const uint8_t* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float ld_scale(const __half* p) {
+  unsigned short u;
+  asm("ld.global.nc.u16 %0, [%1];" : "=h"(u) : "l"(p));
+  return __half2float(__ushort_as_half(u));
+}
+
+// ------------------------------------------------------ packed fp32 x2 ---
+typedef unsigned long long f2_t;   // two fp32 lanes in one 64-bit register pair
+
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+  f2_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f2_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+  f2_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// ------------------------------------------------- nibble -> float trick ---
+// A 4-bit code n placed in mantissa bits [15,19) of the fp32 pattern of 256.0
+// reads as exactly 256 + n; placed in bits [19,23) of 16.0 it reads as 16 + n.
+// One LOP3 per code, no integer-to-float conversion.  The constant parts
+// (256 or 16, plus the -8 midpoint) are removed through a per-block bias
+//   bias = -264 * sum(x at even columns) - 24 * sum(x at odd columns),
+// so that bias + sum_k F_k x_k = sum_k (code_k - 8) x_k.
+__device__ __forceinline__ float nib_even(uint32_t s) {  // bits [15,19) -> 256 + n
+  return __uint_as_float((s & 0x00078000u) | 0x43800000u);
+}
+__device__ __forceinline__ float nib_odd(uint32_t s) {   // bits [19,23) -> 16 + n
+  return __uint_as_float((s & 0x00780000u) | 0x41800000u);
+}
+
+// sum_k (code_k - 8) * x_k over one 32-column block.
+// c: the block's 16 code bytes (column 2j in the low nibble of byte j).
+// xv: x of the block as 8 float4 (columns 4t..4t+3 in xv[t]).
+__device__ __forceinline__ float q4_block_dot(const uint4 c, const float4 (&xv)[8], float bias) {
+  f2_t acc = f2_pack(bias, 0.f);
+  const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w = w4[i];          // columns 8i .. 8i+7, nibble j = column 8i+j
+    const uint32_t s0 = w << 15, s1 = w << 7, s2 = w >> 1, s3 = w >> 9;
+    acc = f2_fma(f2_pack(nib_even(s0), nib_odd(s0)), f2_pack(xv[2 * i].x, xv[2 * i].y), acc);
+    acc = f2_fma(f2_pack(nib_even(s1), nib_odd(s1)), f2_pack(xv[2 * i].z, xv[2 * i].w), acc);
+    acc = f2_fma(f2_pack(nib_even(s2), nib_odd(s2)), f2_pack(xv[2 * i + 1].x, xv[2 * i + 1].y), acc);
+    acc = f2_fma(f2_pack(nib_even(s3), nib_odd(s3)), f2_pack(xv[2 * i + 1].z, xv[2 * i + 1].w), acc);
+  }
+  float lo, hi;
+  f2_unpack(acc, lo, hi);
+  return lo + hi;
+}
+
+__device__ __forceinline__ void load_xblock(const float* xs, int blk, float4 (&xv)[8], float& bias) {
+  const float4* p = reinterpret_cast<const float4*>(xs + blk * kXStride);
+#pragma unroll
+  for (int t = 0; t < 8; ++t) xv[t] = p[t];
+  bias = xs[blk * kXStride + 32];
+}
+
+// ----------------------------------------------------------- reductions ---
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum over the CTA (kThreads threads); every thread gets the result.
+__device__ __forceinline__ float block_sum(float v, float* red /* kWarps floats */) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) t += red[i];
+  return t;
+}
+
+__device__ __forceinline__ float f16_round(float v) { return __half2float(__float2half_rn(v)); }
+
+// x into the padded shared layout, then the per-block biases.
+__device__ __forceinline__ void xs_store(float* xs, int k, float v) {
+  xs[(k >> 5) * kXStride + (k & 31)] = v;
+}
+__device__ __forceinline__ float xs_load(const float* xs, int k) {
+  return xs[(k >> 5) * kXStride + (k & 31)];
+}
+__device__ __forceinline__ void xs_biases(float* xs, int nb) {
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+    const float* p = xs + b * kXStride;
+    float se = 0.f, so = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      se += p[2 * i];
+      so += p[2 * i + 1];
+    }
+    xs[b * kXStride + 32] = -264.f * se - 24.f * so;
+  }
+}
+
+// gelu with the tanh form, in fp32 with the accurate tanhf.
+__device__ __forceinline__ float gelu_tanh_f32(float x) {
+  const float c = 0.7978845608028654f;   // sqrt(2/pi)
+  return 0.5f * x * (1.f + tanhf(c * (x + 0.044715f * x * x * x)));
+}
+
+}  // namespace q4w

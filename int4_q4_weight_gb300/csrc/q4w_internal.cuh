@@ -1,0 +1,68 @@
+// Internal declarations shared by the translation units of libq4w.so.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/q4w.h"
+
+namespace q4w {
+
+// ---------------------------------------------------------------- errors ---
+// Records a thread-local message and returns the status (host side).
+int fail(int status, const char* fmt, ...);
+int cuda_fail(cudaError_t e, const char* what);
+void clear_error();
+
+// Device facts cached per device (queried once).
+struct DeviceInfo {
+  int sms;
+  int cc_major, cc_minor;
+  size_t smem_optin;
+};
+// Returns Q4_OK and fills *info for the current device, or an error status.
+int current_device(DeviceInfo* info);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------- launch plumbing ---
+// One matrix of a fused GEMV stage and where its rows go.
+struct StageMat {
+  const uint8_t* codes;
+  const __half* scales;
+  int rows;
+  float* out32;
+  __half* out16;
+};
+
+struct StageArgs {
+  StageMat mat[3];
+  int nmat;
+  int pair;          // 1: mat[0]=gate, mat[1]=up -> m16 = f16(gelu(g) * u) into mat[0].out16
+  int K;
+  const void* in;
+  int in_mode;       // q4_stage_in
+  float eps;
+};
+
+// Launches one fused stage (prologue + GEMV + epilogue).  `pdl` adds the
+// programmatic-dependent-launch attribute.  Returns a q4_status.
+int launch_stage(const StageArgs& a, const DeviceInfo& dev, cudaStream_t s, bool pdl);
+int launch_gemv_batched(const uint8_t* codes, const __half* scales, const __half* x, float* y,
+                        int N, int K, int batch, const DeviceInfo& dev, cudaStream_t s);
+int launch_rmsnorm_f16(const float* in, int H, float eps, __half* out, cudaStream_t s, bool pdl);
+int launch_quantize(const float* W, int N, int K, uint8_t* codes, __half* scales, int32_t* err,
+                    const DeviceInfo& dev, cudaStream_t s);
+int launch_lmhead(const uint8_t* codes, const __half* scales, const __half* h, int b, int V, int K,
+                  float cap, int32_t* idx, float* top1, float* top2, float* logits, void* ws,
+                  const DeviceInfo& dev, cudaStream_t s);
+size_t lmhead_ws_bytes(int V, int K, int b, const DeviceInfo& dev);
+int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_scale, int V, int L,
+               int ld, float embed_scale, const float* proj, const __half* hidden, int D,
+               const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
+               const DeviceInfo& dev, cudaStream_t s);
+int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
+                      int N, int K, const DeviceInfo& dev, cudaStream_t s);
+
+}  // namespace q4w

@@ -1,0 +1,111 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports every
+symbol the header declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import int4_q4_weight_gb300 as q4w
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q4w.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    q4w.build()
+    return q4w.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "return")))
+
+
+def test_header_lists_the_entry_points():
+    names = _declared_functions()
+    for n in ("q4_gemv", "q4_gemm_chunk", "ple_gather_project", "lmhead_softcap_argmax",
+              "q4_quantize", "q4_decode_pass", "q4_workspace_bytes", "q4_status_string",
+              "q4_last_error"):
+        assert n in names, n
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), f"libq4w.so does not export {n}"
+
+
+def test_status_strings(lib):
+    names = [lib.q4_status_string(i).decode() for i in range(9)]
+    assert names == ["Q4_OK", "Q4_ERR_NULL", "Q4_ERR_SHAPE", "Q4_ERR_ALIGN", "Q4_ERR_WORKSPACE",
+                     "Q4_ERR_ARCH", "Q4_ERR_CUDA", "Q4_ERR_TIMEOUT", "Q4_ERR_DEVICE"]
+    assert lib.q4_status_string(99) == b"Q4_ERR_UNKNOWN"
+    assert lib.q4_version() == 100
+
+
+def test_decode_workspace_formula(lib):
+    up = lambda n: (n + 255) // 256 * 256
+    H, QKV, I = 1536, 4096 + 1024, 12288
+    want = up(QKV * 2) + up(QKV * 4) + up(H * 4) + up(I * 2) + up(H * 4)
+    assert lib.q4_workspace_bytes(q4w.Q4_OP_DECODE_PASS, H, QKV, I) == want
+    assert lib.q4_workspace_bytes(q4w.Q4_OP_GEMV, 10, 64, 1) == 0
+
+
+A = 1 << 20  # an aligned, never-dereferenced stand-in address
+
+
+def test_null_and_shape_rejections(lib):
+    assert lib.q4_gemv(None, A, A, A, 16, 64, 1, None, 0, None) == 1
+    assert b"codes" in lib.q4_last_error()
+    assert lib.q4_gemv(A, A, A, A, 16, 48, 1, None, 0, None) == 2       # K % 32
+    assert b"K=48" in lib.q4_last_error()
+    assert lib.q4_gemv(A, A, A, A, 16, 64, 9, None, 0, None) == 2       # batch > 8
+    assert lib.q4_gemv(A, A, A, A, 0, 64, 1, None, 0, None) == 2        # N < 1
+    assert lib.q4_gemv(A, A, A, A, 16, 65536, 1, None, 0, None) == 2    # K too large
+    assert lib.q4_gemm_chunk(A, A, A, A, 32, 128, 64, None, 0, None) == 2   # M != 64
+    assert lib.q4_gemm_chunk(A, A, A, A, 64, 100, 64, None, 0, None) == 2   # N % 128
+    assert lib.ple_gather_project(A, 4, A, A, 10, 35, 128, 16.0, A, A, 64, A, 1e-6, A, None, None,
+                                  None) == 2                                # ld != 256
+    assert lib.lmhead_softcap_argmax(A, A, A, 9, 100, 64, 30.0, A, A, A, None, A, 1 << 20,
+                                     None) == 2                             # b > 8
+    assert lib.lmhead_softcap_argmax(A, A, A, 1, 100, 64, 0.0, A, A, A, None, A, 1 << 20,
+                                     None) == 2                             # cap <= 0
+    assert lib.q4_quantize(A, 4, 40, A, A, None, None) == 2
+
+
+def test_alignment_rejection(lib):
+    assert lib.q4_gemv(A + 4, A, A, A, 16, 64, 1, None, 0, None) == 3
+    assert b"16-byte" in lib.q4_last_error()
+    assert lib.q4_quantize(A, 4, 64, A, A + 2, None, None) == 3
+
+
+def test_decode_pass_rejections(lib):
+    layer = q4w.q4_layer()
+    layer.q_rows, layer.kv_rows, layer.mlp_rows = 64, 0, 64
+    assert lib.q4_decode_pass(ctypes.byref(layer), 1, 64, A, A, 1e-6, A, 1 << 20, None) == 1
+    assert b"layers[0].q" in lib.q4_last_error()
+    for f in ("q", "o", "gate", "up", "down"):
+        setattr(layer, f, q4w.q4_matrix(A, A))
+    layer.mlp_rows = 40
+    assert lib.q4_decode_pass(ctypes.byref(layer), 1, 64, A, A, 1e-6, A, 1 << 20, None) == 2
+    layer.mlp_rows = 64
+    assert lib.q4_decode_pass(ctypes.byref(layer), 1, 64, A, A, 1e-6, A, 16, None) == 4   # ws small
+
+
+def test_valid_call_without_gpu_fails_loudly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = lib.q4_gemv(A, A, A, A, 16, 64, 1, None, 0, None)
+    assert st in (5, 6)            # no device: CUDA error (never a silent success)
+    assert lib.q4_last_error() != b""
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    W = torch.zeros(4, 64)
+    with pytest.raises(q4w.Q4Error):
+        q4w.q4_quantize(W)
