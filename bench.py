@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""Benchmark of the q4_0 decode path on GB300.
+
+One step = one E2B-shaped decode weight pass at S=1: 35 layers at hidden 1536
+(q/o 2048 or 4096 wide, k/v one head on L0-L14, gated MLP 6144 / 12288), q4_0
+weights (1,032,486,912 weight bytes per step, more than L2 holds, so no flush
+is needed between steps), fp16 activations, fp32 accumulation, run as one CUDA
+graph of 141 kernel launches.  The line printed is steps/s for the whole job.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the pass
+does not shard); time is the maximum over ranks.  ``--impl reference`` times
+the CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import resource
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "q4_0 dequant-GEMV HBM GB/s vs peak; E2B-shaped decode weight-pass steps/s"
+WORKLOAD = "e2b_decode_weight_pass_s1"
+FALLBACK_HBM_GBS = 6800.0
+SEED = 1003
+
+
+# --------------------------------------------------------------- helpers ---
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "int4_q4_weight_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel_key):
+    """DRAM bytes per unit from a committed ncu summary, if the kernels have not
+    changed since it was taken; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_unit")
+
+
+def e2b_step_bytes(layer_dims, H=1536):
+    """Algorithmic bytes of one pass: every weight byte once (codes 0.5 B and
+    scales 2/32 B per weight) plus each stage's input and output vectors."""
+    wbytes = 0
+    abytes = 2 * H + 2 * H                          # h0 in, h out (fp16)
+    for li, d in enumerate(layer_dims):
+        rows = d["q"] + 2 * d["kv"]
+        n = rows * H + H * d["q"] + 2 * d["mlp"] * H + H * d["mlp"]
+        wbytes += n * 9 // 16
+        abytes += (2 * H if li == 0 else 4 * H) + 2 * d["q"] + 4 * 2 * d["kv"]   # qkv stage
+        abytes += 2 * d["q"] + 4 * H                                             # o stage
+        abytes += 4 * H + 2 * d["mlp"]                                           # gate/up stage
+        abytes += 2 * d["mlp"] + 4 * H                                           # down stage
+    return wbytes, abytes
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms (read-only)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.lines = []
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(device_index)
+            target = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+        except Exception:
+            target = str(device_index)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", target],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_gemv_rate(layers_np, min_seconds):
+    """Bytes/s of the oracle's dequant-GEMV over whole matrices, and the number
+    of threads it used (process CPU time / wall time)."""
+    from oracle import q4_oracle as O
+    done = 0
+    r0 = resource.getrusage(resource.RUSAGE_SELF)
+    t0 = time.perf_counter()
+    while True:
+        for mats in layers_np:
+            for (codes, scales, x) in mats:
+                O.q4_gemv(codes, scales, x)
+                done += codes.size + scales.size * 2
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    r1 = resource.getrusage(resource.RUSAGE_SELF)
+    cpu = (r1.ru_utime - r0.ru_utime) + (r1.ru_stime - r0.ru_stime)
+    return done / el, max(1, math.ceil(cpu / el - 0.05)), el, done
+
+
+def oracle_sample_layers(layer_ids, device):
+    """Oracle-quantised matrices of the sampled layers with fp16 inputs."""
+    import torch
+    from int4_q4_weight_gb300 import synth
+    from oracle import q4_oracle as O
+    out = []
+    for layer in layer_ids:
+        mats = []
+        for name, (r, c) in synth.e2b_matrix_shapes(layer).items():
+            W = synth.e2b_weight(SEED, layer, name, device).cpu().numpy()
+            codes, scales = O.quantize_q4_0(W)
+            x = synth.normal_f16((c,), synth.sub_seed(SEED, "x", layer, name), device).cpu().numpy()
+            mats.append((codes, scales, x))
+        out.append(mats)
+    return out
+
+
+# ------------------------------------------------------------ our arm ---
+def run_ours(args, world, rank, local):
+    import torch
+    import int4_q4_weight_gb300 as q4w
+    from int4_q4_weight_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    q4w.build()
+    q4w.load()
+
+    H = synth.E2B_HIDDEN
+    layer_ids = list(range(synth.E2B_N_LAYERS - args.layers, synth.E2B_N_LAYERS))
+    dims = [synth.e2b_dims(l) for l in layer_ids]
+    layers = []
+    for layer in layer_ids:
+        g = {}
+        for name in synth.e2b_matrix_shapes(layer):
+            W = synth.e2b_weight(SEED, layer, name, dev)
+            g[name] = q4w.q4_quantize(W)
+            del W
+        layers.append(g)
+    torch.cuda.synchronize()
+    plan = q4w.Q4DecodePlan(layers, H, device=dev)
+    plan.h_in.copy_(synth.e2b_h0(SEED, dev))
+    plan.capture()
+    wbytes, abytes = e2b_step_bytes(dims, H)
+    step_bytes = wbytes + abytes
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        plan.step_device()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        plan.step_device()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+    value = world * args.steps / elapsed
+    ms_per_step = elapsed / args.steps * 1e3
+
+    # end to end through the public API: pinned host h -> device, one graph
+    # replay, device -> pinned host result, synchronised every step
+    h_host = synth.e2b_h0(SEED, dev).cpu().pin_memory()
+    out_host = torch.empty(H, dtype=torch.float16).pin_memory()
+    ke = min(args.steps, 2000)
+    for _ in range(3):
+        plan.step_host(h_host, out_host)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(ke):
+        plan.step_host(h_host, out_host)
+    te = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([te], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        te = float(t.item())
+
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
+    launches = plan.launches_per_step
+    traffic = stored_traffic("e2b_pass_step") if args.layers == 35 else None
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,0.02) weights quantised to q4_0 on the device, N(0,1) fp16 h0)",
+        "config": {"workload": WORKLOAD if args.layers == 35 else f"{WORKLOAD}_last{args.layers}",
+                   "layers": args.layers, "hidden": H, "weight_format": "q4_0",
+                   "weight_bytes_per_step": wbytes, "algorithmic_bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2 (1.03 GB of weights per step)",
+                   "launch": f"one CUDA graph per step, {4 * args.layers + 1} kernels, programmatic dependent launch",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(world * ke / te, 3), "unit": "steps/s", "h2d_bytes_per_step": 2 * H,
+                "d2h_bytes_per_step": 2 * H,
+                "how": "pinned host h0 -> device, graph replay, device -> pinned host h, sync per step"},
+        "gpu_launches": launches * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": traffic,
+                     "kernel": "stage_kernel (fused q4_0 GEMV stage), all launches of one step",
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "frac_of_nominal_8TBs": round(achieved / 8000.0, 4)},
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.layers == 35:
+        line["cpu_baseline"] = cpu_baseline(dev, step_bytes)
+    if rank == 0 and world == 1 and not args.no_rows:
+        line["rows"] = measure_rows(q4w, synth, dev, hbm, clocks)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def cpu_baseline(dev, step_bytes):
+    """The oracle as it stands on the host cores, on a bounded sample: its
+    dequant-GEMV over one layer of each E2B layer type, repeated for >= 10 s."""
+    sample_layers = [0, 4, 15, 19]
+    mats = oracle_sample_layers(sample_layers, dev)
+    rate, threads, el, done = oracle_gemv_rate(mats, 10.0)
+    return {"value": round(rate / step_bytes, 5), "unit": "steps/s", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"oracle q4_gemv over every matrix of layers {sample_layers} (one of each "
+                       f"E2B layer type), {done} weight bytes in {el:.1f} s, scaled to the "
+                       f"{step_bytes}-byte step")}
+
+
+# ---------------------------------------------------------- other rows ---
+def _time_graph(fn, reps, stream=None):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    for _ in range(reps):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / reps
+
+
+def measure_rows(q4w, synth, dev, hbm, clocks):
+    import torch
+    rows = {}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    # config 1: [2048, 1536] GEMV streamed over distinct copies totalling >= 4x L2
+    W, x = synth.gemv_inputs(seed=1001, device=dev)
+    c, s = q4w.q4_quantize(W)
+    per = c.numel() + s.numel() * 2
+    copies = max(8, math.ceil(4 * l2 / per))
+    cs = [(c.clone(), s.clone()) for _ in range(copies)]
+    y = torch.empty(2048, dtype=torch.float32, device=dev)
+    xv = x[0].contiguous()
+    t = _time_graph(lambda: [q4w.q4_gemv(ci, si, xv, y) for ci, si in cs], 10) / copies
+    b = per + 2 * 1536 + 4 * 2048
+    t_iso = _time_graph(lambda: [q4w.q4_gemv(c, s, xv, y) for _ in range(100)], 10) / 100
+    rows["gemv_2048x1536"] = {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4),
+                              "us_per_gemv_streamed": round(t * 1e6, 3),
+                              "us_per_gemv_isolated_l2_resident": round(t_iso * 1e6, 3),
+                              "bytes": b, "copies": copies}
+    del cs
+    # config 4: LM head, b = 1 and 8
+    Wh, _ = synth.head_inputs(seed=1004, device=dev, batch=1)
+    hc, hs = q4w.q4_quantize(Wh)
+    del Wh
+    for bsz in (1, 8):
+        _, h = synth.head_inputs(seed=1004, device=dev, batch=bsz, V=1, K=1536)
+        ws = q4w.lmhead_ws(262144, 1536, bsz, dev)
+        outs = (torch.empty(bsz, dtype=torch.int32, device=dev),
+                torch.empty(bsz, dtype=torch.float32, device=dev),
+                torch.empty(bsz, dtype=torch.float32, device=dev))
+        t = _time_graph(lambda: q4w.lmhead_softcap_argmax(hc, hs, h, ws=ws, idx=outs[0], top1=outs[1],
+                                                          top2=outs[2]), 20)
+        b = hc.numel() + hs.numel() * 2 + 2 * 1536 * bsz + 12 * bsz
+        rows[f"lmhead_b{bsz}"] = {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4),
+                                  "us": round(t * 1e6, 2), "bytes": b}
+    del hc, hs
+    # config 2: PLE gather + projection, S = 64, proj rotated over copies beyond L2
+    p = synth.ple_inputs(seed=1002, device=dev)
+    ncp = max(2, math.ceil(2 * l2 / p.proj.numel() / 4))
+    projs = [p.proj.clone() for _ in range(ncp)]
+    out = torch.empty((64, 8960), dtype=torch.float32, device=dev)
+    t = _time_graph(lambda: [q4w.ple_gather_project(p.ids, p.table, p.row_scale, pj, p.hidden,
+                                                    p.norm_w, out=out) for pj in projs], 10) / ncp
+    b = 64 * 8960 + 64 * 4 + p.proj.numel() * 4 + 64 * 1536 * 2 + 256 * 4 + 64 * 8960 * 4 + 64 * 4
+    flops = 2 * 64 * 8960 * 1536
+    sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    fp32_peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * sm_mhz * 1e6
+    rows["ple_s64"] = {"GB/s": round(b / t / 1e9, 1), "TFLOP/s": round(flops / t / 1e12, 2),
+                       "fp32_peak_TFLOP/s": round(fp32_peak / 1e12, 1),
+                       "frac": round(max(b / t / 1e9 / hbm, flops / t / fp32_peak), 4),
+                       "bound": "alu (fp32 FFMA)", "us": round(t * 1e6, 2), "bytes": b}
+    del p, projs
+    return rows
+
+
+# ------------------------------------------------------ reference arm ---
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return
+    import torch
+    from int4_q4_weight_gb300 import synth
+    from oracle import q4_oracle as O
+
+    dims = [synth.e2b_dims(l) for l in range(synth.E2B_N_LAYERS)]
+    wbytes, abytes = e2b_step_bytes(dims)
+    step_bytes = wbytes + abytes
+    # the pass's matrices, row-sliced so that the whole run stays within ~60 s
+    mats = []
+    for layer in (0, 4, 15, 19):
+        for name, (r, c) in synth.e2b_matrix_shapes(layer).items():
+            W = synth.e2b_weight(SEED, layer, name, "cpu").numpy()
+            codes, scales = O.quantize_q4_0(W)
+            x = synth.normal_f16((c,), synth.sub_seed(SEED, "x", layer, name), "cpu").numpy()
+            mats.append((codes, scales, x))
+    c0, s0, x0 = mats[0]
+    t0 = time.perf_counter()
+    O.q4_gemv(c0, s0, x0)
+    per_byte = (time.perf_counter() - t0) / (c0.size + s0.size * 2)
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    sl = []
+    for codes, scales, x in mats:
+        rows = int(max(8, min(codes.shape[0], budget / per_byte / (codes.shape[1] + scales.shape[1] * 2))))
+        sl.append((codes[:rows], scales[:rows], x))
+    for i in range(args.warmup):
+        cc, ss, xx = sl[i % len(sl)]
+        O.q4_gemv(cc, ss, xx)
+    done = 0
+    r0 = resource.getrusage(resource.RUSAGE_SELF)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        cc, ss, xx = sl[i % len(sl)]
+        O.q4_gemv(cc, ss, xx)
+        done += cc.size + ss.size * 2
+    el = time.perf_counter() - t0
+    r1 = resource.getrusage(resource.RUSAGE_SELF)
+    threads = max(1, math.ceil(((r1.ru_utime - r0.ru_utime) + (r1.ru_stime - r0.ru_stime)) / el - 0.05))
+    value = done / el / step_bytes
+    sample = (f"each step: the oracle's q4_gemv on a row slice of one matrix of the E2B layers "
+              f"0/4/15/19 (cycled), {done} weight bytes over {args.steps} steps in {el:.1f} s, "
+              f"scaled to the {step_bytes}-byte pass")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "steps/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 / value, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": 35, "hidden": 1536, "weight_format": "q4_0",
+                       "algorithmic_bytes_per_step": step_bytes},
+            "cpu_baseline": {"value": round(value, 5), "unit": "steps/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": "steps/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=35,
+                    help="run only the last N E2B layers (a small case for profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -298,3 +298,51 @@ def q4_gemm_chunk(codes, scales, X, Y=None):
     _check(lib.q4_gemm_chunk(_ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, N, K, None, 0,
                              _stream()), "q4_gemm_chunk")
     return Y
+
+
+class Q4DecodePlan:
+    """A decode weight pass bound to fixed device buffers and captured once into
+    a CUDA graph, so that a step is one graph launch.
+
+    ``layers``: list of dicts name -> (codes, scales) as for q4_decode_pass.
+    ``step_device()`` replays the graph on the current stream (h_in -> h_out,
+    both device buffers).  ``step_host(h_pinned, out_pinned)`` copies one fp16
+    hidden vector host->device, replays, and copies the result back.
+    """
+
+    def __init__(self, layers, H, eps=1e-6, device="cuda"):
+        self.layers = layers
+        self.H = H
+        self.eps = eps
+        self.descs = make_layers(layers)
+        self.ws = torch.empty(decode_pass_ws_bytes(layers, H), dtype=torch.uint8, device=device)
+        self.h_in = torch.zeros(H, dtype=torch.float16, device=device)
+        self.h_out = torch.zeros(H, dtype=torch.float16, device=device)
+        self.stream = torch.cuda.Stream(device=device)
+        self.graph = None
+
+    def run_eager(self):
+        q4_decode_pass(self.layers, self.h_in, self.h_out, self.ws, self.eps, descs=self.descs)
+
+    def capture(self):
+        with torch.cuda.stream(self.stream):
+            self.run_eager()                       # warm-up outside the capture
+        torch.cuda.current_stream().wait_stream(self.stream)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self.run_eager()
+        torch.cuda.synchronize()
+        return self
+
+    def step_device(self):
+        self.graph.replay()
+
+    def step_host(self, h_pinned, out_pinned):
+        self.h_in.copy_(h_pinned, non_blocking=True)
+        self.graph.replay()
+        out_pinned.copy_(self.h_out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return out_pinned
+
+    launches_per_step = property(lambda self: 4 * len(self.layers) + 1)
