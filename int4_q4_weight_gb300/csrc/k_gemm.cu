@@ -1,12 +1,437 @@
-// S=64 chunked-prefill dequant-GEMM on the tcgen05 tensor cores (in progress).
+// S=64 chunked-prefill dequant-GEMM on the 5th-generation tensor cores.
+//
+// "visible-cx/gemma-4-E2B-CoreAI", Provenance / Performance: the prefill
+// entry point has a static query width of 64 and serves full-width chunks.
+// Y[t][n] = sum_k bf16(scale*(code-8))[n][k] * bf16(x[t][k]), fp32 accumulate.
+//
+// Swap-AB: the weight tile is the M=128 operand (A, dequantised in shared
+// memory), the 64 tokens are the N=64 operand (B), the accumulator D[128][64]
+// (fp32) lives in tensor memory.  One CTA per SM, persistent over work items
+// (a 128-row tile and a range of 64-column K chunks; K is split across CTAs
+// when there are fewer tiles than SMs, the splits then add into Y).
+//
+// Warp roles (416 threads):
+//   warps 0-3   epilogue: tcgen05.ld of their TMEM lane quarter, store to Y
+//   warps 4-11  producers: codes + scales + x from global, nibble -> bf16
+//               (exact d*(q-8) in fp32, then round to nearest even), x fp16 ->
+//               bf16, written in the no-swizzle K-major core-matrix layout
+//   warp 12     TMEM allocator and the single thread that issues tcgen05.mma
+// A ring of kStages operand stages (A 16 KB + B 8 KB) is guarded by full /
+// empty mbarriers; two TMEM accumulators (2 x 64 columns) let the epilogue of
+// one item overlap the MMAs of the next.  Every mbarrier wait is bounded in
+// clock cycles; on expiry the CTA raises an abort flag, every role leaves its
+// loop, the MMA thread drains its own tcgen05 work (bounded again), TMEM is
+// freed and the kernel returns with the device error word set.
+#include <cstdlib>
+
+#include "q4w_device.cuh"
 #include "q4w_internal.cuh"
 
 namespace q4w {
 
+__device__ unsigned int g_device_error = 0;   // bit 0: a bounded wait ran out
+
+namespace gemm {
+
+constexpr int kStages = 4;
+constexpr int kTileM = 128;            // weight rows per tile (MMA M)
+constexpr int kTok = 64;               // tokens (MMA N)
+constexpr int kChunk = 64;             // K columns per operand stage
+constexpr int kABytes = kTileM * kChunk * 2;   // 16 KB bf16
+constexpr int kBBytes = kTok * kChunk * 2;     // 8 KB bf16
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kEpiWarps = 4, kProdWarps = 8;
+constexpr int kProdThreads = kProdWarps * 32;
+constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 12
+constexpr int kThreadsG = (kMmaWarp + 1) * 32;      // 416
+constexpr int kTmemCols = 128;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M=128, N=64.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTok >> 3) << 17) |
+                            ((uint32_t)(kTileM >> 4) << 24);
+
+// Shared-memory matrix descriptor, no swizzle: 8x(16 B) core matrices;
+// lbo = byte step between core matrices along K, sbo = along M/N.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+         ((uint64_t)(sbo >> 4) << 32) | (1ull << 46);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait.  Returns false when the wait ran out or the CTA is aborting.
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, long long limit,
+                                          volatile int* abort_flag) {
+  const long long t0 = clock64();
+  while (!mbar_test(a, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      *abort_flag = 1;
+      atomicOr(&g_device_error, 1u);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Dequantised word: 8 columns (nibble j = column j) -> 4 bf16x2 in column order.
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, f2_t dd, f2_t bias) {
+  const uint32_t s[4] = {w << 15, w << 7, w >> 1, w >> 9};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    // (256 + n_even, 16 + n_odd) * (d, d) + (-264 d, -24 d) = (d (n_even - 8), d (n_odd - 8)), exact
+    const f2_t v = f2_fma(f2_pack(nib_even(s[i]), nib_odd(s[i])), dd, bias);
+    float lo, hi;
+    f2_unpack(v, lo, hi);
+    o[i] = bf16x2(lo, hi);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint32_t h2_to_bf16x2(uint32_t h2) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  return bf16x2(f.x, f.y);
+}
+
+struct Params {
+  const uint8_t* codes;
+  const __half* scales;
+  const __half* X;
+  float* Y;
+  int N, K;
+  int tiles, splits, cps, nchunks, items;
+  long long wait_limit;
+};
+
+__device__ __forceinline__ void item_range(const Params& p, int item, int& tile, int& c0, int& c1) {
+  tile = item / p.splits;
+  const int sp = item - tile * p.splits;
+  c0 = sp * p.cps;
+  c1 = min(c0 + p.cps, p.nchunks);
+}
+
+struct ProdRegs {
+  uint4 code;
+  float d;
+  uint4 x0, x1;
+};
+
+__global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* stage_base = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStageBytes);
+  // bars: full[kStages], empty[kStages], accfull[2], accempty[2], drain
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+  const uint32_t accfull0 = smem_u32(bars + 2 * kStages), accempty0 = smem_u32(bars + 2 * kStages + 2);
+  const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
+  volatile int* abort_flag = &abort_sh;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, kProdThreads);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accfull0 + 8 * a, 1);
+      mbar_init(accempty0 + 8 * a, kEpiWarps * 32);
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_sh)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int K2 = p.K >> 1, K32 = p.K >> 5;
+
+  if (warp >= kEpiWarps && warp < kMmaWarp) {
+    // ------------------------------------------------------------ producers
+    const int pt = threadIdx.x - kEpiWarps * 32;
+    const int r = pt >> 1, h = pt & 1;        // A: row of the tile, 32-block in the chunk
+    const int t = pt >> 2, q = pt & 3;        // B: token, 16-column quarter of the chunk
+    const uint32_t a_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 16);
+    const uint32_t b_off = (uint32_t)((t >> 3) * 1024 + (t & 7) * 16);
+    uint32_t g = 0;                           // global chunk counter (ring position)
+    bool have = false;
+    ProdRegs cur;
+    int item = blockIdx.x, tile = 0, c0 = 0, c1 = 0, c = 0;
+    auto fetch = [&](int tl, int ch, ProdRegs& R) {
+      const size_t row = (size_t)tl * kTileM + r;
+      R.code = ld_stream16(p.codes + row * K2 + (size_t)(ch * 2 + h) * 16);
+      R.d = ld_scale(p.scales + row * K32 + ch * 2 + h);
+      const uint4* xp = reinterpret_cast<const uint4*>(p.X + (size_t)t * p.K + ch * kChunk + q * 16);
+      R.x0 = __ldg(xp);
+      R.x1 = __ldg(xp + 1);
+    };
+    if (item < p.items) {
+      item_range(p, item, tile, c0, c1);
+      c = c0;
+      fetch(tile, c, cur);
+      have = true;
+    }
+    while (have) {
+      // next (item, chunk) in this CTA's sequence
+      int ntile = tile, nc0 = c0, nc1 = c1, nc = c + 1, nitem = item;
+      if (nc >= c1) {
+        nitem = item + gridDim.x;
+        if (nitem < p.items) {
+          item_range(p, nitem, ntile, nc0, nc1);
+          nc = nc0;
+        }
+      }
+      const bool more = nitem < p.items;
+      ProdRegs nxt;
+      if (more) fetch(ntile, nc, nxt);
+
+      const uint32_t s = g % kStages, round = g / kStages;
+      if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag)) break;
+      uint8_t* A = stage_base + (size_t)s * kStageBytes;
+      uint8_t* B = A + kABytes;
+      const f2_t dd = f2_pack(cur.d, cur.d);
+      const f2_t bias = f2_pack(-264.f * cur.d, -24.f * cur.d);
+      const uint32_t w4[4] = {cur.code.x, cur.code.y, cur.code.z, cur.code.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(A + a_off + (h * 4 + j) * 128) = dequant_word(w4[j], dd, bias);
+      const uint4 b0 = make_uint4(h2_to_bf16x2(cur.x0.x), h2_to_bf16x2(cur.x0.y), h2_to_bf16x2(cur.x0.z),
+                                  h2_to_bf16x2(cur.x0.w));
+      const uint4 b1 = make_uint4(h2_to_bf16x2(cur.x1.x), h2_to_bf16x2(cur.x1.y), h2_to_bf16x2(cur.x1.z),
+                                  h2_to_bf16x2(cur.x1.w));
+      *reinterpret_cast<uint4*>(B + b_off + (2 * q) * 128) = b0;
+      *reinterpret_cast<uint4*>(B + b_off + (2 * q + 1) * 128) = b1;
+      fence_proxy_async();
+      mbar_arrive(full0 + 8 * s);
+      ++g;
+      if (!more) break;
+      item = nitem;
+      tile = ntile;
+      c0 = nc0;
+      c1 = nc1;
+      c = nc;
+      cur = nxt;
+    }
+  } else if (warp == kMmaWarp) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t g = 0;
+      int it = 0;
+      bool ok = true;
+      const uint32_t stage0 = smem_u32(stage_base);
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
+        int tile, c0, c1;
+        item_range(p, item, tile, c0, c1);
+        const int a = it & 1;
+        if (!mbar_wait(accempty0 + 8 * a, ((it >> 1) & 1) ^ 1, p.wait_limit, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(a * kTok);
+        for (int c = c0; c < c1; ++c, ++g) {
+          const uint32_t s = g % kStages, round = g / kStages;
+          if (!mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t A = stage0 + s * kStageBytes, B = A + kABytes;
+#pragma unroll
+          for (int ks = 0; ks < kChunk / 16; ++ks) {
+            const uint64_t ad = smem_desc(A + ks * 256, 128, 1024);
+            const uint64_t bd = smem_desc(B + ks * 256, 128, 1024);
+            tc_mma(d_tmem, ad, bd, (c > c0 || ks > 0) ? 1u : 0u);
+          }
+          tc_commit(empty0 + 8 * s);
+        }
+        if (!ok) break;
+        tc_commit(accfull0 + 8 * a);
+      }
+      // drain: every tcgen05 op this thread issued has finished before TMEM is freed
+      tc_commit(drain);
+      const long long t0 = clock64();
+      while (!mbar_test(drain, 0)) {
+        if (clock64() - t0 > p.wait_limit) {
+          atomicOr(&g_device_error, 1u);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int row = warp * 32 + lane;          // TMEM lane = tile row
+    int it = 0;
+    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
+      int tile, c0, c1;
+      item_range(p, item, tile, c0, c1);
+      const int a = it & 1;
+      if (!mbar_wait(accfull0 + 8 * a, (it >> 1) & 1, p.wait_limit, abort_flag)) break;
+      tc_fence_after();
+      float* yrow = p.Y + (size_t)tile * kTileM + row;
+#pragma unroll
+      for (int cb = 0; cb < kTok / 16; ++cb) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(a * kTok + cb * 16), v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float* dst = yrow + (size_t)(cb * 16 + j) * p.N;
+          if (p.splits == 1)
+            *dst = v[j];
+          else
+            atomicAdd(dst, v[j]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(accempty0 + 8 * a);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+}  // namespace gemm
+
+static long long wait_limit_cycles() {
+  static long long v = -1;
+  if (v < 0) {
+    const char* e = getenv("Q4W_WAIT_LIMIT_CYCLES");
+    v = e ? atoll(e) : 4000000000LL;   // about 2 s at 2 GHz
+    if (v < 0) v = 0;
+  }
+  return v;
+}
+
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, const DeviceInfo& dev, cudaStream_t s) {
-  (void)codes; (void)scales; (void)X; (void)Y; (void)M; (void)N; (void)K; (void)dev; (void)s;
-  return fail(Q4_ERR_SHAPE, "q4_gemm_chunk: tensor-core kernel not built yet");
+  (void)M;
+  gemm::Params p;
+  p.codes = codes;
+  p.scales = scales;
+  p.X = X;
+  p.Y = Y;
+  p.N = N;
+  p.K = K;
+  p.tiles = N / gemm::kTileM;
+  p.nchunks = K / gemm::kChunk;
+  int splits = (dev.sms + p.tiles - 1) / p.tiles;
+  if (splits > p.nchunks) splits = p.nchunks;
+  if (splits < 1) splits = 1;
+  p.cps = (p.nchunks + splits - 1) / splits;
+  p.splits = (p.nchunks + p.cps - 1) / p.cps;
+  p.items = p.tiles * p.splits;
+  p.wait_limit = wait_limit_cycles();
+  cudaError_t e;
+  if (p.splits > 1) {
+    e = cudaMemsetAsync(Y, 0, (size_t)gemm::kTok * N * sizeof(float), s);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm output clear");
+  }
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(gemm::gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gemm::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm smem attribute");
+    attr_set = true;
+  }
+  const int grid = p.items < dev.sms ? p.items : dev.sms;
+  gemm::gemm_kernel<<<grid, gemm::kThreadsG, gemm::kSmemBytes, s>>>(p);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? Q4_OK : cuda_fail(e, "gemm launch");
 }
 
 }  // namespace q4w
+
+extern "C" int q4_device_status(q4_stream_t stream) {
+  using namespace q4w;
+  clear_error();
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "q4_device_status: stream");
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "q4_device_status: read");
+  if (v) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "q4_device_status: clear");
+    return fail(Q4_ERR_TIMEOUT, "a bounded device-side wait ran out (error word 0x%x)", v);
+  }
+  return Q4_OK;
+}
