@@ -245,6 +245,19 @@ size_t q4_workspace_bytes(int op, int a, int b, int c);
 const char* q4_status_string(int status);
 const char* q4_last_error(void);   /* thread-local; "" when no error yet */
 
+/* q4_device_status: waits for `stream` to finish, then reads and clears the
+ * library's device error word.  Returns Q4_ERR_TIMEOUT if a bounded
+ * device-side wait of a kernel (an mbarrier or inter-CTA wait) ran out since
+ * the last check; such a kernel returned early and its outputs are invalid. */
+int q4_device_status(q4_stream_t stream);
+
+/* q4_set_wait_limit: clock-cycle budget of every bounded device-side wait in
+ * kernels launched after the call (default 4e9, about 2 s; the environment
+ * variable Q4W_WAIT_LIMIT_CYCLES sets the initial value).  Returns the
+ * previous budget.  A budget of 0 makes any wait that is not already
+ * satisfied give up at once (used to test the timeout path). */
+long long q4_set_wait_limit(long long cycles);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int q4_version(void);
 

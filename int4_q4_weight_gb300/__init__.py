@@ -60,6 +60,8 @@ _SIGS = {
     "q4_status_string": (ctypes.c_char_p, [ci]),
     "q4_last_error": (ctypes.c_char_p, []),
     "q4_version": (ci, []),
+    "q4_device_status": (ci, [vp]),
+    "q4_set_wait_limit": (ctypes.c_longlong, [ctypes.c_longlong]),
 }
 
 
@@ -113,6 +115,15 @@ def _dev(t, dtype, name):
         raise Q4Error(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise Q4Error(f"{name} must be contiguous")
+
+
+def q4_device_status():
+    """Synchronise the current stream; raise if a kernel's bounded wait ran out."""
+    _check(load().q4_device_status(_stream()), "q4_device_status")
+
+
+def q4_set_wait_limit(cycles: int) -> int:
+    return int(load().q4_set_wait_limit(cycles))
 
 
 def q4_version() -> int:

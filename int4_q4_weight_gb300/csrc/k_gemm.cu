@@ -22,14 +22,26 @@
 // clock cycles; on expiry the CTA raises an abort flag, every role leaves its
 // loop, the MMA thread drains its own tcgen05 work (bounded again), TMEM is
 // freed and the kernel returns with the device error word set.
-#include <cstdlib>
-
 #include "q4w_device.cuh"
 #include "q4w_internal.cuh"
 
 namespace q4w {
 
 __device__ unsigned int g_device_error = 0;   // bit 0: a bounded wait ran out
+
+// Device address of g_device_error for the current device (kernels in other
+// translation units receive it as an argument).  Queried once per device.
+unsigned* device_error_word() {
+  static unsigned* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned*>(p);
+  }
+  return cache[dev];
+}
 
 namespace gemm {
 
@@ -46,6 +58,7 @@ constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 12
 constexpr int kThreadsG = (kMmaWarp + 1) * 32;      // 416
 constexpr int kTmemCols = 128;
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+constexpr long long kDrainCycles = 2000000000LL;
 
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M=128, N=64.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTok >> 3) << 17) |
@@ -323,7 +336,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const Params p) {
       tc_commit(drain);
       const long long t0 = clock64();
       while (!mbar_test(drain, 0)) {
-        if (clock64() - t0 > p.wait_limit) {
+        if (clock64() - t0 > kDrainCycles) {   // independent of the (possibly zero) wait budget
           atomicOr(&g_device_error, 1u);
           break;
         }
@@ -369,16 +382,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const Params p) {
 
 }  // namespace gemm
 
-static long long wait_limit_cycles() {
-  static long long v = -1;
-  if (v < 0) {
-    const char* e = getenv("Q4W_WAIT_LIMIT_CYCLES");
-    v = e ? atoll(e) : 4000000000LL;   // about 2 s at 2 GHz
-    if (v < 0) v = 0;
-  }
-  return v;
-}
-
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, const DeviceInfo& dev, cudaStream_t s) {
   (void)M;
@@ -397,7 +400,7 @@ int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* 
   p.cps = (p.nchunks + splits - 1) / splits;
   p.splits = (p.nchunks + p.cps - 1) / p.cps;
   p.items = p.tiles * p.splits;
-  p.wait_limit = wait_limit_cycles();
+  p.wait_limit = wait_limit();
   cudaError_t e;
   if (p.splits > 1) {
     e = cudaMemsetAsync(Y, 0, (size_t)gemm::kTok * N * sizeof(float), s);

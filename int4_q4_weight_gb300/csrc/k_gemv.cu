@@ -293,6 +293,7 @@ static cudaError_t launch_stage_l(const StageArgs& a, int total, const DeviceInf
 }
 
 int launch_stage(const StageArgs& a, const DeviceInfo& dev, cudaStream_t s, bool pdl) {
+  if (stream_eligible(a.K)) return launch_stage_stream(a, dev, s, pdl);
   int total = 0;
   if (a.pair) {
     total = a.mat[0].rows;

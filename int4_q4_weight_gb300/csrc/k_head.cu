@@ -15,71 +15,9 @@
 
 #include "q4w_device.cuh"
 #include "q4w_internal.cuh"
+#include "q4w_top2.cuh"
 
 namespace q4w {
-
-struct Top2 {
-  float v1, v2;
-  int i1, i2;
-};
-
-__device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
-  return a > b || (a == b && ia < ib);
-}
-__device__ __forceinline__ void top2_init(Top2& t) {
-  t.v1 = t.v2 = -INFINITY;
-  t.i1 = t.i2 = INT_MAX;
-}
-__device__ __forceinline__ void top2_insert(Top2& t, float v, int i) {
-  if (better(v, i, t.v1, t.i1)) {
-    t.v2 = t.v1;
-    t.i2 = t.i1;
-    t.v1 = v;
-    t.i1 = i;
-  } else if (better(v, i, t.v2, t.i2)) {
-    t.v2 = v;
-    t.i2 = i;
-  }
-}
-__device__ __forceinline__ void top2_merge(Top2& t, const Top2& o) {
-  top2_insert(t, o.v1, o.i1);
-  top2_insert(t, o.v2, o.i2);
-}
-
-constexpr int kMaxBatch = 8;
-constexpr size_t kTicketBytes = 256;
-
-__device__ __forceinline__ Top2 load_cg(const Top2* p) {
-  Top2 t;
-  t.v1 = __ldcg(&p->v1);
-  t.v2 = __ldcg(&p->v2);
-  t.i1 = __ldcg(&p->i1);
-  t.i2 = __ldcg(&p->i2);
-  return t;
-}
-
-// Second level: runs in the CTA that finishes last.
-__device__ void head_finish(const Top2* partials, unsigned* ticket, int B, float cap, int32_t* idx,
-                            float* top1, float* top2) {
-  __shared__ bool last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  if (threadIdx.x < B) {
-    const int b = threadIdx.x;
-    Top2 t;
-    top2_init(t);
-    for (int c = 0; c < (int)gridDim.x; ++c) top2_merge(t, load_cg(partials + (size_t)c * kMaxBatch + b));
-    idx[b] = t.i1;
-    top1[b] = cap * tanhf(t.v1 / cap);
-    top2[b] = cap * tanhf(t.v2 / cap);
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) *ticket = 0u;
-}
 
 // b == 1: lane groups own R rows each, like the decode GEMV stages.
 template <int LPR, int R>
@@ -239,7 +177,7 @@ static int lpr_for(int nb) {
   return l;
 }
 
-static int head_grid(const DeviceInfo& dev) { return 2 * dev.sms; }
+static int head_grid(const DeviceInfo& dev) { return 2 * dev.sms; }   // >= the streaming head's grid
 
 size_t lmhead_ws_bytes(int V, int K, int b, const DeviceInfo& dev) {
   (void)V;
@@ -289,6 +227,8 @@ int launch_lmhead(const uint8_t* codes, const __half* scales, const __half* h, i
                   const DeviceInfo& dev, cudaStream_t s) {
   if ((size_t)b * (K >> 5) * kXStride * sizeof(float) > (size_t)200 * 1024)
     return fail(Q4_ERR_SHAPE, "lmhead: batch %d x K %d does not fit in shared memory", b, K);
+  if (b == 1 && stream_eligible(K))
+    return launch_head_stream(codes, scales, h, V, K, cap, idx, top1, top2, logits, ws, dev, s);
   unsigned* ticket = reinterpret_cast<unsigned*>(ws);
   Top2* partials = reinterpret_cast<Top2*>(reinterpret_cast<char*>(ws) + kTicketBytes);
   cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);

@@ -1,0 +1,763 @@
+// Streaming q4_0 GEMV engine: the fast path of the S=1 decode GEMV, of every
+// decode-pass stage, of the b=1 LM head, and the persistent decode-pass kernel.
+//
+// Weights stream through shared memory: one producer thread issues 1-D bulk
+// copies (cp.async.bulk, completion on an mbarrier) of contiguous row tiles
+// (codes, then scales) into a ring of kSlots slots, with an L2 evict-first
+// hint; 8 consumer warps dequantise and dot against x held in registers.
+// A row group of P lanes covers all K/32 blocks of a row, each lane up to
+// three blocks (x of those blocks, 96 values, stays in registers for the
+// whole stage); Gc = 256/P groups take the rows of a tile in turn; P <= 32
+// reduces with shuffles, P > 32 through shared memory.  The per-row
+// arithmetic (block order, bias trick, reduction tree) depends only on K, so
+// every entry point produces the same bits for the same row.
+//
+// The decode pass runs as one cooperative launch: every CTA walks the same
+// stage list; the producer runs ahead across stage boundaries (weights do
+// not depend on activations), while consumers wait for the previous stage's
+// completion counter (all CTAs done), read its output from L2, apply the
+// stage prologue and compute.  All waits are bounded in clock cycles; on
+// expiry the CTA raises an abort flag (and a grid-wide one), every role
+// leaves its loop, in-flight bulk copies are drained (bounded) and the
+// kernel returns with the device error word set.
+#include "q4w_device.cuh"
+#include "q4w_internal.cuh"
+#include "q4w_top2.cuh"
+
+namespace q4w {
+
+namespace eng {
+
+constexpr int kCW = 8;                    // consumer warps
+constexpr int kCT = kCW * 32;             // consumer threads
+constexpr int kTS = kCT + 32;             // threads per CTA
+constexpr int kSlots = 5;
+constexpr int kSlotBytes = 28 * 1024;
+constexpr int kMaxNb = 384;               // K <= 12288 on this path
+constexpr int kBPL = 3;                   // blocks per lane (upper bound)
+constexpr size_t kXsBytes = (size_t)kMaxNb * kXStride * sizeof(float);
+constexpr size_t kSmemBytes = 128 + (size_t)kSlots * kSlotBytes + kXsBytes + 64 * sizeof(float) +
+                              2 * kSlots * sizeof(uint64_t) + 64;
+constexpr long long kDrainCycles = 2000000000LL;   // in-flight copies always land well within this
+
+// ----------------------------------------------------------- primitives ---
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Named barrier that also ANDs a predicate over its threads (uniform result).
+__device__ __forceinline__ bool bar_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+struct Ctl {
+  volatile int* abort_cta;   // shared
+  int* abort_grid;           // global (decode pass) or nullptr
+  long long limit;
+  unsigned* err;             // the library's device error word
+};
+
+__device__ __forceinline__ void raise_abort(const Ctl& c) {
+  *c.abort_cta = 1;
+  atomicOr(c.err, 1u);
+  if (c.abort_grid) atomicExch(c.abort_grid, 1);
+}
+
+__device__ __forceinline__ bool aborting(const Ctl& c) {
+  return *c.abort_cta || (c.abort_grid && *(volatile int*)c.abort_grid);
+}
+
+// Bounded mbarrier wait; false on expiry (raises the abort) or when aborting.
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, const Ctl& c) {
+  const long long t0 = clock64();
+  while (!mbar_test(a, parity)) {
+    if (aborting(c)) return false;
+    if (clock64() - t0 > c.limit) {
+      raise_abort(c);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(mbar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ float lds_half(const uint8_t* p) {
+  return __half2float(*reinterpret_cast<const __half*>(p));
+}
+
+// ------------------------------------------------------------- geometry ---
+struct Geo {
+  int K2, nb, P, Gc, T, total, lo, hi;
+};
+
+__device__ __forceinline__ int lanes_per_row(int nb) {
+  int P = 1;
+  while (P * kBPL < nb) P <<= 1;
+  return P;
+}
+
+__device__ __forceinline__ Geo make_geo(const StageArgs& a, int NM) {
+  Geo g;
+  g.K2 = a.K >> 1;
+  g.nb = a.K >> 5;
+  g.P = lanes_per_row(g.nb);
+  g.Gc = kCT / g.P;
+  int T = kSlotBytes / (NM * (g.K2 + g.nb * 2));
+  g.T = T < 1 ? 1 : T;
+  g.total = a.pair ? a.mat[0].rows : a.mat[0].rows + (a.nmat > 1 ? a.mat[1].rows : 0) +
+                                         (a.nmat > 2 ? a.mat[2].rows : 0);
+  const int rpc = (g.total + gridDim.x - 1) / gridDim.x;
+  g.lo = min(g.total, (int)blockIdx.x * rpc);
+  g.hi = min(g.total, g.lo + rpc);
+  return g;
+}
+
+// Next tile [r0, r0+n) of matrix m (pair: of both matrices) in [pos, hi).
+__device__ __forceinline__ bool tile_next(const StageArgs& a, const Geo& g, int& pos, int& m, int& r0,
+                                          int& n) {
+  if (pos >= g.hi) return false;
+  int base = 0;
+  m = 0;
+  if (!a.pair) {
+    while (m < a.nmat - 1 && pos >= base + a.mat[m].rows) {
+      base += a.mat[m].rows;
+      ++m;
+    }
+  }
+  r0 = pos - base;
+  n = min(g.T, min(g.hi - pos, a.mat[m].rows - r0));
+  pos += n;
+  return true;
+}
+
+// ------------------------------------------------------------- producer ---
+// Issues the bulk copies of one stage's tiles; false when aborting.
+template <int NM>
+__device__ bool produce_stage(const StageArgs& a, uint32_t& gcount, uint32_t slots0, uint32_t full0,
+                              uint32_t empty0, uint64_t policy, const Ctl& c) {
+  const Geo g = make_geo(a, NM);
+  int pos = g.lo, m, r0, n;
+  while (tile_next(a, g, pos, m, r0, n)) {
+    const uint32_t s = gcount % kSlots, round = gcount / kSlots;
+    if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, c)) return false;
+    const uint32_t per = (uint32_t)n * (g.K2 + g.nb * 2);
+    mbar_expect_tx(full0 + 8 * s, NM * per);
+    uint32_t dst = slots0 + s * kSlotBytes;
+#pragma unroll
+    for (int t = 0; t < NM; ++t) {
+      const StageMat& M = a.mat[NM == 2 ? t : m];
+      bulk_g2s(dst, M.codes + (size_t)r0 * g.K2, (uint32_t)n * g.K2, full0 + 8 * s, policy);
+      bulk_g2s(dst + (uint32_t)n * g.K2, M.scales + (size_t)r0 * g.nb, (uint32_t)n * g.nb * 2, full0 + 8 * s,
+               policy);
+      dst += per;
+    }
+    ++gcount;
+  }
+  return true;
+}
+
+// After the producer stops: every issued copy has landed before the CTA exits.
+__device__ void producer_drain(uint32_t gcount, uint32_t full0, unsigned* err) {
+  const uint32_t first = gcount > (uint32_t)kSlots ? gcount - kSlots : 0u;
+  for (uint32_t g = first; g < gcount; ++g) {
+    const uint32_t s = g % kSlots, round = g / kSlots;
+    const long long t0 = clock64();
+    while (!mbar_test(full0 + 8 * s, round & 1)) {
+      if (clock64() - t0 > kDrainCycles) {
+        atomicOr(err, 1u);
+        break;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ consumers ---
+__device__ __forceinline__ float consumer_sum(float v, float* red8) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  bar_sync(1, kCT);
+  if (l == 0) red8[w] = v;
+  bar_sync(1, kCT);
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < kCW; ++i) t += red8[i];
+  return t;
+}
+
+__device__ __forceinline__ float load_in_cg(const void* in, int mode, int k) {
+  if (mode == Q4_IN_F16 || mode == Q4_IN_RMS_F16)
+    return __half2float(__ldcg(reinterpret_cast<const __half*>(in) + k));
+  return __ldcg(reinterpret_cast<const float*>(in) + k);
+}
+
+// x = prologue(in) into the padded shared layout with per-block biases.
+__device__ void eng_prologue(const void* in, int mode, int K, float eps, float* xs, float* red8) {
+  const int tid = threadIdx.x;
+  if (mode == Q4_IN_F16) {
+    for (int k = tid; k < K; k += kCT) xs_store(xs, k, load_in_cg(in, mode, k));
+  } else {
+    float ss = 0.f;
+    for (int k = tid; k < K; k += kCT) {
+      const float v = load_in_cg(in, mode, k);
+      ss += v * v;
+    }
+    ss = consumer_sum(ss, red8);
+    const float r = 1.f / sqrtf(ss / (float)K + eps);
+    if (mode != Q4_IN_RMS2_F32) {
+      for (int k = tid; k < K; k += kCT) xs_store(xs, k, f16_round(load_in_cg(in, mode, k) * r));
+    } else {
+      float ss2 = 0.f;
+      for (int k = tid; k < K; k += kCT) {
+        const float t = f16_round(load_in_cg(in, mode, k) * r);
+        xs_store(xs, k, t);
+        ss2 += t * t;
+      }
+      ss2 = consumer_sum(ss2, red8);
+      const float r2 = 1.f / sqrtf(ss2 / (float)K + eps);
+      for (int k = tid; k < K; k += kCT) xs_store(xs, k, f16_round(xs_load(xs, k) * r2));
+    }
+  }
+  bar_sync(1, kCT);
+  const int nb = K >> 5;
+  for (int b = tid; b < nb; b += kCT) {
+    const float* p = xs + b * kXStride;
+    float se = 0.f, so = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      se += p[2 * i];
+      so += p[2 * i + 1];
+    }
+    xs[b * kXStride + 32] = -264.f * se - 24.f * so;
+  }
+  bar_sync(1, kCT);
+}
+
+struct StageEpi {
+  const StageArgs* a;
+  template <int NM>
+  __device__ __forceinline__ void operator()(int m, int row, const float (&acc)[NM]) const {
+    if (NM == 2) {
+      const float gv = acc[0], uv = acc[NM - 1];
+      if (a->mat[0].out32) a->mat[0].out32[row] = gv;
+      if (a->mat[1].out32) a->mat[1].out32[row] = uv;
+      a->mat[0].out16[row] = __float2half_rn(gelu_tanh_f32(gv) * uv);
+    } else {
+      const StageMat& M = a->mat[m];
+      if (M.out32) M.out32[row] = acc[0];
+      if (M.out16) M.out16[row] = __float2half_rn(acc[0]);
+    }
+  }
+};
+
+struct HeadEpi {
+  Top2* best;
+  float* logits;
+  float cap;
+  template <int NM>
+  __device__ __forceinline__ void operator()(int m, int row, const float (&acc)[NM]) const {
+    (void)m;
+    top2_insert(*best, acc[0], row);
+    if (logits) logits[row] = cap * tanhf(acc[0] / cap);
+  }
+};
+
+// Processes one stage's tiles; false when aborting (uniform over consumers).
+template <int NM, class Epi>
+__device__ bool consume_stage(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
+                              uint32_t empty0, const float* xs, float* red, const Ctl& c, const Epi& epi) {
+  const Geo g = make_geo(a, NM);
+  const int ct = threadIdx.x, lane = ct & 31;
+  const int gid = ct / g.P, li = ct % g.P;
+  const unsigned gmask = g.P >= 32 ? 0xffffffffu : (((1u << g.P) - 1u) << (lane & ~(g.P - 1)));
+  float4 xr[kBPL][8];
+  float bias[kBPL];
+#pragma unroll
+  for (int b = 0; b < kBPL; ++b) {
+    const int j = li + g.P * b;
+    if (j < g.nb) {
+      load_xblock(xs, j, xr[b], bias[b]);
+    } else {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) xr[b][t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      bias[b] = 0.f;
+    }
+  }
+  int pos = g.lo, m, r0, n;
+  while (tile_next(a, g, pos, m, r0, n)) {
+    const uint32_t s = gcount % kSlots, round = gcount / kSlots;
+    const bool landed = mbar_wait(full0 + 8 * s, round & 1, c);
+    if (!bar_and(1, kCT, landed)) return false;
+    const uint8_t* S = slots + (size_t)s * kSlotBytes;
+    const int per = n * (g.K2 + g.nb * 2);
+    for (int r = gid; r < n; r += g.Gc) {
+      float acc[NM];
+#pragma unroll
+      for (int t = 0; t < NM; ++t) acc[t] = 0.f;
+#pragma unroll
+      for (int b = 0; b < kBPL; ++b) {
+        const int j = li + g.P * b;
+        if (j < g.nb) {
+#pragma unroll
+          for (int t = 0; t < NM; ++t) {
+            const uint8_t* base = S + t * per;
+            const uint4 cw = lds128(base + r * g.K2 + 16 * j);
+            const float d = lds_half(base + n * g.K2 + (r * g.nb + j) * 2);
+            acc[t] = fmaf(d, q4_block_dot(cw, xr[b], bias[b]), acc[t]);
+          }
+        }
+      }
+      if (g.P <= 32) {
+#pragma unroll
+        for (int t = 0; t < NM; ++t)
+          for (int o = g.P >> 1; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(gmask, acc[t], o);
+      } else {
+        const int wpg = g.P >> 5, wig = (ct >> 5) - gid * wpg;
+#pragma unroll
+        for (int t = 0; t < NM; ++t) {
+          acc[t] = warp_sum(acc[t]);
+          if (lane == 0) red[(gid * wpg + wig) * NM + t] = acc[t];
+        }
+        bar_sync(2 + gid, g.P);
+        if (li == 0) {
+#pragma unroll
+          for (int t = 0; t < NM; ++t) {
+            float v = 0.f;
+            for (int w = 0; w < wpg; ++w) v += red[(gid * wpg + w) * NM + t];
+            acc[t] = v;
+          }
+        }
+        bar_sync(2 + gid, g.P);
+      }
+      if (li == 0) epi.template operator()<NM>(m, r0 + r, acc);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    ++gcount;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------- shared memory ---
+struct Smem {
+  uint8_t* slots;
+  float* xs;
+  float* red;
+  uint32_t slots0, full0, empty0;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* raw) {
+  Smem s;
+  uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 127) & ~(uintptr_t)127);
+  s.slots = p;
+  p += (size_t)kSlots * kSlotBytes;
+  s.xs = reinterpret_cast<float*>(p);
+  p += kXsBytes;
+  s.red = reinterpret_cast<float*>(p);
+  p += 64 * sizeof(float);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(p);
+  s.slots0 = smem_u32(s.slots);
+  s.full0 = smem_u32(bars);
+  s.empty0 = smem_u32(bars + kSlots);
+  return s;
+}
+
+__device__ __forceinline__ void init_barriers(const Smem& S) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(S.full0 + 8 * i, 1);
+      mbar_init(S.empty0 + 8 * i, kCW);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+}
+
+// ------------------------------------------------------- single stage ---
+template <int NM>
+__global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a, long long limit, unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_sh;
+  const Smem S = carve(smem_raw);
+  if (threadIdx.x == 0) abort_sh = 0;
+  init_barriers(S);
+  __syncthreads();
+  pdl_trigger();
+  const Ctl c{&abort_sh, nullptr, limit, err};
+  uint32_t gcount = 0;
+  if (threadIdx.x >= kCT) {
+    if (threadIdx.x == kCT) {
+      const uint64_t pol = evict_first_policy();
+      produce_stage<NM>(a, gcount, S.slots0, S.full0, S.empty0, pol, c);
+      producer_drain(gcount, S.full0, c.err);
+    }
+  } else {
+    pdl_wait();
+    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
+    StageEpi epi{&a};
+    consume_stage<NM>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+  }
+  __syncthreads();
+}
+
+// ----------------------------------------------------------- LM head b=1 ---
+__global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, float cap, float* logits,
+                                                            Top2* partials, unsigned* ticket, int32_t* idx,
+                                                            float* top1, float* top2, long long limit, unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_sh;
+  __shared__ Top2 st[kTS];
+  const Smem S = carve(smem_raw);
+  if (threadIdx.x == 0) abort_sh = 0;
+  init_barriers(S);
+  __syncthreads();
+  const Ctl c{&abort_sh, nullptr, limit, err};
+  uint32_t gcount = 0;
+  Top2 best;
+  top2_init(best);
+  if (threadIdx.x >= kCT) {
+    if (threadIdx.x == kCT) {
+      const uint64_t pol = evict_first_policy();
+      produce_stage<1>(a, gcount, S.slots0, S.full0, S.empty0, pol, c);
+      producer_drain(gcount, S.full0, c.err);
+    }
+  } else {
+    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
+    HeadEpi epi{&best, logits, cap};
+    consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+  }
+  st[threadIdx.x] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Top2 t;
+    top2_init(t);
+    for (int i = 0; i < kTS; ++i) top2_merge(t, st[i]);
+    partials[(size_t)blockIdx.x * kMaxBatch] = t;
+  }
+  head_finish(partials, ticket, 1, cap, idx, top1, top2);
+}
+
+// --------------------------------------------------------- decode pass ---
+constexpr int kMaxMegaLayers = 48;
+
+struct MegaLayer {
+  const uint8_t* codes[7];      // q, k, v, o, gate, up, down
+  const __half* scales[7];
+  int q_rows, kv_rows, mlp_rows;
+};
+
+struct MegaArgs {
+  MegaLayer L[kMaxMegaLayers];
+  int n_layers, H;
+  float eps;
+  const __half* h0;
+  __half* h_out;
+  __half* q16;
+  float* kv32;
+  float* o32;
+  __half* m16;
+  float* y32;
+  int* counters;                // [4 * n_layers], zeroed before the launch
+  int* abort_grid;              // zeroed before the launch
+  long long limit;
+  unsigned* err;
+};
+
+// Stage s of the pass as StageArgs (the same stages the launch path issues).
+__device__ __forceinline__ StageArgs mega_stage(const MegaArgs& A, int s) {
+  const MegaLayer& L = A.L[s >> 2];
+  StageArgs a = {};
+  a.eps = A.eps;
+  switch (s & 3) {
+    case 0:
+      a.mat[0] = {L.codes[0], L.scales[0], L.q_rows, nullptr, A.q16};
+      a.nmat = 1;
+      if (L.kv_rows > 0) {
+        a.mat[1] = {L.codes[1], L.scales[1], L.kv_rows, A.kv32, nullptr};
+        a.mat[2] = {L.codes[2], L.scales[2], L.kv_rows, A.kv32 + L.kv_rows, nullptr};
+        a.nmat = 3;
+      }
+      a.K = A.H;
+      a.in = (s == 0) ? static_cast<const void*>(A.h0) : static_cast<const void*>(A.y32);
+      a.in_mode = (s == 0) ? Q4_IN_RMS_F16 : Q4_IN_RMS2_F32;
+      break;
+    case 1:
+      a.mat[0] = {L.codes[3], L.scales[3], A.H, A.o32, nullptr};
+      a.nmat = 1;
+      a.K = L.q_rows;
+      a.in = A.q16;
+      a.in_mode = Q4_IN_F16;
+      break;
+    case 2:
+      a.mat[0] = {L.codes[4], L.scales[4], L.mlp_rows, nullptr, A.m16};
+      a.mat[1] = {L.codes[5], L.scales[5], L.mlp_rows, nullptr, nullptr};
+      a.nmat = 2;
+      a.pair = 1;
+      a.K = A.H;
+      a.in = A.o32;
+      a.in_mode = Q4_IN_RMS_F32;
+      break;
+    default:
+      a.mat[0] = {L.codes[6], L.scales[6], A.H, A.y32, nullptr};
+      a.nmat = 1;
+      a.K = L.mlp_rows;
+      a.in = A.m16;
+      a.in_mode = Q4_IN_F16;
+      break;
+  }
+  return a;
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Consumers of this CTA wait until `cnt` reaches `target`; uniform result.
+__device__ bool wait_counter(const int* cnt, int target, const Ctl& c) {
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    const long long t0 = clock64();
+    while (ld_acquire(cnt) < target) {
+      if (aborting(c)) {
+        ok = false;
+        break;
+      }
+      if (clock64() - t0 > c.limit) {
+        raise_abort(c);
+        ok = false;
+        break;
+      }
+    }
+    __threadfence();
+  }
+  return bar_and(1, kCT, ok);
+}
+
+__global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_constant__ MegaArgs A) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int abort_sh;
+  const Smem S = carve(smem_raw);
+  if (threadIdx.x == 0) abort_sh = 0;
+  init_barriers(S);
+  __syncthreads();
+  const Ctl c{&abort_sh, A.abort_grid, A.limit, A.err};
+  const int nst = 4 * A.n_layers;
+  uint32_t gcount = 0;
+  if (threadIdx.x >= kCT) {
+    if (threadIdx.x == kCT) {
+      const uint64_t pol = evict_first_policy();
+      for (int s = 0; s < nst; ++s) {
+        const StageArgs a = mega_stage(A, s);
+        const bool ok = a.pair ? produce_stage<2>(a, gcount, S.slots0, S.full0, S.empty0, pol, c)
+                               : produce_stage<1>(a, gcount, S.slots0, S.full0, S.empty0, pol, c);
+        if (!ok) break;
+      }
+      producer_drain(gcount, S.full0, c.err);
+    }
+  } else {
+    bool ok = true;
+    for (int s = 0; s < nst && ok; ++s) {
+      const StageArgs a = mega_stage(A, s);
+      if (s > 0 && !wait_counter(A.counters + s - 1, (int)gridDim.x, c)) break;
+      eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
+      StageEpi epi{&a};
+      ok = a.pair ? consume_stage<2>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
+                  : consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+      if (!ok) break;
+      bar_sync(1, kCT);
+      if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(A.counters + s, 1);
+      }
+    }
+    // closing RMSNorm of the last down-projection output, by CTA 0
+    if (ok && blockIdx.x == 0 && wait_counter(A.counters + nst - 1, (int)gridDim.x, c)) {
+      float ss = 0.f;
+      for (int k = threadIdx.x; k < A.H; k += kCT) {
+        const float v = __ldcg(A.y32 + k);
+        ss += v * v;
+      }
+      ss = consumer_sum(ss, S.red);
+      const float r = 1.f / sqrtf(ss / (float)A.H + A.eps);
+      for (int k = threadIdx.x; k < A.H; k += kCT) A.h_out[k] = __float2half_rn(__ldcg(A.y32 + k) * r);
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace eng
+
+// ------------------------------------------------------------- launchers ---
+bool stream_eligible(int K) { return K % 256 == 0 && (K >> 5) <= eng::kMaxNb; }
+
+static cudaError_t set_smem(const void* fn) {
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)eng::kSmemBytes);
+}
+
+int launch_stage_stream(const StageArgs& a, const DeviceInfo& dev, cudaStream_t s, bool pdl) {
+  static bool attr = false;
+  cudaError_t e;
+  if (!attr) {
+    if ((e = set_smem((const void*)eng::stage_stream_kernel<1>)) != cudaSuccess ||
+        (e = set_smem((const void*)eng::stage_stream_kernel<2>)) != cudaSuccess)
+      return cuda_fail(e, "stream stage smem attribute");
+    attr = true;
+  }
+  int total = a.pair ? a.mat[0].rows : 0;
+  if (!a.pair)
+    for (int i = 0; i < a.nmat; ++i) total += a.mat[i].rows;
+  const int K2 = a.K >> 1, nb = a.K >> 5;
+  const int rows_per_tile = eng::kSlotBytes / ((a.pair ? 2 : 1) * (K2 + nb * 2));
+  int grid = (total + rows_per_tile - 1) / rows_per_tile;
+  if (grid < dev.sms) grid = total < dev.sms ? total : dev.sms;
+  if (grid > dev.sms) grid = dev.sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(eng::kTS);
+  cfg.dynamicSmemBytes = eng::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr1[1];
+  attr1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr1[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr1;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const long long lim = wait_limit();
+  unsigned* err = device_error_word();
+  if (!err) return fail(Q4_ERR_CUDA, "device error word unavailable");
+  e = a.pair ? cudaLaunchKernelEx(&cfg, eng::stage_stream_kernel<2>, a, lim, err)
+             : cudaLaunchKernelEx(&cfg, eng::stage_stream_kernel<1>, a, lim, err);
+  return e == cudaSuccess ? Q4_OK : cuda_fail(e, "stream stage launch");
+}
+
+int launch_head_stream(const uint8_t* codes, const __half* scales, const __half* h, int V, int K, float cap,
+                       int32_t* idx, float* top1, float* top2, float* logits, void* ws, const DeviceInfo& dev,
+                       cudaStream_t s) {
+  static bool attr = false;
+  cudaError_t e;
+  if (!attr) {
+    if ((e = set_smem((const void*)eng::head_stream_kernel)) != cudaSuccess)
+      return cuda_fail(e, "stream head smem attribute");
+    attr = true;
+  }
+  unsigned* ticket = reinterpret_cast<unsigned*>(ws);
+  Top2* partials = reinterpret_cast<Top2*>(reinterpret_cast<char*>(ws) + kTicketBytes);
+  e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return cuda_fail(e, "lmhead ticket reset");
+  StageArgs a = {};
+  a.mat[0] = {codes, scales, V, nullptr, nullptr};
+  a.nmat = 1;
+  a.K = K;
+  a.in = h;
+  a.in_mode = Q4_IN_F16;
+  unsigned* err = device_error_word();
+  if (!err) return fail(Q4_ERR_CUDA, "device error word unavailable");
+  const int grid = V < dev.sms ? V : dev.sms;
+  eng::head_stream_kernel<<<grid, eng::kTS, eng::kSmemBytes, s>>>(a, cap, logits, partials, ticket, idx, top1,
+                                                                  top2, wait_limit(), err);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? Q4_OK : cuda_fail(e, "stream head launch");
+}
+
+size_t decode_counters_bytes() { return (size_t)(4 * 256 + 64) * sizeof(int); }
+
+int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const __half* h0, __half* h_out,
+                              float eps, __half* q16, float* kv32, float* o32, __half* m16, float* y32,
+                              int* counters, const DeviceInfo& dev, cudaStream_t s) {
+  if (n_layers > eng::kMaxMegaLayers) return fail(Q4_ERR_SHAPE, "persistent pass holds at most %d layers",
+                                                  eng::kMaxMegaLayers);
+  static bool attr = false;
+  cudaError_t e;
+  if (!attr) {
+    if ((e = set_smem((const void*)eng::decode_pass_kernel)) != cudaSuccess)
+      return cuda_fail(e, "decode pass smem attribute");
+    attr = true;
+  }
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, eng::decode_pass_kernel, eng::kTS, eng::kSmemBytes);
+  if (e != cudaSuccess) return cuda_fail(e, "decode pass occupancy");
+  if (per_sm < 1) return fail(Q4_ERR_CUDA, "decode pass kernel does not fit on an SM");
+  static eng::MegaArgs A;   // host staging of the kernel parameter
+  memset(&A, 0, sizeof(A));
+  for (int l = 0; l < n_layers; ++l) {
+    const q4_layer& L = layers[l];
+    const q4_matrix* m[7] = {&L.q, &L.k, &L.v, &L.o, &L.gate, &L.up, &L.down};
+    for (int i = 0; i < 7; ++i) {
+      A.L[l].codes[i] = m[i]->codes;
+      A.L[l].scales[i] = reinterpret_cast<const __half*>(m[i]->scales);
+    }
+    A.L[l].q_rows = L.q_rows;
+    A.L[l].kv_rows = L.kv_rows;
+    A.L[l].mlp_rows = L.mlp_rows;
+  }
+  A.n_layers = n_layers;
+  A.H = H;
+  A.eps = eps;
+  A.h0 = h0;
+  A.h_out = h_out;
+  A.q16 = q16;
+  A.kv32 = kv32;
+  A.o32 = o32;
+  A.m16 = m16;
+  A.y32 = y32;
+  A.counters = counters;
+  A.abort_grid = counters + 4 * 256;
+  A.limit = wait_limit();
+  A.err = device_error_word();
+  if (!A.err) return fail(Q4_ERR_CUDA, "device error word unavailable");
+  e = cudaMemsetAsync(counters, 0, decode_counters_bytes(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode pass counter reset");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(dev.sms);
+  cfg.blockDim = dim3(eng::kTS);
+  cfg.dynamicSmemBytes = eng::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;
+  at[0].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, eng::decode_pass_kernel, A);
+  return e == cudaSuccess ? Q4_OK : cuda_fail(e, "decode pass launch");
+}
+
+}  // namespace q4w

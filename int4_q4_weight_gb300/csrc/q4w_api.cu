@@ -1,6 +1,7 @@
 // C ABI of libq4w.so: argument checks, status codes, dispatch to launchers.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "q4w_internal.cuh"
@@ -24,6 +25,17 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 void clear_error() { g_err[0] = '\0'; }
+
+static long long g_wait_limit = -1;
+
+long long wait_limit() {
+  if (g_wait_limit < 0) {
+    const char* e = getenv("Q4W_WAIT_LIMIT_CYCLES");
+    long long v = e ? atoll(e) : 4000000000LL;   // about 2 s at 2 GHz
+    g_wait_limit = v < 0 ? 0 : v;
+  }
+  return g_wait_limit;
+}
 
 int current_device(DeviceInfo* info) {
   static DeviceInfo cache[64];
@@ -101,11 +113,17 @@ const char* q4_status_string(int status) {
 
 const char* q4_last_error(void) { return g_err; }
 
+long long q4_set_wait_limit(long long cycles) {
+  const long long old = wait_limit();
+  g_wait_limit = cycles < 0 ? 0 : cycles;
+  return old;
+}
+
 static size_t decode_ws_bytes(size_t H, size_t QKV, size_t I) {
-  // q16 [QKV] fp16 | k,v f32 [QKV] | o [H] f32 | m16 [I] fp16 | y [H] f32,
-  // each region 256-byte aligned.
+  // q16 [QKV] fp16 | k,v f32 [QKV] | o [H] f32 | m16 [I] fp16 | y [H] f32 |
+  // stage counters of the persistent pass; each region 256-byte aligned.
   auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
-  return up(QKV * 2) + up(QKV * 4) + up(H * 4) + up(I * 2) + up(H * 4);
+  return up(QKV * 2) + up(QKV * 4) + up(H * 4) + up(I * 2) + up(H * 4) + up(decode_counters_bytes());
 }
 
 size_t q4_workspace_bytes(int op, int a, int b, int c) {
@@ -278,6 +296,17 @@ int q4_decode_pass(const q4_layer* layers, int n_layers, int H, const uint16_t* 
   __half* m16 = reinterpret_cast<__half*>(p);
   p += up((size_t)max_mlp * 2);
   float* y32 = reinterpret_cast<float*>(p);
+  p += up((size_t)H * 4);
+  int* counters = reinterpret_cast<int*>(p);
+
+  // One persistent cooperative launch when every stage fits the streaming engine.
+  bool persistent = stream_eligible(H) && n_layers <= 48;
+  for (int l = 0; l < n_layers && persistent; ++l)
+    persistent = stream_eligible(layers[l].q_rows) && stream_eligible(layers[l].mlp_rows);
+  if (persistent)
+    return launch_decode_pass_stream(layers, n_layers, H, reinterpret_cast<const __half*>(h0_f16),
+                                     reinterpret_cast<__half*>(h_out_f16), eps, q16, kv32, o32, m16, y32, counters,
+                                     dev, s);
 
   for (int l = 0; l < n_layers; ++l) {
     const q4_layer& L = layers[l];

@@ -24,6 +24,12 @@ struct DeviceInfo {
 // Returns Q4_OK and fills *info for the current device, or an error status.
 int current_device(DeviceInfo* info);
 
+// Cycle budget of every bounded device-side wait (q4_set_wait_limit; the
+// Q4W_WAIT_LIMIT_CYCLES environment variable sets the initial value).
+long long wait_limit();
+// Device address of the library's error word on the current device.
+unsigned* device_error_word();
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ------------------------------------------------------- launch plumbing ---
@@ -62,6 +68,16 @@ int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_
                int ld, float embed_scale, const float* proj, const __half* hidden, int D,
                const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
                const DeviceInfo& dev, cudaStream_t s);
+// Streaming engine (bulk-copy ring; K % 256 == 0 and K <= 12288).
+bool stream_eligible(int K);
+int launch_stage_stream(const StageArgs& a, const DeviceInfo& dev, cudaStream_t s, bool pdl);
+int launch_head_stream(const uint8_t* codes, const __half* scales, const __half* h, int V, int K, float cap,
+                       int32_t* idx, float* top1, float* top2, float* logits, void* ws, const DeviceInfo& dev,
+                       cudaStream_t s);
+size_t decode_counters_bytes();
+int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const __half* h0, __half* h_out,
+                              float eps, __half* q16, float* kv32, float* o32, __half* m16, float* y32,
+                              int* counters, const DeviceInfo& dev, cudaStream_t s);
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, const DeviceInfo& dev, cudaStream_t s);
 

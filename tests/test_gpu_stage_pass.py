@@ -238,3 +238,18 @@ def test_full_e2b_pass(cuda_lib):
     assert torch.isfinite(hv).all()
     assert abs(float((hv * hv).mean()) - 1.0) < 5e-3
     assert torch.equal(h1, _composed(q4w, gl, h0, H))
+
+
+def test_persistent_pass_is_stage_composition(cuda_lib):
+    """Shapes the persistent kernel takes (all K multiples of 256): its output
+    equals the stage-by-stage launches bit for bit."""
+    H = 512
+    dims = [{"q": 768, "kv": 128, "mlp": 1280}, {"q": 1024, "kv": 0, "mlp": 2048},
+            {"q": 512, "kv": 256, "mlp": 768}, {"q": 768, "kv": 0, "mlp": 1536}]
+    gl, ol = _layers(cuda_lib, dims, H, 72)
+    h0 = synth.normal_f16((H,), 73, "cuda")
+    hp = _pass(cuda_lib, gl, h0, H)
+    cuda_lib.q4_device_status()
+    assert torch.equal(hp, _composed(cuda_lib, gl, h0, H))
+    h1 = _pass(cuda_lib, gl[:1], h0, H)
+    assert_close(h1.cpu().numpy(), O.e2b_layer(h0.cpu().numpy(), ol[0], eps=EPS)["h"], what="layer 0")
