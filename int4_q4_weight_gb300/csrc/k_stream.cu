@@ -429,6 +429,7 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
       produce_stage<NM>(a, gcount, S.slots0, S.full0, S.empty0, pol, c);
       producer_drain(gcount, S.full0, c.err);
     }
+    __syncwarp();
   } else {
     pdl_wait();
     eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
@@ -459,6 +460,7 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
       produce_stage<1>(a, gcount, S.slots0, S.full0, S.empty0, pol, c);
       producer_drain(gcount, S.full0, c.err);
     }
+    __syncwarp();
   } else {
     eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
     HeadEpi epi{&best, logits, cap};
@@ -594,6 +596,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       }
       producer_drain(gcount, S.full0, c.err);
     }
+    __syncwarp();
   } else {
     bool ok = true;
     for (int s = 0; s < nst && ok; ++s) {
