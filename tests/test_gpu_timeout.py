@@ -24,6 +24,9 @@ def test_zero_budget_times_out_then_recovers(cuda_lib):
     W, X = synth.gemm_inputs(seed=110, device="cuda", N=512, K=1536)
     codes, scales = q4w.q4_quantize(W)
     x1 = X[0].contiguous()
+    Wg = synth.normal((65536, 1536), 0.02, synth.sub_seed(113), "cuda")   # many tiles per CTA:
+    gc, gs = q4w.q4_quantize(Wg)                                         # the ring must wrap
+    del Wg
     layers = []
     for i in range(2):
         g = {}
@@ -38,7 +41,7 @@ def test_zero_budget_times_out_then_recovers(cuda_lib):
     try:
         q4w.q4_gemm_chunk(codes, scales, X)
         _expect_timeout(q4w)
-        q4w.q4_gemv(codes, scales, x1)           # streaming GEMV (K = 1536)
+        q4w.q4_gemv(gc, gs, x1)                  # streaming GEMV (K = 1536)
         _expect_timeout(q4w)
         q4w.q4_decode_pass(layers, h0, h, ws)    # persistent pass
         _expect_timeout(q4w)
