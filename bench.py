@@ -292,7 +292,7 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.layers == 35:
         line["cpu_baseline"] = cpu_baseline(dev, step_bytes)
     if rank == 0 and world == 1 and not args.no_rows:
-        line["rows"] = measure_rows(q4w, synth, dev, hbm, clocks)
+        line["rows"] = measure_rows(q4w, synth, dev, hbm, clocks, float(peaks.get("bf16_tflops", 1900.0)))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -336,11 +336,10 @@ def _time_graph(fn, reps, stream=None):
     return e0.elapsed_time(e1) / 1e3 / reps
 
 
-def measure_rows(q4w, synth, dev, hbm, clocks):
+def row_gemv(q4w, synth, dev, hbm, reps=10):
+    """[2048, 1536] GEMV streamed over distinct weight copies totalling >= 4x L2."""
     import torch
-    rows = {}
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    # config 1: [2048, 1536] GEMV streamed over distinct copies totalling >= 4x L2
     W, x = synth.gemv_inputs(seed=1001, device=dev)
     c, s = q4w.q4_quantize(W)
     per = c.numel() + s.numel() * 2
@@ -348,47 +347,110 @@ def measure_rows(q4w, synth, dev, hbm, clocks):
     cs = [(c.clone(), s.clone()) for _ in range(copies)]
     y = torch.empty(2048, dtype=torch.float32, device=dev)
     xv = x[0].contiguous()
-    t = _time_graph(lambda: [q4w.q4_gemv(ci, si, xv, y) for ci, si in cs], 10) / copies
+    t = _time_graph(lambda: [q4w.q4_gemv(ci, si, xv, y) for ci, si in cs], reps) / copies
     b = per + 2 * 1536 + 4 * 2048
-    t_iso = _time_graph(lambda: [q4w.q4_gemv(c, s, xv, y) for _ in range(100)], 10) / 100
-    rows["gemv_2048x1536"] = {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4),
-                              "us_per_gemv_streamed": round(t * 1e6, 3),
-                              "us_per_gemv_isolated_l2_resident": round(t_iso * 1e6, 3),
-                              "bytes": b, "copies": copies}
-    del cs
-    # config 4: LM head, b = 1 and 8
-    Wh, _ = synth.head_inputs(seed=1004, device=dev, batch=1)
-    hc, hs = q4w.q4_quantize(Wh)
-    del Wh
-    for bsz in (1, 8):
-        _, h = synth.head_inputs(seed=1004, device=dev, batch=bsz, V=1, K=1536)
-        ws = q4w.lmhead_ws(262144, 1536, bsz, dev)
-        outs = (torch.empty(bsz, dtype=torch.int32, device=dev),
-                torch.empty(bsz, dtype=torch.float32, device=dev),
-                torch.empty(bsz, dtype=torch.float32, device=dev))
-        t = _time_graph(lambda: q4w.lmhead_softcap_argmax(hc, hs, h, ws=ws, idx=outs[0], top1=outs[1],
-                                                          top2=outs[2]), 20)
-        b = hc.numel() + hs.numel() * 2 + 2 * 1536 * bsz + 12 * bsz
-        rows[f"lmhead_b{bsz}"] = {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4),
-                                  "us": round(t * 1e6, 2), "bytes": b}
-    del hc, hs
-    # config 2: PLE gather + projection, S = 64, proj rotated over copies beyond L2
+    t_iso = _time_graph(lambda: [q4w.q4_gemv(c, s, xv, y) for _ in range(100)], reps) / 100
+    return {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4),
+            "us_per_gemv_streamed": round(t * 1e6, 3),
+            "us_per_gemv_isolated_l2_resident": round(t_iso * 1e6, 3), "bytes": b, "copies": copies}
+
+
+def row_head(q4w, synth, dev, hbm, bsz, reps=20, weights=None):
+    import torch
+    if weights is None:
+        Wh, _ = synth.head_inputs(seed=1004, device=dev, batch=1)
+        weights = q4w.q4_quantize(Wh)
+        del Wh
+    hc, hs = weights
+    _, h = synth.head_inputs(seed=1004, device=dev, batch=bsz, V=1, K=1536)
+    ws = q4w.lmhead_ws(262144, 1536, bsz, dev)
+    outs = (torch.empty(bsz, dtype=torch.int32, device=dev), torch.empty(bsz, dtype=torch.float32, device=dev),
+            torch.empty(bsz, dtype=torch.float32, device=dev))
+    t = _time_graph(lambda: q4w.lmhead_softcap_argmax(hc, hs, h, ws=ws, idx=outs[0], top1=outs[1],
+                                                      top2=outs[2]), reps)
+    b = hc.numel() + hs.numel() * 2 + 2 * 1536 * bsz + 12 * bsz
+    return {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4), "us": round(t * 1e6, 2),
+            "bytes": b}
+
+
+def row_ple(q4w, synth, dev, hbm, clocks, reps=10):
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     p = synth.ple_inputs(seed=1002, device=dev)
     ncp = max(2, math.ceil(2 * l2 / p.proj.numel() / 4))
     projs = [p.proj.clone() for _ in range(ncp)]
     out = torch.empty((64, 8960), dtype=torch.float32, device=dev)
     t = _time_graph(lambda: [q4w.ple_gather_project(p.ids, p.table, p.row_scale, pj, p.hidden,
-                                                    p.norm_w, out=out) for pj in projs], 10) / ncp
+                                                    p.norm_w, out=out) for pj in projs], reps) / ncp
     b = 64 * 8960 + 64 * 4 + p.proj.numel() * 4 + 64 * 1536 * 2 + 256 * 4 + 64 * 8960 * 4 + 64 * 4
     flops = 2 * 64 * 8960 * 1536
     sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
     fp32_peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * sm_mhz * 1e6
-    rows["ple_s64"] = {"GB/s": round(b / t / 1e9, 1), "TFLOP/s": round(flops / t / 1e12, 2),
-                       "fp32_peak_TFLOP/s": round(fp32_peak / 1e12, 1),
-                       "frac": round(max(b / t / 1e9 / hbm, flops / t / fp32_peak), 4),
-                       "bound": "alu (fp32 FFMA)", "us": round(t * 1e6, 2), "bytes": b}
-    del p, projs
+    return {"GB/s": round(b / t / 1e9, 1), "TFLOP/s": round(flops / t / 1e12, 2),
+            "fp32_peak_TFLOP/s": round(fp32_peak / 1e12, 1),
+            "frac": round(max(b / t / 1e9 / hbm, flops / t / fp32_peak), 4),
+            "bound": "alu (fp32 FFMA)", "us": round(t * 1e6, 2), "bytes": b}
+
+
+def row_gemm(q4w, synth, dev, hbm, bf16_peak, N, K, reps=10):
+    """S=64 prefill GEMM; small weights rotate over copies beyond L2."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    W, X = synth.gemm_inputs(seed=1005, device=dev, N=N, K=K)
+    c, s = q4w.q4_quantize(W)
+    del W
+    per = c.numel() + s.numel() * 2
+    copies = max(1, math.ceil(2 * l2 / per)) if per < l2 else 1
+    cs = [(c, s)] + [(c.clone(), s.clone()) for _ in range(copies - 1)]
+    Y = torch.empty((64, N), dtype=torch.float32, device=dev)
+    t = _time_graph(lambda: [q4w.q4_gemm_chunk(ci, si, X, Y) for ci, si in cs], reps) / copies
+    b = per + 64 * K * 2 + 64 * N * 4
+    flops = 2 * 64 * N * K
+    return {"GB/s": round(b / t / 1e9, 1), "TFLOP/s": round(flops / t / 1e12, 2),
+            "frac_hbm": round(b / t / 1e9 / hbm, 4), "frac_bf16": round(flops / t / 1e12 / bf16_peak, 4),
+            "us": round(t * 1e6, 2), "bytes": b, "flops": flops, "copies": copies}
+
+
+def measure_rows(q4w, synth, dev, hbm, clocks, bf16_peak):
+    rows = {"gemv_2048x1536": row_gemv(q4w, synth, dev, hbm)}
+    Wh, _ = synth.head_inputs(seed=1004, device=dev, batch=1)
+    hw = q4w.q4_quantize(Wh)
+    del Wh
+    rows["lmhead_b1"] = row_head(q4w, synth, dev, hbm, 1, weights=hw)
+    rows["lmhead_b8"] = row_head(q4w, synth, dev, hbm, 8, weights=hw)
+    del hw
+    rows["ple_s64"] = row_ple(q4w, synth, dev, hbm, clocks)
+    for name, (N, K) in (("gemm_s64_up", (6144, 1536)), ("gemm_s64_down", (1536, 6144)),
+                         ("gemm_s64_head", (262144, 1536))):
+        rows[name] = row_gemm(q4w, synth, dev, hbm, bf16_peak, N, K)
     return rows
+
+
+CASES = ("gemv", "head_b1", "head_b8", "ple", "gemm_up", "gemm_down", "gemm_head")
+
+
+def run_case(args):
+    """One row's workload only (used for single-kernel profiling captures)."""
+    import torch
+    import int4_q4_weight_gb300 as q4w
+    from int4_q4_weight_gb300 import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    q4w.build()
+    q4w.load()
+    peaks, _ = measured_peaks()
+    hbm, bf16 = float(peaks["hbm_gbs"]), float(peaks.get("bf16_tflops", 1900.0))
+    reps = max(1, args.steps)
+    if args.case == "gemv":
+        r = row_gemv(q4w, synth, dev, hbm, reps)
+    elif args.case in ("head_b1", "head_b8"):
+        r = row_head(q4w, synth, dev, hbm, 1 if args.case == "head_b1" else 8, reps)
+    elif args.case == "ple":
+        r = row_ple(q4w, synth, dev, hbm, None, reps)
+    else:
+        N, K = {"gemm_up": (6144, 1536), "gemm_down": (1536, 6144), "gemm_head": (262144, 1536)}[args.case]
+        r = row_gemm(q4w, synth, dev, hbm, bf16, N, K, reps)
+    print(json.dumps({"case": args.case, **r}), flush=True)
 
 
 # ------------------------------------------------------ reference arm ---
@@ -457,12 +519,17 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="time one row's workload only (--steps = graph replays), for profiling")
     ap.add_argument("--layers", type=int, default=35,
                     help="run only the last N E2B layers (a small case for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
+    if args.case:
+        run_case(args)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank, local)
     else:
