@@ -120,11 +120,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
-__device__ __forceinline__ float lds_half(const uint8_t* p) {
-  return __half2float(*reinterpret_cast<const __half*>(p));
-}
-
 // ------------------------------------------------------------- geometry ---
 struct Geo {
   int K2, nb, P, Gc, T, total, lo, hi;
@@ -301,19 +296,124 @@ struct HeadEpi {
   }
 };
 
-// Processes one stage's tiles; false when aborting (uniform over consumers).
-template <int NM, class Epi>
-__device__ bool consume_stage(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
-                              uint32_t empty0, const float* xs, float* red, const Ctl& c, const Epi& epi) {
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ float lds_half(const uint8_t* p) {
+  return __half2float(*reinterpret_cast<const __half*>(p));
+}
+
+// Fast consumer: P lanes per row, BPL blocks per lane, nb == P * BPL exactly.
+// Rows are taken two at a time (independent chains); for P <= 32 the row
+// loop is uniform across the warp so shuffles use the full mask.  The tile
+// handshake is per warp (P <= 32) or per row group (P > 32); the stage result
+// is made uniform over all consumers at the end.
+template <int NM, int P, int BPL, class Epi>
+__device__ bool consume_fast(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
+                             uint32_t empty0, const float* xs, float* red, const Ctl& c, const Epi& epi) {
+  constexpr int Gc = kCT / P;
+  constexpr int GW = P <= 32 ? 32 / P : 1;       // groups per warp
+  constexpr int WPG = P > 32 ? P / 32 : 1;       // warps per group
   const Geo g = make_geo(a, NM);
-  const int ct = threadIdx.x, lane = ct & 31;
-  const int gid = ct / g.P, li = ct % g.P;
-  const unsigned gmask = g.P >= 32 ? 0xffffffffu : (((1u << g.P) - 1u) << (lane & ~(g.P - 1)));
+  const int ct = threadIdx.x, lane = ct & 31, warp = ct >> 5;
+  const int gid = ct / P, li = ct % P;
+  float4 xr[BPL][8];
+  float bias[BPL];
+#pragma unroll
+  for (int b = 0; b < BPL; ++b) load_xblock(xs, li + P * b, xr[b], bias[b]);
+  const int K2 = g.K2, nb = g.nb;
+  const int row_first = P <= 32 ? warp * GW : gid;   // first row (group base) this warp walks
+  const int row_lane = P <= 32 ? lane / P : 0;       // offset of this lane's group
+  bool ok = true;
+  int pos = g.lo, m, r0, n;
+  while (tile_next(a, g, pos, m, r0, n)) {
+    const uint32_t s = gcount % kSlots, round = gcount / kSlots;
+    const bool landed = mbar_wait(full0 + 8 * s, round & 1, c);
+    const bool all = (P <= 32) ? (__all_sync(0xffffffffu, landed) != 0) : bar_and(2 + gid, P, landed);
+    if (!all) {
+      ok = false;
+      break;
+    }
+    const uint8_t* S = slots + (size_t)s * kSlotBytes;
+    const int per = n * (K2 + nb * 2);
+    for (int rb = row_first; rb < n; rb += 2 * Gc) {
+      const int ra = rb + row_lane, rc = ra + Gc;
+      const bool va = ra < n, vc = rc < n;
+      float acc[2][NM];
+#pragma unroll
+      for (int t = 0; t < NM; ++t) acc[0][t] = acc[1][t] = 0.f;
+#pragma unroll
+      for (int b = 0; b < BPL; ++b) {
+        const int j = li + P * b;
+#pragma unroll
+        for (int t = 0; t < NM; ++t) {
+          const uint8_t* base = S + t * per;
+          if (va) {
+            const uint4 cw = lds128(base + ra * K2 + 16 * j);
+            const float d = lds_half(base + n * K2 + (ra * nb + j) * 2);
+            acc[0][t] = fmaf(d, q4_block_dot(cw, xr[b], bias[b]), acc[0][t]);
+          }
+          if (vc) {
+            const uint4 cw = lds128(base + rc * K2 + 16 * j);
+            const float d = lds_half(base + n * K2 + (rc * nb + j) * 2);
+            acc[1][t] = fmaf(d, q4_block_dot(cw, xr[b], bias[b]), acc[1][t]);
+          }
+        }
+      }
+      if (P <= 32) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int t = 0; t < NM; ++t)
+#pragma unroll
+            for (int o = P / 2; o > 0; o >>= 1) acc[q][t] += __shfl_xor_sync(0xffffffffu, acc[q][t], o);
+      } else {
+        const int wig = warp - gid * WPG;
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int t = 0; t < NM; ++t) {
+            acc[q][t] = warp_sum(acc[q][t]);
+            if (lane == 0) red[((gid * WPG + wig) * 2 + q) * NM + t] = acc[q][t];
+          }
+        bar_sync(2 + gid, P);
+        if (li == 0) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+#pragma unroll
+            for (int t = 0; t < NM; ++t) {
+              float v = 0.f;
+#pragma unroll
+              for (int w = 0; w < WPG; ++w) v += red[((gid * WPG + w) * 2 + q) * NM + t];
+              acc[q][t] = v;
+            }
+        }
+        bar_sync(2 + gid, P);
+      }
+      if (li == 0) {
+        if (va) epi.template operator()<NM>(m, r0 + ra, acc[0]);
+        if (vc) epi.template operator()<NM>(m, r0 + rc, acc[1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    ++gcount;
+  }
+  return bar_and(1, kCT, ok);
+}
+
+// Generic consumer for any K % 256 == 0 up to kMaxNb blocks: runtime P,
+// up to kBPL blocks per lane with masking, one row at a time.
+template <int NM, class Epi>
+__device__ bool consume_generic(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
+                                uint32_t empty0, const float* xs, float* red, const Ctl& c, const Epi& epi) {
+  const Geo g = make_geo(a, NM);
+  const int ct = threadIdx.x, lane = ct & 31, warp = ct >> 5;
+  const int P = g.P, Gc = g.Gc;
+  const int gid = ct / P, li = ct % P;
   float4 xr[kBPL][8];
   float bias[kBPL];
 #pragma unroll
   for (int b = 0; b < kBPL; ++b) {
-    const int j = li + g.P * b;
+    const int j = li + P * b;
     if (j < g.nb) {
       load_xblock(xs, j, xr[b], bias[b]);
     } else {
@@ -322,21 +422,31 @@ __device__ bool consume_stage(const StageArgs& a, uint32_t& gcount, const uint8_
       bias[b] = 0.f;
     }
   }
+  const int GW = P <= 32 ? 32 / P : 1, WPG = P > 32 ? P / 32 : 1;
+  const int row_first = P <= 32 ? warp * GW : gid;
+  const int row_lane = P <= 32 ? lane / P : 0;
+  bool ok = true;
   int pos = g.lo, m, r0, n;
   while (tile_next(a, g, pos, m, r0, n)) {
     const uint32_t s = gcount % kSlots, round = gcount / kSlots;
     const bool landed = mbar_wait(full0 + 8 * s, round & 1, c);
-    if (!bar_and(1, kCT, landed)) return false;
+    const bool all = (P <= 32) ? (__all_sync(0xffffffffu, landed) != 0) : bar_and(2 + gid, P, landed);
+    if (!all) {
+      ok = false;
+      break;
+    }
     const uint8_t* S = slots + (size_t)s * kSlotBytes;
     const int per = n * (g.K2 + g.nb * 2);
-    for (int r = gid; r < n; r += g.Gc) {
+    for (int rb = row_first; rb < n; rb += Gc) {
+      const int r = rb + row_lane;
+      const bool v = r < n;
       float acc[NM];
 #pragma unroll
       for (int t = 0; t < NM; ++t) acc[t] = 0.f;
 #pragma unroll
       for (int b = 0; b < kBPL; ++b) {
-        const int j = li + g.P * b;
-        if (j < g.nb) {
+        const int j = li + P * b;
+        if (v && j < g.nb) {
 #pragma unroll
           for (int t = 0; t < NM; ++t) {
             const uint8_t* base = S + t * per;
@@ -346,35 +456,49 @@ __device__ bool consume_stage(const StageArgs& a, uint32_t& gcount, const uint8_
           }
         }
       }
-      if (g.P <= 32) {
+      if (P <= 32) {
 #pragma unroll
         for (int t = 0; t < NM; ++t)
-          for (int o = g.P >> 1; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(gmask, acc[t], o);
+          for (int o = P >> 1; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
       } else {
-        const int wpg = g.P >> 5, wig = (ct >> 5) - gid * wpg;
+        const int wig = warp - gid * WPG;
 #pragma unroll
         for (int t = 0; t < NM; ++t) {
           acc[t] = warp_sum(acc[t]);
-          if (lane == 0) red[(gid * wpg + wig) * NM + t] = acc[t];
+          if (lane == 0) red[(gid * WPG + wig) * NM + t] = acc[t];
         }
-        bar_sync(2 + gid, g.P);
+        bar_sync(2 + gid, P);
         if (li == 0) {
 #pragma unroll
           for (int t = 0; t < NM; ++t) {
-            float v = 0.f;
-            for (int w = 0; w < wpg; ++w) v += red[(gid * wpg + w) * NM + t];
-            acc[t] = v;
+            float vv = 0.f;
+            for (int w = 0; w < WPG; ++w) vv += red[(gid * WPG + w) * NM + t];
+            acc[t] = vv;
           }
         }
-        bar_sync(2 + gid, g.P);
+        bar_sync(2 + gid, P);
       }
-      if (li == 0) epi.template operator()<NM>(m, r0 + r, acc);
+      if (li == 0 && v) epi.template operator()<NM>(m, r0 + r, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
     ++gcount;
   }
-  return true;
+  return bar_and(1, kCT, ok);
+}
+
+// Processes one stage's tiles; false when aborting (uniform over consumers).
+template <int NM, class Epi>
+__device__ bool consume_stage(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
+                              uint32_t empty0, const float* xs, float* red, const Ctl& c, const Epi& epi) {
+  switch (a.K) {
+    case 1536: return consume_fast<NM, 16, 3>(a, gcount, slots, full0, empty0, xs, red, c, epi);
+    case 2048: return consume_fast<NM, 32, 2>(a, gcount, slots, full0, empty0, xs, red, c, epi);
+    case 4096: return consume_fast<NM, 64, 2>(a, gcount, slots, full0, empty0, xs, red, c, epi);
+    case 6144: return consume_fast<NM, 64, 3>(a, gcount, slots, full0, empty0, xs, red, c, epi);
+    case 12288: return consume_fast<NM, 128, 3>(a, gcount, slots, full0, empty0, xs, red, c, epi);
+    default: return consume_generic<NM>(a, gcount, slots, full0, empty0, xs, red, c, epi);
+  }
 }
 
 // ---------------------------------------------------------- shared memory ---
@@ -385,16 +509,18 @@ struct Smem {
   uint32_t slots0, full0, empty0;
 };
 
+// Carves the dynamic shared memory (declared 1024-byte aligned) by offsets so
+// that the compiler keeps shared-space loads.
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
   Smem s;
-  uint8_t* p = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 127) & ~(uintptr_t)127);
-  s.slots = p;
-  p += (size_t)kSlots * kSlotBytes;
-  s.xs = reinterpret_cast<float*>(p);
-  p += kXsBytes;
-  s.red = reinterpret_cast<float*>(p);
-  p += 64 * sizeof(float);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(p);
+  size_t off = 0;
+  s.slots = raw + off;
+  off += (size_t)kSlots * kSlotBytes;
+  s.xs = reinterpret_cast<float*>(raw + off);
+  off += kXsBytes;
+  s.red = reinterpret_cast<float*>(raw + off);
+  off += 64 * sizeof(float);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + off);
   s.slots0 = smem_u32(s.slots);
   s.full0 = smem_u32(bars);
   s.empty0 = smem_u32(bars + kSlots);
@@ -414,7 +540,7 @@ __device__ __forceinline__ void init_barriers(const Smem& S) {
 // ------------------------------------------------------- single stage ---
 template <int NM>
 __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a, long long limit, unsigned* err) {
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int abort_sh;
   const Smem S = carve(smem_raw);
   if (threadIdx.x == 0) abort_sh = 0;
@@ -443,7 +569,7 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
 __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, float cap, float* logits,
                                                             Top2* partials, unsigned* ticket, int32_t* idx,
                                                             float* top1, float* top2, long long limit, unsigned* err) {
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int abort_sh;
   __shared__ Top2 st[kTS];
   const Smem S = carve(smem_raw);
@@ -576,7 +702,7 @@ __device__ bool wait_counter(const int* cnt, int target, const Ctl& c) {
 }
 
 __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_constant__ MegaArgs A) {
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int abort_sh;
   const Smem S = carve(smem_raw);
   if (threadIdx.x == 0) abort_sh = 0;

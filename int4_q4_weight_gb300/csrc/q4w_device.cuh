@@ -72,26 +72,27 @@ __device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
 // sum_k (code_k - 8) * x_k over one 32-column block.
 // c: the block's 16 code bytes (column 2j in the low nibble of byte j).
 // xv: x of the block as 8 float4 (columns 4t..4t+3 in xv[t]).
-// Four independent accumulator pairs (one per 32-bit word of codes) keep the
-// dependent FMA chain four deep; they are summed pairwise at the end.
+// Four independent accumulators (one per 32-bit word of codes, eight FMAs
+// deep) are summed pairwise at the end.
 __device__ __forceinline__ float q4_block_dot(const uint4 c, const float4 (&xv)[8], float bias) {
   const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
-  f2_t acc[4];
+  float a[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t w = w4[i];          // columns 8i .. 8i+7, nibble j = column 8i+j
     const uint32_t s0 = w << 15, s1 = w << 7, s2 = w >> 1, s3 = w >> 9;
-    f2_t a = f2_pack(i == 0 ? bias : 0.f, 0.f);
-    a = f2_fma(f2_pack(nib_even(s0), nib_odd(s0)), f2_pack(xv[2 * i].x, xv[2 * i].y), a);
-    a = f2_fma(f2_pack(nib_even(s1), nib_odd(s1)), f2_pack(xv[2 * i].z, xv[2 * i].w), a);
-    a = f2_fma(f2_pack(nib_even(s2), nib_odd(s2)), f2_pack(xv[2 * i + 1].x, xv[2 * i + 1].y), a);
-    a = f2_fma(f2_pack(nib_even(s3), nib_odd(s3)), f2_pack(xv[2 * i + 1].z, xv[2 * i + 1].w), a);
-    acc[i] = a;
+    float t = i == 0 ? bias : 0.f;
+    t = fmaf(nib_even(s0), xv[2 * i].x, t);
+    t = fmaf(nib_odd(s0), xv[2 * i].y, t);
+    t = fmaf(nib_even(s1), xv[2 * i].z, t);
+    t = fmaf(nib_odd(s1), xv[2 * i].w, t);
+    t = fmaf(nib_even(s2), xv[2 * i + 1].x, t);
+    t = fmaf(nib_odd(s2), xv[2 * i + 1].y, t);
+    t = fmaf(nib_even(s3), xv[2 * i + 1].z, t);
+    t = fmaf(nib_odd(s3), xv[2 * i + 1].w, t);
+    a[i] = t;
   }
-  const f2_t t = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
-  float lo, hi;
-  f2_unpack(t, lo, hi);
-  return lo + hi;
+  return (a[0] + a[1]) + (a[2] + a[3]);
 }
 
 __device__ __forceinline__ void load_xblock(const float* xs, int blk, float4 (&xv)[8], float& bias) {
