@@ -28,14 +28,17 @@ namespace q4w {
 
 namespace eng {
 
-constexpr int kCW = 8;                    // consumer warps
+constexpr int kCW = 12;                   // consumer warps
 constexpr int kCT = kCW * 32;             // consumer threads
 constexpr int kTS = kCT + 32;             // threads per CTA
 constexpr int kSlots = 5;
 constexpr int kSlotBytes = 28 * 1024;
 constexpr int kMaxNb = 384;               // K <= 12288 on this path
 constexpr int kBPL = 3;                   // blocks per lane (upper bound)
-constexpr size_t kXsBytes = (size_t)kMaxNb * kXStride * sizeof(float);
+constexpr int kXhStride = 20;             // uint32 per block: 16 half pairs, bias, 3 pad (80 B:
+                                          // 8 lanes reading 8 consecutive blocks hit 8 bank groups)
+constexpr size_t kXhalfBytes = (size_t)kMaxNb * 32 * sizeof(__half);
+constexpr size_t kXsBytes = kXhalfBytes + (size_t)kMaxNb * kXhStride * sizeof(uint32_t);
 constexpr size_t kSmemBytes = 128 + (size_t)kSlots * kSlotBytes + kXsBytes + 64 * sizeof(float) +
                               2 * kSlots * sizeof(uint64_t) + 64;
 constexpr long long kDrainCycles = 2000000000LL;   // in-flight copies always land well within this
@@ -225,11 +228,13 @@ __device__ __forceinline__ float load_in_cg(const void* in, int mode, int k) {
   return __ldcg(reinterpret_cast<const float*>(in) + k);
 }
 
-// x = prologue(in) into the padded shared layout with per-block biases.
-__device__ void eng_prologue(const void* in, int mode, int K, float eps, float* xs, float* red8) {
+// x = prologue(in) as fp16 into xhalf, then per block the half pairs
+// (x[8i+j], x[8i+j+4]) and the bias -72 * sum(x) into xh (kXhStride words).
+__device__ void eng_prologue(const void* in, int mode, int K, float eps, __half* xhalf, uint32_t* xh,
+                             float* red8) {
   const int tid = threadIdx.x;
   if (mode == Q4_IN_F16) {
-    for (int k = tid; k < K; k += kCT) xs_store(xs, k, load_in_cg(in, mode, k));
+    for (int k = tid; k < K; k += kCT) xhalf[k] = __float2half_rn(load_in_cg(in, mode, k));
   } else {
     float ss = 0.f;
     for (int k = tid; k < K; k += kCT) {
@@ -239,32 +244,51 @@ __device__ void eng_prologue(const void* in, int mode, int K, float eps, float* 
     ss = consumer_sum(ss, red8);
     const float r = 1.f / sqrtf(ss / (float)K + eps);
     if (mode != Q4_IN_RMS2_F32) {
-      for (int k = tid; k < K; k += kCT) xs_store(xs, k, f16_round(load_in_cg(in, mode, k) * r));
+      for (int k = tid; k < K; k += kCT) xhalf[k] = __float2half_rn(load_in_cg(in, mode, k) * r);
     } else {
       float ss2 = 0.f;
       for (int k = tid; k < K; k += kCT) {
-        const float t = f16_round(load_in_cg(in, mode, k) * r);
-        xs_store(xs, k, t);
-        ss2 += t * t;
+        const __half t = __float2half_rn(load_in_cg(in, mode, k) * r);
+        xhalf[k] = t;
+        const float tf = __half2float(t);
+        ss2 += tf * tf;
       }
       ss2 = consumer_sum(ss2, red8);
       const float r2 = 1.f / sqrtf(ss2 / (float)K + eps);
-      for (int k = tid; k < K; k += kCT) xs_store(xs, k, f16_round(xs_load(xs, k) * r2));
+      for (int k = tid; k < K; k += kCT) xhalf[k] = __float2half_rn(__half2float(xhalf[k]) * r2);
     }
   }
   bar_sync(1, kCT);
   const int nb = K >> 5;
   for (int b = tid; b < nb; b += kCT) {
-    const float* p = xs + b * kXStride;
-    float se = 0.f, so = 0.f;
+    const __half* p = xhalf + 32 * b;
+    uint32_t* q = xh + b * kXhStride;
+    float sum = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      se += p[2 * i];
-      so += p[2 * i + 1];
-    }
-    xs[b * kXStride + 32] = -264.f * se - 24.f * so;
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half a = p[8 * i + j], c = p[8 * i + j + 4];
+        q[4 * i + j] = (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(c) << 16);
+      }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) sum += __half2float(p[k]);
+    q[16] = __float_as_uint(-72.f * sum);
   }
   bar_sync(1, kCT);
+}
+
+__device__ __forceinline__ void load_xh(const uint32_t* xh, int blk, uint32_t (&v)[16], float& bias) {
+  const uint4* p = reinterpret_cast<const uint4*>(xh + blk * kXhStride);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint4 u = p[t];
+    v[4 * t] = u.x;
+    v[4 * t + 1] = u.y;
+    v[4 * t + 2] = u.z;
+    v[4 * t + 3] = u.w;
+  }
+  bias = __uint_as_float(xh[blk * kXhStride + 16]);
 }
 
 struct StageEpi {
@@ -308,17 +332,17 @@ __device__ __forceinline__ float lds_half(const uint8_t* p) {
 // is made uniform over all consumers at the end.
 template <int NM, int P, int BPL, class Epi>
 __device__ bool consume_fast(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
-                             uint32_t empty0, const float* xs, float* red, const Ctl& c, const Epi& epi) {
+                             uint32_t empty0, const uint32_t* xs, float* red, const Ctl& c, const Epi& epi) {
   constexpr int Gc = kCT / P;
   constexpr int GW = P <= 32 ? 32 / P : 1;       // groups per warp
   constexpr int WPG = P > 32 ? P / 32 : 1;       // warps per group
   const Geo g = make_geo(a, NM);
   const int ct = threadIdx.x, lane = ct & 31, warp = ct >> 5;
   const int gid = ct / P, li = ct % P;
-  float4 xr[BPL][8];
+  uint32_t xr[BPL][16];
   float bias[BPL];
 #pragma unroll
-  for (int b = 0; b < BPL; ++b) load_xblock(xs, li + P * b, xr[b], bias[b]);
+  for (int b = 0; b < BPL; ++b) load_xh(xs, li + P * b, xr[b], bias[b]);
   const int K2 = g.K2, nb = g.nb;
   const int row_first = P <= 32 ? warp * GW : gid;   // first row (group base) this warp walks
   const int row_lane = P <= 32 ? lane / P : 0;       // offset of this lane's group
@@ -337,6 +361,8 @@ __device__ bool consume_fast(const StageArgs& a, uint32_t& gcount, const uint8_t
     for (int rb = row_first; rb < n; rb += 2 * Gc) {
       const int ra = rb + row_lane, rc = ra + Gc;
       const bool va = ra < n, vc = rc < n;
+      // rows past the tile read the tile's last row (in bounds) and are dropped
+      const int la = va ? ra : n - 1, lc = vc ? rc : n - 1;
       float acc[2][NM];
 #pragma unroll
       for (int t = 0; t < NM; ++t) acc[0][t] = acc[1][t] = 0.f;
@@ -346,16 +372,12 @@ __device__ bool consume_fast(const StageArgs& a, uint32_t& gcount, const uint8_t
 #pragma unroll
         for (int t = 0; t < NM; ++t) {
           const uint8_t* base = S + t * per;
-          if (va) {
-            const uint4 cw = lds128(base + ra * K2 + 16 * j);
-            const float d = lds_half(base + n * K2 + (ra * nb + j) * 2);
-            acc[0][t] = fmaf(d, q4_block_dot(cw, xr[b], bias[b]), acc[0][t]);
-          }
-          if (vc) {
-            const uint4 cw = lds128(base + rc * K2 + 16 * j);
-            const float d = lds_half(base + n * K2 + (rc * nb + j) * 2);
-            acc[1][t] = fmaf(d, q4_block_dot(cw, xr[b], bias[b]), acc[1][t]);
-          }
+          const uint4 ca = lds128(base + la * K2 + 16 * j);
+          const uint4 cc = lds128(base + lc * K2 + 16 * j);
+          const float da = lds_half(base + n * K2 + (la * nb + j) * 2);
+          const float dc = lds_half(base + n * K2 + (lc * nb + j) * 2);
+          acc[0][t] = fmaf(da, q4_block_dot_h(ca, xr[b], bias[b]), acc[0][t]);
+          acc[1][t] = fmaf(dc, q4_block_dot_h(cc, xr[b], bias[b]), acc[1][t]);
         }
       }
       if (P <= 32) {
@@ -404,21 +426,21 @@ __device__ bool consume_fast(const StageArgs& a, uint32_t& gcount, const uint8_t
 // up to kBPL blocks per lane with masking, one row at a time.
 template <int NM, class Epi>
 __device__ bool consume_generic(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
-                                uint32_t empty0, const float* xs, float* red, const Ctl& c, const Epi& epi) {
+                                uint32_t empty0, const uint32_t* xs, float* red, const Ctl& c, const Epi& epi) {
   const Geo g = make_geo(a, NM);
   const int ct = threadIdx.x, lane = ct & 31, warp = ct >> 5;
   const int P = g.P, Gc = g.Gc;
   const int gid = ct / P, li = ct % P;
-  float4 xr[kBPL][8];
+  uint32_t xr[kBPL][16];
   float bias[kBPL];
 #pragma unroll
   for (int b = 0; b < kBPL; ++b) {
     const int j = li + P * b;
     if (j < g.nb) {
-      load_xblock(xs, j, xr[b], bias[b]);
+      load_xh(xs, j, xr[b], bias[b]);
     } else {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) xr[b][t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int t = 0; t < 16; ++t) xr[b][t] = 0u;
       bias[b] = 0.f;
     }
   }
@@ -452,7 +474,7 @@ __device__ bool consume_generic(const StageArgs& a, uint32_t& gcount, const uint
             const uint8_t* base = S + t * per;
             const uint4 cw = lds128(base + r * g.K2 + 16 * j);
             const float d = lds_half(base + n * g.K2 + (r * g.nb + j) * 2);
-            acc[t] = fmaf(d, q4_block_dot(cw, xr[b], bias[b]), acc[t]);
+            acc[t] = fmaf(d, q4_block_dot_h(cw, xr[b], bias[b]), acc[t]);
           }
         }
       }
@@ -490,7 +512,7 @@ __device__ bool consume_generic(const StageArgs& a, uint32_t& gcount, const uint
 // Processes one stage's tiles; false when aborting (uniform over consumers).
 template <int NM, class Epi>
 __device__ bool consume_stage(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
-                              uint32_t empty0, const float* xs, float* red, const Ctl& c, const Epi& epi) {
+                              uint32_t empty0, const uint32_t* xs, float* red, const Ctl& c, const Epi& epi) {
   switch (a.K) {
     case 1536: return consume_fast<NM, 16, 3>(a, gcount, slots, full0, empty0, xs, red, c, epi);
     case 2048: return consume_fast<NM, 32, 2>(a, gcount, slots, full0, empty0, xs, red, c, epi);
@@ -504,7 +526,8 @@ __device__ bool consume_stage(const StageArgs& a, uint32_t& gcount, const uint8_
 // ---------------------------------------------------------- shared memory ---
 struct Smem {
   uint8_t* slots;
-  float* xs;
+  __half* xhalf;
+  uint32_t* xs;   // half pairs + bias per block
   float* red;
   uint32_t slots0, full0, empty0;
 };
@@ -516,7 +539,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   size_t off = 0;
   s.slots = raw + off;
   off += (size_t)kSlots * kSlotBytes;
-  s.xs = reinterpret_cast<float*>(raw + off);
+  s.xhalf = reinterpret_cast<__half*>(raw + off);
+  s.xs = reinterpret_cast<uint32_t*>(raw + off + kXhalfBytes);
   off += kXsBytes;
   s.red = reinterpret_cast<float*>(raw + off);
   off += 64 * sizeof(float);
@@ -558,7 +582,7 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
     __syncwarp();
   } else {
     pdl_wait();
-    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
+    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xhalf, S.xs, S.red);
     StageEpi epi{&a};
     consume_stage<NM>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
   }
@@ -588,7 +612,7 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
     }
     __syncwarp();
   } else {
-    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
+    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xhalf, S.xs, S.red);
     HeadEpi epi{&best, logits, cap};
     consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
   }
@@ -728,7 +752,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
     for (int s = 0; s < nst && ok; ++s) {
       const StageArgs a = mega_stage(A, s);
       if (s > 0 && !wait_counter(A.counters + s - 1, (int)gridDim.x, c)) break;
-      eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
+      eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xhalf, S.xs, S.red);
       StageEpi epi{&a};
       ok = a.pair ? consume_stage<2>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
                   : consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);

@@ -95,6 +95,56 @@ __device__ __forceinline__ float q4_block_dot(const uint4 c, const float4 (&xv)[
   return (a[0] + a[1]) + (a[2] + a[3]);
 }
 
+
+// ---------------------------------------------- fp16-magic block dot (fast) ---
+// Two codes per LOP3: a 32-bit word of codes shifted so that nibbles j and
+// j+4 sit in bits [4,8) and [20,24) is OR-ed into two fp16 64.0 patterns,
+// giving the half pair (64 + n_j, 64 + n_{j+4}) exactly.  Each half is
+// multiplied by the matching fp16 x with the mixed-precision fp32 FMA
+// (fma.rn.f32.f16: exact product, one fp32 rounding).  x is held as half
+// pairs xh[4i + j] = (x[8i+j], x[8i+j+4]); bias = -72 * sum(x over the block)
+// removes the 64 + 8 offset, so bias + sum F_k x_k = sum (code_k - 8) x_k.
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(magic));
+  return d;
+}
+__device__ __forceinline__ uint32_t shl_u32(uint32_t a, uint32_t n) {
+  uint32_t d;
+  asm("shl.b32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(n));
+  return d;
+}
+__device__ __forceinline__ uint32_t shr_u32(uint32_t a, uint32_t n) {
+  uint32_t d;
+  asm("shr.b32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(n));
+  return d;
+}
+__device__ __forceinline__ void fhfma2(float& lo, float& hi, uint32_t a, uint32_t b) {
+  asm("{\n .reg .f16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %2;\n mov.b32 {b0, b1}, %3;\n"
+      " fma.rn.f32.f16 %0, a0, b0, %0;\n fma.rn.f32.f16 %1, a1, b1, %1;\n}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(a), "r"(b));
+}
+
+constexpr uint32_t kH64Mask = 0x00F000F0u;
+constexpr uint32_t kH64Magic = 0x54005400u;   // fp16 64.0 in both halves
+
+__device__ __forceinline__ float q4_block_dot_h(const uint4 c, const uint32_t (&xh)[16], float bias) {
+  const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+  float lo[4], hi[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w = w4[i];
+    const uint32_t sh[4] = {shl_u32(w, 4), w, shr_u32(w, 4), shr_u32(w, 8)};
+    float t0 = i == 0 ? bias : 0.f, t1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) fhfma2(t0, t1, lop3_and_or(sh[j], kH64Mask, kH64Magic), xh[4 * i + j]);
+    lo[i] = t0;
+    hi[i] = t1;
+  }
+  return ((lo[0] + hi[0]) + (lo[1] + hi[1])) + ((lo[2] + hi[2]) + (lo[3] + hi[3]));
+}
+
 __device__ __forceinline__ void load_xblock(const float* xs, int blk, float4 (&xv)[8], float& bias) {
   const float4* p = reinterpret_cast<const float4*>(xs + blk * kXStride);
 #pragma unroll
