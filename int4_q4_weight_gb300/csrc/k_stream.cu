@@ -31,14 +31,13 @@ namespace eng {
 constexpr int kCW = 12;                   // consumer warps
 constexpr int kCT = kCW * 32;             // consumer threads
 constexpr int kTS = kCT + 32;             // threads per CTA
-constexpr int kSlots = 5;
-constexpr int kSlotBytes = 28 * 1024;
+constexpr int kSlots = 4;
+constexpr int kSlotBytes = 42 * 1024;
 constexpr int kMaxNb = 384;               // K <= 12288 on this path
 constexpr int kBPL = 3;                   // blocks per lane (upper bound)
 constexpr int kXhStride = 20;             // uint32 per block: 16 half pairs, bias, 3 pad (80 B:
                                           // 8 lanes reading 8 consecutive blocks hit 8 bank groups)
-constexpr size_t kXhalfBytes = (size_t)kMaxNb * 32 * sizeof(__half);
-constexpr size_t kXsBytes = kXhalfBytes + (size_t)kMaxNb * kXhStride * sizeof(uint32_t);
+constexpr size_t kXsBytes = (size_t)kMaxNb * kXhStride * sizeof(uint32_t);
 constexpr size_t kSmemBytes = 128 + (size_t)kSlots * kSlotBytes + kXsBytes + 64 * sizeof(float) +
                               2 * kSlots * sizeof(uint64_t) + 64;
 constexpr long long kDrainCycles = 2000000000LL;   // in-flight copies always land well within this
@@ -125,7 +124,7 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 
 // ------------------------------------------------------------- geometry ---
 struct Geo {
-  int K2, nb, P, Gc, T, total, lo, hi;
+  int K2, nb, P, Gc, R, T, total, lo, hi;
 };
 
 __device__ __forceinline__ int lanes_per_row(int nb) {
@@ -134,19 +133,24 @@ __device__ __forceinline__ int lanes_per_row(int nb) {
   return P;
 }
 
+// Rows in flight per row group (R) and rows per tile (T = Gc * R when it
+// fits a slot): two rows when every group gets at least two rows per CTA,
+// so a tile has no idle row slots except at the end of a CTA's range.
 __device__ __forceinline__ Geo make_geo(const StageArgs& a, int NM) {
   Geo g;
   g.K2 = a.K >> 1;
   g.nb = a.K >> 5;
   g.P = lanes_per_row(g.nb);
   g.Gc = kCT / g.P;
-  int T = kSlotBytes / (NM * (g.K2 + g.nb * 2));
-  g.T = T < 1 ? 1 : T;
   g.total = a.pair ? a.mat[0].rows : a.mat[0].rows + (a.nmat > 1 ? a.mat[1].rows : 0) +
                                          (a.nmat > 2 ? a.mat[2].rows : 0);
   const int rpc = (g.total + gridDim.x - 1) / gridDim.x;
   g.lo = min(g.total, (int)blockIdx.x * rpc);
   g.hi = min(g.total, g.lo + rpc);
+  const int row_bytes = NM * (g.K2 + g.nb * 2);
+  const int fit = kSlotBytes / row_bytes;
+  g.R = (rpc >= 2 * g.Gc && fit >= 2 * g.Gc) ? 2 : 1;
+  g.T = g.Gc * g.R <= fit ? g.Gc * g.R : (fit < 1 ? 1 : fit);
   return g;
 }
 
@@ -228,51 +232,50 @@ __device__ __forceinline__ float load_in_cg(const void* in, int mode, int k) {
   return __ldcg(reinterpret_cast<const float*>(in) + k);
 }
 
-// x = prologue(in) as fp16 into xhalf, then per block the half pairs
-// (x[8i+j], x[8i+j+4]) and the bias -72 * sum(x) into xh (kXhStride words).
-__device__ void eng_prologue(const void* in, int mode, int K, float eps, __half* xhalf, uint32_t* xh,
-                             float* red8) {
+// x = prologue(in), written per 32-column block as the half pairs
+// (x[8i+j], x[8i+j+4]) plus the bias -72 * sum(x) (kXhStride words).  The
+// fp16 rounding of each x is recomputed from the input where it is needed.
+__device__ __forceinline__ float prologue_x(const void* in, int mode, int k, float r, float r2) {
+  const float v = load_in_cg(in, mode, k);
+  if (mode == Q4_IN_F16) return v;
+  const float t = f16_round(v * r);
+  return mode == Q4_IN_RMS2_F32 ? f16_round(t * r2) : t;
+}
+
+__device__ void eng_prologue(const void* in, int mode, int K, float eps, uint32_t* xh, float* red8) {
   const int tid = threadIdx.x;
-  if (mode == Q4_IN_F16) {
-    for (int k = tid; k < K; k += kCT) xhalf[k] = __float2half_rn(load_in_cg(in, mode, k));
-  } else {
+  float r = 1.f, r2 = 1.f;
+  if (mode != Q4_IN_F16) {
     float ss = 0.f;
     for (int k = tid; k < K; k += kCT) {
       const float v = load_in_cg(in, mode, k);
       ss += v * v;
     }
     ss = consumer_sum(ss, red8);
-    const float r = 1.f / sqrtf(ss / (float)K + eps);
-    if (mode != Q4_IN_RMS2_F32) {
-      for (int k = tid; k < K; k += kCT) xhalf[k] = __float2half_rn(load_in_cg(in, mode, k) * r);
-    } else {
+    r = 1.f / sqrtf(ss / (float)K + eps);
+    if (mode == Q4_IN_RMS2_F32) {
       float ss2 = 0.f;
       for (int k = tid; k < K; k += kCT) {
-        const __half t = __float2half_rn(load_in_cg(in, mode, k) * r);
-        xhalf[k] = t;
-        const float tf = __half2float(t);
-        ss2 += tf * tf;
+        const float t = f16_round(load_in_cg(in, mode, k) * r);
+        ss2 += t * t;
       }
       ss2 = consumer_sum(ss2, red8);
-      const float r2 = 1.f / sqrtf(ss2 / (float)K + eps);
-      for (int k = tid; k < K; k += kCT) xhalf[k] = __float2half_rn(__half2float(xhalf[k]) * r2);
+      r2 = 1.f / sqrtf(ss2 / (float)K + eps);
     }
   }
-  bar_sync(1, kCT);
   const int nb = K >> 5;
   for (int b = tid; b < nb; b += kCT) {
-    const __half* p = xhalf + 32 * b;
     uint32_t* q = xh + b * kXhStride;
     float sum = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const __half a = p[8 * i + j], c = p[8 * i + j + 4];
+        const __half a = __float2half_rn(prologue_x(in, mode, 32 * b + 8 * i + j, r, r2));
+        const __half c = __float2half_rn(prologue_x(in, mode, 32 * b + 8 * i + j + 4, r, r2));
+        sum += __half2float(a) + __half2float(c);
         q[4 * i + j] = (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(c) << 16);
       }
-#pragma unroll
-    for (int k = 0; k < 32; ++k) sum += __half2float(p[k]);
     q[16] = __float_as_uint(-72.f * sum);
   }
   bar_sync(1, kCT);
@@ -330,13 +333,13 @@ __device__ __forceinline__ float lds_half(const uint8_t* p) {
 // loop is uniform across the warp so shuffles use the full mask.  The tile
 // handshake is per warp (P <= 32) or per row group (P > 32); the stage result
 // is made uniform over all consumers at the end.
-template <int NM, int P, int BPL, class Epi>
-__device__ bool consume_fast(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
-                             uint32_t empty0, const uint32_t* xs, float* red, const Ctl& c, const Epi& epi) {
+template <int NM, int P, int BPL, int R, class Epi>
+__device__ bool consume_fast(const StageArgs& a, const Geo& g, uint32_t& gcount, const uint8_t* slots,
+                             uint32_t full0, uint32_t empty0, const uint32_t* xs, float* red, const Ctl& c,
+                             const Epi& epi) {
   constexpr int Gc = kCT / P;
   constexpr int GW = P <= 32 ? 32 / P : 1;       // groups per warp
   constexpr int WPG = P > 32 ? P / 32 : 1;       // warps per group
-  const Geo g = make_geo(a, NM);
   const int ct = threadIdx.x, lane = ct & 31, warp = ct >> 5;
   const int gid = ct / P, li = ct % P;
   uint32_t xr[BPL][16];
@@ -344,8 +347,7 @@ __device__ bool consume_fast(const StageArgs& a, uint32_t& gcount, const uint8_t
 #pragma unroll
   for (int b = 0; b < BPL; ++b) load_xh(xs, li + P * b, xr[b], bias[b]);
   const int K2 = g.K2, nb = g.nb;
-  const int row_first = P <= 32 ? warp * GW : gid;   // first row (group base) this warp walks
-  const int row_lane = P <= 32 ? lane / P : 0;       // offset of this lane's group
+  const int row_first = P <= 32 ? warp * GW + lane / P : gid;   // this lane's first row of a tile
   bool ok = true;
   int pos = g.lo, m, r0, n;
   while (tile_next(a, g, pos, m, r0, n)) {
@@ -358,62 +360,72 @@ __device__ bool consume_fast(const StageArgs& a, uint32_t& gcount, const uint8_t
     }
     const uint8_t* S = slots + (size_t)s * kSlotBytes;
     const int per = n * (K2 + nb * 2);
-    for (int rb = row_first; rb < n; rb += 2 * Gc) {
-      const int ra = rb + row_lane, rc = ra + Gc;
-      const bool va = ra < n, vc = rc < n;
-      // rows past the tile read the tile's last row (in bounds) and are dropped
-      const int la = va ? ra : n - 1, lc = vc ? rc : n - 1;
-      float acc[2][NM];
+    const uint8_t* sc_base = S + n * K2;
+    // rows row_first + q * Gc (q < R); a partial last tile computes a clamped
+    // copy of its last row in the idle slots and drops the result
+    int rr[R];
+    bool vv[R];
 #pragma unroll
-      for (int t = 0; t < NM; ++t) acc[0][t] = acc[1][t] = 0.f;
+    for (int q = 0; q < R; ++q) {
+      const int r = row_first + q * Gc;
+      vv[q] = r < n;
+      rr[q] = vv[q] ? r : n - 1;
+    }
+    float acc[R][NM];
 #pragma unroll
-      for (int b = 0; b < BPL; ++b) {
-        const int j = li + P * b;
+    for (int q = 0; q < R; ++q)
+#pragma unroll
+      for (int t = 0; t < NM; ++t) acc[q][t] = 0.f;
+#pragma unroll
+    for (int b = 0; b < BPL; ++b) {
+      const int j = li + P * b;
+#pragma unroll
+      for (int t = 0; t < NM; ++t) {
+        uint4 cw[R];
+        float d[R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+          cw[q] = lds128(S + t * per + rr[q] * K2 + 16 * j);
+          d[q] = lds_half(sc_base + t * per + (rr[q] * nb + j) * 2);
+        }
+#pragma unroll
+        for (int q = 0; q < R; ++q) acc[q][t] = fmaf(d[q], q4_block_dot_h(cw[q], xr[b], bias[b]), acc[q][t]);
+      }
+    }
+    if (P <= 32) {
+#pragma unroll
+      for (int q = 0; q < R; ++q)
+#pragma unroll
+        for (int t = 0; t < NM; ++t)
+#pragma unroll
+          for (int o = P / 2; o > 0; o >>= 1) acc[q][t] += __shfl_xor_sync(0xffffffffu, acc[q][t], o);
+    } else {
+      const int wig = warp - gid * WPG;
+#pragma unroll
+      for (int q = 0; q < R; ++q)
 #pragma unroll
         for (int t = 0; t < NM; ++t) {
-          const uint8_t* base = S + t * per;
-          const uint4 ca = lds128(base + la * K2 + 16 * j);
-          const uint4 cc = lds128(base + lc * K2 + 16 * j);
-          const float da = lds_half(base + n * K2 + (la * nb + j) * 2);
-          const float dc = lds_half(base + n * K2 + (lc * nb + j) * 2);
-          acc[0][t] = fmaf(da, q4_block_dot_h(ca, xr[b], bias[b]), acc[0][t]);
-          acc[1][t] = fmaf(dc, q4_block_dot_h(cc, xr[b], bias[b]), acc[1][t]);
+          acc[q][t] = warp_sum(acc[q][t]);
+          if (lane == 0) red[((gid * WPG + wig) * R + q) * NM + t] = acc[q][t];
         }
-      }
-      if (P <= 32) {
+      bar_sync(2 + gid, P);
+      if (li == 0) {
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-          for (int t = 0; t < NM; ++t)
-#pragma unroll
-            for (int o = P / 2; o > 0; o >>= 1) acc[q][t] += __shfl_xor_sync(0xffffffffu, acc[q][t], o);
-      } else {
-        const int wig = warp - gid * WPG;
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < R; ++q)
 #pragma unroll
           for (int t = 0; t < NM; ++t) {
-            acc[q][t] = warp_sum(acc[q][t]);
-            if (lane == 0) red[((gid * WPG + wig) * 2 + q) * NM + t] = acc[q][t];
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < WPG; ++w) v += red[((gid * WPG + w) * R + q) * NM + t];
+            acc[q][t] = v;
           }
-        bar_sync(2 + gid, P);
-        if (li == 0) {
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int t = 0; t < NM; ++t) {
-              float v = 0.f;
-#pragma unroll
-              for (int w = 0; w < WPG; ++w) v += red[((gid * WPG + w) * 2 + q) * NM + t];
-              acc[q][t] = v;
-            }
-        }
-        bar_sync(2 + gid, P);
       }
-      if (li == 0) {
-        if (va) epi.template operator()<NM>(m, r0 + ra, acc[0]);
-        if (vc) epi.template operator()<NM>(m, r0 + rc, acc[1]);
-      }
+      bar_sync(2 + gid, P);
+    }
+    if (li == 0) {
+#pragma unroll
+      for (int q = 0; q < R; ++q)
+        if (vv[q]) epi.template operator()<NM>(m, r0 + rr[q], acc[q]);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
@@ -425,9 +437,9 @@ __device__ bool consume_fast(const StageArgs& a, uint32_t& gcount, const uint8_t
 // Generic consumer for any K % 256 == 0 up to kMaxNb blocks: runtime P,
 // up to kBPL blocks per lane with masking, one row at a time.
 template <int NM, class Epi>
-__device__ bool consume_generic(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
-                                uint32_t empty0, const uint32_t* xs, float* red, const Ctl& c, const Epi& epi) {
-  const Geo g = make_geo(a, NM);
+__device__ bool consume_generic(const StageArgs& a, const Geo& g, uint32_t& gcount, const uint8_t* slots,
+                                uint32_t full0, uint32_t empty0, const uint32_t* xs, float* red, const Ctl& c,
+                                const Epi& epi) {
   const int ct = threadIdx.x, lane = ct & 31, warp = ct >> 5;
   const int P = g.P, Gc = g.Gc;
   const int gid = ct / P, li = ct % P;
@@ -513,20 +525,27 @@ __device__ bool consume_generic(const StageArgs& a, uint32_t& gcount, const uint
 template <int NM, class Epi>
 __device__ bool consume_stage(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
                               uint32_t empty0, const uint32_t* xs, float* red, const Ctl& c, const Epi& epi) {
-  switch (a.K) {
-    case 1536: return consume_fast<NM, 16, 3>(a, gcount, slots, full0, empty0, xs, red, c, epi);
-    case 2048: return consume_fast<NM, 32, 2>(a, gcount, slots, full0, empty0, xs, red, c, epi);
-    case 4096: return consume_fast<NM, 64, 2>(a, gcount, slots, full0, empty0, xs, red, c, epi);
-    case 6144: return consume_fast<NM, 64, 3>(a, gcount, slots, full0, empty0, xs, red, c, epi);
-    case 12288: return consume_fast<NM, 128, 3>(a, gcount, slots, full0, empty0, xs, red, c, epi);
-    default: return consume_generic<NM>(a, gcount, slots, full0, empty0, xs, red, c, epi);
+  const Geo g = make_geo(a, NM);
+#define Q4W_FAST(P, BPL)                                                                              \
+  return g.R == 2 ? consume_fast<NM, P, BPL, 2>(a, g, gcount, slots, full0, empty0, xs, red, c, epi)  \
+                  : consume_fast<NM, P, BPL, 1>(a, g, gcount, slots, full0, empty0, xs, red, c, epi)
+  if (g.T == g.Gc * g.R) {
+    switch (a.K) {
+      case 1536: Q4W_FAST(16, 3);
+      case 2048: Q4W_FAST(32, 2);
+      case 4096: Q4W_FAST(64, 2);
+      case 6144: Q4W_FAST(64, 3);
+      case 12288: Q4W_FAST(128, 3);
+      default: break;
+    }
   }
+#undef Q4W_FAST
+  return consume_generic<NM>(a, g, gcount, slots, full0, empty0, xs, red, c, epi);
 }
 
 // ---------------------------------------------------------- shared memory ---
 struct Smem {
   uint8_t* slots;
-  __half* xhalf;
   uint32_t* xs;   // half pairs + bias per block
   float* red;
   uint32_t slots0, full0, empty0;
@@ -539,8 +558,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   size_t off = 0;
   s.slots = raw + off;
   off += (size_t)kSlots * kSlotBytes;
-  s.xhalf = reinterpret_cast<__half*>(raw + off);
-  s.xs = reinterpret_cast<uint32_t*>(raw + off + kXhalfBytes);
+  s.xs = reinterpret_cast<uint32_t*>(raw + off);
   off += kXsBytes;
   s.red = reinterpret_cast<float*>(raw + off);
   off += 64 * sizeof(float);
@@ -582,7 +600,7 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
     __syncwarp();
   } else {
     pdl_wait();
-    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xhalf, S.xs, S.red);
+    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
     StageEpi epi{&a};
     consume_stage<NM>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
   }
@@ -612,7 +630,7 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
     }
     __syncwarp();
   } else {
-    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xhalf, S.xs, S.red);
+    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
     HeadEpi epi{&best, logits, cap};
     consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
   }
@@ -752,7 +770,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
     for (int s = 0; s < nst && ok; ++s) {
       const StageArgs a = mega_stage(A, s);
       if (s > 0 && !wait_counter(A.counters + s - 1, (int)gridDim.x, c)) break;
-      eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xhalf, S.xs, S.red);
+      eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
       StageEpi epi{&a};
       ok = a.pair ? consume_stage<2>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
                   : consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
