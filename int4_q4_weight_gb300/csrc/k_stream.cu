@@ -263,20 +263,19 @@ __device__ void eng_prologue(const void* in, int mode, int K, float eps, uint32_
       r2 = 1.f / sqrtf(ss2 / (float)K + eps);
     }
   }
-  const int nb = K >> 5;
-  for (int b = tid; b < nb; b += kCT) {
-    uint32_t* q = xh + b * kXhStride;
-    float sum = 0.f;
+  // one thread per half pair; the 16 pairs of a block are 16 aligned lanes
+  // of one warp (nb * 16 is a multiple of 128 for K % 256 == 0)
+  const int npairs = (K >> 5) * 16;
+  for (int idx = tid; idx < npairs; idx += kCT) {
+    const int b = idx >> 4, pr = idx & 15, i = pr >> 2, j = pr & 3;
+    const int k = 32 * b + 8 * i + j;
+    const __half va = __float2half_rn(prologue_x(in, mode, k, r, r2));
+    const __half vc = __float2half_rn(prologue_x(in, mode, k + 4, r, r2));
+    xh[b * kXhStride + pr] = (uint32_t)__half_as_ushort(va) | ((uint32_t)__half_as_ushort(vc) << 16);
+    float sum = __half2float(va) + __half2float(vc);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __half a = __float2half_rn(prologue_x(in, mode, 32 * b + 8 * i + j, r, r2));
-        const __half c = __float2half_rn(prologue_x(in, mode, 32 * b + 8 * i + j + 4, r, r2));
-        sum += __half2float(a) + __half2float(c);
-        q[4 * i + j] = (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(c) << 16);
-      }
-    q[16] = __float_as_uint(-72.f * sum);
+    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (pr == 0) xh[b * kXhStride + 16] = __float_as_uint(-72.f * sum);
   }
   bar_sync(1, kCT);
 }
