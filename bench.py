@@ -426,7 +426,56 @@ def measure_rows(q4w, synth, dev, hbm, clocks, bf16_peak):
     return rows
 
 
-CASES = ("gemv", "head_b1", "head_b8", "ple", "gemm_up", "gemm_down", "gemm_head")
+CASES = ("gemv", "head_b1", "head_b8", "ple", "gemm_up", "gemm_down", "gemm_head", "pass_trace")
+
+
+def pass_trace(q4w, synth, dev, reps):
+    """Per-stage timing of the persistent pass from the device trace stamps."""
+    import torch
+    H = synth.E2B_HIDDEN
+    layers = []
+    for layer in range(synth.E2B_N_LAYERS):
+        g = {}
+        for name in synth.e2b_matrix_shapes(layer):
+            W = synth.e2b_weight(SEED, layer, name, dev)
+            g[name] = q4w.q4_quantize(W)
+            del W
+        layers.append(g)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    nst = 4 * len(layers)
+    buf = torch.zeros(nst * sms * 4, dtype=torch.int64, device=dev)
+    ws = torch.empty(q4w.decode_pass_ws_bytes(layers, H), dtype=torch.uint8, device=dev)
+    h0 = synth.e2b_h0(SEED, dev)
+    h = torch.empty(H, dtype=torch.float16, device=dev)
+    descs = q4w.make_layers(layers)
+    for _ in range(3):
+        q4w.q4_decode_pass(layers, h0, h, ws, descs=descs)
+    q4w.q4_set_trace(buf)
+    acc = None
+    for _ in range(reps):
+        q4w.q4_decode_pass(layers, h0, h, ws, descs=descs)
+        torch.cuda.synchronize()
+        t = buf.view(nst, sms, 4).cpu().numpy().astype(np.float64)
+        acc = t if acc is None else acc
+    q4w.q4_set_trace(None)
+    t = acc
+    t0 = t[0, :, 0].min()
+    kinds = ["qkv", "o", "gate_up", "down"]
+    out = {"stages": nst, "total_us": round((t[:, :, 3].max() - t0) / 1e3, 2)}
+    agg = {k: {"wait": 0.0, "prologue": 0.0, "compute_max": 0.0, "compute_med": 0.0, "skew": 0.0} for k in kinds}
+    for s in range(nst):
+        k = kinds[s % 4]
+        wait = np.median(t[s, :, 1] - t[s, :, 0])
+        pro = np.median(t[s, :, 2] - t[s, :, 1])
+        comp = t[s, :, 3] - t[s, :, 2]
+        agg[k]["wait"] += wait / 1e3
+        agg[k]["prologue"] += pro / 1e3
+        agg[k]["compute_max"] += comp.max() / 1e3
+        agg[k]["compute_med"] += np.median(comp) / 1e3
+        if s > 0:   # last signal of the previous stage to this stage's median wake-up
+            agg[k]["skew"] += (np.median(t[s, :, 1]) - t[s - 1, :, 3].max()) / 1e3
+    out["per_kind_us_summed_over_layers"] = {k: {q: round(v, 2) for q, v in d.items()} for k, d in agg.items()}
+    return out
 
 
 def run_case(args):
@@ -447,6 +496,8 @@ def run_case(args):
         r = row_head(q4w, synth, dev, hbm, 1 if args.case == "head_b1" else 8, reps)
     elif args.case == "ple":
         r = row_ple(q4w, synth, dev, hbm, None, reps)
+    elif args.case == "pass_trace":
+        r = pass_trace(q4w, synth, dev, reps)
     else:
         N, K = {"gemm_up": (6144, 1536), "gemm_down": (1536, 6144), "gemm_head": (262144, 1536)}[args.case]
         r = row_gemm(q4w, synth, dev, hbm, bf16, N, K, reps)

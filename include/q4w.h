@@ -258,6 +258,14 @@ int q4_device_status(q4_stream_t stream);
  * satisfied give up at once (used to test the timeout path). */
 long long q4_set_wait_limit(long long cycles);
 
+/* q4_set_trace: diagnostic.  While `buf` (device memory) is set, every
+ * persistent q4_decode_pass launch writes, per stage s and CTA c, four
+ * globaltimer stamps (ns) to buf[(s * grid + c) * 4 + i]: before waiting for
+ * the previous stage, after that wait, after the stage prologue, and after
+ * the CTA's share of the stage (grid = the SM count).  Needs
+ * 4 * n_layers * grid * 4 * 8 bytes.  NULL turns tracing off. */
+int q4_set_trace(void* buf, size_t bytes);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int q4_version(void);
 

@@ -62,6 +62,7 @@ _SIGS = {
     "q4_version": (ci, []),
     "q4_device_status": (ci, [vp]),
     "q4_set_wait_limit": (ctypes.c_longlong, [ctypes.c_longlong]),
+    "q4_set_trace": (ci, [vp, csz]),
 }
 
 
@@ -124,6 +125,15 @@ def q4_device_status():
 
 def q4_set_wait_limit(cycles: int) -> int:
     return int(load().q4_set_wait_limit(cycles))
+
+
+def q4_set_trace(buf=None):
+    """Diagnostic stamps of the persistent decode pass into ``buf`` (uint64 CUDA tensor), or off."""
+    if buf is None:
+        _check(load().q4_set_trace(None, 0), "q4_set_trace")
+    else:
+        _dev(buf, torch.int64, "trace")
+        _check(load().q4_set_trace(_ptr(buf), buf.numel() * 8), "q4_set_trace")
 
 
 def q4_version() -> int:

@@ -668,7 +668,14 @@ struct MegaArgs {
   int* abort_grid;              // zeroed before the launch
   long long limit;
   unsigned* err;
+  unsigned long long* trace;    // optional: [4 * n_layers][gridDim.x][4] globaltimer stamps
 };
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
 
 // Stage s of the pass as StageArgs (the same stages the launch path issues).
 __device__ __forceinline__ StageArgs mega_stage(const MegaArgs& A, int s) {
@@ -766,10 +773,17 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
     __syncwarp();
   } else {
     bool ok = true;
+    unsigned long long* tr = nullptr;
     for (int s = 0; s < nst && ok; ++s) {
       const StageArgs a = mega_stage(A, s);
+      if (A.trace && threadIdx.x == 0) {
+        tr = A.trace + ((size_t)s * gridDim.x + blockIdx.x) * 4;
+        tr[0] = globaltimer();
+      }
       if (s > 0 && !wait_counter(A.counters + s - 1, (int)gridDim.x, c)) break;
+      if (tr) tr[1] = globaltimer();
       eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
+      if (tr) tr[2] = globaltimer();
       StageEpi epi{&a};
       ok = a.pair ? consume_stage<2>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
                   : consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
@@ -778,6 +792,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       if (threadIdx.x == 0) {
         __threadfence();
         atomicAdd(A.counters + s, 1);
+        if (tr) tr[3] = globaltimer();
       }
     }
     // closing RMSNorm of the last down-projection output, by CTA 0
@@ -868,6 +883,9 @@ int launch_head_stream(const uint8_t* codes, const __half* scales, const __half*
   return e == cudaSuccess ? Q4_OK : cuda_fail(e, "stream head launch");
 }
 
+static void* g_trace_buf = nullptr;
+static size_t g_trace_bytes = 0;
+
 size_t decode_counters_bytes() { return (size_t)(4 * 256 + 64) * sizeof(int); }
 
 int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const __half* h0, __half* h_out,
@@ -912,6 +930,9 @@ int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const
   A.counters = counters;
   A.abort_grid = counters + 4 * 256;
   A.limit = wait_limit();
+  A.trace = static_cast<unsigned long long*>(g_trace_buf);
+  if (A.trace && g_trace_bytes < (size_t)4 * n_layers * dev.sms * 4 * sizeof(unsigned long long))
+    return fail(Q4_ERR_WORKSPACE, "trace buffer too small for %d layers", n_layers);
   A.err = device_error_word();
   if (!A.err) return fail(Q4_ERR_CUDA, "device error word unavailable");
   e = cudaMemsetAsync(counters, 0, decode_counters_bytes(), s);
@@ -931,3 +952,9 @@ int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const
 }
 
 }  // namespace q4w
+
+extern "C" int q4_set_trace(void* buf, size_t bytes) {
+  q4w::g_trace_buf = buf;
+  q4w::g_trace_bytes = buf ? bytes : 0;
+  return Q4_OK;
+}
