@@ -31,15 +31,16 @@ namespace eng {
 constexpr int kCW = 12;                   // consumer warps
 constexpr int kCT = kCW * 32;             // consumer threads
 constexpr int kTS = kCT + 32;             // threads per CTA
-constexpr int kSlots = 4;
+constexpr int kSlots = 3;
 constexpr int kSlotBytes = 42 * 1024;
+constexpr int kStageInBytes = 24 * 1024;   // stage input staged in shared memory when it fits
 constexpr int kMaxNb = 384;               // K <= 12288 on this path
 constexpr int kBPL = 3;                   // blocks per lane (upper bound)
 constexpr int kXhStride = 20;             // uint32 per block: 16 half pairs, bias, 3 pad (80 B:
                                           // 8 lanes reading 8 consecutive blocks hit 8 bank groups)
 constexpr size_t kXsBytes = (size_t)kMaxNb * kXhStride * sizeof(uint32_t);
-constexpr size_t kSmemBytes = 128 + (size_t)kSlots * kSlotBytes + kXsBytes + 64 * sizeof(float) +
-                              2 * kSlots * sizeof(uint64_t) + 64;
+constexpr size_t kSmemBytes = 128 + (size_t)kSlots * kSlotBytes + kXsBytes + kStageInBytes +
+                              64 * sizeof(float) + 2 * kSlots * sizeof(uint64_t) + 64;
 constexpr long long kDrainCycles = 2000000000LL;   // in-flight copies always land well within this
 
 // ----------------------------------------------------------- primitives ---
@@ -234,21 +235,45 @@ __device__ __forceinline__ float load_in_cg(const void* in, int mode, int k) {
 
 // x = prologue(in), written per 32-column block as the half pairs
 // (x[8i+j], x[8i+j+4]) plus the bias -72 * sum(x) (kXhStride words).  The
-// fp16 rounding of each x is recomputed from the input where it is needed.
-__device__ __forceinline__ float prologue_x(const void* in, int mode, int k, float r, float r2) {
-  const float v = load_in_cg(in, mode, k);
-  if (mode == Q4_IN_F16) return v;
+// input vector is first copied to shared memory with one round of 16-byte
+// loads from L2 (when it fits); the fp16 rounding of each x is recomputed
+// where it is needed.
+struct InVec {
+  const void* g;        // global input
+  const uint8_t* s;     // shared copy or nullptr
+  int mode;
+  __device__ __forceinline__ float operator()(int k) const {
+    const bool f16 = mode == Q4_IN_F16 || mode == Q4_IN_RMS_F16;
+    if (s) return f16 ? __half2float(reinterpret_cast<const __half*>(s)[k]) : reinterpret_cast<const float*>(s)[k];
+    return load_in_cg(g, mode, k);
+  }
+};
+
+__device__ __forceinline__ float prologue_x(const InVec& in, int k, float r, float r2) {
+  const float v = in(k);
+  if (in.mode == Q4_IN_F16) return v;
   const float t = f16_round(v * r);
-  return mode == Q4_IN_RMS2_F32 ? f16_round(t * r2) : t;
+  return in.mode == Q4_IN_RMS2_F32 ? f16_round(t * r2) : t;
 }
 
-__device__ void eng_prologue(const void* in, int mode, int K, float eps, uint32_t* xh, float* red8) {
+__device__ void eng_prologue(const void* gin, int mode, int K, float eps, uint32_t* xh, uint8_t* stage_in,
+                             float* red8) {
   const int tid = threadIdx.x;
+  const int esz = (mode == Q4_IN_F16 || mode == Q4_IN_RMS_F16) ? 2 : 4;
+  InVec in{gin, nullptr, mode};
+  if (K * esz <= kStageInBytes) {
+    const int nvec = K * esz / 16;
+    const uint4* src = reinterpret_cast<const uint4*>(gin);
+    uint4* dst = reinterpret_cast<uint4*>(stage_in);
+    for (int v = tid; v < nvec; v += kCT) dst[v] = __ldcg(src + v);
+    bar_sync(1, kCT);
+    in.s = stage_in;
+  }
   float r = 1.f, r2 = 1.f;
   if (mode != Q4_IN_F16) {
     float ss = 0.f;
     for (int k = tid; k < K; k += kCT) {
-      const float v = load_in_cg(in, mode, k);
+      const float v = in(k);
       ss += v * v;
     }
     ss = consumer_sum(ss, red8);
@@ -256,7 +281,7 @@ __device__ void eng_prologue(const void* in, int mode, int K, float eps, uint32_
     if (mode == Q4_IN_RMS2_F32) {
       float ss2 = 0.f;
       for (int k = tid; k < K; k += kCT) {
-        const float t = f16_round(load_in_cg(in, mode, k) * r);
+        const float t = f16_round(in(k) * r);
         ss2 += t * t;
       }
       ss2 = consumer_sum(ss2, red8);
@@ -269,8 +294,8 @@ __device__ void eng_prologue(const void* in, int mode, int K, float eps, uint32_
   for (int idx = tid; idx < npairs; idx += kCT) {
     const int b = idx >> 4, pr = idx & 15, i = pr >> 2, j = pr & 3;
     const int k = 32 * b + 8 * i + j;
-    const __half va = __float2half_rn(prologue_x(in, mode, k, r, r2));
-    const __half vc = __float2half_rn(prologue_x(in, mode, k + 4, r, r2));
+    const __half va = __float2half_rn(prologue_x(in, k, r, r2));
+    const __half vc = __float2half_rn(prologue_x(in, k + 4, r, r2));
     xh[b * kXhStride + pr] = (uint32_t)__half_as_ushort(va) | ((uint32_t)__half_as_ushort(vc) << 16);
     float sum = __half2float(va) + __half2float(vc);
 #pragma unroll
@@ -546,6 +571,7 @@ __device__ bool consume_stage(const StageArgs& a, uint32_t& gcount, const uint8_
 struct Smem {
   uint8_t* slots;
   uint32_t* xs;   // half pairs + bias per block
+  uint8_t* stage_in;
   float* red;
   uint32_t slots0, full0, empty0;
 };
@@ -559,6 +585,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   off += (size_t)kSlots * kSlotBytes;
   s.xs = reinterpret_cast<uint32_t*>(raw + off);
   off += kXsBytes;
+  s.stage_in = raw + off;
+  off += kStageInBytes;
   s.red = reinterpret_cast<float*>(raw + off);
   off += 64 * sizeof(float);
   uint64_t* bars = reinterpret_cast<uint64_t*>(raw + off);
@@ -599,7 +627,7 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
     __syncwarp();
   } else {
     pdl_wait();
-    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
+    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.stage_in, S.red);
     StageEpi epi{&a};
     consume_stage<NM>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
   }
@@ -629,7 +657,7 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
     }
     __syncwarp();
   } else {
-    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
+    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.stage_in, S.red);
     HeadEpi epi{&best, logits, cap};
     consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
   }
@@ -782,7 +810,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       }
       if (s > 0 && !wait_counter(A.counters + s - 1, (int)gridDim.x, c)) break;
       if (tr) tr[1] = globaltimer();
-      eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.red);
+      eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.stage_in, S.red);
       if (tr) tr[2] = globaltimer();
       StageEpi epi{&a};
       ok = a.pair ? consume_stage<2>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
@@ -790,8 +818,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       if (!ok) break;
       bar_sync(1, kCT);
       if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(A.counters + s, 1);
+        asm volatile("fence.acq_rel.gpu;\n red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(A.counters + s) : "memory");
         if (tr) tr[3] = globaltimer();
       }
     }
