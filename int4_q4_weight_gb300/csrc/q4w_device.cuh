@@ -131,18 +131,15 @@ constexpr uint32_t kH64Magic = 0x54005400u;   // fp16 64.0 in both halves
 
 __device__ __forceinline__ float q4_block_dot_h(const uint4 c, const uint32_t (&xh)[16], float bias) {
   const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
-  float lo[4], hi[4];
+  float lo = bias, hi = 0.f;   // even/odd halves accumulate separately (two chains)
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t w = w4[i];
     const uint32_t sh[4] = {shl_u32(w, 4), w, shr_u32(w, 4), shr_u32(w, 8)};
-    float t0 = i == 0 ? bias : 0.f, t1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) fhfma2(t0, t1, lop3_and_or(sh[j], kH64Mask, kH64Magic), xh[4 * i + j]);
-    lo[i] = t0;
-    hi[i] = t1;
+    for (int j = 0; j < 4; ++j) fhfma2(lo, hi, lop3_and_or(sh[j], kH64Mask, kH64Magic), xh[4 * i + j]);
   }
-  return ((lo[0] + hi[0]) + (lo[1] + hi[1])) + ((lo[2] + hi[2]) + (lo[3] + hi[3]));
+  return lo + hi;
 }
 
 __device__ __forceinline__ void load_xblock(const float* xs, int blk, float4 (&xv)[8], float& bias) {
