@@ -28,7 +28,7 @@ namespace q4w {
 
 namespace eng {
 
-constexpr int kCW = 16;                   // consumer warps
+constexpr int kCW = 12;                   // consumer warps
 constexpr int kCT = kCW * 32;             // consumer threads
 constexpr int kTS = kCT + 32;             // threads per CTA
 constexpr int kSlots = 3;
@@ -608,7 +608,7 @@ __device__ __forceinline__ void init_barriers(const Smem& S) {
 
 // ------------------------------------------------------- single stage ---
 template <int NM>
-__global__ void __maxnreg__(120) stage_stream_kernel(const StageArgs a, long long limit, unsigned* err) {
+__global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a, long long limit, unsigned* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int abort_sh;
   const Smem S = carve(smem_raw);
@@ -635,7 +635,7 @@ __global__ void __maxnreg__(120) stage_stream_kernel(const StageArgs a, long lon
 }
 
 // ----------------------------------------------------------- LM head b=1 ---
-__global__ void __maxnreg__(120) head_stream_kernel(const StageArgs a, float cap, float* logits,
+__global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, float cap, float* logits,
                                                             Top2* partials, unsigned* ticket, int32_t* idx,
                                                             float* top1, float* top2, long long limit, unsigned* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -777,7 +777,7 @@ __device__ bool wait_counter(const int* cnt, int target, const Ctl& c) {
   return bar_and(1, kCT, ok);
 }
 
-__global__ void __maxnreg__(120) decode_pass_kernel(const __grid_constant__ MegaArgs A) {
+__global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_constant__ MegaArgs A) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int abort_sh;
   const Smem S = carve(smem_raw);
