@@ -164,6 +164,25 @@ int lmhead_softcap_argmax(const uint8_t* codes, const uint16_t* scales,
                           int32_t* idx, float* top1, float* top2, float* logits_opt,
                           void* ws, size_t ws_bytes, q4_stream_t stream);
 
+/* lmhead_softcap_argmax_noalloc: the same operation as lmhead_softcap_argmax
+ * for callers that cannot allocate device memory (engines that fix every
+ * device allocation at start-up, or C hosts that only own the buffers they
+ * pass in; cudaMalloc would also synchronise the device inside a token loop).
+ * The pages have no counterpart: this is a library convenience.  Its scratch
+ * is a file-scope device array of 64 KiB that every GPU loading the library
+ * holds until the process exits; a device whose head needs more scratch
+ * than that (q4_workspace_bytes(Q4_OP_LMHEAD, ...) > 65536) gets
+ * Q4_ERR_WORKSPACE.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls share the one array: calls
+ * whose kernels overlap on the GPU (other streams, other host threads) race
+ * and must be serialised by the caller.  Arguments and results as in
+ * lmhead_softcap_argmax, without ws / ws_bytes; nothing is allocated. */
+int lmhead_softcap_argmax_noalloc(const uint8_t* codes, const uint16_t* scales,
+                                  const uint16_t* h_f16, int b, int V, int K, float cap,
+                                  int32_t* idx, float* top1, float* top2, float* logits_opt,
+                                  q4_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Decode weight pass over a stack of layers (S=1).                        */
 /* ---------------------------------------------------------------------- */

@@ -52,6 +52,7 @@ _SIGS = {
     "q4_gemm_chunk": (ci, [vp, vp, vp, vp, ci, ci, ci, vp, csz, vp]),
     "ple_gather_project": (ci, [vp, ci, vp, vp, ci, ci, ci, cf, vp, vp, ci, vp, cf, vp, vp, vp, vp]),
     "lmhead_softcap_argmax": (ci, [vp, vp, vp, ci, ci, ci, cf, vp, vp, vp, vp, vp, csz, vp]),
+    "lmhead_softcap_argmax_noalloc": (ci, [vp, vp, vp, ci, ci, ci, cf, vp, vp, vp, vp, vp]),
     "q4_decode_pass": (ci, [ctypes.POINTER(q4_layer), ci, ci, vp, vp, cf, vp, csz, vp]),
     "q4_gemv_stage": (ci, [ctypes.POINTER(q4_matrix), ctypes.POINTER(ci), ci, ci, vp, ci, cf, ci,
                            ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
