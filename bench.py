@@ -443,7 +443,7 @@ def pass_trace(q4w, synth, dev, reps):
         layers.append(g)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     nst = 4 * len(layers)
-    buf = torch.zeros(nst * sms * 4, dtype=torch.int64, device=dev)
+    buf = torch.zeros(nst * sms * 8, dtype=torch.int64, device=dev)
     ws = torch.empty(q4w.decode_pass_ws_bytes(layers, H), dtype=torch.uint8, device=dev)
     h0 = synth.e2b_h0(SEED, dev)
     h = torch.empty(H, dtype=torch.float16, device=dev)
@@ -455,14 +455,15 @@ def pass_trace(q4w, synth, dev, reps):
     for _ in range(reps):
         q4w.q4_decode_pass(layers, h0, h, ws, descs=descs)
         torch.cuda.synchronize()
-        t = buf.view(nst, sms, 4).cpu().numpy().astype(np.float64)
+        t = buf.view(nst, sms, 8).cpu().numpy().astype(np.float64)
         acc = t if acc is None else acc
     q4w.q4_set_trace(None)
     t = acc
     t0 = t[0, :, 0].min()
     kinds = ["qkv", "o", "gate_up", "down"]
     out = {"stages": nst, "total_us": round((t[:, :, 3].max() - t0) / 1e3, 2)}
-    agg = {k: {"wait": 0.0, "prologue": 0.0, "compute_max": 0.0, "compute_med": 0.0, "skew": 0.0} for k in kinds}
+    agg = {k: {"wait": 0.0, "prologue": 0.0, "compute_max": 0.0, "compute_med": 0.0, "rows_med": 0.0,
+               "cta_sync_med": 0.0, "signal_med": 0.0, "skew": 0.0} for k in kinds}
     for s in range(nst):
         k = kinds[s % 4]
         wait = np.median(t[s, :, 1] - t[s, :, 0])
@@ -472,6 +473,9 @@ def pass_trace(q4w, synth, dev, reps):
         agg[k]["prologue"] += pro / 1e3
         agg[k]["compute_max"] += comp.max() / 1e3
         agg[k]["compute_med"] += np.median(comp) / 1e3
+        agg[k]["rows_med"] += np.median(t[s, :, 4] - t[s, :, 2]) / 1e3
+        agg[k]["cta_sync_med"] += np.median(t[s, :, 5] - t[s, :, 4]) / 1e3
+        agg[k]["signal_med"] += np.median(t[s, :, 3] - t[s, :, 5]) / 1e3
         if s > 0:   # last signal of the previous stage to this stage's median wake-up
             agg[k]["skew"] += (np.median(t[s, :, 1]) - t[s - 1, :, 3].max()) / 1e3
     out["per_kind_us_summed_over_layers"] = {k: {q: round(v, 2) for q, v in d.items()} for k, d in agg.items()}

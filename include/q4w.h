@@ -278,11 +278,12 @@ int q4_device_status(q4_stream_t stream);
 long long q4_set_wait_limit(long long cycles);
 
 /* q4_set_trace: diagnostic.  While `buf` (device memory) is set, every
- * persistent q4_decode_pass launch writes, per stage s and CTA c, four
- * globaltimer stamps (ns) to buf[(s * grid + c) * 4 + i]: before waiting for
- * the previous stage, after that wait, after the stage prologue, and after
- * the CTA's share of the stage (grid = the SM count).  Needs
- * 4 * n_layers * grid * 4 * 8 bytes.  NULL turns tracing off. */
+ * persistent q4_decode_pass launch writes, per stage s and CTA c, globaltimer
+ * stamps (ns) to buf[(s * grid + c) * 8 + i]: i=0 before waiting for the
+ * previous stage, 1 after that wait, 2 after the stage prologue, 3 after the
+ * stage's completion signal, 4 when this thread finished its share of the
+ * stage's rows, 5 after the CTA's consumers all finished (grid = the SM
+ * count).  Needs 4 * n_layers * grid * 8 * 8 bytes.  NULL turns it off. */
 int q4_set_trace(void* buf, size_t bytes);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */

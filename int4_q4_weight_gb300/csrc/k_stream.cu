@@ -696,7 +696,7 @@ struct MegaArgs {
   int* abort_grid;              // zeroed before the launch
   long long limit;
   unsigned* err;
-  unsigned long long* trace;    // optional: [4 * n_layers][gridDim.x][4] globaltimer stamps
+  unsigned long long* trace;    // optional: [4 * n_layers][gridDim.x][8] globaltimer stamps
 };
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -805,7 +805,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
     for (int s = 0; s < nst && ok; ++s) {
       const StageArgs a = mega_stage(A, s);
       if (A.trace && threadIdx.x == 0) {
-        tr = A.trace + ((size_t)s * gridDim.x + blockIdx.x) * 4;
+        tr = A.trace + ((size_t)s * gridDim.x + blockIdx.x) * 8;
         tr[0] = globaltimer();
       }
       if (s > 0 && !wait_counter(A.counters + s - 1, (int)gridDim.x, c)) break;
@@ -816,7 +816,9 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       ok = a.pair ? consume_stage<2>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
                   : consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
       if (!ok) break;
+      if (tr) tr[4] = globaltimer();
       bar_sync(1, kCT);
+      if (tr) tr[5] = globaltimer();
       if (threadIdx.x == 0) {
         asm volatile("fence.acq_rel.gpu;\n red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(A.counters + s) : "memory");
         if (tr) tr[3] = globaltimer();
@@ -958,7 +960,7 @@ int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const
   A.abort_grid = counters + 4 * 256;
   A.limit = wait_limit();
   A.trace = static_cast<unsigned long long*>(g_trace_buf);
-  if (A.trace && g_trace_bytes < (size_t)4 * n_layers * dev.sms * 4 * sizeof(unsigned long long))
+  if (A.trace && g_trace_bytes < (size_t)4 * n_layers * dev.sms * 8 * sizeof(unsigned long long))
     return fail(Q4_ERR_WORKSPACE, "trace buffer too small for %d layers", n_layers);
   A.err = device_error_word();
   if (!A.err) return fail(Q4_ERR_CUDA, "device error word unavailable");
