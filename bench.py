@@ -463,7 +463,7 @@ def pass_trace(q4w, synth, dev, reps):
     kinds = ["qkv", "o", "gate_up", "down"]
     out = {"stages": nst, "total_us": round((t[:, :, 3].max() - t0) / 1e3, 2)}
     agg = {k: {"wait": 0.0, "prologue": 0.0, "compute_max": 0.0, "compute_med": 0.0, "rows_med": 0.0,
-               "cta_sync_med": 0.0, "signal_med": 0.0, "skew": 0.0} for k in kinds}
+               "cta_sync_med": 0.0, "signal_med": 0.0, "skew": 0.0, "first_tile_med": 0.0} for k in kinds}
     for s in range(nst):
         k = kinds[s % 4]
         wait = np.median(t[s, :, 1] - t[s, :, 0])
@@ -476,9 +476,14 @@ def pass_trace(q4w, synth, dev, reps):
         agg[k]["rows_med"] += np.median(t[s, :, 4] - t[s, :, 2]) / 1e3
         agg[k]["cta_sync_med"] += np.median(t[s, :, 5] - t[s, :, 4]) / 1e3
         agg[k]["signal_med"] += np.median(t[s, :, 3] - t[s, :, 5]) / 1e3
+        agg[k]["first_tile_med"] += np.median(np.maximum(t[s, :, 6] - t[s, :, 2], 0)) / 1e3
         if s > 0:   # last signal of the previous stage to this stage's median wake-up
             agg[k]["skew"] += (np.median(t[s, :, 1]) - t[s - 1, :, 3].max()) / 1e3
     out["per_kind_us_summed_over_layers"] = {k: {q: round(v, 2) for q, v in d.items()} for k, d in agg.items()}
+    cta = int(np.argmax(t[8, :, 3]))
+    out["cta0_layer2_stages_us"] = [[round((t[s, 0, i] - t[8, 0, 0]) / 1e3, 2) for i in range(7)] for s in range(8, 12)]
+    out["slowest_cta_layer2_stages_us"] = [[round((t[s, cta, i] - t[8, 0, 0]) / 1e3, 2) for i in range(7)]
+                                           for s in range(8, 12)]
     return out
 
 

@@ -84,6 +84,7 @@ struct Ctl {
   int* abort_grid;           // global (decode pass) or nullptr
   long long limit;
   unsigned* err;             // the library's device error word
+  unsigned long long* tr;    // trace stamps of the current stage (thread 0), or nullptr
 };
 
 __device__ __forceinline__ void raise_abort(const Ctl& c) {
@@ -107,6 +108,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, const Ctl
     }
   }
   return true;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
 }
 
 __device__ __forceinline__ uint64_t evict_first_policy() {
@@ -382,6 +389,7 @@ __device__ bool consume_fast(const StageArgs& a, const Geo& g, uint32_t& gcount,
       ok = false;
       break;
     }
+    if (c.tr && ct == 0 && pos == g.lo + n) c.tr[6] = globaltimer();
     const uint8_t* S = slots + (size_t)s * kSlotBytes;
     const int per = n * (K2 + nb * 2);
     const uint8_t* sc_base = S + n * K2;
@@ -616,7 +624,7 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
   init_barriers(S);
   __syncthreads();
   pdl_trigger();
-  const Ctl c{&abort_sh, nullptr, limit, err};
+  const Ctl c{&abort_sh, nullptr, limit, err, nullptr};
   uint32_t gcount = 0;
   if (threadIdx.x >= kCT) {
     if (threadIdx.x == kCT) {
@@ -645,7 +653,7 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
   if (threadIdx.x == 0) abort_sh = 0;
   init_barriers(S);
   __syncthreads();
-  const Ctl c{&abort_sh, nullptr, limit, err};
+  const Ctl c{&abort_sh, nullptr, limit, err, nullptr};
   uint32_t gcount = 0;
   Top2 best;
   top2_init(best);
@@ -698,12 +706,6 @@ struct MegaArgs {
   unsigned* err;
   unsigned long long* trace;    // optional: [4 * n_layers][gridDim.x][8] globaltimer stamps
 };
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
 
 // Stage s of the pass as StageArgs (the same stages the launch path issues).
 __device__ __forceinline__ StageArgs mega_stage(const MegaArgs& A, int s) {
@@ -784,7 +786,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
   if (threadIdx.x == 0) abort_sh = 0;
   init_barriers(S);
   __syncthreads();
-  const Ctl c{&abort_sh, A.abort_grid, A.limit, A.err};
+  Ctl c{&abort_sh, A.abort_grid, A.limit, A.err, nullptr};
   const int nst = 4 * A.n_layers;
   uint32_t gcount = 0;
   if (threadIdx.x >= kCT) {
@@ -807,6 +809,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       if (A.trace && threadIdx.x == 0) {
         tr = A.trace + ((size_t)s * gridDim.x + blockIdx.x) * 8;
         tr[0] = globaltimer();
+        c.tr = tr;
       }
       if (s > 0 && !wait_counter(A.counters + s - 1, (int)gridDim.x, c)) break;
       if (tr) tr[1] = globaltimer();
