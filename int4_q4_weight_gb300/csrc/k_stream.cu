@@ -98,16 +98,22 @@ __device__ __forceinline__ bool aborting(const Ctl& c) {
 }
 
 // Bounded mbarrier wait; false on expiry (raises the abort) or when aborting.
+// The shared abort flag is read every iteration; the grid-wide flag (a
+// global load, about an L2 round trip) and the clock only every 256.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, const Ctl& c) {
+  if (mbar_test(a, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_test(a, parity)) {
-    if (aborting(c)) return false;
-    if (clock64() - t0 > c.limit) {
-      raise_abort(c);
-      return false;
+  for (unsigned it = 1;; ++it) {
+    if (mbar_test(a, parity)) return true;
+    if (*c.abort_cta) return false;
+    if ((it & 255u) == 0) {
+      if (c.abort_grid && *(volatile int*)c.abort_grid) return false;
+      if (clock64() - t0 > c.limit) {
+        raise_abort(c);
+        return false;
+      }
     }
   }
-  return true;
 }
 
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -295,19 +301,48 @@ __device__ void eng_prologue(const void* gin, int mode, int K, float eps, uint32
       r2 = 1.f / sqrtf(ss2 / (float)K + eps);
     }
   }
-  // one thread per half pair; the 16 pairs of a block are 16 aligned lanes
-  // of one warp (nb * 16 is a multiple of 128 for K % 256 == 0)
-  const int npairs = (K >> 5) * 16;
-  for (int idx = tid; idx < npairs; idx += kCT) {
-    const int b = idx >> 4, pr = idx & 15, i = pr >> 2, j = pr & 3;
-    const int k = 32 * b + 8 * i + j;
-    const __half va = __float2half_rn(prologue_x(in, k, r, r2));
-    const __half vc = __float2half_rn(prologue_x(in, k + 4, r, r2));
-    xh[b * kXhStride + pr] = (uint32_t)__half_as_ushort(va) | ((uint32_t)__half_as_ushort(vc) << 16);
-    float sum = __half2float(va) + __half2float(vc);
+  // one thread per 32-column block: 32 values, 16 half pairs, the bias
+  const int nb = K >> 5;
+  for (int b = tid; b < nb; b += kCT) {
+    uint32_t* q = xh + b * kXhStride;
+    float sum = 0.f;
+    if (in.s && mode == Q4_IN_F16) {
+      // raw fp16 words hold (x[2t], x[2t+1]); pair (x[8i+j], x[8i+j+4]) by byte permute
+      const uint4* src = reinterpret_cast<const uint4*>(in.s + (size_t)b * 64);
+      uint32_t w[16];
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (pr == 0) xh[b * kXhStride + 16] = __float_as_uint(-72.f * sum);
+      for (int t = 0; t < 4; ++t) {
+        const uint4 u = src[t];
+        w[4 * t] = u.x;
+        w[4 * t + 1] = u.y;
+        w[4 * t + 2] = u.z;
+        w[4 * t + 3] = u.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t a = w[4 * i + (j >> 1)], c2 = w[4 * i + 2 + (j >> 1)];
+          q[4 * i + j] = __byte_perm(a, c2, (j & 1) ? 0x7632 : 0x5410);
+        }
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
+        sum += f.x + f.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int k = 32 * b + 8 * i + j;
+          const __half va = __float2half_rn(prologue_x(in, k, r, r2));
+          const __half vc = __float2half_rn(prologue_x(in, k + 4, r, r2));
+          q[4 * i + j] = (uint32_t)__half_as_ushort(va) | ((uint32_t)__half_as_ushort(vc) << 16);
+          sum += __half2float(va) + __half2float(vc);
+        }
+    }
+    q[16] = __float_as_uint(-72.f * sum);
   }
   bar_sync(1, kCT);
 }
@@ -763,15 +798,17 @@ __device__ bool wait_counter(const int* cnt, int target, const Ctl& c) {
   bool ok = true;
   if (threadIdx.x == 0) {
     const long long t0 = clock64();
-    while (ld_acquire(cnt) < target) {
-      if (aborting(c)) {
-        ok = false;
-        break;
-      }
-      if (clock64() - t0 > c.limit) {
-        raise_abort(c);
-        ok = false;
-        break;
+    for (unsigned it = 0; ld_acquire(cnt) < target; ++it) {
+      if ((it & 63u) == 63u) {
+        if (aborting(c)) {
+          ok = false;
+          break;
+        }
+        if (clock64() - t0 > c.limit) {
+          raise_abort(c);
+          ok = false;
+          break;
+        }
       }
     }
     __threadfence();
