@@ -99,14 +99,15 @@ __device__ __forceinline__ bool aborting(const Ctl& c) {
 
 // Bounded mbarrier wait; false on expiry (raises the abort) or when aborting.
 // The shared abort flag is read every iteration; the grid-wide flag (a
-// global load, about an L2 round trip) and the clock only every 256.
+// global load, about an L2 round trip) and the clock on the first retry and
+// then every 256 (so a zero budget gives up at once).
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, const Ctl& c) {
   if (mbar_test(a, parity)) return true;
   const long long t0 = clock64();
   for (unsigned it = 1;; ++it) {
     if (mbar_test(a, parity)) return true;
     if (*c.abort_cta) return false;
-    if ((it & 255u) == 0) {
+    if ((it & 255u) == 1) {   // first failed retry, then every 256
       if (c.abort_grid && *(volatile int*)c.abort_grid) return false;
       if (clock64() - t0 > c.limit) {
         raise_abort(c);
@@ -799,7 +800,7 @@ __device__ bool wait_counter(const int* cnt, int target, const Ctl& c) {
   if (threadIdx.x == 0) {
     const long long t0 = clock64();
     for (unsigned it = 0; ld_acquire(cnt) < target; ++it) {
-      if ((it & 63u) == 63u) {
+      if ((it & 63u) == 0) {   // first failed poll, then every 64
         if (aborting(c)) {
           ok = false;
           break;
