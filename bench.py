@@ -461,28 +461,26 @@ def pass_trace(q4w, synth, dev, reps):
     t = acc
     t0 = t[0, :, 0].min()
     kinds = ["qkv", "o", "gate_up", "down"]
-    out = {"stages": nst, "total_us": round((t[:, :, 3].max() - t0) / 1e3, 2)}
-    agg = {k: {"wait": 0.0, "prologue": 0.0, "compute_max": 0.0, "compute_med": 0.0, "rows_med": 0.0,
-               "cta_sync_med": 0.0, "signal_med": 0.0, "skew": 0.0, "first_tile_med": 0.0} for k in kinds}
+    # stamps per (stage, CTA): 0 stage entered, 1 input complete and staged,
+    # 2 x built, 6 first weight tile usable, 4 own rows written
+    out = {"stages": nst, "total_us": round((t[:, :, 4].max() - t0) / 1e3, 2)}
+    agg = {k: {"input_wait": 0.0, "xform": 0.0, "rows_med": 0.0, "rows_max": 0.0, "first_tile_med": 0.0,
+               "handoff": 0.0} for k in kinds}
     for s in range(nst):
         k = kinds[s % 4]
-        wait = np.median(t[s, :, 1] - t[s, :, 0])
-        pro = np.median(t[s, :, 2] - t[s, :, 1])
-        comp = t[s, :, 3] - t[s, :, 2]
-        agg[k]["wait"] += wait / 1e3
-        agg[k]["prologue"] += pro / 1e3
-        agg[k]["compute_max"] += comp.max() / 1e3
-        agg[k]["compute_med"] += np.median(comp) / 1e3
-        agg[k]["rows_med"] += np.median(t[s, :, 4] - t[s, :, 2]) / 1e3
-        agg[k]["cta_sync_med"] += np.median(t[s, :, 5] - t[s, :, 4]) / 1e3
-        agg[k]["signal_med"] += np.median(t[s, :, 3] - t[s, :, 5]) / 1e3
+        agg[k]["input_wait"] += np.median(t[s, :, 1] - t[s, :, 0]) / 1e3
+        agg[k]["xform"] += np.median(t[s, :, 2] - t[s, :, 1]) / 1e3
+        rows = t[s, :, 4] - t[s, :, 2]
+        agg[k]["rows_med"] += np.median(rows) / 1e3
+        agg[k]["rows_max"] += rows.max() / 1e3
         agg[k]["first_tile_med"] += np.median(np.maximum(t[s, :, 6] - t[s, :, 2], 0)) / 1e3
-        if s > 0:   # last signal of the previous stage to this stage's median wake-up
-            agg[k]["skew"] += (np.median(t[s, :, 1]) - t[s - 1, :, 3].max()) / 1e3
+        if s > 0:   # last CTA done with the previous stage -> median CTA has this stage's input
+            agg[k]["handoff"] += (np.median(t[s, :, 1]) - t[s - 1, :, 4].max()) / 1e3
     out["per_kind_us_summed_over_layers"] = {k: {q: round(v, 2) for q, v in d.items()} for k, d in agg.items()}
-    cta = int(np.argmax(t[8, :, 3]))
-    out["cta0_layer2_stages_us"] = [[round((t[s, 0, i] - t[8, 0, 0]) / 1e3, 2) for i in range(7)] for s in range(8, 12)]
-    out["slowest_cta_layer2_stages_us"] = [[round((t[s, cta, i] - t[8, 0, 0]) / 1e3, 2) for i in range(7)]
+    cta = int(np.argmax(t[8, :, 4]))
+    cols = [0, 1, 2, 6, 4]
+    out["cta0_layer2_stages_us"] = [[round((t[s, 0, i] - t[8, 0, 0]) / 1e3, 2) for i in cols] for s in range(8, 12)]
+    out["slowest_cta_layer2_stages_us"] = [[round((t[s, cta, i] - t[8, 0, 0]) / 1e3, 2) for i in cols]
                                            for s in range(8, 12)]
     return out
 

@@ -215,9 +215,15 @@ typedef struct q4_layer {
  *   h0_f16, h_out_f16: device [H]; 1 <= n_layers <= 256; H % 32 == 0;
  *   q_rows, mlp_rows % 32 == 0 and in [32, 32768]; kv_rows >= 0.
  *   ws: q4_workspace_bytes(Q4_OP_DECODE_PASS, H, max(q_rows + 2 kv_rows),
- *   max(mlp_rows)) bytes.  Every stage is one kernel launch on `stream`
- *   (programmatic dependent launch between stages); the sequence can be
- *   captured into a CUDA graph.                                            */
+ *   max(mlp_rows)) bytes; overlapping calls must not share it.
+ *   When H <= 4096, n_layers <= 48 and H, every q_rows and every mlp_rows
+ *   are multiples of 256 up to 12288, the whole pass is one persistent
+ *   cooperative launch (one CTA per SM) preceded by two memsets on `stream`:
+ *   each stage output word carries the index of the stage that wrote it,
+ *   and the next stage polls its input (bounded; Q4_ERR_TIMEOUT via
+ *   q4_device_status) until every word carries that index.  Otherwise
+ *   every stage is one kernel launch (programmatic dependent launch between
+ *   stages).  Either form can be captured into a CUDA graph.              */
 int q4_decode_pass(const q4_layer* layers, int n_layers, int H, const uint16_t* h0_f16,
                    uint16_t* h_out_f16, float eps, void* ws, size_t ws_bytes,
                    q4_stream_t stream);

@@ -248,68 +248,117 @@ __device__ __forceinline__ float load_in_cg(const void* in, int mode, int k) {
 }
 
 // x = prologue(in), written per 32-column block as the half pairs
-// (x[8i+j], x[8i+j+4]) plus the bias -72 * sum(x) (kXhStride words).  The
-// input vector is first copied to shared memory with one round of 16-byte
-// loads from L2 (when it fits); the fp16 rounding of each x is recomputed
-// where it is needed.
-struct InVec {
-  const void* g;        // global input
-  const uint8_t* s;     // shared copy or nullptr
-  int mode;
-  __device__ __forceinline__ float operator()(int k) const {
-    const bool f16 = mode == Q4_IN_F16 || mode == Q4_IN_RMS_F16;
-    if (s) return f16 ? __half2float(reinterpret_cast<const __half*>(s)[k]) : reinterpret_cast<const float*>(s)[k];
-    return load_in_cg(g, mode, k);
-  }
-};
-
-__device__ __forceinline__ float prologue_x(const InVec& in, int k, float r, float r2) {
-  const float v = in(k);
-  if (in.mode == Q4_IN_F16) return v;
-  const float t = f16_round(v * r);
-  return in.mode == Q4_IN_RMS2_F32 ? f16_round(t * r2) : t;
+// (x[8i+j], x[8i+j+4]) plus the bias -72 * sum(x) (kXhStride words).
+//
+// Staged path (the input and its fp16 x fit kStageInBytes): the input is
+// copied to shared memory with 16-byte loads from L2 -- for a tagged input
+// (persistent pass) each element is re-read until it carries the expected
+// stage tag, which is how a stage learns that its input is complete -- then
+// the RMS factors, one fp16 x per element in parallel, and one thread per
+// block builds the pairs with byte permutes.  Otherwise x is computed per pair
+// straight from global memory.
+__device__ __forceinline__ uint4 ldcg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
 }
 
-__device__ void eng_prologue(const void* gin, int mode, int K, float eps, uint32_t* xh, uint8_t* stage_in,
-                             float* red8) {
-  const int tid = threadIdx.x;
-  const int esz = (mode == Q4_IN_F16 || mode == Q4_IN_RMS_F16) ? 2 : 4;
-  InVec in{gin, nullptr, mode};
-  if (K * esz <= kStageInBytes) {
-    const int nvec = K * esz / 16;
-    const uint4* src = reinterpret_cast<const uint4*>(gin);
-    uint4* dst = reinterpret_cast<uint4*>(stage_in);
-    for (int v = tid; v < nvec; v += kCT) dst[v] = __ldcg(src + v);
-    bar_sync(1, kCT);
-    in.s = stage_in;
-  }
-  float r = 1.f, r2 = 1.f;
-  if (mode != Q4_IN_F16) {
-    float ss = 0.f;
-    for (int k = tid; k < K; k += kCT) {
-      const float v = in(k);
-      ss += v * v;
-    }
-    ss = consumer_sum(ss, red8);
-    r = 1.f / sqrtf(ss / (float)K + eps);
-    if (mode == Q4_IN_RMS2_F32) {
-      float ss2 = 0.f;
-      for (int k = tid; k < K; k += kCT) {
-        const float t = f16_round(in(k) * r);
-        ss2 += t * t;
+// Bounded re-read of one 16-byte group of tagged words until all tags match.
+__device__ __forceinline__ bool poll_tags(const uint4* p, uint4& u, bool f16, uint32_t tag, const Ctl& c) {
+  auto ready = [&](const uint4& v) {
+    return f16 ? ((v.x >> 16) == tag && (v.y >> 16) == tag && (v.z >> 16) == tag && (v.w >> 16) == tag)
+               : (v.y == tag && v.w == tag);
+  };
+  u = ldcg_v4(p);
+  if (ready(u)) return true;
+  const long long t0 = clock64();
+  for (unsigned it = 0;; ++it) {
+    u = ldcg_v4(p);
+    if (ready(u)) return true;
+    if ((it & 63u) == 0) {
+      if (aborting(c)) return false;
+      if (clock64() - t0 > c.limit) {
+        raise_abort(c);
+        return false;
       }
-      ss2 = consumer_sum(ss2, red8);
-      r2 = 1.f / sqrtf(ss2 / (float)K + eps);
     }
   }
-  // one thread per 32-column block: 32 values, 16 half pairs, the bias
-  const int nb = K >> 5;
-  for (int b = tid; b < nb; b += kCT) {
-    uint32_t* q = xh + b * kXhStride;
-    float sum = 0.f;
-    if (in.s && mode == Q4_IN_F16) {
-      // raw fp16 words hold (x[2t], x[2t+1]); pair (x[8i+j], x[8i+j+4]) by byte permute
-      const uint4* src = reinterpret_cast<const uint4*>(in.s + (size_t)b * 64);
+}
+
+struct InVec {   // plain (untagged) input read from global memory
+  const void* g;
+  const uint8_t* s;
+  int mode;
+  __device__ __forceinline__ float operator()(int k) const { return load_in_cg(g, mode, k); }
+};
+
+__device__ __forceinline__ float xform(float v, int mode, float r, float r2) {
+  if (mode == Q4_IN_F16) return v;
+  const float t = f16_round(v * r);
+  return mode == Q4_IN_RMS2_F32 ? f16_round(t * r2) : t;
+}
+
+// false when aborting (uniform over the consumers)
+__device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in, float* red8, const Ctl& c) {
+  const int tid = threadIdx.x, K = a.K, mode = a.in_mode;
+  const bool f16in = mode == Q4_IN_F16 || mode == Q4_IN_RMS_F16;
+  const int esz = f16in ? 2 : 4;
+  const int xoff = (mode == Q4_IN_F16) ? 0 : K * esz;      // where the fp16 x array starts
+  const bool staged = xoff + K * 2 <= kStageInBytes;
+  float r = 1.f, r2 = 1.f;
+  if (staged) {
+    bool ok = true;
+    if (a.in_tag == 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.in);
+      uint4* dst = reinterpret_cast<uint4*>(stage_in);
+      for (int v = tid; v < K * esz / 16; v += kCT) dst[v] = ldcg_v4(src + v);
+    } else if (f16in) {       // uint32 words: half | tag << 16, four per 16 bytes
+      const uint4* src = reinterpret_cast<const uint4*>(a.in);
+      uint2* dst = reinterpret_cast<uint2*>(stage_in);
+      for (int v = tid; v < K / 4 && ok; v += kCT) {
+        uint4 u;
+        ok = poll_tags(src + v, u, true, (uint32_t)a.in_tag, c);
+        dst[v] = make_uint2(__byte_perm(u.x, u.y, 0x5410), __byte_perm(u.z, u.w, 0x5410));
+      }
+    } else {                  // uint64 words: float | tag << 32, two per 16 bytes
+      const uint4* src = reinterpret_cast<const uint4*>(a.in);
+      uint2* dst = reinterpret_cast<uint2*>(stage_in);
+      for (int v = tid; v < K / 2 && ok; v += kCT) {
+        uint4 u;
+        ok = poll_tags(src + v, u, false, (uint32_t)a.in_tag, c);
+        dst[v] = make_uint2(u.x, u.z);
+      }
+    }
+    if (!bar_and(1, kCT, ok)) return false;
+    if (c.tr) c.tr[1] = globaltimer();   // input complete and staged
+    const __half* sh = reinterpret_cast<const __half*>(stage_in);
+    const float* sf = reinterpret_cast<const float*>(stage_in);
+    auto val = [&](int k) { return f16in ? __half2float(sh[k]) : sf[k]; };
+    if (mode != Q4_IN_F16) {
+      float ss = 0.f;
+      for (int k = tid; k < K; k += kCT) {
+        const float v = val(k);
+        ss += v * v;
+      }
+      ss = consumer_sum(ss, red8);
+      r = 1.f / sqrtf(ss / (float)K + a.eps);
+      if (mode == Q4_IN_RMS2_F32) {
+        float ss2 = 0.f;
+        for (int k = tid; k < K; k += kCT) {
+          const float t = f16_round(val(k) * r);
+          ss2 += t * t;
+        }
+        ss2 = consumer_sum(ss2, red8);
+        r2 = 1.f / sqrtf(ss2 / (float)K + a.eps);
+      }
+      __half* x16 = reinterpret_cast<__half*>(stage_in + xoff);
+      for (int k = tid; k < K; k += kCT) x16[k] = __float2half_rn(xform(val(k), mode, r, r2));
+      bar_sync(1, kCT);
+    }
+    // one thread per 32-column block: fp16 words (x[2t], x[2t+1]) -> pairs by byte permute
+    const int nb = K >> 5;
+    for (int b = tid; b < nb; b += kCT) {
+      const uint4* src = reinterpret_cast<const uint4*>(stage_in + xoff + (size_t)b * 64);
       uint32_t w[16];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -319,33 +368,59 @@ __device__ void eng_prologue(const void* gin, int mode, int K, float eps, uint32
         w[4 * t + 2] = u.z;
         w[4 * t + 3] = u.w;
       }
+      uint32_t* q = xh + b * kXhStride;
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t a = w[4 * i + (j >> 1)], c2 = w[4 * i + 2 + (j >> 1)];
-          q[4 * i + j] = __byte_perm(a, c2, (j & 1) ? 0x7632 : 0x5410);
+          const uint32_t lo = w[4 * i + (j >> 1)], hi = w[4 * i + 2 + (j >> 1)];
+          q[4 * i + j] = __byte_perm(lo, hi, (j & 1) ? 0x7632 : 0x5410);
         }
+      float sum = 0.f;
 #pragma unroll
       for (int t = 0; t < 16; ++t) {
         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
         sum += f.x + f.y;
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int k = 32 * b + 8 * i + j;
-          const __half va = __float2half_rn(prologue_x(in, k, r, r2));
-          const __half vc = __float2half_rn(prologue_x(in, k + 4, r, r2));
-          q[4 * i + j] = (uint32_t)__half_as_ushort(va) | ((uint32_t)__half_as_ushort(vc) << 16);
-          sum += __half2float(va) + __half2float(vc);
-        }
+      q[16] = __float_as_uint(-72.f * sum);
     }
-    q[16] = __float_as_uint(-72.f * sum);
+    bar_sync(1, kCT);
+    return true;
+  }
+  // unstaged (large fp32 input, untagged only): per pair from global memory
+  InVec in{a.in, nullptr, mode};
+  if (mode != Q4_IN_F16) {
+    float ss = 0.f;
+    for (int k = tid; k < K; k += kCT) {
+      const float v = in(k);
+      ss += v * v;
+    }
+    ss = consumer_sum(ss, red8);
+    r = 1.f / sqrtf(ss / (float)K + a.eps);
+    if (mode == Q4_IN_RMS2_F32) {
+      float ss2 = 0.f;
+      for (int k = tid; k < K; k += kCT) {
+        const float t = f16_round(in(k) * r);
+        ss2 += t * t;
+      }
+      ss2 = consumer_sum(ss2, red8);
+      r2 = 1.f / sqrtf(ss2 / (float)K + a.eps);
+    }
+  }
+  const int npairs = (K >> 5) * 16;
+  for (int idx = tid; idx < npairs; idx += kCT) {
+    const int b = idx >> 4, pr = idx & 15, i = pr >> 2, j = pr & 3;
+    const int k = 32 * b + 8 * i + j;
+    const __half va = __float2half_rn(xform(in(k), mode, r, r2));
+    const __half vc = __float2half_rn(xform(in(k + 4), mode, r, r2));
+    xh[b * kXhStride + pr] = (uint32_t)__half_as_ushort(va) | ((uint32_t)__half_as_ushort(vc) << 16);
+    float sum = __half2float(va) + __half2float(vc);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (pr == 0) xh[b * kXhStride + 16] = __float_as_uint(-72.f * sum);
   }
   bar_sync(1, kCT);
+  return true;
 }
 
 __device__ __forceinline__ void load_xh(const uint32_t* xh, int blk, uint32_t (&v)[16], float& bias) {
@@ -365,15 +440,29 @@ struct StageEpi {
   const StageArgs* a;
   template <int NM>
   __device__ __forceinline__ void operator()(int m, int row, const float (&acc)[NM]) const {
+    const uint32_t tag = (uint32_t)a->out_tag;
     if (NM == 2) {
       const float gv = acc[0], uv = acc[NM - 1];
       if (a->mat[0].out32) a->mat[0].out32[row] = gv;
       if (a->mat[1].out32) a->mat[1].out32[row] = uv;
-      a->mat[0].out16[row] = __float2half_rn(gelu_tanh_f32(gv) * uv);
+      const __half mh = __float2half_rn(gelu_tanh_f32(gv) * uv);
+      if (a->mat[0].tagged)
+        reinterpret_cast<uint32_t*>(a->mat[0].out16)[row] = (uint32_t)__half_as_ushort(mh) | (tag << 16);
+      else
+        a->mat[0].out16[row] = mh;
     } else {
       const StageMat& M = a->mat[m];
-      if (M.out32) M.out32[row] = acc[0];
-      if (M.out16) M.out16[row] = __float2half_rn(acc[0]);
+      if (M.tagged) {
+        if (M.out32)
+          reinterpret_cast<unsigned long long*>(M.out32)[row] =
+              (unsigned long long)__float_as_uint(acc[0]) | ((unsigned long long)tag << 32);
+        if (M.out16)
+          reinterpret_cast<uint32_t*>(M.out16)[row] =
+              (uint32_t)__half_as_ushort(__float2half_rn(acc[0])) | (tag << 16);
+      } else {
+        if (M.out32) M.out32[row] = acc[0];
+        if (M.out16) M.out16[row] = __float2half_rn(acc[0]);
+      }
     }
   }
 };
@@ -671,9 +760,10 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
     __syncwarp();
   } else {
     pdl_wait();
-    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.stage_in, S.red);
-    StageEpi epi{&a};
-    consume_stage<NM>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+    if (eng_prologue(a, S.xs, S.stage_in, S.red, c)) {
+      StageEpi epi{&a};
+      consume_stage<NM>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+    }
   }
   __syncthreads();
 }
@@ -701,9 +791,10 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
     }
     __syncwarp();
   } else {
-    eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.stage_in, S.red);
-    HeadEpi epi{&best, logits, cap};
-    consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+    if (eng_prologue(a, S.xs, S.stage_in, S.red, c)) {
+      HeadEpi epi{&best, logits, cap};
+      consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+    }
   }
   st[threadIdx.x] = best;
   __syncthreads();
@@ -731,12 +822,11 @@ struct MegaArgs {
   float eps;
   const __half* h0;
   __half* h_out;
-  __half* q16;
-  float* kv32;
-  float* o32;
-  __half* m16;
-  float* y32;
-  int* counters;                // [4 * n_layers], zeroed before the launch
+  float* kv32;                  // k and v outputs (plain: nothing in the pass reads them)
+  uint32_t* q16t;               // stage outputs, each word carrying its stage tag;
+  unsigned long long* o32t;     // all zeroed before every launch
+  uint32_t* m16t;
+  unsigned long long* y32t;
   int* abort_grid;              // zeroed before the launch
   long long limit;
   unsigned* err;
@@ -744,77 +834,52 @@ struct MegaArgs {
 };
 
 // Stage s of the pass as StageArgs (the same stages the launch path issues).
+// Stage s tags its outputs s + 1; its input is complete once every element
+// carries tag s (stage 0 reads the untagged h0).
 __device__ __forceinline__ StageArgs mega_stage(const MegaArgs& A, int s) {
   const MegaLayer& L = A.L[s >> 2];
   StageArgs a = {};
   a.eps = A.eps;
+  a.in_tag = s;
+  a.out_tag = s + 1;
   switch (s & 3) {
     case 0:
-      a.mat[0] = {L.codes[0], L.scales[0], L.q_rows, nullptr, A.q16};
+      a.mat[0] = {L.codes[0], L.scales[0], L.q_rows, nullptr, reinterpret_cast<__half*>(A.q16t), 1};
       a.nmat = 1;
       if (L.kv_rows > 0) {
-        a.mat[1] = {L.codes[1], L.scales[1], L.kv_rows, A.kv32, nullptr};
-        a.mat[2] = {L.codes[2], L.scales[2], L.kv_rows, A.kv32 + L.kv_rows, nullptr};
+        a.mat[1] = {L.codes[1], L.scales[1], L.kv_rows, A.kv32, nullptr, 0};
+        a.mat[2] = {L.codes[2], L.scales[2], L.kv_rows, A.kv32 + L.kv_rows, nullptr, 0};
         a.nmat = 3;
       }
       a.K = A.H;
-      a.in = (s == 0) ? static_cast<const void*>(A.h0) : static_cast<const void*>(A.y32);
+      a.in = (s == 0) ? static_cast<const void*>(A.h0) : static_cast<const void*>(A.y32t);
       a.in_mode = (s == 0) ? Q4_IN_RMS_F16 : Q4_IN_RMS2_F32;
       break;
     case 1:
-      a.mat[0] = {L.codes[3], L.scales[3], A.H, A.o32, nullptr};
+      a.mat[0] = {L.codes[3], L.scales[3], A.H, reinterpret_cast<float*>(A.o32t), nullptr, 1};
       a.nmat = 1;
       a.K = L.q_rows;
-      a.in = A.q16;
+      a.in = A.q16t;
       a.in_mode = Q4_IN_F16;
       break;
     case 2:
-      a.mat[0] = {L.codes[4], L.scales[4], L.mlp_rows, nullptr, A.m16};
-      a.mat[1] = {L.codes[5], L.scales[5], L.mlp_rows, nullptr, nullptr};
+      a.mat[0] = {L.codes[4], L.scales[4], L.mlp_rows, nullptr, reinterpret_cast<__half*>(A.m16t), 1};
+      a.mat[1] = {L.codes[5], L.scales[5], L.mlp_rows, nullptr, nullptr, 0};
       a.nmat = 2;
       a.pair = 1;
       a.K = A.H;
-      a.in = A.o32;
+      a.in = A.o32t;
       a.in_mode = Q4_IN_RMS_F32;
       break;
     default:
-      a.mat[0] = {L.codes[6], L.scales[6], A.H, A.y32, nullptr};
+      a.mat[0] = {L.codes[6], L.scales[6], A.H, reinterpret_cast<float*>(A.y32t), nullptr, 1};
       a.nmat = 1;
       a.K = L.mlp_rows;
-      a.in = A.m16;
+      a.in = A.m16t;
       a.in_mode = Q4_IN_F16;
       break;
   }
   return a;
-}
-
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Consumers of this CTA wait until `cnt` reaches `target`; uniform result.
-__device__ bool wait_counter(const int* cnt, int target, const Ctl& c) {
-  bool ok = true;
-  if (threadIdx.x == 0) {
-    const long long t0 = clock64();
-    for (unsigned it = 0; ld_acquire(cnt) < target; ++it) {
-      if ((it & 63u) == 0) {   // first failed poll, then every 64
-        if (aborting(c)) {
-          ok = false;
-          break;
-        }
-        if (clock64() - t0 > c.limit) {
-          raise_abort(c);
-          ok = false;
-          break;
-        }
-      }
-    }
-    __threadfence();
-  }
-  return bar_and(1, kCT, ok);
 }
 
 __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_constant__ MegaArgs A) {
@@ -841,40 +906,42 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
     __syncwarp();
   } else {
     bool ok = true;
-    unsigned long long* tr = nullptr;
     for (int s = 0; s < nst && ok; ++s) {
       const StageArgs a = mega_stage(A, s);
+      unsigned long long* tr = nullptr;
       if (A.trace && threadIdx.x == 0) {
         tr = A.trace + ((size_t)s * gridDim.x + blockIdx.x) * 8;
         tr[0] = globaltimer();
-        c.tr = tr;
       }
-      if (s > 0 && !wait_counter(A.counters + s - 1, (int)gridDim.x, c)) break;
-      if (tr) tr[1] = globaltimer();
-      eng_prologue(a.in, a.in_mode, a.K, a.eps, S.xs, S.stage_in, S.red);
+      c.tr = tr;
+      // the prologue waits (bounded) until its whole input carries tag s
+      ok = eng_prologue(a, S.xs, S.stage_in, S.red, c);
+      if (!ok) break;
       if (tr) tr[2] = globaltimer();
       StageEpi epi{&a};
       ok = a.pair ? consume_stage<2>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
                   : consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
-      if (!ok) break;
       if (tr) tr[4] = globaltimer();
-      bar_sync(1, kCT);
-      if (tr) tr[5] = globaltimer();
-      if (threadIdx.x == 0) {
-        asm volatile("fence.acq_rel.gpu;\n red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(A.counters + s) : "memory");
-        if (tr) tr[3] = globaltimer();
-      }
     }
-    // closing RMSNorm of the last down-projection output, by CTA 0
-    if (ok && blockIdx.x == 0 && wait_counter(A.counters + nst - 1, (int)gridDim.x, c)) {
-      float ss = 0.f;
-      for (int k = threadIdx.x; k < A.H; k += kCT) {
-        const float v = __ldcg(A.y32 + k);
-        ss += v * v;
+    // closing RMSNorm of the last down-projection output (tag nst), by CTA 0,
+    // with the summation order of q4_rmsnorm_f16 (256 partial sums)
+    if (ok && blockIdx.x == 0) {
+      const int H = A.H;
+      float* sf = reinterpret_cast<float*>(S.stage_in);
+      bool ok2 = true;
+      for (int v = threadIdx.x; v < H / 2 && ok2; v += kCT) {
+        uint4 u;
+        ok2 = poll_tags(reinterpret_cast<const uint4*>(A.y32t) + v, u, false, (uint32_t)nst, c);
+        sf[2 * v] = __uint_as_float(u.x);
+        sf[2 * v + 1] = __uint_as_float(u.z);
       }
-      ss = consumer_sum(ss, S.red);
-      const float r = 1.f / sqrtf(ss / (float)A.H + A.eps);
-      for (int k = threadIdx.x; k < A.H; k += kCT) A.h_out[k] = __float2half_rn(__ldcg(A.y32 + k) * r);
+      if (bar_and(1, kCT, ok2)) {
+        float ss = 0.f;
+        for (int k = threadIdx.x; k < H; k += kCT) ss += sf[k] * sf[k];
+        ss = consumer_sum(ss, S.red);
+        const float r = 1.f / sqrtf(ss / (float)H + A.eps);
+        for (int k = threadIdx.x; k < H; k += kCT) A.h_out[k] = __float2half_rn(sf[k] * r);
+      }
     }
   }
   __syncthreads();
@@ -956,11 +1023,11 @@ int launch_head_stream(const uint8_t* codes, const __half* scales, const __half*
 static void* g_trace_buf = nullptr;
 static size_t g_trace_bytes = 0;
 
-size_t decode_counters_bytes() { return (size_t)(4 * 256 + 64) * sizeof(int); }
+size_t decode_ctl_bytes() { return 256; }
 
 int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const __half* h0, __half* h_out,
-                              float eps, __half* q16, float* kv32, float* o32, __half* m16, float* y32,
-                              int* counters, const DeviceInfo& dev, cudaStream_t s) {
+                              float eps, float* kv32, void* tagged, size_t tagged_bytes, int* ctl,
+                              const DeviceInfo& dev, cudaStream_t s) {
   if (n_layers > eng::kMaxMegaLayers) return fail(Q4_ERR_SHAPE, "persistent pass holds at most %d layers",
                                                   eng::kMaxMegaLayers);
   static bool attr = false;
@@ -976,6 +1043,7 @@ int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const
   if (per_sm < 1) return fail(Q4_ERR_CUDA, "decode pass kernel does not fit on an SM");
   static eng::MegaArgs A;   // host staging of the kernel parameter
   memset(&A, 0, sizeof(A));
+  int max_qkv = 0, max_mlp = 0;
   for (int l = 0; l < n_layers; ++l) {
     const q4_layer& L = layers[l];
     const q4_matrix* m[7] = {&L.q, &L.k, &L.v, &L.o, &L.gate, &L.up, &L.down};
@@ -986,27 +1054,39 @@ int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const
     A.L[l].q_rows = L.q_rows;
     A.L[l].kv_rows = L.kv_rows;
     A.L[l].mlp_rows = L.mlp_rows;
+    if (L.q_rows + 2 * L.kv_rows > max_qkv) max_qkv = L.q_rows + 2 * L.kv_rows;
+    if (L.mlp_rows > max_mlp) max_mlp = L.mlp_rows;
   }
+  // tagged regions, in this order: q [QKV] x 4 B, o [H] x 8 B, m [I] x 4 B, y [H] x 8 B
+  auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
+  char* p = static_cast<char*>(tagged);
+  A.q16t = reinterpret_cast<uint32_t*>(p);
+  p += up((size_t)max_qkv * 4);
+  A.o32t = reinterpret_cast<unsigned long long*>(p);
+  p += up((size_t)H * 8);
+  A.m16t = reinterpret_cast<uint32_t*>(p);
+  p += up((size_t)max_mlp * 4);
+  A.y32t = reinterpret_cast<unsigned long long*>(p);
+  p += up((size_t)H * 8);
+  if ((size_t)(p - static_cast<char*>(tagged)) > tagged_bytes)
+    return fail(Q4_ERR_WORKSPACE, "tagged stage buffers need %zu bytes", (size_t)(p - static_cast<char*>(tagged)));
   A.n_layers = n_layers;
   A.H = H;
   A.eps = eps;
   A.h0 = h0;
   A.h_out = h_out;
-  A.q16 = q16;
   A.kv32 = kv32;
-  A.o32 = o32;
-  A.m16 = m16;
-  A.y32 = y32;
-  A.counters = counters;
-  A.abort_grid = counters + 4 * 256;
+  A.abort_grid = ctl;
   A.limit = wait_limit();
   A.trace = static_cast<unsigned long long*>(g_trace_buf);
   if (A.trace && g_trace_bytes < (size_t)4 * n_layers * dev.sms * 8 * sizeof(unsigned long long))
     return fail(Q4_ERR_WORKSPACE, "trace buffer too small for %d layers", n_layers);
   A.err = device_error_word();
   if (!A.err) return fail(Q4_ERR_CUDA, "device error word unavailable");
-  e = cudaMemsetAsync(counters, 0, decode_counters_bytes(), s);
-  if (e != cudaSuccess) return cuda_fail(e, "decode pass counter reset");
+  // every tag (and the abort word) back to 0 before the pass
+  e = cudaMemsetAsync(tagged, 0, tagged_bytes, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctl, 0, decode_ctl_bytes(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode pass tag reset");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(dev.sms);
   cfg.blockDim = dim3(eng::kTS);

@@ -119,11 +119,16 @@ long long q4_set_wait_limit(long long cycles) {
   return old;
 }
 
+// Decode-pass workspace, each region 256-byte aligned: k/v outputs [QKV] f32,
+// then the four stage buffers sized for their tagged form (q [QKV] x 4 B,
+// o [H] x 8 B, m [I] x 4 B, y [H] x 8 B; the launch-per-stage path uses the
+// same regions untagged), then a 256-byte control block.
+static size_t up256(size_t n) { return (n + 255) & ~(size_t)255; }
+static size_t decode_tagged_bytes(size_t H, size_t QKV, size_t I) {
+  return up256(QKV * 4) + up256(H * 8) + up256(I * 4) + up256(H * 8);
+}
 static size_t decode_ws_bytes(size_t H, size_t QKV, size_t I) {
-  // q16 [QKV] fp16 | k,v f32 [QKV] | o [H] f32 | m16 [I] fp16 | y [H] f32 |
-  // stage counters of the persistent pass; each region 256-byte aligned.
-  auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
-  return up(QKV * 2) + up(QKV * 4) + up(H * 4) + up(I * 2) + up(H * 4) + up(decode_counters_bytes());
+  return up256(QKV * 4) + decode_tagged_bytes(H, QKV, I) + up256(decode_ctl_bytes());
 }
 
 size_t q4_workspace_bytes(int op, int a, int b, int c) {
@@ -285,28 +290,30 @@ int q4_decode_pass(const q4_layer* layers, int n_layers, int H, const uint16_t* 
   DEVICE_OR_RETURN(dev);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
   char* p = reinterpret_cast<char*>(ws);
-  __half* q16 = reinterpret_cast<__half*>(p);
-  p += up((size_t)max_qkv * 2);
   float* kv32 = reinterpret_cast<float*>(p);
-  p += up((size_t)max_qkv * 4);
+  p += up256((size_t)max_qkv * 4);
+  char* tagged = p;
+  const size_t tagged_bytes = decode_tagged_bytes((size_t)H, (size_t)max_qkv, (size_t)max_mlp);
+  __half* q16 = reinterpret_cast<__half*>(p);
+  p += up256((size_t)max_qkv * 4);
   float* o32 = reinterpret_cast<float*>(p);
-  p += up((size_t)H * 4);
+  p += up256((size_t)H * 8);
   __half* m16 = reinterpret_cast<__half*>(p);
-  p += up((size_t)max_mlp * 2);
+  p += up256((size_t)max_mlp * 4);
   float* y32 = reinterpret_cast<float*>(p);
-  p += up((size_t)H * 4);
-  int* counters = reinterpret_cast<int*>(p);
+  p += up256((size_t)H * 8);
+  int* ctl = reinterpret_cast<int*>(p);
 
-  // One persistent cooperative launch when every stage fits the streaming engine.
-  bool persistent = stream_eligible(H) && n_layers <= 48;
+  // One persistent cooperative launch when every stage fits the streaming
+  // engine and every stage input fits its shared staging area (H <= 4096).
+  bool persistent = stream_eligible(H) && H <= 4096 && n_layers <= 48;
   for (int l = 0; l < n_layers && persistent; ++l)
     persistent = stream_eligible(layers[l].q_rows) && stream_eligible(layers[l].mlp_rows);
   if (persistent)
     return launch_decode_pass_stream(layers, n_layers, H, reinterpret_cast<const __half*>(h0_f16),
-                                     reinterpret_cast<__half*>(h_out_f16), eps, q16, kv32, o32, m16, y32, counters,
-                                     dev, s);
+                                     reinterpret_cast<__half*>(h_out_f16), eps, kv32, tagged, tagged_bytes, ctl, dev,
+                                     s);
 
   for (int l = 0; l < n_layers; ++l) {
     const q4_layer& L = layers[l];

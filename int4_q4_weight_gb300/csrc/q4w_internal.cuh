@@ -40,6 +40,8 @@ struct StageMat {
   int rows;
   float* out32;
   __half* out16;
+  int tagged;        // outputs carry the stage tag (persistent pass): out16 -> uint32
+                     // (half | tag << 16), out32 -> uint64 (float | tag << 32)
 };
 
 struct StageArgs {
@@ -50,6 +52,8 @@ struct StageArgs {
   const void* in;
   int in_mode;       // q4_stage_in
   float eps;
+  int in_tag;        // > 0: `in` is tagged (as out16/out32 above); wait until every tag equals it
+  int out_tag;       // tag written with tagged outputs
 };
 
 // Launches one fused stage (prologue + GEMV + epilogue).  `pdl` adds the
@@ -74,10 +78,10 @@ int launch_stage_stream(const StageArgs& a, const DeviceInfo& dev, cudaStream_t 
 int launch_head_stream(const uint8_t* codes, const __half* scales, const __half* h, int V, int K, float cap,
                        int32_t* idx, float* top1, float* top2, float* logits, void* ws, const DeviceInfo& dev,
                        cudaStream_t s);
-size_t decode_counters_bytes();
+size_t decode_ctl_bytes();
 int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const __half* h0, __half* h_out,
-                              float eps, __half* q16, float* kv32, float* o32, __half* m16, float* y32,
-                              int* counters, const DeviceInfo& dev, cudaStream_t s);
+                              float eps, float* kv32, void* tagged, size_t tagged_bytes, int* ctl,
+                              const DeviceInfo& dev, cudaStream_t s);
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, const DeviceInfo& dev, cudaStream_t s);
 

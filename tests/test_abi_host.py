@@ -49,8 +49,9 @@ def test_status_strings(lib):
 def test_decode_workspace_formula(lib):
     up = lambda n: (n + 255) // 256 * 256
     H, QKV, I = 1536, 4096 + 1024, 12288
-    counters = (4 * 256 + 64) * 4          # stage counters of the persistent pass
-    want = up(QKV * 2) + up(QKV * 4) + up(H * 4) + up(I * 2) + up(H * 4) + up(counters)
+    # k/v f32, then q, o, m, y in their tagged form (half|tag: 4 B, float|tag: 8 B),
+    # then a 256-byte control block
+    want = up(QKV * 4) + up(QKV * 4) + up(H * 8) + up(I * 4) + up(H * 8) + 256
     assert lib.q4_workspace_bytes(q4w.Q4_OP_DECODE_PASS, H, QKV, I) == want
     assert lib.q4_workspace_bytes(q4w.Q4_OP_GEMV, 10, 64, 1) == 0
 
