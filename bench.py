@@ -455,32 +455,43 @@ def pass_trace(q4w, synth, dev, reps):
     for _ in range(reps):
         q4w.q4_decode_pass(layers, h0, h, ws, descs=descs)
         torch.cuda.synchronize()
-        t = buf.view(nst, sms, 8).cpu().numpy().astype(np.float64)
-        acc = t if acc is None else acc
+        ti = buf.view(nst, sms, 8).cpu().numpy()
+        acc = ti if acc is None else acc
     q4w.q4_set_trace(None)
-    t = acc
+    ti = acc
+    # stamp 0: globaltimer ns at stage entry; the others: SM cycles since entry
+    # (stamp 5 shifted left by one, bit 0 = first tile had landed already)
+    ghz = 2.07
+    early = (ti[:, :, 5] & 1).reshape(-1, 4, sms)
+    ti = ti.copy()
+    ti[:, :, 0] -= ti[:, :, 0].min()   # relative ns first: float64 cannot hold absolute ns to 1 ns
+    ti[:, :, 5] >>= 1
+    t = ti.astype(np.float64)
+    for i in range(1, 8):
+        t[:, :, i] = t[:, :, 0] + t[:, :, i] / ghz
     t0 = t[0, :, 0].min()
     kinds = ["qkv", "o", "gate_up", "down"]
-    # stamps per (stage, CTA): 0 stage entered, 1 input complete and staged,
-    # 2 x built, 6 first weight tile usable, 4 own rows written
-    out = {"stages": nst, "total_us": round((t[:, :, 4].max() - t0) / 1e3, 2)}
-    agg = {k: {"input_wait": 0.0, "xform": 0.0, "rows_med": 0.0, "rows_max": 0.0, "first_tile_med": 0.0,
-               "handoff": 0.0} for k in kinds}
+    # per (stage, CTA): 0 entered, 7 descriptor read, 1 input complete and
+    # staged, 2 x built, 3 x in registers, 5 first tile landed, 6 first tile
+    # usable by the whole warp, 4 own rows written
+    out = {"stages": nst, "total_us": round((t[:, :, 4].max() - t0) / 1e3, 2), "sm_ghz_assumed": ghz}
+    out["first_tile_already_landed_frac"] = {k: round(float(early[:, i].mean()), 3) for i, k in enumerate(kinds)}
+    names = {"desc": (0, 7), "input_wait": (7, 1), "xform": (1, 2), "x_regs": (2, 3), "tile_wait": (3, 5),
+             "warp_sync": (5, 6), "rows": (6, 4)}
+    agg = {k: {n: 0.0 for n in list(names) + ["rows_max", "handoff", "next_entry"]} for k in kinds}
     for s in range(nst):
         k = kinds[s % 4]
-        agg[k]["input_wait"] += np.median(t[s, :, 1] - t[s, :, 0]) / 1e3
-        agg[k]["xform"] += np.median(t[s, :, 2] - t[s, :, 1]) / 1e3
-        rows = t[s, :, 4] - t[s, :, 2]
-        agg[k]["rows_med"] += np.median(rows) / 1e3
-        agg[k]["rows_max"] += rows.max() / 1e3
-        agg[k]["first_tile_med"] += np.median(np.maximum(t[s, :, 6] - t[s, :, 2], 0)) / 1e3
+        for n, (i, j) in names.items():
+            agg[k][n] += np.median(t[s, :, j] - t[s, :, i]) / 1e3
+        agg[k]["rows_max"] += (t[s, :, 4] - t[s, :, 6]).max() / 1e3
         if s > 0:   # last CTA done with the previous stage -> median CTA has this stage's input
             agg[k]["handoff"] += (np.median(t[s, :, 1]) - t[s - 1, :, 4].max()) / 1e3
+            agg[k]["next_entry"] += np.median(t[s, :, 0] - t[s - 1, :, 4]) / 1e3
     out["per_kind_us_summed_over_layers"] = {k: {q: round(v, 2) for q, v in d.items()} for k, d in agg.items()}
     cta = int(np.argmax(t[8, :, 4]))
-    cols = [0, 1, 2, 6, 4]
-    out["cta0_layer2_stages_us"] = [[round((t[s, 0, i] - t[8, 0, 0]) / 1e3, 2) for i in cols] for s in range(8, 12)]
-    out["slowest_cta_layer2_stages_us"] = [[round((t[s, cta, i] - t[8, 0, 0]) / 1e3, 2) for i in cols]
+    cols = [0, 7, 1, 2, 3, 5, 6, 4]
+    out["cta0_layer2_stages_us"] = [[round((t[s, 0, i] - t[8, 0, 0]) / 1e3, 3) for i in cols] for s in range(8, 12)]
+    out["slowest_cta_layer2_stages_us"] = [[round((t[s, cta, i] - t[8, 0, 0]) / 1e3, 3) for i in cols]
                                            for s in range(8, 12)]
     return out
 

@@ -85,6 +85,7 @@ struct Ctl {
   long long limit;
   unsigned* err;             // the library's device error word
   unsigned long long* tr;    // trace stamps of the current stage (thread 0), or nullptr
+  long long tr_c0;           // clock64() when the current stage began (trace only)
 };
 
 __device__ __forceinline__ void raise_abort(const Ctl& c) {
@@ -121,6 +122,11 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
+}
+
+// Trace stamp: SM cycles since the current stage began.
+__device__ __forceinline__ unsigned long long stamp(const Ctl& c) {
+  return (unsigned long long)(clock64() - c.tr_c0);
 }
 
 __device__ __forceinline__ uint64_t evict_first_policy() {
@@ -264,17 +270,42 @@ __device__ __forceinline__ uint4 ldcg_v4(const void* p) {
 }
 
 // Bounded re-read of one 16-byte group of tagged words until all tags match.
+// Reads of tagged words are relaxed gpu-scope loads (and their writes relaxed
+// gpu-scope stores): a plain load in a polling loop is a weak access the
+// compiler may merge with an earlier read of the same address.  Half words
+// are 32-bit elements, float words 64-bit elements, each read whole.
+__device__ __forceinline__ uint4 ld_tagged(const uint4* p, bool f16) {
+  uint4 r;
+  if (f16) {
+    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p)
+                 : "memory");
+  } else {
+    unsigned long long a, b;
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+    r = make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b, (uint32_t)(b >> 32));
+  }
+  return r;
+}
+__device__ __forceinline__ void st_tagged32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_tagged64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ bool tags_ready(const uint4& v, bool f16, uint32_t tag) {
+  return f16 ? ((v.x >> 16) == tag && (v.y >> 16) == tag && (v.z >> 16) == tag && (v.w >> 16) == tag)
+             : (v.y == tag && v.w == tag);
+}
+
+// u holds a read of p whose tags were not all current.
 __device__ __forceinline__ bool poll_tags(const uint4* p, uint4& u, bool f16, uint32_t tag, const Ctl& c) {
-  auto ready = [&](const uint4& v) {
-    return f16 ? ((v.x >> 16) == tag && (v.y >> 16) == tag && (v.z >> 16) == tag && (v.w >> 16) == tag)
-               : (v.y == tag && v.w == tag);
-  };
-  u = ldcg_v4(p);
-  if (ready(u)) return true;
   const long long t0 = clock64();
   for (unsigned it = 0;; ++it) {
-    u = ldcg_v4(p);
-    if (ready(u)) return true;
+    u = ld_tagged(p, f16);
+    if (tags_ready(u, f16, tag)) return true;
     if ((it & 63u) == 0) {
       if (aborting(c)) return false;
       if (clock64() - t0 > c.limit) {
@@ -312,25 +343,33 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
       const uint4* src = reinterpret_cast<const uint4*>(a.in);
       uint4* dst = reinterpret_cast<uint4*>(stage_in);
       for (int v = tid; v < K * esz / 16; v += kCT) dst[v] = ldcg_v4(src + v);
-    } else if (f16in) {       // uint32 words: half | tag << 16, four per 16 bytes
+    } else {
+      // Tagged words: half | tag << 16 (four per 16 bytes) or float | tag << 32
+      // (two per 16 bytes).  A thread issues all of its 16-byte reads at once
+      // (one L2 round trip), then re-reads only groups whose tags are stale.
       const uint4* src = reinterpret_cast<const uint4*>(a.in);
       uint2* dst = reinterpret_cast<uint2*>(stage_in);
-      for (int v = tid; v < K / 4 && ok; v += kCT) {
-        uint4 u;
-        ok = poll_tags(src + v, u, true, (uint32_t)a.in_tag, c);
-        dst[v] = make_uint2(__byte_perm(u.x, u.y, 0x5410), __byte_perm(u.z, u.w, 0x5410));
-      }
-    } else {                  // uint64 words: float | tag << 32, two per 16 bytes
-      const uint4* src = reinterpret_cast<const uint4*>(a.in);
-      uint2* dst = reinterpret_cast<uint2*>(stage_in);
-      for (int v = tid; v < K / 2 && ok; v += kCT) {
-        uint4 u;
-        ok = poll_tags(src + v, u, false, (uint32_t)a.in_tag, c);
-        dst[v] = make_uint2(u.x, u.z);
+      const int nv = f16in ? K / 4 : K / 2;
+      const uint32_t tag = (uint32_t)a.in_tag;
+      constexpr int kPB = 1;
+      for (int v0 = tid; v0 < nv && ok; v0 += kPB * kCT) {
+        uint4 u[kPB];
+#pragma unroll
+        for (int i = 0; i < kPB; ++i)
+          if (v0 + i * kCT < nv) u[i] = ld_tagged(src + v0 + i * kCT, f16in);
+#pragma unroll
+        for (int i = 0; i < kPB; ++i) {
+          const int v = v0 + i * kCT;
+          if (v < nv && ok) {
+            if (!tags_ready(u[i], f16in, tag)) ok = poll_tags(src + v, u[i], f16in, tag, c);
+            dst[v] = f16in ? make_uint2(__byte_perm(u[i].x, u[i].y, 0x5410), __byte_perm(u[i].z, u[i].w, 0x5410))
+                           : make_uint2(u[i].x, u[i].z);
+          }
+        }
       }
     }
     if (!bar_and(1, kCT, ok)) return false;
-    if (c.tr) c.tr[1] = globaltimer();   // input complete and staged
+    if (c.tr) c.tr[1] = stamp(c);   // input complete and staged
     const __half* sh = reinterpret_cast<const __half*>(stage_in);
     const float* sf = reinterpret_cast<const float*>(stage_in);
     auto val = [&](int k) { return f16in ? __half2float(sh[k]) : sf[k]; };
@@ -447,18 +486,18 @@ struct StageEpi {
       if (a->mat[1].out32) a->mat[1].out32[row] = uv;
       const __half mh = __float2half_rn(gelu_tanh_f32(gv) * uv);
       if (a->mat[0].tagged)
-        reinterpret_cast<uint32_t*>(a->mat[0].out16)[row] = (uint32_t)__half_as_ushort(mh) | (tag << 16);
+        st_tagged32(reinterpret_cast<uint32_t*>(a->mat[0].out16) + row, (uint32_t)__half_as_ushort(mh) | (tag << 16));
       else
         a->mat[0].out16[row] = mh;
     } else {
       const StageMat& M = a->mat[m];
       if (M.tagged) {
         if (M.out32)
-          reinterpret_cast<unsigned long long*>(M.out32)[row] =
-              (unsigned long long)__float_as_uint(acc[0]) | ((unsigned long long)tag << 32);
+          st_tagged64(reinterpret_cast<unsigned long long*>(M.out32) + row,
+                      (unsigned long long)__float_as_uint(acc[0]) | ((unsigned long long)tag << 32));
         if (M.out16)
-          reinterpret_cast<uint32_t*>(M.out16)[row] =
-              (uint32_t)__half_as_ushort(__float2half_rn(acc[0])) | (tag << 16);
+          st_tagged32(reinterpret_cast<uint32_t*>(M.out16) + row,
+                      (uint32_t)__half_as_ushort(__float2half_rn(acc[0])) | (tag << 16));
       } else {
         if (M.out32) M.out32[row] = acc[0];
         if (M.out16) M.out16[row] = __float2half_rn(acc[0]);
@@ -504,17 +543,21 @@ __device__ bool consume_fast(const StageArgs& a, const Geo& g, uint32_t& gcount,
   for (int b = 0; b < BPL; ++b) load_xh(xs, li + P * b, xr[b], bias[b]);
   const int K2 = g.K2, nb = g.nb;
   const int row_first = P <= 32 ? warp * GW + lane / P : gid;   // this lane's first row of a tile
+  if (c.tr && ct == 0) c.tr[3] = stamp(c);   // x in registers
   bool ok = true;
   int pos = g.lo, m, r0, n;
   while (tile_next(a, g, pos, m, r0, n)) {
     const uint32_t s = gcount % kSlots, round = gcount / kSlots;
+    const bool early = c.tr && mbar_test(full0 + 8 * s, round & 1);
     const bool landed = mbar_wait(full0 + 8 * s, round & 1, c);
+    // first tile landed; bit 0 set when it had landed before the consumers asked
+    if (c.tr && ct == 0 && pos == g.lo + n) c.tr[5] = (stamp(c) << 1) | (early ? 1ull : 0ull);
     const bool all = (P <= 32) ? (__all_sync(0xffffffffu, landed) != 0) : bar_and(2 + gid, P, landed);
     if (!all) {
       ok = false;
       break;
     }
-    if (c.tr && ct == 0 && pos == g.lo + n) c.tr[6] = globaltimer();
+    if (c.tr && ct == 0 && pos == g.lo + n) c.tr[6] = stamp(c);
     const uint8_t* S = slots + (size_t)s * kSlotBytes;
     const int per = n * (K2 + nb * 2);
     const uint8_t* sc_base = S + n * K2;
@@ -616,16 +659,20 @@ __device__ bool consume_generic(const StageArgs& a, const Geo& g, uint32_t& gcou
   const int GW = P <= 32 ? 32 / P : 1, WPG = P > 32 ? P / 32 : 1;
   const int row_first = P <= 32 ? warp * GW : gid;
   const int row_lane = P <= 32 ? lane / P : 0;
+  if (c.tr && ct == 0) c.tr[3] = stamp(c);   // x in registers
   bool ok = true;
   int pos = g.lo, m, r0, n;
   while (tile_next(a, g, pos, m, r0, n)) {
     const uint32_t s = gcount % kSlots, round = gcount / kSlots;
+    const bool early = c.tr && mbar_test(full0 + 8 * s, round & 1);
     const bool landed = mbar_wait(full0 + 8 * s, round & 1, c);
+    if (c.tr && ct == 0 && pos == g.lo + n) c.tr[5] = (stamp(c) << 1) | (early ? 1ull : 0ull);
     const bool all = (P <= 32) ? (__all_sync(0xffffffffu, landed) != 0) : bar_and(2 + gid, P, landed);
     if (!all) {
       ok = false;
       break;
     }
+    if (c.tr && ct == 0 && pos == g.lo + n) c.tr[6] = stamp(c);
     const uint8_t* S = slots + (size_t)s * kSlotBytes;
     const int per = n * (g.K2 + g.nb * 2);
     for (int rb = row_first; rb < n; rb += Gc) {
@@ -836,8 +883,8 @@ struct MegaArgs {
 // Stage s of the pass as StageArgs (the same stages the launch path issues).
 // Stage s tags its outputs s + 1; its input is complete once every element
 // carries tag s (stage 0 reads the untagged h0).
-__device__ __forceinline__ StageArgs mega_stage(const MegaArgs& A, int s) {
-  const MegaLayer& L = A.L[s >> 2];
+__device__ __forceinline__ StageArgs mega_stage(const MegaArgs& A, const MegaLayer* Ls, int s) {
+  const MegaLayer& L = Ls[s >> 2];
   StageArgs a = {};
   a.eps = A.eps;
   a.in_tag = s;
@@ -885,18 +932,27 @@ __device__ __forceinline__ StageArgs mega_stage(const MegaArgs& A, int s) {
 __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_constant__ MegaArgs A) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int abort_sh;
+  // layer descriptors copied once from the parameter space: a stage reads its
+  // descriptor from shared memory instead of through the constant caches
+  __shared__ __align__(16) MegaLayer Ls[kMaxMegaLayers];
   const Smem S = carve(smem_raw);
   if (threadIdx.x == 0) abort_sh = 0;
   init_barriers(S);
+  {
+    constexpr int kWords = (int)(sizeof(MegaLayer) / sizeof(uint32_t));
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(A.L);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(Ls);
+    for (int i = threadIdx.x; i < A.n_layers * kWords; i += blockDim.x) dst[i] = src[i];
+  }
   __syncthreads();
-  Ctl c{&abort_sh, A.abort_grid, A.limit, A.err, nullptr};
+  Ctl c{&abort_sh, A.abort_grid, A.limit, A.err, nullptr, 0};
   const int nst = 4 * A.n_layers;
   uint32_t gcount = 0;
   if (threadIdx.x >= kCT) {
     if (threadIdx.x == kCT) {
       const uint64_t pol = evict_first_policy();
       for (int s = 0; s < nst; ++s) {
-        const StageArgs a = mega_stage(A, s);
+        const StageArgs a = mega_stage(A, Ls, s);
         const bool ok = a.pair ? produce_stage<2>(a, gcount, S.slots0, S.full0, S.empty0, pol, c)
                                : produce_stage<1>(a, gcount, S.slots0, S.full0, S.empty0, pol, c);
         if (!ok) break;
@@ -907,21 +963,23 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
   } else {
     bool ok = true;
     for (int s = 0; s < nst && ok; ++s) {
-      const StageArgs a = mega_stage(A, s);
       unsigned long long* tr = nullptr;
       if (A.trace && threadIdx.x == 0) {
         tr = A.trace + ((size_t)s * gridDim.x + blockIdx.x) * 8;
         tr[0] = globaltimer();
+        c.tr_c0 = clock64();
       }
       c.tr = tr;
+      const StageArgs a = mega_stage(A, Ls, s);
+      if (tr) tr[7] = stamp(c);
       // the prologue waits (bounded) until its whole input carries tag s
       ok = eng_prologue(a, S.xs, S.stage_in, S.red, c);
       if (!ok) break;
-      if (tr) tr[2] = globaltimer();
+      if (tr) tr[2] = stamp(c);
       StageEpi epi{&a};
       ok = a.pair ? consume_stage<2>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
                   : consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
-      if (tr) tr[4] = globaltimer();
+      if (tr) tr[4] = stamp(c);
     }
     // closing RMSNorm of the last down-projection output (tag nst), by CTA 0,
     // with the summation order of q4_rmsnorm_f16 (256 partial sums)
@@ -930,8 +988,9 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       float* sf = reinterpret_cast<float*>(S.stage_in);
       bool ok2 = true;
       for (int v = threadIdx.x; v < H / 2 && ok2; v += kCT) {
-        uint4 u;
-        ok2 = poll_tags(reinterpret_cast<const uint4*>(A.y32t) + v, u, false, (uint32_t)nst, c);
+        const uint4* p = reinterpret_cast<const uint4*>(A.y32t) + v;
+        uint4 u = ld_tagged(p, false);
+        if (!tags_ready(u, false, (uint32_t)nst)) ok2 = poll_tags(p, u, false, (uint32_t)nst, c);
         sf[2 * v] = __uint_as_float(u.x);
         sf[2 * v + 1] = __uint_as_float(u.z);
       }
