@@ -935,6 +935,13 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
   // layer descriptors copied once from the parameter space: a stage reads its
   // descriptor from shared memory instead of through the constant caches
   __shared__ __align__(16) MegaLayer Ls[kMaxMegaLayers];
+  // Stage descriptors live in shared memory: as per-thread values they would
+  // sit in local memory (the matrix array is indexed at run time), hundreds
+  // of KB per CTA that the small L1 left beside the shared carve-out cannot
+  // hold.  sa[s & 1] is stage s for the consumers (thread 0 fills the next
+  // one while a stage runs); sp is the producer's.
+  __shared__ __align__(16) StageArgs sa[2];
+  __shared__ __align__(16) StageArgs sp;
   const Smem S = carve(smem_raw);
   if (threadIdx.x == 0) abort_sh = 0;
   init_barriers(S);
@@ -945,6 +952,8 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
     for (int i = threadIdx.x; i < A.n_layers * kWords; i += blockDim.x) dst[i] = src[i];
   }
   __syncthreads();
+  if (threadIdx.x == 0) sa[0] = mega_stage(A, Ls, 0);
+  __syncthreads();
   Ctl c{&abort_sh, A.abort_grid, A.limit, A.err, nullptr, 0};
   const int nst = 4 * A.n_layers;
   uint32_t gcount = 0;
@@ -952,7 +961,8 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
     if (threadIdx.x == kCT) {
       const uint64_t pol = evict_first_policy();
       for (int s = 0; s < nst; ++s) {
-        const StageArgs a = mega_stage(A, Ls, s);
+        sp = mega_stage(A, Ls, s);
+        const StageArgs& a = sp;
         const bool ok = a.pair ? produce_stage<2>(a, gcount, S.slots0, S.full0, S.empty0, pol, c)
                                : produce_stage<1>(a, gcount, S.slots0, S.full0, S.empty0, pol, c);
         if (!ok) break;
@@ -970,7 +980,10 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
         c.tr_c0 = clock64();
       }
       c.tr = tr;
-      const StageArgs a = mega_stage(A, Ls, s);
+      // every consumer finished stage s - 1 (the barrier closing its rows), so
+      // the slot of stage s + 1 is free; the barrier closing stage s publishes it
+      if (threadIdx.x == 0 && s + 1 < nst) sa[(s + 1) & 1] = mega_stage(A, Ls, s + 1);
+      const StageArgs& a = sa[s & 1];
       if (tr) tr[7] = stamp(c);
       // the prologue waits (bounded) until its whole input carries tag s
       ok = eng_prologue(a, S.xs, S.stage_in, S.red, c);
