@@ -351,7 +351,7 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
       uint2* dst = reinterpret_cast<uint2*>(stage_in);
       const int nv = f16in ? K / 4 : K / 2;
       const uint32_t tag = (uint32_t)a.in_tag;
-      constexpr int kPB = 1;
+      constexpr int kPB = 4;
       for (int v0 = tid; v0 < nv && ok; v0 += kPB * kCT) {
         uint4 u[kPB];
 #pragma unroll
