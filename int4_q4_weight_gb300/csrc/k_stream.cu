@@ -334,8 +334,7 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
   const int tid = threadIdx.x, K = a.K, mode = a.in_mode;
   const bool f16in = mode == Q4_IN_F16 || mode == Q4_IN_RMS_F16;
   const int esz = f16in ? 2 : 4;
-  const int xoff = (mode == Q4_IN_F16) ? 0 : K * esz;      // where the fp16 x array starts
-  const bool staged = xoff + K * 2 <= kStageInBytes;
+  const bool staged = K * esz <= kStageInBytes;
   float r = 1.f, r2 = 1.f;
   if (staged) {
     bool ok = true;
@@ -370,58 +369,77 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
     }
     if (!bar_and(1, kCT, ok)) return false;
     if (c.tr) c.tr[1] = stamp(c);   // input complete and staged
-    const __half* sh = reinterpret_cast<const __half*>(stage_in);
-    const float* sf = reinterpret_cast<const float*>(stage_in);
-    auto val = [&](int k) { return f16in ? __half2float(sh[k]) : sf[k]; };
+    // Each thread takes chunks of eight consecutive elements (four chunks per
+    // 32-column block): sums of squares for the RMS factors, then x, whose
+    // half pairs (x[8i+j], x[8i+j+4]) lie within one chunk; the bias sums the
+    // block's four chunks across adjacent lanes.
+    const int nch = K >> 3;
+    auto load8 = [&](int ch, float (&v)[8]) {
+      if (f16in) {
+        const uint4 u = *reinterpret_cast<const uint4*>(stage_in + (size_t)ch * 16);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+          v[2 * i] = f.x;
+          v[2 * i + 1] = f.y;
+        }
+      } else {
+        const float4 f0 = *reinterpret_cast<const float4*>(stage_in + (size_t)ch * 32);
+        const float4 f1 = *reinterpret_cast<const float4*>(stage_in + (size_t)ch * 32 + 16);
+        v[0] = f0.x;
+        v[1] = f0.y;
+        v[2] = f0.z;
+        v[3] = f0.w;
+        v[4] = f1.x;
+        v[5] = f1.y;
+        v[6] = f1.z;
+        v[7] = f1.w;
+      }
+    };
     if (mode != Q4_IN_F16) {
       float ss = 0.f;
-      for (int k = tid; k < K; k += kCT) {
-        const float v = val(k);
-        ss += v * v;
+      for (int ch = tid; ch < nch; ch += kCT) {
+        float v[8];
+        load8(ch, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss += v[e] * v[e];
       }
       ss = consumer_sum(ss, red8);
       r = 1.f / sqrtf(ss / (float)K + a.eps);
       if (mode == Q4_IN_RMS2_F32) {
         float ss2 = 0.f;
-        for (int k = tid; k < K; k += kCT) {
-          const float t = f16_round(val(k) * r);
-          ss2 += t * t;
+        for (int ch = tid; ch < nch; ch += kCT) {
+          float v[8];
+          load8(ch, v);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float t = f16_round(v[e] * r);
+            ss2 += t * t;
+          }
         }
         ss2 = consumer_sum(ss2, red8);
         r2 = 1.f / sqrtf(ss2 / (float)K + a.eps);
       }
-      __half* x16 = reinterpret_cast<__half*>(stage_in + xoff);
-      for (int k = tid; k < K; k += kCT) x16[k] = __float2half_rn(xform(val(k), mode, r, r2));
-      bar_sync(1, kCT);
     }
-    // one thread per 32-column block: fp16 words (x[2t], x[2t+1]) -> pairs by byte permute
-    const int nb = K >> 5;
-    for (int b = tid; b < nb; b += kCT) {
-      const uint4* src = reinterpret_cast<const uint4*>(stage_in + xoff + (size_t)b * 64);
-      uint32_t w[16];
+    // K % 256 == 0 here, so every pass of this loop keeps whole warps active
+    for (int ch = tid; ch < nch; ch += kCT) {
+      float v[8];
+      load8(ch, v);
+      uint32_t hx[8];
+      float part = 0.f;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const uint4 u = src[t];
-        w[4 * t] = u.x;
-        w[4 * t + 1] = u.y;
-        w[4 * t + 2] = u.z;
-        w[4 * t + 3] = u.w;
+      for (int e = 0; e < 8; ++e) {
+        const __half x = __float2half_rn(xform(v[e], mode, r, r2));
+        hx[e] = __half_as_ushort(x);
+        part += __half2float(x);
       }
-      uint32_t* q = xh + b * kXhStride;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t lo = w[4 * i + (j >> 1)], hi = w[4 * i + 2 + (j >> 1)];
-          q[4 * i + j] = __byte_perm(lo, hi, (j & 1) ? 0x7632 : 0x5410);
-        }
-      float sum = 0.f;
-#pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[t]));
-        sum += f.x + f.y;
-      }
-      q[16] = __float_as_uint(-72.f * sum);
+      const int blk = ch >> 2, i = ch & 3;
+      *reinterpret_cast<uint4*>(xh + blk * kXhStride + 4 * i) =
+          make_uint4(hx[0] | (hx[4] << 16), hx[1] | (hx[5] << 16), hx[2] | (hx[6] << 16), hx[3] | (hx[7] << 16));
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if (i == 0) xh[blk * kXhStride + 16] = __float_as_uint(-72.f * part);
     }
     bar_sync(1, kCT);
     return true;
