@@ -745,9 +745,9 @@ __device__ bool consume_generic(const StageArgs& a, const Geo& g, uint32_t& gcou
 
 // Processes one stage's tiles; false when aborting (uniform over consumers).
 template <int NM, class Epi>
-__device__ bool consume_stage(const StageArgs& a, uint32_t& gcount, const uint8_t* slots, uint32_t full0,
-                              uint32_t empty0, const uint32_t* xs, float* red, const Ctl& c, const Epi& epi) {
-  const Geo g = make_geo(a, NM);
+__device__ bool consume_stage(const StageArgs& a, const Geo& g, uint32_t& gcount, const uint8_t* slots,
+                              uint32_t full0, uint32_t empty0, const uint32_t* xs, float* red, const Ctl& c,
+                              const Epi& epi) {
 #define Q4W_FAST(P, BPL)                                                                              \
   return g.R == 2 ? consume_fast<NM, P, BPL, 2>(a, g, gcount, slots, full0, empty0, xs, red, c, epi)  \
                   : consume_fast<NM, P, BPL, 1>(a, g, gcount, slots, full0, empty0, xs, red, c, epi)
@@ -827,7 +827,7 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
     pdl_wait();
     if (eng_prologue(a, S.xs, S.stage_in, S.red, c)) {
       StageEpi epi{&a};
-      consume_stage<NM>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+      consume_stage<NM>(a, make_geo(a, NM), gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
     }
   }
   __syncthreads();
@@ -858,7 +858,7 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
   } else {
     if (eng_prologue(a, S.xs, S.stage_in, S.red, c)) {
       HeadEpi epi{&best, logits, cap};
-      consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+      consume_stage<1>(a, make_geo(a, 1), gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
     }
   }
   st[threadIdx.x] = best;
@@ -960,6 +960,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
   // one while a stage runs); sp is the producer's.
   __shared__ __align__(16) StageArgs sa[2];
   __shared__ __align__(16) StageArgs sp;
+  __shared__ Geo sg[2];   // the consumers' tile geometry of sa[0], sa[1]
   const Smem S = carve(smem_raw);
   if (threadIdx.x == 0) abort_sh = 0;
   init_barriers(S);
@@ -970,7 +971,10 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
     for (int i = threadIdx.x; i < A.n_layers * kWords; i += blockDim.x) dst[i] = src[i];
   }
   __syncthreads();
-  if (threadIdx.x == 0) sa[0] = mega_stage(A, Ls, 0);
+  if (threadIdx.x == 0) {
+    sa[0] = mega_stage(A, Ls, 0);
+    sg[0] = make_geo(sa[0], sa[0].pair ? 2 : 1);
+  }
   __syncthreads();
   Ctl c{&abort_sh, A.abort_grid, A.limit, A.err, nullptr, 0};
   const int nst = 4 * A.n_layers;
@@ -1000,7 +1004,11 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       c.tr = tr;
       // every consumer finished stage s - 1 (the barrier closing its rows), so
       // the slot of stage s + 1 is free; the barrier closing stage s publishes it
-      if (threadIdx.x == 0 && s + 1 < nst) sa[(s + 1) & 1] = mega_stage(A, Ls, s + 1);
+      if (threadIdx.x == 0 && s + 1 < nst) {
+        StageArgs& nx = sa[(s + 1) & 1];
+        nx = mega_stage(A, Ls, s + 1);
+        sg[(s + 1) & 1] = make_geo(nx, nx.pair ? 2 : 1);
+      }
       const StageArgs& a = sa[s & 1];
       if (tr) tr[7] = stamp(c);
       // the prologue waits (bounded) until its whole input carries tag s
@@ -1008,8 +1016,9 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       if (!ok) break;
       if (tr) tr[2] = stamp(c);
       StageEpi epi{&a};
-      ok = a.pair ? consume_stage<2>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
-                  : consume_stage<1>(a, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+      const Geo& g = sg[s & 1];
+      ok = a.pair ? consume_stage<2>(a, g, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
+                  : consume_stage<1>(a, g, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
       if (tr) tr[4] = stamp(c);
     }
     // closing RMSNorm of the last down-projection output (tag nst), by CTA 0,
