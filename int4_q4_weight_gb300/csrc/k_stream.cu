@@ -102,8 +102,18 @@ __device__ __forceinline__ bool aborting(const Ctl& c) {
 // The shared abort flag is read every iteration; the grid-wide flag (a
 // global load, about an L2 round trip) and the clock on the first retry and
 // then every 256 (so a zero budget gives up at once).
+__device__ __forceinline__ bool mbar_probe(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, const Ctl& c) {
-  if (mbar_test(a, parity)) return true;
+  if (mbar_probe(a, parity)) return true;
   const long long t0 = clock64();
   for (unsigned it = 1;; ++it) {
     if (mbar_test(a, parity)) return true;
@@ -175,23 +185,34 @@ __device__ __forceinline__ Geo make_geo(const StageArgs& a, int NM) {
   return g;
 }
 
-// Next tile [r0, r0+n) of matrix m (pair: of both matrices) in [pos, hi).
-__device__ __forceinline__ bool tile_next(const StageArgs& a, const Geo& g, int& pos, int& m, int& r0,
-                                          int& n) {
-  if (pos >= g.hi) return false;
-  int base = 0;
-  m = 0;
-  if (!a.pair) {
-    while (m < a.nmat - 1 && pos >= base + a.mat[m].rows) {
-      base += a.mat[m].rows;
-      ++m;
-    }
+// Walk over this CTA's rows [lo, hi) of a stage, tile by tile: the next tile
+// [r0, r0 + n) of matrix m (pair: of both matrices), at most T rows and never
+// across a matrix boundary.  The boundaries are held in registers.
+struct TileIter {
+  int pos, hi, T, e0, e1, first_end;
+  __device__ __forceinline__ TileIter(const StageArgs& a, const Geo& g) {
+    pos = g.lo;
+    hi = g.hi;
+    T = g.T;
+    const int r0 = a.mat[0].rows, r1 = a.mat[1].rows;
+    const int nm = a.pair ? 1 : a.nmat;
+    e0 = nm > 1 ? r0 : g.total;
+    e1 = nm > 2 ? r0 + r1 : g.total;
+    first_end = -1;
   }
-  r0 = pos - base;
-  n = min(g.T, min(g.hi - pos, a.mat[m].rows - r0));
-  pos += n;
-  return true;
-}
+  __device__ __forceinline__ bool next(int& m, int& r0, int& n) {
+    if (pos >= hi) return false;
+    m = (pos >= e0 ? 1 : 0) + (pos >= e1 ? 1 : 0);
+    const int base = m == 0 ? 0 : (m == 1 ? e0 : e1);
+    const int end = min(hi, m == 0 ? e0 : (m == 1 ? e1 : hi));
+    r0 = pos - base;
+    n = min(T, end - pos);
+    pos += n;
+    if (first_end < 0) first_end = pos;
+    return true;
+  }
+  __device__ __forceinline__ bool first() const { return pos == first_end; }
+};
 
 // ------------------------------------------------------------- producer ---
 // Issues the bulk copies of one stage's tiles; false when aborting.
@@ -199,8 +220,9 @@ template <int NM>
 __device__ bool produce_stage(const StageArgs& a, uint32_t& gcount, uint32_t slots0, uint32_t full0,
                               uint32_t empty0, uint64_t policy, const Ctl& c) {
   const Geo g = make_geo(a, NM);
-  int pos = g.lo, m, r0, n;
-  while (tile_next(a, g, pos, m, r0, n)) {
+  TileIter it(a, g);
+  int m, r0, n;
+  while (it.next(m, r0, n)) {
     const uint32_t s = gcount % kSlots, round = gcount / kSlots;
     if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, c)) return false;
     const uint32_t per = (uint32_t)n * (g.K2 + g.nb * 2);
@@ -563,19 +585,20 @@ __device__ bool consume_fast(const StageArgs& a, const Geo& g, uint32_t& gcount,
   const int row_first = P <= 32 ? warp * GW + lane / P : gid;   // this lane's first row of a tile
   if (c.tr && ct == 0) c.tr[3] = stamp(c);   // x in registers
   bool ok = true;
-  int pos = g.lo, m, r0, n;
-  while (tile_next(a, g, pos, m, r0, n)) {
+  TileIter it(a, g);
+  int m, r0, n;
+  while (it.next(m, r0, n)) {
     const uint32_t s = gcount % kSlots, round = gcount / kSlots;
-    const bool early = c.tr && mbar_test(full0 + 8 * s, round & 1);
+    const bool early = c.tr && mbar_probe(full0 + 8 * s, round & 1);
     const bool landed = mbar_wait(full0 + 8 * s, round & 1, c);
     // first tile landed; bit 0 set when it had landed before the consumers asked
-    if (c.tr && ct == 0 && pos == g.lo + n) c.tr[5] = (stamp(c) << 1) | (early ? 1ull : 0ull);
+    if (c.tr && ct == 0 && it.first()) c.tr[5] = (stamp(c) << 1) | (early ? 1ull : 0ull);
     const bool all = (P <= 32) ? (__all_sync(0xffffffffu, landed) != 0) : bar_and(2 + gid, P, landed);
     if (!all) {
       ok = false;
       break;
     }
-    if (c.tr && ct == 0 && pos == g.lo + n) c.tr[6] = stamp(c);
+    if (c.tr && ct == 0 && it.first()) c.tr[6] = stamp(c);
     const uint8_t* S = slots + (size_t)s * kSlotBytes;
     const int per = n * (K2 + nb * 2);
     const uint8_t* sc_base = S + n * K2;
@@ -679,18 +702,19 @@ __device__ bool consume_generic(const StageArgs& a, const Geo& g, uint32_t& gcou
   const int row_lane = P <= 32 ? lane / P : 0;
   if (c.tr && ct == 0) c.tr[3] = stamp(c);   // x in registers
   bool ok = true;
-  int pos = g.lo, m, r0, n;
-  while (tile_next(a, g, pos, m, r0, n)) {
+  TileIter it(a, g);
+  int m, r0, n;
+  while (it.next(m, r0, n)) {
     const uint32_t s = gcount % kSlots, round = gcount / kSlots;
-    const bool early = c.tr && mbar_test(full0 + 8 * s, round & 1);
+    const bool early = c.tr && mbar_probe(full0 + 8 * s, round & 1);
     const bool landed = mbar_wait(full0 + 8 * s, round & 1, c);
-    if (c.tr && ct == 0 && pos == g.lo + n) c.tr[5] = (stamp(c) << 1) | (early ? 1ull : 0ull);
+    if (c.tr && ct == 0 && it.first()) c.tr[5] = (stamp(c) << 1) | (early ? 1ull : 0ull);
     const bool all = (P <= 32) ? (__all_sync(0xffffffffu, landed) != 0) : bar_and(2 + gid, P, landed);
     if (!all) {
       ok = false;
       break;
     }
-    if (c.tr && ct == 0 && pos == g.lo + n) c.tr[6] = stamp(c);
+    if (c.tr && ct == 0 && it.first()) c.tr[6] = stamp(c);
     const uint8_t* S = slots + (size_t)s * kSlotBytes;
     const int per = n * (g.K2 + g.nb * 2);
     for (int rb = row_first; rb < n; rb += Gc) {
