@@ -228,6 +228,13 @@ int q4_decode_pass(const q4_layer* layers, int n_layers, int H, const uint16_t* 
                    uint16_t* h_out_f16, float eps, void* ws, size_t ws_bytes,
                    q4_stream_t stream);
 
+/* q4_decode_pass_launches: how many kernels one q4_decode_pass call with
+ * these arguments launches: 1 (the persistent form) or 4 * n_layers + 1
+ * (one per stage, then the closing RMSNorm).  Memsets are not counted.
+ * Returns a negative Q4_ERR_* when layers is NULL or n_layers is out of
+ * range; shapes are otherwise checked by q4_decode_pass itself. */
+int q4_decode_pass_launches(const q4_layer* layers, int n_layers, int H);
+
 /* Prologue of one decode-pass stage, exposed for stage tests. */
 typedef enum q4_stage_in {
   Q4_IN_F16 = 0,          /* x = in (fp16) */
@@ -284,12 +291,14 @@ int q4_device_status(q4_stream_t stream);
 long long q4_set_wait_limit(long long cycles);
 
 /* q4_set_trace: diagnostic.  While `buf` (device memory) is set, every
- * persistent q4_decode_pass launch writes, per stage s and CTA c, globaltimer
- * stamps (ns) to buf[(s * grid + c) * 8 + i]: i=0 before waiting for the
- * previous stage, 1 after that wait, 2 after the stage prologue, 3 after the
- * stage's completion signal, 4 when this thread finished its share of the
- * stage's rows, 5 after the CTA's consumers all finished (grid = the SM
- * count).  Needs 4 * n_layers * grid * 8 * 8 bytes.  NULL turns it off. */
+ * persistent q4_decode_pass launch writes, per stage s and CTA c, eight
+ * stamps to buf[(s * grid + c) * 8 + i] (grid = the SM count): i=0 the
+ * globaltimer (ns) when the CTA entered the stage; the others SM clock
+ * cycles since then: 1 input complete and staged, 2 x built, 3 x in
+ * registers, 5 first weight tile landed (shifted left by one; bit 0 set when
+ * it had landed before the consumers asked), 6 first tile usable by the
+ * whole warp, 4 this CTA's rows written; 7 unused.  Needs
+ * 4 * n_layers * grid * 8 * 8 bytes.  NULL turns it off. */
 int q4_set_trace(void* buf, size_t bytes);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */

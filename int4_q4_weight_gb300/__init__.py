@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "load", "build", "Q4Error", "q4_quantize", "q4_gemv", "q4_gemv_stage", "q4_rmsnorm_f16",
-    "q4_decode_pass", "lmhead_softcap_argmax", "ple_gather_project", "q4_gemm_chunk",
+    "q4_decode_pass", "q4_decode_pass_launches", "lmhead_softcap_argmax", "ple_gather_project", "q4_gemm_chunk",
     "q4_workspace_bytes", "q4_version", "Q4_IN_F16", "Q4_IN_RMS_F16", "Q4_IN_RMS_F32",
     "Q4_IN_RMS2_F32", "Q4_OP_GEMV", "Q4_OP_GEMM_CHUNK", "Q4_OP_PLE", "Q4_OP_LMHEAD",
     "Q4_OP_DECODE_PASS", "q4_layer", "q4_matrix",
@@ -54,6 +54,7 @@ _SIGS = {
     "lmhead_softcap_argmax": (ci, [vp, vp, vp, ci, ci, ci, cf, vp, vp, vp, vp, vp, csz, vp]),
     "lmhead_softcap_argmax_noalloc": (ci, [vp, vp, vp, ci, ci, ci, cf, vp, vp, vp, vp, vp]),
     "q4_decode_pass": (ci, [ctypes.POINTER(q4_layer), ci, ci, vp, vp, cf, vp, csz, vp]),
+    "q4_decode_pass_launches": (ci, [ctypes.POINTER(q4_layer), ci, ci]),
     "q4_gemv_stage": (ci, [ctypes.POINTER(q4_matrix), ctypes.POINTER(ci), ci, ci, vp, ci, cf, ci,
                            ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
     "q4_rmsnorm_f16": (ci, [vp, ci, cf, vp, vp]),
@@ -322,6 +323,14 @@ def q4_gemm_chunk(codes, scales, X, Y=None):
     return Y
 
 
+def q4_decode_pass_launches(descs, H):
+    """Kernels one q4_decode_pass call over ``descs`` (make_layers output) launches."""
+    n = load().q4_decode_pass_launches(descs, len(descs), H)
+    if n < 0:
+        _check(-n, "q4_decode_pass_launches")
+    return n
+
+
 class Q4DecodePlan:
     """A decode weight pass bound to fixed device buffers and captured once into
     a CUDA graph, so that a step is one graph launch.
@@ -367,4 +376,7 @@ class Q4DecodePlan:
         torch.cuda.current_stream().synchronize()
         return out_pinned
 
-    launches_per_step = property(lambda self: 4 * len(self.layers) + 1)
+    @property
+    def launches_per_step(self):
+        """Kernels one replay launches (the library's own count)."""
+        return q4_decode_pass_launches(self.descs, self.H)

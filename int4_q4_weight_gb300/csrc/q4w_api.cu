@@ -127,6 +127,14 @@ static size_t up256(size_t n) { return (n + 255) & ~(size_t)255; }
 static size_t decode_tagged_bytes(size_t H, size_t QKV, size_t I) {
   return up256(QKV * 4) + up256(H * 8) + up256(I * 4) + up256(H * 8);
 }
+// One persistent cooperative launch when every stage fits the streaming
+// engine and every stage input fits its shared staging area (H <= 4096).
+static bool decode_persistent(const q4_layer* layers, int n_layers, int H) {
+  bool ok = stream_eligible(H) && H <= 4096 && n_layers <= 48;
+  for (int l = 0; l < n_layers && ok; ++l) ok = stream_eligible(layers[l].q_rows) && stream_eligible(layers[l].mlp_rows);
+  return ok;
+}
+
 static size_t decode_ws_bytes(size_t H, size_t QKV, size_t I) {
   return up256(QKV * 4) + decode_tagged_bytes(H, QKV, I) + up256(decode_ctl_bytes());
 }
@@ -250,6 +258,13 @@ int q4_rmsnorm_f16(const float* in, int H, float eps, uint16_t* out_f16, q4_stre
                             reinterpret_cast<cudaStream_t>(stream), false);
 }
 
+int q4_decode_pass_launches(const q4_layer* layers, int n_layers, int H) {
+  clear_error();
+  if (!layers) return -fail(Q4_ERR_NULL, "layers is NULL");
+  if (n_layers < 1 || n_layers > 256) return -fail(Q4_ERR_SHAPE, "n_layers=%d must be in [1, 256]", n_layers);
+  return decode_persistent(layers, n_layers, H) ? 1 : 4 * n_layers + 1;
+}
+
 int q4_decode_pass(const q4_layer* layers, int n_layers, int H, const uint16_t* h0_f16,
                    uint16_t* h_out_f16, float eps, void* ws, size_t ws_bytes, q4_stream_t stream) {
   clear_error();
@@ -305,12 +320,7 @@ int q4_decode_pass(const q4_layer* layers, int n_layers, int H, const uint16_t* 
   p += up256((size_t)H * 8);
   int* ctl = reinterpret_cast<int*>(p);
 
-  // One persistent cooperative launch when every stage fits the streaming
-  // engine and every stage input fits its shared staging area (H <= 4096).
-  bool persistent = stream_eligible(H) && H <= 4096 && n_layers <= 48;
-  for (int l = 0; l < n_layers && persistent; ++l)
-    persistent = stream_eligible(layers[l].q_rows) && stream_eligible(layers[l].mlp_rows);
-  if (persistent)
+  if (decode_persistent(layers, n_layers, H))
     return launch_decode_pass_stream(layers, n_layers, H, reinterpret_cast<const __half*>(h0_f16),
                                      reinterpret_cast<__half*>(h_out_f16), eps, kv32, tagged, tagged_bytes, ctl, dev,
                                      s);

@@ -97,6 +97,22 @@ def test_decode_pass_rejections(lib):
     assert lib.q4_decode_pass(ctypes.byref(layer), 1, 64, A, A, 1e-6, A, 16, None) == 4   # ws small
 
 
+def test_decode_pass_launch_count(lib):
+    """One persistent launch when H <= 4096, every K a multiple of 256 up to
+    12288 and at most 48 layers; otherwise one launch per stage plus the
+    closing RMSNorm."""
+    L = (q4w.q4_layer * 3)()
+    for l in L:
+        l.q_rows, l.kv_rows, l.mlp_rows = 2048, 256, 6144
+    assert lib.q4_decode_pass_launches(L, 3, 1536) == 1
+    assert lib.q4_decode_pass_launches(L, 3, 4352) == 13      # H above the staging limit
+    assert lib.q4_decode_pass_launches(L, 3, 1568) == 13      # H not a multiple of 256
+    L[1].mlp_rows = 16384                                      # K above 12288
+    assert lib.q4_decode_pass_launches(L, 3, 1536) == 13
+    assert lib.q4_decode_pass_launches(None, 3, 1536) == -1
+    assert lib.q4_decode_pass_launches(L, 0, 1536) == -2
+
+
 def test_valid_call_without_gpu_fails_loudly(lib):
     import torch
     if torch.cuda.is_available():
