@@ -10,18 +10,25 @@
 // (a 128-row tile and a range of 64-column K chunks; K is split across CTAs
 // when there are fewer tiles than SMs, the splits then add into Y).
 //
-// Warp roles (416 threads):
+// Warp roles (448 threads):
 //   warps 0-3   epilogue: tcgen05.ld of their TMEM lane quarter, store to Y
-//   warps 4-11  producers: codes + scales + x from global, nibble -> bf16
-//               (exact d*(q-8) in fp32, then round to nearest even), x fp16 ->
-//               bf16, written in the no-swizzle K-major core-matrix layout
+//   warps 4-11  converters: raw codes + x from the raw ring, scales from
+//               global, nibble -> bf16 (exact d*(q-8) in fp32, then round to
+//               nearest even), x fp16 -> bf16, written in the no-swizzle
+//               K-major core-matrix layout of the operand ring
 //   warp 12     TMEM allocator and the single thread that issues tcgen05.mma
-// A ring of kStages operand stages (A 16 KB + B 8 KB) is guarded by full /
-// empty mbarriers; two TMEM accumulators (2 x 64 columns) let the epilogue of
-// one item overlap the MMAs of the next.  Every mbarrier wait is bounded in
+//   warp 13     one thread issuing the TMA tile loads of the raw ring
+// The raw ring (kRawStages x (codes 4 KB + x 8 KB), 2-D tensor-map loads)
+// keeps several chunks of weight bytes in flight per SM; the operand ring
+// (kStages x (A 16 KB + B 8 KB)) feeds the tensor cores.  Both are guarded by
+// full / empty mbarriers; two TMEM accumulators (2 x 64 columns) let the
+// epilogue of one item overlap the MMAs of the next.  Every mbarrier wait is bounded in
 // clock cycles; on expiry the CTA raises an abort flag, every role leaves its
 // loop, the MMA thread drains its own tcgen05 work (bounded again), TMEM is
 // freed and the kernel returns with the device error word set.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "q4w_device.cuh"
 #include "q4w_internal.cuh"
 
@@ -46,18 +53,24 @@ unsigned* device_error_word() {
 namespace gemm {
 
 constexpr int kStages = 4;
+constexpr int kRawStages = 6;
 constexpr int kTileM = 128;            // weight rows per tile (MMA M)
 constexpr int kTok = 64;               // tokens (MMA N)
 constexpr int kChunk = 64;             // K columns per operand stage
 constexpr int kABytes = kTileM * kChunk * 2;   // 16 KB bf16
 constexpr int kBBytes = kTok * kChunk * 2;     // 8 KB bf16
 constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kRawCodeBytes = kTileM * kChunk / 2;   // 4 KB: [128 rows][32 B]
+constexpr int kRawXBytes = kTok * kChunk * 2;        // 8 KB: [64 tokens][64 fp16]
+constexpr int kRawBytes = kRawCodeBytes + kRawXBytes;
 constexpr int kEpiWarps = 4, kProdWarps = 8;
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 12
-constexpr int kThreadsG = (kMmaWarp + 1) * 32;      // 416
+constexpr int kTmaWarp = kMmaWarp + 1;             // 13
+constexpr int kThreadsG = (kTmaWarp + 1) * 32;     // 448
 constexpr int kTmemCols = 128;
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+constexpr int kBars = 2 * kStages + 2 * kRawStages + 5;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)kRawStages * kRawBytes + kBars * 8;
 constexpr long long kDrainCycles = 2000000000LL;
 
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M=128, N=64.
@@ -168,14 +181,27 @@ __device__ __forceinline__ uint32_t h2_to_bf16x2(uint32_t h2) {
 }
 
 struct Params {
-  const uint8_t* codes;
+  CUtensorMap tm_codes;   // codes [N][K/2] u8, box [128 rows][32 B]
+  CUtensorMap tm_x;       // X [64][K] fp16 (as u16), box [64 tokens][64 columns]
   const __half* scales;
-  const __half* X;
   float* Y;
   int N, K;
   int tiles, splits, cps, nchunks, items;
   long long wait_limit;
 };
+
+// 2-D tensor-map tile load into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t mbar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(mbar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ void item_range(const Params& p, int item, int& tile, int& c0, int& c1) {
   tile = item / p.splits;
@@ -184,18 +210,24 @@ __device__ __forceinline__ void item_range(const Params& p, int item, int& tile,
   c1 = min(c0 + p.cps, p.nchunks);
 }
 
-struct ProdRegs {
-  uint4 code;
-  float d;
-  uint4 x0, x1;
-};
+// Next (item, chunk) of this CTA's sequence after (item, c); false at the end.
+__device__ __forceinline__ bool next_chunk(const Params& p, int& item, int& tile, int& c0, int& c1, int& c) {
+  if (++c < c1) return true;
+  item += gridDim.x;
+  if (item >= p.items) return false;
+  item_range(p, item, tile, c0, c1);
+  c = c0;
+  return true;
+}
 
-__global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* stage_base = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStageBytes);
-  // bars: full[kStages], empty[kStages], accfull[2], accempty[2], drain
+  uint8_t* raw_base = smem + (size_t)kStages * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw_base + (size_t)kRawStages * kRawBytes);
+  // bars: full[kStages], empty[kStages], accfull[2], accempty[2], drain,
+  //       rawfull[kRawStages], rawempty[kRawStages]
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -203,6 +235,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const Params p) {
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
   const uint32_t accfull0 = smem_u32(bars + 2 * kStages), accempty0 = smem_u32(bars + 2 * kStages + 2);
   const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
+  const uint32_t rawfull0 = smem_u32(bars + 2 * kStages + 5), rawempty0 = rawfull0 + 8 * kRawStages;
   volatile int* abort_flag = &abort_sh;
 
   if (threadIdx.x == 0) {
@@ -216,6 +249,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const Params p) {
       mbar_init(accempty0 + 8 * a, kEpiWarps * 32);
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(rawfull0 + 8 * s, 1);
+      mbar_init(rawempty0 + 8 * s, kProdWarps);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {
@@ -228,73 +265,94 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const Params p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const int K2 = p.K >> 1, K32 = p.K >> 5;
+  const int K32 = p.K >> 5;
 
-  if (warp >= kEpiWarps && warp < kMmaWarp) {
-    // ------------------------------------------------------------ producers
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------- raw tile loads
+    if (lane == 0 && blockIdx.x < p.items) {
+      uint64_t pol_stream, pol_keep;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_stream));
+      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
+      const uint32_t raw0 = smem_u32(raw_base);
+      int item = blockIdx.x, tile, c0, c1, c;
+      item_range(p, item, tile, c0, c1);
+      c = c0;
+      uint32_t g = 0;
+      do {
+        const uint32_t s = g % kRawStages, round = g / kRawStages;
+        if (!mbar_wait(rawempty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag)) break;
+        const uint32_t dst = raw0 + s * kRawBytes;
+        mbar_expect_tx(rawfull0 + 8 * s, kRawBytes);
+        tma_load_2d(dst, &p.tm_codes, c * (kChunk / 2), tile * kTileM, rawfull0 + 8 * s, pol_stream);
+        tma_load_2d(dst + kRawCodeBytes, &p.tm_x, c * kChunk, 0, rawfull0 + 8 * s, pol_keep);
+        ++g;
+      } while (next_chunk(p, item, tile, c0, c1, c));
+      // every issued load lands before the CTA may exit
+      const uint32_t first = g > (uint32_t)kRawStages ? g - kRawStages : 0u;
+      for (uint32_t q = first; q < g; ++q) {
+        const long long t0 = clock64();
+        while (!mbar_test(rawfull0 + 8 * (q % kRawStages), (q / kRawStages) & 1)) {
+          if (clock64() - t0 > kDrainCycles) {
+            atomicOr(&g_device_error, 1u);
+            break;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= kEpiWarps && warp < kMmaWarp) {
+    // ----------------------------------------------------------- converters
     const int pt = threadIdx.x - kEpiWarps * 32;
     const int r = pt >> 1, h = pt & 1;        // A: row of the tile, 32-block in the chunk
     const int t = pt >> 2, q = pt & 3;        // B: token, 16-column quarter of the chunk
     const uint32_t a_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 16);
     const uint32_t b_off = (uint32_t)((t >> 3) * 1024 + (t & 7) * 16);
-    uint32_t g = 0;                           // global chunk counter (ring position)
-    bool have = false;
-    ProdRegs cur;
-    int item = blockIdx.x, tile = 0, c0 = 0, c1 = 0, c = 0;
-    auto fetch = [&](int tl, int ch, ProdRegs& R) {
-      const size_t row = (size_t)tl * kTileM + r;
-      R.code = ld_stream16(p.codes + row * K2 + (size_t)(ch * 2 + h) * 16);
-      R.d = ld_scale(p.scales + row * K32 + ch * 2 + h);
-      const uint4* xp = reinterpret_cast<const uint4*>(p.X + (size_t)t * p.K + ch * kChunk + q * 16);
-      R.x0 = __ldg(xp);
-      R.x1 = __ldg(xp + 1);
-    };
-    if (item < p.items) {
+    if (blockIdx.x < p.items) {
+      int item = blockIdx.x, tile, c0, c1, c;
       item_range(p, item, tile, c0, c1);
       c = c0;
-      fetch(tile, c, cur);
-      have = true;
-    }
-    while (have) {
-      // next (item, chunk) in this CTA's sequence
-      int ntile = tile, nc0 = c0, nc1 = c1, nc = c + 1, nitem = item;
-      if (nc >= c1) {
-        nitem = item + gridDim.x;
-        if (nitem < p.items) {
-          item_range(p, nitem, ntile, nc0, nc1);
-          nc = nc0;
-        }
-      }
-      const bool more = nitem < p.items;
-      ProdRegs nxt;
-      if (more) fetch(ntile, nc, nxt);
+      float d = ld_scale(p.scales + ((size_t)tile * kTileM + r) * K32 + c * 2 + h);
+      uint32_t g = 0;
+      bool more;
+      do {
+        // the next chunk's scale is requested before this chunk is converted
+        int ni = item, nt = tile, n0 = c0, n1 = c1, nc = c;
+        more = next_chunk(p, ni, nt, n0, n1, nc);
+        const float dn = more ? ld_scale(p.scales + ((size_t)nt * kTileM + r) * K32 + nc * 2 + h) : 0.f;
 
-      const uint32_t s = g % kStages, round = g / kStages;
-      if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag)) break;
-      uint8_t* A = stage_base + (size_t)s * kStageBytes;
-      uint8_t* B = A + kABytes;
-      const f2_t dd = f2_pack(cur.d, cur.d);
-      const f2_t bias = f2_pack(-264.f * cur.d, -24.f * cur.d);
-      const uint32_t w4[4] = {cur.code.x, cur.code.y, cur.code.z, cur.code.w};
+        const uint32_t rs = g % kRawStages, rround = g / kRawStages;
+        if (!mbar_wait(rawfull0 + 8 * rs, rround & 1, p.wait_limit, abort_flag)) break;
+        const uint8_t* raw = raw_base + (size_t)rs * kRawBytes;
+        const uint4 code = *reinterpret_cast<const uint4*>(raw + r * 32 + h * 16);
+        const uint4 x0 = *reinterpret_cast<const uint4*>(raw + kRawCodeBytes + t * 128 + q * 32);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(raw + kRawCodeBytes + t * 128 + q * 32 + 16);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rawempty0 + 8 * rs);
+
+        const uint32_t s = g % kStages, round = g / kStages;
+        if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag)) break;
+        uint8_t* A = stage_base + (size_t)s * kStageBytes;
+        uint8_t* B = A + kABytes;
+        const f2_t dd = f2_pack(d, d);
+        const f2_t bias = f2_pack(-264.f * d, -24.f * d);
+        const uint32_t w4[4] = {code.x, code.y, code.z, code.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(A + a_off + (h * 4 + j) * 128) = dequant_word(w4[j], dd, bias);
-      const uint4 b0 = make_uint4(h2_to_bf16x2(cur.x0.x), h2_to_bf16x2(cur.x0.y), h2_to_bf16x2(cur.x0.z),
-                                  h2_to_bf16x2(cur.x0.w));
-      const uint4 b1 = make_uint4(h2_to_bf16x2(cur.x1.x), h2_to_bf16x2(cur.x1.y), h2_to_bf16x2(cur.x1.z),
-                                  h2_to_bf16x2(cur.x1.w));
-      *reinterpret_cast<uint4*>(B + b_off + (2 * q) * 128) = b0;
-      *reinterpret_cast<uint4*>(B + b_off + (2 * q + 1) * 128) = b1;
-      fence_proxy_async();
-      mbar_arrive(full0 + 8 * s);
-      ++g;
-      if (!more) break;
-      item = nitem;
-      tile = ntile;
-      c0 = nc0;
-      c1 = nc1;
-      c = nc;
-      cur = nxt;
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(A + a_off + (h * 4 + j) * 128) = dequant_word(w4[j], dd, bias);
+        const uint4 b0 = make_uint4(h2_to_bf16x2(x0.x), h2_to_bf16x2(x0.y), h2_to_bf16x2(x0.z), h2_to_bf16x2(x0.w));
+        const uint4 b1 = make_uint4(h2_to_bf16x2(x1.x), h2_to_bf16x2(x1.y), h2_to_bf16x2(x1.z), h2_to_bf16x2(x1.w));
+        *reinterpret_cast<uint4*>(B + b_off + (2 * q) * 128) = b0;
+        *reinterpret_cast<uint4*>(B + b_off + (2 * q + 1) * 128) = b1;
+        fence_proxy_async();
+        mbar_arrive(full0 + 8 * s);
+        ++g;
+        item = ni;
+        tile = nt;
+        c0 = n0;
+        c1 = n1;
+        c = nc;
+        d = dn;
+      } while (more);
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------- MMA issuer
@@ -382,13 +440,49 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const Params p) {
 
 }  // namespace gemm
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (the library does not link the driver library itself).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D row-major tensor [rows][cols] of 1- or 2-byte elements, one box per load.
+static int encode_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type, int esize, uint64_t cols,
+                     uint64_t rows, uint32_t box_cols, uint32_t box_rows, const char* what) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * (uint64_t)esize};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(tm, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(Q4_ERR_CUDA, "tensor map for %s: driver error %d", what, (int)r);
+  return Q4_OK;
+}
+
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, const DeviceInfo& dev, cudaStream_t s) {
   (void)M;
   gemm::Params p;
-  p.codes = codes;
+  memset(&p, 0, sizeof(p));
+  int st = encode_2d(&p.tm_codes, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N,
+                     gemm::kChunk / 2, gemm::kTileM, "codes");
+  if (st != Q4_OK) return st;
+  st = encode_2d(&p.tm_x, X, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)K, gemm::kTok, gemm::kChunk, gemm::kTok,
+                 "X");
+  if (st != Q4_OK) return st;
   p.scales = scales;
-  p.X = X;
   p.Y = Y;
   p.N = N;
   p.K = K;
