@@ -18,7 +18,8 @@
 //               K-major core-matrix layout of the operand ring
 //   warp 12     TMEM allocator and the single thread that issues tcgen05.mma
 //   warp 13     one thread issuing the TMA tile loads of the raw ring
-// The raw ring (kRawStages x (codes 4 KB + x 8 KB), 2-D tensor-map loads)
+// The raw ring (kRawStages x (codes 4 KB + x 8 KB + scales 2 KB), 2-D
+// tensor-map loads)
 // keeps several chunks of weight bytes in flight per SM; the operand ring
 // (kStages x (A 16 KB + B 8 KB)) feeds the tensor cores.  Both are guarded by
 // full / empty mbarriers; two TMEM accumulators (2 x 64 columns) let the
@@ -62,7 +63,9 @@ constexpr int kBBytes = kTok * kChunk * 2;     // 8 KB bf16
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kRawCodeBytes = kTileM * kChunk / 2;   // 4 KB: [128 rows][32 B]
 constexpr int kRawXBytes = kTok * kChunk * 2;        // 8 KB: [64 tokens][64 fp16]
-constexpr int kRawBytes = kRawCodeBytes + kRawXBytes;
+constexpr int kRawScaleBytes = kTileM * 16;         // 2 KB: [128 rows][8 fp16] (the 8-scale group
+                                                     // holding the chunk's two scales)
+constexpr int kRawBytes = kRawCodeBytes + kRawXBytes + kRawScaleBytes;
 constexpr int kEpiWarps = 4, kProdWarps = 8;
 constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 12
@@ -183,7 +186,9 @@ __device__ __forceinline__ uint32_t h2_to_bf16x2(uint32_t h2) {
 struct Params {
   CUtensorMap tm_codes;   // codes [N][K/2] u8, box [128 rows][32 B]
   CUtensorMap tm_x;       // X [64][K] fp16 (as u16), box [64 tokens][64 columns]
-  const __half* scales;
+  CUtensorMap tm_sc;      // scales [N][K/32] fp16 (as u16), box [128 rows][8 scales]; K % 256 == 0
+  const __half* scales;   // read directly when K % 256 != 0 (row stride not a multiple of 16 B)
+  int sc_tma;
   float* Y;
   int N, K;
   int tiles, splits, cps, nchunks, items;
@@ -265,8 +270,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const int K32 = p.K >> 5;
-
   if (warp == kTmaWarp) {
     // ------------------------------------------------------- raw tile loads
     if (lane == 0 && blockIdx.x < p.items) {
@@ -282,9 +285,12 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         const uint32_t s = g % kRawStages, round = g / kRawStages;
         if (!mbar_wait(rawempty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag)) break;
         const uint32_t dst = raw0 + s * kRawBytes;
-        mbar_expect_tx(rawfull0 + 8 * s, kRawBytes);
+        mbar_expect_tx(rawfull0 + 8 * s, p.sc_tma ? kRawBytes : kRawBytes - kRawScaleBytes);
         tma_load_2d(dst, &p.tm_codes, c * (kChunk / 2), tile * kTileM, rawfull0 + 8 * s, pol_stream);
         tma_load_2d(dst + kRawCodeBytes, &p.tm_x, c * kChunk, 0, rawfull0 + 8 * s, pol_keep);
+        if (p.sc_tma)
+          tma_load_2d(dst + kRawCodeBytes + kRawXBytes, &p.tm_sc, (c * 2) & ~7, tile * kTileM, rawfull0 + 8 * s,
+                      pol_stream);
         ++g;
       } while (next_chunk(p, item, tile, c0, c1, c));
       // every issued load lands before the CTA may exit
@@ -311,14 +317,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       int item = blockIdx.x, tile, c0, c1, c;
       item_range(p, item, tile, c0, c1);
       c = c0;
-      float d = ld_scale(p.scales + ((size_t)tile * kTileM + r) * K32 + c * 2 + h);
       uint32_t g = 0;
       bool more;
       do {
-        // the next chunk's scale is requested before this chunk is converted
         int ni = item, nt = tile, n0 = c0, n1 = c1, nc = c;
         more = next_chunk(p, ni, nt, n0, n1, nc);
-        const float dn = more ? ld_scale(p.scales + ((size_t)nt * kTileM + r) * K32 + nc * 2 + h) : 0.f;
 
         const uint32_t rs = g % kRawStages, rround = g / kRawStages;
         if (!mbar_wait(rawfull0 + 8 * rs, rround & 1, p.wait_limit, abort_flag)) break;
@@ -326,6 +329,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         const uint4 code = *reinterpret_cast<const uint4*>(raw + r * 32 + h * 16);
         const uint4 x0 = *reinterpret_cast<const uint4*>(raw + kRawCodeBytes + t * 128 + q * 32);
         const uint4 x1 = *reinterpret_cast<const uint4*>(raw + kRawCodeBytes + t * 128 + q * 32 + 16);
+        const float d =
+            p.sc_tma ? __half2float(*reinterpret_cast<const __half*>(raw + kRawCodeBytes + kRawXBytes + r * 16 +
+                                                                      ((c * 2 + h) & 7) * 2))
+                     : ld_scale(p.scales + ((size_t)tile * kTileM + r) * (p.K >> 5) + c * 2 + h);
         __syncwarp();
         if (lane == 0) mbar_arrive(rawempty0 + 8 * rs);
 
@@ -351,7 +358,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         c0 = n0;
         c1 = n1;
         c = nc;
-        d = dn;
       } while (more);
     }
   } else if (warp == kMmaWarp) {
@@ -483,6 +489,12 @@ int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* 
                  "X");
   if (st != Q4_OK) return st;
   p.scales = scales;
+  p.sc_tma = K % 256 == 0;
+  if (p.sc_tma) {
+    st = encode_2d(&p.tm_sc, scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)K / 32, (uint64_t)N, 8,
+                   gemm::kTileM, "scales");
+    if (st != Q4_OK) return st;
+  }
   p.Y = Y;
   p.N = N;
   p.K = K;
