@@ -112,7 +112,10 @@ int q4_gemv(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16,
  * chunks only; the remainder goes through main).
  *   X_f16: [M][K] with M == 64; Y: f32 [M][N]; codes/scales [N][K].
  *   N % 128 == 0, K % 64 == 0, 64 <= K <= 32768.
- *   ws/ws_bytes: unused (may be NULL/0).                                   */
+ *   ws: q4_workspace_bytes(Q4_OP_GEMM_CHUNK, N, K, 64) bytes (64 * K * 2,
+ *   rounded up to 256), 16-byte aligned; it receives X rounded to bf16
+ *   (by a conversion kernel launched on `stream` before the GEMM) and must
+ *   not be shared by overlapping calls.  NULL or smaller: Q4_ERR_WORKSPACE. */
 int q4_gemm_chunk(const uint8_t* codes, const uint16_t* scales, const uint16_t* X_f16,
                   float* Y, int M, int N, int K, void* ws, size_t ws_bytes,
                   q4_stream_t stream);

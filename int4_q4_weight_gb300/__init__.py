@@ -318,7 +318,9 @@ def q4_gemm_chunk(codes, scales, X, Y=None):
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
     _dev(Y, torch.float32, "Y")
-    _check(lib.q4_gemm_chunk(_ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, N, K, None, 0,
+    nws = lib.q4_workspace_bytes(Q4_OP_GEMM_CHUNK, N, K, M)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=X.device)
+    _check(lib.q4_gemm_chunk(_ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, N, K, _ptr(ws), nws,
                              _stream()), "q4_gemm_chunk")
     return Y
 

@@ -10,20 +10,23 @@
 // (a 128-row tile and a range of 64-column K chunks; K is split across CTAs
 // when there are fewer tiles than SMs, the splits then add into Y).
 //
-// Warp roles (448 threads):
+// Warp roles (480 threads):
 //   warps 0-3   epilogue: tcgen05.ld of their TMEM lane quarter, store to Y
-//   warps 4-11  converters: raw codes + x from the raw ring, scales from
-//               global, nibble -> bf16 (exact d*(q-8) in fp32, then round to
-//               nearest even), x fp16 -> bf16, written in the no-swizzle
-//               K-major core-matrix layout of the operand ring
+//   warps 4-11  converters: raw codes + scales from the raw ring, nibble ->
+//               bf16 (exact d*(q-8) in fp32, then round to nearest even),
+//               written in the no-swizzle K-major core-matrix layout (A)
 //   warp 12     TMEM allocator and the single thread that issues tcgen05.mma
-//   warp 13     one thread issuing the TMA tile loads of the raw ring
-// The raw ring (kRawStages x (codes 4 KB + x 8 KB + scales 2 KB), 2-D
-// tensor-map loads)
-// keeps several chunks of weight bytes in flight per SM; the operand ring
-// (kStages x (A 16 KB + B 8 KB)) feeds the tensor cores.  Both are guarded by
-// full / empty mbarriers; two TMEM accumulators (2 x 64 columns) let the
-// epilogue of one item overlap the MMAs of the next.  Every mbarrier wait is bounded in
+//   warp 13     one thread issuing the TMA loads of the raw ring
+//   warp 14     one thread loading the token tile (B) of each operand stage
+//               straight from the bf16 copy of X (a 3-D tensor map whose box
+//               lands in the core-matrix layout)
+// X is rounded to bf16 once per call by a small kernel ahead of the GEMM (in
+// the caller's workspace) instead of once per tile and chunk.  The raw ring
+// (kRawStages x 256 K columns: codes 16 KB + scales 2 KB) keeps weight bytes
+// in flight; the operand ring (kStages x (A 16 KB + B 8 KB)) feeds the tensor
+// cores.  Both are guarded by full / empty mbarriers; two TMEM accumulators
+// (2 x 64 columns) let the epilogue of one item overlap the MMAs of the next.
+// Every mbarrier wait is bounded in
 // clock cycles; on expiry the CTA raises an abort flag, every role leaves its
 // loop, the MMA thread drains its own tcgen05 work (bounded again), TMEM is
 // freed and the kernel returns with the device error word set.
@@ -54,25 +57,24 @@ unsigned* device_error_word() {
 namespace gemm {
 
 constexpr int kStages = 4;
-constexpr int kRawStages = 6;
+constexpr int kRawStages = 4;
+constexpr int kRawChunks = 4;          // operand chunks per raw stage (256 K columns)
 constexpr int kTileM = 128;            // weight rows per tile (MMA M)
 constexpr int kTok = 64;               // tokens (MMA N)
 constexpr int kChunk = 64;             // K columns per operand stage
 constexpr int kABytes = kTileM * kChunk * 2;   // 16 KB bf16
 constexpr int kBBytes = kTok * kChunk * 2;     // 8 KB bf16
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kRawCodeBytes = kTileM * kChunk / 2;   // 4 KB: [128 rows][32 B]
-constexpr int kRawXBytes = kTok * kChunk * 2;        // 8 KB: [64 tokens][64 fp16]
-constexpr int kRawScaleBytes = kTileM * 16;         // 2 KB: [128 rows][8 fp16] (the 8-scale group
-                                                     // holding the chunk's two scales)
-constexpr int kRawBytes = kRawCodeBytes + kRawXBytes + kRawScaleBytes;
+constexpr int kRawCodeBytes = kTileM * kChunk * kRawChunks / 2;   // 16 KB: [128 rows][128 B]
+constexpr int kRawScaleBytes = kTileM * 16;                         // 2 KB: [128 rows][8 fp16]
+constexpr int kRawBytes = kRawCodeBytes + kRawScaleBytes;
 constexpr int kEpiWarps = 4, kProdWarps = 8;
-constexpr int kProdThreads = kProdWarps * 32;
 constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 12
 constexpr int kTmaWarp = kMmaWarp + 1;             // 13
-constexpr int kThreadsG = (kTmaWarp + 1) * 32;     // 448
+constexpr int kBWarp = kTmaWarp + 1;               // 14
+constexpr int kThreadsG = (kBWarp + 1) * 32;       // 480
 constexpr int kTmemCols = 128;
-constexpr int kBars = 2 * kStages + 2 * kRawStages + 5;
+constexpr int kBars = 3 * kStages + 2 * kRawStages + 5;
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)kRawStages * kRawBytes + kBars * 8;
 constexpr long long kDrainCycles = 2000000000LL;
 
@@ -108,10 +110,13 @@ __device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
 }
 
 // Bounded wait.  Returns false when the wait ran out or the CTA is aborting.
+// sleep_ns > 0: roles off the critical path back off between polls, so that
+// their spinning does not take issue slots from the converter warps.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, long long limit,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag, unsigned sleep_ns = 0) {
   const long long t0 = clock64();
   while (!mbar_test(a, parity)) {
+    if (sleep_ns) __nanosleep(sleep_ns);
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       *abort_flag = 1;
@@ -184,8 +189,8 @@ __device__ __forceinline__ uint32_t h2_to_bf16x2(uint32_t h2) {
 }
 
 struct Params {
-  CUtensorMap tm_codes;   // codes [N][K/2] u8, box [128 rows][32 B]
-  CUtensorMap tm_x;       // X [64][K] fp16 (as u16), box [64 tokens][64 columns]
+  CUtensorMap tm_codes;   // codes [N][K/2] u8, box [128 rows][128 B]
+  const uint8_t* xb;      // bf16 X as [K/8 column groups][64 tokens][8]: chunk c = bytes [8 KB c, 8 KB (c+1))
   CUtensorMap tm_sc;      // scales [N][K/32] fp16 (as u16), box [128 rows][8 scales]; K % 256 == 0
   const __half* scales;   // read directly when K % 256 != 0 (row stride not a multiple of 16 B)
   int sc_tma;
@@ -193,7 +198,10 @@ struct Params {
   int N, K;
   int tiles, splits, cps, nchunks, items;
   long long wait_limit;
+  unsigned long long* trace;   // optional: CTA 0 stamps [chunk < kTraceChunks][8], SM cycles
 };
+
+constexpr int kTraceChunks = 256;
 
 // 2-D tensor-map tile load into shared memory, completing on an mbarrier.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t mbar,
@@ -202,6 +210,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(mbar), "l"(policy)
+      : "memory");
+}
+// Contiguous bulk copy global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(mbar), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
@@ -215,16 +232,6 @@ __device__ __forceinline__ void item_range(const Params& p, int item, int& tile,
   c1 = min(c0 + p.cps, p.nchunks);
 }
 
-// Next (item, chunk) of this CTA's sequence after (item, c); false at the end.
-__device__ __forceinline__ bool next_chunk(const Params& p, int& item, int& tile, int& c0, int& c1, int& c) {
-  if (++c < c1) return true;
-  item += gridDim.x;
-  if (item >= p.items) return false;
-  item_range(p, item, tile, c0, c1);
-  c = c0;
-  return true;
-}
-
 __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -232,26 +239,34 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   uint8_t* raw_base = smem + (size_t)kStages * kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(raw_base + (size_t)kRawStages * kRawBytes);
   // bars: full[kStages], empty[kStages], accfull[2], accempty[2], drain,
-  //       rawfull[kRawStages], rawempty[kRawStages]
+  //       rawfull[kRawStages], rawempty[kRawStages], bfull[kStages]
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ long long t0_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned long long* const tr = (p.trace && blockIdx.x == 0) ? p.trace : nullptr;
+  auto stamp = [&](uint32_t chunk, int k) {
+    if (tr && chunk < (uint32_t)kTraceChunks) tr[chunk * 8 + k] = (unsigned long long)(clock64() - t0_sh);
+  };
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
   const uint32_t accfull0 = smem_u32(bars + 2 * kStages), accempty0 = smem_u32(bars + 2 * kStages + 2);
   const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
   const uint32_t rawfull0 = smem_u32(bars + 2 * kStages + 5), rawempty0 = rawfull0 + 8 * kRawStages;
+  const uint32_t bfull0 = rawempty0 + 8 * kRawStages;
   volatile int* abort_flag = &abort_sh;
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
+    t0_sh = clock64();
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, kProdThreads);
+      mbar_init(full0 + 8 * s, kProdWarps);   // one arrival per converter warp
+      mbar_init(bfull0 + 8 * s, 1);           // the B loader's arrival with its bytes
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accfull0 + 8 * a, 1);
-      mbar_init(accempty0 + 8 * a, kEpiWarps * 32);
+      mbar_init(accempty0 + 8 * a, kEpiWarps);
     }
     mbar_init(drain, 1);
     for (int s = 0; s < kRawStages; ++s) {
@@ -273,26 +288,29 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   if (warp == kTmaWarp) {
     // ------------------------------------------------------- raw tile loads
     if (lane == 0 && blockIdx.x < p.items) {
-      uint64_t pol_stream, pol_keep;
+      uint64_t pol_stream;
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_stream));
-      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
       const uint32_t raw0 = smem_u32(raw_base);
-      int item = blockIdx.x, tile, c0, c1, c;
-      item_range(p, item, tile, c0, c1);
-      c = c0;
-      uint32_t g = 0;
-      do {
-        const uint32_t s = g % kRawStages, round = g / kRawStages;
-        if (!mbar_wait(rawempty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag)) break;
-        const uint32_t dst = raw0 + s * kRawBytes;
-        mbar_expect_tx(rawfull0 + 8 * s, p.sc_tma ? kRawBytes : kRawBytes - kRawScaleBytes);
-        tma_load_2d(dst, &p.tm_codes, c * (kChunk / 2), tile * kTileM, rawfull0 + 8 * s, pol_stream);
-        tma_load_2d(dst + kRawCodeBytes, &p.tm_x, c * kChunk, 0, rawfull0 + 8 * s, pol_keep);
-        if (p.sc_tma)
-          tma_load_2d(dst + kRawCodeBytes + kRawXBytes, &p.tm_sc, (c * 2) & ~7, tile * kTileM, rawfull0 + 8 * s,
-                      pol_stream);
-        ++g;
-      } while (next_chunk(p, item, tile, c0, c1, c));
+      uint32_t g = 0, gc = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
+        int tile, c0, c1;
+        item_range(p, item, tile, c0, c1);
+        for (int cs = c0; cs < c1; cs += kRawChunks, ++g) {
+          const uint32_t s = g % kRawStages, round = g / kRawStages;
+          if (!mbar_wait(rawempty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, 64)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = raw0 + s * kRawBytes;
+          stamp(gc, 0);
+          gc += min(cs + kRawChunks, c1) - cs;
+          mbar_expect_tx(rawfull0 + 8 * s, p.sc_tma ? kRawBytes : kRawCodeBytes);
+          tma_load_2d(dst, &p.tm_codes, cs * (kChunk / 2), tile * kTileM, rawfull0 + 8 * s, pol_stream);
+          if (p.sc_tma)   // cs % kRawChunks == 0 here: the x coordinate is 16-byte aligned
+            tma_load_2d(dst + kRawCodeBytes, &p.tm_sc, cs * 2, tile * kTileM, rawfull0 + 8 * s, pol_stream);
+        }
+      }
       // every issued load lands before the CTA may exit
       const uint32_t first = g > (uint32_t)kRawStages ? g - kRawStages : 0u;
       for (uint32_t q = first; q < g; ++q) {
@@ -306,59 +324,93 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       }
     }
     __syncwarp();
+  } else if (warp == kBWarp) {
+    // ------------------------------------------- token tiles (B operand)
+    if (lane == 0) {
+      uint64_t pol_keep;
+      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
+      pdl_wait();   // the bf16 copy of X is written by the kernel launched just before
+      const uint32_t stage0 = smem_u32(stage_base);
+      uint32_t g = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
+        int tile, c0, c1;
+        item_range(p, item, tile, c0, c1);
+        for (int c = c0; c < c1; ++c, ++g) {
+          const uint32_t s = g % kStages, round = g / kStages;
+          if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, 64)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bfull0 + 8 * s, kBBytes);
+          // [8 column groups][64 tokens][8]: core matrices 128 B apart along the
+          // tokens, 1024 B apart along K
+          bulk_load(stage0 + s * kStageBytes + kABytes, p.xb + (size_t)c * kBBytes, kBBytes, bfull0 + 8 * s,
+                    pol_keep);
+        }
+      }
+      // every issued load lands before the CTA may exit
+      const uint32_t first = g > (uint32_t)kStages ? g - kStages : 0u;
+      for (uint32_t q = first; q < g; ++q) {
+        const long long t0 = clock64();
+        while (!mbar_test(bfull0 + 8 * (q % kStages), (q / kStages) & 1)) {
+          if (clock64() - t0 > kDrainCycles) {
+            atomicOr(&g_device_error, 1u);
+            break;
+          }
+        }
+      }
+    }
+    __syncwarp();
   } else if (warp >= kEpiWarps && warp < kMmaWarp) {
     // ----------------------------------------------------------- converters
     const int pt = threadIdx.x - kEpiWarps * 32;
     const int r = pt >> 1, h = pt & 1;        // A: row of the tile, 32-block in the chunk
-    const int t = pt >> 2, q = pt & 3;        // B: token, 16-column quarter of the chunk
     const uint32_t a_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 16);
-    const uint32_t b_off = (uint32_t)((t >> 3) * 1024 + (t & 7) * 16);
-    if (blockIdx.x < p.items) {
-      int item = blockIdx.x, tile, c0, c1, c;
+    uint32_t g = 0, gr = 0;   // operand chunks, raw stages
+    bool ok = true;
+    for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
+      int tile, c0, c1;
       item_range(p, item, tile, c0, c1);
-      c = c0;
-      uint32_t g = 0;
-      bool more;
-      do {
-        int ni = item, nt = tile, n0 = c0, n1 = c1, nc = c;
-        more = next_chunk(p, ni, nt, n0, n1, nc);
-
-        const uint32_t rs = g % kRawStages, rround = g / kRawStages;
-        if (!mbar_wait(rawfull0 + 8 * rs, rround & 1, p.wait_limit, abort_flag)) break;
+      for (int cs = c0; cs < c1 && ok; cs += kRawChunks, ++gr) {
+        const uint32_t rs = gr % kRawStages, rround = gr / kRawStages;
+        if (!mbar_wait(rawfull0 + 8 * rs, rround & 1, p.wait_limit, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (pt == 0) stamp(g, 1);
         const uint8_t* raw = raw_base + (size_t)rs * kRawBytes;
-        const uint4 code = *reinterpret_cast<const uint4*>(raw + r * 32 + h * 16);
-        const uint4 x0 = *reinterpret_cast<const uint4*>(raw + kRawCodeBytes + t * 128 + q * 32);
-        const uint4 x1 = *reinterpret_cast<const uint4*>(raw + kRawCodeBytes + t * 128 + q * 32 + 16);
-        const float d =
-            p.sc_tma ? __half2float(*reinterpret_cast<const __half*>(raw + kRawCodeBytes + kRawXBytes + r * 16 +
-                                                                      ((c * 2 + h) & 7) * 2))
-                     : ld_scale(p.scales + ((size_t)tile * kTileM + r) * (p.K >> 5) + c * 2 + h);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(rawempty0 + 8 * rs);
-
-        const uint32_t s = g % kStages, round = g / kStages;
-        if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag)) break;
-        uint8_t* A = stage_base + (size_t)s * kStageBytes;
-        uint8_t* B = A + kABytes;
-        const f2_t dd = f2_pack(d, d);
-        const f2_t bias = f2_pack(-264.f * d, -24.f * d);
-        const uint32_t w4[4] = {code.x, code.y, code.z, code.w};
+        const int ce = min(cs + kRawChunks, c1);
+        for (int c = cs; c < ce; ++c, ++g) {
+          const int cc = c - cs;
+          const uint4 code = *reinterpret_cast<const uint4*>(raw + r * 128 + cc * 32 + h * 16);
+          const float d =
+              p.sc_tma ? __half2float(*reinterpret_cast<const __half*>(raw + kRawCodeBytes + r * 16 +
+                                                                        (cc * 2 + h) * 2))
+                       : ld_scale(p.scales + ((size_t)tile * kTileM + r) * (p.K >> 5) + c * 2 + h);
+          if (c == ce - 1) {   // the raw stage has been read
+            __syncwarp();
+            if (lane == 0) mbar_arrive(rawempty0 + 8 * rs);
+          }
+          const uint32_t s = g % kStages, round = g / kStages;
+          if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (pt == 0) stamp(g, 2);
+          uint8_t* A = stage_base + (size_t)s * kStageBytes;
+          const f2_t dd = f2_pack(d, d);
+          const f2_t bias = f2_pack(-264.f * d, -24.f * d);
+          const uint32_t w4[4] = {code.x, code.y, code.z, code.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(A + a_off + (h * 4 + j) * 128) = dequant_word(w4[j], dd, bias);
-        const uint4 b0 = make_uint4(h2_to_bf16x2(x0.x), h2_to_bf16x2(x0.y), h2_to_bf16x2(x0.z), h2_to_bf16x2(x0.w));
-        const uint4 b1 = make_uint4(h2_to_bf16x2(x1.x), h2_to_bf16x2(x1.y), h2_to_bf16x2(x1.z), h2_to_bf16x2(x1.w));
-        *reinterpret_cast<uint4*>(B + b_off + (2 * q) * 128) = b0;
-        *reinterpret_cast<uint4*>(B + b_off + (2 * q + 1) * 128) = b1;
-        fence_proxy_async();
-        mbar_arrive(full0 + 8 * s);
-        ++g;
-        item = ni;
-        tile = nt;
-        c0 = n0;
-        c1 = n1;
-        c = nc;
-      } while (more);
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(A + a_off + (h * 4 + j) * 128) = dequant_word(w4[j], dd, bias);
+          fence_proxy_async();   // this thread's stores, before the tensor core reads them
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full0 + 8 * s);
+          if (pt == 0) stamp(g, 3);
+        }
+      }
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------- MMA issuer
@@ -379,19 +431,22 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         const uint32_t d_tmem = tmem + (uint32_t)(a * kTok);
         for (int c = c0; c < c1; ++c, ++g) {
           const uint32_t s = g % kStages, round = g / kStages;
-          if (!mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag)) {
+          if (!mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag) ||
+              !mbar_wait(bfull0 + 8 * s, round & 1, p.wait_limit, abort_flag)) {
             ok = false;
             break;
           }
+          stamp(g, 4);
           tc_fence_after();
           const uint32_t A = stage0 + s * kStageBytes, B = A + kABytes;
 #pragma unroll
           for (int ks = 0; ks < kChunk / 16; ++ks) {
             const uint64_t ad = smem_desc(A + ks * 256, 128, 1024);
-            const uint64_t bd = smem_desc(B + ks * 256, 128, 1024);
+            const uint64_t bd = smem_desc(B + ks * 2048, 1024, 128);
             tc_mma(d_tmem, ad, bd, (c > c0 || ks > 0) ? 1u : 0u);
           }
           tc_commit(empty0 + 8 * s);
+          stamp(g, 5);
         }
         if (!ok) break;
         tc_commit(accfull0 + 8 * a);
@@ -411,11 +466,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     // ------------------------------------------------------------ epilogue
     const int row = warp * 32 + lane;          // TMEM lane = tile row
     int it = 0;
+    uint32_t ge = 0;   // this item's first chunk in the CTA's sequence (trace only)
     for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
       int tile, c0, c1;
       item_range(p, item, tile, c0, c1);
       const int a = it & 1;
-      if (!mbar_wait(accfull0 + 8 * a, (it >> 1) & 1, p.wait_limit, abort_flag)) break;
+      if (!mbar_wait(accfull0 + 8 * a, (it >> 1) & 1, p.wait_limit, abort_flag, 256)) break;
+      if (threadIdx.x == 0) stamp(ge, 6);
       tc_fence_after();
       float* yrow = p.Y + (size_t)tile * kTileM + row;
 #pragma unroll
@@ -432,7 +489,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         }
       }
       tc_fence_before();
-      mbar_arrive(accempty0 + 8 * a);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accempty0 + 8 * a);
+      if (threadIdx.x == 0) stamp(ge, 7);
+      ge += c1 - c0;
     }
   }
 
@@ -442,6 +502,20 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
+}
+
+// X fp16 [64][K] -> bf16 (nearest even) as [K/8 column groups][64 tokens][8]:
+// each 64-column chunk becomes one contiguous 8 KB token tile in the
+// core-matrix layout.  One thread per (group, token).
+__global__ void __launch_bounds__(256) x_to_bf16_kernel(const __half* __restrict__ X, uint8_t* __restrict__ xb,
+                                                        int K) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;   // = group * 64 + token
+  if (i >= (K >> 3) * kTok) return;
+  const int grp = i / kTok, tok = i - grp * kTok;
+  const uint4 v = *reinterpret_cast<const uint4*>(X + (size_t)tok * K + grp * 8);
+  const uint4 o = make_uint4(h2_to_bf16x2(v.x), h2_to_bf16x2(v.y), h2_to_bf16x2(v.z), h2_to_bf16x2(v.w));
+  *reinterpret_cast<uint4*>(xb + (size_t)i * 16) = o;
+  pdl_trigger();
 }
 
 }  // namespace gemm
@@ -477,17 +551,17 @@ static int encode_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type
   return Q4_OK;
 }
 
+size_t gemm_ws_bytes(int K) { return ((size_t)gemm::kTok * K * 2 + 255) & ~(size_t)255; }
+
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
-                      int N, int K, const DeviceInfo& dev, cudaStream_t s) {
+                      int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s) {
   (void)M;
   gemm::Params p;
   memset(&p, 0, sizeof(p));
   int st = encode_2d(&p.tm_codes, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N,
-                     gemm::kChunk / 2, gemm::kTileM, "codes");
+                     gemm::kChunk * gemm::kRawChunks / 2, gemm::kTileM, "codes");
   if (st != Q4_OK) return st;
-  st = encode_2d(&p.tm_x, X, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)K, gemm::kTok, gemm::kChunk, gemm::kTok,
-                 "X");
-  if (st != Q4_OK) return st;
+  p.xb = static_cast<const uint8_t*>(ws);
   p.scales = scales;
   p.sc_tma = K % 256 == 0;
   if (p.sc_tma) {
@@ -504,9 +578,15 @@ int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* 
   if (splits > p.nchunks) splits = p.nchunks;
   if (splits < 1) splits = 1;
   p.cps = (p.nchunks + splits - 1) / splits;
+  p.cps = (p.cps + gemm::kRawChunks - 1) / gemm::kRawChunks * gemm::kRawChunks;   // raw stages start aligned
   p.splits = (p.nchunks + p.cps - 1) / p.cps;
   p.items = p.tiles * p.splits;
   p.wait_limit = wait_limit();
+  size_t tbytes = 0;
+  void* tb = trace_buffer(&tbytes);
+  p.trace = (tb && tbytes >= (size_t)gemm::kTraceChunks * 8 * sizeof(unsigned long long))
+                ? static_cast<unsigned long long*>(tb)
+                : nullptr;
   cudaError_t e;
   if (p.splits > 1) {
     e = cudaMemsetAsync(Y, 0, (size_t)gemm::kTok * N * sizeof(float), s);
@@ -519,9 +599,23 @@ int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* 
     if (e != cudaSuccess) return cuda_fail(e, "gemm smem attribute");
     attr_set = true;
   }
-  const int grid = p.items < dev.sms ? p.items : dev.sms;
-  gemm::gemm_kernel<<<grid, gemm::kThreadsG, gemm::kSmemBytes, s>>>(p);
+  const int nx = (K >> 3) * gemm::kTok;
+  gemm::x_to_bf16_kernel<<<(nx + 255) / 256, 256, 0, s>>>(X, static_cast<uint8_t*>(ws), K);
   e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "gemm x conversion launch");
+  // the GEMM starts while the conversion runs; only its B loader waits for it
+  const int grid = p.items < dev.sms ? p.items : dev.sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(gemm::kThreadsG);
+  cfg.dynamicSmemBytes = gemm::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm::gemm_kernel, p);
   return e == cudaSuccess ? Q4_OK : cuda_fail(e, "gemm launch");
 }
 

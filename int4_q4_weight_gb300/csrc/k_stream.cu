@@ -1146,6 +1146,11 @@ int launch_head_stream(const uint8_t* codes, const __half* scales, const __half*
 static void* g_trace_buf = nullptr;
 static size_t g_trace_bytes = 0;
 
+void* trace_buffer(size_t* bytes) {
+  *bytes = g_trace_bytes;
+  return g_trace_buf;
+}
+
 size_t decode_ctl_bytes() { return 256; }
 
 int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const __half* h0, __half* h_out,

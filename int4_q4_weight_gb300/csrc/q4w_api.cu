@@ -142,7 +142,7 @@ static size_t decode_ws_bytes(size_t H, size_t QKV, size_t I) {
 size_t q4_workspace_bytes(int op, int a, int b, int c) {
   switch (op) {
     case Q4_OP_GEMV: return 0;
-    case Q4_OP_GEMM_CHUNK: return 0;
+    case Q4_OP_GEMM_CHUNK: return (b >= 64 && b % 64 == 0) ? gemm_ws_bytes(b) : 0;
     case Q4_OP_PLE: return 0;
     case Q4_OP_LMHEAD: {
       DeviceInfo dev;
@@ -443,8 +443,6 @@ int ple_gather_project(const int32_t* ids, int S, const int8_t* table, const flo
 
 int q4_gemm_chunk(const uint8_t* codes, const uint16_t* scales, const uint16_t* X_f16, float* Y, int M,
                   int N, int K, void* ws, size_t ws_bytes, q4_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   clear_error();
   CHECK_NULL(codes);
   CHECK_NULL(scales);
@@ -457,9 +455,12 @@ int q4_gemm_chunk(const uint8_t* codes, const uint16_t* scales, const uint16_t* 
   CHECK(M == 64, "M=%d must be 64 (the static prefill width)", M);
   CHECK(N >= 128 && N % 128 == 0, "N=%d must be a positive multiple of 128", N);
   CHECK(K >= 64 && K % 64 == 0 && K <= kMaxK, "K=%d must be a multiple of 64 in [64, %d]", K, kMaxK);
+  CHECK_ALIGN(ws);
+  if (ws == nullptr || ws_bytes < gemm_ws_bytes(K))
+    return fail(Q4_ERR_WORKSPACE, "ws must hold %zu bytes (got %zu)", gemm_ws_bytes(K), ws ? ws_bytes : (size_t)0);
   DEVICE_OR_RETURN(dev);
   return launch_gemm_chunk(codes, reinterpret_cast<const __half*>(scales),
-                           reinterpret_cast<const __half*>(X_f16), Y, M, N, K, dev,
+                           reinterpret_cast<const __half*>(X_f16), Y, M, N, K, ws, dev,
                            reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -69,6 +69,9 @@ def test_null_and_shape_rejections(lib):
     assert lib.q4_gemv(A, A, A, A, 16, 65536, 1, None, 0, None) == 2    # K too large
     assert lib.q4_gemm_chunk(A, A, A, A, 32, 128, 64, None, 0, None) == 2   # M != 64
     assert lib.q4_gemm_chunk(A, A, A, A, 64, 100, 64, None, 0, None) == 2   # N % 128
+    assert lib.q4_gemm_chunk(A, A, A, A, 64, 128, 64, None, 0, None) == 4   # no workspace
+    assert lib.q4_gemm_chunk(A, A, A, A, 64, 128, 1536, A, 1000, None) == 4  # workspace too small
+    assert lib.q4_workspace_bytes(q4w.Q4_OP_GEMM_CHUNK, 128, 1536, 64) == 64 * 1536 * 2
     assert lib.ple_gather_project(A, 4, A, A, 10, 35, 128, 16.0, A, A, 64, A, 1e-6, A, None, None,
                                   None) == 2                                # ld != 256
     assert lib.lmhead_softcap_argmax(A, A, A, 9, 100, 64, 30.0, A, A, A, None, A, 1 << 20,
