@@ -366,7 +366,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     // ----------------------------------------------------------- converters
     const int pt = threadIdx.x - kEpiWarps * 32;
     const int r = pt >> 1, h = pt & 1;        // A: row of the tile, 32-block in the chunk
-    const uint32_t a_off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 16);
+    // A: core matrix (8 rows x 16 B) of row block r/8 and column block kb at
+    // kb * 2048 + (r/8) * 128, so the 16 row blocks of one column block are
+    // contiguous (the tensor core reads them together without bank conflicts)
+    const uint32_t a_off = (uint32_t)((r >> 3) * 128 + (r & 7) * 16);
     uint32_t g = 0, gr = 0;   // operand chunks, raw stages
     bool ok = true;
     for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           const uint32_t w4[4] = {code.x, code.y, code.z, code.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(A + a_off + (h * 4 + j) * 128) = dequant_word(w4[j], dd, bias);
+            *reinterpret_cast<uint4*>(A + a_off + (h * 4 + j) * 2048) = dequant_word(w4[j], dd, bias);
           fence_proxy_async();   // this thread's stores, before the tensor core reads them
           __syncwarp();
           if (lane == 0) mbar_arrive(full0 + 8 * s);
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           const uint32_t A = stage0 + s * kStageBytes, B = A + kABytes;
 #pragma unroll
           for (int ks = 0; ks < kChunk / 16; ++ks) {
-            const uint64_t ad = smem_desc(A + ks * 256, 128, 1024);
+            const uint64_t ad = smem_desc(A + ks * 4096, 2048, 128);
             const uint64_t bd = smem_desc(B + ks * 2048, 1024, 128);
             tc_mma(d_tmem, ad, bd, (c > c0 || ks > 0) ? 1u : 0u);
           }
