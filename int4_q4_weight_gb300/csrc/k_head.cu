@@ -171,6 +171,11 @@ __global__ void __launch_bounds__(kThreads) head_batched_kernel(const uint8_t* _
   head_finish(partials, ticket, B, cap, idx, top1, top2);
 }
 
+size_t head_batch_smem(int b, int K);
+int launch_head_batch(const uint8_t* codes, const __half* scales, const __half* h, int b, int V, int K, float cap,
+                      int32_t* idx, float* top1, float* top2, float* logits, Top2* partials, unsigned* ticket,
+                      int grid, cudaStream_t s);
+
 static int lpr_for(int nb) {
   int l = 32;
   while (l > 1 && nb % l) l >>= 1;
@@ -225,7 +230,9 @@ static cudaError_t launch_head_t(const uint8_t* codes, const __half* scales, con
 int launch_lmhead(const uint8_t* codes, const __half* scales, const __half* h, int b, int V, int K,
                   float cap, int32_t* idx, float* top1, float* top2, float* logits, void* ws,
                   const DeviceInfo& dev, cudaStream_t s) {
-  if ((size_t)b * (K >> 5) * kXStride * sizeof(float) > (size_t)200 * 1024)
+  if (b == 1 && (size_t)(K >> 5) * kXStride * sizeof(float) > (size_t)200 * 1024)
+    return fail(Q4_ERR_SHAPE, "lmhead: K %d does not fit in shared memory", K);
+  if (b > 1 && head_batch_smem(b, K) > (size_t)220 * 1024)
     return fail(Q4_ERR_SHAPE, "lmhead: batch %d x K %d does not fit in shared memory", b, K);
   if (b == 1 && stream_eligible(K))
     return launch_head_stream(codes, scales, h, V, K, cap, idx, top1, top2, logits, ws, dev, s);
@@ -233,6 +240,12 @@ int launch_lmhead(const uint8_t* codes, const __half* scales, const __half* h, i
   Top2* partials = reinterpret_cast<Top2*>(reinterpret_cast<char*>(ws) + kTicketBytes);
   cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return cuda_fail(e, "lmhead ticket reset");
+  if (b > 1) {
+    int grid = head_grid(dev);
+    const int need = (V + 7) / 8;   // at least one row per group of the smallest grouping
+    if (grid > need) grid = need;
+    return launch_head_batch(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, grid, s);
+  }
   switch (lpr_for(K >> 5)) {
     case 32: e = launch_head_t<32>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
     case 16: e = launch_head_t<16>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;

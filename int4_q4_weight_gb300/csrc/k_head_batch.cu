@@ -1,0 +1,218 @@
+// LM head for a batch of 2..8 hidden vectors (the S=4 / S=8 verify shapes):
+// z[b][v] = sum_k W[v][k] h[b][k] with the same softcap and two-level top-two
+// selection as the single-vector head ("Gemma 4 E2B (text decoder) - Core
+// AI", Signature features and What it took).
+//
+// Each weight block is decoded once and applied to every batch vector: a
+// lane turns its 16 code bytes into 16 fp16 half pairs (64 + n_j,
+// 64 + n_{j+4}) with one LOP3 each, then for each batch vector multiplies
+// them into two fp32 accumulators with the mixed-precision FMA, against the
+// vector's half pairs (x[8i+j], x[8i+j+4]) staged in shared memory.  Per
+// vector the arithmetic and its order are those of the single-vector head
+// (bias -72 * sum(x) per block, lo/hi accumulators, one fmaf with the scale
+// per block, the lane-group reduction from P/2 down), so row 0 of a batch
+// gives the single-vector result.
+#include "q4w_device.cuh"
+#include "q4w_internal.cuh"
+#include "q4w_top2.cuh"
+
+namespace q4w {
+
+namespace hb {
+
+constexpr int kThr = 256;
+constexpr int kWarpsHB = kThr / 32;
+__device__ __forceinline__ void top2_shfl_merge(Top2& t, int o) {
+  Top2 u;
+  u.v1 = __shfl_xor_sync(0xffffffffu, t.v1, o);
+  u.v2 = __shfl_xor_sync(0xffffffffu, t.v2, o);
+  u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
+  u.i2 = __shfl_xor_sync(0xffffffffu, t.i2, o);
+  top2_merge(t, u);
+}
+
+// NBP: batch vectors computed (B rounded up to 4 or 8; the rest have x = 0).
+// lgP: log2 of the lanes per row (P <= 32, P divides the block count).
+template <int NBP>
+__global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restrict__ codes,
+                                                         const __half* __restrict__ scales,
+                                                         const __half* __restrict__ h, int B, int V, int K,
+                                                         int lgP, float cap, float* __restrict__ logits,
+                                                         Top2* partials, unsigned* ticket, int32_t* idx,
+                                                         float* top1, float* top2) {
+  extern __shared__ __align__(16) uint32_t hb_smem[];
+  const int nb = K >> 5;
+  const int xstride = 16 * NBP + 4;           // words per block (+4: lanes of a group hit other banks)
+  uint32_t* xw = hb_smem;                     // [nb][16 pairs][NBP] half pairs
+  float* xb = reinterpret_cast<float*>(hb_smem + (size_t)nb * xstride);   // [nb][NBP] biases
+  __shared__ Top2 st[kWarpsHB][kMaxBatch];
+
+  // stage the half pairs (x[32j+8i+jj], x[32j+8i+jj+4]) and the block biases
+  for (int e = threadIdx.x; e < nb * 16 * NBP; e += kThr) {
+    const int b = e % NBP, p = (e / NBP) & 15, j = e / (16 * NBP);
+    uint32_t w = 0u;
+    if (b < B) {
+      const int k = 32 * j + 8 * (p >> 2) + (p & 3);
+      const __half* hv = h + (size_t)b * K;
+      w = (uint32_t)__half_as_ushort(hv[k]) | ((uint32_t)__half_as_ushort(hv[k + 4]) << 16);
+    }
+    xw[j * xstride + p * NBP + b] = w;
+  }
+  for (int e = threadIdx.x; e < nb * NBP; e += kThr) {
+    const int b = e % NBP, j = e / NBP;
+    float sum = 0.f;
+    if (b < B) {
+      const __half* hv = h + (size_t)b * K + 32 * j;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          sum += __half2float(hv[8 * i + jj]) + __half2float(hv[8 * i + jj + 4]);
+    }
+    xb[j * NBP + b] = -72.f * sum;
+  }
+  __syncthreads();
+
+  const int P = 1 << lgP;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int li = lane & (P - 1);
+  const int gid = threadIdx.x >> lgP, ngroups = kThr >> lgP;
+  const size_t K2 = (size_t)(K >> 1);
+  Top2 best[NBP];
+#pragma unroll
+  for (int b = 0; b < NBP; ++b) top2_init(best[b]);
+
+  // Row groups of a warp advance together (the shuffles use the full mask);
+  // a group past the last row recomputes row V - 1 and drops it.
+  const int step = gridDim.x * ngroups;
+  const int wg0 = (warp * 32) >> lgP;                  // the warp's first group
+  const int bpl = nb >> lgP;                           // blocks per lane (P divides nb)
+  for (int wrow = blockIdx.x * ngroups + wg0; wrow < V; wrow += step) {   // uniform per warp
+    const int row0 = wrow + (gid - wg0);
+    const bool valid = row0 < V;
+    const int row = valid ? row0 : V - 1;
+    const uint8_t* cp = codes + (size_t)row * K2;
+    const __half* sp = scales + (size_t)row * nb;
+    float acc[NBP];
+#pragma unroll
+    for (int b = 0; b < NBP; ++b) acc[b] = 0.f;
+    for (int t = 0; t < bpl; ++t) {
+      const int j = li + P * t;
+      const uint4 c = ld_stream16(cp + 16 * j);
+      const float d = ld_scale(sp + j);
+      uint32_t wq[16];
+      const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t wv = w4[i];
+        const uint32_t sh[4] = {shl_u32(wv, 4), wv, shr_u32(wv, 4), shr_u32(wv, 8)};
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) wq[4 * i + jj] = lop3_and_or(sh[jj], kH64Mask, kH64Magic);
+      }
+      float lo[NBP], hi[NBP];
+#pragma unroll
+      for (int b = 0; b < NBP; ++b) {
+        lo[b] = xb[j * NBP + b];
+        hi[b] = 0.f;
+      }
+      const uint32_t* xj = xw + j * xstride;
+#pragma unroll
+      for (int p = 0; p < 16; ++p) {
+        uint32_t xq[NBP];
+#pragma unroll
+        for (int q = 0; q < NBP / 4; ++q) {
+          const uint4 u = *reinterpret_cast<const uint4*>(xj + p * NBP + 4 * q);
+          xq[4 * q] = u.x;
+          xq[4 * q + 1] = u.y;
+          xq[4 * q + 2] = u.z;
+          xq[4 * q + 3] = u.w;
+        }
+#pragma unroll
+        for (int b = 0; b < NBP; ++b) fhfma2(lo[b], hi[b], wq[p], xq[b]);
+      }
+#pragma unroll
+      for (int b = 0; b < NBP; ++b) acc[b] = fmaf(d, lo[b] + hi[b], acc[b]);
+    }
+#pragma unroll
+    for (int b = 0; b < NBP; ++b)
+      for (int o = P >> 1; o > 0; o >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], o);
+    if (li == 0 && valid) {
+#pragma unroll
+      for (int b = 0; b < NBP; ++b) {
+        if (b < B) {
+          top2_insert(best[b], acc[b], row);
+          if (logits) logits[(size_t)b * V + row] = cap * tanhf(acc[b] / cap);
+        }
+      }
+    }
+  }
+  // groups of a warp -> lane 0, warps -> the CTA's partial per batch row
+#pragma unroll
+  for (int b = 0; b < NBP; ++b)
+    for (int o = P; o < 32; o <<= 1) top2_shfl_merge(best[b], o);
+  if (lane == 0) {
+#pragma unroll
+    for (int b = 0; b < NBP; ++b)
+      if (b < B) st[warp][b] = best[b];
+  }
+  __syncthreads();
+  if (threadIdx.x < B) {
+    Top2 t;
+    top2_init(t);
+    for (int w = 0; w < kWarpsHB; ++w) top2_merge(t, st[w][threadIdx.x]);
+    partials[(size_t)blockIdx.x * kMaxBatch + threadIdx.x] = t;
+  }
+  head_finish(partials, ticket, B, cap, idx, top1, top2);
+}
+
+}  // namespace hb
+
+// Lanes per row: the largest power of two up to 32 that divides the block count.
+static int head_batch_lgp(int nb) {
+  int lg = 5;
+  while (lg > 0 && nb % (1 << lg)) --lg;
+  return lg;
+}
+
+// b in [2, 8]; K % 32 == 0: shared memory of the x staging.
+size_t head_batch_smem(int b, int K) {
+  const int NBP = b <= 4 ? 4 : 8;
+  const int nb = K >> 5;
+  size_t bytes = (size_t)nb * (16 * NBP + 4) * 4 + (size_t)nb * NBP * 4;
+  return bytes;
+}
+
+int launch_head_batch(const uint8_t* codes, const __half* scales, const __half* h, int b, int V, int K, float cap,
+                      int32_t* idx, float* top1, float* top2, float* logits, Top2* partials, unsigned* ticket,
+                      int grid, cudaStream_t s) {
+  const int lgP = head_batch_lgp(K >> 5);
+  const size_t smem = head_batch_smem(b, K);
+  cudaError_t e;
+  // one wave: the grid is capped at the CTAs that are resident at once
+  int sms = 0, per_sm = 0;
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "batched head device query");
+  if (b <= 4) {
+    e = cudaFuncSetAttribute(hb::head_batch_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hb::head_batch_kernel<4>, hb::kThr, smem);
+    if (e == cudaSuccess && per_sm > 0 && grid > sms * per_sm) grid = sms * per_sm;
+    if (e == cudaSuccess)
+      hb::head_batch_kernel<4><<<grid, hb::kThr, smem, s>>>(codes, scales, h, b, V, K, lgP, cap, logits, partials,
+                                                           ticket, idx, top1, top2);
+  } else {
+    e = cudaFuncSetAttribute(hb::head_batch_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hb::head_batch_kernel<8>, hb::kThr, smem);
+    if (e == cudaSuccess && per_sm > 0 && grid > sms * per_sm) grid = sms * per_sm;
+    if (e == cudaSuccess)
+      hb::head_batch_kernel<8><<<grid, hb::kThr, smem, s>>>(codes, scales, h, b, V, K, lgP, cap, logits, partials,
+                                                           ticket, idx, top1, top2);
+  }
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e == cudaSuccess ? Q4_OK : cuda_fail(e, "batched head launch");
+}
+
+}  // namespace q4w
