@@ -469,25 +469,35 @@ def pass_trace(q4w, synth, dev, reps):
     early = (ti[:, :, 5] & 1).reshape(-1, 4, sms)
     ti = ti.copy()
     ti[:, :, 0] -= ti[:, :, 0].min()   # relative ns first: float64 cannot hold absolute ns to 1 ns
+    early_last = (ti[:, :, 7] & 1).reshape(-1, 4, sms)
+    multi = (ti[:, :, 7] > 0).reshape(-1, 4, sms)
     ti[:, :, 5] >>= 1
+    ti[:, :, 7] >>= 1
     t = ti.astype(np.float64)
     for i in range(1, 8):
         t[:, :, i] = t[:, :, 0] + t[:, :, i] / ghz
     t0 = t[0, :, 0].min()
     kinds = ["qkv", "o", "gate_up", "down"]
-    # per (stage, CTA): 0 entered, 7 descriptor read, 1 input complete and
+    # per (stage, CTA): 0 entered, 7 last tile landed (0: one tile), 1 input complete and
     # staged, 2 x built, 3 x in registers, 5 first tile landed, 6 first tile
     # usable by the whole warp, 4 own rows written
     out = {"stages": nst, "total_us": round((t[:, :, 4].max() - t0) / 1e3, 2), "sm_ghz_assumed": ghz}
+    out["last_tile_already_landed_frac"] = {k: round(float(early_last[:, i][multi[:, i]].mean()), 3)
+                                             if multi[:, i].any() else None for i, k in enumerate(kinds)}
     out["first_tile_already_landed_frac"] = {k: round(float(early[:, i].mean()), 3) for i, k in enumerate(kinds)}
-    names = {"desc": (0, 7), "input_wait": (7, 1), "xform": (1, 2), "x_regs": (2, 3), "tile_wait": (3, 5),
+    names = {"input_wait": (0, 1), "xform": (1, 2), "x_regs": (2, 3), "tile_wait": (3, 5),
              "warp_sync": (5, 6), "rows": (6, 4)}
-    agg = {k: {n: 0.0 for n in list(names) + ["rows_max", "handoff", "next_entry"]} for k in kinds}
+    agg = {k: {n: 0.0 for n in list(names) + ["rows_max", "handoff", "next_entry", "last_tile_after_first",
+                                                "rows_after_last_tile"]} for k in kinds}
     for s in range(nst):
         k = kinds[s % 4]
         for n, (i, j) in names.items():
             agg[k][n] += np.median(t[s, :, j] - t[s, :, i]) / 1e3
         agg[k]["rows_max"] += (t[s, :, 4] - t[s, :, 6]).max() / 1e3
+        m = ti[s, :, 7] > 0
+        if m.any():
+            agg[k]["last_tile_after_first"] += np.median(t[s, m, 7] - t[s, m, 6]) / 1e3
+            agg[k]["rows_after_last_tile"] += np.median(t[s, m, 4] - t[s, m, 7]) / 1e3
         if s > 0:   # last CTA done with the previous stage -> median CTA has this stage's input
             agg[k]["handoff"] += (np.median(t[s, :, 1]) - t[s - 1, :, 4].max()) / 1e3
             agg[k]["next_entry"] += np.median(t[s, :, 0] - t[s - 1, :, 4]) / 1e3

@@ -4,14 +4,14 @@
 // AI", Signature features and What it took).
 //
 // Each weight block is decoded once and applied to every batch vector: a
-// lane turns its 16 code bytes into 16 fp16 half pairs (64 + n_j,
-// 64 + n_{j+4}) with one LOP3 each, then for each batch vector multiplies
+// lane turns its 16 code bytes into 16 fp16 half pairs (q4_word_pairs: one
+// LOP3 each), then for each batch vector multiplies
 // them into two fp32 accumulators with the mixed-precision FMA, against the
 // vector's half pairs (x[8i+j], x[8i+j+4]) staged in shared memory.  Per
-// vector the arithmetic and its order are those of the single-vector head
-// (bias -72 * sum(x) per block, lo/hi accumulators, one fmaf with the scale
-// per block, the lane-group reduction from P/2 down), so row 0 of a batch
-// gives the single-vector result.
+// vector the arithmetic is that of the single-vector head (the block bias of
+// q4_block_dot_h, lo/hi accumulators, one fmaf with the scale
+// per block, the lane-group reduction from P/2 down); only the order in
+// which the block bias sums x differs.
 #include "q4w_device.cuh"
 #include "q4w_internal.cuh"
 #include "q4w_top2.cuh"
@@ -60,16 +60,16 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
   }
   for (int e = threadIdx.x; e < nb * NBP; e += kThr) {
     const int b = e % NBP, j = e / NBP;
-    float sum = 0.f;
+    float se = 0.f, so = 0.f;   // even / odd columns of the block
     if (b < B) {
       const __half* hv = h + (size_t)b * K + 32 * j;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          sum += __half2float(hv[8 * i + jj]) + __half2float(hv[8 * i + jj + 4]);
+      for (int k = 0; k < 32; k += 2) {
+        se += __half2float(hv[k]);
+        so += __half2float(hv[k + 1]);
+      }
     }
-    xb[j * NBP + b] = -72.f * sum;
+    xb[j * NBP + b] = kBiasEven * se + kBiasOdd * so;
   }
   __syncthreads();
 
@@ -104,10 +104,10 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
       const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t wv = w4[i];
-        const uint32_t sh[4] = {shl_u32(wv, 4), wv, shr_u32(wv, 4), shr_u32(wv, 8)};
+        uint32_t pr[4];
+        q4_word_pairs(w4[i], pr);
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) wq[4 * i + jj] = lop3_and_or(sh[jj], kH64Mask, kH64Magic);
+        for (int jj = 0; jj < 4; ++jj) wq[4 * i + jj] = pr[jj];
       }
       float lo[NBP], hi[NBP];
 #pragma unroll

@@ -276,7 +276,7 @@ __device__ __forceinline__ float load_in_cg(const void* in, int mode, int k) {
 }
 
 // x = prologue(in), written per 32-column block as the half pairs
-// (x[8i+j], x[8i+j+4]) plus the bias -72 * sum(x) (kXhStride words).
+// (x[8i+j], x[8i+j+4]) plus the bias of q4_block_dot_h (kXhStride words).
 //
 // Staged path (the input and its fp16 x fit kStageInBytes): the input is
 // copied to shared memory with 16-byte loads from L2 -- for a tagged input
@@ -449,19 +449,24 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
       float v[8];
       load8(ch, v);
       uint32_t hx[8];
-      float part = 0.f;
+      float pe = 0.f, po = 0.f;   // sums over the chunk's even / odd columns
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const __half x = __float2half_rn(xform(v[e], mode, r, r2));
         hx[e] = __half_as_ushort(x);
-        part += __half2float(x);
+        if (e & 1)
+          po += __half2float(x);
+        else
+          pe += __half2float(x);
       }
       const int blk = ch >> 2, i = ch & 3;
       *reinterpret_cast<uint4*>(xh + blk * kXhStride + 4 * i) =
           make_uint4(hx[0] | (hx[4] << 16), hx[1] | (hx[5] << 16), hx[2] | (hx[6] << 16), hx[3] | (hx[7] << 16));
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      if (i == 0) xh[blk * kXhStride + 16] = __float_as_uint(-72.f * part);
+      pe += __shfl_xor_sync(0xffffffffu, pe, 1);
+      po += __shfl_xor_sync(0xffffffffu, po, 1);
+      pe += __shfl_xor_sync(0xffffffffu, pe, 2);
+      po += __shfl_xor_sync(0xffffffffu, po, 2);
+      if (i == 0) xh[blk * kXhStride + 16] = __float_as_uint(kBiasEven * pe + kBiasOdd * po);
     }
     bar_sync(1, kCT);
     return true;
@@ -493,10 +498,15 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
     const __half va = __float2half_rn(xform(in(k), mode, r, r2));
     const __half vc = __float2half_rn(xform(in(k + 4), mode, r, r2));
     xh[b * kXhStride + pr] = (uint32_t)__half_as_ushort(va) | ((uint32_t)__half_as_ushort(vc) << 16);
-    float sum = __half2float(va) + __half2float(vc);
+    // columns 8i+j and 8i+j+4 share the parity of j
+    const float sum = __half2float(va) + __half2float(vc);
+    float se = (j & 1) ? 0.f : sum, so = (j & 1) ? sum : 0.f;
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (pr == 0) xh[b * kXhStride + 16] = __float_as_uint(-72.f * sum);
+    for (int o = 8; o > 0; o >>= 1) {
+      se += __shfl_xor_sync(0xffffffffu, se, o);
+      so += __shfl_xor_sync(0xffffffffu, so, o);
+    }
+    if (pr == 0) xh[b * kXhStride + 16] = __float_as_uint(kBiasEven * se + kBiasOdd * so);
   }
   bar_sync(1, kCT);
   return true;
@@ -593,6 +603,8 @@ __device__ bool consume_fast(const StageArgs& a, const Geo& g, uint32_t& gcount,
     const bool landed = mbar_wait(full0 + 8 * s, round & 1, c);
     // first tile landed; bit 0 set when it had landed before the consumers asked
     if (c.tr && ct == 0 && it.first()) c.tr[5] = (stamp(c) << 1) | (early ? 1ull : 0ull);
+    // every later tile: stamp 7 ends as the last tile's landing (bit 0: it had landed already)
+    if (c.tr && ct == 0 && !it.first()) c.tr[7] = (stamp(c) << 1) | (early ? 1ull : 0ull);
     const bool all = (P <= 32) ? (__all_sync(0xffffffffu, landed) != 0) : bar_and(2 + gid, P, landed);
     if (!all) {
       ok = false;
@@ -709,6 +721,8 @@ __device__ bool consume_generic(const StageArgs& a, const Geo& g, uint32_t& gcou
     const bool early = c.tr && mbar_probe(full0 + 8 * s, round & 1);
     const bool landed = mbar_wait(full0 + 8 * s, round & 1, c);
     if (c.tr && ct == 0 && it.first()) c.tr[5] = (stamp(c) << 1) | (early ? 1ull : 0ull);
+    // every later tile: stamp 7 ends as the last tile's landing (bit 0: it had landed already)
+    if (c.tr && ct == 0 && !it.first()) c.tr[7] = (stamp(c) << 1) | (early ? 1ull : 0ull);
     const bool all = (P <= 32) ? (__all_sync(0xffffffffu, landed) != 0) : bar_and(2 + gid, P, landed);
     if (!all) {
       ok = false;
@@ -1034,7 +1048,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
         sg[(s + 1) & 1] = make_geo(nx, nx.pair ? 2 : 1);
       }
       const StageArgs& a = sa[s & 1];
-      if (tr) tr[7] = stamp(c);
+      if (tr) tr[7] = 0;
       // the prologue waits (bounded) until its whole input carries tag s
       ok = eng_prologue(a, S.xs, S.stage_in, S.red, c);
       if (!ok) break;

@@ -97,13 +97,20 @@ __device__ __forceinline__ float q4_block_dot(const uint4 c, const float4 (&xv)[
 
 
 // ---------------------------------------------- fp16-magic block dot (fast) ---
-// Two codes per LOP3: a 32-bit word of codes shifted so that nibbles j and
-// j+4 sit in bits [4,8) and [20,24) is OR-ed into two fp16 64.0 patterns,
-// giving the half pair (64 + n_j, 64 + n_{j+4}) exactly.  Each half is
-// multiplied by the matching fp16 x with the mixed-precision fp32 FMA
-// (fma.rn.f32.f16: exact product, one fp32 rounding).  x is held as half
-// pairs xh[4i + j] = (x[8i+j], x[8i+j+4]); bias = -72 * sum(x over the block)
-// removes the 64 + 8 offset, so bias + sum F_k x_k = sum (code_k - 8) x_k.
+// Two codes per LOP3.  In a 32-bit word of codes (columns 8i..8i+7, byte b =
+// columns 8i+2b (low nibble) and 8i+2b+1 (high nibble)) the low nibbles of
+// bytes 0 and 2 sit in bits [0,4) and [16,20): OR-ed into two fp16 1024.0
+// patterns they read as the half pair (1024 + n, 1024 + n') exactly (fp16
+// spacing at 1024 is 1); the high nibbles sit in bits [4,8) and [20,24) and
+// read as (64 + n, 64 + n') in two fp16 64.0 patterns (spacing 1/16, the
+// nibble counted in sixteenths).  The word shifted by 8 gives bytes 1 and 3
+// the same way: four LOP3 and one shift per word.  Each half is multiplied by
+// the matching fp16 x with the mixed-precision fp32 FMA (fma.rn.f32.f16:
+// exact product, one fp32 rounding).  x is held as half pairs
+// xh[4i + j] = (x[8i+j], x[8i+j+4]); the bias
+//   -1032 * sum(x at even columns) - 72 * sum(x at odd columns)
+// removes the 1024 + 8 and 64 + 8 offsets, so bias + sum F_k x_k =
+// sum (code_k - 8) x_k.
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t magic) {
   uint32_t d;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(magic));
@@ -127,17 +134,29 @@ __device__ __forceinline__ void fhfma2(float& lo, float& hi, uint32_t a, uint32_
 }
 
 constexpr uint32_t kH64Mask = 0x00F000F0u;
-constexpr uint32_t kH64Magic = 0x54005400u;   // fp16 64.0 in both halves
+constexpr uint32_t kH64Magic = 0x54005400u;     // fp16 64.0 in both halves
+constexpr uint32_t kH1024Mask = 0x000F000Fu;
+constexpr uint32_t kH1024Magic = 0x64006400u;   // fp16 1024.0 in both halves
+constexpr float kBiasEven = -1032.f, kBiasOdd = -72.f;
+
+// Half pair j (j = 0..3) of a code word, as q4_block_dot_h uses it.
+__device__ __forceinline__ void q4_word_pairs(uint32_t w, uint32_t (&p)[4]) {
+  const uint32_t w8 = shr_u32(w, 8);
+  p[0] = lop3_and_or(w, kH1024Mask, kH1024Magic);    // columns 8i+0, 8i+4
+  p[1] = lop3_and_or(w, kH64Mask, kH64Magic);        // columns 8i+1, 8i+5
+  p[2] = lop3_and_or(w8, kH1024Mask, kH1024Magic);   // columns 8i+2, 8i+6
+  p[3] = lop3_and_or(w8, kH64Mask, kH64Magic);       // columns 8i+3, 8i+7
+}
 
 __device__ __forceinline__ float q4_block_dot_h(const uint4 c, const uint32_t (&xh)[16], float bias) {
   const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
   float lo = bias, hi = 0.f;   // even/odd halves accumulate separately (two chains)
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t w = w4[i];
-    const uint32_t sh[4] = {shl_u32(w, 4), w, shr_u32(w, 4), shr_u32(w, 8)};
+    uint32_t pr[4];
+    q4_word_pairs(w4[i], pr);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) fhfma2(lo, hi, lop3_and_or(sh[j], kH64Mask, kH64Magic), xh[4 * i + j]);
+    for (int j = 0; j < 4; ++j) fhfma2(lo, hi, pr[j], xh[4 * i + j]);
   }
   return lo + hi;
 }
