@@ -58,8 +58,8 @@ __global__ void __launch_bounds__(kPleThreads) ple_kernel(const int32_t* __restr
     return reinterpret_cast<__half*>(ple_smem + (size_t)st * kPleStageBytes + (size_t)kProjTileFloats * 4);
   };
   // tile kt of the projection (256 rows x 32 columns, 8 x 16 B per row) and of
-  // the hidden rows (16 tokens x 32 fp16, 4 x 16 B per token; missing tokens
-  // read row 0 and are zeroed when used)
+  // the hidden rows (16 tokens x 32 fp16, 4 x 16 B per token; tokens past S
+  // read token t0's row)
   auto issue = [&](int kt) {
     if (kt < nkt) {
       float* ps = stage_proj(kt % kPleStages);
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kPleThreads) ple_kernel(const int32_t* __restr
     __syncthreads();                                        // ... and everyone else's
     const float* ps = stage_proj(kt % kPleStages);
     const __half* hs = stage_hid(kt % kPleStages);
-#pragma unroll 2
+#pragma unroll
     for (int k = 0; k < kKT; k += 4) {
       float4 pv[4];
 #pragma unroll
@@ -103,9 +103,8 @@ __global__ void __launch_bounds__(kPleThreads) ple_kernel(const int32_t* __restr
         const uint2 hh = *reinterpret_cast<const uint2*>(hs + tt * kKT + k);
         const float2 h01 = __half22float2(*reinterpret_cast<const __half2*>(&hh.x));
         const float2 h23 = __half22float2(*reinterpret_cast<const __half2*>(&hh.y));
-        const bool live = tt < ntok;
-        const float x0 = live ? h01.x : 0.f, x1 = live ? h01.y : 0.f;
-        const float x2 = live ? h23.x : 0.f, x3 = live ? h23.y : 0.f;
+        // tokens past S read token t0's row; their sums are never used
+        const float x0 = h01.x, x1 = h01.y, x2 = h23.x, x3 = h23.y;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float a = acc[i][t];
