@@ -857,6 +857,7 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
   if (threadIdx.x >= kCT) {
     if (threadIdx.x == kCT) {
       const uint64_t pol = evict_first_policy();
+      if (!a.weights_early) pdl_wait();
       produce_stage<NM>(a, gcount, S.slots0, S.full0, S.empty0, pol, c);
       producer_drain(gcount, S.full0, c.err);
     }

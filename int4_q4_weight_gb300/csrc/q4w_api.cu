@@ -200,7 +200,7 @@ int q4_gemv(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16,
     a.in = x_f16;
     a.in_mode = Q4_IN_F16;
     a.eps = 0.f;
-    return launch_stage(a, dev, s, false);
+    return launch_stage(a, dev, s, true);
   }
   return launch_gemv_batched(codes, reinterpret_cast<const __half*>(scales),
                              reinterpret_cast<const __half*>(x_f16), y, N, K, batch, dev, s);
@@ -242,7 +242,7 @@ int q4_gemv_stage(const q4_matrix* mats, const int* rows, int nmat, int K, const
   a.in_mode = in_mode;
   a.eps = eps;
   DEVICE_OR_RETURN(dev);
-  return launch_stage(a, dev, reinterpret_cast<cudaStream_t>(stream), false);
+  return launch_stage(a, dev, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 int q4_rmsnorm_f16(const float* in, int H, float eps, uint16_t* out_f16, q4_stream_t stream) {
@@ -342,6 +342,7 @@ int q4_decode_pass(const q4_layer* layers, int n_layers, int H, const uint16_t* 
     a.in = first ? static_cast<const void*>(h0_f16) : static_cast<const void*>(y32);
     a.in_mode = first ? Q4_IN_RMS_F16 : Q4_IN_RMS2_F32;
     a.eps = eps;
+    a.weights_early = !first;   // after the first launch the preceding kernel is one of ours
     int st = launch_stage(a, dev, s, !first);
     if (st != Q4_OK) return st;
     // o = W_o f16(q)
@@ -352,6 +353,7 @@ int q4_decode_pass(const q4_layer* layers, int n_layers, int H, const uint16_t* 
     b.in = q16;
     b.in_mode = Q4_IN_F16;
     b.eps = eps;
+    b.weights_early = 1;
     if ((st = launch_stage(b, dev, s, true)) != Q4_OK) return st;
     // m = f16(gelu(W_g b) * W_u b),  b = f16(RMSNorm(o))
     StageArgs c = {};
@@ -363,6 +365,7 @@ int q4_decode_pass(const q4_layer* layers, int n_layers, int H, const uint16_t* 
     c.in = o32;
     c.in_mode = Q4_IN_RMS_F32;
     c.eps = eps;
+    c.weights_early = 1;
     if ((st = launch_stage(c, dev, s, true)) != Q4_OK) return st;
     // y = W_down m
     StageArgs d = {};
@@ -372,6 +375,7 @@ int q4_decode_pass(const q4_layer* layers, int n_layers, int H, const uint16_t* 
     d.in = m16;
     d.in_mode = Q4_IN_F16;
     d.eps = eps;
+    d.weights_early = 1;
     if ((st = launch_stage(d, dev, s, true)) != Q4_OK) return st;
   }
   return launch_rmsnorm_f16(y32, H, eps, reinterpret_cast<__half*>(h_out_f16), s, true);

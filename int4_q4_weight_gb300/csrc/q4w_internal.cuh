@@ -54,6 +54,8 @@ struct StageArgs {
   float eps;
   int in_tag;        // > 0: `in` is tagged (as out16/out32 above); wait until every tag equals it
   int out_tag;       // tag written with tagged outputs
+  int weights_early; // 1: the weights are not written by the preceding kernel, so with programmatic
+                     // dependent launch they may be fetched before that kernel has finished
 };
 
 // Launches one fused stage (prologue + GEMV + epilogue).  `pdl` adds the
