@@ -415,6 +415,24 @@ def row_gemm(q4w, synth, dev, hbm, bf16_peak, N, K, reps=10):
             "us": round(t * 1e6, 2), "bytes": b, "flops": flops, "copies": copies}
 
 
+def row_q2(q4w, synth, dev, hbm, which, reps=10):
+    """INT2 GEMV of the mixed-bit recipe: the FFN gate/up shape streamed over
+    distinct weight copies totalling >= 4x L2, or the tied head (> L2 alone)."""
+    import torch
+    N, K = synth.Q2_SHAPES[which]
+    codes, scales, x = synth.q2_inputs(seed=1006, device=dev, N=N, K=K)
+    per = codes.numel() + 4 * N
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = 1 if per > 2 * l2 else max(8, math.ceil(4 * l2 / per))
+    cs = [(codes, scales)] + [(codes.clone(), scales.clone()) for _ in range(copies - 1)]
+    y = torch.empty(N, dtype=torch.float32, device=dev)
+    xv = x[0].contiguous()
+    t = _time_graph(lambda: [q4w.q2_gemv(c, s, xv, y) for c, s in cs], reps) / copies
+    b = per + 2 * K + 4 * N
+    return {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4), "us": round(t * 1e6, 3),
+            "bytes": b, "copies": copies}
+
+
 def measure_rows(q4w, synth, dev, hbm, clocks, bf16_peak):
     rows = {"gemv_2048x1536": row_gemv(q4w, synth, dev, hbm)}
     Wh, _ = synth.head_inputs(seed=1004, device=dev, batch=1)
@@ -427,10 +445,13 @@ def measure_rows(q4w, synth, dev, hbm, clocks, bf16_peak):
     for name, (N, K) in (("gemm_s64_up", (6144, 1536)), ("gemm_s64_down", (1536, 6144)),
                          ("gemm_s64_head", (262144, 1536))):
         rows[name] = row_gemm(q4w, synth, dev, hbm, bf16_peak, N, K)
+    rows["q2_gemv_12288x1536"] = row_q2(q4w, synth, dev, hbm, "gate")
+    rows["q2_gemv_head_262144x1536"] = row_q2(q4w, synth, dev, hbm, "head")
     return rows
 
 
-CASES = ("gemv", "head_b1", "head_b8", "ple", "gemm_up", "gemm_down", "gemm_head", "pass_trace")
+CASES = ("gemv", "head_b1", "head_b8", "ple", "gemm_up", "gemm_down", "gemm_head", "q2_gate", "q2_head",
+         "pass_trace")
 
 
 def pass_trace(q4w, synth, dev, reps):
@@ -528,6 +549,8 @@ def run_case(args):
         r = row_head(q4w, synth, dev, hbm, 1 if args.case == "head_b1" else 8, reps)
     elif args.case == "ple":
         r = row_ple(q4w, synth, dev, hbm, None, reps)
+    elif args.case in ("q2_gate", "q2_head"):
+        r = row_q2(q4w, synth, dev, hbm, args.case[3:], reps)
     elif args.case == "pass_trace":
         r = pass_trace(q4w, synth, dev, reps)
     else:

@@ -102,6 +102,20 @@ int q4_gemv(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16,
             float* y, int N, int K, int batch, void* ws, size_t ws_bytes,
             q4_stream_t stream);
 
+/* q2_gemv: INT2 per-row symmetric GEMV (the mixed-bit recipe's FFN of
+ * L15-L34 and tied head):  y[n] = scale[n] * sum_k (code[n][k] - 2) x[k],
+ * fp32 accumulation, the row scale applied once after the row sum.
+ * Source: "Gemma-4 E2B mobile mixed-bit QAT weights - extraction + Core AI
+ * transplant", The decode recipe (Section 10: INT2, 4 codes per byte, first
+ * code in bits[1:0], per-channel symmetric), P6 DONE (unsigned code minus the
+ * midpoint 2), P3 DONE (scale after the reduction).
+ *   codes: device [N][K/4] bytes; scales: device f32 [N]; x_f16: device [K];
+ *   y: device f32 [N].  All 16-byte aligned.  N >= 1; K % 64 == 0,
+ *   64 <= K <= 32768.  No workspace.  Asynchronous on `stream`.
+ *   Errors: Q4_ERR_NULL / Q4_ERR_ALIGN / Q4_ERR_SHAPE before any launch.  */
+int q2_gemv(const uint8_t* codes, const float* scales, const uint16_t* x_f16, float* y, int N, int K,
+            q4_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* S=64 chunked-prefill GEMM ("prefill", static query width 64).           */
 /* ---------------------------------------------------------------------- */

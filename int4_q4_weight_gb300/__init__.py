@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "load", "build", "Q4Error", "q4_quantize", "q4_gemv", "q4_gemv_stage", "q4_rmsnorm_f16",
-    "q4_decode_pass", "q4_decode_pass_launches", "lmhead_softcap_argmax", "ple_gather_project", "q4_gemm_chunk",
+    "q4_decode_pass", "q4_decode_pass_launches", "q2_gemv", "lmhead_softcap_argmax", "ple_gather_project", "q4_gemm_chunk",
     "q4_workspace_bytes", "q4_version", "Q4_IN_F16", "Q4_IN_RMS_F16", "Q4_IN_RMS_F32",
     "Q4_IN_RMS2_F32", "Q4_OP_GEMV", "Q4_OP_GEMM_CHUNK", "Q4_OP_PLE", "Q4_OP_LMHEAD",
     "Q4_OP_DECODE_PASS", "q4_layer", "q4_matrix",
@@ -55,6 +55,7 @@ _SIGS = {
     "lmhead_softcap_argmax_noalloc": (ci, [vp, vp, vp, ci, ci, ci, cf, vp, vp, vp, vp, vp]),
     "q4_decode_pass": (ci, [ctypes.POINTER(q4_layer), ci, ci, vp, vp, cf, vp, csz, vp]),
     "q4_decode_pass_launches": (ci, [ctypes.POINTER(q4_layer), ci, ci]),
+    "q2_gemv": (ci, [vp, vp, vp, vp, ci, ci, vp]),
     "q4_gemv_stage": (ci, [ctypes.POINTER(q4_matrix), ctypes.POINTER(ci), ci, ci, vp, ci, cf, ci,
                            ctypes.POINTER(vp), ctypes.POINTER(vp), vp]),
     "q4_rmsnorm_f16": (ci, [vp, ci, cf, vp, vp]),
@@ -323,6 +324,20 @@ def q4_gemm_chunk(codes, scales, X, Y=None):
     _check(lib.q4_gemm_chunk(_ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, N, K, _ptr(ws), nws,
                              _stream()), "q4_gemm_chunk")
     return Y
+
+
+def q2_gemv(codes, scales, x, y=None):
+    """INT2 per-row symmetric GEMV: y [N] f32 = scale[n] * sum_k (code - 2) x[k] (x fp16 [K])."""
+    lib = load()
+    _dev(codes, torch.uint8, "codes")
+    _dev(scales, torch.float32, "scales")
+    _dev(x, torch.float16, "x")
+    N, K = codes.shape[0], codes.shape[1] * 4
+    if y is None:
+        y = torch.empty(N, dtype=torch.float32, device=x.device)
+    _dev(y, torch.float32, "y")
+    _check(lib.q2_gemv(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), N, K, _stream()), "q2_gemv")
+    return y
 
 
 def q4_decode_pass_launches(descs, H):

@@ -102,6 +102,20 @@ def gemv_inputs(seed: int = 1001, device="cpu", N: int = GEMV_N, K: int = GEMV_K
     return W, x
 
 
+# INT2 shapes of the mixed-bit recipe: FFN gate/up and down of L15-L34, the tied head
+Q2_SHAPES = {"gate": (12288, 1536), "down": (1536, 12288), "head": (262144, 1536)}
+
+
+def q2_inputs(seed: int = 1006, device="cpu", N: int = 12288, K: int = 1536, batch: int = 1):
+    """INT2 weights drawn directly (the format comes from QAT, no quantiser):
+    codes [N, K/4] uint8 with every 2-bit code uniform in 0..3, per-row f32
+    scales 0.02 * (0.5 + U[0,1)), and x [batch, K] ~ N(0, 1) fp16."""
+    codes = randint((N, K // 4), 0, 255, sub_seed(seed, "codes", N, K), device, dtype=torch.int32).to(torch.uint8)
+    scales = uniform((N,), 0.01, 0.03, sub_seed(seed, "scales", N), device)
+    x = normal_f16((batch, K), sub_seed(seed, "x", batch, K), device)
+    return codes, scales, x
+
+
 @dataclass
 class PleInputs:
     ids: torch.Tensor        # int32 [S]

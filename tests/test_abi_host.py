@@ -100,6 +100,14 @@ def test_decode_pass_rejections(lib):
     assert lib.q4_decode_pass(ctypes.byref(layer), 1, 64, A, A, 1e-6, A, 16, None) == 4   # ws small
 
 
+def test_q2_gemv_rejections(lib):
+    assert lib.q2_gemv(None, A, A, A, 4, 64, None) == 1                 # NULL
+    assert lib.q2_gemv(A + 4, A, A, A, 4, 64, None) == 3                # alignment
+    assert lib.q2_gemv(A, A, A, A, 4, 96, None) == 2                    # K % 64
+    assert b"K=96" in lib.q4_last_error()
+    assert lib.q2_gemv(A, A, A, A, 0, 64, None) == 2                    # N
+
+
 def test_decode_pass_launch_count(lib):
     """One persistent launch when H <= 4096, every K a multiple of 256 up to
     12288 and at most 48 layers; otherwise one launch per stage plus the
