@@ -63,21 +63,30 @@ __global__ void __launch_bounds__(kThr) q2_gemv_kernel(const uint8_t* __restrict
                                                       int K, int lgP) {
   extern __shared__ __align__(16) uint32_t q2_smem[];
   const int nc = K >> 6;
-  // x half pairs per chunk: word i (16 columns), pair 4h + j
-  for (int e = threadIdx.x; e < nc * 32; e += kThr) {
-    const int ch = e >> 5, p = e & 31, i = p >> 3, hj = p & 7, h = hj >> 2, j = hj & 3;
-    const int k = 64 * ch + 16 * i + 4 * h + j;
-    q2_smem[ch * kChunkWords + p] =
-        (uint32_t)__half_as_ushort(x[k]) | ((uint32_t)__half_as_ushort(x[k + 8]) << 16);
+  // x half pairs per chunk: word i (16 columns), pair 4h + j.  A thread takes
+  // 8 consecutive halves x[16i + 8u .. 16i + 8u + 7] of one word half u: the
+  // low halves of pairs 4h + j (u = 0) or the high halves (u = 1).
+  for (int e = threadIdx.x; e < nc * 8; e += kThr) {
+    const int ch = e >> 3, i = (e >> 1) & 3, u = e & 1;
+    const uint4 v = *reinterpret_cast<const uint4*>(x + 64 * ch + 16 * i + 8 * u);
+    const uint32_t hv[4] = {v.x, v.y, v.z, v.w};
+    uint16_t* dst = reinterpret_cast<uint16_t*>(q2_smem + ch * kChunkWords + 8 * i) + u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {   // column 8u + c of the word -> half u of pair c
+      dst[2 * (2 * q)] = (uint16_t)(hv[q] & 0xFFFFu);
+      dst[2 * (2 * q + 1)] = (uint16_t)(hv[q] >> 16);
+    }
   }
+  __syncthreads();
+  // per-chunk bias from the staged pairs: -sum over pairs of (M_j + 2)(lo + hi)
   for (int ch = threadIdx.x; ch < nc; ch += kThr) {
+    const uint32_t* xp = q2_smem + ch * kChunkWords;
     float s = 0.f;
-    for (int i = 0; i < 4; ++i)
-      for (int h = 0; h < 2; ++h)
-        for (int j = 0; j < 4; ++j) {
-          const int k = 64 * ch + 16 * i + 4 * h + j;
-          s -= magic_offset(j) * (__half2float(x[k]) + __half2float(x[k + 8]));
-        }
+#pragma unroll
+    for (int p = 0; p < 32; ++p) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(xp + p));
+      s -= magic_offset(p & 3) * (f.x + f.y);
+    }
     q2_smem[ch * kChunkWords + 32] = __float_as_uint(s);
   }
   __syncthreads();
