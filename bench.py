@@ -359,6 +359,23 @@ def row_gemv(q4w, synth, dev, hbm, reps=10):
             "us_per_gemv_isolated_l2_resident": round(t_iso * 1e6, 3), "bytes": b, "copies": copies}
 
 
+def row_gemv_batch(q4w, synth, dev, hbm, batch=4, reps=10):
+    """[2048, 1536] GEMV of `batch` vectors (the S=4 verify shape), weights read
+    once per call, streamed over distinct weight copies totalling >= 4x L2."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    W, x = synth.gemv_inputs(seed=1001, device=dev, batch=batch)
+    c, s = q4w.q4_quantize(W)
+    per = c.numel() + s.numel() * 2
+    copies = max(8, math.ceil(4 * l2 / per))
+    cs = [(c.clone(), s.clone()) for _ in range(copies)]
+    y = torch.empty((batch, 2048), dtype=torch.float32, device=dev)
+    t = _time_graph(lambda: [q4w.q4_gemv(ci, si, x, y) for ci, si in cs], reps) / copies
+    b = per + 2 * 1536 * batch + 4 * 2048 * batch
+    return {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4), "us": round(t * 1e6, 3),
+            "batch": batch, "bytes": b, "copies": copies}
+
+
 def row_head(q4w, synth, dev, hbm, bsz, reps=20, weights=None):
     import torch
     if weights is None:
@@ -434,7 +451,8 @@ def row_q2(q4w, synth, dev, hbm, which, reps=10):
 
 
 def measure_rows(q4w, synth, dev, hbm, clocks, bf16_peak):
-    rows = {"gemv_2048x1536": row_gemv(q4w, synth, dev, hbm)}
+    rows = {"gemv_2048x1536": row_gemv(q4w, synth, dev, hbm),
+            "gemv_b4_2048x1536": row_gemv_batch(q4w, synth, dev, hbm, 4)}
     Wh, _ = synth.head_inputs(seed=1004, device=dev, batch=1)
     hw = q4w.q4_quantize(Wh)
     del Wh
@@ -450,7 +468,7 @@ def measure_rows(q4w, synth, dev, hbm, clocks, bf16_peak):
     return rows
 
 
-CASES = ("gemv", "head_b1", "head_b8", "ple", "gemm_up", "gemm_down", "gemm_head", "q2_gate", "q2_head",
+CASES = ("gemv", "gemv_b4", "head_b1", "head_b8", "ple", "gemm_up", "gemm_down", "gemm_head", "q2_gate", "q2_head",
          "pass_trace")
 
 
@@ -545,6 +563,8 @@ def run_case(args):
     reps = max(1, args.steps)
     if args.case == "gemv":
         r = row_gemv(q4w, synth, dev, hbm, reps)
+    elif args.case == "gemv_b4":
+        r = row_gemv_batch(q4w, synth, dev, hbm, 4, reps)
     elif args.case in ("head_b1", "head_b8"):
         r = row_head(q4w, synth, dev, hbm, 1 if args.case == "head_b1" else 8, reps)
     elif args.case == "ple":

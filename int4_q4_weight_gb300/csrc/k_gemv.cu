@@ -322,7 +322,11 @@ static cudaError_t launch_batched_t(const uint8_t* codes, const __half* scales, 
 
 int launch_gemv_batched(const uint8_t* codes, const __half* scales, const __half* x, float* y,
                         int N, int K, int batch, const DeviceInfo& dev, cudaStream_t s) {
-  // Split the batch into launches whose x fits in shared memory.
+  // Batch 2..8 with x staged whole: each weight block decoded once for all
+  // batch rows (the batched head's kernel).
+  if (batch >= 2 && batch <= 8 && head_batch_smem(batch, K) <= (size_t)220 * 1024)
+    return launch_gemv_batch_decoded(codes, scales, x, y, N, K, batch, dev, s);
+  // Otherwise split the batch into launches whose x fits in shared memory.
   const size_t per_row = (size_t)(K >> 5) * kXStride * sizeof(float);
   int chunk = (int)((size_t)200 * 1024 / per_row);
   if (chunk < 1) return fail(Q4_ERR_SHAPE, "K=%d too large for the batched GEMV", K);

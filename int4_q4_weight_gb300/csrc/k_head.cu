@@ -171,10 +171,9 @@ __global__ void __launch_bounds__(kThreads) head_batched_kernel(const uint8_t* _
   head_finish(partials, ticket, B, cap, idx, top1, top2);
 }
 
-size_t head_batch_smem(int b, int K);
 int launch_head_batch(const uint8_t* codes, const __half* scales, const __half* h, int b, int V, int K, float cap,
                       int32_t* idx, float* top1, float* top2, float* logits, Top2* partials, unsigned* ticket,
-                      int grid, cudaStream_t s);
+                      int grid, cudaStream_t s, float* ydirect = nullptr);
 
 static int lpr_for(int nb) {
   int l = 32;

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
                                                          const __half* __restrict__ h, int B, int V, int K,
                                                          int lgP, float cap, float* __restrict__ logits,
                                                          Top2* partials, unsigned* ticket, int32_t* idx,
-                                                         float* top1, float* top2) {
+                                                         float* top1, float* top2, float* __restrict__ ydirect) {
   extern __shared__ __align__(16) uint32_t hb_smem[];
   const int nb = K >> 5;
   const int xstride = 16 * NBP + 4;           // words per block (+4: lanes of a group hit other banks)
@@ -140,12 +140,17 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
 #pragma unroll
       for (int b = 0; b < NBP; ++b) {
         if (b < B) {
-          top2_insert(best[b], acc[b], row);
-          if (logits) logits[(size_t)b * V + row] = cap * tanhf(acc[b] / cap);
+          if (ydirect) {   // batched GEMV: the raw row sums
+            ydirect[(size_t)b * V + row] = acc[b];
+          } else {
+            top2_insert(best[b], acc[b], row);
+            if (logits) logits[(size_t)b * V + row] = cap * tanhf(acc[b] / cap);
+          }
         }
       }
     }
   }
+  if (ydirect) return;   // uniform over the grid
   // groups of a warp -> lane 0, warps -> the CTA's partial per batch row
 #pragma unroll
   for (int b = 0; b < NBP; ++b)
@@ -182,9 +187,11 @@ size_t head_batch_smem(int b, int K) {
   return bytes;
 }
 
+// ydirect != nullptr: batched GEMV, ydirect[b][row] = the row sums (no
+// softcap, no selection; partials, ticket, idx, top1, top2 unused).
 int launch_head_batch(const uint8_t* codes, const __half* scales, const __half* h, int b, int V, int K, float cap,
                       int32_t* idx, float* top1, float* top2, float* logits, Top2* partials, unsigned* ticket,
-                      int grid, cudaStream_t s) {
+                      int grid, cudaStream_t s, float* ydirect) {
   const int lgP = head_batch_lgp(K >> 5);
   const size_t smem = head_batch_smem(b, K);
   cudaError_t e;
@@ -201,7 +208,7 @@ int launch_head_batch(const uint8_t* codes, const __half* scales, const __half* 
     if (e == cudaSuccess && per_sm > 0 && grid > sms * per_sm) grid = sms * per_sm;
     if (e == cudaSuccess)
       hb::head_batch_kernel<4><<<grid, hb::kThr, smem, s>>>(codes, scales, h, b, V, K, lgP, cap, logits, partials,
-                                                           ticket, idx, top1, top2);
+                                                           ticket, idx, top1, top2, ydirect);
   } else {
     e = cudaFuncSetAttribute(hb::head_batch_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess)
@@ -209,10 +216,23 @@ int launch_head_batch(const uint8_t* codes, const __half* scales, const __half* 
     if (e == cudaSuccess && per_sm > 0 && grid > sms * per_sm) grid = sms * per_sm;
     if (e == cudaSuccess)
       hb::head_batch_kernel<8><<<grid, hb::kThr, smem, s>>>(codes, scales, h, b, V, K, lgP, cap, logits, partials,
-                                                           ticket, idx, top1, top2);
+                                                           ticket, idx, top1, top2, ydirect);
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? Q4_OK : cuda_fail(e, "batched head launch");
+}
+
+// Batched GEMV (batch 2..8) through the same kernel: y[b][n] = sum_k W[n][k] x[b][k].
+// Returns Q4_ERR_SHAPE when the x staging does not fit in shared memory.
+int launch_gemv_batch_decoded(const uint8_t* codes, const __half* scales, const __half* x, float* y, int N, int K,
+                              int batch, const DeviceInfo& dev, cudaStream_t s) {
+  if (batch < 2 || batch > 8 || head_batch_smem(batch, K) > (size_t)220 * 1024)
+    return fail(Q4_ERR_SHAPE, "batched GEMV: batch %d x K %d does not fit", batch, K);
+  int grid = 2 * dev.sms;
+  const int need = (N + 7) / 8;
+  if (grid > need) grid = need;
+  return launch_head_batch(codes, scales, x, batch, N, K, 1.f, nullptr, nullptr, nullptr, nullptr, nullptr,
+                           nullptr, grid, s, y);
 }
 
 }  // namespace q4w

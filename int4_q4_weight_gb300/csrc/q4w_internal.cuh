@@ -86,6 +86,9 @@ void* trace_buffer(size_t* bytes);
 int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const __half* h0, __half* h_out,
                               float eps, float* kv32, void* tagged, size_t tagged_bytes, int* ctl,
                               const DeviceInfo& dev, cudaStream_t s);
+size_t head_batch_smem(int b, int K);
+int launch_gemv_batch_decoded(const uint8_t* codes, const __half* scales, const __half* x, float* y, int N, int K,
+                              int batch, const DeviceInfo& dev, cudaStream_t s);
 size_t gemm_ws_bytes(int K);   // the bf16 copy of X [64][K]
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s);
