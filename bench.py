@@ -394,7 +394,7 @@ def row_head(q4w, synth, dev, hbm, bsz, reps=20, weights=None):
             "bytes": b}
 
 
-def row_ple(q4w, synth, dev, hbm, clocks, reps=10):
+def row_ple(q4w, synth, dev, hbm, bf16_peak, reps=10):
     import torch
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     p = synth.ple_inputs(seed=1002, device=dev)
@@ -405,12 +405,13 @@ def row_ple(q4w, synth, dev, hbm, clocks, reps=10):
                                                     p.norm_w, out=out) for pj in projs], reps) / ncp
     b = 64 * 8960 + 64 * 4 + p.proj.numel() * 4 + 64 * 1536 * 2 + 256 * 4 + 64 * 8960 * 4 + 64 * 4
     flops = 2 * 64 * 8960 * 1536
-    sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
-    fp32_peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * sm_mhz * 1e6
-    return {"GB/s": round(b / t / 1e9, 1), "TFLOP/s": round(flops / t / 1e12, 2),
-            "fp32_peak_TFLOP/s": round(fp32_peak / 1e12, 1),
-            "frac": round(max(b / t / 1e9 / hbm, flops / t / fp32_peak), 4),
-            "bound": "alu (fp32 FFMA)", "us": round(t * 1e6, 2), "bytes": b}
+    # TF32 peak: the measured bf16 peak x the nominal dense TF32 / BF16 ratio (1.1 / 2.25)
+    tf32_peak = bf16_peak * 1.1 / 2.25
+    return {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4),
+            "TFLOP/s": round(flops / t / 1e12, 2), "tf32_peak_TFLOP/s": round(tf32_peak, 1),
+            "frac_tf32": round(flops / t / 1e12 / tf32_peak, 4),
+            "bound": "hbm (projection on the tensor cores, kind::tf32)", "us": round(t * 1e6, 2), "bytes": b,
+            "copies": ncp}
 
 
 def row_gemm(q4w, synth, dev, hbm, bf16_peak, N, K, reps=10):
@@ -459,7 +460,7 @@ def measure_rows(q4w, synth, dev, hbm, clocks, bf16_peak):
     rows["lmhead_b1"] = row_head(q4w, synth, dev, hbm, 1, weights=hw)
     rows["lmhead_b8"] = row_head(q4w, synth, dev, hbm, 8, weights=hw)
     del hw
-    rows["ple_s64"] = row_ple(q4w, synth, dev, hbm, clocks)
+    rows["ple_s64"] = row_ple(q4w, synth, dev, hbm, bf16_peak)
     for name, (N, K) in (("gemm_s64_up", (6144, 1536)), ("gemm_s64_down", (1536, 6144)),
                          ("gemm_s64_head", (262144, 1536))):
         rows[name] = row_gemm(q4w, synth, dev, hbm, bf16_peak, N, K)
@@ -568,7 +569,7 @@ def run_case(args):
     elif args.case in ("head_b1", "head_b8"):
         r = row_head(q4w, synth, dev, hbm, 1 if args.case == "head_b1" else 8, reps)
     elif args.case == "ple":
-        r = row_ple(q4w, synth, dev, hbm, None, reps)
+        r = row_ple(q4w, synth, dev, hbm, bf16, reps)
     elif args.case in ("q2_gate", "q2_head"):
         r = row_q2(q4w, synth, dev, hbm, args.case[3:], reps)
     elif args.case == "pass_trace":

@@ -538,9 +538,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D row-major tensor [rows][cols] of 1- or 2-byte elements, one box per load.
-static int encode_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type, int esize, uint64_t cols,
-                     uint64_t rows, uint32_t box_cols, uint32_t box_rows, const char* what) {
+// 2-D row-major tensor [rows][cols] of esize-byte elements, one box per load.
+int encode_tensor_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type, int esize, uint64_t cols,
+                     uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle,
+                     const char* what) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[2] = {cols, rows};
@@ -548,8 +549,7 @@ static int encode_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(tm, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(Q4_ERR_CUDA, "tensor map for %s: driver error %d", what, (int)r);
   return Q4_OK;
 }
@@ -561,15 +561,15 @@ int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* 
   (void)M;
   gemm::Params p;
   memset(&p, 0, sizeof(p));
-  int st = encode_2d(&p.tm_codes, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N,
-                     gemm::kChunk * gemm::kRawChunks / 2, gemm::kTileM, "codes");
+  int st = encode_tensor_2d(&p.tm_codes, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N,
+                            gemm::kChunk * gemm::kRawChunks / 2, gemm::kTileM, CU_TENSOR_MAP_SWIZZLE_NONE, "codes");
   if (st != Q4_OK) return st;
   p.xb = static_cast<const uint8_t*>(ws);
   p.scales = scales;
   p.sc_tma = K % 256 == 0;
   if (p.sc_tma) {
-    st = encode_2d(&p.tm_sc, scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)K / 32, (uint64_t)N, 8,
-                   gemm::kTileM, "scales");
+    st = encode_tensor_2d(&p.tm_sc, scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)K / 32, (uint64_t)N, 8,
+                          gemm::kTileM, CU_TENSOR_MAP_SWIZZLE_NONE, "scales");
     if (st != Q4_OK) return st;
   }
   p.Y = Y;

@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libq4w.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -89,6 +90,11 @@ int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const
 size_t head_batch_smem(int b, int K);
 int launch_gemv_batch_decoded(const uint8_t* codes, const __half* scales, const __half* x, float* y, int N, int K,
                               int batch, const DeviceInfo& dev, cudaStream_t s);
+// Tensor map of a 2-D row-major [rows][cols] array (esize-byte elements) with
+// boxes of box_rows x box_cols; Q4_OK or an error status naming `what`.
+int encode_tensor_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type, int esize, uint64_t cols,
+                     uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle,
+                     const char* what);
 size_t gemm_ws_bytes(int K);   // the bf16 copy of X [64][K]
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s);

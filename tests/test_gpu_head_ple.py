@@ -107,6 +107,21 @@ def test_ple_small(cuda_lib, S, V, L, D):
     _ple_check(cuda_lib, p, L)
 
 
+@pytest.mark.parametrize("S,V,L,D", [(130, 900, 2, 96), (65, 300, 3, 1536)])
+def test_ple_token_groups(cuda_lib, S, V, L, D):
+    # several 64-token groups with a ragged last group
+    p = synth.ple_inputs(seed=94, device="cuda", S=S, V=V, L=L, D=D)
+    _ple_check(cuda_lib, p, L)
+
+
+def test_ple_projection_term_alone(cuda_lib):
+    # zero table bytes: out is the normalised projection alone, so the TF32
+    # projection error is not hidden behind the larger gathered term
+    p = synth.ple_inputs(seed=93, device="cuda", S=64, V=512, L=35, D=1536)
+    p.table.zero_()
+    _ple_check(cuda_lib, p, 35)
+
+
 def test_ple_proj_zero_bit_exact(cuda_lib):
     p = synth.ple_inputs(seed=91, device="cuda", S=20, V=700, L=4, D=96)
     p.proj.zero_()
