@@ -11,26 +11,32 @@
 // The fp16 hidden values are exact in TF32; the f32 projection enters with a
 // 10-bit mantissa (the tensor core reads the top 19 bits of each fp32 word).
 //
-// One CTA per (128-row half of a 256-row layer chunk, group of 64 tokens);
-// the two halves of a chunk form a cluster of two and swap their per-token
-// sums of squares through distributed shared memory, so each finishes the
-// chunk's RMSNorm for its own rows and adds the gathered table term in the
-// same epilogue.
+// A 256-row layer chunk and a group of up to 64 tokens belong to a cluster of
+// four CTAs: rank r = m + 2 kh takes the 128-row half m of the chunk over the
+// K half kh of the hidden width.  The two K halves of a row half swap the
+// partial sums of the rows the other one finishes (64 rows each) through
+// distributed shared memory and add them in a fixed order; then every CTA
+// sends its per-token sum of squares over its 64 finished rows to all four,
+// so each finishes the chunk's RMSNorm for its own rows and adds the
+// gathered table term in the same epilogue.
 //
 // Warp roles (192 threads):
-//   warp 0     one thread issuing the TMA loads: the projection tile [128
-//              rows][32 fp32] (128-byte swizzle, the tensor core's K-major
-//              layout) and the hidden tile [64 tokens][32 fp16]
-//   warp 1     TMEM allocation and the single thread issuing the MMAs
-//   warps 2-5  widen the hidden tile to fp32 in the 128-byte swizzle layout
+//   warp 0     TMA loads (one elected lane): per stage two K sub-chunks of
+//              32 columns, each a projection tile [128 rows][32 fp32]
+//              (128-byte swizzle, the tensor core's K-major layout) and a
+//              hidden tile [64 tokens][32 fp16]
+//   warp 1     TMEM allocation; the warp runs the MMA loop together and one
+//              elected lane issues the MMAs (8 per stage) and the commits
+//   warps 2-5  widen the hidden tiles to fp32 in the 128-byte swizzle layout
 //              (the B operand), then run the epilogue on their TMEM lane
 //              quarters (warp w reads lanes 32 (w % 4) .. + 31)
-// A ring of kStages stages (A 16 KB + B 8 KB + hidden 4 KB) is guarded by
-// full (TMA bytes), bready (converter warps) and empty (MMA commit)
-// mbarriers.  Every mbarrier wait is bounded; on expiry the CTA sets its
-// abort flag and the device error word, every role leaves its loop, work in
-// flight is drained, and both CTAs of the cluster still meet at the cluster
-// barriers, so neither waits for a partner that has given up.
+// A ring of kStages stages (A 32 KB + B 16 KB + hidden 8 KB) is guarded by
+// full (TMA bytes), bready (converter warps, which arrive only after seeing
+// full) and empty (MMA commit) mbarriers; the MMA warp waits on bready alone.
+// Every mbarrier wait is bounded; on expiry the CTA sets its abort flag and
+// the device error word, every role leaves its loop, work in flight is
+// drained, and all four CTAs still meet at every cluster barrier, so none
+// waits for a partner that has given up.
 #include "q4w_device.cuh"
 #include "q4w_internal.cuh"
 #include "q4w_tc.cuh"
@@ -42,16 +48,20 @@ namespace ple {
 constexpr int kLd = 256;                            // rows of one layer chunk
 constexpr int kRows = 128;                          // rows per CTA (MMA M)
 constexpr int kTok = 64;                            // tokens per CTA (MMA N <= 64)
-constexpr int kKC = 32;                             // K columns per stage (128 B of fp32)
-constexpr int kStages = 6;
-constexpr int kABytes = kRows * kKC * 4;            // 16 KB
-constexpr int kBBytes = kTok * kKC * 4;             // 8 KB
-constexpr int kHBytes = kTok * kKC * 2;             // 4 KB
-constexpr int kStageBytes = kABytes + kBBytes + kHBytes;   // 28 KB, a multiple of 1024
+constexpr int kKC = 32;                             // K columns per sub-chunk (128 B of fp32)
+constexpr int kSub = 2;                             // sub-chunks per stage
+constexpr int kStages = 3;
+constexpr int kABytes = kRows * kKC * 4;            // 16 KB per sub-chunk
+constexpr int kBBytes = kTok * kKC * 4;             // 8 KB per sub-chunk
+constexpr int kHBytes = kTok * kKC * 2;             // 4 KB per sub-chunk
+constexpr int kStageBytes = kSub * (kABytes + kBBytes + kHBytes);   // 56 KB, a multiple of 1024
+constexpr int kRecvBytes = kTok * 64 * 4;           // partner's partial sums of 64 rows
+constexpr int kGtabBytes = kTok * 64;               // table bytes of the 64 finished rows per token
 constexpr int kThreads = 192;
 constexpr int kEpi0 = 2;                            // first converter / epilogue warp
 constexpr int kTmemCols = 64;
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes;
+constexpr int kCluster = 4;
+constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kRecvBytes + kGtabBytes;
 constexpr long long kDrainCycles = 2000000000LL;
 
 // Instruction descriptor, kind::tf32: D f32, A and B tf32, both K-major,
@@ -83,10 +93,10 @@ struct Params {
   int S, V, L, D;
   float embed_scale, eps;
   long long wait_limit;
-  unsigned long long* trace;   // optional: CTA 0 stamps [chunk][8], SM cycles since the start
+  unsigned long long* trace;   // optional: CTA 0 stamps [stage][8], SM cycles since the start
 };
 
-constexpr int kTraceChunks = 256;
+constexpr int kTraceRows = 256;
 
 // Sum over the 32 lanes of v[0..15] for 16 tokens: a halving exchange leaves
 // lanes 2i and 2i+1 with the total of token i (16 shuffles instead of 80).
@@ -105,39 +115,58 @@ __device__ __forceinline__ float lane_token_sums16(float (&v)[16], int lane) {
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n .reg .pred P;\n .reg .b32 R;\n elect.sync R|P, 0xffffffff;\n selp.b32 %0, 1, 0, P;\n}"
+               : "=r"(pred));
+  return pred != 0;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t bars[3 * kStages + 2];   // full, bready, empty, accfull, drain
+  // partner's partial sums, [token / 4][64 rows][4 tokens]
+  float* recv = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
+  // table bytes of this CTA's 64 finished rows, [token][64]
+  int8_t* gtab = reinterpret_cast<int8_t*>(smem + (size_t)kStages * kStageBytes + kRecvBytes);
+  __shared__ __align__(8) uint64_t bars[3 * kStages + 3];   // full, bready, empty, accfull, drain, gbar
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
-  __shared__ float red[4][kTok];     // per epilogue warp: per-token sums of squares over its 32 rows
-  __shared__ float ssq_peer[kTok];   // written by the other half of the chunk
-  __shared__ float rfac[kTok];       // per-token RMS factor
-  __shared__ float tsc[kTok];        // per-token table scale (0 for a bad id)
-  __shared__ int tid_sh[kTok];       // per-token id (-1: out of range)
   __shared__ long long t0_sh;
+  __shared__ float red[2][kTok];            // per finishing warp: per-token sums of squares over 32 rows
+  __shared__ float ssq_in[kCluster][kTok];  // per cluster rank: sums over its 64 finished rows
+  __shared__ float rfac[kTok];              // per-token RMS factor
+  __shared__ float tsc[kTok];               // per-token table scale (0 for a bad id)
+  __shared__ int tid_sh[kTok];              // per-token id (-1: out of range)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = blockIdx.x & 1;                 // rank in the cluster of two
-  const int chunk = blockIdx.x >> 1;
-  const int row0 = chunk * kLd + half * kRows;     // first projection row of this CTA
+  const int rank = blockIdx.x & (kCluster - 1);
+  const int m = rank & 1, kh = rank >> 1;          // row half, K half
+  const int chunk = blockIdx.x / kCluster;
+  const int row0 = chunk * kLd + m * kRows;        // first projection row of this CTA
   const int t0 = blockIdx.y * kTok;
   const int ntok = min(kTok, p.S - t0);
   const int npad = (ntok + 15) & ~15;
-  const int nk = p.D / kKC;
+  const int nsub = p.D / kKC;
+  const int sb = kh == 0 ? 0 : (nsub + 1) / 2, se = kh == 0 ? (nsub + 1) / 2 : nsub;   // my sub-chunks
+  const int ns = (se - sb + kSub - 1) / kSub;      // my stages (0 only when D has one sub-chunk)
   const int PLD = p.L * kLd;
   const uint32_t full0 = tc::smem_u32(bars), bready0 = full0 + 8 * kStages, empty0 = bready0 + 8 * kStages;
-  const uint32_t accfull = empty0 + 8 * kStages, drain = accfull + 8;
+  const uint32_t accfull = empty0 + 8 * kStages, drain = accfull + 8, gbar = drain + 8;
   volatile int* abort_flag = &abort_sh;
   unsigned long long* const tr = (p.trace && blockIdx.x == 0 && blockIdx.y == 0) ? p.trace : nullptr;
-  auto stamp = [&](int c, int k) {
-    if (tr && c < kTraceChunks) tr[c * 8 + k] = (unsigned long long)(clock64() - t0_sh);
+  // with a trace: every CTA's start and end (globaltimer ns) after the stage stamps
+  unsigned long long* const trc =
+      p.trace ? p.trace + kTraceRows * 8 + 2 * ((size_t)blockIdx.y * gridDim.x + blockIdx.x) : nullptr;
+  auto stamp = [&](int r, int k) {
+    if (tr && r < kTraceRows) tr[r * 8 + k] = (unsigned long long)(clock64() - t0_sh);
   };
+  auto nsc_of = [&](int st) { return min(kSub, se - sb - kSub * st); };
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
     t0_sh = clock64();
+    if (trc) trc[0] = tc::globaltimer();
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(full0 + 8 * s, 1);
       tc::mbar_init(bready0 + 8 * s, 4);
@@ -145,9 +174,15 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     }
     tc::mbar_init(accfull, 1);
     tc::mbar_init(drain, 1);
+    tc::mbar_init(gbar, 1);
     tc::mbar_fence_init();
   }
   if (warp == 1) tc::tmem_alloc(tc::smem_u32(&tmem_sh), kTmemCols);
+  // programmatic dependent launch: the next kernel in the stream may be
+  // scheduled now; this one reads its inputs only after the previous
+  // kernel's results are visible
+  pdl_trigger();
+  pdl_wait();
   if (threadIdx.x >= kEpi0 * 32 && threadIdx.x < kEpi0 * 32 + kTok) {
     const int t = threadIdx.x - kEpi0 * 32;
     int id = -1;
@@ -167,157 +202,240 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  // the peer CTA has started before anyone stores into its shared memory
-  // (this phase is waited for just before the exchange)
+  // cluster phase 1: every CTA of the cluster has started before anyone
+  // stores into a peer's shared memory (waited for just before the first store)
   tc::cluster_arrive_relaxed();
   const uint32_t tmem = tmem_sh;
 
   if (warp == 0) {
     // ------------------------------------------------------------- TMA loads
-    if (lane == 0) {
-      const uint64_t pol_once = tc::policy_evict_first(), pol_keep = tc::policy_evict_last();
-      const uint32_t st0 = tc::smem_u32(smem);
-      int c = 0;
-      for (; c < nk; ++c) {
-        const int s = c % kStages, round = c / kStages;
-        if (!tc::mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, p.dev_err)) break;
-        const uint32_t A = st0 + s * kStageBytes, H = A + kABytes + kBBytes;
-        stamp(c, 0);
-        tc::mbar_expect_tx(full0 + 8 * s, kABytes + kHBytes);
-        // x = 32 c fp32 (128 c bytes) and 32 c fp16 (64 c bytes): 16-byte aligned
-        tc::tma_load_2d(A, &p.tm_proj, c * kKC, row0, full0 + 8 * s, pol_once);
-        tc::tma_load_2d(H, &p.tm_hid, c * kKC, t0, full0 + 8 * s, pol_keep);
+    const uint64_t pol_once = tc::policy_evict_first(), pol_keep = tc::policy_evict_last();
+    const uint32_t st0 = tc::smem_u32(smem);
+    int st = 0;
+    for (; st < ns; ++st) {
+      const int s = st % kStages, round = st / kStages;
+      const bool free_ = tc::mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, p.dev_err);
+      if (!__all_sync(0xffffffffu, free_)) break;
+      if (elect_one()) {
+        const int nsc = nsc_of(st);
+        const uint32_t A = st0 + s * kStageBytes, H = A + kSub * (kABytes + kBBytes);
+        stamp(st, 0);
+        tc::mbar_expect_tx(full0 + 8 * s, (uint32_t)nsc * (kABytes + kHBytes));
+        for (int a = 0; a < nsc; ++a) {
+          // x = 32 (sb + 2 st + a) fp32 / fp16 columns: 16-byte aligned
+          const int x = (sb + kSub * st + a) * kKC;
+          tc::tma_load_2d(A + a * kABytes, &p.tm_proj, x, row0, full0 + 8 * s, pol_once);
+          tc::tma_load_2d(H + a * kHBytes, &p.tm_hid, x, t0, full0 + 8 * s, pol_keep);
+        }
       }
-      // every issued load lands before the CTA may exit
-      for (int q = max(0, c - kStages); q < c; ++q)
-        tc::mbar_drain(full0 + 8 * (q % kStages), (q / kStages) & 1, kDrainCycles, p.dev_err);
+      __syncwarp();
     }
-    __syncwarp();
+    // every issued load lands before the CTA may exit
+    for (int q = max(0, st - kStages); q < st; ++q)
+      tc::mbar_drain(full0 + 8 * (q % kStages), (q / kStages) & 1, kDrainCycles, p.dev_err);
+    tc::mbar_drain(gbar, 0, kDrainCycles, p.dev_err);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t st0 = tc::smem_u32(smem);
-      const uint32_t idesc = idesc_tf32(npad);
-      bool ok = true;
-      for (int c = 0; c < nk && ok; ++c) {
-        const int s = c % kStages, round = c / kStages;
-        if (!tc::mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err) ||
-            !tc::mbar_wait(bready0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after();
-        stamp(c, 3);
-        const uint32_t A = st0 + s * kStageBytes, B = A + kABytes;
-#pragma unroll
-        for (int k = 0; k < kKC / 8; ++k)   // K = 8 tf32 (32 bytes) per MMA
-          mma_tf32(tmem, tc::desc_sw128(A + 32 * k), tc::desc_sw128(B + 32 * k), idesc, (c | k) ? 1u : 0u);
-        tc::commit(empty0 + 8 * s);
-        stamp(c, 4);
+    const uint32_t st0 = tc::smem_u32(smem);
+    const uint32_t idesc = idesc_tf32(npad);
+    bool ok = true;
+    for (int st = 0; st < ns; ++st) {
+      const int s = st % kStages, round = st / kStages;
+      // bready completes only after the converter warps have seen this
+      // stage's TMA bytes land (full), so it orders the projection tile too
+      ok = tc::mbar_wait(bready0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
       }
-      if (ok) tc::commit(accfull);
+      tc::fence_after();
+      if (elect_one()) {
+        stamp(st, 3);
+        const int nsc = nsc_of(st);
+        const uint32_t A = st0 + s * kStageBytes, B = A + kSub * kABytes;
+        for (int a = 0; a < nsc; ++a) {
+#pragma unroll
+          for (int k = 0; k < kKC / 8; ++k)   // K = 8 tf32 (32 bytes) per MMA
+            mma_tf32(tmem, tc::desc_sw128(A + a * kABytes + 32 * k), tc::desc_sw128(B + a * kBBytes + 32 * k), idesc,
+                     (st | a | k) ? 1u : 0u);
+        }
+        tc::commit(empty0 + 8 * s);
+        stamp(st, 4);
+      }
+      __syncwarp();
+    }
+    if (elect_one()) {
+      if (ok && ns > 0) tc::commit(accfull);
       // every tcgen05 operation issued here has finished before TMEM is freed
       tc::commit(drain);
-      tc::mbar_drain(drain, 0, kDrainCycles, p.dev_err);
     }
     __syncwarp();
+    tc::mbar_drain(drain, 0, kDrainCycles, p.dev_err);
   } else {
     // ------------------------------------- B operand: fp16 hidden -> fp32 tile
     const int ct = threadIdx.x - kEpi0 * 32;   // 0..127
+    // the table bytes of the finished rows: one 64-byte copy per valid token,
+    // issued by that token's thread (column row0 + 64 kh and the row width
+    // L * 256 are multiples of 16 bytes); thread 0 posts the byte count
+    if (ct < ntok && tid_sh[ct] >= 0)
+      tc::bulk_load(tc::smem_u32(gtab + ct * 64), p.table + (size_t)tid_sh[ct] * PLD + (size_t)row0 + 64 * kh, 64,
+                    gbar, tc::policy_evict_first());
+    if (ct == 0) {
+      uint32_t nb = 0;
+      for (int t = 0; t < ntok; ++t) nb += tid_sh[t] >= 0 ? 64u : 0u;
+      tc::mbar_expect_tx(gbar, nb);
+    }
     bool ok = true;
-    for (int c = 0; c < nk; ++c) {
-      const int s = c % kStages, round = c / kStages;
+    for (int st = 0; st < ns; ++st) {
+      const int s = st % kStages, round = st / kStages;
       const bool landed = tc::mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
       if (!__all_sync(0xffffffffu, landed)) {   // leave the loop as a whole warp
         ok = false;
         break;
       }
-      if (ct == 0) stamp(c, 1);
-      uint8_t* st = smem + (size_t)s * kStageBytes;
-      uint8_t* B = st + kABytes;
-      const uint8_t* H = B + kBBytes;
+      if (ct == 0) stamp(st, 1);
+      uint8_t* B = smem + (size_t)s * kStageBytes + kSub * kABytes;
+      const uint8_t* H = B + kSub * kBBytes;
+      const int nsc = nsc_of(st);
+      for (int a = 0; a < nsc; ++a) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int idx = ct + 128 * i;      // (token t, 16-byte group j of its 128-byte row)
-        const int t = idx >> 3, j = idx & 7;
-        // tokens past S: zero rows (the tensor map already reads them as zero)
-        const uint2 h = t < ntok ? *reinterpret_cast<const uint2*>(H + t * (kKC * 2) + j * 8) : make_uint2(0u, 0u);
-        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
-        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
-        // 128-byte swizzle: group j of row t sits at group j ^ (t % 8) of its row
-        *reinterpret_cast<float4*>(B + (t >> 3) * 1024 + (t & 7) * 128 + ((j ^ (t & 7)) << 4)) =
-            make_float4(a.x, a.y, b.x, b.y);
+        for (int i = 0; i < 4; ++i) {
+          const int idx = ct + 128 * i;      // (token t, 16-byte group j of its 128-byte row)
+          const int t = idx >> 3, j = idx & 7;
+          // tokens past S: zero rows (the tensor map already reads them as zero)
+          const uint2 h = t < ntok ? *reinterpret_cast<const uint2*>(H + a * kHBytes + t * (kKC * 2) + j * 8)
+                                   : make_uint2(0u, 0u);
+          const float2 x0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+          const float2 x1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+          // 128-byte swizzle: group j of row t sits at group j ^ (t % 8) of its row
+          *reinterpret_cast<float4*>(B + a * kBBytes + (t >> 3) * 1024 + (t & 7) * 128 + ((j ^ (t & 7)) << 4)) =
+              make_float4(x0.x, x0.y, x1.x, x1.y);
+        }
       }
       tc::fence_proxy_async();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(bready0 + 8 * s);
-      if (ct == 0) stamp(c, 2);
+      if (ct == 0) stamp(st, 2);
     }
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;                    // TMEM lane quarter
     const int row = 32 * q + lane;             // row of this CTA's tile
+    const bool mine = (q >> 1) == kh;          // rows 64 kh .. 64 kh + 63 are finished here
+    const int r64 = row & 63;
     const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
-    if (ok) ok = tc::mbar_wait(accfull, 0, p.wait_limit, abort_flag, p.dev_err, 128);
-    ok = __all_sync(0xffffffffu, ok);   // the TMEM loads below are warp-wide
+    const bool has = ns > 0;                   // without K work the partial sums are zero
+    if (ok && has) ok = tc::mbar_wait(accfull, 0, p.wait_limit, abort_flag, p.dev_err, 128);
+    ok = __all_sync(0xffffffffu, ok);          // the TMEM loads below are warp-wide
     tc::fence_after();
-    if (ct == 0) stamp(0, 5);
-    if (ok) {
+    if (ct == 0) stamp(kTraceRows - 1, 5);
+    tc::cluster_wait();                        // phase 1: every peer is running
+    if (!mine) {                               // the partner finishes these rows
+      const uint32_t peer = tc::cluster_addr(recv, (uint32_t)(rank ^ 2));
       for (int cb = 0; cb < npad / 16; ++cb) {
         float v[16];
-        tc::tmem_ld16(taddr + cb * 16, v);
+        if (ok && has) {
+          tc::tmem_ld16(taddr + cb * 16, v);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] *= v[j];
-        const float s = lane_token_sums16(v, lane);
-        if ((lane & 1) == 0) red[q][cb * 16 + (lane >> 1)] = s;
+          for (int u = 0; u < 16; ++u) v[u] = 0.f;
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g)   // tokens 16 cb + 4 g .. + 3 of this row
+          tc::st_cluster_v4(peer + (uint32_t)((((cb * 4 + g) * 64) + r64) * 16), v[4 * g], v[4 * g + 1],
+                            v[4 * g + 2], v[4 * g + 3]);
+      }
+    }
+    tc::cluster_arrive_release();
+    tc::cluster_wait();                        // phase 2: the partner's partial sums are here
+    // p = (K half 0) + (K half 1), the same order in both CTAs
+    auto sums16 = [&](int cb, float (&v)[16]) {
+      float own[16];
+      if (ok && has) {
+        tc::tmem_ld16(taddr + cb * 16, own);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) own[u] = 0.f;
+      }
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const float4 o4 = *reinterpret_cast<const float4*>(recv + (((cb * 4 + g) * 64) + r64) * 4);
+        const float other[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int u = 4 * g + e;
+          v[u] = kh == 0 ? own[u] + other[e] : other[e] + own[u];
+        }
+      }
+    };
+    if (mine) {
+      for (int cb = 0; cb < npad / 16; ++cb) {
+        float v[16];
+        sums16(cb, v);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) v[u] *= v[u];
+        const float s2 = lane_token_sums16(v, lane);
+        if ((lane & 1) == 0) red[q & 1][cb * 16 + (lane >> 1)] = s2;
       }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    // this half's sums (warp quarters added in row order), then the swap
-    float own = 0.f;
-    if (ct < kTok) own = ((red[0][ct] + red[1][ct]) + red[2][ct]) + red[3][ct];
-    tc::cluster_wait();   // phase 1: the peer is running
-    if (ct < kTok) tc::st_cluster_f32(&ssq_peer[ct], (uint32_t)(half ^ 1), own);
-    tc::cluster_arrive_release();
-    tc::cluster_wait();   // phase 2: both halves' sums are in place
     if (ct < kTok) {
-      const float lo = half == 0 ? own : ssq_peer[ct], hi = half == 0 ? ssq_peer[ct] : own;
-      rfac[ct] = 1.f / sqrtf((lo + hi) / (float)kLd + p.eps);
+      const float own = red[0][ct] + red[1][ct];   // rows in order within this CTA's 64
+#pragma unroll
+      for (int r = 0; r < kCluster; ++r) tc::st_cluster_f32(tc::cluster_addr(&ssq_in[rank][ct], (uint32_t)r), own);
     }
+    tc::cluster_arrive_release();
+    tc::cluster_wait();                        // phase 3: all four row quarters' sums are here
+    if (ct < kTok) rfac[ct] = 1.f / sqrtf((((ssq_in[0][ct] + ssq_in[1][ct]) + ssq_in[2][ct]) + ssq_in[3][ct]) /
+                                                (float)kLd +
+                                            p.eps);
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (ct == 0) stamp(0, 6);
-    if (ok) {
+    if (ct == 0) stamp(kTraceRows - 1, 6);
+    if (mine) {   // warp-uniform: the TMEM loads below are warp-wide
+      const bool g = ok && tc::mbar_wait(gbar, 0, p.wait_limit, abort_flag, p.dev_err);
+      ok = __all_sync(0xffffffffu, g);
+    }
+    if (ok && mine) {
       const int j = row0 + row;                        // output column
-      const float nw = p.norm_w[half * kRows + row];
+      const float nw = p.norm_w[m * kRows + row];
       for (int cb = 0; cb < npad / 16; ++cb) {
         float v[16];
-        tc::tmem_ld16(taddr + cb * 16, v);
+        sums16(cb, v);
+        // branch-free over the 16 tokens so that the shared-memory reads of
+        // all of them are in flight together; a bad id writes zeros
+        int8_t tq[16];
+        float val[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int t = cb * 16 + u;
-          if (t >= ntok) break;
-          const size_t o = (size_t)(t0 + t) * PLD + j;
-          const int id = tid_sh[t];
-          if (id < 0) {
-            p.out[o] = 0.f;
-            if (p.gathered) p.gathered[o] = 0;
-            continue;
-          }
-          const int8_t tq = p.table[(size_t)id * PLD + j];
-          const float g = __fmul_rn(__fmul_rn((float)tq, tsc[t]), p.embed_scale);
-          p.out[o] = v[u] * rfac[t] * nw + g;
-          if (p.gathered) p.gathered[o] = tq;
+          const bool valid = tid_sh[t] >= 0;
+          tq[u] = valid ? gtab[t * 64 + r64] : (int8_t)0;
+          const float g = __fmul_rn(__fmul_rn((float)tq[u], tsc[t]), p.embed_scale);
+          val[u] = valid ? v[u] * rfac[t] * nw + g : 0.f;
+        }
+        float* outp = p.out + (size_t)(t0 + cb * 16) * PLD + j;
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          if (cb * 16 + u < ntok) outp[(size_t)u * PLD] = val[u];
+        if (p.gathered) {
+          int8_t* gp = p.gathered + (size_t)(t0 + cb * 16) * PLD + j;
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            if (cb * 16 + u < ntok) gp[(size_t)u * PLD] = tq[u];
         }
       }
     }
+    if (ct == 0) stamp(kTraceRows - 1, 7);
   }
-  if (threadIdx.x == kEpi0 * 32) stamp(0, 7);
-  if (warp < kEpi0) {   // the TMA and MMA warps take part in both cluster phases too
+  if (warp < kEpi0) {   // the TMA and MMA warps take part in every cluster phase too
+    tc::cluster_wait();
+    tc::cluster_arrive_release();
     tc::cluster_wait();
     tc::cluster_arrive_release();
     tc::cluster_wait();
   }
   tc::fence_before();
   __syncthreads();
+  if (trc && threadIdx.x == 0) trc[1] = tc::globaltimer();
   if (warp == 1) {
     tc::fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -358,7 +476,8 @@ int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_
   p.wait_limit = wait_limit();
   size_t tbytes = 0;
   void* tb = trace_buffer(&tbytes);
-  p.trace = (tb && tbytes >= (size_t)ple::kTraceChunks * 8 * sizeof(unsigned long long))
+  const size_t trace_words = (size_t)ple::kTraceRows * 8 + 2 * (size_t)ple::kCluster * L * ((S + ple::kTok - 1) / ple::kTok);
+  p.trace = (tb && tbytes >= trace_words * sizeof(unsigned long long))
                 ? static_cast<unsigned long long*>(tb)
                 : nullptr;
   static bool attr = false;
@@ -369,17 +488,19 @@ int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * L, (S + ple::kTok - 1) / ple::kTok);
+  cfg.gridDim = dim3(ple::kCluster * L, (S + ple::kTok - 1) / ple::kTok);
   cfg.blockDim = dim3(ple::kThreads);
   cfg.dynamicSmemBytes = ple::kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.x = ple::kCluster;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, ple::ple_tc_kernel, p);
   return e == cudaSuccess ? Q4_OK : cuda_fail(e, "ple launch");
 }
