@@ -82,6 +82,8 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
 struct Params {
   CUtensorMap tm_proj;   // f32 [L*ld][D], box [128 rows][32], 128-byte swizzle
   CUtensorMap tm_hid;    // fp16 bits [S][D], box [64 rows][32]; rows past S read as zero
+  CUtensorMap tm_out;    // f32 out [S][L*ld], box [64 tokens][64 columns]; rows past S not written
+  CUtensorMap tm_gat;    // int8 gathered [S][L*ld], box [64 tokens][64 columns] (when gathered != NULL)
   const int32_t* ids;
   const int8_t* table;
   const float* row_scale;
@@ -135,9 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   __shared__ long long t0_sh;
   __shared__ float red[2][kTok];            // per finishing warp: per-token sums of squares over 32 rows
   __shared__ float ssq_in[kCluster][kTok];  // per cluster rank: sums over its 64 finished rows
-  __shared__ float rfac[kTok];              // per-token RMS factor
-  __shared__ float tsc[kTok];               // per-token table scale (0 for a bad id)
-  __shared__ int tid_sh[kTok];              // per-token id (-1: out of range)
+  __shared__ __align__(16) float rfac[kTok];   // per-token RMS factor
+  __shared__ __align__(16) float tsc[kTok];    // per-token table scale (0 for a bad id)
+  __shared__ __align__(16) int tid_sh[kTok];   // per-token id (-1: out of range)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = blockIdx.x & (kCluster - 1);
@@ -159,13 +161,13 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   unsigned long long* const trc =
       p.trace ? p.trace + kTraceRows * 8 + 2 * ((size_t)blockIdx.y * gridDim.x + blockIdx.x) : nullptr;
   auto stamp = [&](int r, int k) {
-    if (tr && r < kTraceRows) tr[r * 8 + k] = (unsigned long long)(clock64() - t0_sh);
+    if (tr && r < kTraceRows) tr[r * 8 + k] = (unsigned long long)(tc::clock_ordered() - t0_sh);
   };
   auto nsc_of = [&](int st) { return min(kSub, se - sb - kSub * st); };
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
-    t0_sh = clock64();
+    t0_sh = tc::clock_ordered();
     if (trc) trc[0] = tc::globaltimer();
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(full0 + 8 * s, 1);
@@ -277,6 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     // the table bytes of the finished rows: one 64-byte copy per valid token,
     // issued by that token's thread (column row0 + 64 kh and the row width
     // L * 256 are multiples of 16 bytes); thread 0 posts the byte count
+    if (ct < kTok && !(ct < ntok && tid_sh[ct] >= 0))   // no copy: the gathered bytes are zero
+      for (int e = 0; e < 64; e += 16) *reinterpret_cast<uint4*>(gtab + ct * 64 + e) = make_uint4(0u, 0u, 0u, 0u);
     if (ct < ntok && tid_sh[ct] >= 0)
       tc::bulk_load(tc::smem_u32(gtab + ct * 64), p.table + (size_t)tid_sh[ct] * PLD + (size_t)row0 + 64 * kh, 64,
                     gbar, tc::policy_evict_first());
@@ -329,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     tc::fence_after();
     if (ct == 0) stamp(kTraceRows - 1, 5);
     tc::cluster_wait();                        // phase 1: every peer is running
+    if (ct == 0) stamp(kTraceRows - 2, 0);
     if (!mine) {                               // the partner finishes these rows
       const uint32_t peer = tc::cluster_addr(recv, (uint32_t)(rank ^ 2));
       for (int cb = 0; cb < npad / 16; ++cb) {
@@ -347,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     }
     tc::cluster_arrive_release();
     tc::cluster_wait();                        // phase 2: the partner's partial sums are here
+    if (ct == 0) stamp(kTraceRows - 2, 1);
     // p = (K half 0) + (K half 1), the same order in both CTAs
     auto sums16 = [&](int cb, float (&v)[16]) {
       float own[16];
@@ -367,14 +373,22 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
         }
       }
     };
-    if (mine) {
-      for (int cb = 0; cb < npad / 16; ++cb) {
+    float pv[kTok];   // this row's projection sums, kept for the output pass
+#pragma unroll
+    for (int cb = 0; cb < kTok / 16; ++cb) {
+      if (mine && cb < npad / 16) {   // warp-uniform
         float v[16];
         sums16(cb, v);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) v[u] *= v[u];
+        for (int u = 0; u < 16; ++u) {
+          pv[cb * 16 + u] = v[u];
+          v[u] *= v[u];
+        }
         const float s2 = lane_token_sums16(v, lane);
         if ((lane & 1) == 0) red[q & 1][cb * 16 + (lane >> 1)] = s2;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) pv[cb * 16 + u] = 0.f;
       }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -385,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     }
     tc::cluster_arrive_release();
     tc::cluster_wait();                        // phase 3: all four row quarters' sums are here
+    if (ct == 0) stamp(kTraceRows - 2, 2);
     if (ct < kTok) rfac[ct] = 1.f / sqrtf((((ssq_in[0][ct] + ssq_in[1][ct]) + ssq_in[2][ct]) + ssq_in[3][ct]) /
                                                 (float)kLd +
                                             p.eps);
@@ -395,35 +410,49 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
       ok = __all_sync(0xffffffffu, g);
     }
     if (ok && mine) {
-      const int j = row0 + row;                        // output column
+      // the output tile [64 tokens][64 columns] in shared memory (the partner's
+      // partial sums are no longer needed), then one tensor store; padding
+      // tokens are outside the tensor and not written
+      float* tile = recv;
       const float nw = p.norm_w[m * kRows + row];
-      for (int cb = 0; cb < npad / 16; ++cb) {
-        float v[16];
-        sums16(cb, v);
-        // branch-free over the 16 tokens so that the shared-memory reads of
-        // all of them are in flight together; a bad id writes zeros
+      const float es = p.embed_scale;
+      // 16 tokens at a time: every shared-memory read of the group is issued
+      // before its stores (the compiler cannot move reads across the stores)
+#pragma unroll
+      for (int cb = 0; cb < kTok / 16; ++cb) {
+        float sc[16], rf[16], val[16];
+        int id[16];
         int8_t tq[16];
-        float val[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 a = *reinterpret_cast<const float4*>(tsc + cb * 16 + 4 * i);
+          const float4 b = *reinterpret_cast<const float4*>(rfac + cb * 16 + 4 * i);
+          const int4 c = *reinterpret_cast<const int4*>(tid_sh + cb * 16 + 4 * i);
+          sc[4 * i] = a.x, sc[4 * i + 1] = a.y, sc[4 * i + 2] = a.z, sc[4 * i + 3] = a.w;
+          rf[4 * i] = b.x, rf[4 * i + 1] = b.y, rf[4 * i + 2] = b.z, rf[4 * i + 3] = b.w;
+          id[4 * i] = c.x, id[4 * i + 1] = c.y, id[4 * i + 2] = c.z, id[4 * i + 3] = c.w;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) tq[u] = gtab[(cb * 16 + u) * 64 + r64];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const int t = cb * 16 + u;
-          const bool valid = tid_sh[t] >= 0;
-          tq[u] = valid ? gtab[t * 64 + r64] : (int8_t)0;
-          const float g = __fmul_rn(__fmul_rn((float)tq[u], tsc[t]), p.embed_scale);
-          val[u] = valid ? v[u] * rfac[t] * nw + g : 0.f;
+          const float g = __fmul_rn(__fmul_rn((float)tq[u], sc[u]), es);
+          val[u] = id[u] >= 0 ? pv[cb * 16 + u] * rf[u] * nw + g : 0.f;
         }
-        float* outp = p.out + (size_t)(t0 + cb * 16) * PLD + j;
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          if (cb * 16 + u < ntok) outp[(size_t)u * PLD] = val[u];
-        if (p.gathered) {
-          int8_t* gp = p.gathered + (size_t)(t0 + cb * 16) * PLD + j;
-#pragma unroll
-          for (int u = 0; u < 16; ++u)
-            if (cb * 16 + u < ntok) gp[(size_t)u * PLD] = tq[u];
-        }
+        for (int u = 0; u < 16; ++u) tile[(cb * 16 + u) * 64 + r64] = val[u];
       }
     }
+    tc::fence_proxy_async();   // the tile (and the zeroed table rows) before the tensor stores read them
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (ct == 0 && ok) {
+      const int x = row0 + 64 * kh;   // 64 f32 = 256 bytes, 64 int8: 16-byte aligned
+      tc::tma_store_2d(&p.tm_out, x, t0, tc::smem_u32(recv));
+      if (p.gathered) tc::tma_store_2d(&p.tm_gat, x, t0, tc::smem_u32(gtab));
+      tc::bulk_commit();
+      tc::bulk_wait_all();
+    }
+    if (mine && (q & 1) == 0 && lane == 0) stamp(kTraceRows - 2, 3);
     if (ct == 0) stamp(kTraceRows - 1, 7);
   }
   if (warp < kEpi0) {   // the TMA and MMA warps take part in every cluster phase too
@@ -436,6 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   tc::fence_before();
   __syncthreads();
   if (trc && threadIdx.x == 0) trc[1] = tc::globaltimer();
+  if (threadIdx.x == 0) stamp(kTraceRows - 2, 4);
   if (warp == 1) {
     tc::fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -458,6 +488,14 @@ int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_
   st = encode_tensor_2d(&p.tm_hid, hidden, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)D, (uint64_t)S, ple::kKC,
                         ple::kTok, CU_TENSOR_MAP_SWIZZLE_NONE, "hidden");
   if (st != Q4_OK) return st;
+  st = encode_tensor_2d(&p.tm_out, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)L * ld, (uint64_t)S, 64,
+                        ple::kTok, CU_TENSOR_MAP_SWIZZLE_NONE, "out");
+  if (st != Q4_OK) return st;
+  if (gathered) {
+    st = encode_tensor_2d(&p.tm_gat, gathered, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)L * ld, (uint64_t)S, 64,
+                          ple::kTok, CU_TENSOR_MAP_SWIZZLE_NONE, "gathered");
+    if (st != Q4_OK) return st;
+  }
   p.ids = ids;
   p.table = table;
   p.row_scale = row_scale;

@@ -66,9 +66,17 @@ __device__ __forceinline__ void mbar_drain(uint32_t a, uint32_t parity, long lon
   }
 }
 
+// Global nanosecond timer; the memory clobber keeps the read in program order
+// with the barriers and memory operations around it.
 __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t) : : "memory");
+  return t;
+}
+// SM cycle counter, kept in program order like globaltimer().
+__device__ __forceinline__ long long clock_ordered() {
+  long long t;
+  asm volatile("mov.u64 %0, %clock64;" : "=l"(t) : : "memory");
   return t;
 }
 
@@ -92,6 +100,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(mbar), "l"(policy)
       : "memory");
 }
+
+// 2-D tensor-map tile store from this CTA's shared memory (elements outside
+// the tensor are not written), tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Every bulk store this thread committed has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Contiguous bulk copy global -> this CTA's shared memory (16-byte aligned
 // addresses, size a multiple of 16), completing on an mbarrier.
