@@ -15,20 +15,22 @@
 //   warps 4-11  converters: raw codes + scales from the raw ring, nibble ->
 //               bf16 (exact d*(q-8) in fp32, then round to nearest even),
 //               written in the no-swizzle K-major core-matrix layout (A)
-//   warp 12     TMEM allocator and the single thread that issues tcgen05.mma
-//   warp 13     one thread issuing the TMA loads of the raw ring
-//   warp 14     one thread loading the token tile (B) of each operand stage
-//               straight from the bf16 copy of X (a 3-D tensor map whose box
-//               lands in the core-matrix layout)
+//   warp 12     TMEM allocator and MMA issuer: the warp walks the pipeline
+//               and waits together, one elected lane issues the 8 MMAs of a
+//               128-column stage and the commits
+//   warp 13     raw-ring TMA loads (one elected lane issues)
+//   warp 14     token tile (B) of each operand stage: one bulk copy from the
+//               bf16 copy of X, completing on the stage's full barrier
 // X is rounded to bf16 once per call by a small kernel ahead of the GEMM (in
 // the caller's workspace) instead of once per tile and chunk.  The raw ring
 // (kRawStages x 256 K columns: codes 16 KB + scales 2 KB) keeps weight bytes
-// in flight; the operand ring (kStages x (A 16 KB + B 8 KB)) feeds the tensor
-// cores.  Both are guarded by full / empty mbarriers; two TMEM accumulators
-// (2 x 64 columns) let the epilogue of one item overlap the MMAs of the next.
-// Every mbarrier wait is bounded in
+// in flight; the operand ring (kStages x (A 32 KB + B 16 KB), 128 K columns
+// each) feeds the tensor cores.  full counts the converter warps and the B
+// loader (with its bytes), so the MMA issuer waits on one barrier per stage.
+// Two TMEM accumulators (2 x 64 columns) let the epilogue of one item
+// overlap the MMAs of the next.  Every mbarrier wait is bounded in
 // clock cycles; on expiry the CTA raises an abort flag, every role leaves its
-// loop, the MMA thread drains its own tcgen05 work (bounded again), TMEM is
+// loop, the MMA issuer drains its own tcgen05 work (bounded again), TMEM is
 // freed and the kernel returns with the device error word set.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -56,14 +58,14 @@ unsigned* device_error_word() {
 
 namespace gemm {
 
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kRawStages = 4;
-constexpr int kRawChunks = 4;          // operand chunks per raw stage (256 K columns)
+constexpr int kRawChunks = 2;          // operand chunks per raw stage (256 K columns)
 constexpr int kTileM = 128;            // weight rows per tile (MMA M)
 constexpr int kTok = 64;               // tokens (MMA N)
-constexpr int kChunk = 64;             // K columns per operand stage
-constexpr int kABytes = kTileM * kChunk * 2;   // 16 KB bf16
-constexpr int kBBytes = kTok * kChunk * 2;     // 8 KB bf16
+constexpr int kChunk = 128;            // K columns per operand stage (8 MMAs of K = 16)
+constexpr int kABytes = kTileM * kChunk * 2;   // 32 KB bf16
+constexpr int kBBytes = kTok * kChunk * 2;     // 16 KB bf16
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kRawCodeBytes = kTileM * kChunk * kRawChunks / 2;   // 16 KB: [128 rows][128 B]
 constexpr int kRawScaleBytes = kTileM * 16;                         // 2 KB: [128 rows][8 fp16]
@@ -74,9 +76,17 @@ constexpr int kTmaWarp = kMmaWarp + 1;             // 13
 constexpr int kBWarp = kTmaWarp + 1;               // 14
 constexpr int kThreadsG = (kBWarp + 1) * 32;       // 480
 constexpr int kTmemCols = 128;
-constexpr int kBars = 3 * kStages + 2 * kRawStages + 5;
+constexpr int kBars = 2 * kStages + 2 * kRawStages + 5;
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)kRawStages * kRawBytes + kBars * 8;
 constexpr long long kDrainCycles = 2000000000LL;
+constexpr long long kShortDrainCycles = 4000000LL;   // aborting: copies in flight land well within this
+
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n .reg .pred P;\n .reg .b32 R;\n elect.sync R|P, 0xffffffff;\n selp.b32 %0, 1, 0, P;\n}"
+               : "=r"(pred));
+  return pred != 0;
+}
 
 // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M=128, N=64.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTok >> 3) << 17) |
@@ -239,7 +249,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   uint8_t* raw_base = smem + (size_t)kStages * kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(raw_base + (size_t)kRawStages * kRawBytes);
   // bars: full[kStages], empty[kStages], accfull[2], accempty[2], drain,
-  //       rawfull[kRawStages], rawempty[kRawStages], bfull[kStages]
+  //       rawfull[kRawStages], rawempty[kRawStages]
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ long long t0_sh;
@@ -253,15 +263,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   const uint32_t accfull0 = smem_u32(bars + 2 * kStages), accempty0 = smem_u32(bars + 2 * kStages + 2);
   const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
   const uint32_t rawfull0 = smem_u32(bars + 2 * kStages + 5), rawempty0 = rawfull0 + 8 * kRawStages;
-  const uint32_t bfull0 = rawempty0 + 8 * kRawStages;
   volatile int* abort_flag = &abort_sh;
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
     t0_sh = clock64();
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, kProdWarps);   // one arrival per converter warp
-      mbar_init(bfull0 + 8 * s, 1);           // the B loader's arrival with its bytes
+      mbar_init(full0 + 8 * s, kProdWarps + 1);   // one arrival per converter warp + the B loader's, with its bytes
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -287,7 +295,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   const uint32_t tmem = tmem_base_sh;
   if (warp == kTmaWarp) {
     // ------------------------------------------------------- raw tile loads
-    if (lane == 0 && blockIdx.x < p.items) {
+    // (the whole warp walks the loop, one elected lane issues)
+    if (blockIdx.x < p.items) {
       uint64_t pol_stream;
       asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_stream));
       const uint32_t raw0 = smem_u32(raw_base);
@@ -298,17 +307,22 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         item_range(p, item, tile, c0, c1);
         for (int cs = c0; cs < c1; cs += kRawChunks, ++g) {
           const uint32_t s = g % kRawStages, round = g / kRawStages;
-          if (!mbar_wait(rawempty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, 64)) {
+          const bool free_ = mbar_wait(rawempty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, 64);
+          if (!__all_sync(0xffffffffu, free_)) {
             ok = false;
             break;
           }
-          const uint32_t dst = raw0 + s * kRawBytes;
-          stamp(gc, 0);
+          if (elect_one()) {
+            const uint32_t dst = raw0 + s * kRawBytes;
+            stamp(gc, 0);
+            mbar_expect_tx(rawfull0 + 8 * s, p.sc_tma ? kRawBytes : kRawCodeBytes);
+            tma_load_2d(dst, &p.tm_codes, cs * (kChunk / 2), tile * kTileM, rawfull0 + 8 * s, pol_stream);
+            if (p.sc_tma)   // cs % kRawChunks == 0 here: the x coordinate is 16-byte aligned
+              tma_load_2d(dst + kRawCodeBytes, &p.tm_sc, cs * (kChunk / 32), tile * kTileM, rawfull0 + 8 * s,
+                          pol_stream);
+          }
+          __syncwarp();
           gc += min(cs + kRawChunks, c1) - cs;
-          mbar_expect_tx(rawfull0 + 8 * s, p.sc_tma ? kRawBytes : kRawCodeBytes);
-          tma_load_2d(dst, &p.tm_codes, cs * (kChunk / 2), tile * kTileM, rawfull0 + 8 * s, pol_stream);
-          if (p.sc_tma)   // cs % kRawChunks == 0 here: the x coordinate is 16-byte aligned
-            tma_load_2d(dst + kRawCodeBytes, &p.tm_sc, cs * 2, tile * kTileM, rawfull0 + 8 * s, pol_stream);
         }
       }
       // every issued load lands before the CTA may exit
@@ -326,38 +340,43 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     __syncwarp();
   } else if (warp == kBWarp) {
     // ------------------------------------------- token tiles (B operand)
-    if (lane == 0) {
-      uint64_t pol_keep;
-      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
-      pdl_wait();   // the bf16 copy of X is written by the kernel launched just before
-      const uint32_t stage0 = smem_u32(stage_base);
-      uint32_t g = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
-        int tile, c0, c1;
-        item_range(p, item, tile, c0, c1);
-        for (int c = c0; c < c1; ++c, ++g) {
-          const uint32_t s = g % kStages, round = g / kStages;
-          if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, 64)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(bfull0 + 8 * s, kBBytes);
-          // [8 column groups][64 tokens][8]: core matrices 128 B apart along the
-          // tokens, 1024 B apart along K
-          bulk_load(stage0 + s * kStageBytes + kABytes, p.xb + (size_t)c * kBBytes, kBBytes, bfull0 + 8 * s,
-                    pol_keep);
+    uint64_t pol_keep;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
+    pdl_wait();   // the bf16 copy of X is written by the kernel launched just before
+    const uint32_t stage0 = smem_u32(stage_base);
+    uint32_t g = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
+      int tile, c0, c1;
+      item_range(p, item, tile, c0, c1);
+      for (int c = c0; c < c1; ++c, ++g) {
+        const uint32_t s = g % kStages, round = g / kStages;
+        const bool free_ = mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, 64);
+        if (!__all_sync(0xffffffffu, free_)) {
+          ok = false;
+          break;
         }
+        if (elect_one()) {
+          // [16 column groups][64 tokens][8]: core matrices 128 B apart along
+          // the tokens, 1024 B apart along K; a last chunk of 64 columns is 8 KB
+          const uint32_t bytes = (uint32_t)(min(kChunk, p.K - c * kChunk) / 64) * (kBBytes / 2);
+          mbar_expect_tx(full0 + 8 * s, bytes);   // also this loader's arrival on full
+          bulk_load(stage0 + s * kStageBytes + kABytes, p.xb + (size_t)c * kBBytes, bytes, full0 + 8 * s, pol_keep);
+        }
+        __syncwarp();
       }
-      // every issued load lands before the CTA may exit
-      const uint32_t first = g > (uint32_t)kStages ? g - kStages : 0u;
-      for (uint32_t q = first; q < g; ++q) {
-        const long long t0 = clock64();
-        while (!mbar_test(bfull0 + 8 * (q % kStages), (q / kStages) & 1)) {
-          if (clock64() - t0 > kDrainCycles) {
-            atomicOr(&g_device_error, 1u);
-            break;
-          }
+    }
+    // every issued copy lands before the CTA may exit (full also waits for
+    // the converters, which an aborting CTA may never bring, hence the
+    // short bound then)
+    const uint32_t first = g > (uint32_t)kStages ? g - kStages : 0u;
+    for (uint32_t q = first; q < g; ++q) {
+      const long long lim = *abort_flag ? kShortDrainCycles : kDrainCycles;
+      const long long t0 = clock64();
+      while (!mbar_test(full0 + 8 * (q % kStages), (q / kStages) & 1)) {
+        if (clock64() - t0 > lim) {
+          atomicOr(&g_device_error, 1u);
+          break;
         }
       }
     }
@@ -365,7 +384,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   } else if (warp >= kEpiWarps && warp < kMmaWarp) {
     // ----------------------------------------------------------- converters
     const int pt = threadIdx.x - kEpiWarps * 32;
-    const int r = pt >> 1, h = pt & 1;        // A: row of the tile, 32-block in the chunk
+    const int r = pt >> 1, h = pt & 1;   // A: row of the tile; 32-column blocks h and h + 2 of a chunk
     // A: core matrix (8 rows x 16 B) of row block r/8 and column block kb at
     // kb * 2048 + (r/8) * 128, so the 16 row blocks of one column block are
     // contiguous (the tensor core reads them together without bank conflicts)
@@ -377,7 +396,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       item_range(p, item, tile, c0, c1);
       for (int cs = c0; cs < c1 && ok; cs += kRawChunks, ++gr) {
         const uint32_t rs = gr % kRawStages, rround = gr / kRawStages;
-        if (!mbar_wait(rawfull0 + 8 * rs, rround & 1, p.wait_limit, abort_flag)) {
+        const bool landed = mbar_wait(rawfull0 + 8 * rs, rround & 1, p.wait_limit, abort_flag);
+        if (!__all_sync(0xffffffffu, landed)) {
           ok = false;
           break;
         }
@@ -386,28 +406,43 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         const int ce = min(cs + kRawChunks, c1);
         for (int c = cs; c < ce; ++c, ++g) {
           const int cc = c - cs;
-          const uint4 code = *reinterpret_cast<const uint4*>(raw + r * 128 + cc * 32 + h * 16);
-          const float d =
-              p.sc_tma ? __half2float(*reinterpret_cast<const __half*>(raw + kRawCodeBytes + r * 16 +
-                                                                        (cc * 2 + h) * 2))
-                       : ld_scale(p.scales + ((size_t)tile * kTileM + r) * (p.K >> 5) + c * 2 + h);
+          const int nb = min(kChunk, p.K - c * kChunk) / 32;   // 32-column blocks in this chunk: 4, or 2 at the end
+          uint4 code[2];
+          float d[2];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int bb = h + 2 * i;
+            if (bb < nb) {
+              code[i] = *reinterpret_cast<const uint4*>(raw + r * 128 + cc * 64 + bb * 16);
+              d[i] = p.sc_tma ? __half2float(*reinterpret_cast<const __half*>(raw + kRawCodeBytes + r * 16 +
+                                                                                (cc * 4 + bb) * 2))
+                              : ld_scale(p.scales + ((size_t)tile * kTileM + r) * (p.K >> 5) + c * 4 + bb);
+            }
+          }
           if (c == ce - 1) {   // the raw stage has been read
             __syncwarp();
             if (lane == 0) mbar_arrive(rawempty0 + 8 * rs);
           }
           const uint32_t s = g % kStages, round = g / kStages;
-          if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag)) {
+          const bool free_ = mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag);
+          if (!__all_sync(0xffffffffu, free_)) {
             ok = false;
             break;
           }
           if (pt == 0) stamp(g, 2);
           uint8_t* A = stage_base + (size_t)s * kStageBytes;
-          const f2_t dd = f2_pack(d, d);
-          const f2_t bias = f2_pack(-264.f * d, -24.f * d);
-          const uint32_t w4[4] = {code.x, code.y, code.z, code.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(A + a_off + (h * 4 + j) * 2048) = dequant_word(w4[j], dd, bias);
+          for (int i = 0; i < 2; ++i) {
+            const int bb = h + 2 * i;
+            if (bb < nb) {
+              const f2_t dd = f2_pack(d[i], d[i]);
+              const f2_t bias = f2_pack(-264.f * d[i], -24.f * d[i]);
+              const uint32_t w4[4] = {code[i].x, code[i].y, code[i].z, code[i].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(A + a_off + (bb * 4 + j) * 2048) = dequant_word(w4[j], dd, bias);
+            }
+          }
           fence_proxy_async();   // this thread's stores, before the tensor core reads them
           __syncwarp();
           if (lane == 0) mbar_arrive(full0 + 8 * s);
@@ -417,51 +452,60 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      uint32_t g = 0;
-      int it = 0;
-      bool ok = true;
-      const uint32_t stage0 = smem_u32(stage_base);
-      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
-        int tile, c0, c1;
-        item_range(p, item, tile, c0, c1);
-        const int a = it & 1;
-        if (!mbar_wait(accempty0 + 8 * a, ((it >> 1) & 1) ^ 1, p.wait_limit, abort_flag)) {
+    // (the whole warp walks the loop and waits, one elected lane issues)
+    uint32_t g = 0;
+    int it = 0;
+    bool ok = true;
+    const uint32_t stage0 = smem_u32(stage_base);
+    for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
+      int tile, c0, c1;
+      item_range(p, item, tile, c0, c1);
+      const int a = it & 1;
+      const bool acc_free = mbar_wait(accempty0 + 8 * a, ((it >> 1) & 1) ^ 1, p.wait_limit, abort_flag);
+      if (!__all_sync(0xffffffffu, acc_free)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + (uint32_t)(a * kTok);
+      for (int c = c0; c < c1; ++c, ++g) {
+        const uint32_t s = g % kStages, round = g / kStages;
+        // full: the converter warps' A tile and the B loader's token tile
+        const bool landed = mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag);
+        if (!__all_sync(0xffffffffu, landed)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(a * kTok);
-        for (int c = c0; c < c1; ++c, ++g) {
-          const uint32_t s = g % kStages, round = g / kStages;
-          if (!mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag) ||
-              !mbar_wait(bfull0 + 8 * s, round & 1, p.wait_limit, abort_flag)) {
-            ok = false;
-            break;
-          }
+        if (elect_one()) {
           stamp(g, 4);
-          tc_fence_after();
           const uint32_t A = stage0 + s * kStageBytes, B = A + kABytes;
+          const int nks = min(kChunk, p.K - c * kChunk) / 16;
 #pragma unroll
           for (int ks = 0; ks < kChunk / 16; ++ks) {
-            const uint64_t ad = smem_desc(A + ks * 4096, 2048, 128);
-            const uint64_t bd = smem_desc(B + ks * 2048, 1024, 128);
-            tc_mma(d_tmem, ad, bd, (c > c0 || ks > 0) ? 1u : 0u);
+            if (ks < nks) {
+              const uint64_t ad = smem_desc(A + ks * 4096, 2048, 128);
+              const uint64_t bd = smem_desc(B + ks * 2048, 1024, 128);
+              tc_mma(d_tmem, ad, bd, (c > c0 || ks > 0) ? 1u : 0u);
+            }
           }
           tc_commit(empty0 + 8 * s);
           stamp(g, 5);
         }
-        if (!ok) break;
-        tc_commit(accfull0 + 8 * a);
+        __syncwarp();
       }
-      // drain: every tcgen05 op this thread issued has finished before TMEM is freed
-      tc_commit(drain);
-      const long long t0 = clock64();
-      while (!mbar_test(drain, 0)) {
-        if (clock64() - t0 > kDrainCycles) {   // independent of the (possibly zero) wait budget
-          atomicOr(&g_device_error, 1u);
-          break;
-        }
+      if (!ok) break;
+      if (elect_one()) tc_commit(accfull0 + 8 * a);
+      __syncwarp();
+    }
+    // drain: every tcgen05 op issued here has finished before TMEM is freed
+    if (elect_one()) tc_commit(drain);
+    __syncwarp();
+    const long long t0 = clock64();
+    while (!mbar_test(drain, 0)) {
+      if (clock64() - t0 > kDrainCycles) {   // independent of the (possibly zero) wait budget
+        atomicOr(&g_device_error, 1u);
+        break;
       }
     }
     __syncwarp();
@@ -576,7 +620,7 @@ int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* 
   p.N = N;
   p.K = K;
   p.tiles = N / gemm::kTileM;
-  p.nchunks = K / gemm::kChunk;
+  p.nchunks = (K + gemm::kChunk - 1) / gemm::kChunk;
   int splits = (dev.sms + p.tiles - 1) / p.tiles;
   if (splits > p.nchunks) splits = p.nchunks;
   if (splits < 1) splits = 1;

@@ -39,7 +39,9 @@ def test_zero_budget_times_out_then_recovers(cuda_lib):
     h = torch.empty(256, dtype=torch.float16, device="cuda")
     old = q4w.q4_set_wait_limit(0)
     try:
-        q4w.q4_gemm_chunk(codes, scales, X)
+        # several tiles per CTA, so that some wait outlasts the hardware's own
+        # suspend window of mbarrier.try_wait and the zero budget is seen
+        q4w.q4_gemm_chunk(gc, gs, X)
         _expect_timeout(q4w)
         q4w.q4_gemv(gc, gs, x1)                  # streaming GEMV (K = 1536)
         _expect_timeout(q4w)
