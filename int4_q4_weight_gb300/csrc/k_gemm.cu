@@ -37,6 +37,7 @@
 
 #include "q4w_device.cuh"
 #include "q4w_internal.cuh"
+#include "q4w_tc.cuh"
 
 namespace q4w {
 
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned long long* const tr = (p.trace && blockIdx.x == 0) ? p.trace : nullptr;
   auto stamp = [&](uint32_t chunk, int k) {
-    if (tr && chunk < (uint32_t)kTraceChunks) tr[chunk * 8 + k] = (unsigned long long)(clock64() - t0_sh);
+    if (tr && chunk < (uint32_t)kTraceChunks) tr[chunk * 8 + k] = (unsigned long long)(tc::clock_ordered() - t0_sh);
   };
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
   const uint32_t accfull0 = smem_u32(bars + 2 * kStages), accempty0 = smem_u32(bars + 2 * kStages + 2);
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
-    t0_sh = clock64();
+    t0_sh = tc::clock_ordered();
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, kProdWarps + 1);   // one arrival per converter warp + the B loader's, with its bytes
       mbar_init(empty0 + 8 * s, 1);
