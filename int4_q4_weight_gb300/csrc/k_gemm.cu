@@ -63,11 +63,13 @@ constexpr int kStages = 3;
 constexpr int kRawStages = 4;
 constexpr int kRawChunks = 2;          // operand chunks per raw stage (256 K columns)
 constexpr int kTileM = 128;            // weight rows per tile (MMA M)
-constexpr int kTok = 64;               // tokens (MMA N)
+constexpr int kTok = 64;               // tokens of the prefill GEMM (MMA N)
 constexpr int kChunk = 128;            // K columns per operand stage (8 MMAs of K = 16)
-constexpr int kABytes = kTileM * kChunk * 2;   // 32 KB bf16
-constexpr int kBBytes = kTok * kChunk * 2;     // 16 KB bf16
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kABytes = kTileM * kChunk * 2;   // 32 KB of 16-bit weights
+// per token count N (the MMA N): token tile bytes per stage, stage bytes, TMEM columns (two accumulators)
+__host__ __device__ constexpr int b_bytes(int n) { return n * kChunk * 2; }
+__host__ __device__ constexpr int stage_bytes(int n) { return kABytes + b_bytes(n); }
+__host__ __device__ constexpr int tmem_cols(int n) { return 2 * n < 32 ? 32 : 2 * n; }
 constexpr int kRawCodeBytes = kTileM * kChunk * kRawChunks / 2;   // 16 KB: [128 rows][128 B]
 constexpr int kRawScaleBytes = kTileM * 16;                         // 2 KB: [128 rows][8 fp16]
 constexpr int kRawBytes = kRawCodeBytes + kRawScaleBytes;
@@ -76,9 +78,10 @@ constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 12
 constexpr int kTmaWarp = kMmaWarp + 1;             // 13
 constexpr int kBWarp = kTmaWarp + 1;               // 14
 constexpr int kThreadsG = (kBWarp + 1) * 32;       // 480
-constexpr int kTmemCols = 128;
 constexpr int kBars = 2 * kStages + 2 * kRawStages + 5;
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)kRawStages * kRawBytes + kBars * 8;
+__host__ __device__ constexpr size_t smem_bytes(int n) {
+  return 1024 + (size_t)kStages * stage_bytes(n) + (size_t)kRawStages * kRawBytes + kBars * 8;
+}
 constexpr long long kDrainCycles = 2000000000LL;
 constexpr long long kShortDrainCycles = 4000000LL;   // aborting: copies in flight land well within this
 
@@ -89,9 +92,12 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
-// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M=128, N=64.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTok >> 3) << 17) |
-                            ((uint32_t)(kTileM >> 4) << 24);
+// Instruction descriptor, kind::f16: D f32, A and B bf16 (format 1) or fp16
+// (format 0), both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc(int n, bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(kTileM >> 4) << 24);
+}
 
 // Shared-memory matrix descriptor, no swizzle: 8x(16 B) core matrices;
 // lbo = byte step between core matrices along K, sbo = along M/N.
@@ -151,11 +157,12 @@ __device__ __forceinline__ void tc_commit(uint32_t mbar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
                : "memory");
 }
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t id,
+                                       uint32_t accum) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum)
+      "l"(adesc), "l"(bdesc), "r"(id), "r"(accum)
       : "memory");
 }
 
@@ -194,6 +201,27 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, f2_t dd, f2_t bias) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// The same 8 columns as fp16: fp16(d (n - 8)), rounded once.  A nibble lands
+// in the mantissa of fp16 1024 (bits 0-3 of each half) or 64 (bits 4-7):
+// (1024 + n) - 1032 and (64 + n) - 72 are the exact small integers n - 8, and
+// the half multiply by d rounds the exact product to nearest even.  Halves
+// come out as column pairs (0,4), (2,6), (1,5), (3,7) and are put back in
+// column order with byte permutes.
+__device__ __forceinline__ uint4 dequant_word_f16(uint32_t w, __half2 dd) {
+  const uint32_t w8 = w >> 8;
+  const __half2 m_even = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+  const __half2 m_odd = __halves2half2(__ushort_as_half(0x5480), __ushort_as_half(0x5480));    // 72
+  const uint32_t p04 = lop3_and_or(w, 0x000F000Fu, 0x64006400u), p26 = lop3_and_or(w8, 0x000F000Fu, 0x64006400u);
+  const uint32_t p15 = lop3_and_or(w, 0x00F000F0u, 0x54005400u), p37 = lop3_and_or(w8, 0x00F000F0u, 0x54005400u);
+  auto dq = [&](uint32_t pv, __half2 m) {
+    const __half2 v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&pv), m), dd);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  };
+  const uint32_t v04 = dq(p04, m_even), v26 = dq(p26, m_even), v15 = dq(p15, m_odd), v37 = dq(p37, m_odd);
+  return make_uint4(__byte_perm(v04, v15, 0x5410), __byte_perm(v26, v37, 0x5410), __byte_perm(v04, v15, 0x7632),
+                    __byte_perm(v26, v37, 0x7632));
+}
+
 __device__ __forceinline__ uint32_t h2_to_bf16x2(uint32_t h2) {
   const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
   return bf16x2(f.x, f.y);
@@ -207,6 +235,7 @@ struct Params {
   int sc_tma;
   float* Y;
   int N, K;
+  int ntok;               // tokens written to Y (the rows of Y; the MMA N may be padded beyond)
   int tiles, splits, cps, nchunks, items;
   long long wait_limit;
   unsigned long long* trace;   // optional: CTA 0 stamps [chunk < kTraceChunks][8], SM cycles
@@ -243,7 +272,13 @@ __device__ __forceinline__ void item_range(const Params& p, int item, int& tile,
   c1 = min(c0 + p.cps, p.nchunks);
 }
 
+// NT: the MMA N (token tile), F16: fp16 tiles (else bf16).
+template <int NT, bool F16>
 __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constant__ Params p) {
+  constexpr int kStageBytes = stage_bytes(NT);
+  constexpr int kBBytes = b_bytes(NT);
+  constexpr int kTmemCols = tmem_cols(NT);
+  constexpr uint32_t kId = idesc(NT, F16);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* stage_base = smem;
@@ -436,12 +471,19 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           for (int i = 0; i < 2; ++i) {
             const int bb = h + 2 * i;
             if (bb < nb) {
-              const f2_t dd = f2_pack(d[i], d[i]);
-              const f2_t bias = f2_pack(-264.f * d[i], -24.f * d[i]);
               const uint32_t w4[4] = {code[i].x, code[i].y, code[i].z, code[i].w};
+              if (F16) {
+                const __half2 dd = __float2half2_rn(d[i]);   // d is an fp16 value: exact
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint4*>(A + a_off + (bb * 4 + j) * 2048) = dequant_word(w4[j], dd, bias);
+                for (int j = 0; j < 4; ++j)
+                  *reinterpret_cast<uint4*>(A + a_off + (bb * 4 + j) * 2048) = dequant_word_f16(w4[j], dd);
+              } else {
+                const f2_t dd = f2_pack(d[i], d[i]);
+                const f2_t bias = f2_pack(-264.f * d[i], -24.f * d[i]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  *reinterpret_cast<uint4*>(A + a_off + (bb * 4 + j) * 2048) = dequant_word(w4[j], dd, bias);
+              }
             }
           }
           fence_proxy_async();   // this thread's stores, before the tensor core reads them
@@ -468,7 +510,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem + (uint32_t)(a * kTok);
+      const uint32_t d_tmem = tmem + (uint32_t)(a * NT);
       for (int c = c0; c < c1; ++c, ++g) {
         const uint32_t s = g % kStages, round = g / kStages;
         // full: the converter warps' A tile and the B loader's token tile
@@ -486,8 +528,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           for (int ks = 0; ks < kChunk / 16; ++ks) {
             if (ks < nks) {
               const uint64_t ad = smem_desc(A + ks * 4096, 2048, 128);
-              const uint64_t bd = smem_desc(B + ks * 2048, 1024, 128);
-              tc_mma(d_tmem, ad, bd, (c > c0 || ks > 0) ? 1u : 0u);
+              // B: [16 column groups][NT tokens][8]: groups NT * 16 B apart
+              const uint64_t bd = smem_desc(B + ks * NT * 32, NT * 16, 128);
+              tc_mma(d_tmem, ad, bd, kId, (c > c0 || ks > 0) ? 1u : 0u);
             }
           }
           tc_commit(empty0 + 8 * s);
@@ -524,11 +567,12 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       tc_fence_after();
       float* yrow = p.Y + (size_t)tile * kTileM + row;
 #pragma unroll
-      for (int cb = 0; cb < kTok / 16; ++cb) {
+      for (int cb = 0; cb < NT / 16; ++cb) {
         float v[16];
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(a * kTok + cb * 16), v);
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(a * NT + cb * 16), v);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
+          if (cb * 16 + j >= p.ntok) break;
           float* dst = yrow + (size_t)(cb * 16 + j) * p.N;
           if (p.splits == 1)
             *dst = v[j];
@@ -552,17 +596,24 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   }
 }
 
-// X fp16 [64][K] -> bf16 (nearest even) as [K/8 column groups][64 tokens][8]:
-// each 64-column chunk becomes one contiguous 8 KB token tile in the
-// core-matrix layout.  One thread per (group, token).
-__global__ void __launch_bounds__(256) x_to_bf16_kernel(const __half* __restrict__ X, uint8_t* __restrict__ xb,
-                                                        int K) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;   // = group * 64 + token
-  if (i >= (K >> 3) * kTok) return;
-  const int grp = i / kTok, tok = i - grp * kTok;
-  const uint4 v = *reinterpret_cast<const uint4*>(X + (size_t)tok * K + grp * 8);
-  const uint4 o = make_uint4(h2_to_bf16x2(v.x), h2_to_bf16x2(v.y), h2_to_bf16x2(v.z), h2_to_bf16x2(v.w));
-  *reinterpret_cast<uint4*>(xb + (size_t)i * 16) = o;
+// X fp16 [ntok][K] -> the token operand as [K/8 column groups][NT tokens][8]:
+// bf16 (nearest even) for bf16 tiles, the fp16 bits unchanged for fp16 tiles;
+// tokens ntok .. NT-1 are zero.  Each 128-column chunk is one contiguous
+// NT * 256-byte token tile in the core-matrix layout.  One thread per
+// (group, token).
+template <int NT, bool F16>
+__global__ void __launch_bounds__(256) x_layout_kernel(const __half* __restrict__ X, uint8_t* __restrict__ xb,
+                                                       int K, int ntok) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;   // = group * NT + token
+  if (i < (K >> 3) * NT) {
+    const int grp = i / NT, tok = i - grp * NT;
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (tok < ntok) {
+      const uint4 v = *reinterpret_cast<const uint4*>(X + (size_t)tok * K + grp * 8);
+      o = F16 ? v : make_uint4(h2_to_bf16x2(v.x), h2_to_bf16x2(v.y), h2_to_bf16x2(v.z), h2_to_bf16x2(v.w));
+    }
+    *reinterpret_cast<uint4*>(xb + (size_t)i * 16) = o;
+  }
   pdl_trigger();
 }
 
@@ -600,10 +651,14 @@ int encode_tensor_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type
 }
 
 size_t gemm_ws_bytes(int K) { return ((size_t)gemm::kTok * K * 2 + 255) & ~(size_t)255; }
+size_t mma16_ws_bytes(int K) { return ((size_t)16 * K * 2 + 255) & ~(size_t)255; }
 
-int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
-                      int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s) {
-  (void)M;
+// Y[t][n] (t < ntok) = the dequantised weights times X through gemm_kernel<NT, F16>.
+// allow_split: K may be split across CTAs (the splits add into Y with fp32
+// atomics, so the summation order is not fixed); else one CTA per tile.
+template <int NT, bool F16>
+static int launch_mma(const uint8_t* codes, const __half* scales, const __half* X, int ntok, float* Y, int N,
+                      int K, void* ws, bool allow_split, const DeviceInfo& dev, cudaStream_t s) {
   gemm::Params p;
   memset(&p, 0, sizeof(p));
   int st = encode_tensor_2d(&p.tm_codes, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N,
@@ -620,9 +675,10 @@ int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* 
   p.Y = Y;
   p.N = N;
   p.K = K;
+  p.ntok = ntok;
   p.tiles = N / gemm::kTileM;
   p.nchunks = (K + gemm::kChunk - 1) / gemm::kChunk;
-  int splits = (dev.sms + p.tiles - 1) / p.tiles;
+  int splits = allow_split ? (dev.sms + p.tiles - 1) / p.tiles : 1;
   if (splits > p.nchunks) splits = p.nchunks;
   if (splits < 1) splits = 1;
   p.cps = (p.nchunks + splits - 1) / splits;
@@ -637,34 +693,46 @@ int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* 
                 : nullptr;
   cudaError_t e;
   if (p.splits > 1) {
-    e = cudaMemsetAsync(Y, 0, (size_t)gemm::kTok * N * sizeof(float), s);
+    e = cudaMemsetAsync(Y, 0, (size_t)ntok * N * sizeof(float), s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm output clear");
   }
-  static bool attr_set = false;
+  static bool attr_set = false;   // one per instantiation
   if (!attr_set) {
-    e = cudaFuncSetAttribute(gemm::gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)gemm::kSmemBytes);
+    e = cudaFuncSetAttribute(gemm::gemm_kernel<NT, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gemm::smem_bytes(NT));
     if (e != cudaSuccess) return cuda_fail(e, "gemm smem attribute");
     attr_set = true;
   }
-  const int nx = (K >> 3) * gemm::kTok;
-  gemm::x_to_bf16_kernel<<<(nx + 255) / 256, 256, 0, s>>>(X, static_cast<uint8_t*>(ws), K);
+  const int nx = (K >> 3) * NT;
+  gemm::x_layout_kernel<NT, F16><<<(nx + 255) / 256, 256, 0, s>>>(X, static_cast<uint8_t*>(ws), K, ntok);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "gemm x conversion launch");
-  // the GEMM starts while the conversion runs; only its B loader waits for it
+  if (e != cudaSuccess) return cuda_fail(e, "gemm token layout launch");
+  // the GEMM starts while the token layout is written; only its B loader waits for it
   const int grid = p.items < dev.sms ? p.items : dev.sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(gemm::kThreadsG);
-  cfg.dynamicSmemBytes = gemm::kSmemBytes;
+  cfg.dynamicSmemBytes = gemm::smem_bytes(NT);
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemm::gemm_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<NT, F16>, p);
   return e == cudaSuccess ? Q4_OK : cuda_fail(e, "gemm launch");
+}
+
+int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
+                      int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s) {
+  (void)M;
+  return launch_mma<gemm::kTok, false>(codes, scales, X, gemm::kTok, Y, N, K, ws, true, dev, s);
+}
+
+int launch_mma16_f16(const uint8_t* codes, const __half* scales, const __half* X, int ntok, float* Y, int N, int K,
+                     void* ws, const DeviceInfo& dev, cudaStream_t s) {
+  if (ntok < 1 || ntok > 16) return fail(Q4_ERR_SHAPE, "token count %d must be in [1, 16]", ntok);
+  return launch_mma<16, true>(codes, scales, X, ntok, Y, N, K, ws, false, dev, s);
 }
 
 }  // namespace q4w

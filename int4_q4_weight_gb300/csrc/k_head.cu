@@ -183,11 +183,57 @@ static int lpr_for(int nb) {
 
 static int head_grid(const DeviceInfo& dev) { return 2 * dev.sms; }   // >= the streaming head's grid
 
-size_t lmhead_ws_bytes(int V, int K, int b, const DeviceInfo& dev) {
-  (void)V;
-  (void)K;
-  (void)b;
-  return kTicketBytes + (size_t)head_grid(dev) * kMaxBatch * sizeof(Top2);
+// Batch rows 2..8 go through the tensor-core kernel (fp16 weight tiles, one
+// CTA per 128-row tile) when the vocabulary fills every SM with tiles.
+static bool head_tc_eligible(int b, int V, int K, const DeviceInfo& dev) {
+  return b >= 2 && V % 128 == 0 && V >= 128 * dev.sms && K % 64 == 0;
+}
+
+static size_t up256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+size_t lmhead_ws_bytes(int V, int K, int b, const DeviceInfo& dev, bool tensor_cores) {
+  size_t n = kTicketBytes + up256((size_t)head_grid(dev) * kMaxBatch * sizeof(Top2));
+  if (tensor_cores && head_tc_eligible(b, V, K, dev)) n += mma16_ws_bytes(K) + up256((size_t)b * V * sizeof(float));
+  return n;
+}
+
+// Softcap and two-level top-two selection over finished sums z [B][V]: each
+// CTA takes a contiguous slice of rows for every batch row, the last CTA to
+// finish merges the per-CTA partials (head_finish).
+__global__ void __launch_bounds__(256) head_select_kernel(const float* __restrict__ z, int B, int V, float cap,
+                                                          float* __restrict__ logits, Top2* partials,
+                                                          unsigned* ticket, int32_t* idx, float* top1, float* top2) {
+  __shared__ Top2 st[8][kMaxBatch];
+  const int per = (V + gridDim.x - 1) / gridDim.x;
+  const int v0 = blockIdx.x * per, v1 = min(V, v0 + per);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int b = 0; b < B; ++b) {
+    Top2 t;
+    top2_init(t);
+    const float* zr = z + (size_t)b * V;
+    for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+      const float x = zr[v];
+      top2_insert(t, x, v);
+      if (logits) logits[(size_t)b * V + v] = cap * tanhf(x / cap);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      Top2 u;
+      u.v1 = __shfl_xor_sync(0xffffffffu, t.v1, o);
+      u.v2 = __shfl_xor_sync(0xffffffffu, t.v2, o);
+      u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
+      u.i2 = __shfl_xor_sync(0xffffffffu, t.i2, o);
+      top2_merge(t, u);
+    }
+    if (lane == 0) st[warp][b] = t;
+  }
+  __syncthreads();
+  if (threadIdx.x < B) {
+    Top2 t;
+    top2_init(t);
+    for (int w = 0; w < 8; ++w) top2_merge(t, st[w][threadIdx.x]);
+    partials[(size_t)blockIdx.x * kMaxBatch + threadIdx.x] = t;
+  }
+  head_finish(partials, ticket, B, cap, idx, top1, top2);
 }
 
 template <int LPR>
@@ -228,10 +274,10 @@ static cudaError_t launch_head_t(const uint8_t* codes, const __half* scales, con
 
 int launch_lmhead(const uint8_t* codes, const __half* scales, const __half* h, int b, int V, int K,
                   float cap, int32_t* idx, float* top1, float* top2, float* logits, void* ws,
-                  const DeviceInfo& dev, cudaStream_t s) {
+                  const DeviceInfo& dev, cudaStream_t s, bool tensor_cores) {
   if (b == 1 && (size_t)(K >> 5) * kXStride * sizeof(float) > (size_t)200 * 1024)
     return fail(Q4_ERR_SHAPE, "lmhead: K %d does not fit in shared memory", K);
-  if (b > 1 && head_batch_smem(b, K) > (size_t)220 * 1024)
+  if (b > 1 && !(tensor_cores && head_tc_eligible(b, V, K, dev)) && head_batch_smem(b, K) > (size_t)220 * 1024)
     return fail(Q4_ERR_SHAPE, "lmhead: batch %d x K %d does not fit in shared memory", b, K);
   if (b == 1 && stream_eligible(K))
     return launch_head_stream(codes, scales, h, V, K, cap, idx, top1, top2, logits, ws, dev, s);
@@ -239,6 +285,18 @@ int launch_lmhead(const uint8_t* codes, const __half* scales, const __half* h, i
   Top2* partials = reinterpret_cast<Top2*>(reinterpret_cast<char*>(ws) + kTicketBytes);
   cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return cuda_fail(e, "lmhead ticket reset");
+  if (tensor_cores && head_tc_eligible(b, V, K, dev)) {
+    // z = W h on the tensor cores into the workspace, then softcap + top-two
+    char* base = reinterpret_cast<char*>(ws) + kTicketBytes + up256((size_t)head_grid(dev) * kMaxBatch * sizeof(Top2));
+    void* xws = base;
+    float* z = reinterpret_cast<float*>(base + mma16_ws_bytes(K));
+    const int st = launch_mma16_f16(codes, scales, h, b, z, V, K, xws, dev, s);
+    if (st != Q4_OK) return st;
+    int grid = head_grid(dev);
+    head_select_kernel<<<grid, 256, 0, s>>>(z, b, V, cap, logits, partials, ticket, idx, top1, top2);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? Q4_OK : cuda_fail(e, "lmhead select launch");
+  }
   if (b > 1) {
     int grid = head_grid(dev);
     const int need = (V + 7) / 8;   // at least one row per group of the smallest grouping

@@ -66,7 +66,7 @@ extern "C" int lmhead_softcap_argmax_noalloc(const uint8_t* codes, const uint16_
   DeviceInfo dev;
   int st = current_device(&dev);
   if (st != Q4_OK) return st;
-  const size_t need = lmhead_ws_bytes(V, K, b, dev);
+  const size_t need = lmhead_ws_bytes(V, K, b, dev, false);
   if (need > kHeadStaticScratchBytes)
     return fail(Q4_ERR_WORKSPACE,
                 "this device needs %zu bytes of head scratch, above the %zu-byte static maximum; use "
@@ -77,5 +77,5 @@ extern "C" int lmhead_softcap_argmax_noalloc(const uint8_t* codes, const uint16_
   // The launcher clears the ticket word on the stream before the kernel; the
   // partial records are fully rewritten by every call.
   return launch_lmhead(codes, reinterpret_cast<const __half*>(scales), reinterpret_cast<const __half*>(h_f16), b,
-                       V, K, cap, idx, top1, top2, logits_opt, ws, dev, reinterpret_cast<cudaStream_t>(stream));
+                       V, K, cap, idx, top1, top2, logits_opt, ws, dev, reinterpret_cast<cudaStream_t>(stream), false);
 }

@@ -67,10 +67,13 @@ int launch_gemv_batched(const uint8_t* codes, const __half* scales, const __half
 int launch_rmsnorm_f16(const float* in, int H, float eps, __half* out, cudaStream_t s, bool pdl);
 int launch_quantize(const float* W, int N, int K, uint8_t* codes, __half* scales, int32_t* err,
                     const DeviceInfo& dev, cudaStream_t s);
+// tensor_cores: batch rows 2..8 may use the tensor-core kernel (fp16 weight
+// tiles; its workspace holds z [b][V]); false keeps every batch on the CUDA
+// cores with the small workspace.
 int launch_lmhead(const uint8_t* codes, const __half* scales, const __half* h, int b, int V, int K,
                   float cap, int32_t* idx, float* top1, float* top2, float* logits, void* ws,
-                  const DeviceInfo& dev, cudaStream_t s);
-size_t lmhead_ws_bytes(int V, int K, int b, const DeviceInfo& dev);
+                  const DeviceInfo& dev, cudaStream_t s, bool tensor_cores = true);
+size_t lmhead_ws_bytes(int V, int K, int b, const DeviceInfo& dev, bool tensor_cores = true);
 int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_scale, int V, int L,
                int ld, float embed_scale, const float* proj, const __half* hidden, int D,
                const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
@@ -98,5 +101,12 @@ int encode_tensor_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type
 size_t gemm_ws_bytes(int K);   // the bf16 copy of X [64][K]
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s);
+// Y[t][n] for t < ntok <= 16 through the tensor-core kernel with fp16 tiles
+// (weights rounded once to fp16, tokens exact), one CTA per 128-row tile (no
+// split of K, so every row is summed in one fixed order).  N % 128 == 0,
+// K % 64 == 0; ws: mma16_ws_bytes(K) bytes for the token operand.
+size_t mma16_ws_bytes(int K);
+int launch_mma16_f16(const uint8_t* codes, const __half* scales, const __half* X, int ntok, float* Y, int N, int K,
+                     void* ws, const DeviceInfo& dev, cudaStream_t s);
 
 }  // namespace q4w
