@@ -197,33 +197,48 @@ size_t lmhead_ws_bytes(int V, int K, int b, const DeviceInfo& dev, bool tensor_c
   return n;
 }
 
-// Softcap and two-level top-two selection over finished sums z [B][V]: each
-// CTA takes a contiguous slice of rows for every batch row, the last CTA to
-// finish merges the per-CTA partials (head_finish).
+// Softcap and two-level top-two selection over finished sums z [B][V]
+// (V % 4 == 0): each CTA takes a contiguous slice of rows for every batch row,
+// four per thread per pass as one 16-byte load (the loads of a pass are
+// independent, so they are in flight together); the last CTA to finish
+// merges the per-CTA partials (head_finish).
 __global__ void __launch_bounds__(256) head_select_kernel(const float* __restrict__ z, int B, int V, float cap,
                                                           float* __restrict__ logits, Top2* partials,
                                                           unsigned* ticket, int32_t* idx, float* top1, float* top2) {
   __shared__ Top2 st[8][kMaxBatch];
-  const int per = (V + gridDim.x - 1) / gridDim.x;
-  const int v0 = blockIdx.x * per, v1 = min(V, v0 + per);
+  const int V4 = V >> 2;
+  const int per = (V4 + gridDim.x - 1) / gridDim.x;
+  const int q0 = blockIdx.x * per, q1 = min(V4, q0 + per);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int b = 0; b < B; ++b) {
     Top2 t;
     top2_init(t);
-    const float* zr = z + (size_t)b * V;
-    for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-      const float x = zr[v];
-      top2_insert(t, x, v);
-      if (logits) logits[(size_t)b * V + v] = cap * tanhf(x / cap);
+    const float4* zr = reinterpret_cast<const float4*>(z + (size_t)b * V);
+    float4* lr = logits ? reinterpret_cast<float4*>(logits + (size_t)b * V) : nullptr;
+    for (int q = q0 + threadIdx.x; q < q1; q += 4 * blockDim.x) {
+      float4 x[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int qk = q + k * blockDim.x;
+        x[k] = qk < q1 ? __ldcg(zr + qk) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int qk = q + k * blockDim.x;
+        if (qk < q1) {
+          const int v = 4 * qk;
+          top2_insert(t, x[k].x, v);
+          top2_insert(t, x[k].y, v + 1);
+          top2_insert(t, x[k].z, v + 2);
+          top2_insert(t, x[k].w, v + 3);
+          if (lr)
+            lr[qk] = make_float4(cap * tanhf(x[k].x / cap), cap * tanhf(x[k].y / cap), cap * tanhf(x[k].z / cap),
+                                 cap * tanhf(x[k].w / cap));
+        }
+      }
     }
-    for (int o = 16; o > 0; o >>= 1) {
-      Top2 u;
-      u.v1 = __shfl_xor_sync(0xffffffffu, t.v1, o);
-      u.v2 = __shfl_xor_sync(0xffffffffu, t.v2, o);
-      u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
-      u.i2 = __shfl_xor_sync(0xffffffffu, t.i2, o);
-      top2_merge(t, u);
-    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) top2_shfl_xor_merge(t, o);
     if (lane == 0) st[warp][b] = t;
   }
   __syncthreads();
