@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(kThreads) head_rows_kernel(const uint8_t* __re
                                                             int tasks) {
   extern __shared__ float4 dyn_smem4[];
   float* xs = reinterpret_cast<float*>(dyn_smem4);
-  __shared__ Top2 st[kThreads];
+  __shared__ Top2 st[kWarps];
   const int nb = K >> 5;
   for (int k = threadIdx.x; k < K; k += kThreads) xs_store(xs, k, __half2float(h[k]));
   __syncthreads();
@@ -86,13 +86,24 @@ __global__ void __launch_bounds__(kThreads) head_rows_kernel(const uint8_t* __re
       }
     }
   }
-  st[threadIdx.x] = best;   // non-leaders hold the empty state
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    Top2 t;
-    top2_init(t);
-    for (int i = 0; i < kThreads; ++i) top2_merge(t, st[i]);
-    partials[(size_t)blockIdx.x * kMaxBatch] = t;
+  // the CTA's record (non-leaders hold the empty state): shuffle merges
+  // within each warp, then across the warps
+  {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) top2_shfl_xor_merge(best, o);
+    if (lane == 0) st[warp] = best;
+    __syncthreads();
+    if (warp == 0) {
+      Top2 t;
+      if (lane < kWarps)
+        t = st[lane];
+      else
+        top2_init(t);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) top2_shfl_xor_merge(t, o);
+      if (lane == 0) partials[(size_t)blockIdx.x * kMaxBatch] = t;
+    }
   }
   head_finish(partials, ticket, 1, cap, idx, top1, top2);
 }

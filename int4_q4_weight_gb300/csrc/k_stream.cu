@@ -878,7 +878,7 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
                                                             float* top1, float* top2, long long limit, unsigned* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ int abort_sh;
-  __shared__ Top2 st[kTS];
+  __shared__ Top2 st[kTS / 32];
   const Smem S = carve(smem_raw);
   if (threadIdx.x == 0) abort_sh = 0;
   init_barriers(S);
@@ -900,13 +900,21 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
       consume_stage<1>(a, make_geo(a, 1), gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
     }
   }
-  st[threadIdx.x] = best;
+  // the CTA's record: shuffle merges within each warp, then across the warps
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) top2_shfl_xor_merge(best, o);
+  if (lane == 0) st[warp] = best;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (warp == 0) {
     Top2 t;
-    top2_init(t);
-    for (int i = 0; i < kTS; ++i) top2_merge(t, st[i]);
-    partials[(size_t)blockIdx.x * kMaxBatch] = t;
+    if (lane < kTS / 32)
+      t = st[lane];
+    else
+      top2_init(t);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) top2_shfl_xor_merge(t, o);
+    if (lane == 0) partials[(size_t)blockIdx.x * kMaxBatch] = t;
   }
   head_finish(partials, ticket, 1, cap, idx, top1, top2);
 }
