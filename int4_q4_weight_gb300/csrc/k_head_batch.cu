@@ -47,29 +47,38 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
   float* xb = reinterpret_cast<float*>(hb_smem + (size_t)nb * xstride);   // [nb][NBP] biases
   __shared__ Top2 st[kWarpsHB][kMaxBatch];
 
-  // stage the half pairs (x[32j+8i+jj], x[32j+8i+jj+4]) and the block biases
-  for (int e = threadIdx.x; e < nb * 16 * NBP; e += kThr) {
-    const int b = e % NBP, p = (e / NBP) & 15, j = e / (16 * NBP);
-    uint32_t w = 0u;
-    if (b < B) {
-      const int k = 32 * j + 8 * (p >> 2) + (p & 3);
-      const __half* hv = h + (size_t)b * K;
-      w = (uint32_t)__half_as_ushort(hv[k]) | ((uint32_t)__half_as_ushort(hv[k + 4]) << 16);
-    }
-    xw[j * xstride + p * NBP + b] = w;
-  }
-  for (int e = threadIdx.x; e < nb * NBP; e += kThr) {
-    const int b = e % NBP, j = e / NBP;
-    float se = 0.f, so = 0.f;   // even / odd columns of the block
-    if (b < B) {
-      const __half* hv = h + (size_t)b * K + 32 * j;
+  // stage the half pairs (x[32j+8i+jj], x[32j+8i+jj+4]) and the block biases:
+  // one thread per (batch row b, block j, 8-column chunk i), one 16-byte load
+  // giving the chunk's four pairs and its even / odd column sums; the four
+  // chunks of a block sit in adjacent lanes and add by shuffles (the same
+  // order as the single-vector engine).  Rows b >= B are zero.
+  const int nch = nb * 4;
+  for (int e0 = 0; e0 < NBP * nch; e0 += kThr) {   // uniform trip count: the shuffles use the full mask
+    const int e = e0 + threadIdx.x;
+    const bool in = e < NBP * nch;
+    const int i = e & 3, j = (e >> 2) % nb, b = (e >> 2) / nb;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (in && b < B) v = __ldg(reinterpret_cast<const uint4*>(h + (size_t)b * K + 32 * j + 8 * i));
+    float pe = 0.f, po = 0.f;
+    const uint32_t hv[4] = {v.x, v.y, v.z, v.w};   // hv[q] = (x[8i+2q], x[8i+2q+1])
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        se += __half2float(hv[k]);
-        so += __half2float(hv[k + 1]);
-      }
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hv[q]));
+      pe += f.x;
+      po += f.y;
     }
-    xb[j * NBP + b] = kBiasEven * se + kBiasOdd * so;
+    pe += __shfl_xor_sync(0xffffffffu, pe, 1);
+    po += __shfl_xor_sync(0xffffffffu, po, 1);
+    pe += __shfl_xor_sync(0xffffffffu, pe, 2);
+    po += __shfl_xor_sync(0xffffffffu, po, 2);
+    if (in) {
+      uint32_t* dst = xw + j * xstride + (4 * i) * NBP + b;
+      dst[0 * NBP] = __byte_perm(hv[0], hv[2], 0x5410);   // (x[8i], x[8i+4])
+      dst[1 * NBP] = __byte_perm(hv[0], hv[2], 0x7632);   // (x[8i+1], x[8i+5])
+      dst[2 * NBP] = __byte_perm(hv[1], hv[3], 0x5410);   // (x[8i+2], x[8i+6])
+      dst[3 * NBP] = __byte_perm(hv[1], hv[3], 0x7632);   // (x[8i+3], x[8i+7])
+      if (i == 0) xb[j * NBP + b] = kBiasEven * pe + kBiasOdd * po;
+    }
   }
   __syncthreads();
 
