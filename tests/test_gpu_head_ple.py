@@ -74,6 +74,24 @@ def test_head_full_vocab(cuda_lib, b):
     _head_check(cuda_lib, codes, scales, h, oc, os_, want_logits=(b == 1))
 
 
+@pytest.mark.parametrize("b", [2, 3, 8])
+def test_head_batch_tensor_core_path(cuda_lib, b):
+    # V a multiple of 128 with at least one 128-row tile per SM: batch rows go
+    # through the tensor-core kernel (fp16 weight tiles) and the select pass,
+    # including its softcapped logits output and a repeat with the same bits
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    V, K = 128 * (sms + 9), 1536
+    W, h = synth.head_inputs(seed=83 + b, device="cuda", batch=b, V=V, K=K)
+    codes, scales = cuda_lib.q4_quantize(W)
+    torch.cuda.synchronize()
+    oc, os_ = codes.cpu().numpy(), scales.cpu().numpy().view(np.uint16)
+    _head_check(cuda_lib, codes, scales, h, oc, os_, want_logits=True)
+    a = [t.clone() for t in cuda_lib.lmhead_softcap_argmax(codes, scales, h)[:3]]
+    c = cuda_lib.lmhead_softcap_argmax(codes, scales, h)[:3]
+    torch.cuda.synchronize()
+    assert all(torch.equal(x, y) for x, y in zip(a, c))
+
+
 def test_head_repeatable(cuda_lib):
     W, h = synth.head_inputs(seed=82, device="cuda", batch=2, V=3000, K=512)
     codes, scales = cuda_lib.q4_quantize(W)

@@ -50,3 +50,23 @@ def test_noalloc_head_matches_workspace_head(cuda_lib):
         assert np.all(same | (margin < MARGIN_EXEMPT)), (gi, ri)
         assert_close(g1.cpu().numpy(), r1.cpu().numpy(), what=f"top1 call {call}")
         assert_close(g2.cpu().numpy(), r2.cpu().numpy(), what=f"top2 call {call}")
+
+
+def test_noalloc_head_batch_on_a_tensor_core_sized_vocabulary(cuda_lib):
+    # a vocabulary that sends batch rows of the workspace entry point to the
+    # tensor cores: the no-alloc entry keeps them on the CUDA cores (its static
+    # scratch cannot hold the logits) and agrees within the parity tolerance
+    q4w = cuda_lib
+    lib = q4w.load()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    V = 128 * (sms + 3)
+    W, h = synth.head_inputs(seed=124, device="cuda", batch=8, V=V, K=1536)
+    codes, scales = q4w.q4_quantize(W)
+    gi, g1, g2 = _noalloc(lib, codes, scales, h)
+    ri, r1, r2, _ = q4w.lmhead_softcap_argmax(codes, scales, h)
+    torch.cuda.synchronize()
+    margin = (r1 - r2).cpu().numpy()
+    same = (gi == ri).cpu().numpy()
+    assert np.all(same | (margin < MARGIN_EXEMPT)), (gi, ri)
+    assert_close(g1.cpu().numpy(), r1.cpu().numpy(), what="top1")
+    assert_close(g2.cpu().numpy(), r2.cpu().numpy(), what="top2")
