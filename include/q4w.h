@@ -175,7 +175,13 @@ int ple_gather_project(const int32_t* ids, int S, const int8_t* table,
  *   logits_opt: f32 [b][V] softcapped logits, or NULL.
  *   1 <= b <= 8; V >= 2; K % 32 == 0, 32 <= K <= 32768; cap > 0.
  *   ws: q4_workspace_bytes(Q4_OP_LMHEAD, V, K, b) bytes; its contents on
- *   entry do not matter.  Calls that share one ws must not overlap.       */
+ *   entry do not matter.  Calls that share one ws must not overlap.
+ * Arithmetic: b = 1 sums exact products (fp32 accumulation).  For b >= 2
+ * with V % 128 == 0, V >= 128 x (SM count) and K % 64 == 0, z is computed on
+ * the tensor cores with each weight rounded once to fp16, fp16(d*(q-8)), and
+ * fp32 accumulation (the workspace then also holds z, b*V floats); other
+ * shapes sum exact products on the CUDA cores.  Either way each row's sum
+ * has a fixed order: repeated calls give the same bits.                    */
 int lmhead_softcap_argmax(const uint8_t* codes, const uint16_t* scales,
                           const uint16_t* h_f16, int b, int V, int K, float cap,
                           int32_t* idx, float* top1, float* top2, float* logits_opt,
@@ -194,7 +200,8 @@ int lmhead_softcap_argmax(const uint8_t* codes, const uint16_t* scales,
  * call before any stream capture.  All calls share the one array: calls
  * whose kernels overlap on the GPU (other streams, other host threads) race
  * and must be serialised by the caller.  Arguments and results as in
- * lmhead_softcap_argmax, without ws / ws_bytes; nothing is allocated. */
+ * lmhead_softcap_argmax, without ws / ws_bytes; nothing is allocated;
+ * every batch size sums exact products on the CUDA cores. */
 int lmhead_softcap_argmax_noalloc(const uint8_t* codes, const uint16_t* scales,
                                   const uint16_t* h_f16, int b, int V, int K, float cap,
                                   int32_t* idx, float* top1, float* top2, float* logits_opt,
