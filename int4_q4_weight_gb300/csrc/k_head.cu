@@ -108,80 +108,6 @@ __global__ void __launch_bounds__(kThreads) head_rows_kernel(const uint8_t* __re
   head_finish(partials, ticket, 1, cap, idx, top1, top2);
 }
 
-// b >= 2: one warp per row, lane group g serves batch rows g, g+G, ...
-template <int LPR>
-__global__ void __launch_bounds__(kThreads) head_batched_kernel(const uint8_t* __restrict__ codes,
-                                                               const __half* __restrict__ scales,
-                                                               const __half* __restrict__ h, int B,
-                                                               int V, int K, float cap,
-                                                               float* __restrict__ logits,
-                                                               Top2* partials, unsigned* ticket,
-                                                               int32_t* idx, float* top1,
-                                                               float* top2) {
-  extern __shared__ float4 dyn_smem4[];
-  float* xs = reinterpret_cast<float*>(dyn_smem4);
-  __shared__ Top2 st[kWarps][kMaxBatch];
-  const int nb = K >> 5;
-  const int xstride = nb * kXStride;
-  for (int i = threadIdx.x; i < B * K; i += kThreads) {
-    const int b = i / K, k = i - b * K;
-    xs_store(xs + b * xstride, k, __half2float(h[i]));
-  }
-  __syncthreads();
-  for (int b = 0; b < B; ++b) xs_biases(xs + b * xstride, nb);
-  __syncthreads();
-
-  constexpr int G = 32 / LPR;
-  constexpr int T = (kMaxBatch + G - 1) / G;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane / LPR, li = lane % LPR;
-  const size_t row_bytes = (size_t)(K >> 1);
-  Top2 best[T];
-#pragma unroll
-  for (int t = 0; t < T; ++t) top2_init(best[t]);
-
-  for (int row = blockIdx.x * kWarps + warp; row < V; row += gridDim.x * kWarps) {
-    const uint8_t* cp = codes + (size_t)row * row_bytes;
-    const __half* sp = scales + (size_t)row * nb;
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      if (t * G >= B) break;   // uniform across the warp
-      const int b = g + G * t;
-      const bool okb = b < B;
-      float acc = 0.f;
-      for (int j = li; j < nb; j += LPR) {
-        const uint4 c = ld_stream16(cp + 16 * j);
-        const float d = ld_scale(sp + j);
-        float4 xv[8];
-        float bias;
-        load_xblock(xs + (okb ? b : 0) * xstride, j, xv, bias);
-        acc = fmaf(d, q4_block_dot(c, xv, bias), acc);
-      }
-#pragma unroll
-      for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (li == 0 && okb) {
-        top2_insert(best[t], acc, row);
-        if (logits) logits[(size_t)b * V + row] = cap * tanhf(acc / cap);
-      }
-    }
-  }
-  if (li == 0) {
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      const int b = g + G * t;
-      if (b < B) st[warp][b] = best[t];
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x < B) {
-    Top2 t;
-    top2_init(t);
-    for (int w = 0; w < kWarps; ++w) top2_merge(t, st[w][threadIdx.x]);
-    partials[(size_t)blockIdx.x * kMaxBatch + threadIdx.x] = t;
-  }
-  head_finish(partials, ticket, B, cap, idx, top1, top2);
-}
-
 int launch_head_batch(const uint8_t* codes, const __half* scales, const __half* h, int b, int V, int K, float cap,
                       int32_t* idx, float* top1, float* top2, float* logits, Top2* partials, unsigned* ticket,
                       int grid, cudaStream_t s, float* ydirect = nullptr);
@@ -262,39 +188,25 @@ __global__ void __launch_bounds__(256) head_select_kernel(const float* __restric
   head_finish(partials, ticket, B, cap, idx, top1, top2);
 }
 
+// b = 1 on the CUDA-core kernel (K not eligible for the streaming engine).
 template <int LPR>
-static cudaError_t launch_head_t(const uint8_t* codes, const __half* scales, const __half* h, int B,
-                                 int V, int K, float cap, int32_t* idx, float* top1, float* top2,
-                                 float* logits, Top2* partials, unsigned* ticket, const DeviceInfo& dev,
-                                 cudaStream_t s) {
+static cudaError_t launch_head_t(const uint8_t* codes, const __half* scales, const __half* h, int V, int K,
+                                 float cap, int32_t* idx, float* top1, float* top2, float* logits, Top2* partials,
+                                 unsigned* ticket, const DeviceInfo& dev, cudaStream_t s) {
   const int nb = K >> 5;
   int grid = head_grid(dev);
-  if (B == 1) {
-    constexpr int G = 32 / LPR;
-    constexpr int R = 4;
-    const int tasks = (V + G * R - 1) / (G * R);
-    const int need = (tasks + kWarps - 1) / kWarps;
-    if (grid > need) grid = need;
-    const size_t smem = (size_t)nb * kXStride * sizeof(float);
-    auto k = head_rows_kernel<LPR, R>;
-    if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-    }
-    k<<<grid, kThreads, smem, s>>>(codes, scales, h, V, K, cap, logits, partials, ticket, idx, top1,
-                                   top2, tasks);
-  } else {
-    const int need = (V + kWarps - 1) / kWarps;
-    if (grid > need) grid = need;
-    const size_t smem = (size_t)B * nb * kXStride * sizeof(float);
-    auto k = head_batched_kernel<LPR>;
-    if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-    }
-    k<<<grid, kThreads, smem, s>>>(codes, scales, h, B, V, K, cap, logits, partials, ticket, idx, top1,
-                                   top2);
+  constexpr int G = 32 / LPR;
+  constexpr int R = 4;
+  const int tasks = (V + G * R - 1) / (G * R);
+  const int need = (tasks + kWarps - 1) / kWarps;
+  if (grid > need) grid = need;
+  const size_t smem = (size_t)nb * kXStride * sizeof(float);
+  auto k = head_rows_kernel<LPR, R>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
   }
+  k<<<grid, kThreads, smem, s>>>(codes, scales, h, V, K, cap, logits, partials, ticket, idx, top1, top2, tasks);
   return cudaGetLastError();
 }
 
@@ -330,12 +242,12 @@ int launch_lmhead(const uint8_t* codes, const __half* scales, const __half* h, i
     return launch_head_batch(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, grid, s);
   }
   switch (lpr_for(K >> 5)) {
-    case 32: e = launch_head_t<32>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
-    case 16: e = launch_head_t<16>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
-    case 8: e = launch_head_t<8>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
-    case 4: e = launch_head_t<4>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
-    case 2: e = launch_head_t<2>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
-    default: e = launch_head_t<1>(codes, scales, h, b, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+    case 32: e = launch_head_t<32>(codes, scales, h, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+    case 16: e = launch_head_t<16>(codes, scales, h, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+    case 8: e = launch_head_t<8>(codes, scales, h, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+    case 4: e = launch_head_t<4>(codes, scales, h, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+    case 2: e = launch_head_t<2>(codes, scales, h, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
+    default: e = launch_head_t<1>(codes, scales, h, V, K, cap, idx, top1, top2, logits, partials, ticket, dev, s); break;
   }
   return e == cudaSuccess ? Q4_OK : cuda_fail(e, "lmhead launch");
 }
