@@ -17,8 +17,10 @@
 // partial sums of the rows the other one finishes (64 rows each) through
 // distributed shared memory and add them in a fixed order; then every CTA
 // sends its per-token sum of squares over its 64 finished rows to all four,
-// so each finishes the chunk's RMSNorm for its own rows and adds the
-// gathered table term in the same epilogue.
+// so each finishes the chunk's RMSNorm for its own rows, adds the gathered
+// table term, and writes its [64 tokens][64 columns] output tile (and the
+// gathered bytes) from shared memory with tensor stores.  The table bytes of
+// those columns are fetched at the start by one 64-byte bulk copy per token.
 //
 // Warp roles (192 threads):
 //   warp 0     TMA loads (one elected lane): per stage two K sub-chunks of
@@ -27,16 +29,19 @@
 //              hidden tile [64 tokens][32 fp16]
 //   warp 1     TMEM allocation; the warp runs the MMA loop together and one
 //              elected lane issues the MMAs (8 per stage) and the commits
-//   warps 2-5  widen the hidden tiles to fp32 in the 128-byte swizzle layout
-//              (the B operand), then run the epilogue on their TMEM lane
-//              quarters (warp w reads lanes 32 (w % 4) .. + 31)
+//   warps 2-5  issue the table copies, widen the hidden tiles to fp32 in the
+//              128-byte swizzle layout (the B operand), then run the
+//              epilogue on their TMEM lane quarters (warp w reads lanes
+//              32 (w % 4) .. + 31)
 // A ring of kStages stages (A 32 KB + B 16 KB + hidden 8 KB) is guarded by
 // full (TMA bytes), bready (converter warps, which arrive only after seeing
 // full) and empty (MMA commit) mbarriers; the MMA warp waits on bready alone.
-// Every mbarrier wait is bounded; on expiry the CTA sets its abort flag and
-// the device error word, every role leaves its loop, work in flight is
-// drained, and all four CTAs still meet at every cluster barrier, so none
-// waits for a partner that has given up.
+// The kernel is launched with programmatic dependent launch: its set-up
+// overlaps the previous kernel, its first reads of inputs come after
+// griddepcontrol.wait.  Every mbarrier wait is bounded; on expiry the CTA
+// sets its abort flag and the device error word, every role leaves its loop,
+// work in flight is drained, and all four CTAs still meet at every cluster
+// barrier, so none waits for a partner that has given up.
 #include "q4w_device.cuh"
 #include "q4w_internal.cuh"
 #include "q4w_tc.cuh"
