@@ -131,17 +131,18 @@ __device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
 // their spinning does not take issue slots from the converter warps.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, long long limit,
                                           volatile int* abort_flag, unsigned sleep_ns = 0) {
+  if (tc::mbar_probe(a, parity)) return true;   // the first check does not suspend
   const long long t0 = clock64();
-  while (!mbar_test(a, parity)) {
-    if (sleep_ns) __nanosleep(sleep_ns);
+  for (;;) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > limit) {
+    if (clock64() - t0 > limit) {   // checked before every suspending retry: a zero budget gives up at once
       *abort_flag = 1;
       atomicOr(&g_device_error, 1u);
       return false;
     }
+    if (mbar_test(a, parity)) return true;
+    if (sleep_ns) __nanosleep(sleep_ns);
   }
-  return true;
 }
 
 __device__ __forceinline__ void fence_proxy_async() {

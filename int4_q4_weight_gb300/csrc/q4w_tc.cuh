@@ -36,22 +36,35 @@ __device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_probe(uint32_t a, uint32_t parity) {   // never suspends
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on phase `parity` of an mbarrier.  False when the budget ran
 // out (the CTA's abort flag and bit 0 of *err are then set) or when another
-// role of the CTA is aborting.
+// role of the CTA is aborting.  The first check does not suspend and the
+// budget is checked before every suspending retry, so a zero budget gives up
+// at once on a phase that is not complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, long long limit, volatile int* abort_flag,
                                           unsigned* err, unsigned sleep_ns = 0) {
+  if (mbar_probe(a, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_test(a, parity)) {
-    if (sleep_ns) __nanosleep(sleep_ns);
+  for (;;) {
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       *abort_flag = 1;
       atomicOr(err, 1u);
       return false;
     }
+    if (mbar_test(a, parity)) return true;
+    if (sleep_ns) __nanosleep(sleep_ns);
   }
-  return true;
 }
 
 // Waits (bounded by `cycles`, independent of the wait budget) for phase

@@ -37,6 +37,7 @@ def test_zero_budget_times_out_then_recovers(cuda_lib):
     h0 = synth.normal_f16((256,), 112, "cuda")
     ws = torch.empty(q4w.decode_pass_ws_bytes(layers, 256), dtype=torch.uint8, device="cuda")
     h = torch.empty(256, dtype=torch.float16, device="cuda")
+    pp = synth.ple_inputs(seed=114, device="cuda", S=70, V=300, L=2, D=1536)
     old = q4w.q4_set_wait_limit(0)
     try:
         # several tiles per CTA, so that some wait outlasts the hardware's own
@@ -47,6 +48,8 @@ def test_zero_budget_times_out_then_recovers(cuda_lib):
         _expect_timeout(q4w)
         q4w.q4_decode_pass(layers, h0, h, ws)    # persistent pass
         _expect_timeout(q4w)
+        q4w.ple_gather_project(pp.ids, pp.table, pp.row_scale, pp.proj, pp.hidden, pp.norm_w, L=2)
+        _expect_timeout(q4w)                     # PLE: clusters of four still meet at every barrier
     finally:
         q4w.q4_set_wait_limit(old)
     Y = q4w.q4_gemm_chunk(codes, scales, X)
@@ -55,3 +58,8 @@ def test_zero_budget_times_out_then_recovers(cuda_lib):
     oc, os_ = codes.cpu().numpy(), scales.cpu().numpy().view(np.uint16)
     assert_close(Y.cpu().numpy(), O.q4_gemm_chunk(oc, os_, X.cpu().numpy()), what="gemm after")
     assert_close(y.cpu().numpy(), O.q4_gemv(oc, os_, x1.cpu().numpy()), what="gemv after")
+    out, _ = q4w.ple_gather_project(pp.ids, pp.table, pp.row_scale, pp.proj, pp.hidden, pp.norm_w, L=2)
+    q4w.q4_device_status()
+    ro, _ = O.ple_gather_project(pp.ids.cpu().numpy(), pp.table.cpu().numpy(), pp.row_scale.cpu().numpy(),
+                                 pp.proj.cpu().numpy(), pp.hidden.cpu().numpy(), pp.norm_w.cpu().numpy(), L=2, ld=256)
+    assert_close(out.cpu().numpy(), ro, what="ple after")
