@@ -351,19 +351,27 @@ __device__ __forceinline__ float xform(float v, int mode, float r, float r2) {
   return mode == Q4_IN_RMS2_F32 ? f16_round(t * r2) : t;
 }
 
-// false when aborting (uniform over the consumers)
+// false when aborting (uniform over the consumers).  kDirect: an untagged
+// fp16 input with no normalisation may be read straight from global memory
+// (single-stage kernels; the persistent pass never has such an input).
+template <bool kDirect>
 __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in, float* red8, const Ctl& c) {
   const int tid = threadIdx.x, K = a.K, mode = a.in_mode;
   const bool f16in = mode == Q4_IN_F16 || mode == Q4_IN_RMS_F16;
   const int esz = f16in ? 2 : 4;
   const bool staged = K * esz <= kStageInBytes;
+  // an untagged fp16 input with no normalisation is read once, so each
+  // thread takes its 8-element chunks straight from global memory
+  const bool direct = kDirect && a.in_tag == 0 && mode == Q4_IN_F16;
   float r = 1.f, r2 = 1.f;
   if (staged) {
     bool ok = true;
     if (a.in_tag == 0) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.in);
-      uint4* dst = reinterpret_cast<uint4*>(stage_in);
-      for (int v = tid; v < K * esz / 16; v += kCT) dst[v] = ldcg_v4(src + v);
+      if (!direct) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.in);
+        uint4* dst = reinterpret_cast<uint4*>(stage_in);
+        for (int v = tid; v < K * esz / 16; v += kCT) dst[v] = ldcg_v4(src + v);
+      }
     } else {
       // Tagged words: half | tag << 16 (four per 16 bytes) or float | tag << 32
       // (two per 16 bytes).  A thread issues all of its 16-byte reads at once
@@ -389,7 +397,7 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
         }
       }
     }
-    if (!bar_and(1, kCT, ok)) return false;
+    if (!direct && !bar_and(1, kCT, ok)) return false;
     if (c.tr) c.tr[1] = stamp(c);   // input complete and staged
     // Each thread takes chunks of eight consecutive elements (four chunks per
     // 32-column block): sums of squares for the RMS factors, then x, whose
@@ -398,7 +406,8 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
     const int nch = K >> 3;
     auto load8 = [&](int ch, float (&v)[8]) {
       if (f16in) {
-        const uint4 u = *reinterpret_cast<const uint4*>(stage_in + (size_t)ch * 16);
+        const uint4 u = direct ? ldcg_v4(reinterpret_cast<const uint4*>(a.in) + ch)
+                               : *reinterpret_cast<const uint4*>(stage_in + (size_t)ch * 16);
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -864,7 +873,7 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
     __syncwarp();
   } else {
     pdl_wait();
-    if (eng_prologue(a, S.xs, S.stage_in, S.red, c)) {
+    if (eng_prologue<true>(a, S.xs, S.stage_in, S.red, c)) {
       StageEpi epi{&a};
       consume_stage<NM>(a, make_geo(a, NM), gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
     }
@@ -895,7 +904,7 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
     }
     __syncwarp();
   } else {
-    if (eng_prologue(a, S.xs, S.stage_in, S.red, c)) {
+    if (eng_prologue<true>(a, S.xs, S.stage_in, S.red, c)) {
       HeadEpi epi{&best, logits, cap};
       consume_stage<1>(a, make_geo(a, 1), gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
     }
@@ -1059,7 +1068,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       const StageArgs& a = sa[s & 1];
       if (tr) tr[7] = 0;
       // the prologue waits (bounded) until its whole input carries tag s
-      ok = eng_prologue(a, S.xs, S.stage_in, S.red, c);
+      ok = eng_prologue<false>(a, S.xs, S.stage_in, S.red, c);
       if (!ok) break;
       if (tr) tr[2] = stamp(c);
       StageEpi epi{&a};
