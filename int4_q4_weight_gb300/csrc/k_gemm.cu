@@ -450,7 +450,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           for (int i = 0; i < 2; ++i) {
             const int bb = h + 2 * i;
             if (bb < nb) {
-              code[i] = *reinterpret_cast<const uint4*>(raw + r * 128 + cc * 64 + bb * 16);
+              // the codes tile arrives in the 128-byte swizzle: 16-byte group
+              // j of row r sits at group j ^ (r % 8), so the rows read by a
+              // warp spread over the banks
+              code[i] = *reinterpret_cast<const uint4*>(raw + r * 128 + (((cc * 4 + bb) ^ (r & 7)) << 4));
               d[i] = p.sc_tma ? __half2float(*reinterpret_cast<const __half*>(raw + kRawCodeBytes + r * 16 +
                                                                                 (cc * 4 + bb) * 2))
                               : ld_scale(p.scales + ((size_t)tile * kTileM + r) * (p.K >> 5) + c * 4 + bb);
@@ -663,7 +666,7 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
   gemm::Params p;
   memset(&p, 0, sizeof(p));
   int st = encode_tensor_2d(&p.tm_codes, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N,
-                            gemm::kChunk * gemm::kRawChunks / 2, gemm::kTileM, CU_TENSOR_MAP_SWIZZLE_NONE, "codes");
+                            gemm::kChunk * gemm::kRawChunks / 2, gemm::kTileM, CU_TENSOR_MAP_SWIZZLE_128B, "codes");
   if (st != Q4_OK) return st;
   p.xb = static_cast<const uint8_t*>(ws);
   p.scales = scales;
