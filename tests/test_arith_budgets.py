@@ -1,0 +1,52 @@
+"""Error budgets of the two tensor-core operand roundings (CPU only).
+
+The PLE projection runs in TF32 (the f32 projection keeps a 10-bit mantissa)
+and the batched LM head rounds each dequantised weight once to fp16.  Both
+budgets are checked here by feeding the rounded operand to the oracle (exact
+fp64 arithmetic otherwise) and comparing with the oracle on the exact operand
+under the parity rule, at the real row widths and vocabulary-scale samples.
+The GPU parity tests then gate the kernels themselves against the exact
+oracle.
+"""
+import numpy as np
+
+from oracle import q4_oracle as O
+from parity import MARGIN_EXEMPT, TOL, rel_err
+
+
+def _tf32_truncate(a):
+    """Drop the 13 low mantissa bits of fp32 values (what the tensor core reads)."""
+    u = np.asarray(a, np.float32).view(np.uint32) & np.uint32(0xFFFFE000)
+    return u.view(np.float32)
+
+
+def test_tf32_projection_budget():
+    rng = np.random.default_rng(71)
+    S, L, ld, D, V = 16, 8, 256, 1536, 64
+    proj = (rng.standard_normal((L * ld, D)) * 0.02).astype(np.float32)
+    hidden = rng.standard_normal((S, D)).astype(np.float16)
+    table = np.zeros((V, L * ld), np.int8)        # no gathered term: the projection alone
+    row_scale = rng.uniform(0.001, 0.02, V).astype(np.float32)
+    norm_w = rng.uniform(0.5, 1.5, ld).astype(np.float32)
+    ids = rng.integers(0, V, S).astype(np.int32)
+    exact, _ = O.ple_gather_project(ids, table, row_scale, proj, hidden, norm_w, L=L, ld=ld)
+    tf32, _ = O.ple_gather_project(ids, table, row_scale, _tf32_truncate(proj), hidden, norm_w, L=L, ld=ld)
+    e = rel_err(tf32, exact)
+    assert 0 < e < 0.75 * TOL, e
+
+
+def test_fp16_weight_tile_head_budget():
+    rng = np.random.default_rng(73)
+    V, K, b = 4096, 1536, 8
+    W = (rng.standard_normal((V, K)) * 0.02).astype(np.float32)
+    h = rng.standard_normal((b, K)).astype(np.float16)
+    codes, scales = O.quantize_q4_0(W)
+    _, r1, r2, margin, rs = O.lmhead_softcap_argmax(codes, scales, h)
+    w16 = O.dequantize_q4_0(codes, scales).astype(np.float16).astype(np.float64)   # fp16(d (q - 8))
+    z = h.astype(np.float64) @ w16.T
+    s = O.softcap(z)
+    assert rel_err(s, rs) < 0.75 * TOL
+    gi = np.argmax(s, axis=1)
+    ri = np.argmax(rs, axis=1)
+    for i in range(b):
+        assert gi[i] == ri[i] or margin[i] < MARGIN_EXEMPT
