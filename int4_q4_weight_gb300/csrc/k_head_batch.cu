@@ -47,6 +47,31 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
   float* xb = reinterpret_cast<float*>(hb_smem + (size_t)nb * xstride);   // [nb][NBP] biases
   __shared__ Top2 st[kWarpsHB][kMaxBatch];
 
+  const int P = 1 << lgP;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int li = lane & (P - 1);
+  const int gid = threadIdx.x >> lgP, ngroups = kThr >> lgP;
+  const size_t K2 = (size_t)(K >> 1);
+  const int wg0 = (warp * 32) >> lgP;                  // the warp's first group
+  const int bpl = nb >> lgP;                           // blocks per lane (P divides nb)
+  const int wrow0 = blockIdx.x * ngroups + wg0;        // the warp's first row block
+  // the first kPre blocks of this lane's first row are fetched before x is
+  // staged (they do not depend on x), so their latency overlaps the staging
+  constexpr int kPre = 4;
+  uint4 pc[kPre];
+  float pd[kPre];
+  if (wrow0 < V) {   // uniform per warp
+    const int row0 = wrow0 + (gid - wg0);
+    const int row = row0 < V ? row0 : V - 1;
+#pragma unroll
+    for (int t = 0; t < kPre; ++t) {
+      if (t < bpl) {
+        const int j = li + P * t;
+        pc[t] = ld_stream16(codes + (size_t)row * K2 + 16 * j);
+        pd[t] = ld_scale(scales + (size_t)row * nb + j);
+      }
+    }
+  }
   // stage the half pairs (x[32j+8i+jj], x[32j+8i+jj+4]) and the block biases:
   // one thread per (batch row b, block j, 8-column chunk i), one 16-byte load
   // giving the chunk's four pairs and its even / odd column sums; the four
@@ -82,11 +107,6 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
   }
   __syncthreads();
 
-  const int P = 1 << lgP;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int li = lane & (P - 1);
-  const int gid = threadIdx.x >> lgP, ngroups = kThr >> lgP;
-  const size_t K2 = (size_t)(K >> 1);
   Top2 best[NBP];
 #pragma unroll
   for (int b = 0; b < NBP; ++b) top2_init(best[b]);
@@ -94,9 +114,7 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
   // Row groups of a warp advance together (the shuffles use the full mask);
   // a group past the last row recomputes row V - 1 and drops it.
   const int step = gridDim.x * ngroups;
-  const int wg0 = (warp * 32) >> lgP;                  // the warp's first group
-  const int bpl = nb >> lgP;                           // blocks per lane (P divides nb)
-  for (int wrow = blockIdx.x * ngroups + wg0; wrow < V; wrow += step) {   // uniform per warp
+  for (int wrow = wrow0; wrow < V; wrow += step) {   // uniform per warp
     const int row0 = wrow + (gid - wg0);
     const bool valid = row0 < V;
     const int row = valid ? row0 : V - 1;
@@ -105,10 +123,9 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
     float acc[NBP];
 #pragma unroll
     for (int b = 0; b < NBP; ++b) acc[b] = 0.f;
-    for (int t = 0; t < bpl; ++t) {
+    // block t of this lane: code word c and scale d, into acc
+    auto block = [&](int t, const uint4 c, const float d) {
       const int j = li + P * t;
-      const uint4 c = ld_stream16(cp + 16 * j);
-      const float d = ld_scale(sp + j);
       uint32_t wq[16];
       const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
@@ -141,6 +158,21 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
       }
 #pragma unroll
       for (int b = 0; b < NBP; ++b) acc[b] = fmaf(d, lo[b] + hi[b], acc[b]);
+    };
+    const bool first = wrow == wrow0;
+#pragma unroll
+    for (int t = 0; t < kPre; ++t) {
+      if (t < bpl) {
+        const int j = li + P * t;
+        if (first)
+          block(t, pc[t], pd[t]);
+        else
+          block(t, ld_stream16(cp + 16 * j), ld_scale(sp + j));
+      }
+    }
+    for (int t = kPre; t < bpl; ++t) {
+      const int j = li + P * t;
+      block(t, ld_stream16(cp + 16 * j), ld_scale(sp + j));
     }
 #pragma unroll
     for (int b = 0; b < NBP; ++b)
