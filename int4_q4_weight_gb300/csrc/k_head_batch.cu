@@ -47,28 +47,26 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
   float* xb = reinterpret_cast<float*>(hb_smem + (size_t)nb * xstride);   // [nb][NBP] biases
   __shared__ Top2 st[kWarpsHB][kMaxBatch];
 
-  const int P = 1 << lgP;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int li = lane & (P - 1);
-  const int gid = threadIdx.x >> lgP, ngroups = kThr >> lgP;
-  const size_t K2 = (size_t)(K >> 1);
-  const int wg0 = (warp * 32) >> lgP;                  // the warp's first group
-  const int bpl = nb >> lgP;                           // blocks per lane (P divides nb)
-  const int wrow0 = blockIdx.x * ngroups + wg0;        // the warp's first row block
   // the first kPre blocks of this lane's first row are fetched before x is
   // staged (they do not depend on x), so their latency overlaps the staging
-  constexpr int kPre = 4;
-  uint4 pc[kPre];
-  float pd[kPre];
-  if (wrow0 < V) {   // uniform per warp
-    const int row0 = wrow0 + (gid - wg0);
-    const int row = row0 < V ? row0 : V - 1;
+  // (batch 2..4 only: with 8 vectors the registers would cut the occupancy)
+  constexpr int kPre = NBP == 4 ? 4 : 0;
+  uint4 pc[kPre > 0 ? kPre : 1];
+  float pd[kPre > 0 ? kPre : 1];
+  if constexpr (kPre > 0) {
+    const int P = 1 << lgP, li = (threadIdx.x & 31) & (P - 1), gid = threadIdx.x >> lgP;
+    const int wg0 = ((threadIdx.x >> 5) * 32) >> lgP;
+    const int wrow0 = blockIdx.x * (kThr >> lgP) + wg0;
+    if (wrow0 < V) {   // uniform per warp
+      const int row0 = wrow0 + (gid - wg0);
+      const int row = row0 < V ? row0 : V - 1;
 #pragma unroll
-    for (int t = 0; t < kPre; ++t) {
-      if (t < bpl) {
-        const int j = li + P * t;
-        pc[t] = ld_stream16(codes + (size_t)row * K2 + 16 * j);
-        pd[t] = ld_scale(scales + (size_t)row * nb + j);
+      for (int t = 0; t < kPre; ++t) {
+        if (t < (nb >> lgP)) {
+          const int j = li + P * t;
+          pc[t] = ld_stream16(codes + (size_t)row * (K >> 1) + 16 * j);
+          pd[t] = ld_scale(scales + (size_t)row * nb + j);
+        }
       }
     }
   }
@@ -107,6 +105,14 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
   }
   __syncthreads();
 
+  const int P = 1 << lgP;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int li = lane & (P - 1);
+  const int gid = threadIdx.x >> lgP, ngroups = kThr >> lgP;
+  const size_t K2 = (size_t)(K >> 1);
+  const int wg0 = (warp * 32) >> lgP;                  // the warp's first group
+  const int bpl = nb >> lgP;                           // blocks per lane (P divides nb)
+  const int wrow0 = blockIdx.x * ngroups + wg0;        // the warp's first row block
   Top2 best[NBP];
 #pragma unroll
   for (int b = 0; b < NBP; ++b) top2_init(best[b]);
@@ -159,15 +165,17 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
 #pragma unroll
       for (int b = 0; b < NBP; ++b) acc[b] = fmaf(d, lo[b] + hi[b], acc[b]);
     };
-    const bool first = wrow == wrow0;
+    if constexpr (kPre > 0) {
+      const bool first = wrow == wrow0;
 #pragma unroll
-    for (int t = 0; t < kPre; ++t) {
-      if (t < bpl) {
-        const int j = li + P * t;
-        if (first)
-          block(t, pc[t], pd[t]);
-        else
-          block(t, ld_stream16(cp + 16 * j), ld_scale(sp + j));
+      for (int t = 0; t < kPre; ++t) {
+        if (t < bpl) {
+          const int j = li + P * t;
+          if (first)
+            block(t, pc[t], pd[t]);
+          else
+            block(t, ld_stream16(cp + 16 * j), ld_scale(sp + j));
+        }
       }
     }
     for (int t = kPre; t < bpl; ++t) {
