@@ -7,3 +7,4 @@ imports nothing from the CUDA library.  See :mod:`oracle.q4_oracle`.
 from .q4_oracle import *  # noqa: F401,F403
 from . import q4_oracle  # noqa: F401
 from . import q2_oracle  # noqa: F401
+from . import q8_oracle  # noqa: F401

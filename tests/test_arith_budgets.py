@@ -50,3 +50,23 @@ def test_fp16_weight_tile_head_budget():
     ri = np.argmax(rs, axis=1)
     for i in range(b):
         assert gi[i] == ri[i] or margin[i] < MARGIN_EXEMPT
+
+
+def test_fp16_tile_q8_projection_budget():
+    """The int8 projection enters the tensor core as fp16(code * d), one
+    rounding per weight (2^-11 relative); hidden fp16 is exact."""
+    from oracle import q8_oracle as Q8
+    rng = np.random.default_rng(79)
+    S, L, ld, D, V = 16, 8, 256, 1536, 64
+    proj = (rng.standard_normal((L * ld, D)) * 0.02).astype(np.float32)
+    codes, scales = Q8.quantize_q8_0(proj)
+    hidden = rng.standard_normal((S, D)).astype(np.float16)
+    table = np.zeros((V, L * ld), np.int8)        # no gathered term: the projection alone
+    row_scale = rng.uniform(0.001, 0.02, V).astype(np.float32)
+    norm_w = rng.uniform(0.5, 1.5, ld).astype(np.float32)
+    ids = rng.integers(0, V, S).astype(np.int32)
+    exact, _ = Q8.ple_gather_project_q8(ids, table, row_scale, codes, scales, hidden, norm_w, L=L, ld=ld)
+    tile = Q8.dequantize_q8_0(codes, scales).astype(np.float16).astype(np.float32)
+    rounded, _ = O.ple_gather_project(ids, table, row_scale, tile, hidden, norm_w, L=L, ld=ld)
+    e = rel_err(rounded, exact)
+    assert 0 < e < 0.75 * TOL, e
