@@ -418,6 +418,27 @@ def row_ple(q4w, synth, dev, hbm, bf16_peak, reps=10):
             "copies": ncp}
 
 
+def row_ple_q8(q4w, synth, dev, hbm, bf16_peak, reps=10):
+    """The PLE with the int8 per-block-32 projection (14.6 MB instead of 55 MB)."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    p = synth.ple_inputs(seed=1002, device=dev)
+    codes, scales = q4w.q8_quantize(p.proj)
+    per = codes.numel() + scales.numel() * 2
+    ncp = max(2, math.ceil(2 * l2 / per))
+    cs = [(codes, scales)] + [(codes.clone(), scales.clone()) for _ in range(ncp - 1)]
+    out = torch.empty((64, 8960), dtype=torch.float32, device=dev)
+    t = _time_graph(lambda: [q4w.ple_gather_project_q8(p.ids, p.table, p.row_scale, c, s, p.hidden,
+                                                       p.norm_w, out=out) for c, s in cs], reps) / ncp
+    b = 64 * 8960 + 64 * 4 + per + 64 * 1536 * 2 + 256 * 4 + 64 * 8960 * 4 + 64 * 4
+    flops = 2 * 64 * 8960 * 1536
+    # fp16 operands: the measured bf16 peak (the same nominal dense rate)
+    return {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4),
+            "TFLOP/s": round(flops / t / 1e12, 2), "frac_f16": round(flops / t / 1e12 / bf16_peak, 4),
+            "bound": "hbm (int8 projection widened to fp16 tiles, kind::f16)", "us": round(t * 1e6, 2), "bytes": b,
+            "copies": ncp}
+
+
 def row_gemm(q4w, synth, dev, hbm, bf16_peak, N, K, reps=10):
     """S=64 prefill GEMM; small weights rotate over copies beyond L2."""
     import torch
@@ -465,6 +486,7 @@ def measure_rows(q4w, synth, dev, hbm, clocks, bf16_peak):
     rows["lmhead_b8"] = row_head(q4w, synth, dev, hbm, 8, weights=hw)
     del hw
     rows["ple_s64"] = row_ple(q4w, synth, dev, hbm, bf16_peak)
+    rows["ple_q8_s64"] = row_ple_q8(q4w, synth, dev, hbm, bf16_peak)
     for name, (N, K) in (("gemm_s64_up", (6144, 1536)), ("gemm_s64_down", (1536, 6144)),
                          ("gemm_s64_head", (262144, 1536))):
         rows[name] = row_gemm(q4w, synth, dev, hbm, bf16_peak, N, K)
@@ -473,7 +495,7 @@ def measure_rows(q4w, synth, dev, hbm, clocks, bf16_peak):
     return rows
 
 
-CASES = ("gemv", "gemv_b4", "head_b1", "head_b8", "ple", "gemm_up", "gemm_down", "gemm_head", "q2_gate", "q2_head",
+CASES = ("gemv", "gemv_b4", "head_b1", "head_b8", "ple", "ple_q8", "gemm_up", "gemm_down", "gemm_head", "q2_gate", "q2_head",
          "pass_trace")
 
 
@@ -574,6 +596,8 @@ def run_case(args):
         r = row_head(q4w, synth, dev, hbm, 1 if args.case == "head_b1" else 8, reps)
     elif args.case == "ple":
         r = row_ple(q4w, synth, dev, hbm, bf16, reps)
+    elif args.case == "ple_q8":
+        r = row_ple_q8(q4w, synth, dev, hbm, bf16, reps)
     elif args.case in ("q2_gate", "q2_head"):
         r = row_q2(q4w, synth, dev, hbm, args.case[3:], reps)
     elif args.case == "pass_trace":

@@ -87,6 +87,22 @@ typedef enum q4_op {
 int q4_quantize(const float* W, int N, int K, uint8_t* codes, uint16_t* scales,
                 int32_t* err, q4_stream_t stream);
 
+/* q8_quantize: fp32 W [N][K] -> int8 per-block-32 codes [N][K] + fp16 scales
+ * [N][K/32], the form of the PLE projection ("Gemma-4 E2B mobile mixed-bit
+ * QAT weights", decode recipe: PLE gate/proj and the per-layer model
+ * projection are INT8; official-checkpoint notes: genuinely signed int8, the
+ * projection re-quantised to int8 per block of 32).  Per 32-column block:
+ * a = max |w|; d = a / 127 in fp32; code = clamp(round(w/d), -127, 127) with
+ * an IEEE fp32 quotient and rounding half away from zero; the stored scale
+ * is d rounded to fp16 (nearest-even).  The weight value is scale * code
+ * (two's-complement code, no midpoint).  A block whose d is zero stores
+ * scale +0 and codes 0.
+ *   N >= 1, K >= 32, K % 32 == 0.
+ *   err: optional device int32; set to 1 if a block had a non-finite weight
+ *   or a scale beyond the fp16 range (those blocks are stored as zero).    */
+int q8_quantize(const float* W, int N, int K, int8_t* codes, uint16_t* scales,
+                int32_t* err, q4_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* S=1 decode GEMV ("main", one token per call).                           */
 /* ---------------------------------------------------------------------- */
@@ -158,6 +174,24 @@ int ple_gather_project(const int32_t* ids, int S, const int8_t* table,
                        const float* proj, const uint16_t* hidden_f16, int D,
                        const float* norm_w, float eps, float* out, int8_t* gathered_opt,
                        int32_t* err, q4_stream_t stream);
+
+/* ple_gather_project_q8: ple_gather_project with the projection in int8
+ * per-block-32 form (the q8_quantize layout): proj[j][d] =
+ * proj_scales[j][d/32] * proj_codes[j][d].  On the tensor cores every
+ * projection weight enters as fp16(scale * code), rounded once to nearest
+ * even (hidden fp16 is exact), with fp32 accumulation; the rest is the f32
+ * form's arithmetic.  Source: "Gemma-4 E2B mobile mixed-bit QAT weights",
+ * decode recipe (per_layer_model_projection [8960,1536] INT8) and
+ * official-checkpoint notes (re-quantised to int8 per block of 32).
+ *   proj_codes: int8 [L*ld][D]; proj_scales: fp16 bits [L*ld][D/32]; every
+ *   scale * 127 must be finite in fp16 (|weights| <= 65504).  D % 128 == 0,
+ *   128 <= D <= 2048; every other argument, limit and error as
+ *   ple_gather_project.                                                    */
+int ple_gather_project_q8(const int32_t* ids, int S, const int8_t* table,
+                          const float* row_scale, int V, int L, int ld, float embed_scale,
+                          const int8_t* proj_codes, const uint16_t* proj_scales,
+                          const uint16_t* hidden_f16, int D, const float* norm_w, float eps,
+                          float* out, int8_t* gathered_opt, int32_t* err, q4_stream_t stream);
 
 /* ---------------------------------------------------------------------- */
 /* LM head + softcap + argmax.                                             */

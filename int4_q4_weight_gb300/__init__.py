@@ -17,6 +17,7 @@ import torch
 __all__ = [
     "load", "build", "Q4Error", "q4_quantize", "q4_gemv", "q4_gemv_stage", "q4_rmsnorm_f16",
     "q4_decode_pass", "q4_decode_pass_launches", "q2_gemv", "lmhead_softcap_argmax", "ple_gather_project", "q4_gemm_chunk",
+    "q8_quantize", "ple_gather_project_q8",
     "q4_workspace_bytes", "q4_version", "Q4_IN_F16", "Q4_IN_RMS_F16", "Q4_IN_RMS_F32",
     "Q4_IN_RMS2_F32", "Q4_OP_GEMV", "Q4_OP_GEMM_CHUNK", "Q4_OP_PLE", "Q4_OP_LMHEAD",
     "Q4_OP_DECODE_PASS", "q4_layer", "q4_matrix",
@@ -51,6 +52,8 @@ _SIGS = {
     "q4_gemv": (ci, [vp, vp, vp, vp, ci, ci, ci, vp, csz, vp]),
     "q4_gemm_chunk": (ci, [vp, vp, vp, vp, ci, ci, ci, vp, csz, vp]),
     "ple_gather_project": (ci, [vp, ci, vp, vp, ci, ci, ci, cf, vp, vp, ci, vp, cf, vp, vp, vp, vp]),
+    "q8_quantize": (ci, [vp, ci, ci, vp, vp, vp, vp]),
+    "ple_gather_project_q8": (ci, [vp, ci, vp, vp, ci, ci, ci, cf, vp, vp, vp, ci, vp, cf, vp, vp, vp, vp]),
     "lmhead_softcap_argmax": (ci, [vp, vp, vp, ci, ci, ci, cf, vp, vp, vp, vp, vp, csz, vp]),
     "lmhead_softcap_argmax_noalloc": (ci, [vp, vp, vp, ci, ci, ci, cf, vp, vp, vp, vp, vp]),
     "q4_decode_pass": (ci, [ctypes.POINTER(q4_layer), ci, ci, vp, vp, cf, vp, csz, vp]),
@@ -161,6 +164,23 @@ def q4_quantize(W, codes=None, scales=None, err=None):
     _dev(err, torch.int32, "err")
     _check(lib.q4_quantize(_ptr(W), N, K, _ptr(codes), _ptr(scales), _ptr(err), _stream()),
            "q4_quantize")
+    return codes, scales
+
+
+def q8_quantize(W, codes=None, scales=None, err=None):
+    """fp32 W [N, K] -> (codes int8 [N, K], scales fp16 [N, K/32]), int8 per block of 32."""
+    lib = load()
+    _dev(W, torch.float32, "W")
+    N, K = W.shape
+    if codes is None:
+        codes = torch.empty((N, K), dtype=torch.int8, device=W.device)
+    if scales is None:
+        scales = torch.empty((N, K // 32), dtype=torch.float16, device=W.device)
+    _dev(codes, torch.int8, "codes")
+    _dev(scales, torch.float16, "scales")
+    _dev(err, torch.int32, "err")
+    _check(lib.q8_quantize(_ptr(W), N, K, _ptr(codes), _ptr(scales), _ptr(err), _stream()),
+           "q8_quantize")
     return codes, scales
 
 
@@ -305,6 +325,32 @@ def ple_gather_project(ids, table, row_scale, proj, hidden, norm_w, L=35, ld=256
     _check(lib.ple_gather_project(_ptr(ids), S, _ptr(table), _ptr(row_scale), V, L, ld, embed_scale,
                                   _ptr(proj), _ptr(hidden), D, _ptr(norm_w), eps, _ptr(out),
                                   _ptr(gathered), _ptr(err), _stream()), "ple_gather_project")
+    return out, gathered
+
+
+def ple_gather_project_q8(ids, table, row_scale, proj_codes, proj_scales, hidden, norm_w, L=35, ld=256,
+                          embed_scale=16.0, eps=1e-6, out=None, gathered=None, err=None):
+    """ple_gather_project with the projection as int8 codes [L*ld, D] and fp16
+    scales [L*ld, D/32]; returns (out f32 [S, L*ld], gathered int8 or None)."""
+    lib = load()
+    _dev(ids, torch.int32, "ids")
+    _dev(table, torch.int8, "table")
+    _dev(row_scale, torch.float32, "row_scale")
+    _dev(proj_codes, torch.int8, "proj_codes")
+    _dev(proj_scales, torch.float16, "proj_scales")
+    _dev(hidden, torch.float16, "hidden")
+    _dev(norm_w, torch.float32, "norm_w")
+    S = ids.numel()
+    V = table.shape[0]
+    D = proj_codes.shape[1]
+    if out is None:
+        out = torch.empty((S, L * ld), dtype=torch.float32, device=ids.device)
+    _dev(out, torch.float32, "out")
+    _dev(gathered, torch.int8, "gathered")
+    _dev(err, torch.int32, "err")
+    _check(lib.ple_gather_project_q8(_ptr(ids), S, _ptr(table), _ptr(row_scale), V, L, ld, embed_scale,
+                                     _ptr(proj_codes), _ptr(proj_scales), _ptr(hidden), D, _ptr(norm_w), eps,
+                                     _ptr(out), _ptr(gathered), _ptr(err), _stream()), "ple_gather_project_q8")
     return out, gathered
 
 

@@ -25,8 +25,8 @@
 // Warp roles (192 threads):
 //   warp 0     TMA loads (one elected lane): per stage two K sub-chunks of
 //              32 columns, each a projection tile [128 rows][32 fp32]
-//              (128-byte swizzle, the tensor core's K-major layout) and a
-//              hidden tile [64 tokens][32 fp16]
+//              (128-byte swizzle, the tensor core's K-major layout), and the
+//              stage's hidden tile [64 tokens][64 fp16]
 //   warp 1     TMEM allocation; the warp runs the MMA loop together and one
 //              elected lane issues the MMAs (8 per stage) and the commits
 //   warps 2-5  issue the table copies, widen the hidden tiles to fp32 in the
@@ -66,8 +66,31 @@ constexpr int kThreads = 192;
 constexpr int kEpi0 = 2;                            // first converter / epilogue warp
 constexpr int kTmemCols = 64;
 constexpr int kCluster = 4;
-constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kRecvBytes + kGtabBytes;
 constexpr long long kDrainCycles = 2000000000LL;
+
+// int8 projection (per-block-32 codes + fp16 scales): one stage is 128 K
+// columns, so that every code row of the tile is one full 128-byte line; the
+// operands are two 64-column halves, each a 128-byte row of fp16 per operand
+// row in the 128-byte swizzle.
+constexpr int kQC = 128;                            // K columns per stage
+constexpr int kQStages = 3;
+constexpr int kQAHalf = kRows * 64 * 2;             // 16 KB: fp16 weights of 64 columns
+constexpr int kQBHalf = kTok * 64 * 2;              // 8 KB: fp16 hidden of 64 columns (tensor load)
+constexpr int kQABytes = 2 * kQAHalf;
+constexpr int kQBBytes = 2 * kQBHalf;
+constexpr int kQRawBytes = kRows * kQC;             // 16 KB int8 codes [128 rows][128]
+constexpr int kQStageBytes = kQABytes + kQBBytes + kQRawBytes;   // 64 KB, a multiple of 1024
+constexpr int kQMaxStages = 8;                      // stages per K half: D <= 2048
+constexpr int kQScBytes = kQMaxStages * kRows * 8;  // per (stage, row): the stage's four fp16 scales
+
+template <bool Q8>
+constexpr size_t ring_bytes() {
+  return Q8 ? (size_t)kQStages * kQStageBytes : (size_t)kStages * kStageBytes;
+}
+template <bool Q8>
+constexpr size_t smem_bytes() {
+  return 1024 + ring_bytes<Q8>() + kRecvBytes + kGtabBytes + (Q8 ? kQScBytes : 0);
+}
 
 // Instruction descriptor, kind::tf32: D f32, A and B tf32, both K-major,
 // M = 128, N = n (a multiple of 16).
@@ -84,11 +107,44 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Instruction descriptor, kind::f16: D f32, A and B fp16, both K-major.
+__device__ __forceinline__ uint32_t idesc_f16(int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+// Eight int8 codes (two words, column order) -> the fp16 values fp16(code * d)
+// in column order.  Each byte, offset to code + 128, becomes the low byte of
+// the fp16 number 1024 + (code + 128) (the byte lands in the mantissa);
+// subtracting 1152 leaves the exact integer code, and the half multiply
+// rounds code * d once, to nearest even.
+__device__ __forceinline__ uint4 dequant_i8_f16(uint2 c, __half2 dd) {
+  const __half2 off = __half2half2(__ushort_as_half(0x6480));   // 1152
+  auto two = [&](uint32_t u, uint32_t sel) {
+    const uint32_t h = __byte_perm(u, 0x64646464u, sel);
+    const __half2 v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&h), off), dd);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  };
+  const uint32_t u0 = c.x ^ 0x80808080u, u1 = c.y ^ 0x80808080u;
+  return make_uint4(two(u0, 0x4140u), two(u0, 0x4342u), two(u1, 0x4140u), two(u1, 0x4342u));
+}
+
 struct Params {
-  CUtensorMap tm_proj;   // f32 [L*ld][D], box [128 rows][32], 128-byte swizzle
-  CUtensorMap tm_hid;    // fp16 bits [S][D], box [64 rows][32]; rows past S read as zero
+  CUtensorMap tm_proj;   // f32 [L*ld][D], box [128 rows][32], 128-byte swizzle;
+                         // int8 form: codes [L*ld][D], box [128 rows][64], no swizzle
+  CUtensorMap tm_hid;    // fp16 bits [S][D], box [64 rows][32]; rows past S read as zero;
+                         // int8 form: box [64 rows][64], 128-byte swizzle
   CUtensorMap tm_out;    // f32 out [S][L*ld], box [64 tokens][64 columns]; rows past S not written
   CUtensorMap tm_gat;    // int8 gathered [S][L*ld], box [64 tokens][64 columns] (when gathered != NULL)
+  const uint2* proj_sc;      // int8 form: fp16 scales [L*ld][D/32] read as quads [L*ld][D/128]
   const int32_t* ids;
   const int8_t* table;
   const float* row_scale;
@@ -98,6 +154,7 @@ struct Params {
   int32_t* err;          // optional id-range flag
   unsigned* dev_err;     // the library's device error word (bounded waits)
   int S, V, L, D;
+  uint32_t hid_box_bytes;   // f32 form: bytes of one hidden tile (64 columns, or 32 when D == 32)
   float embed_scale, eps;
   long long wait_limit;
   unsigned long long* trace;   // optional: CTA 0 stamps [stage][8], SM cycles since the start
@@ -129,14 +186,22 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Q8: the projection is int8 per-block-32 (codes + fp16 scales), widened to
+// fp16 tiles by the converter warps and multiplied on kind::f16 (the hidden
+// tile then goes to the tensor core straight from its tensor load).
+template <bool Q8>
 __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_constant__ Params p) {
+  constexpr int kSt = Q8 ? kQStages : kStages;            // ring stages
+  constexpr int kStB = Q8 ? kQStageBytes : kStageBytes;   // bytes per stage
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   // partner's partial sums, [token / 4][64 rows][4 tokens]
-  float* recv = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
+  float* recv = reinterpret_cast<float*>(smem + ring_bytes<Q8>());
   // table bytes of this CTA's 64 finished rows, [token][64]
-  int8_t* gtab = reinterpret_cast<int8_t*>(smem + (size_t)kStages * kStageBytes + kRecvBytes);
-  __shared__ __align__(8) uint64_t bars[3 * kStages + 3];   // full, bready, empty, accfull, drain, gbar
+  int8_t* gtab = reinterpret_cast<int8_t*>(smem + ring_bytes<Q8>() + kRecvBytes);
+  // Q8: per (stage, row) the stage's four block scales, [stage][128 rows]
+  uint2* scs = reinterpret_cast<uint2*>(smem + ring_bytes<Q8>() + kRecvBytes + kGtabBytes);
+  __shared__ __align__(8) uint64_t bars[3 * kSt + 3];   // full, bready, empty, accfull, drain, gbar
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
   __shared__ long long t0_sh;
@@ -154,12 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   const int t0 = blockIdx.y * kTok;
   const int ntok = min(kTok, p.S - t0);
   const int npad = (ntok + 15) & ~15;
-  const int nsub = p.D / kKC;
-  const int sb = kh == 0 ? 0 : (nsub + 1) / 2, se = kh == 0 ? (nsub + 1) / 2 : nsub;   // my sub-chunks
-  const int ns = (se - sb + kSub - 1) / kSub;      // my stages (0 only when D has one sub-chunk)
+  // K units: 32-column sub-chunks (f32), a contiguous half per K half; or
+  // 128-column stages (int8), interleaved: stage st of K half kh is unit
+  // 2 st + kh
+  const int nsub = p.D / (Q8 ? kQC : kKC);
+  const int sb = kh == 0 ? 0 : (nsub + 1) / 2, se = kh == 0 ? (nsub + 1) / 2 : nsub;   // f32: my units
+  const int ns = Q8 ? (nsub + 1 - kh) / 2 : (se - sb + kSub - 1) / kSub;   // my stages (0 only when D has one unit)
   const int PLD = p.L * kLd;
-  const uint32_t full0 = tc::smem_u32(bars), bready0 = full0 + 8 * kStages, empty0 = bready0 + 8 * kStages;
-  const uint32_t accfull = empty0 + 8 * kStages, drain = accfull + 8, gbar = drain + 8;
+  const uint32_t full0 = tc::smem_u32(bars), bready0 = full0 + 8 * kSt, empty0 = bready0 + 8 * kSt;
+  const uint32_t accfull = empty0 + 8 * kSt, drain = accfull + 8, gbar = drain + 8;
   volatile int* abort_flag = &abort_sh;
   unsigned long long* const tr = (p.trace && blockIdx.x == 0 && blockIdx.y == 0) ? p.trace : nullptr;
   // with a trace: every CTA's start and end (globaltimer ns) after the stage stamps
@@ -174,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     abort_sh = 0;
     t0_sh = tc::clock_ordered();
     if (trc) trc[0] = tc::globaltimer();
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSt; ++s) {
       tc::mbar_init(full0 + 8 * s, 1);
       tc::mbar_init(bready0 + 8 * s, 4);
       tc::mbar_init(empty0 + 8 * s, 1);
@@ -190,22 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   // kernel's results are visible
   pdl_trigger();
   pdl_wait();
-  if (threadIdx.x >= kEpi0 * 32 && threadIdx.x < kEpi0 * 32 + kTok) {
-    const int t = threadIdx.x - kEpi0 * 32;
-    int id = -1;
-    float sc = 0.f;
-    if (t < ntok) {
-      const int v = p.ids[t0 + t];
-      if (v >= 0 && v < p.V) {
-        id = v;
-        sc = p.row_scale[v];
-      } else if (p.err) {
-        atomicExch(p.err, 1);
-      }
-    }
-    tid_sh[t] = id;
-    tsc[t] = sc;
-  }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -220,34 +272,47 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     const uint32_t st0 = tc::smem_u32(smem);
     int st = 0;
     for (; st < ns; ++st) {
-      const int s = st % kStages, round = st / kStages;
+      const int s = st % kSt, round = st / kSt;
       const bool free_ = tc::mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, p.dev_err);
       if (!__all_sync(0xffffffffu, free_)) break;
-      if (elect_one()) {
+      if constexpr (Q8) {
+        if (elect_one()) {
+          const uint32_t A = st0 + s * kStB;
+          stamp(st, 0);
+          tc::mbar_expect_tx(full0 + 8 * s, (uint32_t)(kQRawBytes + kQBBytes));
+          // x = 128 (2 st + kh) int8 code bytes / fp16 hidden columns (+ 64): 16-byte aligned
+          const int x = (2 * st + kh) * kQC;
+          tc::tma_load_2d(A + kQABytes + kQBBytes, &p.tm_proj, x, row0, full0 + 8 * s, pol_once);
+          tc::tma_load_2d(A + kQABytes, &p.tm_hid, x, t0, full0 + 8 * s, pol_keep);
+          tc::tma_load_2d(A + kQABytes + kQBHalf, &p.tm_hid, x + 64, t0, full0 + 8 * s, pol_keep);
+        }
+      } else if (elect_one()) {
         const int nsc = nsc_of(st);
         const uint32_t A = st0 + s * kStageBytes, H = A + kSub * (kABytes + kBBytes);
         stamp(st, 0);
-        tc::mbar_expect_tx(full0 + 8 * s, (uint32_t)nsc * (kABytes + kHBytes));
+        // the hidden tile of the whole stage is one box of 128-byte rows
+        // [64 tokens][64 fp16] (columns past D read as zero)
+        tc::mbar_expect_tx(full0 + 8 * s, (uint32_t)nsc * kABytes + p.hid_box_bytes);
         for (int a = 0; a < nsc; ++a) {
-          // x = 32 (sb + 2 st + a) fp32 / fp16 columns: 16-byte aligned
+          // x = 32 (sb + 2 st + a) fp32 columns: 16-byte aligned
           const int x = (sb + kSub * st + a) * kKC;
           tc::tma_load_2d(A + a * kABytes, &p.tm_proj, x, row0, full0 + 8 * s, pol_once);
-          tc::tma_load_2d(H + a * kHBytes, &p.tm_hid, x, t0, full0 + 8 * s, pol_keep);
         }
+        tc::tma_load_2d(H, &p.tm_hid, (sb + kSub * st) * kKC, t0, full0 + 8 * s, pol_keep);
       }
       __syncwarp();
     }
     // every issued load lands before the CTA may exit
-    for (int q = max(0, st - kStages); q < st; ++q)
-      tc::mbar_drain(full0 + 8 * (q % kStages), (q / kStages) & 1, kDrainCycles, p.dev_err);
+    for (int q = max(0, st - kSt); q < st; ++q)
+      tc::mbar_drain(full0 + 8 * (q % kSt), (q / kSt) & 1, kDrainCycles, p.dev_err);
     tc::mbar_drain(gbar, 0, kDrainCycles, p.dev_err);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t st0 = tc::smem_u32(smem);
-    const uint32_t idesc = idesc_tf32(npad);
+    const uint32_t idesc = Q8 ? idesc_f16(npad) : idesc_tf32(npad);
     bool ok = true;
     for (int st = 0; st < ns; ++st) {
-      const int s = st % kStages, round = st / kStages;
+      const int s = st % kSt, round = st / kSt;
       // bready completes only after the converter warps have seen this
       // stage's TMA bytes land (full), so it orders the projection tile too
       ok = tc::mbar_wait(bready0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
@@ -258,13 +323,23 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
       tc::fence_after();
       if (elect_one()) {
         stamp(st, 3);
-        const int nsc = nsc_of(st);
-        const uint32_t A = st0 + s * kStageBytes, B = A + kSub * kABytes;
-        for (int a = 0; a < nsc; ++a) {
+        if constexpr (Q8) {
+          const uint32_t A = st0 + s * kStB, B = A + kQABytes;
 #pragma unroll
-          for (int k = 0; k < kKC / 8; ++k)   // K = 8 tf32 (32 bytes) per MMA
-            mma_tf32(tmem, tc::desc_sw128(A + a * kABytes + 32 * k), tc::desc_sw128(B + a * kBBytes + 32 * k), idesc,
-                     (st | a | k) ? 1u : 0u);
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)   // K = 16 fp16 (32 bytes) per MMA
+              mma_f16(tmem, tc::desc_sw128(A + h * kQAHalf + 32 * k), tc::desc_sw128(B + h * kQBHalf + 32 * k), idesc,
+                      (st | h | k) ? 1u : 0u);
+        } else {
+          const int nsc = nsc_of(st);
+          const uint32_t A = st0 + s * kStB, B = A + kSub * kABytes;
+          for (int a = 0; a < nsc; ++a) {
+#pragma unroll
+            for (int k = 0; k < kKC / 8; ++k)   // K = 8 tf32 (32 bytes) per MMA
+              mma_tf32(tmem, tc::desc_sw128(A + a * kABytes + 32 * k), tc::desc_sw128(B + a * kBBytes + 32 * k),
+                       idesc, (st | a | k) ? 1u : 0u);
+          }
         }
         tc::commit(empty0 + 8 * s);
         stamp(st, 4);
@@ -281,22 +356,82 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   } else {
     // ------------------------------------- B operand: fp16 hidden -> fp32 tile
     const int ct = threadIdx.x - kEpi0 * 32;   // 0..127
-    // the table bytes of the finished rows: one 64-byte copy per valid token,
-    // issued by that token's thread (column row0 + 64 kh and the row width
-    // L * 256 are multiples of 16 bytes); thread 0 posts the byte count
-    if (ct < kTok && !(ct < ntok && tid_sh[ct] >= 0))   // no copy: the gathered bytes are zero
-      for (int e = 0; e < 64; e += 16) *reinterpret_cast<uint4*>(gtab + ct * 64 + e) = make_uint4(0u, 0u, 0u, 0u);
-    if (ct < ntok && tid_sh[ct] >= 0)
-      tc::bulk_load(tc::smem_u32(gtab + ct * 64), p.table + (size_t)tid_sh[ct] * PLD + (size_t)row0 + 64 * kh, 64,
-                    gbar, tc::policy_evict_first());
+    // token ct's id; the table bytes of the finished rows: one 64-byte copy
+    // per valid token, issued by that token's thread (column row0 + 64 kh and
+    // the row width L * 256 are multiples of 16 bytes); thread 0 posts the
+    // byte count.  The token's table scale is only needed by the epilogue:
+    // its load stays in flight through the stage loop.
+    int my_id = -1;
+    float my_sc = 0.f;
+    if (ct < ntok) {
+      const int v = p.ids[t0 + ct];
+      if (v >= 0 && v < p.V)
+        my_id = v;
+      else if (p.err)
+        atomicExch(p.err, 1);
+    }
+    if (ct < kTok) {
+      tid_sh[ct] = my_id;
+      if (my_id >= 0) {
+        tc::bulk_load(tc::smem_u32(gtab + ct * 64), p.table + (size_t)my_id * PLD + (size_t)row0 + 64 * kh, 64,
+                      gbar, tc::policy_evict_first());
+        my_sc = p.row_scale[my_id];
+      } else {   // no copy: the gathered bytes are zero
+        for (int e = 0; e < 64; e += 16) *reinterpret_cast<uint4*>(gtab + ct * 64 + e) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    if constexpr (Q8) {
+      // the block scales of this CTA's rows over its stages (row stride D/128
+      // quads), all loads in flight together
+      const uint2* src = p.proj_sc + (size_t)(row0 + ct) * (p.D / kQC) + kh;
+      uint2 v[kQMaxStages];
+#pragma unroll
+      for (int u = 0; u < kQMaxStages; ++u) v[u] = u < ns ? __ldg(src + 2 * u) : make_uint2(0u, 0u);
+#pragma unroll
+      for (int u = 0; u < kQMaxStages; ++u)
+        if (u < ns) scs[u * kRows + ct] = v[u];
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // every id (and block scale) is in shared memory
     if (ct == 0) {
       uint32_t nb = 0;
       for (int t = 0; t < ntok; ++t) nb += tid_sh[t] >= 0 ? 64u : 0u;
       tc::mbar_expect_tx(gbar, nb);
     }
     bool ok = true;
+    if constexpr (Q8) {
+      // ------------------------------- A operand: int8 codes -> fp16 tile
+      for (int st = 0; st < ns; ++st) {
+        const int s = st % kSt, round = st / kSt;
+        const bool landed = tc::mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
+        if (!__all_sync(0xffffffffu, landed)) {   // leave the loop as a whole warp
+          ok = false;
+          break;
+        }
+        if (ct == 0) stamp(st, 1);
+        uint8_t* A = smem + (size_t)s * kStB;
+        const uint8_t* raw = A + kQABytes + kQBBytes;
+        // (row r, 8-column group j of its 128 columns): j = ct % 16 is fixed
+        // per thread, so is its block (j / 4) and operand half (j / 8)
+        const int j = ct & 15, jj = j & 7, h = j >> 3, blk = j >> 2;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = (ct >> 4) + 8 * i;
+          const uint2 c = *reinterpret_cast<const uint2*>(raw + r * kQC + j * 8);
+          const uint2 s4 = scs[st * kRows + r];   // scales of columns 0-31, 32-63 (x), 64-95, 96-127 (y)
+          const uint32_t sw = blk < 2 ? s4.x : s4.y;
+          const __half2 dd = __half2half2(__ushort_as_half((uint16_t)((blk & 1) ? sw >> 16 : sw & 0xFFFFu)));
+          // 128-byte swizzle: group jj of row r sits at group jj ^ (r % 8) of its row
+          *reinterpret_cast<uint4*>(A + h * kQAHalf + (r >> 3) * 1024 + (r & 7) * 128 + ((jj ^ (r & 7)) << 4)) =
+              dequant_i8_f16(c, dd);
+        }
+        tc::fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(bready0 + 8 * s);
+        if (ct == 0) stamp(st, 2);
+      }
+    } else {
     for (int st = 0; st < ns; ++st) {
-      const int s = st % kStages, round = st / kStages;
+      const int s = st % kSt, round = st / kSt;
       const bool landed = tc::mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
       if (!__all_sync(0xffffffffu, landed)) {   // leave the loop as a whole warp
         ok = false;
@@ -304,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
       }
       if (ct == 0) stamp(st, 1);
       uint8_t* B = smem + (size_t)s * kStageBytes + kSub * kABytes;
+      const int hrow = (int)p.hid_box_bytes / kTok;   // bytes per token row of the hidden tile
       const uint8_t* H = B + kSub * kBBytes;
       const int nsc = nsc_of(st);
       for (int a = 0; a < nsc; ++a) {
@@ -312,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
           const int idx = ct + 128 * i;      // (token t, 16-byte group j of its 128-byte row)
           const int t = idx >> 3, j = idx & 7;
           // tokens past S: zero rows (the tensor map already reads them as zero)
-          const uint2 h = t < ntok ? *reinterpret_cast<const uint2*>(H + a * kHBytes + t * (kKC * 2) + j * 8)
+          const uint2 h = t < ntok ? *reinterpret_cast<const uint2*>(H + t * hrow + a * (kKC * 2) + j * 8)
                                    : make_uint2(0u, 0u);
           const float2 x0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
           const float2 x1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
@@ -326,7 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
       if (lane == 0) tc::mbar_arrive(bready0 + 8 * s);
       if (ct == 0) stamp(st, 2);
     }
+    }
     // ------------------------------------------------------------- epilogue
+    if (ct < kTok) tsc[ct] = my_sc;            // read after the barriers below
     const int q = warp & 3;                    // TMEM lane quarter
     const int row = 32 * q + lane;             // row of this CTA's tile
     const bool mine = (q >> 1) == kh;          // rows 64 kh .. 64 kh + 63 are finished here
@@ -455,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
       tc::tma_store_2d(&p.tm_out, x, t0, tc::smem_u32(recv));
       if (p.gathered) tc::tma_store_2d(&p.tm_gat, x, t0, tc::smem_u32(gtab));
       tc::bulk_commit();
-      tc::bulk_wait_all();
+      tc::bulk_wait_read_all();   // the tile has been read; the writes complete with the grid
     }
     if (mine && (q & 1) == 0 && lane == 0) stamp(kTraceRows - 2, 3);
     if (ct == 0) stamp(kTraceRows - 1, 7);
@@ -479,20 +617,34 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
 
 }  // namespace ple
 
-int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_scale, int V, int L,
-               int ld, float embed_scale, const float* proj, const __half* hidden, int D,
-               const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
-               const DeviceInfo& dev, cudaStream_t s) {
-  (void)dev;
+// proj: f32 [L*ld][D], or (Q8) int8 codes [L*ld][D] with fp16 scales proj_sc [L*ld][D/32].
+template <bool Q8>
+static int launch_ple_t(const int32_t* ids, int S, const int8_t* table, const float* row_scale, int V, int L,
+                        int ld, float embed_scale, const void* proj, const uint16_t* proj_sc, const __half* hidden,
+                        int D, const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
+                        cudaStream_t s) {
   if (ld != ple::kLd) return fail(Q4_ERR_SHAPE, "ple_gather_project: ld must be %d", ple::kLd);
   ple::Params p;
   memset(&p, 0, sizeof(p));
-  int st = encode_tensor_2d(&p.tm_proj, proj, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)D, (uint64_t)L * ld,
-                            ple::kKC, ple::kRows, CU_TENSOR_MAP_SWIZZLE_128B, "proj");
-  if (st != Q4_OK) return st;
-  st = encode_tensor_2d(&p.tm_hid, hidden, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)D, (uint64_t)S, ple::kKC,
-                        ple::kTok, CU_TENSOR_MAP_SWIZZLE_NONE, "hidden");
-  if (st != Q4_OK) return st;
+  int st;
+  if (Q8) {
+    st = encode_tensor_2d(&p.tm_proj, proj, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)D, (uint64_t)L * ld, ple::kQC,
+                          ple::kRows, CU_TENSOR_MAP_SWIZZLE_NONE, "proj_codes");
+    if (st != Q4_OK) return st;
+    st = encode_tensor_2d(&p.tm_hid, hidden, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)D, (uint64_t)S, 64,
+                          ple::kTok, CU_TENSOR_MAP_SWIZZLE_128B, "hidden");
+    if (st != Q4_OK) return st;
+    p.proj_sc = reinterpret_cast<const uint2*>(proj_sc);
+  } else {
+    st = encode_tensor_2d(&p.tm_proj, proj, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)D, (uint64_t)L * ld,
+                          ple::kKC, ple::kRows, CU_TENSOR_MAP_SWIZZLE_128B, "proj");
+    if (st != Q4_OK) return st;
+    const int hcols = D >= ple::kSub * ple::kKC ? ple::kSub * ple::kKC : ple::kKC;   // box no wider than D
+    st = encode_tensor_2d(&p.tm_hid, hidden, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)D, (uint64_t)S, hcols,
+                          ple::kTok, CU_TENSOR_MAP_SWIZZLE_NONE, "hidden");
+    p.hid_box_bytes = (uint32_t)(hcols * ple::kTok * 2);
+    if (st != Q4_OK) return st;
+  }
   st = encode_tensor_2d(&p.tm_out, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)L * ld, (uint64_t)S, 64,
                         ple::kTok, CU_TENSOR_MAP_SWIZZLE_NONE, "out");
   if (st != Q4_OK) return st;
@@ -523,17 +675,18 @@ int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_
   p.trace = (tb && tbytes >= trace_words * sizeof(unsigned long long))
                 ? static_cast<unsigned long long*>(tb)
                 : nullptr;
+  constexpr size_t smem = ple::smem_bytes<Q8>();
   static bool attr = false;
   cudaError_t e;
   if (!attr) {
-    e = cudaFuncSetAttribute(ple::ple_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ple::kSmem);
+    e = cudaFuncSetAttribute(ple::ple_tc_kernel<Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "ple smem attribute");
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ple::kCluster * L, (S + ple::kTok - 1) / ple::kTok);
   cfg.blockDim = dim3(ple::kThreads);
-  cfg.dynamicSmemBytes = ple::kSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -544,8 +697,29 @@ int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, ple::ple_tc_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, ple::ple_tc_kernel<Q8>, p);
   return e == cudaSuccess ? Q4_OK : cuda_fail(e, "ple launch");
+}
+
+int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_scale, int V, int L,
+               int ld, float embed_scale, const float* proj, const __half* hidden, int D,
+               const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
+               const DeviceInfo& dev, cudaStream_t s) {
+  (void)dev;
+  return launch_ple_t<false>(ids, S, table, row_scale, V, L, ld, embed_scale, proj, nullptr, hidden, D, norm_w, eps,
+                             out, gathered, err, s);
+}
+
+int launch_ple_q8(const int32_t* ids, int S, const int8_t* table, const float* row_scale, int V, int L, int ld,
+                  float embed_scale, const int8_t* proj_codes, const uint16_t* proj_scales, const __half* hidden,
+                  int D, const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
+                  const DeviceInfo& dev, cudaStream_t s) {
+  (void)dev;
+  if (D % ple::kQC != 0 || D > 2 * ple::kQMaxStages * ple::kQC)
+    return fail(Q4_ERR_SHAPE, "ple_gather_project_q8: D=%d must be a multiple of %d up to %d", D, ple::kQC,
+                2 * ple::kQMaxStages * ple::kQC);
+  return launch_ple_t<true>(ids, S, table, row_scale, V, L, ld, embed_scale, proj_codes, proj_scales, hidden, D,
+                            norm_w, eps, out, gathered, err, s);
 }
 
 }  // namespace q4w

@@ -173,6 +173,23 @@ int q4_quantize(const float* W, int N, int K, uint8_t* codes, uint16_t* scales, 
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+int q8_quantize(const float* W, int N, int K, int8_t* codes, uint16_t* scales, int32_t* err,
+                q4_stream_t stream) {
+  clear_error();
+  CHECK_NULL(W);
+  CHECK_NULL(codes);
+  CHECK_NULL(scales);
+  CHECK_ALIGN(W);
+  CHECK_ALIGN(codes);
+  CHECK_ALIGN(scales);
+  CHECK_ALIGN(err);
+  CHECK(N >= 1, "N=%d must be >= 1", N);
+  CHECK(K >= 32 && K % 32 == 0, "K=%d must be a positive multiple of 32", K);
+  DEVICE_OR_RETURN(dev);
+  return launch_quantize_q8(W, N, K, codes, reinterpret_cast<__half*>(scales), err, dev,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
 int q4_gemv(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16, float* y, int N,
             int K, int batch, void* ws, size_t ws_bytes, q4_stream_t stream) {
   (void)ws;
@@ -443,6 +460,41 @@ int ple_gather_project(const int32_t* ids, int S, const int8_t* table, const flo
   return launch_ple(ids, S, table, row_scale, V, L, ld, embed_scale, proj,
                     reinterpret_cast<const __half*>(hidden_f16), D, norm_w, eps, out, gathered_opt, err,
                     dev, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ple_gather_project_q8(const int32_t* ids, int S, const int8_t* table, const float* row_scale, int V, int L,
+                          int ld, float embed_scale, const int8_t* proj_codes, const uint16_t* proj_scales,
+                          const uint16_t* hidden_f16, int D, const float* norm_w, float eps, float* out,
+                          int8_t* gathered_opt, int32_t* err, q4_stream_t stream) {
+  clear_error();
+  CHECK_NULL(ids);
+  CHECK_NULL(table);
+  CHECK_NULL(row_scale);
+  CHECK_NULL(proj_codes);
+  CHECK_NULL(proj_scales);
+  CHECK_NULL(hidden_f16);
+  CHECK_NULL(norm_w);
+  CHECK_NULL(out);
+  CHECK_ALIGN(ids);
+  CHECK_ALIGN(table);
+  CHECK_ALIGN(row_scale);
+  CHECK_ALIGN(proj_codes);
+  CHECK_ALIGN(proj_scales);
+  CHECK_ALIGN(hidden_f16);
+  CHECK_ALIGN(norm_w);
+  CHECK_ALIGN(out);
+  CHECK_ALIGN(gathered_opt);
+  CHECK_ALIGN(err);
+  CHECK(S >= 1 && S <= 4096, "S=%d must be in [1, 4096]", S);
+  CHECK(ld == 256, "ld=%d must be 256", ld);
+  CHECK(L >= 1 && L <= 256, "L=%d must be in [1, 256]", L);
+  CHECK(D >= 128 && D % 128 == 0 && D <= 2048, "D=%d must be a multiple of 128 in [128, 2048]", D);
+  CHECK(V >= 1, "V=%d must be >= 1", V);
+  CHECK(!(eps < 0.f), "eps must be >= 0");
+  DEVICE_OR_RETURN(dev);
+  return launch_ple_q8(ids, S, table, row_scale, V, L, ld, embed_scale, proj_codes, proj_scales,
+                       reinterpret_cast<const __half*>(hidden_f16), D, norm_w, eps, out, gathered_opt, err, dev,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 int q4_gemm_chunk(const uint8_t* codes, const uint16_t* scales, const uint16_t* X_f16, float* Y, int M,

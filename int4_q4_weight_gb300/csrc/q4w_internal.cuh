@@ -78,6 +78,14 @@ int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_
                int ld, float embed_scale, const float* proj, const __half* hidden, int D,
                const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
                const DeviceInfo& dev, cudaStream_t s);
+// The same with the projection in int8 per-block-32 form (codes [L*ld][D], fp16
+// scales [L*ld][D/32]); D % 128 == 0, D <= 2048.
+int launch_ple_q8(const int32_t* ids, int S, const int8_t* table, const float* row_scale, int V, int L, int ld,
+                  float embed_scale, const int8_t* proj_codes, const uint16_t* proj_scales, const __half* hidden,
+                  int D, const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
+                  const DeviceInfo& dev, cudaStream_t s);
+int launch_quantize_q8(const float* W, int N, int K, int8_t* codes, __half* scales, int32_t* err,
+                       const DeviceInfo& dev, cudaStream_t s);
 // Streaming engine (bulk-copy ring; K % 256 == 0 and K <= 12288).
 bool stream_eligible(int K);
 int launch_stage_stream(const StageArgs& a, const DeviceInfo& dev, cudaStream_t s, bool pdl);

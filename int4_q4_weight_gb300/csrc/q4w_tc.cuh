@@ -125,6 +125,10 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, uin
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Every bulk store this thread committed has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Every bulk store this thread committed has finished reading its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // Contiguous bulk copy global -> this CTA's shared memory (16-byte aligned
 // addresses, size a multiple of 16), completing on an mbarrier.

@@ -108,6 +108,29 @@ def test_q2_gemv_rejections(lib):
     assert lib.q2_gemv(A, A, A, A, 0, 64, None) == 2                    # N
 
 
+def test_q8_entry_rejections(lib):
+    F = ctypes.c_float
+    assert lib.q8_quantize(None, 4, 64, A, A, None, None) == 1              # NULL
+    assert lib.q8_quantize(A, 4, 48, A, A, None, None) == 2                 # K % 32
+    assert lib.q8_quantize(A, 4, 64, A + 8, A, None, None) == 3             # alignment
+
+    def ple(**kw):
+        a = dict(ids=A, S=8, table=A, rs=A, V=10, L=2, ld=256, codes=A, scales=A, hid=A, D=128,
+                 nw=A, out=A)
+        a.update(kw)
+        return lib.ple_gather_project_q8(a["ids"], a["S"], a["table"], a["rs"], a["V"], a["L"], a["ld"],
+                                         F(16.0), a["codes"], a["scales"], a["hid"], a["D"], a["nw"],
+                                         F(1e-6), a["out"], None, None, None)
+    assert ple(scales=None) == 1
+    assert b"proj_scales" in lib.q4_last_error()
+    assert ple(codes=A + 4) == 3
+    assert ple(D=192) == 2                                                  # D % 128
+    assert b"D=192" in lib.q4_last_error()
+    assert ple(D=2176) == 2                                                 # D > 2048
+    assert ple(ld=128) == 2
+    assert ple(S=0) == 2
+
+
 def test_decode_pass_launch_count(lib):
     """One persistent launch when H <= 4096, every K a multiple of 256 up to
     12288 and at most 48 layers; otherwise one launch per stage plus the
