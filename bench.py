@@ -398,10 +398,10 @@ def row_head(q4w, synth, dev, hbm, bsz, reps=20, weights=None):
             "bytes": b}
 
 
-def row_ple(q4w, synth, dev, hbm, bf16_peak, reps=10):
+def row_ple(q4w, synth, dev, hbm, bf16_peak, reps=10, V=None):
     import torch
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    p = synth.ple_inputs(seed=1002, device=dev)
+    p = synth.ple_inputs(seed=1002, device=dev, **({"V": V} if V else {}))
     ncp = max(2, math.ceil(2 * l2 / p.proj.numel() / 4))
     projs = [p.proj.clone() for _ in range(ncp)]
     out = torch.empty((64, 8960), dtype=torch.float32, device=dev)
@@ -418,11 +418,11 @@ def row_ple(q4w, synth, dev, hbm, bf16_peak, reps=10):
             "copies": ncp}
 
 
-def row_ple_q8(q4w, synth, dev, hbm, bf16_peak, reps=10):
+def row_ple_q8(q4w, synth, dev, hbm, bf16_peak, reps=10, V=None):
     """The PLE with the int8 per-block-32 projection (14.6 MB instead of 55 MB)."""
     import torch
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    p = synth.ple_inputs(seed=1002, device=dev)
+    p = synth.ple_inputs(seed=1002, device=dev, **({"V": V} if V else {}))
     codes, scales = q4w.q8_quantize(p.proj)
     per = codes.numel() + scales.numel() * 2
     ncp = max(2, math.ceil(2 * l2 / per))
@@ -595,9 +595,9 @@ def run_case(args):
     elif args.case in ("head_b1", "head_b8"):
         r = row_head(q4w, synth, dev, hbm, 1 if args.case == "head_b1" else 8, reps)
     elif args.case == "ple":
-        r = row_ple(q4w, synth, dev, hbm, bf16, reps)
+        r = row_ple(q4w, synth, dev, hbm, bf16, reps, V=args.ple_vocab)
     elif args.case == "ple_q8":
-        r = row_ple_q8(q4w, synth, dev, hbm, bf16, reps)
+        r = row_ple_q8(q4w, synth, dev, hbm, bf16, reps, V=args.ple_vocab)
     elif args.case in ("q2_gate", "q2_head"):
         r = row_q2(q4w, synth, dev, hbm, args.case[3:], reps)
     elif args.case == "pass_trace":
@@ -676,6 +676,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=CASES, default=None,
                     help="time one row's workload only (--steps = graph replays), for profiling")
+    ap.add_argument("--ple-vocab", type=int, default=None,
+                    help="with --case ple/ple_q8: table rows (default the full 262144; smaller for profiling captures)")
     ap.add_argument("--layers", type=int, default=35,
                     help="run only the last N E2B layers (a small case for profiling)")
     args = ap.parse_args()

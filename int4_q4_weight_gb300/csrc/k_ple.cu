@@ -36,6 +36,14 @@
 // A ring of kStages stages (A 32 KB + B 16 KB + hidden 8 KB) is guarded by
 // full (TMA bytes), bready (converter warps, which arrive only after seeing
 // full) and empty (MMA commit) mbarriers; the MMA warp waits on bready alone.
+// The int8 form (ple_tc_kernel<true>; "Gemma-4 E2B mobile mixed-bit QAT
+// weights", decode recipe and official-checkpoint notes: the model projection
+// is int8 per block of 32) keeps the clusters, roles and epilogue.  A stage is
+// 128 K columns: the code tile [128 rows][128 int8] and two hidden tiles
+// [64 tokens][64 fp16] (128-byte swizzle, the B operand as loaded) come from
+// TMA; warps 2-5 widen the codes to fp16(scale * code) into two swizzled A
+// halves, and 8 MMAs of kind::f16 follow.  The K halves of a cluster take
+// alternate 128-column units.
 // The kernel is launched with programmatic dependent launch: its set-up
 // overlaps the previous kernel, its first reads of inputs come after
 // griddepcontrol.wait.  Every mbarrier wait is bounded; on expiry the CTA
