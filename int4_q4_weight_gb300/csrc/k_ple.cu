@@ -438,38 +438,38 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
         if (ct == 0) stamp(st, 2);
       }
     } else {
-    for (int st = 0; st < ns; ++st) {
-      const int s = st % kSt, round = st / kSt;
-      const bool landed = tc::mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
-      if (!__all_sync(0xffffffffu, landed)) {   // leave the loop as a whole warp
-        ok = false;
-        break;
-      }
-      if (ct == 0) stamp(st, 1);
-      uint8_t* B = smem + (size_t)s * kStageBytes + kSub * kABytes;
-      const int hrow = (int)p.hid_box_bytes / kTok;   // bytes per token row of the hidden tile
-      const uint8_t* H = B + kSub * kBBytes;
-      const int nsc = nsc_of(st);
-      for (int a = 0; a < nsc; ++a) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int idx = ct + 128 * i;      // (token t, 16-byte group j of its 128-byte row)
-          const int t = idx >> 3, j = idx & 7;
-          // tokens past S: zero rows (the tensor map already reads them as zero)
-          const uint2 h = t < ntok ? *reinterpret_cast<const uint2*>(H + t * hrow + a * (kKC * 2) + j * 8)
-                                   : make_uint2(0u, 0u);
-          const float2 x0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
-          const float2 x1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
-          // 128-byte swizzle: group j of row t sits at group j ^ (t % 8) of its row
-          *reinterpret_cast<float4*>(B + a * kBBytes + (t >> 3) * 1024 + (t & 7) * 128 + ((j ^ (t & 7)) << 4)) =
-              make_float4(x0.x, x0.y, x1.x, x1.y);
+      for (int st = 0; st < ns; ++st) {
+        const int s = st % kSt, round = st / kSt;
+        const bool landed = tc::mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
+        if (!__all_sync(0xffffffffu, landed)) {   // leave the loop as a whole warp
+          ok = false;
+          break;
         }
+        if (ct == 0) stamp(st, 1);
+        uint8_t* B = smem + (size_t)s * kStageBytes + kSub * kABytes;
+        const int hrow = (int)p.hid_box_bytes / kTok;   // bytes per token row of the hidden tile
+        const uint8_t* H = B + kSub * kBBytes;
+        const int nsc = nsc_of(st);
+        for (int a = 0; a < nsc; ++a) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int idx = ct + 128 * i;      // (token t, 16-byte group j of its 128-byte row)
+            const int t = idx >> 3, j = idx & 7;
+            // tokens past S: zero rows (the tensor map already reads them as zero)
+            const uint2 h = t < ntok ? *reinterpret_cast<const uint2*>(H + t * hrow + a * (kKC * 2) + j * 8)
+                                     : make_uint2(0u, 0u);
+            const float2 x0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+            const float2 x1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+            // 128-byte swizzle: group j of row t sits at group j ^ (t % 8) of its row
+            *reinterpret_cast<float4*>(B + a * kBBytes + (t >> 3) * 1024 + (t & 7) * 128 + ((j ^ (t & 7)) << 4)) =
+                make_float4(x0.x, x0.y, x1.x, x1.y);
+          }
+        }
+        tc::fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(bready0 + 8 * s);
+        if (ct == 0) stamp(st, 2);
       }
-      tc::fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(bready0 + 8 * s);
-      if (ct == 0) stamp(st, 2);
-    }
     }
     // ------------------------------------------------------------- epilogue
     if (ct < kTok) tsc[ct] = my_sc;            // read after the barriers below
@@ -679,7 +679,8 @@ static int launch_ple_t(const int32_t* ids, int S, const int8_t* table, const fl
   p.wait_limit = wait_limit();
   size_t tbytes = 0;
   void* tb = trace_buffer(&tbytes);
-  const size_t trace_words = (size_t)ple::kTraceRows * 8 + 2 * (size_t)ple::kCluster * L * ((S + ple::kTok - 1) / ple::kTok);
+  const size_t trace_words =
+      (size_t)ple::kTraceRows * 8 + 2 * (size_t)ple::kCluster * L * ((S + ple::kTok - 1) / ple::kTok);
   p.trace = (tb && tbytes >= trace_words * sizeof(unsigned long long))
                 ? static_cast<unsigned long long*>(tb)
                 : nullptr;
