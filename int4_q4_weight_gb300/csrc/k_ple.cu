@@ -483,63 +483,62 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     ok = __all_sync(0xffffffffu, ok);          // the TMEM loads below are warp-wide
     tc::fence_after();
     if (ct == 0) stamp(kTraceRows - 1, 5);
+    // this row's accumulator columns (one per token): one load and one wait
+    float acc[kTok];
+    if (ok && has) {
+      tc::tmem_ld64(taddr, acc);
+    } else {
+#pragma unroll
+      for (int u = 0; u < kTok; ++u) acc[u] = 0.f;
+    }
     tc::cluster_wait();                        // phase 1: every peer is running
     if (ct == 0) stamp(kTraceRows - 2, 0);
     if (!mine) {                               // the partner finishes these rows
       const uint32_t peer = tc::cluster_addr(recv, (uint32_t)(rank ^ 2));
-      for (int cb = 0; cb < npad / 16; ++cb) {
-        float v[16];
-        if (ok && has) {
-          tc::tmem_ld16(taddr + cb * 16, v);
-        } else {
 #pragma unroll
-          for (int u = 0; u < 16; ++u) v[u] = 0.f;
+      for (int cb = 0; cb < kTok / 16; ++cb) {
+        if (cb < npad / 16) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {   // tokens 16 cb + 4 g .. + 3 of this row
+            const int u = 16 * cb + 4 * g;
+            tc::st_cluster_v4(peer + (uint32_t)((((cb * 4 + g) * 64) + r64) * 16), acc[u], acc[u + 1], acc[u + 2],
+                              acc[u + 3]);
+          }
         }
-#pragma unroll
-        for (int g = 0; g < 4; ++g)   // tokens 16 cb + 4 g .. + 3 of this row
-          tc::st_cluster_v4(peer + (uint32_t)((((cb * 4 + g) * 64) + r64) * 16), v[4 * g], v[4 * g + 1],
-                            v[4 * g + 2], v[4 * g + 3]);
       }
     }
     tc::cluster_arrive_release();
     tc::cluster_wait();                        // phase 2: the partner's partial sums are here
     if (ct == 0) stamp(kTraceRows - 2, 1);
-    // p = (K half 0) + (K half 1), the same order in both CTAs
-    auto sums16 = [&](int cb, float (&v)[16]) {
-      float own[16];
-      if (ok && has) {
-        tc::tmem_ld16(taddr + cb * 16, own);
-      } else {
-#pragma unroll
-        for (int u = 0; u < 16; ++u) own[u] = 0.f;
-      }
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const float4 o4 = *reinterpret_cast<const float4*>(recv + (((cb * 4 + g) * 64) + r64) * 4);
-        const float other[4] = {o4.x, o4.y, o4.z, o4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int u = 4 * g + e;
-          v[u] = kh == 0 ? own[u] + other[e] : other[e] + own[u];
-        }
-      }
-    };
+    // p = (K half 0) + (K half 1), the same order in both CTAs; the four token
+    // groups' reductions are independent of one another
     float pv[kTok];   // this row's projection sums, kept for the output pass
 #pragma unroll
     for (int cb = 0; cb < kTok / 16; ++cb) {
       if (mine && cb < npad / 16) {   // warp-uniform
-        float v[16];
-        sums16(cb, v);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          pv[cb * 16 + u] = v[u];
-          v[u] *= v[u];
+        for (int g = 0; g < 4; ++g) {
+          const float4 o4 = *reinterpret_cast<const float4*>(recv + (((cb * 4 + g) * 64) + r64) * 4);
+          const float other[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int u = 16 * cb + 4 * g + e;
+            pv[u] = kh == 0 ? acc[u] + other[e] : other[e] + acc[u];
+          }
         }
-        const float s2 = lane_token_sums16(v, lane);
-        if ((lane & 1) == 0) red[q & 1][cb * 16 + (lane >> 1)] = s2;
       } else {
 #pragma unroll
         for (int u = 0; u < 16; ++u) pv[cb * 16 + u] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int cb = 0; cb < kTok / 16; ++cb) {
+      if (mine && cb < npad / 16) {
+        float v[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) v[u] = pv[cb * 16 + u] * pv[cb * 16 + u];
+        const float s2 = lane_token_sums16(v, lane);
+        if ((lane & 1) == 0) red[q & 1][cb * 16 + (lane >> 1)] = s2;
       }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
