@@ -63,3 +63,25 @@ def test_zero_budget_times_out_then_recovers(cuda_lib):
     ro, _ = O.ple_gather_project(pp.ids.cpu().numpy(), pp.table.cpu().numpy(), pp.row_scale.cpu().numpy(),
                                  pp.proj.cpu().numpy(), pp.hidden.cpu().numpy(), pp.norm_w.cpu().numpy(), L=2, ld=256)
     assert_close(out.cpu().numpy(), ro, what="ple after")
+
+
+def test_zero_budget_int8_ple_times_out_then_recovers(cuda_lib):
+    """The int8 PLE form shares the clusters' bounded waits and abort path."""
+    from oracle import q8_oracle as Q8
+    q4w = cuda_lib
+    q4w.q4_device_status()
+    pp = synth.ple_inputs(seed=115, device="cuda", S=70, V=300, L=2, D=1536)
+    codes, scales = q4w.q8_quantize(pp.proj)
+    old = q4w.q4_set_wait_limit(0)
+    try:
+        q4w.ple_gather_project_q8(pp.ids, pp.table, pp.row_scale, codes, scales, pp.hidden, pp.norm_w, L=2)
+        _expect_timeout(q4w)
+    finally:
+        q4w.q4_set_wait_limit(old)
+    out, _ = q4w.ple_gather_project_q8(pp.ids, pp.table, pp.row_scale, codes, scales, pp.hidden, pp.norm_w, L=2)
+    q4w.q4_device_status()
+    rc, rs = Q8.quantize_q8_0(pp.proj.cpu().numpy())
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    ro, _ = Q8.ple_gather_project_q8(pp.ids.cpu().numpy(), pp.table.cpu().numpy(), pp.row_scale.cpu().numpy(),
+                                     rc, rs, pp.hidden.cpu().numpy(), pp.norm_w.cpu().numpy(), L=2, ld=256)
+    assert_close(out.cpu().numpy(), ro, what="ple q8 after")
