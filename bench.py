@@ -152,6 +152,21 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(seconds, world, device=None):
+    """The slowest rank's time (every rank receives it); the value itself when alone."""
+    if world <= 1:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(world, steps, seconds):
+    """Whole-job steps/s: every replica ran `steps` steps within `seconds`."""
+    return world * steps / seconds
+
+
 def oracle_gemv_rate(layers_np, min_seconds):
     """Bytes/s of the oracle's dequant-GEMV over whole matrices, and the number
     of threads it used (process CPU time / wall time)."""
@@ -241,12 +256,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop() if sampler else None
-    elapsed = ev0.elapsed_time(ev1) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
-    value = world * args.steps / elapsed
+    elapsed = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    value = replica_value(world, args.steps, elapsed)
     ms_per_step = elapsed / args.steps * 1e3
 
     # end to end through the public API: pinned host h -> device, one graph
@@ -260,11 +271,7 @@ def run_ours(args, world, rank, local):
     t0 = time.perf_counter()
     for _ in range(ke):
         plan.step_host(h_host, out_host)
-    te = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([te], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        te = float(t.item())
+    te = max_over_ranks(time.perf_counter() - t0, world, dev)
 
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
@@ -284,7 +291,7 @@ def run_ours(args, world, rank, local):
                               "(one CTA per SM)" if launches == 1 else
                               f"one CUDA graph per step, {launches} kernels, programmatic dependent launch"),
                    "parallelism": f"replicas x{world}"},
-        "e2e": {"value": round(world * ke / te, 3), "unit": "steps/s", "h2d_bytes_per_step": 2 * H,
+        "e2e": {"value": round(replica_value(world, ke, te), 3), "unit": "steps/s", "h2d_bytes_per_step": 2 * H,
                 "d2h_bytes_per_step": 2 * H,
                 "how": "pinned host h0 -> device, graph replay, device -> pinned host h, sync per step"},
         "gpu_launches": launches * args.steps,
@@ -495,8 +502,8 @@ def measure_rows(q4w, synth, dev, hbm, clocks, bf16_peak):
     return rows
 
 
-CASES = ("gemv", "gemv_b4", "head_b1", "head_b8", "ple", "ple_q8", "gemm_up", "gemm_down", "gemm_head", "q2_gate", "q2_head",
-         "pass_trace")
+CASES = ("gemv", "gemv_b4", "head_b1", "head_b8", "ple", "ple_q8", "gemm_up", "gemm_down", "gemm_head", "q2_gate",
+         "q2_head", "pass_trace")
 
 
 def pass_trace(q4w, synth, dev, reps):
