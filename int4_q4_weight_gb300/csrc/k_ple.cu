@@ -42,8 +42,13 @@
 // 128 K columns: the code tile [128 rows][128 int8] and two hidden tiles
 // [64 tokens][64 fp16] (128-byte swizzle, the B operand as loaded) come from
 // TMA; warps 2-5 widen the codes to fp16(scale * code) into two swizzled A
-// halves, and 8 MMAs of kind::f16 follow.  The K halves of a cluster take
-// alternate 128-column units.
+// halves, and 8 MMAs of kind::f16 follow (3 stages of 64 KB: A 32 KB, B 16 KB,
+// codes 16 KB; the block scales of the CTA's rows sit in shared memory).  The
+// K halves of a cluster take alternate 128-column units.
+//
+// In both forms the token ids, table copies and table scales are handled by
+// warps 2-5 while the first tiles load, and the epilogue reads each row's 64
+// accumulator columns with one TMEM load.
 // The kernel is launched with programmatic dependent launch: its set-up
 // overlaps the previous kernel, its first reads of inputs come after
 // griddepcontrol.wait.  Every mbarrier wait is bounded; on expiry the CTA
