@@ -68,3 +68,17 @@ def test_reference_arm_other_ranks_do_nothing(capsys):
     args = argparse.Namespace(steps=3, warmup=3, gpus=2, impl="reference")
     assert bench.run_reference(args, world=2, rank=1, local=1) is None
     assert capsys.readouterr().out == ""
+
+
+def test_stored_traffic_only_for_the_captured_sources(monkeypatch):
+    """The committed DRAM figure is reported while the pass's sources hash to
+    the value recorded with it, and withheld (None) once they differ."""
+    import json
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    entry = rec["e2b_pass_step"]
+    assert entry["dram_bytes_per_unit"] == entry["dram_bytes_read"] + entry["dram_bytes_write"]
+    assert entry["source_hash"] == bench.source_hash()       # captured on the current sources
+    assert bench.stored_traffic("e2b_pass_step") == entry["dram_bytes_per_unit"]
+    monkeypatch.setattr(bench, "source_hash", lambda names=bench.PASS_SOURCES: "f" * 16)   # a changed kernel
+    assert bench.stored_traffic("e2b_pass_step") is None
+    assert bench.stored_traffic("no_such_kernel") is None
