@@ -356,7 +356,23 @@ long long q4_set_wait_limit(long long cycles);
  * registers, 5 first weight tile landed (shifted left by one; bit 0 set when
  * it had landed before the consumers asked), 6 first tile usable by the
  * whole warp, 4 this CTA's rows written; 7 unused.  Needs
- * 4 * n_layers * grid * 8 * 8 bytes.  NULL turns it off. */
+ * 4 * n_layers * grid * 8 * 8 bytes.
+ * The other tensor-core kernels use the same buffer when it is large enough
+ * for their layout (else they write nothing):
+ *   ple_gather_project / _q8: CTA 0 writes row r < 256 of 8 words (SM
+ *   cycles since its start) per stage r: 0 tile loads issued, 1 tiles seen
+ *   by the converter warps, 2 operand converted, 3 MMAs started, 4 MMAs
+ *   committed; row 255 words 5-7 and row 254 words 0-4 mark the epilogue
+ *   (accumulator ready, cluster phases 1-3, RMS factors, output written,
+ *   exit); then every CTA writes its start and end globaltimer (ns) as two
+ *   words at 2048 + 2 * (blockIdx.y * gridDim.x + blockIdx.x).  Needs
+ *   (2048 + 2 * 4 * L * ceil(S / 64)) * 8 bytes.
+ *   q4_gemm_chunk and the batched LM head: CTA 0 writes 8 words (SM cycles)
+ *   per 128-column chunk g < 256 of its work: 0 weight tile load issued,
+ *   1 landed, 2 operand slot free, 3 operand converted, 4 MMAs started,
+ *   5 committed, 6 accumulator ready, 7 written out (6 and 7 on an item's
+ *   first chunk).  Needs 256 * 8 * 8 bytes.
+ * NULL turns it off. */
 int q4_set_trace(void* buf, size_t bytes);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
