@@ -113,6 +113,13 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
+def _numel(t, n, name):
+    """An array a kernel reads or writes holds exactly the elements its sizes imply
+    (the kernels trust the sizes, so a short buffer would be overrun)."""
+    if t is not None and t.numel() != n:
+        raise Q4Error(f"{name} has {t.numel()} elements; the sizes imply {n}")
+
+
 def _dev(t, dtype, name):
     if t is None:
         return
@@ -162,6 +169,8 @@ def q4_quantize(W, codes=None, scales=None, err=None):
     _dev(codes, torch.uint8, "codes")
     _dev(scales, torch.float16, "scales")
     _dev(err, torch.int32, "err")
+    _numel(codes, N * K // 2, "codes")
+    _numel(scales, N * K // 32, "scales")
     _check(lib.q4_quantize(_ptr(W), N, K, _ptr(codes), _ptr(scales), _ptr(err), _stream()),
            "q4_quantize")
     return codes, scales
@@ -179,6 +188,8 @@ def q8_quantize(W, codes=None, scales=None, err=None):
     _dev(codes, torch.int8, "codes")
     _dev(scales, torch.float16, "scales")
     _dev(err, torch.int32, "err")
+    _numel(codes, N * K, "codes")
+    _numel(scales, N * K // 32, "scales")
     _check(lib.q8_quantize(_ptr(W), N, K, _ptr(codes), _ptr(scales), _ptr(err), _stream()),
            "q8_quantize")
     return codes, scales
@@ -195,6 +206,9 @@ def q4_gemv(codes, scales, x, y=None):
     if y is None:
         y = torch.empty((batch, N) if x.dim() == 2 else (N,), dtype=torch.float32, device=x.device)
     _dev(y, torch.float32, "y")
+    _numel(scales, N * K // 32, "scales")
+    _numel(x, batch * K, "x")
+    _numel(y, batch * N, "y")
     _check(lib.q4_gemv(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), N, K, batch, None, 0,
                        _stream()), "q4_gemv")
     return y
@@ -298,10 +312,24 @@ def lmhead_softcap_argmax(codes, scales, h, cap=30.0, ws=None, idx=None, top1=No
                       (top2, torch.float32, "top2"), (logits, torch.float32, "logits"),
                       (ws, torch.uint8, "ws")):
         _dev(t, dt, nm)
+    _numel(scales, V * K // 32, "scales")
+    _numel(h, b * K, "h")
+    for t, nm in ((idx, "idx"), (top1, "top1"), (top2, "top2")):
+        _numel(t, b, nm)
+    _numel(logits, b * V, "logits")
     _check(lib.lmhead_softcap_argmax(_ptr(codes), _ptr(scales), _ptr(h), b, V, K, cap, _ptr(idx),
                                      _ptr(top1), _ptr(top2), _ptr(logits), _ptr(ws), ws.numel(),
                                      _stream()), "lmhead_softcap_argmax")
     return idx, top1, top2, logits
+
+
+def _ple_sizes(S, V, L, ld, D, table, row_scale, hidden, norm_w, out, gathered):
+    _numel(table, V * L * ld, "table (V rows of L*ld bytes)")
+    _numel(row_scale, V, "row_scale")
+    _numel(hidden, S * D, "hidden")
+    _numel(norm_w, ld, "norm_w")
+    _numel(out, S * L * ld, "out")
+    _numel(gathered, S * L * ld, "gathered")
 
 
 def ple_gather_project(ids, table, row_scale, proj, hidden, norm_w, L=35, ld=256,
@@ -322,6 +350,8 @@ def ple_gather_project(ids, table, row_scale, proj, hidden, norm_w, L=35, ld=256
     _dev(out, torch.float32, "out")
     _dev(gathered, torch.int8, "gathered")
     _dev(err, torch.int32, "err")
+    _ple_sizes(S, V, L, ld, D, table, row_scale, hidden, norm_w, out, gathered)
+    _numel(proj, L * ld * D, "proj")
     _check(lib.ple_gather_project(_ptr(ids), S, _ptr(table), _ptr(row_scale), V, L, ld, embed_scale,
                                   _ptr(proj), _ptr(hidden), D, _ptr(norm_w), eps, _ptr(out),
                                   _ptr(gathered), _ptr(err), _stream()), "ple_gather_project")
@@ -348,6 +378,9 @@ def ple_gather_project_q8(ids, table, row_scale, proj_codes, proj_scales, hidden
     _dev(out, torch.float32, "out")
     _dev(gathered, torch.int8, "gathered")
     _dev(err, torch.int32, "err")
+    _ple_sizes(S, V, L, ld, D, table, row_scale, hidden, norm_w, out, gathered)
+    _numel(proj_codes, L * ld * D, "proj_codes")
+    _numel(proj_scales, L * ld * D // 32, "proj_scales")
     _check(lib.ple_gather_project_q8(_ptr(ids), S, _ptr(table), _ptr(row_scale), V, L, ld, embed_scale,
                                      _ptr(proj_codes), _ptr(proj_scales), _ptr(hidden), D, _ptr(norm_w), eps,
                                      _ptr(out), _ptr(gathered), _ptr(err), _stream()), "ple_gather_project_q8")
@@ -365,6 +398,9 @@ def q4_gemm_chunk(codes, scales, X, Y=None):
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
     _dev(Y, torch.float32, "Y")
+    _numel(scales, N * K // 32, "scales")
+    _numel(X, M * K, "X")
+    _numel(Y, M * N, "Y")
     nws = lib.q4_workspace_bytes(Q4_OP_GEMM_CHUNK, N, K, M)
     ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=X.device)
     _check(lib.q4_gemm_chunk(_ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, N, K, _ptr(ws), nws,
@@ -382,6 +418,9 @@ def q2_gemv(codes, scales, x, y=None):
     if y is None:
         y = torch.empty(N, dtype=torch.float32, device=x.device)
     _dev(y, torch.float32, "y")
+    _numel(scales, N, "scales")
+    _numel(x, K, "x")
+    _numel(y, N, "y")
     _check(lib.q2_gemv(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), N, K, _stream()), "q2_gemv")
     return y
 
