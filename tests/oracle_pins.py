@@ -434,4 +434,90 @@ def pin_e2b_layer_structure(O, seed=59):
         assert not np.array_equal(O.e2b_layer(h, lw3)["h"], st["h"]), name
 
 
+def _pack_row_codes(codes_row):
+    """Pack one row of 4-bit codes, column 2j in the low nibble of byte j."""
+    out = []
+    for j in range(0, len(codes_row), 2):
+        out.append((int(codes_row[j]) & 0xF) | ((int(codes_row[j + 1]) & 0xF) << 4))
+    return out
+
+
+def _f16(x):
+    """Round an fp64 value to the nearest fp16 (ties to even), back to fp64."""
+    return float(np.float64(x).astype(np.float16))
+
+
+def _f32(x):
+    return float(np.float64(x).astype(np.float32))
+
+
+def pin_e2b_layer_stage_by_stage(O, seed=61):
+    """One tiny layer restated stage by stage in plain fp64 loops (reading R8),
+    sharing no code with the oracle: the weights are built from integer codes
+    and power-of-two scales, packed here bit by bit; each GEMV output is the
+    correctly rounded fp64 sum (math.fsum of exact products) rounded to fp32;
+    each RMSNorm is v / sqrt(mean(v^2) + 1e-6) with weight 1 ([E2B] Signature
+    features: the weight multiplies directly); gelu is the tanh form ([MB]
+    Speed: fp32 precise-tanh GELU), and the gate feeds the GELU while the up
+    projection multiplies it ([MB] Speed: "gate/up matvecs + gelu + mul").
+    Every stage output of O.e2b_layer must match: fp32 stages to 1e-6
+    relative, fp16 stages to one fp16 step.  The input's RMS is 3 and the
+    projections are scaled so that o's RMS is far from 1, so a dropped norm, a
+    gate/up swap or a dropped fp16 cast moves some stage far outside that."""
+    rng = np.random.default_rng(seed)
+    H, Q, KV, I = 32, 64, 32, 96
+    eps = 1e-6
+
+    def build(rows, cols, scale_exp):
+        codes = rng.integers(0, 16, size=(rows, cols))
+        # one power-of-two scale per 32-column block, exponent scale_exp or one below
+        exps = scale_exp - rng.integers(0, 2, size=(rows, cols // 32))
+        d = [[math.ldexp(1.0, int(e)) for e in row] for row in exps]
+        packed = np.array([_pack_row_codes(codes[n]) for n in range(rows)], dtype=np.uint8)
+        bits = np.array([[np.float16(v).view(np.uint16) for v in row] for row in d], dtype=np.uint16)
+        W = [[d[n][k // 32] * (int(codes[n, k]) - 8) for k in range(cols)] for n in range(rows)]
+        return (packed, bits), W
+
+    def gemv(W, x):
+        return [_f32(math.fsum(w * xv for w, xv in zip(row, x))) for row in W]
+
+    def rms(v):
+        r = math.sqrt(math.fsum(t * t for t in v) / len(v) + eps)
+        return [t / r for t in v]
+
+    def gelu(x):
+        return 0.5 * x * (1.0 + math.tanh(math.sqrt(2.0 / math.pi) * (x + 0.044715 * x * x * x)))
+
+    lw, Wm = {}, {}
+    for name, (r, c, e) in {"q": (Q, H, -5), "k": (KV, H, -5), "v": (KV, H, -5), "o": (H, Q, -3),
+                            "g": (I, H, -5), "u": (I, H, -4), "d": (H, I, -6)}.items():
+        lw[name], Wm[name] = build(r, c, e)
+    h = [_f16(3.0 * v) for v in rng.standard_normal(H)]
+    want = {}
+    want["a"] = [_f16(t) for t in rms(h)]
+    want["q"] = gemv(Wm["q"], want["a"])
+    want["k"] = gemv(Wm["k"], want["a"])
+    want["v"] = gemv(Wm["v"], want["a"])
+    want["o"] = gemv(Wm["o"], [_f16(t) for t in want["q"]])
+    want["b"] = [_f16(t) for t in rms(want["o"])]
+    want["g"] = gemv(Wm["g"], want["b"])
+    want["u"] = gemv(Wm["u"], want["b"])
+    want["m"] = [_f16(gelu(gv) * uv) for gv, uv in zip(want["g"], want["u"])]
+    want["y"] = gemv(Wm["d"], want["m"])
+    want["h"] = [_f16(t) for t in rms(want["y"])]
+    o_rms = math.sqrt(sum(t * t for t in want["o"]) / H)
+    assert o_rms > 2.0 or o_rms < 0.5, o_rms       # the mid norm must change b
+    assert not np.allclose(want["g"], want["u"], rtol=0.1)
+    st = O.e2b_layer(np.array(h, dtype=np.float16), lw, eps=eps)
+    for name in ("a", "q", "k", "v", "o", "b", "g", "u", "m", "y", "h"):
+        got = np.asarray(st[name], dtype=np.float64)
+        w = np.array(want[name], dtype=np.float64)
+        assert got.shape == w.shape, (name, got.shape, w.shape)
+        if name in ("a", "b", "m", "h"):
+            tol = np.abs(w) * 2.0 ** -10 + 2.0 ** -24          # one fp16 step
+        else:
+            tol = np.abs(w) * 1e-6 + 1e-30
+        assert np.all(np.abs(got - w) <= tol), (name, float(np.max(np.abs(got - w) - tol)))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

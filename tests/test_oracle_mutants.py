@@ -66,6 +66,14 @@ MUTANTS = [
      'st["o"] = q4_gemv(*lw["o"], to_f16(st["q"])) + q4_gemv(*lw["k"], st["a"]).sum() * 0.01 if "k" in lw else q4_gemv(*lw["o"], to_f16(st["q"]))'),
     ("chain no final norm", "e2b_layer", 'st["h"] = to_f16(rmsnorm(st["y"], eps=eps))', 'st["h"] = to_f16(st["y"])'),
     ("chain gate only", "e2b_layer", 'to_f16(gelu_tanh(st["g"]) * st["u"].astype(np.float64))', 'to_f16(gelu_tanh(st["g"]))'),
+    ("chain gate and up swapped", "e2b_layer", 'to_f16(gelu_tanh(st["g"]) * st["u"].astype(np.float64))',
+     'to_f16(gelu_tanh(st["u"]) * st["g"].astype(np.float64))'),
+    ("chain pre-attention norm dropped", "e2b_layer",
+     'st["a"] = to_f16(rmsnorm(np.asarray(h_f16, np.float16).astype(np.float64), eps=eps))',
+     'st["a"] = to_f16(np.asarray(h_f16, np.float16).astype(np.float64))'),
+    ("chain mid-layer norm dropped", "e2b_layer", 'st["b"] = to_f16(rmsnorm(st["o"], eps=eps))', 'st["b"] = to_f16(st["o"])'),
+    ("chain down reads the gate", "e2b_layer", 'st["y"] = q4_gemv(*lw["d"], st["m"])',
+     'st["y"] = q4_gemv(*lw["d"], to_f16(st["g"]))'),
 ]
 
 
