@@ -4,22 +4,24 @@
 // Weights stream through shared memory: one producer thread issues 1-D bulk
 // copies (cp.async.bulk, completion on an mbarrier) of contiguous row tiles
 // (codes, then scales) into a ring of kSlots slots, with an L2 evict-first
-// hint; 8 consumer warps dequantise and dot against x held in registers.
-// A row group of P lanes covers all K/32 blocks of a row, each lane up to
-// three blocks (x of those blocks, 96 values, stays in registers for the
-// whole stage); Gc = 256/P groups take the rows of a tile in turn; P <= 32
-// reduces with shuffles, P > 32 through shared memory.  The per-row
+// hint; kCW = 12 consumer warps dequantise and dot against x held in
+// registers.  A row group of P lanes covers all K/32 blocks of a row, each
+// lane up to three blocks (x of those blocks, 96 values, stays in registers
+// for the whole stage); Gc = kCT/P groups take the rows of a tile in turn;
+// P <= 32 reduces with shuffles, P > 32 through shared memory.  The per-row
 // arithmetic (block order, bias trick, reduction tree) depends only on K, so
 // every entry point produces the same bits for the same row.
 //
 // The decode pass runs as one cooperative launch: every CTA walks the same
 // stage list; the producer runs ahead across stage boundaries (weights do
-// not depend on activations), while consumers wait for the previous stage's
-// completion counter (all CTAs done), read its output from L2, apply the
-// stage prologue and compute.  All waits are bounded in clock cycles; on
-// expiry the CTA raises an abort flag (and a grid-wide one), every role
-// leaves its loop, in-flight bulk copies are drained (bounded) and the
-// kernel returns with the device error word set.
+// not depend on activations).  Every stage output word carries the index of
+// the stage that wrote it (relaxed gpu-scope stores of half | tag << 16 or
+// float | tag << 32); the consumers of the next stage re-read their input
+// words until all carry that index (no counters, no fences), apply the stage
+// prologue and compute.  All waits are bounded in clock cycles; on expiry the
+// CTA raises an abort flag (and a grid-wide one), every role leaves its loop,
+// in-flight bulk copies are drained (bounded) and the kernel returns with the
+// device error word set.
 #include "q4w_device.cuh"
 #include "q4w_internal.cuh"
 #include "q4w_top2.cuh"
@@ -33,13 +35,12 @@ constexpr int kCT = kCW * 32;             // consumer threads
 constexpr int kTS = kCT + 32;             // threads per CTA
 constexpr int kSlots = 3;
 constexpr int kSlotBytes = 42 * 1024;
-constexpr int kStageInBytes = 24 * 1024;   // stage input staged in shared memory when it fits
 constexpr int kMaxNb = 384;               // K <= 12288 on this path
 constexpr int kBPL = 3;                   // blocks per lane (upper bound)
 constexpr int kXhStride = 20;             // uint32 per block: 16 half pairs, bias, 3 pad (80 B:
                                           // 8 lanes reading 8 consecutive blocks hit 8 bank groups)
 constexpr size_t kXsBytes = (size_t)kMaxNb * kXhStride * sizeof(uint32_t);
-constexpr size_t kSmemBytes = 128 + (size_t)kSlots * kSlotBytes + kXsBytes + kStageInBytes +
+constexpr size_t kSmemBytes = 128 + (size_t)kSlots * kSlotBytes + kXsBytes +
                               64 * sizeof(float) + 2 * kSlots * sizeof(uint64_t) + 64;
 constexpr long long kDrainCycles = 2000000000LL;   // in-flight copies always land well within this
 
@@ -86,6 +87,7 @@ struct Ctl {
   unsigned* err;             // the library's device error word
   unsigned long long* tr;    // trace stamps of the current stage (thread 0), or nullptr
   long long tr_c0;           // clock64() when the current stage began (trace only)
+  bool trace_on;             // uniform: stamps are being taken (adds a barrier for stamp 1)
 };
 
 __device__ __forceinline__ void raise_abort(const Ctl& c) {
@@ -275,15 +277,36 @@ __device__ __forceinline__ float load_in_cg(const void* in, int mode, int k) {
   return __ldcg(reinterpret_cast<const float*>(in) + k);
 }
 
+// Sum over the consumer threads through red[0 .. kCW); every consumer gets it.
+// The prologue gives each of its reductions its own red range, so one barrier
+// suffices (the barrier that closed the previous user of red orders it).
+__device__ __forceinline__ float consumer_sum1(float v, float* red) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  bar_sync(1, kCT);
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < kCW; ++i) t += red[i];
+  return t;
+}
+
+// An fp32 input is staged in shared memory when it fits after the x words.
+__host__ __device__ constexpr bool staged_f32(int K) {
+  return (size_t)(K >> 5) * kXhStride * 4 + (size_t)K * 4 <= kXsBytes;
+}
+
 // x = prologue(in), written per 32-column block as the half pairs
 // (x[8i+j], x[8i+j+4]) plus the bias of q4_block_dot_h (kXhStride words).
 //
-// Staged path (the input and its fp16 x fit kStageInBytes): the input is
-// copied to shared memory with 16-byte loads from L2 -- for a tagged input
+// Staged path (every fp16 input here, fp32 inputs up to K = 4096): the input
+// is copied to shared memory with 16-byte loads from L2 -- for a tagged input
 // (persistent pass) each element is re-read until it carries the expected
 // stage tag, which is how a stage learns that its input is complete -- then
-// the RMS factors, one fp16 x per element in parallel, and one thread per
-// block builds the pairs with byte permutes.  Otherwise x is computed per pair
+// the RMS factors, and each thread turns its chunks of eight elements into
+// fp16 x, half pairs and block biases.  The staging lives inside the x
+// buffer: an fp16 chunk is staged exactly where its four pair words go (the
+// thread that converts a chunk is the only one reading or writing it), an
+// fp32 input after the x words of this K.  Otherwise x is computed per pair
 // straight from global memory.
 __device__ __forceinline__ uint4 ldcg_v4(const void* p) {
   uint4 r;
@@ -355,11 +378,14 @@ __device__ __forceinline__ float xform(float v, int mode, float r, float r2) {
 // fp16 input with no normalisation may be read straight from global memory
 // (single-stage kernels; the persistent pass never has such an input).
 template <bool kDirect>
-__device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in, float* red8, const Ctl& c) {
+__device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, float* red8, const Ctl& c) {
   const int tid = threadIdx.x, K = a.K, mode = a.in_mode;
   const bool f16in = mode == Q4_IN_F16 || mode == Q4_IN_RMS_F16;
-  const int esz = f16in ? 2 : 4;
-  const bool staged = K * esz <= kStageInBytes;
+  const bool staged = f16in || staged_f32(K);
+  // fp32 staging: after this K's x words (16-byte aligned: 80 bytes per block)
+  float* const st32 = reinterpret_cast<float*>(xh + (K >> 5) * kXhStride);
+  // an fp16 chunk's home: the four pair words of its quarter of its block
+  auto home16 = [&](int ch) { return xh + (ch >> 2) * kXhStride + 4 * (ch & 3); };
   // an untagged fp16 input with no normalisation is read once, so each
   // thread takes its 8-element chunks straight from global memory
   const bool direct = kDirect && a.in_tag == 0 && mode == Q4_IN_F16;
@@ -369,15 +395,19 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
     if (a.in_tag == 0) {
       if (!direct) {
         const uint4* src = reinterpret_cast<const uint4*>(a.in);
-        uint4* dst = reinterpret_cast<uint4*>(stage_in);
-        for (int v = tid; v < K * esz / 16; v += kCT) dst[v] = ldcg_v4(src + v);
+        if (f16in) {
+          for (int v = tid; v < K / 8; v += kCT) *reinterpret_cast<uint4*>(home16(v)) = ldcg_v4(src + v);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(st32);
+          for (int v = tid; v < K / 4; v += kCT) dst[v] = ldcg_v4(src + v);
+        }
       }
     } else {
       // Tagged words: half | tag << 16 (four per 16 bytes) or float | tag << 32
       // (two per 16 bytes).  A thread issues all of its 16-byte reads at once
       // (one L2 round trip), then re-reads only groups whose tags are stale.
       const uint4* src = reinterpret_cast<const uint4*>(a.in);
-      uint2* dst = reinterpret_cast<uint2*>(stage_in);
+      uint2* dst32 = reinterpret_cast<uint2*>(st32);
       const int nv = f16in ? K / 4 : K / 2;
       const uint32_t tag = (uint32_t)a.in_tag;
       constexpr int kPB = 4;
@@ -391,8 +421,12 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
           const int v = v0 + i * kCT;
           if (v < nv && ok) {
             if (!tags_ready(u[i], f16in, tag)) ok = poll_tags(src + v, u[i], f16in, tag, c);
-            dst[v] = f16in ? make_uint2(__byte_perm(u[i].x, u[i].y, 0x5410), __byte_perm(u[i].z, u[i].w, 0x5410))
-                           : make_uint2(u[i].x, u[i].z);
+            // fp16: group v is half (v & 1) of chunk v >> 1
+            if (f16in)
+              *reinterpret_cast<uint2*>(home16(v >> 1) + 2 * (v & 1)) =
+                  make_uint2(__byte_perm(u[i].x, u[i].y, 0x5410), __byte_perm(u[i].z, u[i].w, 0x5410));
+            else
+              dst32[v] = make_uint2(u[i].x, u[i].z);
           }
         }
       }
@@ -407,7 +441,7 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
     auto load8 = [&](int ch, float (&v)[8]) {
       if (f16in) {
         const uint4 u = direct ? ldcg_v4(reinterpret_cast<const uint4*>(a.in) + ch)
-                               : *reinterpret_cast<const uint4*>(stage_in + (size_t)ch * 16);
+                               : *reinterpret_cast<const uint4*>(home16(ch));
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -416,8 +450,8 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
           v[2 * i + 1] = f.y;
         }
       } else {
-        const float4 f0 = *reinterpret_cast<const float4*>(stage_in + (size_t)ch * 32);
-        const float4 f1 = *reinterpret_cast<const float4*>(stage_in + (size_t)ch * 32 + 16);
+        const float4 f0 = *reinterpret_cast<const float4*>(st32 + 8 * ch);
+        const float4 f1 = *reinterpret_cast<const float4*>(st32 + 8 * ch + 4);
         v[0] = f0.x;
         v[1] = f0.y;
         v[2] = f0.z;
@@ -436,7 +470,7 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
 #pragma unroll
         for (int e = 0; e < 8; ++e) ss += v[e] * v[e];
       }
-      ss = consumer_sum(ss, red8);
+      ss = consumer_sum1(ss, red8);
       r = 1.f / sqrtf(ss / (float)K + a.eps);
       if (mode == Q4_IN_RMS2_F32) {
         float ss2 = 0.f;
@@ -449,7 +483,7 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
             ss2 += t * t;
           }
         }
-        ss2 = consumer_sum(ss2, red8);
+        ss2 = consumer_sum1(ss2, red8 + 16);
         r2 = 1.f / sqrtf(ss2 / (float)K + a.eps);
       }
     }
@@ -469,7 +503,7 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, uint8_t* stage_in
           pe += __half2float(x);
       }
       const int blk = ch >> 2, i = ch & 3;
-      *reinterpret_cast<uint4*>(xh + blk * kXhStride + 4 * i) =
+      *reinterpret_cast<uint4*>(home16(ch)) =
           make_uint4(hx[0] | (hx[4] << 16), hx[1] | (hx[5] << 16), hx[2] | (hx[6] << 16), hx[3] | (hx[7] << 16));
       pe += __shfl_xor_sync(0xffffffffu, pe, 1);
       po += __shfl_xor_sync(0xffffffffu, po, 1);
@@ -791,24 +825,49 @@ __device__ bool consume_generic(const StageArgs& a, const Geo& g, uint32_t& gcou
 }
 
 // Processes one stage's tiles; false when aborting (uniform over consumers).
-template <int NM, class Epi>
+// kPass: the persistent pass, which instantiates the fast consumer only for
+// the (K, rows in flight) pairs of the E2B layer shapes (hidden 1536; q/o
+// 2048 or 4096; MLP 6144 or 12288) -- fewer code paths in one kernel keep its
+// register allocation free of spills; any other shape takes the generic
+// consumer, which computes the same bits.
+template <int NM, bool kPass, class Epi>
 __device__ bool consume_stage(const StageArgs& a, const Geo& g, uint32_t& gcount, const uint8_t* slots,
                               uint32_t full0, uint32_t empty0, const uint32_t* xs, float* red, const Ctl& c,
                               const Epi& epi) {
 #define Q4W_FAST(P, BPL)                                                                              \
   return g.R == 2 ? consume_fast<NM, P, BPL, 2>(a, g, gcount, slots, full0, empty0, xs, red, c, epi)  \
                   : consume_fast<NM, P, BPL, 1>(a, g, gcount, slots, full0, empty0, xs, red, c, epi)
+#define Q4W_FAST_R(P, BPL, R) return consume_fast<NM, P, BPL, R>(a, g, gcount, slots, full0, empty0, xs, red, c, epi)
   if (g.T == g.Gc * g.R) {
-    switch (a.K) {
-      case 1536: Q4W_FAST(16, 3);
-      case 2048: Q4W_FAST(32, 2);
-      case 4096: Q4W_FAST(64, 2);
-      case 6144: Q4W_FAST(64, 3);
-      case 12288: Q4W_FAST(128, 3);
-      default: break;
+    if (kPass) {
+      if (NM == 2) {
+        if (a.K == 1536 && g.R == 1) Q4W_FAST_R(16, 3, 1);
+      } else {
+        if (g.R == 1) {
+          switch (a.K) {
+            case 1536: Q4W_FAST_R(16, 3, 1);
+            case 2048: Q4W_FAST_R(32, 2, 1);
+            case 4096: Q4W_FAST_R(64, 2, 1);
+            case 6144: Q4W_FAST_R(64, 3, 1);
+            default: break;
+          }
+        } else if (a.K == 12288) {
+          Q4W_FAST_R(128, 3, 2);
+        }
+      }
+    } else {
+      switch (a.K) {
+        case 1536: Q4W_FAST(16, 3);
+        case 2048: Q4W_FAST(32, 2);
+        case 4096: Q4W_FAST(64, 2);
+        case 6144: Q4W_FAST(64, 3);
+        case 12288: Q4W_FAST(128, 3);
+        default: break;
+      }
     }
   }
 #undef Q4W_FAST
+#undef Q4W_FAST_R
   return consume_generic<NM>(a, g, gcount, slots, full0, empty0, xs, red, c, epi);
 }
 
@@ -816,7 +875,6 @@ __device__ bool consume_stage(const StageArgs& a, const Geo& g, uint32_t& gcount
 struct Smem {
   uint8_t* slots;
   uint32_t* xs;   // half pairs + bias per block
-  uint8_t* stage_in;
   float* red;
   uint32_t slots0, full0, empty0;
 };
@@ -830,8 +888,6 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   off += (size_t)kSlots * kSlotBytes;
   s.xs = reinterpret_cast<uint32_t*>(raw + off);
   off += kXsBytes;
-  s.stage_in = raw + off;
-  off += kStageInBytes;
   s.red = reinterpret_cast<float*>(raw + off);
   off += 64 * sizeof(float);
   uint64_t* bars = reinterpret_cast<uint64_t*>(raw + off);
@@ -873,9 +929,9 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
     __syncwarp();
   } else {
     pdl_wait();
-    if (eng_prologue<true>(a, S.xs, S.stage_in, S.red, c)) {
+    if (eng_prologue<true>(a, S.xs, S.red, c)) {
       StageEpi epi{&a};
-      consume_stage<NM>(a, make_geo(a, NM), gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+      consume_stage<NM, false>(a, make_geo(a, NM), gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
     }
   }
   __syncthreads();
@@ -904,9 +960,9 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
     }
     __syncwarp();
   } else {
-    if (eng_prologue<true>(a, S.xs, S.stage_in, S.red, c)) {
+    if (eng_prologue<true>(a, S.xs, S.red, c)) {
       HeadEpi epi{&best, logits, cap};
-      consume_stage<1>(a, make_geo(a, 1), gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+      consume_stage<1, false>(a, make_geo(a, 1), gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
     }
   }
   // the CTA's record: shuffle merges within each warp, then across the warps
@@ -1032,7 +1088,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
     sg[0] = make_geo(sa[0], sa[0].pair ? 2 : 1);
   }
   __syncthreads();
-  Ctl c{&abort_sh, A.abort_grid, A.limit, A.err, nullptr, 0};
+  Ctl c{&abort_sh, A.abort_grid, A.limit, A.err, nullptr, 0, A.trace != nullptr};
   const int nst = 4 * A.n_layers;
   uint32_t gcount = 0;
   if (threadIdx.x >= kCT) {
@@ -1068,20 +1124,20 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       const StageArgs& a = sa[s & 1];
       if (tr) tr[7] = 0;
       // the prologue waits (bounded) until its whole input carries tag s
-      ok = eng_prologue<false>(a, S.xs, S.stage_in, S.red, c);
+      ok = eng_prologue<false>(a, S.xs, S.red, c);
       if (!ok) break;
       if (tr) tr[2] = stamp(c);
       StageEpi epi{&a};
       const Geo& g = sg[s & 1];
-      ok = a.pair ? consume_stage<2>(a, g, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
-                  : consume_stage<1>(a, g, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
+      ok = a.pair ? consume_stage<2, true>(a, g, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi)
+                  : consume_stage<1, true>(a, g, gcount, S.slots, S.full0, S.empty0, S.xs, S.red, c, epi);
       if (tr) tr[4] = stamp(c);
     }
     // closing RMSNorm of the last down-projection output (tag nst), by CTA 0,
     // with the summation order of q4_rmsnorm_f16 (256 partial sums)
     if (ok && blockIdx.x == 0) {
       const int H = A.H;
-      float* sf = reinterpret_cast<float*>(S.stage_in);
+      float* sf = reinterpret_cast<float*>(S.slots);   // the ring is idle once the last stage is done
       bool ok2 = true;
       for (int v = threadIdx.x; v < H / 2 && ok2; v += kCT) {
         const uint4* p = reinterpret_cast<const uint4*>(A.y32t) + v;
