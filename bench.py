@@ -524,7 +524,7 @@ def pass_trace(q4w, synth, dev, reps):
     ws = torch.empty(q4w.decode_pass_ws_bytes(layers, H), dtype=torch.uint8, device=dev)
     h0 = synth.e2b_h0(SEED, dev)
     h = torch.empty(H, dtype=torch.float16, device=dev)
-    descs = q4w.make_layers(layers)
+    descs = q4w.make_layers(layers, H)
     for _ in range(3):
         q4w.q4_decode_pass(layers, h0, h, ws, descs=descs)
     q4w.q4_set_trace(buf)

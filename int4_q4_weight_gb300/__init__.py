@@ -125,6 +125,11 @@ def _dev(t, dtype, name):
         return
     if not t.is_cuda:
         raise Q4Error(f"{name} must be a CUDA tensor")
+    # every call launches on the current device's stream: a tensor on another
+    # GPU would reach its kernels as a foreign pointer
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise Q4Error(f"{name} is on cuda:{t.device.index}, the current device is cuda:{cur}")
     if t.dtype != dtype:
         raise Q4Error(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -214,11 +219,25 @@ def q4_gemv(codes, scales, x, y=None):
     return y
 
 
+def _matrix_shape(codes, scales, rows, cols, name):
+    """codes uint8 [rows, cols/2] and rows * cols/32 scales, as the sizes imply."""
+    if codes.dim() != 2 or tuple(codes.shape) != (rows, cols // 2):
+        raise Q4Error(f"{name}.codes has shape {tuple(codes.shape)}; the sizes imply ({rows}, {cols // 2})")
+    _numel(scales, rows * cols // 32, f"{name}.scales")
+
+
 def q4_gemv_stage(mats, inp, in_mode, eps=1e-6, pair=False, out32=None, out16=None):
     """One fused decode-pass stage; ``mats`` is a list of (codes, scales)."""
     lib = load()
     n = len(mats)
+    if not 1 <= n <= 3 or (pair and n != 2):
+        raise Q4Error(f"q4_gemv_stage takes 1 to 3 matrices (exactly 2 with pair), got {n}")
     K = mats[0][0].shape[1] * 2
+    for i, (c, s) in enumerate(mats):
+        _matrix_shape(c, s, c.shape[0], K, f"mats[{i}]")
+    if pair and mats[0][0].shape[0] != mats[1][0].shape[0]:
+        raise Q4Error("pair: gate and up must have the same rows")
+    _numel(inp, K, "in")
     arr = (q4_matrix * n)()
     rows = (ci * n)()
     o32 = (vp * n)()
@@ -232,6 +251,8 @@ def q4_gemv_stage(mats, inp, in_mode, eps=1e-6, pair=False, out32=None, out16=No
         rows[i] = c.shape[0]
         _dev(out32[i], torch.float32, f"out32[{i}]")
         _dev(out16[i], torch.float16, f"out16[{i}]")
+        _numel(out32[i], c.shape[0], f"out32[{i}]")
+        _numel(out16[i], c.shape[0], f"out16[{i}]")
         o32[i] = out32[i].data_ptr() if out32[i] is not None else None
         o16[i] = out16[i].data_ptr() if out16[i] is not None else None
     _dev(inp, torch.float16 if in_mode in (Q4_IN_F16, Q4_IN_RMS_F16) else torch.float32, "in")
@@ -246,12 +267,34 @@ def q4_rmsnorm_f16(inp, eps=1e-6, out=None):
     if out is None:
         out = torch.empty(inp.shape, dtype=torch.float16, device=inp.device)
     _dev(out, torch.float16, "out")
+    _numel(out, inp.numel(), "out")
     _check(lib.q4_rmsnorm_f16(_ptr(inp), inp.numel(), eps, _ptr(out), _stream()), "q4_rmsnorm_f16")
     return out
 
 
-def make_layers(layers):
-    """Host descriptor array from a list of dicts name -> (codes, scales)."""
+def _check_layers(layers, H):
+    """Every matrix of every layer has the shape the pass reads for hidden H:
+    q [Q, H], k and v [KV, H] (together or both absent), o [H, Q],
+    gate and up [I, H], down [H, I]."""
+    for i, lw in enumerate(layers):
+        if ("k" in lw) != ("v" in lw):
+            raise Q4Error(f"layers[{i}]: k and v must be given together")
+        Q, I = lw["q"][0].shape[0], lw["g"][0].shape[0]
+        KV = lw["k"][0].shape[0] if "k" in lw else 0
+        want = {"q": (Q, H), "k": (KV, H), "v": (KV, H), "o": (H, Q), "g": (I, H), "u": (I, H), "d": (H, I)}
+        for key, (r, c) in want.items():
+            if key in lw:
+                _matrix_shape(*lw[key], r, c, f"layers[{i}].{key}")
+            elif key not in ("k", "v"):
+                raise Q4Error(f"layers[{i}] has no '{key}' matrix")
+
+
+def make_layers(layers, H=None):
+    """Host descriptor array from a list of dicts name -> (codes, scales); every
+    shape is checked against hidden size H (taken from layer 0's q when None)."""
+    if H is None:
+        H = layers[0]["q"][0].shape[1] * 2
+    _check_layers(layers, H)
     arr = (q4_layer * len(layers))()
     for i, lw in enumerate(layers):
         d = q4_layer()
@@ -276,14 +319,21 @@ def decode_pass_ws_bytes(layers, H):
 
 
 def q4_decode_pass(layers, h0, h_out, ws, eps=1e-6, descs=None):
-    """Run the weight pass over ``layers`` (list of dicts, or a prebuilt descriptor
-    array in ``descs``) from fp16 h0 [H] into fp16 h_out [H]."""
+    """Run the weight pass over ``layers`` (list of dicts) from fp16 h0 [H] into
+    fp16 h_out [H].  ``descs``: the descriptor array make_layers(layers, H) built
+    for the same layers (the layers' shapes are checked either way)."""
     lib = load()
     _dev(h0, torch.float16, "h0")
     _dev(h_out, torch.float16, "h_out")
     _dev(ws, torch.uint8, "ws")
+    H = h0.numel()
+    _numel(h_out, H, "h_out")
     if descs is None:
-        descs = make_layers(layers)
+        descs = make_layers(layers, H)
+    else:
+        if len(descs) != len(layers):
+            raise Q4Error(f"descs holds {len(descs)} layers, layers {len(layers)}")
+        _check_layers(layers, H)
     _check(lib.q4_decode_pass(descs, len(descs), h0.numel(), _ptr(h0), _ptr(h_out), eps, _ptr(ws),
                               ws.numel(), _stream()), "q4_decode_pass")
     return h_out
@@ -447,7 +497,7 @@ class Q4DecodePlan:
         self.layers = layers
         self.H = H
         self.eps = eps
-        self.descs = make_layers(layers)
+        self.descs = make_layers(layers, H)
         self.ws = torch.empty(decode_pass_ws_bytes(layers, H), dtype=torch.uint8, device=device)
         self.h_in = torch.zeros(H, dtype=torch.float16, device=device)
         self.h_out = torch.zeros(H, dtype=torch.float16, device=device)

@@ -103,3 +103,73 @@ def test_mis_sized_arrays_are_refused(lib):
     _rejects(lib, lambda: q4w.ple_gather_project_q8(b["ids"], b["table"], b["row_scale"], b["proj_codes"],
                                                     b["proj_scales"], b["hidden"], b["norm_w"], L=2,
                                                     gathered=_z((5, 256), torch.int8)), "gathered")
+
+
+def _layer(H=64, Q=96, KV=32, I=128, kv=True):
+    def m(r, c):
+        return _z((r, c // 2), torch.uint8), _z((r, c // 32), torch.float16)
+    lw = {"q": m(Q, H), "o": m(H, Q), "g": m(I, H), "u": m(I, H), "d": m(H, I)}
+    if kv:
+        lw.update(k=m(KV, H), v=m(KV, H))
+    return lw
+
+
+def test_stage_and_pass_shapes_reach_the_library(lib):
+    K = 128
+    g, u = (_z((64, K // 2), torch.uint8), _z((64, K // 32), torch.float16)), \
+           (_z((64, K // 2), torch.uint8), _z((64, K // 32), torch.float16))
+    q4w.q4_gemv_stage([g, u], _z(K, torch.float32), q4w.Q4_IN_RMS_F32, pair=True,
+                      out32=[_z(64, torch.float32), None], out16=[_z(64, torch.float16), None])
+    q4w.q4_rmsnorm_f16(_z(64, torch.float32))
+    layers = [_layer(), _layer(kv=False)]
+    q4w.q4_decode_pass(layers, _z(64, torch.float16), _z(64, torch.float16), _z(1, torch.uint8))
+    descs = q4w.make_layers(layers, 64)
+    q4w.q4_decode_pass(layers, _z(64, torch.float16), _z(64, torch.float16), _z(1, torch.uint8), descs=descs)
+    assert lib.calls.count("q4_decode_pass") == 2
+    assert "q4_gemv_stage" in lib.calls and "q4_rmsnorm_f16" in lib.calls
+
+
+def test_mis_shaped_stage_and_pass_are_refused(lib):
+    K = 128
+    a = (_z((64, K // 2), torch.uint8), _z((64, K // 32), torch.float16))
+    narrow = (_z((64, K // 4), torch.uint8), _z((64, K // 64), torch.float16))   # fewer columns than K
+    x = _z(K, torch.float16)
+    _rejects(lib, lambda: q4w.q4_gemv_stage([a, narrow], x, q4w.Q4_IN_F16), r"mats\[1\].codes")
+    _rejects(lib, lambda: q4w.q4_gemv_stage([(a[0], a[1][:-1])], x, q4w.Q4_IN_F16), r"mats\[0\].scales")
+    _rejects(lib, lambda: q4w.q4_gemv_stage([a], x[:-8], q4w.Q4_IN_F16), "in has")
+    _rejects(lib, lambda: q4w.q4_gemv_stage([a], x, q4w.Q4_IN_F16, out32=[_z(63, torch.float32)]), r"out32\[0\]")
+    _rejects(lib, lambda: q4w.q4_gemv_stage([a], x, q4w.Q4_IN_F16, out16=[_z(65, torch.float16)]), r"out16\[0\]")
+    _rejects(lib, lambda: q4w.q4_gemv_stage([a, a, a, a], x, q4w.Q4_IN_F16), "1 to 3")
+    _rejects(lib, lambda: q4w.q4_rmsnorm_f16(_z(64, torch.float32), out=_z(32, torch.float16)), "out")
+    bad = _layer()
+    bad["d"] = (_z((64, 32), torch.uint8), _z((64, 2), torch.float16))        # down narrower than the MLP
+    h = _z(64, torch.float16)
+    _rejects(lib, lambda: q4w.q4_decode_pass([_layer(), bad], h, h, _z(1, torch.uint8)), r"layers\[1\].d")
+    _rejects(lib, lambda: q4w.q4_decode_pass([_layer()], _z(32, torch.float16), _z(32, torch.float16),
+                                             _z(1, torch.uint8)), r"layers\[0\].q")    # h0 of another H
+    _rejects(lib, lambda: q4w.q4_decode_pass([_layer()], h, _z(63, torch.float16), _z(1, torch.uint8)), "h_out")
+    nov = _layer()
+    del nov["v"]
+    _rejects(lib, lambda: q4w.make_layers([nov], 64), "k and v")
+    good = q4w.make_layers([_layer()], 64)
+    _rejects(lib, lambda: q4w.q4_decode_pass([_layer(), _layer()], h, h, _z(1, torch.uint8), descs=good),
+             "descs holds")
+
+
+class _FakeCuda:
+    """Stands in for a CUDA tensor on a given device (the check reads nothing else first)."""
+
+    def __init__(self, index):
+        self.is_cuda = True
+        self.device = torch.device("cuda", index)
+        self.dtype = torch.float16
+
+    def is_contiguous(self):
+        return True
+
+
+def test_tensor_on_another_device_is_refused(monkeypatch):
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    q4w._dev(_FakeCuda(0), torch.float16, "x")                 # the current device passes
+    with pytest.raises(q4w.Q4Error, match="cuda:1"):
+        q4w._dev(_FakeCuda(1), torch.float16, "x")
