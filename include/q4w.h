@@ -227,15 +227,23 @@ int lmhead_softcap_argmax(const uint8_t* codes, const uint16_t* scales,
  * pass in; cudaMalloc would also synchronise the device inside a token loop).
  * The pages have no counterpart: this is a library convenience.  Its scratch
  * is a file-scope device array of 64 KiB that every GPU loading the library
- * holds until the process exits; a device whose head needs more scratch
- * than that (q4_workspace_bytes(Q4_OP_LMHEAD, ...) > 65536) gets
- * Q4_ERR_WORKSPACE.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls share the one array: calls
- * whose kernels overlap on the GPU (other streams, other host threads) race
- * and must be serialised by the caller.  Arguments and results as in
- * lmhead_softcap_argmax, without ws / ws_bytes; nothing is allocated;
- * every batch size sums exact products on the CUDA cores. */
+ * holds until the process exits.  Every batch size (1..8) runs on the CUDA
+ * cores with exact products, whose scratch is a 256-byte ticket block plus
+ * one 16-byte top-two record per batch slot (8) for each of 2 x SMs CTAs:
+ * 256 + 256 x SMs bytes (39,168 on a 152-SM GB300), independent of V, K and
+ * b.  A device with more than 255 SMs gets Q4_ERR_WORKSPACE.  (The figure
+ * q4_workspace_bytes(Q4_OP_LMHEAD, ...) reports is the workspace entry
+ * point's need, which for b >= 2 on a large vocabulary includes the
+ * tensor-core path's logits; it is not this limit.)  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current, and caches it per device without a lock: host threads
+ * whose first calls on one device coincide all store the same address.  Make
+ * that first call before any stream capture.  All calls share the one array,
+ * which keeps the last call's contents (the ticket word is cleared on the
+ * stream before each kernel): calls whose kernels overlap on the GPU (other
+ * streams, other host threads) race and must be serialised by the caller.
+ * Arguments and results as in lmhead_softcap_argmax, without ws / ws_bytes;
+ * nothing is allocated. */
 int lmhead_softcap_argmax_noalloc(const uint8_t* codes, const uint16_t* scales,
                                   const uint16_t* h_f16, int b, int V, int K, float cap,
                                   int32_t* idx, float* top1, float* top2, float* logits_opt,

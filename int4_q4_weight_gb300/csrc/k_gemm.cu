@@ -700,12 +700,12 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
     e = cudaMemsetAsync(Y, 0, (size_t)ntok * N * sizeof(float), s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm output clear");
   }
-  static bool attr_set = false;   // one per instantiation
-  if (!attr_set) {
+  static PerDevice attr_set;   // one per instantiation and device
+  if (!attr_set.get(dev.ordinal)) {
     e = cudaFuncSetAttribute(gemm::gemm_kernel<NT, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)gemm::smem_bytes(NT));
     if (e != cudaSuccess) return cuda_fail(e, "gemm smem attribute");
-    attr_set = true;
+    attr_set.set(dev.ordinal);
   }
   const int nx = (K >> 3) * NT;
   gemm::x_layout_kernel<NT, F16><<<(nx + 255) / 256, 256, 0, s>>>(X, static_cast<uint8_t*>(ws), K, ntok);

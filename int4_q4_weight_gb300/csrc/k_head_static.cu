@@ -20,7 +20,9 @@ static __device__ __align__(256) unsigned char g_head_scratch[kHeadStaticScratch
 
 // Device address of g_head_scratch on the current device, looked up once per
 // device with that device current.  In host code the array's name is only a
-// host-side stand-in, never a device address.
+// host-side stand-in, never a device address.  The per-device cache is filled
+// without a lock: host threads whose first calls on one device coincide each
+// look the address up and store the same value.
 static void* head_scratch_address(int* status) {
   static void* cache[64] = {nullptr};
   int dev = 0;

@@ -634,7 +634,7 @@ template <bool Q8>
 static int launch_ple_t(const int32_t* ids, int S, const int8_t* table, const float* row_scale, int V, int L,
                         int ld, float embed_scale, const void* proj, const uint16_t* proj_sc, const __half* hidden,
                         int D, const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
-                        cudaStream_t s) {
+                        const DeviceInfo& dev, cudaStream_t s) {
   if (ld != ple::kLd) return fail(Q4_ERR_SHAPE, "ple_gather_project: ld must be %d", ple::kLd);
   ple::Params p;
   memset(&p, 0, sizeof(p));
@@ -689,12 +689,12 @@ static int launch_ple_t(const int32_t* ids, int S, const int8_t* table, const fl
                 ? static_cast<unsigned long long*>(tb)
                 : nullptr;
   constexpr size_t smem = ple::smem_bytes<Q8>();
-  static bool attr = false;
+  static PerDevice attr;
   cudaError_t e;
-  if (!attr) {
+  if (!attr.get(dev.ordinal)) {
     e = cudaFuncSetAttribute(ple::ple_tc_kernel<Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "ple smem attribute");
-    attr = true;
+    attr.set(dev.ordinal);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ple::kCluster * L, (S + ple::kTok - 1) / ple::kTok);
@@ -718,21 +718,19 @@ int launch_ple(const int32_t* ids, int S, const int8_t* table, const float* row_
                int ld, float embed_scale, const float* proj, const __half* hidden, int D,
                const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
                const DeviceInfo& dev, cudaStream_t s) {
-  (void)dev;
   return launch_ple_t<false>(ids, S, table, row_scale, V, L, ld, embed_scale, proj, nullptr, hidden, D, norm_w, eps,
-                             out, gathered, err, s);
+                             out, gathered, err, dev, s);
 }
 
 int launch_ple_q8(const int32_t* ids, int S, const int8_t* table, const float* row_scale, int V, int L, int ld,
                   float embed_scale, const int8_t* proj_codes, const uint16_t* proj_scales, const __half* hidden,
                   int D, const float* norm_w, float eps, float* out, int8_t* gathered, int32_t* err,
                   const DeviceInfo& dev, cudaStream_t s) {
-  (void)dev;
   if (D % ple::kQC != 0 || D > 2 * ple::kQMaxStages * ple::kQC)
     return fail(Q4_ERR_SHAPE, "ple_gather_project_q8: D=%d must be a multiple of %d up to %d", D, ple::kQC,
                 2 * ple::kQMaxStages * ple::kQC);
   return launch_ple_t<true>(ids, S, table, row_scale, V, L, ld, embed_scale, proj_codes, proj_scales, hidden, D,
-                            norm_w, eps, out, gathered, err, s);
+                            norm_w, eps, out, gathered, err, dev, s);
 }
 
 }  // namespace q4w

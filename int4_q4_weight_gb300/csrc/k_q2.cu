@@ -132,12 +132,12 @@ int launch_q2_gemv(const uint8_t* codes, const float* scales, const __half* x, f
   int lgP = 5;
   while (lgP > 0 && nc % (1 << lgP)) --lgP;
   const size_t smem = (size_t)nc * q2::kChunkWords * 4;
-  static bool attr = false;
+  static PerDevice attr;
   cudaError_t e;
-  if (!attr) {
+  if (!attr.get(dev.ordinal)) {
     e = cudaFuncSetAttribute(q2::q2_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
     if (e != cudaSuccess) return cuda_fail(e, "q2 smem attribute");
-    attr = true;
+    attr.set(dev.ordinal);
   }
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, q2::q2_gemv_kernel, q2::kThr, smem);

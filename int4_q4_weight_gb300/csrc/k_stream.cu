@@ -1168,13 +1168,13 @@ static cudaError_t set_smem(const void* fn) {
 }
 
 int launch_stage_stream(const StageArgs& a, const DeviceInfo& dev, cudaStream_t s, bool pdl) {
-  static bool attr = false;
+  static PerDevice attr;
   cudaError_t e;
-  if (!attr) {
+  if (!attr.get(dev.ordinal)) {
     if ((e = set_smem((const void*)eng::stage_stream_kernel<1>)) != cudaSuccess ||
         (e = set_smem((const void*)eng::stage_stream_kernel<2>)) != cudaSuccess)
       return cuda_fail(e, "stream stage smem attribute");
-    attr = true;
+    attr.set(dev.ordinal);
   }
   int total = a.pair ? a.mat[0].rows : 0;
   if (!a.pair)
@@ -1205,12 +1205,12 @@ int launch_stage_stream(const StageArgs& a, const DeviceInfo& dev, cudaStream_t 
 int launch_head_stream(const uint8_t* codes, const __half* scales, const __half* h, int V, int K, float cap,
                        int32_t* idx, float* top1, float* top2, float* logits, void* ws, const DeviceInfo& dev,
                        cudaStream_t s) {
-  static bool attr = false;
+  static PerDevice attr;
   cudaError_t e;
-  if (!attr) {
+  if (!attr.get(dev.ordinal)) {
     if ((e = set_smem((const void*)eng::head_stream_kernel)) != cudaSuccess)
       return cuda_fail(e, "stream head smem attribute");
-    attr = true;
+    attr.set(dev.ordinal);
   }
   unsigned* ticket = reinterpret_cast<unsigned*>(ws);
   Top2* partials = reinterpret_cast<Top2*>(reinterpret_cast<char*>(ws) + kTicketBytes);
@@ -1246,12 +1246,12 @@ int launch_decode_pass_stream(const q4_layer* layers, int n_layers, int H, const
                               const DeviceInfo& dev, cudaStream_t s) {
   if (n_layers > eng::kMaxMegaLayers) return fail(Q4_ERR_SHAPE, "persistent pass holds at most %d layers",
                                                   eng::kMaxMegaLayers);
-  static bool attr = false;
+  static PerDevice attr;
   cudaError_t e;
-  if (!attr) {
+  if (!attr.get(dev.ordinal)) {
     if ((e = set_smem((const void*)eng::decode_pass_kernel)) != cudaSuccess)
       return cuda_fail(e, "decode pass smem attribute");
-    attr = true;
+    attr.set(dev.ordinal);
   }
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, eng::decode_pass_kernel, eng::kTS, eng::kSmemBytes);

@@ -48,6 +48,7 @@ int current_device(DeviceInfo* info) {
     return Q4_OK;
   }
   DeviceInfo d = {};
+  d.ordinal = dev;
   int smem = 0;
   if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
       (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||

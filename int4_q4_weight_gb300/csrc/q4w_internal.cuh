@@ -18,12 +18,25 @@ void clear_error();
 
 // Device facts cached per device (queried once).
 struct DeviceInfo {
+  int ordinal;   // the CUDA device number
   int sms;
   int cc_major, cc_minor;
   size_t smem_optin;
 };
 // Returns Q4_OK and fills *info for the current device, or an error status.
 int current_device(DeviceInfo* info);
+
+// "Already done" flags of a one-time set-up step, one per device (a kernel's
+// shared-memory attribute is a per-device setting).  Devices past the table
+// redo the step on every call.  Two host threads may both find a flag clear
+// and both do the step; that is harmless, as the step sets the same value.
+struct PerDevice {
+  bool done[64];
+  bool get(int d) const { return d >= 0 && d < 64 && done[d]; }
+  void set(int d) {
+    if (d >= 0 && d < 64) done[d] = true;
+  }
+};
 
 // Cycle budget of every bounded device-side wait (q4_set_wait_limit; the
 // Q4W_WAIT_LIMIT_CYCLES environment variable sets the initial value).

@@ -3,7 +3,7 @@
 Callers that cannot allocate device memory (start-up-planned engines, plain C
 hosts owning only their own buffers) use lmhead_softcap_argmax_noalloc, whose
 scratch is a static device array inside the library.  Two calls in a row must
-give what the workspace entry point gives.  This file is collected last so a
+give what the workspace entry point gives, and what the CPU oracle gives.  This file is collected last so a
 run that stops at the first failure has already run every other test; it also
 passes alone in a fresh process.
 """
@@ -14,6 +14,7 @@ import pytest
 import torch
 
 from int4_q4_weight_gb300 import synth
+from oracle import q4_oracle as O
 from parity import MARGIN_EXEMPT, assert_close
 
 pytestmark = pytest.mark.gpu
@@ -38,8 +39,9 @@ def _noalloc(lib, codes, scales, h, cap=30.0):
 def test_noalloc_head_matches_workspace_head(cuda_lib):
     q4w = cuda_lib
     lib = q4w.load()
-    W, _ = synth.head_inputs(seed=120, device="cuda", batch=1, V=50000, K=1536)
+    W, _ = synth.head_inputs(seed=120, device="cuda", batch=1, V=20000, K=1536)
     codes, scales = q4w.q4_quantize(W)
+    oc, os_ = codes.cpu().numpy(), scales.cpu().numpy().view(np.uint16)
     for call, b in enumerate((1, 8)):          # two calls in a row
         _, h = synth.head_inputs(seed=121 + call, device="cuda", batch=b, V=1, K=1536)
         gi, g1, g2 = _noalloc(lib, codes, scales, h)
@@ -50,6 +52,11 @@ def test_noalloc_head_matches_workspace_head(cuda_lib):
         assert np.all(same | (margin < MARGIN_EXEMPT)), (gi, ri)
         assert_close(g1.cpu().numpy(), r1.cpu().numpy(), what=f"top1 call {call}")
         assert_close(g2.cpu().numpy(), r2.cpu().numpy(), what=f"top2 call {call}")
+        # and against the oracle (fp64 logits of the same codes)
+        oi, o1, o2, om, _ = O.lmhead_softcap_argmax(oc, os_, h.cpu().numpy())
+        assert np.all((gi.cpu().numpy() == oi) | (om < MARGIN_EXEMPT)), (gi, oi)
+        assert_close(g1.cpu().numpy(), o1, what=f"top1 vs oracle call {call}")
+        assert_close(g2.cpu().numpy(), o2, what=f"top2 vs oracle call {call}")
 
 
 def test_noalloc_head_batch_on_a_tensor_core_sized_vocabulary(cuda_lib):
