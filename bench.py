@@ -20,7 +20,6 @@ import hashlib
 import json
 import math
 import os
-import resource
 import statistics
 import subprocess
 import sys
@@ -167,41 +166,31 @@ def replica_value(world, steps, seconds):
     return world * steps / seconds
 
 
-def oracle_gemv_rate(layers_np, min_seconds):
-    """Bytes/s of the oracle's dequant-GEMV over whole matrices, and the number
-    of threads it used (process CPU time / wall time)."""
-    from oracle import q4_oracle as O
-    done = 0
-    r0 = resource.getrusage(resource.RUSAGE_SELF)
-    t0 = time.perf_counter()
-    while True:
-        for mats in layers_np:
-            for (codes, scales, x) in mats:
-                O.q4_gemv(codes, scales, x)
-                done += codes.size + scales.size * 2
-        el = time.perf_counter() - t0
-        if el >= min_seconds:
-            break
-    r1 = resource.getrusage(resource.RUSAGE_SELF)
-    cpu = (r1.ru_utime - r0.ru_utime) + (r1.ru_stime - r0.ru_stime)
-    return done / el, max(1, math.ceil(cpu / el - 0.05)), el, done
+def host_cores():
+    """Cores this process may run on (sched_getaffinity), the oracle's thread count."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
-def oracle_sample_layers(layer_ids, device):
-    """Oracle-quantised matrices of the sampled layers with fp16 inputs."""
-    import torch
+def oracle_pass_layers(C, device, threads, layer_ids=None):
+    """The E2B layers quantised by the C++ oracle's own quantiser, from the
+    seeded fp32 weights of the input generator (drawn on ``device``)."""
     from int4_q4_weight_gb300 import synth
-    from oracle import q4_oracle as O
     out = []
-    for layer in layer_ids:
-        mats = []
-        for name, (r, c) in synth.e2b_matrix_shapes(layer).items():
+    for layer in (range(synth.E2B_N_LAYERS) if layer_ids is None else layer_ids):
+        lw = {}
+        for name in synth.e2b_matrix_shapes(layer):
             W = synth.e2b_weight(SEED, layer, name, device).cpu().numpy()
-            codes, scales = O.quantize_q4_0(W)
-            x = synth.normal_f16((c,), synth.sub_seed(SEED, "x", layer, name), device).cpu().numpy()
-            mats.append((codes, scales, x))
-        out.append(mats)
+            lw[name] = C.quantize_q4_0(W, threads=threads)
+            del W
+        out.append(lw)
     return out
+
+
+def layer_bytes(lw):
+    return sum(c.size + s.size * 2 for c, s in lw.values())
 
 
 # ------------------------------------------------------------ our arm ---
@@ -315,16 +304,37 @@ def run_ours(args, world, rank, local):
 
 
 def cpu_baseline(dev, step_bytes):
-    """The oracle as it stands on the host cores, on a bounded sample: its
-    dequant-GEMV over one layer of each E2B layer type, repeated for >= 10 s."""
-    sample_layers = [0, 4, 15, 19]
-    mats = oracle_sample_layers(sample_layers, dev)
-    rate, threads, el, done = oracle_gemv_rate(mats, 10.0)
-    return {"value": round(rate / step_bytes, 5), "unit": "steps/s", "cores": threads,
-            "kind": "oracle",
-            "sample": (f"oracle q4_gemv over every matrix of layers {sample_layers} (one of each "
-                       f"E2B layer type), {done} weight bytes in {el:.1f} s, scaled to the "
-                       f"{step_bytes}-byte step")}
+    """The C++ oracle as it stands (plain loops, fp64 sums) on the host cores:
+    the whole 35-layer chain with its rows split over std::thread across every
+    core of sched_getaffinity, and single-threaded on a bounded sample (the
+    chain over one layer of each E2B type), scaled to the step by bytes."""
+    from int4_q4_weight_gb300 import synth
+    from oracle import cpp_oracle
+    C = cpp_oracle.oracle()
+    cores = host_cores()
+    layers = oracle_pass_layers(C, dev, cores)
+    h0 = synth.e2b_h0(SEED, dev).cpu().numpy()
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        C.e2b_pass(h0, layers, threads=cores)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= 3.0:
+            break
+    sample_ids = [0, 4, 15, 19]
+    sample = [layers[i] for i in sample_ids]
+    sbytes = sum(layer_bytes(lw) for lw in sample)
+    t1 = time.perf_counter()
+    C.e2b_pass(h0, sample, threads=1)
+    el1 = time.perf_counter() - t1
+    wbytes = sum(layer_bytes(lw) for lw in layers)
+    return {"value": round(passes / el, 5), "unit": "steps/s", "cores": cores, "threads": cores, "kind": "oracle",
+            "sample": (f"C++ oracle (oracle/q4_oracle.cpp): {passes} full 35-layer passes of the chain in "
+                       f"{el:.1f} s, rows split over {cores} std::thread"),
+            "single_thread": {"value": round(sbytes / el1 / wbytes, 5), "unit": "steps/s", "threads": 1,
+                              "sample": (f"the chain over layers {sample_ids} (one of each E2B layer type, "
+                                         f"{sbytes} weight bytes) in {el1:.1f} s on one thread, scaled to the "
+                                         f"{wbytes}-byte pass")}}
 
 
 # ---------------------------------------------------------- other rows ---
@@ -617,56 +627,57 @@ def run_case(args):
 
 # ------------------------------------------------------ reference arm ---
 def run_reference(args, world, rank, local):
+    """The oracle as the reference arm: the C++ oracle's chain on the host cores."""
     if rank != 0:
         return
     import torch
     from int4_q4_weight_gb300 import synth
-    from oracle import q4_oracle as O
+    from oracle import cpp_oracle
 
+    C = cpp_oracle.oracle()
+    cores = host_cores()
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    layers = oracle_pass_layers(C, dev, cores)
     dims = [synth.e2b_dims(l) for l in range(synth.E2B_N_LAYERS)]
     wbytes, abytes = e2b_step_bytes(dims)
     step_bytes = wbytes + abytes
-    # the pass's matrices, row-sliced so that the whole run stays within ~60 s
-    mats = []
-    for layer in (0, 4, 15, 19):
-        for name, (r, c) in synth.e2b_matrix_shapes(layer).items():
-            W = synth.e2b_weight(SEED, layer, name, "cpu").numpy()
-            codes, scales = O.quantize_q4_0(W)
-            x = synth.normal_f16((c,), synth.sub_seed(SEED, "x", layer, name), "cpu").numpy()
-            mats.append((codes, scales, x))
-    c0, s0, x0 = mats[0]
+    h = synth.e2b_h0(SEED, dev).cpu().numpy()
+    # one step is the full 35-layer pass when the run fits about two minutes;
+    # otherwise each step runs the next few layers of the chain (cycling), and
+    # the rate is scaled to the pass by weight bytes
     t0 = time.perf_counter()
-    O.q4_gemv(c0, s0, x0)
-    per_byte = (time.perf_counter() - t0) / (c0.size + s0.size * 2)
-    budget = 60.0 / max(1, args.steps + args.warmup)
-    sl = []
-    for codes, scales, x in mats:
-        rows = int(max(8, min(codes.shape[0], budget / per_byte / (codes.shape[1] + scales.shape[1] * 2))))
-        sl.append((codes[:rows], scales[:rows], x))
-    for i in range(args.warmup):
-        cc, ss, xx = sl[i % len(sl)]
-        O.q4_gemv(cc, ss, xx)
+    C.e2b_pass(h, layers[:1], threads=cores)
+    t_layer = (time.perf_counter() - t0) * wbytes / layer_bytes(layers[0])
+    per_step = synth.E2B_N_LAYERS
+    if (args.steps + args.warmup) * t_layer > 120.0:
+        per_step = max(1, int(synth.E2B_N_LAYERS * 120.0 / ((args.steps + args.warmup) * t_layer)))
+    pos = 0
+
+    def step():
+        nonlocal pos, h
+        sl = [layers[(pos + i) % len(layers)] for i in range(per_step)]
+        pos = (pos + per_step) % len(layers)
+        h = C.e2b_pass(h, sl, threads=cores)
+        return sum(layer_bytes(lw) for lw in sl)
+
+    for _ in range(args.warmup):
+        step()
     done = 0
-    r0 = resource.getrusage(resource.RUSAGE_SELF)
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        cc, ss, xx = sl[i % len(sl)]
-        O.q4_gemv(cc, ss, xx)
-        done += cc.size + ss.size * 2
+    for _ in range(args.steps):
+        done += step()
     el = time.perf_counter() - t0
-    r1 = resource.getrusage(resource.RUSAGE_SELF)
-    threads = max(1, math.ceil(((r1.ru_utime - r0.ru_utime) + (r1.ru_stime - r0.ru_stime)) / el - 0.05))
-    value = done / el / step_bytes
-    sample = (f"each step: the oracle's q4_gemv on a row slice of one matrix of the E2B layers "
-              f"0/4/15/19 (cycled), {done} weight bytes over {args.steps} steps in {el:.1f} s, "
-              f"scaled to the {step_bytes}-byte pass")
+    value = done / el / wbytes
+    sample = (f"each step: the C++ oracle's chain over {per_step} consecutive E2B layers "
+              f"({'the full pass' if per_step == synth.E2B_N_LAYERS else 'cycling, scaled to the pass by bytes'}), "
+              f"rows split over {cores} std::thread; {done} weight bytes in {el:.1f} s")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "steps/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 / value, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "layers": 35, "hidden": 1536, "weight_format": "q4_0",
                        "algorithmic_bytes_per_step": step_bytes},
-            "cpu_baseline": {"value": round(value, 5), "unit": "steps/s", "cores": threads,
+            "cpu_baseline": {"value": round(value, 5), "unit": "steps/s", "cores": cores, "threads": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 5), "unit": "steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}

@@ -402,6 +402,31 @@ def pin_gelu_tanh(O):
     assert abs(float(O.gelu_tanh(np.array([12.0]))[0]) - 12.0) < 1e-12
 
 
+def pin_f16_rounding(O):
+    """Rounding to binary16 (nearest, ties to even), on values whose exact answer
+    follows from the format: 11 significant bits, subnormal step 2^-24,
+    largest finite 65504 (the fp16 casts of the decode chain and the stored
+    scales use it)."""
+    ldexp = math.ldexp
+    cases = [
+        (1.0, 1.0), (ldexp(1.0, -24), ldexp(1.0, -24)), (65504.0, 65504.0),
+        (1.0 + ldexp(1.0, -11), 1.0),                          # tie: to the even neighbour 1
+        (1.0 + 3 * ldexp(1.0, -11), 1.0 + ldexp(1.0, -9)),     # tie: up to the even neighbour
+        (1.0 + ldexp(1.0, -11) + ldexp(1.0, -40), 1.0 + ldexp(1.0, -10)),   # just past the tie
+        (2049.0, 2048.0), (2051.0, 2052.0),                    # spacing 2 above 2048
+        (-(1.0 + ldexp(1.0, -11)), -1.0),
+        (ldexp(1.0, -25), 0.0),                                # half the smallest subnormal: to 0
+        (3 * ldexp(1.0, -25), ldexp(1.0, -23)),                # subnormal tie: to even (2 steps)
+        (ldexp(1.0, -14) - ldexp(1.0, -25), ldexp(1.0, -14)),  # tie at the normal boundary: up (even)
+        (65519.0, 65504.0), (65520.0, math.inf), (-1e6, -math.inf),
+    ]
+    x = np.array([c[0] for c in cases], dtype=np.float64)
+    with np.errstate(over="ignore"):                           # the overflow cases are intended
+        got = np.asarray(O.to_f16(x)).astype(np.float64)
+    want = np.array([c[1] for c in cases], dtype=np.float64)
+    assert np.array_equal(got, want), [(c[0], g) for c, g, w in zip(cases, got, want) if g != w]
+
+
 def pin_e2b_dims(O):
     for r in _read_golden("e2b_layer_shapes.txt"):
         layer, full, q, kv, mlp = (int(v) for v in r)
