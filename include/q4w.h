@@ -168,7 +168,14 @@ int q4_gemm_chunk(const uint8_t* codes, const uint16_t* scales, const uint16_t* 
  *   or NULL.  1 <= S <= 4096; ld == 256; 1 <= L <= 256; D % 32 == 0,
  *   32 <= D <= 32768; V >= 1.  An id outside [0, V) writes zeros for that
  *   token and sets the optional device int32 *err to 1 (never cleared by
- *   the kernel).                                                          */
+ *   the kernel).
+ *   Arithmetic of p: each projection weight w is multiplied as two fp16
+ *   pieces, p1 = fp16(w) and p2 = fp16((w - p1) * 2^11), both rounded to
+ *   nearest even, so p1 + p2 * 2^-11 keeps 22 significant bits of w
+ *   (relative error <= 2^-22 for |w| >= 2^-14, absolute <= 2^-36 below);
+ *   the fp16 hidden is exact; products are exact and summed in fp32.
+ *   Projection weights must be finite with |w| < 65520 (fp16 range); larger
+ *   ones give an undefined result.                                        */
 int ple_gather_project(const int32_t* ids, int S, const int8_t* table,
                        const float* row_scale, int V, int L, int ld, float embed_scale,
                        const float* proj, const uint16_t* hidden_f16, int D,

@@ -5,11 +5,14 @@
 // P2 DONE: 35 layer-major blocks of 256 on axis 1).
 //
 // The projection p[t] = proj . hidden[t] is a dense contraction (L*ld rows x
-// D x S tokens), so it runs on the 5th-generation tensor cores in TF32:
-// tcgen05.mma kind::tf32, M = 128 projection rows, N = the token group (up to
-// 64, padded to a multiple of 16 with zero rows), fp32 accumulator in TMEM.
-// The fp16 hidden values are exact in TF32; the f32 projection enters with a
-// 10-bit mantissa (the tensor core reads the top 19 bits of each fp32 word).
+// D x S tokens), so it runs on the 5th-generation tensor cores with f32-class
+// arithmetic: each f32 weight w is split into two fp16 pieces,
+// p1 = fp16(w) and p2 = fp16((w - p1) * 2^11), which keep 22 of its 24
+// significant bits (|w - p1 - p2 2^-11| <= 2^-22 |w| in the normal range);
+// the fp16 hidden values are exact, so tcgen05.mma kind::f16 forms exact
+// products, accumulated in fp32 into two TMEM accumulators D1 = P1 . h and
+// D2 = P2 . h, and p = D1 + D2 * 2^-11.  M = 128 projection rows, N = the
+// token group (up to 64, padded to a multiple of 16 with zero rows).
 //
 // A 256-row layer chunk and a group of up to 64 tokens belong to a cluster of
 // four CTAs: rank r = m + 2 kh takes the 128-row half m of the chunk over the
@@ -23,17 +26,19 @@
 // those columns are fetched at the start by one 64-byte bulk copy per token.
 //
 // Warp roles (192 threads):
-//   warp 0     TMA loads (one elected lane): per stage two K sub-chunks of
-//              32 columns, each a projection tile [128 rows][32 fp32]
-//              (128-byte swizzle, the tensor core's K-major layout), and the
-//              stage's hidden tile [64 tokens][64 fp16]
+//   warp 0     TMA loads (one elected lane): per stage of 64 K columns the
+//              raw projection tile as two boxes [128 rows][32 fp32]
+//              (128-byte swizzle) and the hidden tile [64 tokens][64 fp16]
+//              (128-byte swizzle: the B operand as loaded)
 //   warp 1     TMEM allocation; the warp runs the MMA loop together and one
-//              elected lane issues the MMAs (8 per stage) and the commits
-//   warps 2-5  issue the table copies, widen the hidden tiles to fp32 in the
-//              128-byte swizzle layout (the B operand), then run the
-//              epilogue on their TMEM lane quarters (warp w reads lanes
-//              32 (w % 4) .. + 31)
-// A ring of kStages stages (A 32 KB + B 16 KB + hidden 8 KB) is guarded by
+//              elected lane issues the MMAs (8 per stage: 4 per piece) and
+//              the commits
+//   warps 2-5  issue the table copies, split the raw tile in place into the
+//              pieces P1 and P2 (thread = projection row: its two 128-byte
+//              raw rows become its P1 and P2 rows, in the 128-byte swizzle
+//              of a K-major fp16 operand), then run the epilogue on their
+//              TMEM lane quarters (warp w reads lanes 32 (w % 4) .. + 31)
+// A ring of kFStages stages (raw / pieces 32 KB + hidden 8 KB) is guarded by
 // full (TMA bytes), bready (converter warps, which arrive only after seeing
 // full) and empty (MMA commit) mbarriers; the MMA warp waits on bready alone.
 // The int8 form (ple_tc_kernel<true>; "Gemma-4 E2B mobile mixed-bit QAT
@@ -66,18 +71,17 @@ namespace ple {
 constexpr int kLd = 256;                            // rows of one layer chunk
 constexpr int kRows = 128;                          // rows per CTA (MMA M)
 constexpr int kTok = 64;                            // tokens per CTA (MMA N <= 64)
-constexpr int kKC = 32;                             // K columns per sub-chunk (128 B of fp32)
-constexpr int kSub = 2;                             // sub-chunks per stage
-constexpr int kStages = 3;
-constexpr int kABytes = kRows * kKC * 4;            // 16 KB per sub-chunk
-constexpr int kBBytes = kTok * kKC * 4;             // 8 KB per sub-chunk
-constexpr int kHBytes = kTok * kKC * 2;             // 4 KB per sub-chunk
-constexpr int kStageBytes = kSub * (kABytes + kBBytes + kHBytes);   // 56 KB, a multiple of 1024
+// f32 projection: one stage is 64 K columns
+constexpr int kFC = 64;                             // K columns per stage
+constexpr int kFStages = 4;
+constexpr int kFBox = kRows * 32 * 4;               // 16 KB: raw box [128 rows][32 fp32]; then a piece
+constexpr int kFRawBytes = 2 * kFBox;               // 32 KB: raw tile, then P1 (first half) and P2
+constexpr int kFHBytes = kTok * kFC * 2;            // 8 KB: hidden tile [64 tokens][64 fp16]
+constexpr int kFStageBytes = kFRawBytes + kFHBytes;   // 40 KB, a multiple of 1024
 constexpr int kRecvBytes = kTok * 64 * 4;           // partner's partial sums of 64 rows
 constexpr int kGtabBytes = kTok * 64;               // table bytes of the 64 finished rows per token
 constexpr int kThreads = 192;
 constexpr int kEpi0 = 2;                            // first converter / epilogue warp
-constexpr int kTmemCols = 64;
 constexpr int kCluster = 4;
 constexpr long long kDrainCycles = 2000000000LL;
 
@@ -98,26 +102,16 @@ constexpr int kQScBytes = kQMaxStages * kRows * 8;  // per (stage, row): the sta
 
 template <bool Q8>
 constexpr size_t ring_bytes() {
-  return Q8 ? (size_t)kQStages * kQStageBytes : (size_t)kStages * kStageBytes;
+  return Q8 ? (size_t)kQStages * kQStageBytes : (size_t)kFStages * kFStageBytes;
+}
+// TMEM columns: one 64-column accumulator (int8 form) or two (f32 pieces)
+template <bool Q8>
+constexpr int tmem_cols() {
+  return Q8 ? 64 : 128;
 }
 template <bool Q8>
 constexpr size_t smem_bytes() {
   return 1024 + ring_bytes<Q8>() + kRecvBytes + kGtabBytes + (Q8 ? kQScBytes : 0);
-}
-
-// Instruction descriptor, kind::tf32: D f32, A and B tf32, both K-major,
-// M = 128, N = n (a multiple of 16).
-__device__ __forceinline__ uint32_t idesc_tf32(int n) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accum) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-      : "memory");
 }
 
 // Instruction descriptor, kind::f16: D f32, A and B fp16, both K-major.
@@ -150,11 +144,38 @@ __device__ __forceinline__ uint4 dequant_i8_f16(uint2 c, __half2 dd) {
   return make_uint4(two(u0, 0x4140u), two(u0, 0x4342u), two(u1, 0x4140u), two(u1, 0x4342u));
 }
 
+// Eight f32 weights -> their fp16 pieces (column order): p1 = fp16(w) and
+// p2 = fp16((w - p1) * 2^11), both rounded to nearest even; w - p1 is exact
+// in fp32 and the scaling by 2^11 is exact, so p1 + p2 2^-11 differs from w
+// by at most 2^-22 |w| (fp16 normal range) or 2^-36 (below it).
+__device__ __forceinline__ void split_f32_f16(const float (&w)[8], uint4& p1, uint4& p2) {
+  uint32_t a[4], b[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    // two columns at a time: one packed conversion per piece, packed fp32
+    // subtract and scale (both exact)
+    const __half2 h = __floats2half2_rn(w[2 * e], w[2 * e + 1]);
+    const float2 hf = __half22float2(h);
+    unsigned long long d;
+    asm("{\n .reg .b64 v, q;\n mov.b64 v, {%1, %2};\n mov.b64 q, {%3, %4};\n"
+        " sub.rn.f32x2 v, v, q;\n mul.rn.f32x2 %0, v, %5;\n}"
+        : "=l"(d)
+        : "f"(w[2 * e]), "f"(w[2 * e + 1]), "f"(hf.x), "f"(hf.y), "l"(0x4500000045000000ull));   // 2048, 2048
+    float r0, r1;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(d));
+    const __half2 l = __floats2half2_rn(r0, r1);
+    a[e] = *reinterpret_cast<const uint32_t*>(&h);
+    b[e] = *reinterpret_cast<const uint32_t*>(&l);
+  }
+  p1 = make_uint4(a[0], a[1], a[2], a[3]);
+  p2 = make_uint4(b[0], b[1], b[2], b[3]);
+}
+
 struct Params {
   CUtensorMap tm_proj;   // f32 [L*ld][D], box [128 rows][32], 128-byte swizzle;
                          // int8 form: codes [L*ld][D], box [128 rows][64], no swizzle
-  CUtensorMap tm_hid;    // fp16 bits [S][D], box [64 rows][32]; rows past S read as zero;
-                         // int8 form: box [64 rows][64], 128-byte swizzle
+  CUtensorMap tm_hid;    // fp16 bits [S][D], box [64 rows][64], 128-byte swizzle; rows past S
+                         // and columns past D read as zero
   CUtensorMap tm_out;    // f32 out [S][L*ld], box [64 tokens][64 columns]; rows past S not written
   CUtensorMap tm_gat;    // int8 gathered [S][L*ld], box [64 tokens][64 columns] (when gathered != NULL)
   const uint2* proj_sc;      // int8 form: fp16 scales [L*ld][D/32] read as quads [L*ld][D/128]
@@ -167,7 +188,6 @@ struct Params {
   int32_t* err;          // optional id-range flag
   unsigned* dev_err;     // the library's device error word (bounded waits)
   int S, V, L, D;
-  uint32_t hid_box_bytes;   // f32 form: bytes of one hidden tile (64 columns, or 32 when D == 32)
   float embed_scale, eps;
   long long wait_limit;
   unsigned long long* trace;   // optional: CTA 0 stamps [stage][8], SM cycles since the start
@@ -204,8 +224,8 @@ __device__ __forceinline__ bool elect_one() {
 // tile then goes to the tensor core straight from its tensor load).
 template <bool Q8>
 __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_constant__ Params p) {
-  constexpr int kSt = Q8 ? kQStages : kStages;            // ring stages
-  constexpr int kStB = Q8 ? kQStageBytes : kStageBytes;   // bytes per stage
+  constexpr int kSt = Q8 ? kQStages : kFStages;            // ring stages
+  constexpr int kStB = Q8 ? kQStageBytes : kFStageBytes;   // bytes per stage
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   // partner's partial sums, [token / 4][64 rows][4 tokens]
@@ -232,12 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   const int t0 = blockIdx.y * kTok;
   const int ntok = min(kTok, p.S - t0);
   const int npad = (ntok + 15) & ~15;
-  // K units: 32-column sub-chunks (f32), a contiguous half per K half; or
-  // 128-column stages (int8), interleaved: stage st of K half kh is unit
-  // 2 st + kh
-  const int nsub = p.D / (Q8 ? kQC : kKC);
+  // K units: 64-column stages (f32; the last may be half past D, read as
+  // zero), a contiguous half per K half; or 128-column stages (int8),
+  // interleaved: stage st of K half kh is unit 2 st + kh
+  const int nsub = Q8 ? p.D / kQC : (p.D + kFC - 1) / kFC;
   const int sb = kh == 0 ? 0 : (nsub + 1) / 2, se = kh == 0 ? (nsub + 1) / 2 : nsub;   // f32: my units
-  const int ns = Q8 ? (nsub + 1 - kh) / 2 : (se - sb + kSub - 1) / kSub;   // my stages (0 only when D has one unit)
+  const int ns = Q8 ? (nsub + 1 - kh) / 2 : se - sb;   // my stages (0 only when D has one unit)
   const int PLD = p.L * kLd;
   const uint32_t full0 = tc::smem_u32(bars), bready0 = full0 + 8 * kSt, empty0 = bready0 + 8 * kSt;
   const uint32_t accfull = empty0 + 8 * kSt, drain = accfull + 8, gbar = drain + 8;
@@ -249,7 +269,6 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   auto stamp = [&](int r, int k) {
     if (tr && r < kTraceRows) tr[r * 8 + k] = (unsigned long long)(tc::clock_ordered() - t0_sh);
   };
-  auto nsc_of = [&](int st) { return min(kSub, se - sb - kSub * st); };
 
   if (threadIdx.x == 0) {
     abort_sh = 0;
@@ -265,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     tc::mbar_init(gbar, 1);
     tc::mbar_fence_init();
   }
-  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&tmem_sh), kTmemCols);
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&tmem_sh), tmem_cols<Q8>());
   // programmatic dependent launch: the next kernel in the stream may be
   // scheduled now; this one reads its inputs only after the previous
   // kernel's results are visible
@@ -300,18 +319,15 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
           tc::tma_load_2d(A + kQABytes + kQBHalf, &p.tm_hid, x + 64, t0, full0 + 8 * s, pol_keep);
         }
       } else if (elect_one()) {
-        const int nsc = nsc_of(st);
-        const uint32_t A = st0 + s * kStageBytes, H = A + kSub * (kABytes + kBBytes);
+        const uint32_t A = st0 + s * kFStageBytes;
         stamp(st, 0);
-        // the hidden tile of the whole stage is one box of 128-byte rows
-        // [64 tokens][64 fp16] (columns past D read as zero)
-        tc::mbar_expect_tx(full0 + 8 * s, (uint32_t)nsc * kABytes + p.hid_box_bytes);
-        for (int a = 0; a < nsc; ++a) {
-          // x = 32 (sb + 2 st + a) fp32 columns: 16-byte aligned
-          const int x = (sb + kSub * st + a) * kKC;
-          tc::tma_load_2d(A + a * kABytes, &p.tm_proj, x, row0, full0 + 8 * s, pol_once);
-        }
-        tc::tma_load_2d(H, &p.tm_hid, (sb + kSub * st) * kKC, t0, full0 + 8 * s, pol_keep);
+        // x = 64 (sb + st) fp32 / fp16 columns, and + 32: 16-byte aligned (a
+        // box wholly past D reads as zeros and still delivers its bytes)
+        const int x = (sb + st) * kFC;
+        tc::mbar_expect_tx(full0 + 8 * s, (uint32_t)(kFRawBytes + kFHBytes));
+        tc::tma_load_2d(A, &p.tm_proj, x, row0, full0 + 8 * s, pol_once);
+        tc::tma_load_2d(A + kFBox, &p.tm_proj, x + 32, row0, full0 + 8 * s, pol_once);
+        tc::tma_load_2d(A + kFRawBytes, &p.tm_hid, x, t0, full0 + 8 * s, pol_keep);
       }
       __syncwarp();
     }
@@ -322,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t st0 = tc::smem_u32(smem);
-    const uint32_t idesc = Q8 ? idesc_f16(npad) : idesc_tf32(npad);
+    const uint32_t idesc = idesc_f16(npad);
     bool ok = true;
     for (int st = 0; st < ns; ++st) {
       const int s = st % kSt, round = st / kSt;
@@ -345,14 +361,14 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
               mma_f16(tmem, tc::desc_sw128(A + h * kQAHalf + 32 * k), tc::desc_sw128(B + h * kQBHalf + 32 * k), idesc,
                       (st | h | k) ? 1u : 0u);
         } else {
-          const int nsc = nsc_of(st);
-          const uint32_t A = st0 + s * kStB, B = A + kSub * kABytes;
-          for (int a = 0; a < nsc; ++a) {
+          // D1 (columns 0-63) += P1 . h, D2 (columns 64-127) += P2 . h
+          const uint32_t A = st0 + s * kStB, H = A + kFRawBytes;
 #pragma unroll
-            for (int k = 0; k < kKC / 8; ++k)   // K = 8 tf32 (32 bytes) per MMA
-              mma_tf32(tmem, tc::desc_sw128(A + a * kABytes + 32 * k), tc::desc_sw128(B + a * kBBytes + 32 * k),
-                       idesc, (st | a | k) ? 1u : 0u);
-          }
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)   // K = 16 fp16 (32 bytes) per MMA
+              mma_f16(tmem + 64 * h, tc::desc_sw128(A + h * kFBox + 32 * k), tc::desc_sw128(H + 32 * k), idesc,
+                      (st | k) ? 1u : 0u);
         }
         tc::commit(empty0 + 8 * s);
         stamp(st, 4);
@@ -443,6 +459,13 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
         if (ct == 0) stamp(st, 2);
       }
     } else {
+      // ------------------------- A operands: raw f32 tile -> pieces P1, P2
+      // thread ct = projection row r: its 128-byte rows of the two raw boxes
+      // (box b holds columns 32 b .. 32 b + 31) become its P1 row (64 fp16,
+      // first box's slot) and its P2 row (second box's slot); both layouts
+      // put 16-byte group g of row r at group g ^ (r % 8) of its row, so a
+      // quarter-warp (eight consecutive rows) touches eight distinct banks
+      const int r = ct, r8 = r & 7;
       for (int st = 0; st < ns; ++st) {
         const int s = st % kSt, round = st / kSt;
         const bool landed = tc::mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
@@ -451,24 +474,27 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
           break;
         }
         if (ct == 0) stamp(st, 1);
-        uint8_t* B = smem + (size_t)s * kStageBytes + kSub * kABytes;
-        const int hrow = (int)p.hid_box_bytes / kTok;   // bytes per token row of the hidden tile
-        const uint8_t* H = B + kSub * kBBytes;
-        const int nsc = nsc_of(st);
-        for (int a = 0; a < nsc; ++a) {
+        uint8_t* row_p = smem + (size_t)s * kFStageBytes + (r >> 3) * 1024 + r8 * 128;
+        float w[64];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int idx = ct + 128 * i;      // (token t, 16-byte group j of its 128-byte row)
-            const int t = idx >> 3, j = idx & 7;
-            // tokens past S: zero rows (the tensor map already reads them as zero)
-            const uint2 h = t < ntok ? *reinterpret_cast<const uint2*>(H + t * hrow + a * (kKC * 2) + j * 8)
-                                     : make_uint2(0u, 0u);
-            const float2 x0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
-            const float2 x1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
-            // 128-byte swizzle: group j of row t sits at group j ^ (t % 8) of its row
-            *reinterpret_cast<float4*>(B + a * kBBytes + (t >> 3) * 1024 + (t & 7) * 128 + ((j ^ (t & 7)) << 4)) =
-                make_float4(x0.x, x0.y, x1.x, x1.y);
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {   // floats 4c .. 4c+3 of box b
+            const float4 f = *reinterpret_cast<const float4*>(row_p + b * kFBox + ((c ^ r8) << 4));
+            w[32 * b + 4 * c] = f.x;
+            w[32 * b + 4 * c + 1] = f.y;
+            w[32 * b + 4 * c + 2] = f.z;
+            w[32 * b + 4 * c + 3] = f.w;
           }
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {     // fp16 columns 8g .. 8g+7
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = w[8 * g + e];
+          uint4 p1, p2;
+          split_f32_f16(v, p1, p2);
+          *reinterpret_cast<uint4*>(row_p + ((g ^ r8) << 4)) = p1;
+          *reinterpret_cast<uint4*>(row_p + kFBox + ((g ^ r8) << 4)) = p2;
         }
         tc::fence_proxy_async();
         __syncwarp();
@@ -492,6 +518,12 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     float acc[kTok];
     if (ok && has) {
       tc::tmem_ld64(taddr, acc);
+      if constexpr (!Q8) {   // p = D1 + D2 * 2^-11 (the scaling is exact: one rounding)
+        float acc2[kTok];
+        tc::tmem_ld64(taddr + 64, acc2);
+#pragma unroll
+        for (int u = 0; u < kTok; ++u) acc[u] = fmaf(acc2[u], 0x1p-11f, acc[u]);
+      }
     } else {
 #pragma unroll
       for (int u = 0; u < kTok; ++u) acc[u] = 0.f;
@@ -623,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   if (threadIdx.x == 0) stamp(kTraceRows - 2, 4);
   if (warp == 1) {
     tc::fence_after();
-    tc::tmem_dealloc(tmem, kTmemCols);
+    tc::tmem_dealloc(tmem, tmem_cols<Q8>());
   }
 }
 
@@ -648,13 +680,11 @@ static int launch_ple_t(const int32_t* ids, int S, const int8_t* table, const fl
     if (st != Q4_OK) return st;
     p.proj_sc = reinterpret_cast<const uint2*>(proj_sc);
   } else {
-    st = encode_tensor_2d(&p.tm_proj, proj, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)D, (uint64_t)L * ld,
-                          ple::kKC, ple::kRows, CU_TENSOR_MAP_SWIZZLE_128B, "proj");
+    st = encode_tensor_2d(&p.tm_proj, proj, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)D, (uint64_t)L * ld, 32,
+                          ple::kRows, CU_TENSOR_MAP_SWIZZLE_128B, "proj");
     if (st != Q4_OK) return st;
-    const int hcols = D >= ple::kSub * ple::kKC ? ple::kSub * ple::kKC : ple::kKC;   // box no wider than D
-    st = encode_tensor_2d(&p.tm_hid, hidden, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)D, (uint64_t)S, hcols,
-                          ple::kTok, CU_TENSOR_MAP_SWIZZLE_NONE, "hidden");
-    p.hid_box_bytes = (uint32_t)(hcols * ple::kTok * 2);
+    st = encode_tensor_2d(&p.tm_hid, hidden, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)D, (uint64_t)S, ple::kFC,
+                          ple::kTok, CU_TENSOR_MAP_SWIZZLE_128B, "hidden");
     if (st != Q4_OK) return st;
   }
   st = encode_tensor_2d(&p.tm_out, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (uint64_t)L * ld, (uint64_t)S, 64,

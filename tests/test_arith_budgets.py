@@ -1,7 +1,8 @@
-"""Error budgets of the two tensor-core operand roundings (CPU only).
+"""Error budgets of the tensor-core operand roundings (CPU only).
 
-The PLE projection runs in TF32 (the f32 projection keeps a 10-bit mantissa)
-and the batched LM head rounds each dequantised weight once to fp16.  Both
+The PLE projection multiplies two fp16 pieces of each f32 weight (p1 = fp16(w),
+p2 = fp16((w - p1) 2^11), 22 significant bits kept) and the batched LM head
+rounds each dequantised weight once to fp16.  Both
 budgets are checked here by feeding the rounded operand to the oracle (exact
 fp64 arithmetic otherwise) and comparing with the oracle on the exact operand
 under the parity rule, at the real row widths and vocabulary-scale samples.
@@ -14,13 +15,16 @@ from oracle import q4_oracle as O
 from parity import MARGIN_EXEMPT, TOL, rel_err
 
 
-def _tf32_truncate(a):
-    """Drop the 13 low mantissa bits of fp32 values (what the tensor core reads)."""
-    u = np.asarray(a, np.float32).view(np.uint32) & np.uint32(0xFFFFE000)
-    return u.view(np.float32)
+def _fp16_pieces(a):
+    """p1 + p2 2^-11 with p1 = fp16(w), p2 = fp16((w - p1) * 2^11) (what the
+    tensor cores multiply), in fp64."""
+    w = np.asarray(a, np.float32).astype(np.float64)
+    p1 = w.astype(np.float16).astype(np.float64)
+    p2 = ((w - p1) * 2048.0).astype(np.float16).astype(np.float64)
+    return p1 + p2 / 2048.0
 
 
-def test_tf32_projection_budget():
+def test_fp16_pieces_projection_budget():
     rng = np.random.default_rng(71)
     S, L, ld, D, V = 16, 8, 256, 1536, 64
     proj = (rng.standard_normal((L * ld, D)) * 0.02).astype(np.float32)
@@ -29,10 +33,17 @@ def test_tf32_projection_budget():
     row_scale = rng.uniform(0.001, 0.02, V).astype(np.float32)
     norm_w = rng.uniform(0.5, 1.5, ld).astype(np.float32)
     ids = rng.integers(0, V, S).astype(np.int32)
+    # the pieces' sum reproduces the weight to 2^-22 relative (fp16 normal range)
+    w = proj.astype(np.float64)
+    pieces = _fp16_pieces(proj)
+    normal = np.abs(w) >= 2.0 ** -14
+    assert np.all(np.abs(pieces - w)[normal] <= 2.0 ** -22 * np.abs(w)[normal])
+    assert np.all(np.abs(pieces - w)[~normal] <= 2.0 ** -36)
     exact, _ = O.ple_gather_project(ids, table, row_scale, proj, hidden, norm_w, L=L, ld=ld)
-    tf32, _ = O.ple_gather_project(ids, table, row_scale, _tf32_truncate(proj), hidden, norm_w, L=L, ld=ld)
-    e = rel_err(tf32, exact)
-    assert 0 < e < 0.75 * TOL, e
+    # the oracle fed the pieces' sum (as f32, which holds its 22 bits exactly)
+    split, _ = O.ple_gather_project(ids, table, row_scale, pieces.astype(np.float32), hidden, norm_w, L=L, ld=ld)
+    e = rel_err(split, exact)
+    assert e < 1e-5, e
 
 
 def test_fp16_weight_tile_head_budget():

@@ -103,7 +103,7 @@ def test_head_repeatable(cuda_lib):
 
 
 # ----------------------------------------------------------------- PLE ---
-def _ple_check(q4w, p, L, proj_zero=False):
+def _ple_check(q4w, p, L, proj_zero=False, tol=None):
     out, gathered = q4w.ple_gather_project(
         p.ids, p.table, p.row_scale, p.proj, p.hidden, p.norm_w, L=L,
         gathered=torch.empty((p.ids.numel(), L * 256), dtype=torch.int8, device="cuda"))
@@ -115,7 +115,7 @@ def _ple_check(q4w, p, L, proj_zero=False):
     if proj_zero:
         assert np.array_equal(out.cpu().numpy(), ro)
     else:
-        assert_close(out.cpu().numpy(), ro, what="ple out")
+        assert_close(out.cpu().numpy(), ro, what="ple out", **({} if tol is None else {"tol": tol}))
 
 
 @pytest.mark.parametrize("S,V,L,D", [(5, 1000, 3, 64), (17, 333, 2, 1536), (64, 4096, 35, 1536),
@@ -133,11 +133,14 @@ def test_ple_token_groups(cuda_lib, S, V, L, D):
 
 
 def test_ple_projection_term_alone(cuda_lib):
-    # zero table bytes: out is the normalised projection alone, so the TF32
-    # projection error is not hidden behind the larger gathered term
+    # zero table bytes: out is the normalised projection alone, so the
+    # projection's own error is not hidden behind the larger gathered term;
+    # the f32 projection is multiplied as two fp16 pieces (22 bits of each
+    # weight) with fp32 accumulation, so it is held to 1e-4, well inside the
+    # 2e-3 parity rule
     p = synth.ple_inputs(seed=93, device="cuda", S=64, V=512, L=35, D=1536)
     p.table.zero_()
-    _ple_check(cuda_lib, p, 35)
+    _ple_check(cuda_lib, p, 35, tol=1e-4)
 
 
 def test_ple_proj_zero_bit_exact(cuda_lib):
