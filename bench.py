@@ -375,9 +375,15 @@ def row_gemv(q4w, synth, dev, hbm, reps=10):
     t = _time_graph(lambda: [q4w.q4_gemv(ci, si, xv, y) for ci, si in cs], reps) / copies
     b = per + 2 * 1536 + 4 * 2048
     t_iso = _time_graph(lambda: [q4w.q4_gemv(c, s, xv, y) for _ in range(100)], reps) / 100
+    # the read-only-weights form: each GEMV's weight tiles stream while the one
+    # before it finishes
+    t_ro = _time_graph(lambda: [q4w.q4_gemv_weights_ro(ci, si, xv, y) for ci, si in cs], reps) / copies
     return {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4),
             "us_per_gemv_streamed": round(t * 1e6, 3),
-            "us_per_gemv_isolated_l2_resident": round(t_iso * 1e6, 3), "bytes": b, "copies": copies}
+            "us_per_gemv_isolated_l2_resident": round(t_iso * 1e6, 3),
+            "weights_ro": {"GB/s": round(b / t_ro / 1e9, 1), "frac": round(b / t_ro / 1e9 / hbm, 4),
+                           "us_per_gemv_streamed": round(t_ro * 1e6, 3)},
+            "bytes": b, "copies": copies}
 
 
 def row_gemv_batch(q4w, synth, dev, hbm, batch=4, reps=10):

@@ -118,6 +118,19 @@ int q4_gemv(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16,
             float* y, int N, int K, int batch, void* ws, size_t ws_bytes,
             q4_stream_t stream);
 
+/* q4_gemv_weights_ro: q4_gemv with the caller's promise that the weights are
+ * read-only for the call: no kernel issued earlier on the stream that may
+ * still be running writes codes or scales (model weights written once at
+ * load time, say).  The kernel then starts streaming its weight tiles
+ * before the preceding kernel on the stream has finished (programmatic
+ * dependent launch); it reads x, and writes y, only after that kernel's
+ * results are visible, as q4_gemv does.  Same arguments, results and bits
+ * as q4_gemv.  If the promise is broken the kernel may compute with weights
+ * from before the earlier kernel's writes.  batch > 1 behaves as q4_gemv. */
+int q4_gemv_weights_ro(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16,
+                       float* y, int N, int K, int batch, void* ws, size_t ws_bytes,
+                       q4_stream_t stream);
+
 /* q2_gemv: INT2 per-row symmetric GEMV (the mixed-bit recipe's FFN of
  * L15-L34 and tied head):  y[n] = scale[n] * sum_k (code[n][k] - 2) x[k],
  * fp32 accumulation, the row scale applied once after the row sum.

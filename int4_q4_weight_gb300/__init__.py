@@ -15,7 +15,7 @@ import os
 import torch
 
 __all__ = [
-    "load", "build", "Q4Error", "q4_quantize", "q4_gemv", "q4_gemv_stage", "q4_rmsnorm_f16",
+    "load", "build", "Q4Error", "q4_quantize", "q4_gemv", "q4_gemv_weights_ro", "q4_gemv_stage", "q4_rmsnorm_f16",
     "q4_decode_pass", "q4_decode_pass_launches", "q2_gemv", "lmhead_softcap_argmax", "ple_gather_project", "q4_gemm_chunk",
     "q8_quantize", "ple_gather_project_q8",
     "q4_workspace_bytes", "q4_version", "Q4_IN_F16", "Q4_IN_RMS_F16", "Q4_IN_RMS_F32",
@@ -50,6 +50,7 @@ class q4_layer(ctypes.Structure):
 _SIGS = {
     "q4_quantize": (ci, [vp, ci, ci, vp, vp, vp, vp]),
     "q4_gemv": (ci, [vp, vp, vp, vp, ci, ci, ci, vp, csz, vp]),
+    "q4_gemv_weights_ro": (ci, [vp, vp, vp, vp, ci, ci, ci, vp, csz, vp]),
     "q4_gemm_chunk": (ci, [vp, vp, vp, vp, ci, ci, ci, vp, csz, vp]),
     "ple_gather_project": (ci, [vp, ci, vp, vp, ci, ci, ci, cf, vp, vp, ci, vp, cf, vp, vp, vp, vp]),
     "q8_quantize": (ci, [vp, ci, ci, vp, vp, vp, vp]),
@@ -202,6 +203,16 @@ def q8_quantize(W, codes=None, scales=None, err=None):
 
 def q4_gemv(codes, scales, x, y=None):
     """y [b, N] f32 = dequant(codes, scales) @ x[b]  (x fp16 [b, K] or [K])."""
+    return _gemv("q4_gemv", codes, scales, x, y)
+
+
+def q4_gemv_weights_ro(codes, scales, x, y=None):
+    """q4_gemv, promising that no earlier kernel still running on the stream
+    writes codes or scales: the weight tiles stream before that kernel ends."""
+    return _gemv("q4_gemv_weights_ro", codes, scales, x, y)
+
+
+def _gemv(name, codes, scales, x, y):
     lib = load()
     _dev(codes, torch.uint8, "codes")
     _dev(scales, torch.float16, "scales")
@@ -214,8 +225,7 @@ def q4_gemv(codes, scales, x, y=None):
     _numel(scales, N * K // 32, "scales")
     _numel(x, batch * K, "x")
     _numel(y, batch * N, "y")
-    _check(lib.q4_gemv(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), N, K, batch, None, 0,
-                       _stream()), "q4_gemv")
+    _check(getattr(lib, name)(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), N, K, batch, None, 0, _stream()), name)
     return y
 
 

@@ -191,10 +191,8 @@ int q8_quantize(const float* W, int N, int K, int8_t* codes, uint16_t* scales, i
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
-int q4_gemv(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16, float* y, int N,
-            int K, int batch, void* ws, size_t ws_bytes, q4_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
+static int gemv_impl(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16, float* y, int N, int K,
+                     int batch, q4_stream_t stream, bool weights_ro) {
   clear_error();
   CHECK_NULL(codes);
   CHECK_NULL(scales);
@@ -218,10 +216,25 @@ int q4_gemv(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16,
     a.in = x_f16;
     a.in_mode = Q4_IN_F16;
     a.eps = 0.f;
+    a.weights_early = weights_ro ? 1 : 0;
     return launch_stage(a, dev, s, true);
   }
   return launch_gemv_batched(codes, reinterpret_cast<const __half*>(scales),
                              reinterpret_cast<const __half*>(x_f16), y, N, K, batch, dev, s);
+}
+
+int q4_gemv(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16, float* y, int N,
+            int K, int batch, void* ws, size_t ws_bytes, q4_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  return gemv_impl(codes, scales, x_f16, y, N, K, batch, stream, false);
+}
+
+int q4_gemv_weights_ro(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16, float* y, int N,
+                       int K, int batch, void* ws, size_t ws_bytes, q4_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  return gemv_impl(codes, scales, x_f16, y, N, K, batch, stream, true);
 }
 
 int q4_gemv_stage(const q4_matrix* mats, const int* rows, int nmat, int K, const void* in,

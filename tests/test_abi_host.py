@@ -67,6 +67,8 @@ def test_null_and_shape_rejections(lib):
     assert lib.q4_gemv(A, A, A, A, 16, 64, 9, None, 0, None) == 2       # batch > 8
     assert lib.q4_gemv(A, A, A, A, 0, 64, 1, None, 0, None) == 2        # N < 1
     assert lib.q4_gemv(A, A, A, A, 16, 65536, 1, None, 0, None) == 2    # K too large
+    assert lib.q4_gemv_weights_ro(None, A, A, A, 16, 64, 1, None, 0, None) == 1
+    assert lib.q4_gemv_weights_ro(A, A, A, A, 16, 48, 1, None, 0, None) == 2
     assert lib.q4_gemm_chunk(A, A, A, A, 32, 128, 64, None, 0, None) == 2   # M != 64
     assert lib.q4_gemm_chunk(A, A, A, A, 64, 100, 64, None, 0, None) == 2   # N % 128
     assert lib.q4_gemm_chunk(A, A, A, A, 64, 128, 64, None, 0, None) == 4   # no workspace

@@ -118,6 +118,30 @@ def test_gemv_deterministic(cuda_lib):
     assert torch.equal(a, b)
 
 
+def test_gemv_weights_ro_same_bits_and_waits_for_x(cuda_lib):
+    """The read-only-weights form computes q4_gemv's bits; back to back, and
+    when its x comes from the kernel just before it (x must still be read only
+    after that kernel's results are visible)."""
+    W, x = synth.gemv_inputs(seed=27, device="cuda", N=2048, K=1536)
+    codes, scales = cuda_lib.q4_quantize(W)
+    W2 = synth.normal((1536, 2048), 0.02, synth.sub_seed(28), "cuda")
+    c2, s2 = cuda_lib.q4_quantize(W2)
+    torch.cuda.synchronize()                       # the weights exist before the promise starts
+    ref = cuda_lib.q4_gemv(codes, scales, x[0]).clone()
+    outs = [cuda_lib.q4_gemv_weights_ro(codes, scales, x[0]) for _ in range(6)]
+    # a chain: y1 -> fp16 -> the next GEMV's x, each step on the read-only form
+    y1 = cuda_lib.q4_gemv_weights_ro(codes, scales, x[0])
+    x2 = y1.to(torch.float16)
+    y2 = cuda_lib.q4_gemv_weights_ro(c2, s2, x2)
+    y2_ref = cuda_lib.q4_gemv(c2, s2, x2.clone())
+    torch.cuda.synchronize()
+    for y in outs:
+        assert torch.equal(y, ref)
+    assert torch.equal(y1, ref) and torch.equal(y2, y2_ref)
+    yr = O.q4_gemv(c2.cpu().numpy(), s2.cpu().numpy().view(np.uint16), x2.cpu().numpy())
+    assert_close(y2.cpu().numpy(), yr, what="weights_ro chain")
+
+
 def test_gemv_large_activations(cuda_lib):
     """fp16 x near the top of its range and many tiny ones (bias trick headroom)."""
     N, K = 256, 4096
