@@ -49,7 +49,7 @@ def measured_peaks():
 
 # Sources of the persistent decode-pass kernel and its launch: a stored DRAM
 # traffic figure is used only while these are unchanged.
-PASS_SOURCES = ("k_stream.cu", "q4w_device.cuh", "q4w_internal.cuh", "q4w_top2.cuh", "q4w_api.cu")
+PASS_SOURCES = ("k_stream.cu", "q4w_device.cuh", "q4w_internal.cuh", "q4w_tc.cuh", "q4w_top2.cuh", "q4w_api.cu")
 
 
 def source_hash(names=PASS_SOURCES):

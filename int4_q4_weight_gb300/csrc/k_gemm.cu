@@ -85,12 +85,7 @@ __host__ __device__ constexpr size_t smem_bytes(int n) {
 constexpr long long kDrainCycles = 2000000000LL;
 constexpr long long kShortDrainCycles = 4000000LL;   // aborting: copies in flight land well within this
 
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile("{\n .reg .pred P;\n .reg .b32 R;\n elect.sync R|P, 0xffffffff;\n selp.b32 %0, 1, 0, P;\n}"
-               : "=r"(pred));
-  return pred != 0;
-}
+using tc::elect_one;
 
 // Instruction descriptor, kind::f16: D f32, A and B bf16 (format 1) or fp16
 // (format 0), both K-major, M = 128, N = n.
@@ -106,58 +101,26 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          ((uint64_t)(sbo >> 4) << 32) | (1ull << 46);
 }
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t a) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(a), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
+// The shared building blocks (q4w_tc.cuh) under the names this file uses;
+// its bounded waits report to the library's device error word.
+using tc::fence_proxy_async;
+using tc::mbar_arrive;
+using tc::mbar_expect_tx;
+using tc::mbar_init;
+using tc::mbar_test;
+using tc::smem_u32;
+using tc::tmem_ld16;
 
 // Bounded wait.  Returns false when the wait ran out or the CTA is aborting.
 // sleep_ns > 0: roles off the critical path back off between polls, so that
 // their spinning does not take issue slots from the converter warps.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, long long limit,
                                           volatile int* abort_flag, unsigned sleep_ns = 0) {
-  if (tc::mbar_probe(a, parity)) return true;   // the first check does not suspend
-  const long long t0 = clock64();
-  for (;;) {
-    if (*abort_flag) return false;
-    if (clock64() - t0 > limit) {   // checked before every suspending retry: a zero budget gives up at once
-      *abort_flag = 1;
-      atomicOr(&g_device_error, 1u);
-      return false;
-    }
-    if (mbar_test(a, parity)) return true;
-    if (sleep_ns) __nanosleep(sleep_ns);
-  }
+  return tc::mbar_wait(a, parity, limit, abort_flag, &g_device_error, sleep_ns);
 }
-
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
-               : "memory");
-}
+__device__ __forceinline__ void tc_fence_before() { tc::fence_before(); }
+__device__ __forceinline__ void tc_fence_after() { tc::fence_after(); }
+__device__ __forceinline__ void tc_commit(uint32_t mbar) { tc::commit(mbar); }
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t id,
                                        uint32_t accum) {
   asm volatile(
@@ -165,20 +128,6 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(id), "r"(accum)
       : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-        "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
@@ -244,27 +193,8 @@ struct Params {
 
 constexpr int kTraceChunks = 256;
 
-// 2-D tensor-map tile load into shared memory, completing on an mbarrier.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t mbar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(mbar), "l"(policy)
-      : "memory");
-}
-// Contiguous bulk copy global -> shared, completing on an mbarrier.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar,
-                                          uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(mbar), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
-}
+using tc::bulk_load;
+using tc::tma_load_2d;
 
 __device__ __forceinline__ void item_range(const Params& p, int item, int& tile, int& c0, int& c1) {
   tile = item / p.splits;

@@ -212,12 +212,7 @@ __device__ __forceinline__ float lane_token_sums16(float (&v)[16], int lane) {
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile("{\n .reg .pred P;\n .reg .b32 R;\n elect.sync R|P, 0xffffffff;\n selp.b32 %0, 1, 0, P;\n}"
-               : "=r"(pred));
-  return pred != 0;
-}
+using tc::elect_one;
 
 // Q8: the projection is int8 per-block-32 (codes + fp16 scales), widened to
 // fp16 tiles by the converter warps and multiplied on kind::f16 (the hidden

@@ -24,6 +24,7 @@
 // device error word set.
 #include "q4w_device.cuh"
 #include "q4w_internal.cuh"
+#include "q4w_tc.cuh"
 #include "q4w_top2.cuh"
 
 namespace q4w {
@@ -45,9 +46,13 @@ constexpr size_t kSmemBytes = 128 + (size_t)kSlots * kSlotBytes + kXsBytes +
 constexpr long long kDrainCycles = 2000000000LL;   // in-flight copies always land well within this
 
 // ----------------------------------------------------------- primitives ---
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
+// mbarriers, bulk copies, timers and cache policies: the shared building blocks
+using tc::mbar_arrive;
+using tc::mbar_expect_tx;
+using tc::mbar_init;
+using tc::mbar_probe;
+using tc::mbar_test;
+using tc::smem_u32;
 __device__ __forceinline__ void bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -60,24 +65,6 @@ __device__ __forceinline__ bool bar_and(int id, int n, bool v) {
       : "r"((uint32_t)v), "r"(id), "r"(n)
       : "memory");
   return r != 0;
-}
-__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t a) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(a), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 
 struct Ctl {
@@ -104,16 +91,6 @@ __device__ __forceinline__ bool aborting(const Ctl& c) {
 // The shared abort flag is read every iteration; the grid-wide flag (a
 // global load, about an L2 round trip) and the clock on the first retry and
 // then every 256 (so a zero budget gives up at once).
-__device__ __forceinline__ bool mbar_probe(uint32_t a, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(a), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, const Ctl& c) {
   if (mbar_probe(a, parity)) return true;
   const long long t0 = clock64();
@@ -130,29 +107,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, const Ctl
   }
 }
 
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
 // Trace stamp: SM cycles since the current stage began.
 __device__ __forceinline__ unsigned long long stamp(const Ctl& c) {
   return (unsigned long long)(clock64() - c.tr_c0);
-}
-
-__device__ __forceinline__ uint64_t evict_first_policy() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar,
-                                         uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(mbar), "l"(policy)
-      : "memory");
 }
 
 // ------------------------------------------------------------- geometry ---
@@ -233,8 +190,8 @@ __device__ bool produce_stage(const StageArgs& a, uint32_t& gcount, uint32_t slo
 #pragma unroll
     for (int t = 0; t < NM; ++t) {
       const StageMat& M = a.mat[NM == 2 ? t : m];
-      bulk_g2s(dst, M.codes + (size_t)r0 * g.K2, (uint32_t)n * g.K2, full0 + 8 * s, policy);
-      bulk_g2s(dst + (uint32_t)n * g.K2, M.scales + (size_t)r0 * g.nb, (uint32_t)n * g.nb * 2, full0 + 8 * s,
+      tc::bulk_load(dst, M.codes + (size_t)r0 * g.K2, (uint32_t)n * g.K2, full0 + 8 * s, policy);
+      tc::bulk_load(dst + (uint32_t)n * g.K2, M.scales + (size_t)r0 * g.nb, (uint32_t)n * g.nb * 2, full0 + 8 * s,
                policy);
       dst += per;
     }
@@ -921,7 +878,7 @@ __global__ void __launch_bounds__(kTS, 1) stage_stream_kernel(const StageArgs a,
   uint32_t gcount = 0;
   if (threadIdx.x >= kCT) {
     if (threadIdx.x == kCT) {
-      const uint64_t pol = evict_first_policy();
+      const uint64_t pol = tc::policy_evict_first();
       if (!a.weights_early) pdl_wait();
       produce_stage<NM>(a, gcount, S.slots0, S.full0, S.empty0, pol, c);
       producer_drain(gcount, S.full0, c.err);
@@ -954,7 +911,7 @@ __global__ void __launch_bounds__(kTS, 1) head_stream_kernel(const StageArgs a, 
   top2_init(best);
   if (threadIdx.x >= kCT) {
     if (threadIdx.x == kCT) {
-      const uint64_t pol = evict_first_policy();
+      const uint64_t pol = tc::policy_evict_first();
       produce_stage<1>(a, gcount, S.slots0, S.full0, S.empty0, pol, c);
       producer_drain(gcount, S.full0, c.err);
     }
@@ -1093,7 +1050,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
   uint32_t gcount = 0;
   if (threadIdx.x >= kCT) {
     if (threadIdx.x == kCT) {
-      const uint64_t pol = evict_first_policy();
+      const uint64_t pol = tc::policy_evict_first();
       for (int s = 0; s < nst; ++s) {
         sp = mega_stage(A, Ls, s);
         const StageArgs& a = sp;
@@ -1110,7 +1067,7 @@ __global__ void __launch_bounds__(kTS, 1) decode_pass_kernel(const __grid_consta
       unsigned long long* tr = nullptr;
       if (A.trace && threadIdx.x == 0) {
         tr = A.trace + ((size_t)s * gridDim.x + blockIdx.x) * 8;
-        tr[0] = globaltimer();
+        tr[0] = tc::globaltimer();
         c.tr_c0 = clock64();
       }
       c.tr = tr;
