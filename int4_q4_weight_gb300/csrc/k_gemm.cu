@@ -4,29 +4,34 @@
 // entry point has a static query width of 64 and serves full-width chunks.
 // Y[t][n] = sum_k bf16(scale*(code-8))[n][k] * bf16(x[t][k]), fp32 accumulate.
 //
-// Swap-AB: the weight tile is the M=128 operand (A, dequantised in shared
-// memory), the 64 tokens are the N=64 operand (B), the accumulator D[128][64]
-// (fp32) lives in tensor memory.  One CTA per SM, persistent over work items
-// (a 128-row tile and a range of 64-column K chunks; K is split across CTAs
-// when there are fewer tiles than SMs, the splits then add into Y).
+// Swap-AB: the weight tile is the M=128 operand (A, dequantised by the
+// converter warps straight into tensor memory), the 64 tokens are the N=64
+// operand (B, in shared memory), the accumulator D[128][64] (fp32) lives in
+// tensor memory.  With A in tensor memory the shared-memory port carries only
+// the raw codes and the token tiles.  One CTA per SM, persistent over work
+// items (a 128-row tile and a range of 64-column K chunks; K is split across
+// CTAs when there are fewer tiles than SMs, the splits then add into Y).
 //
 // Warp roles (480 threads):
 //   warps 0-3   epilogue: tcgen05.ld of their TMEM lane quarter, store to Y
 //   warps 4-11  converters: raw codes + scales from the raw ring, nibble ->
-//               bf16 (exact d*(q-8) in fp32, then round to nearest even),
-//               written in the no-swizzle K-major core-matrix layout (A)
+//               bf16 (exact d*(q-8) in fp32, then round to nearest even); a
+//               thread owns a tile row (TMEM lane) and 64 of the chunk's 128
+//               columns, written with one tcgen05.st of 32 columns (warps
+//               w and w + 4 share TMEM lane quarter w % 4)
 //   warp 12     TMEM allocator and MMA issuer: the warp walks the pipeline
 //               and waits together, one elected lane issues the 8 MMAs of a
-//               128-column stage and the commits
+//               128-column stage (A from tensor memory) and the commits
 //   warp 13     raw-ring TMA loads (one elected lane issues)
 //   warp 14     token tile (B) of each operand stage: one bulk copy from the
 //               bf16 copy of X, completing on the stage's full barrier
 // X is rounded to bf16 once per call by a small kernel ahead of the GEMM (in
 // the caller's workspace) instead of once per tile and chunk.  The raw ring
 // (kRawStages x 256 K columns: codes 16 KB + scales 2 KB) keeps weight bytes
-// in flight; the operand ring (kStages x (A 32 KB + B 16 KB), 128 K columns
-// each) feeds the tensor cores.  full counts the converter warps and the B
-// loader (with its bytes), so the MMA issuer waits on one barrier per stage.
+// in flight; the operand stages (kStages x (A: 64 TMEM columns, B: 16 KB of
+// shared memory), 128 K columns each) feed the tensor cores.  full counts the
+// converter warps and the B loader (with its bytes), so the MMA issuer waits
+// on one barrier per stage.
 // Two TMEM accumulators (2 x 64 columns) let the epilogue of one item
 // overlap the MMAs of the next.  Every mbarrier wait is bounded in
 // clock cycles; on expiry the CTA raises an abort flag, every role leaves its
@@ -60,16 +65,23 @@ unsigned* device_error_word() {
 namespace gemm {
 
 constexpr int kStages = 3;
-constexpr int kRawStages = 4;
+constexpr int kRawStages = 8;
 constexpr int kRawChunks = 2;          // operand chunks per raw stage (256 K columns)
 constexpr int kTileM = 128;            // weight rows per tile (MMA M)
 constexpr int kTok = 64;               // tokens of the prefill GEMM (MMA N)
 constexpr int kChunk = 128;            // K columns per operand stage (8 MMAs of K = 16)
-constexpr int kABytes = kTileM * kChunk * 2;   // 32 KB of 16-bit weights
-// per token count N (the MMA N): token tile bytes per stage, stage bytes, TMEM columns (two accumulators)
+// A operand stages in tensor memory: 128 lanes (tile rows) x 64 columns (128
+// 16-bit weights of a chunk, two per 32-bit column, K order)
+constexpr int kACols = kChunk / 2;
+// per token count N (the MMA N): token tile bytes per stage (the only operand
+// in shared memory), the first TMEM column of the A stages (after the two
+// accumulators) and the TMEM columns allocated (a power of two)
 __host__ __device__ constexpr int b_bytes(int n) { return n * kChunk * 2; }
-__host__ __device__ constexpr int stage_bytes(int n) { return kABytes + b_bytes(n); }
-__host__ __device__ constexpr int tmem_cols(int n) { return 2 * n < 32 ? 32 : 2 * n; }
+__host__ __device__ constexpr int stage_bytes(int n) { return b_bytes(n); }
+__host__ __device__ constexpr int a_col0(int n) { return 2 * n < 32 ? 32 : 2 * n; }
+__host__ __device__ constexpr int tmem_cols(int n) {
+  return a_col0(n) + kStages * kACols <= 256 ? 256 : 512;
+}
 constexpr int kRawCodeBytes = kTileM * kChunk * kRawChunks / 2;   // 16 KB: [128 rows][128 B]
 constexpr int kRawScaleBytes = kTileM * 16;                         // 2 KB: [128 rows][8 fp16]
 constexpr int kRawBytes = kRawCodeBytes + kRawScaleBytes;
@@ -121,12 +133,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, long long
 __device__ __forceinline__ void tc_fence_before() { tc::fence_before(); }
 __device__ __forceinline__ void tc_fence_after() { tc::fence_after(); }
 __device__ __forceinline__ void tc_commit(uint32_t mbar) { tc::commit(mbar); }
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t id,
-                                       uint32_t accum) {
+// D (+)= A . B with A in tensor memory (128 lanes x 8 columns per K = 16).
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t id,
+                                          uint32_t accum) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(id), "r"(accum)
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(id), "r"(accum)
+      : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane (32x32b shape: warp
+// w % 4 writes lanes 32 (w % 4) .. + 31), then the wait for the stores.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
 
@@ -328,7 +355,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           // the tokens, 1024 B apart along K; a last chunk of 64 columns is 8 KB
           const uint32_t bytes = (uint32_t)(min(kChunk, p.K - c * kChunk) / 64) * (kBBytes / 2);
           mbar_expect_tx(full0 + 8 * s, bytes);   // also this loader's arrival on full
-          bulk_load(stage0 + s * kStageBytes + kABytes, p.xb + (size_t)c * kBBytes, bytes, full0 + 8 * s, pol_keep);
+          bulk_load(stage0 + s * kStageBytes, p.xb + (size_t)c * kBBytes, bytes, full0 + 8 * s, pol_keep);
         }
         __syncwarp();
       }
@@ -350,12 +377,14 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     __syncwarp();
   } else if (warp >= kEpiWarps && warp < kMmaWarp) {
     // ----------------------------------------------------------- converters
-    const int pt = threadIdx.x - kEpiWarps * 32;
-    const int r = pt >> 1, h = pt & 1;   // A: row of the tile; 32-column blocks h and h + 2 of a chunk
-    // A: core matrix (8 rows x 16 B) of row block r/8 and column block kb at
-    // kb * 2048 + (r/8) * 128, so the 16 row blocks of one column block are
-    // contiguous (the tensor core reads them together without bank conflicts)
-    const uint32_t a_off = (uint32_t)((r >> 3) * 128 + (r & 7) * 16);
+    // thread = tile row r (TMEM lane r): warps 4-7 take the chunk's 32-column
+    // blocks 0 and 1, warps 8-11 blocks 2 and 3; warp w writes TMEM lanes
+    // 32 (w % 4) .. + 31, its 64 weights of the row as 32 columns (two 16-bit
+    // weights per column, K order) of the stage's A columns
+    const int wc = warp - kEpiWarps;                 // 0..7
+    const int half = wc >> 2;
+    const int r = 32 * (warp & 3) + lane;
+    const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(a_col0(NT) + 32 * half);
     uint32_t g = 0, gr = 0;   // operand chunks, raw stages
     bool ok = true;
     for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
@@ -368,7 +397,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           ok = false;
           break;
         }
-        if (pt == 0) stamp(g, 1);
+        if (wc == 0 && lane == 0) stamp(g, 1);
         const uint8_t* raw = raw_base + (size_t)rs * kRawBytes;
         const int ce = min(cs + kRawChunks, c1);
         for (int c = cs; c < ce; ++c, ++g) {
@@ -378,10 +407,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           float d[2];
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            const int bb = h + 2 * i;
+            const int bb = 2 * half + i;
             if (bb < nb) {
               // the codes tile arrives in the 128-byte swizzle: 16-byte group
-              // j of row r sits at group j ^ (r % 8), so the rows read by a
+              // j of row r sits at group j ^ (r % 8), so the 32 rows read by a
               // warp spread over the banks
               code[i] = *reinterpret_cast<const uint4*>(raw + r * 128 + (((cc * 4 + bb) ^ (r & 7)) << 4));
               d[i] = p.sc_tma ? __half2float(*reinterpret_cast<const __half*>(raw + kRawCodeBytes + r * 16 +
@@ -399,31 +428,44 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
             ok = false;
             break;
           }
-          if (pt == 0) stamp(g, 2);
-          uint8_t* A = stage_base + (size_t)s * kStageBytes;
+          tc_fence_after();   // the MMAs that read this A stage have completed
+          if (wc == 0 && lane == 0) stamp(g, 2);
+          if (2 * half < nb) {   // warp-uniform: a last chunk of 64 columns has no blocks 2, 3
+            uint32_t v[32];
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int bb = h + 2 * i;
-            if (bb < nb) {
+            for (int i = 0; i < 2; ++i) {
+              const int bb = 2 * half + i;
               const uint32_t w4[4] = {code[i].x, code[i].y, code[i].z, code[i].w};
-              if (F16) {
-                const __half2 dd = __float2half2_rn(d[i]);   // d is an fp16 value: exact
+              uint4 o[4];
+              if (bb < nb) {
+                if (F16) {
+                  const __half2 dd = __float2half2_rn(d[i]);   // d is an fp16 value: exact
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  *reinterpret_cast<uint4*>(A + a_off + (bb * 4 + j) * 2048) = dequant_word_f16(w4[j], dd);
+                  for (int j = 0; j < 4; ++j) o[j] = dequant_word_f16(w4[j], dd);
+                } else {
+                  const f2_t dd = f2_pack(d[i], d[i]);
+                  const f2_t bias = f2_pack(-264.f * d[i], -24.f * d[i]);
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) o[j] = dequant_word(w4[j], dd, bias);
+                }
               } else {
-                const f2_t dd = f2_pack(d[i], d[i]);
-                const f2_t bias = f2_pack(-264.f * d[i], -24.f * d[i]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  *reinterpret_cast<uint4*>(A + a_off + (bb * 4 + j) * 2048) = dequant_word(w4[j], dd, bias);
+                for (int j = 0; j < 4; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                v[16 * i + 4 * j] = o[j].x;
+                v[16 * i + 4 * j + 1] = o[j].y;
+                v[16 * i + 4 * j + 2] = o[j].z;
+                v[16 * i + 4 * j + 3] = o[j].w;
               }
             }
+            tmem_st32(a_lane + (uint32_t)(kACols * s), v);
           }
-          fence_proxy_async();   // this thread's stores, before the tensor core reads them
+          tc_fence_before();   // this warp's TMEM stores, before the MMA issuer reads them
           __syncwarp();
           if (lane == 0) mbar_arrive(full0 + 8 * s);
-          if (pt == 0) stamp(g, 3);
+          if (wc == 0 && lane == 0) stamp(g, 3);
         }
       }
     }
@@ -456,15 +498,15 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         tc_fence_after();
         if (elect_one()) {
           stamp(g, 4);
-          const uint32_t A = stage0 + s * kStageBytes, B = A + kABytes;
+          const uint32_t B = stage0 + s * kStageBytes;
+          const uint32_t A = tmem + (uint32_t)(a_col0(NT) + kACols * s);   // lane 0, the stage's A columns
           const int nks = min(kChunk, p.K - c * kChunk) / 16;
 #pragma unroll
           for (int ks = 0; ks < kChunk / 16; ++ks) {
             if (ks < nks) {
-              const uint64_t ad = smem_desc(A + ks * 4096, 2048, 128);
               // B: [16 column groups][NT tokens][8]: groups NT * 16 B apart
               const uint64_t bd = smem_desc(B + ks * NT * 32, NT * 16, 128);
-              tc_mma(d_tmem, ad, bd, kId, (c > c0 || ks > 0) ? 1u : 0u);
+              tc_mma_ta(d_tmem, A + 8 * ks, bd, kId, (c > c0 || ks > 0) ? 1u : 0u);
             }
           }
           tc_commit(empty0 + 8 * s);
