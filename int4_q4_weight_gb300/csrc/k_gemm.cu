@@ -13,7 +13,12 @@
 // CTAs when there are fewer tiles than SMs, the splits then add into Y).
 //
 // Warp roles (480 threads):
-//   warps 0-3   epilogue: tcgen05.ld of their TMEM lane quarter, store to Y
+//   warps 0-3   epilogue: tcgen05.ld of their TMEM lane quarter, store to Y;
+//               in the LM-head form (16 tokens, fp16 tiles) no Y: each thread
+//               keeps the best two (z, row) per token over its rows, the
+//               warps merge them at the end, and the CTA that finishes last
+//               merges every CTA's record (tanh(z/cap)*cap written only when
+//               the caller asks for the logits)
 //   warps 4-11  converters: raw codes + scales from the raw ring, nibble ->
 //               bf16 (exact d*(q-8) in fp32, then round to nearest even); a
 //               thread owns a tile row (TMEM lane) and 64 of the chunk's 128
@@ -39,10 +44,12 @@
 // freed and the kernel returns with the device error word set.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 
 #include "q4w_device.cuh"
 #include "q4w_internal.cuh"
 #include "q4w_tc.cuh"
+#include "q4w_top2.cuh"
 
 namespace q4w {
 
@@ -163,27 +170,68 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
   return r;
 }
 
-// Dequantised word: 8 columns (nibble j = column j) -> 4 bf16x2 in column order.
-__device__ __forceinline__ uint4 dequant_word(uint32_t w, f2_t dd, f2_t bias) {
-  const uint32_t s[4] = {w << 15, w << 7, w >> 1, w >> 9};
-  uint32_t o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    // (256 + n_even, 16 + n_odd) * (d, d) + (-264 d, -24 d) = (d (n_even - 8), d (n_odd - 8)), exact
-    const f2_t v = f2_fma(f2_pack(nib_even(s[i]), nib_odd(s[i])), dd, bias);
-    float lo, hi;
-    f2_unpack(v, lo, hi);
-    o[i] = bf16x2(lo, hi);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
+// Column order inside every group of 8 K columns, both operands: slot s of
+// the group holds column kSlotCol[s].  A 32-bit word of codes holds columns
+// 0..7 as nibbles; one masked LOP3 takes the nibbles of columns c and c + 4
+// (bits 4c and 4c + 16) into the two halves of a register, so the decoded
+// pairs come out as (0,4), (1,5), (2,6), (3,7).  The token operand is laid
+// out in the same order instead of permuting the weights back.
+//   slot:    0 1 2 3 4 5 6 7
+//   column:  0 4 1 5 2 6 3 7
+
+// bf16x2 arithmetic (round to nearest even; fma rounds once)
+__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
 }
 
-// The same 8 columns as fp16: fp16(d (n - 8)), rounded once.  A nibble lands
-// in the mantissa of fp16 1024 (bits 0-3 of each half) or 64 (bits 4-7):
-// (1024 + n) - 1032 and (64 + n) - 72 are the exact small integers n - 8, and
-// the half multiply by d rounds the exact product to nearest even.  Halves
-// come out as column pairs (0,4), (2,6), (1,5), (3,7) and are put back in
-// column order with byte permutes.
+// The scale d (an fp16 value: 11 significant bits) as two bf16 pieces:
+// hi = bf16(d), lo = d - hi (at most 3 significant bits, exact in bf16).
+struct ScalePieces {
+  uint32_t hi2, lo2;   // (hi, hi), (lo, lo)
+};
+__device__ __forceinline__ ScalePieces scale_pieces(float d) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(d);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(d - __bfloat162float(hi));   // exact
+  const uint32_t h = __bfloat16_as_ushort(hi), l = __bfloat16_as_ushort(lo);
+  return {h | (h << 16), l | (l << 16)};
+}
+
+// 8 columns as bf16(d (n - 8)), rounded once, in slot order.  Nibbles of
+// columns 0 and 4 (and, from w >> 8, 2 and 6) land in mantissa bits 0-3 of
+// bf16 128; those of columns 1 and 5 (3 and 7), shifted right by one, land
+// in mantissa bits 3-6 of bf16 16.  Subtracting 136 or 24 gives the exact
+// integers m = n - 8; m * lo is exact (at most 6 significant bits), and
+// fma(m, hi, m * lo) is m * (hi + lo) = d (n - 8) rounded once to bf16.
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, const ScalePieces& sp) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t v04 = lop3_and_or(w, 0x000F000Fu, 0x43004300u);        // 128 + n
+  const uint32_t v15 = lop3_and_or(w >> 1, 0x00780078u, 0x41804180u);   // 16 + n
+  const uint32_t v26 = lop3_and_or(w8, 0x000F000Fu, 0x43004300u);
+  const uint32_t v37 = lop3_and_or(w8 >> 1, 0x00780078u, 0x41804180u);
+  auto dq = [&](uint32_t v, uint32_t magic) {
+    const uint32_t m = bsub2(v, magic);
+    return bfma2(m, sp.hi2, bmul2(m, sp.lo2));
+  };
+  return make_uint4(dq(v04, 0x43084308u), dq(v15, 0x41C041C0u), dq(v26, 0x43084308u), dq(v37, 0x41C041C0u));
+}
+
+// The same 8 columns as fp16: fp16(d (n - 8)), rounded once, in slot order.
+// A nibble lands in the mantissa of fp16 1024 (bits 0-3 of each half) or 64
+// (bits 4-7): (1024 + n) - 1032 and (64 + n) - 72 are the exact small
+// integers n - 8, and the half multiply by d rounds the exact product to
+// nearest even.
 __device__ __forceinline__ uint4 dequant_word_f16(uint32_t w, __half2 dd) {
   const uint32_t w8 = w >> 8;
   const __half2 m_even = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
@@ -194,9 +242,7 @@ __device__ __forceinline__ uint4 dequant_word_f16(uint32_t w, __half2 dd) {
     const __half2 v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&pv), m), dd);
     return *reinterpret_cast<const uint32_t*>(&v);
   };
-  const uint32_t v04 = dq(p04, m_even), v26 = dq(p26, m_even), v15 = dq(p15, m_odd), v37 = dq(p37, m_odd);
-  return make_uint4(__byte_perm(v04, v15, 0x5410), __byte_perm(v26, v37, 0x5410), __byte_perm(v04, v15, 0x7632),
-                    __byte_perm(v26, v37, 0x7632));
+  return make_uint4(dq(p04, m_even), dq(p15, m_odd), dq(p26, m_even), dq(p37, m_odd));
 }
 
 __device__ __forceinline__ uint32_t h2_to_bf16x2(uint32_t h2) {
@@ -216,6 +262,16 @@ struct Params {
   int tiles, splits, cps, nchunks, items;
   long long wait_limit;
   unsigned long long* trace;   // optional: CTA 0 stamps [chunk < kTraceChunks][8], SM cycles
+  // LM-head form only (the kernel's HEAD instantiation, one CTA per tile):
+  // the epilogue keeps a running top two per token instead of writing Y, and
+  // the CTA that finishes last merges the per-CTA records
+  float cap;           // softcap: logits = cap * tanh(z / cap)
+  float* logits;       // optional softcapped logits [ntok][N]
+  Top2* partials;      // [gridDim.x][kMaxBatch]
+  unsigned* ticket;    // zero before the launch; zero again after it
+  int32_t* idx;
+  float* top1;
+  float* top2;
 };
 
 constexpr int kTraceChunks = 256;
@@ -230,8 +286,9 @@ __device__ __forceinline__ void item_range(const Params& p, int item, int& tile,
   c1 = min(c0 + p.cps, p.nchunks);
 }
 
-// NT: the MMA N (token tile), F16: fp16 tiles (else bf16).
-template <int NT, bool F16>
+// NT: the MMA N (token tile), F16: fp16 tiles (else bf16), HEAD: the LM-head
+// epilogue (softcap and top two per token, no Y).
+template <int NT, bool F16, bool HEAD>
 __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constant__ Params p) {
   constexpr int kStageBytes = stage_bytes(NT);
   constexpr int kBBytes = b_bytes(NT);
@@ -247,6 +304,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ long long t0_sh;
+  __shared__ Top2 head_st[kEpiWarps][HEAD ? NT : 1];   // LM head: per epilogue warp and token
+  __shared__ Top2 head_run[HEAD ? NT : 1][HEAD ? kEpiWarps * 32 : 1];   // LM head: per token and row
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned long long* const tr = (p.trace && blockIdx.x == 0) ? p.trace : nullptr;
@@ -443,10 +502,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
 #pragma unroll
                   for (int j = 0; j < 4; ++j) o[j] = dequant_word_f16(w4[j], dd);
                 } else {
-                  const f2_t dd = f2_pack(d[i], d[i]);
-                  const f2_t bias = f2_pack(-264.f * d[i], -24.f * d[i]);
+                  const ScalePieces sp = scale_pieces(d[i]);
 #pragma unroll
-                  for (int j = 0; j < 4; ++j) o[j] = dequant_word(w4[j], dd, bias);
+                  for (int j = 0; j < 4; ++j) o[j] = dequant_word(w4[j], sp);
                 }
               } else {
 #pragma unroll
@@ -532,6 +590,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   } else {
     // ------------------------------------------------------------ epilogue
     const int row = warp * 32 + lane;          // TMEM lane = tile row
+    // LM head: the best two (z, row) per token over the rows this thread
+    // reads, kept in shared memory (token-major: a warp's records of one token
+    // are 512 contiguous bytes)
+    if constexpr (HEAD) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) top2_init(head_run[t][row]);
+    }
     int it = 0;
     uint32_t ge = 0;   // this item's first chunk in the CTA's sequence (trace only)
     for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
@@ -541,19 +606,27 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       if (!mbar_wait(accfull0 + 8 * a, (it >> 1) & 1, p.wait_limit, abort_flag, 256)) break;
       if (threadIdx.x == 0) stamp(ge, 6);
       tc_fence_after();
-      float* yrow = p.Y + (size_t)tile * kTileM + row;
+      const int n = tile * kTileM + row;   // output row (vocabulary index for the head)
 #pragma unroll
       for (int cb = 0; cb < NT / 16; ++cb) {
         float v[16];
         tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(a * NT + cb * 16), v);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          if (cb * 16 + j >= p.ntok) break;
-          float* dst = yrow + (size_t)(cb * 16 + j) * p.N;
-          if (p.splits == 1)
-            *dst = v[j];
-          else
-            atomicAdd(dst, v[j]);
+          const int t = cb * 16 + j;
+          if (t >= p.ntok) break;
+          if constexpr (HEAD) {
+            Top2 b = head_run[t][row];
+            top2_insert(b, v[j], n);
+            head_run[t][row] = b;
+            if (p.logits) p.logits[(size_t)t * p.N + n] = p.cap * tanhf(v[j] / p.cap);
+          } else {
+            float* dst = p.Y + (size_t)t * p.N + n;
+            if (p.splits == 1)
+              *dst = v[j];
+            else
+              atomicAdd(dst, v[j]);
+          }
         }
       }
       tc_fence_before();
@@ -561,6 +634,15 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       if (lane == 0) mbar_arrive(accempty0 + 8 * a);
       if (threadIdx.x == 0) stamp(ge, 7);
       ge += c1 - c0;
+    }
+    if constexpr (HEAD) {
+      __syncwarp();
+      for (int t = 0; t < p.ntok; ++t) {
+        Top2 b = head_run[t][row];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) top2_shfl_xor_merge(b, o);
+        if (lane == 0) head_st[warp][t] = b;
+      }
     }
   }
 
@@ -570,9 +652,22 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
+  if constexpr (HEAD) {
+    // this CTA's record per token (its epilogue warps' four), then the merge
+    // over all CTAs' records in the CTA that finishes last
+    if (threadIdx.x < p.ntok) {
+      Top2 t;
+      top2_init(t);
+#pragma unroll
+      for (int w = 0; w < kEpiWarps; ++w) top2_merge(t, head_st[w][threadIdx.x]);
+      p.partials[(size_t)blockIdx.x * kMaxBatch + threadIdx.x] = t;
+    }
+    head_finish(p.partials, p.ticket, p.ntok, p.cap, p.idx, p.top1, p.top2);
+  }
 }
 
-// X fp16 [ntok][K] -> the token operand as [K/8 column groups][NT tokens][8]:
+// X fp16 [ntok][K] -> the token operand as [K/8 column groups][NT tokens][8
+// slots] (slot s holds column kSlotCol[s] of its group, the weights' order):
 // bf16 (nearest even) for bf16 tiles, the fp16 bits unchanged for fp16 tiles;
 // tokens ntok .. NT-1 are zero.  Each 128-column chunk is one contiguous
 // NT * 256-byte token tile in the core-matrix layout.  One thread per
@@ -586,7 +681,10 @@ __global__ void __launch_bounds__(256) x_layout_kernel(const __half* __restrict_
     uint4 o = make_uint4(0u, 0u, 0u, 0u);
     if (tok < ntok) {
       const uint4 v = *reinterpret_cast<const uint4*>(X + (size_t)tok * K + grp * 8);
-      o = F16 ? v : make_uint4(h2_to_bf16x2(v.x), h2_to_bf16x2(v.y), h2_to_bf16x2(v.z), h2_to_bf16x2(v.w));
+      // slot order 0 4 1 5 2 6 3 7 (the weights' decoded pairs)
+      const uint4 q = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                                 __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
+      o = F16 ? q : make_uint4(h2_to_bf16x2(q.x), h2_to_bf16x2(q.y), h2_to_bf16x2(q.z), h2_to_bf16x2(q.w));
     }
     *reinterpret_cast<uint4*>(xb + (size_t)i * 16) = o;
   }
@@ -629,14 +727,27 @@ int encode_tensor_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type
 size_t gemm_ws_bytes(int K) { return ((size_t)gemm::kTok * K * 2 + 255) & ~(size_t)255; }
 size_t mma16_ws_bytes(int K) { return ((size_t)16 * K * 2 + 255) & ~(size_t)255; }
 
-// Y[t][n] (t < ntok) = the dequantised weights times X through gemm_kernel<NT, F16>.
+// Y[t][n] (t < ntok) = the dequantised weights times X through gemm_kernel<NT, F16, HEAD>.
 // allow_split: K may be split across CTAs (the splits add into Y with fp32
 // atomics, so the summation order is not fixed); else one CTA per tile.
-template <int NT, bool F16>
+// HEAD: Y is not written; head->* receive the softcapped top two per token
+// (and the softcapped logits when head->logits is set).
+template <int NT, bool F16, bool HEAD>
 static int launch_mma(const uint8_t* codes, const __half* scales, const __half* X, int ntok, float* Y, int N,
-                      int K, void* ws, bool allow_split, const DeviceInfo& dev, cudaStream_t s) {
+                      int K, void* ws, bool allow_split, const HeadOutputs* head, const DeviceInfo& dev,
+                      cudaStream_t s) {
+  if (HEAD && (head == nullptr || allow_split)) return fail(Q4_ERR_SHAPE, "head GEMM: outputs missing or split K");
   gemm::Params p;
   memset(&p, 0, sizeof(p));
+  if (HEAD) {
+    p.cap = head->cap;
+    p.logits = head->logits;
+    p.partials = head->partials;
+    p.ticket = head->ticket;
+    p.idx = head->idx;
+    p.top1 = head->top1;
+    p.top2 = head->top2;
+  }
   int st = encode_tensor_2d(&p.tm_codes, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N,
                             gemm::kChunk * gemm::kRawChunks / 2, gemm::kTileM, CU_TENSOR_MAP_SWIZZLE_128B, "codes");
   if (st != Q4_OK) return st;
@@ -674,7 +785,7 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
   }
   static PerDevice attr_set;   // one per instantiation and device
   if (!attr_set.get(dev.ordinal)) {
-    e = cudaFuncSetAttribute(gemm::gemm_kernel<NT, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gemm::gemm_kernel<NT, F16, HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)gemm::smem_bytes(NT));
     if (e != cudaSuccess) return cuda_fail(e, "gemm smem attribute");
     attr_set.set(dev.ordinal);
@@ -695,20 +806,20 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<NT, F16>, p);
+  e = cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<NT, F16, HEAD>, p);
   return e == cudaSuccess ? Q4_OK : cuda_fail(e, "gemm launch");
 }
 
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s) {
   (void)M;
-  return launch_mma<gemm::kTok, false>(codes, scales, X, gemm::kTok, Y, N, K, ws, true, dev, s);
+  return launch_mma<gemm::kTok, false, false>(codes, scales, X, gemm::kTok, Y, N, K, ws, true, nullptr, dev, s);
 }
 
-int launch_mma16_f16(const uint8_t* codes, const __half* scales, const __half* X, int ntok, float* Y, int N, int K,
-                     void* ws, const DeviceInfo& dev, cudaStream_t s) {
+int launch_head_mma(const uint8_t* codes, const __half* scales, const __half* X, int ntok, int N, int K, void* ws,
+                    const HeadOutputs& head, const DeviceInfo& dev, cudaStream_t s) {
   if (ntok < 1 || ntok > 16) return fail(Q4_ERR_SHAPE, "token count %d must be in [1, 16]", ntok);
-  return launch_mma<16, true>(codes, scales, X, ntok, Y, N, K, ws, false, dev, s);
+  return launch_mma<16, true, true>(codes, scales, X, ntok, nullptr, N, K, ws, false, &head, dev, s);
 }
 
 }  // namespace q4w

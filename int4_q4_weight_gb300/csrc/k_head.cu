@@ -121,7 +121,8 @@ static int lpr_for(int nb) {
 static int head_grid(const DeviceInfo& dev) { return 2 * dev.sms; }   // >= the streaming head's grid
 
 // Batch rows 2..8 go through the tensor-core kernel (fp16 weight tiles, one
-// CTA per 128-row tile) when the vocabulary fills every SM with tiles.
+// CTA per 128-row tile, the selection in its epilogue) when the vocabulary
+// fills every SM with tiles.
 static bool head_tc_eligible(int b, int V, int K, const DeviceInfo& dev) {
   return b >= 2 && V % 128 == 0 && V >= 128 * dev.sms && K % 64 == 0;
 }
@@ -130,62 +131,8 @@ static size_t up256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 size_t lmhead_ws_bytes(int V, int K, int b, const DeviceInfo& dev, bool tensor_cores) {
   size_t n = kTicketBytes + up256((size_t)head_grid(dev) * kMaxBatch * sizeof(Top2));
-  if (tensor_cores && head_tc_eligible(b, V, K, dev)) n += mma16_ws_bytes(K) + up256((size_t)b * V * sizeof(float));
+  if (tensor_cores && head_tc_eligible(b, V, K, dev)) n += mma16_ws_bytes(K);
   return n;
-}
-
-// Softcap and two-level top-two selection over finished sums z [B][V]
-// (V % 4 == 0): each CTA takes a contiguous slice of rows for every batch row,
-// four per thread per pass as one 16-byte load (the loads of a pass are
-// independent, so they are in flight together); the last CTA to finish
-// merges the per-CTA partials (head_finish).
-__global__ void __launch_bounds__(256) head_select_kernel(const float* __restrict__ z, int B, int V, float cap,
-                                                          float* __restrict__ logits, Top2* partials,
-                                                          unsigned* ticket, int32_t* idx, float* top1, float* top2) {
-  __shared__ Top2 st[8][kMaxBatch];
-  const int V4 = V >> 2;
-  const int per = (V4 + gridDim.x - 1) / gridDim.x;
-  const int q0 = blockIdx.x * per, q1 = min(V4, q0 + per);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int b = 0; b < B; ++b) {
-    Top2 t;
-    top2_init(t);
-    const float4* zr = reinterpret_cast<const float4*>(z + (size_t)b * V);
-    float4* lr = logits ? reinterpret_cast<float4*>(logits + (size_t)b * V) : nullptr;
-    for (int q = q0 + threadIdx.x; q < q1; q += 4 * blockDim.x) {
-      float4 x[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int qk = q + k * blockDim.x;
-        x[k] = qk < q1 ? __ldcg(zr + qk) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int qk = q + k * blockDim.x;
-        if (qk < q1) {
-          const int v = 4 * qk;
-          top2_insert(t, x[k].x, v);
-          top2_insert(t, x[k].y, v + 1);
-          top2_insert(t, x[k].z, v + 2);
-          top2_insert(t, x[k].w, v + 3);
-          if (lr)
-            lr[qk] = make_float4(cap * tanhf(x[k].x / cap), cap * tanhf(x[k].y / cap), cap * tanhf(x[k].z / cap),
-                                 cap * tanhf(x[k].w / cap));
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) top2_shfl_xor_merge(t, o);
-    if (lane == 0) st[warp][b] = t;
-  }
-  __syncthreads();
-  if (threadIdx.x < B) {
-    Top2 t;
-    top2_init(t);
-    for (int w = 0; w < 8; ++w) top2_merge(t, st[w][threadIdx.x]);
-    partials[(size_t)blockIdx.x * kMaxBatch + threadIdx.x] = t;
-  }
-  head_finish(partials, ticket, B, cap, idx, top1, top2);
 }
 
 // b = 1 on the CUDA-core kernel (K not eligible for the streaming engine).
@@ -224,16 +171,10 @@ int launch_lmhead(const uint8_t* codes, const __half* scales, const __half* h, i
   cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), s);
   if (e != cudaSuccess) return cuda_fail(e, "lmhead ticket reset");
   if (tensor_cores && head_tc_eligible(b, V, K, dev)) {
-    // z = W h on the tensor cores into the workspace, then softcap + top-two
-    char* base = reinterpret_cast<char*>(ws) + kTicketBytes + up256((size_t)head_grid(dev) * kMaxBatch * sizeof(Top2));
-    void* xws = base;
-    float* z = reinterpret_cast<float*>(base + mma16_ws_bytes(K));
-    const int st = launch_mma16_f16(codes, scales, h, b, z, V, K, xws, dev, s);
-    if (st != Q4_OK) return st;
-    int grid = head_grid(dev);
-    head_select_kernel<<<grid, 256, 0, s>>>(z, b, V, cap, logits, partials, ticket, idx, top1, top2);
-    e = cudaGetLastError();
-    return e == cudaSuccess ? Q4_OK : cuda_fail(e, "lmhead select launch");
+    // z = W h on the tensor cores; its epilogue softcaps and selects
+    void* xws = reinterpret_cast<char*>(ws) + kTicketBytes + up256((size_t)head_grid(dev) * kMaxBatch * sizeof(Top2));
+    const HeadOutputs out = {cap, logits, partials, ticket, idx, top1, top2};
+    return launch_head_mma(codes, scales, h, b, V, K, xws, out, dev, s);
   }
   if (b > 1) {
     int grid = head_grid(dev);

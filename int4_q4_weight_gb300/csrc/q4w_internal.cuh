@@ -122,12 +122,26 @@ int encode_tensor_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type
 size_t gemm_ws_bytes(int K);   // the bf16 copy of X [64][K]
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s);
-// Y[t][n] for t < ntok <= 16 through the tensor-core kernel with fp16 tiles
-// (weights rounded once to fp16, tokens exact), one CTA per 128-row tile (no
-// split of K, so every row is summed in one fixed order).  N % 128 == 0,
-// K % 64 == 0; ws: mma16_ws_bytes(K) bytes for the token operand.
+// The LM head of ntok <= 16 vectors on the tensor cores: z[t][n] through the
+// GEMM kernel with fp16 tiles (weights rounded once to fp16, tokens exact),
+// one CTA per 128-row tile (no split of K, so every row is summed in one fixed
+// order); z never reaches memory: the epilogue softcaps it into head.logits
+// (when set) and keeps a running top two per token, and the CTA that finishes
+// last merges the per-CTA records into idx/top1/top2.  N % 128 == 0,
+// K % 64 == 0; ws: mma16_ws_bytes(K) bytes for the token operand;
+// head.partials: one record per SM and kMaxBatch tokens; head.ticket zero.
+struct Top2;
+struct HeadOutputs {
+  float cap;
+  float* logits;
+  Top2* partials;
+  unsigned* ticket;
+  int32_t* idx;
+  float* top1;
+  float* top2;
+};
 size_t mma16_ws_bytes(int K);
-int launch_mma16_f16(const uint8_t* codes, const __half* scales, const __half* X, int ntok, float* Y, int N, int K,
-                     void* ws, const DeviceInfo& dev, cudaStream_t s);
+int launch_head_mma(const uint8_t* codes, const __half* scales, const __half* X, int ntok, int N, int K, void* ws,
+                    const HeadOutputs& head, const DeviceInfo& dev, cudaStream_t s);
 
 }  // namespace q4w

@@ -77,8 +77,9 @@ def test_head_full_vocab(cuda_lib, b):
 @pytest.mark.parametrize("b", [2, 3, 8])
 def test_head_batch_tensor_core_path(cuda_lib, b):
     # V a multiple of 128 with at least one 128-row tile per SM: batch rows go
-    # through the tensor-core kernel (fp16 weight tiles) and the select pass,
-    # including its softcapped logits output and a repeat with the same bits
+    # through the tensor-core kernel (fp16 weight tiles) whose epilogue
+    # softcaps and selects, including its softcapped logits output and a
+    # repeat with the same bits
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     V, K = 128 * (sms + 9), 1536
     W, h = synth.head_inputs(seed=83 + b, device="cuda", batch=b, V=V, K=K)
@@ -90,6 +91,32 @@ def test_head_batch_tensor_core_path(cuda_lib, b):
     c = cuda_lib.lmhead_softcap_argmax(codes, scales, h)[:3]
     torch.cuda.synchronize()
     assert all(torch.equal(x, y) for x, y in zip(a, c))
+
+
+def test_head_tensor_core_ties_lowest_index(cuda_lib):
+    # each winner copied to rows in other 128-row tiles (other CTAs) below and
+    # above it: the merged pick is the lowest tied row, the runner-up the tie
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    V, K, b = 128 * (sms + 9), 1536, 4
+    W, h = synth.head_inputs(seed=90, device="cuda", batch=b, V=V, K=K)
+    codes, scales = cuda_lib.q4_quantize(W)
+    torch.cuda.synchronize()
+    oc, os_ = codes.cpu().numpy(), scales.cpu().numpy().view(np.uint16)
+    ri = O.lmhead_softcap_argmax(oc, os_, h.cpu().numpy())[0]
+    for i in range(b):
+        w = int(ri[i])
+        for dst in ((w - 128 * (37 + i) - 5) % V, (w + 128 * (5 + i) + 3) % V):
+            codes[dst] = codes[w]
+            scales[dst] = scales[w]
+    oc, os_ = codes.cpu().numpy(), scales.cpu().numpy().view(np.uint16)
+    gi, _ = _head_check(cuda_lib, codes, scales, h, oc, os_, want_logits=False)
+    ri2, r1, r2 = O.lmhead_softcap_argmax(oc, os_, h.cpu().numpy())[:3]
+    assert np.array_equal(gi, ri2)
+    _, t1, t2, _ = cuda_lib.lmhead_softcap_argmax(codes, scales, h)
+    torch.cuda.synchronize()
+    tie = r1 == r2            # the copied winner is the runner-up
+    assert tie.any()
+    assert np.array_equal(t1.cpu().numpy()[tie], t2.cpu().numpy()[tie])
 
 
 def test_head_repeatable(cuda_lib):
