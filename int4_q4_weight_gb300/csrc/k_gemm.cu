@@ -12,23 +12,26 @@
 // items (a 128-row tile and a range of 64-column K chunks; K is split across
 // CTAs when there are fewer tiles than SMs, the splits then add into Y).
 //
-// Warp roles (480 threads):
+// Warp roles (736 threads):
 //   warps 0-3   epilogue: tcgen05.ld of their TMEM lane quarter, store to Y;
 //               in the LM-head form (16 tokens, fp16 tiles) no Y: each thread
 //               keeps the best two (z, row) per token over its rows, the
 //               warps merge them at the end, and the CTA that finishes last
 //               merges every CTA's record (tanh(z/cap)*cap written only when
 //               the caller asks for the logits)
-//   warps 4-11  converters: raw codes + scales from the raw ring, nibble ->
-//               bf16 (exact d*(q-8) in fp32, then round to nearest even); a
-//               thread owns a tile row (TMEM lane) and 64 of the chunk's 128
-//               columns, written with one tcgen05.st of 32 columns (warps
-//               w and w + 4 share TMEM lane quarter w % 4)
-//   warp 12     TMEM allocator and MMA issuer: the warp walks the pipeline
+//   warps 4-19  converters: raw codes + scales from the raw ring, nibble ->
+//               bf16 d*(q-8) rounded once (or fp16 for the head form); a
+//               thread owns a tile row (TMEM lane) and one 32-column block
+//               of the chunk, written with one tcgen05.st of 16 columns
+//               (warps w, w + 4, w + 8, w + 12 share TMEM lane quarter w % 4,
+//               the only lanes their scheduler may access); 16 warps rather
+//               than 8 so that each scheduler has four to switch between
+//               while one waits on its loads, stores or barriers
+//   warp 20     TMEM allocator and MMA issuer: the warp walks the pipeline
 //               and waits together, one elected lane issues the 8 MMAs of a
 //               128-column stage (A from tensor memory) and the commits
-//   warp 13     raw-ring TMA loads (one elected lane issues)
-//   warp 14     token tile (B) of each operand stage: one bulk copy from the
+//   warp 21     raw-ring TMA loads (one elected lane issues)
+//   warp 22     token tile (B) of each operand stage: one bulk copy from the
 //               bf16 copy of X, completing on the stage's full barrier
 // X is rounded to bf16 once per call by a small kernel ahead of the GEMM (in
 // the caller's workspace) instead of once per tile and chunk.  The raw ring
@@ -37,7 +40,7 @@
 // shared memory), 128 K columns each) feed the tensor cores.  full counts the
 // converter warps and the B loader (with its bytes), so the MMA issuer waits
 // on one barrier per stage.
-// Two TMEM accumulators (2 x 64 columns) let the epilogue of one item
+// Two TMEM accumulators (2 x N columns) let the epilogue of one item
 // overlap the MMAs of the next.  Every mbarrier wait is bounded in
 // clock cycles; on expiry the CTA raises an abort flag, every role leaves its
 // loop, the MMA issuer drains its own tcgen05 work (bounded again), TMEM is
@@ -92,11 +95,12 @@ __host__ __device__ constexpr int tmem_cols(int n) {
 constexpr int kRawCodeBytes = kTileM * kChunk * kRawChunks / 2;   // 16 KB: [128 rows][128 B]
 constexpr int kRawScaleBytes = kTileM * 16;                         // 2 KB: [128 rows][8 fp16]
 constexpr int kRawBytes = kRawCodeBytes + kRawScaleBytes;
-constexpr int kEpiWarps = 4, kProdWarps = 8;
-constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 12
-constexpr int kTmaWarp = kMmaWarp + 1;             // 13
-constexpr int kBWarp = kTmaWarp + 1;               // 14
-constexpr int kThreadsG = (kBWarp + 1) * 32;       // 480
+constexpr int kEpiWarps = 4, kProdWarps = 16;
+constexpr int kBPW = 16 / kProdWarps;   // 32-column blocks of a chunk per converter warp
+constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 20
+constexpr int kTmaWarp = kMmaWarp + 1;             // 21
+constexpr int kBWarp = kTmaWarp + 1;               // 22
+constexpr int kThreadsG = (kBWarp + 1) * 32;       // 736
 constexpr int kBars = 2 * kStages + 2 * kRawStages + 5;
 __host__ __device__ constexpr size_t smem_bytes(int n) {
   return 1024 + (size_t)kStages * stage_bytes(n) + (size_t)kRawStages * kRawBytes + kBars * 8;
@@ -131,11 +135,12 @@ using tc::smem_u32;
 using tc::tmem_ld16;
 
 // Bounded wait.  Returns false when the wait ran out or the CTA is aborting.
-// sleep_ns > 0: roles off the critical path back off between polls, so that
-// their spinning does not take issue slots from the converter warps.
+// Waiting warps are suspended in the barrier wait (no polling), so the roles
+// that wait most (MMA issuer, loaders, epilogue) take no issue slots from the
+// converter warps on their schedulers.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, long long limit,
-                                          volatile int* abort_flag, unsigned sleep_ns = 0) {
-  return tc::mbar_wait(a, parity, limit, abort_flag, &g_device_error, sleep_ns);
+                                          volatile int* abort_flag) {
+  return tc::mbar_wait(a, parity, limit, abort_flag, &g_device_error);
 }
 __device__ __forceinline__ void tc_fence_before() { tc::fence_before(); }
 __device__ __forceinline__ void tc_fence_after() { tc::fence_after(); }
@@ -150,8 +155,18 @@ __device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
-// 32 consecutive 32-bit TMEM columns of this thread's lane (32x32b shape: warp
-// w % 4 writes lanes 32 (w % 4) .. + 31), then the wait for the stores.
+// 16 or 32 consecutive 32-bit TMEM columns of this thread's lane (32x32b
+// shape: warp w % 4 writes lanes 32 (w % 4) .. + 31), then the wait for the
+// stores.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -162,6 +177,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 16)
+    tmem_st16(taddr, v);
+  else
+    tmem_st32(taddr, v);
 }
 
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
@@ -360,7 +384,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         item_range(p, item, tile, c0, c1);
         for (int cs = c0; cs < c1; cs += kRawChunks, ++g) {
           const uint32_t s = g % kRawStages, round = g / kRawStages;
-          const bool free_ = mbar_wait(rawempty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, 64);
+          const bool free_ = mbar_wait(rawempty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag);
           if (!__all_sync(0xffffffffu, free_)) {
             ok = false;
             break;
@@ -404,7 +428,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       item_range(p, item, tile, c0, c1);
       for (int c = c0; c < c1; ++c, ++g) {
         const uint32_t s = g % kStages, round = g / kStages;
-        const bool free_ = mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, 64);
+        const bool free_ = mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag);
         if (!__all_sync(0xffffffffu, free_)) {
           ok = false;
           break;
@@ -436,14 +460,16 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     __syncwarp();
   } else if (warp >= kEpiWarps && warp < kMmaWarp) {
     // ----------------------------------------------------------- converters
-    // thread = tile row r (TMEM lane r): warps 4-7 take the chunk's 32-column
-    // blocks 0 and 1, warps 8-11 blocks 2 and 3; warp w writes TMEM lanes
-    // 32 (w % 4) .. + 31, its 64 weights of the row as 32 columns (two 16-bit
-    // weights per column, K order) of the stage's A columns
-    const int wc = warp - kEpiWarps;                 // 0..7
-    const int half = wc >> 2;
+    // thread = tile row r (TMEM lane r): warp w writes TMEM lanes
+    // 32 (w % 4) .. + 31 (the lane quarter its scheduler may access); the
+    // kProdWarps / 4 warps of a quarter split the chunk's four 32-column
+    // blocks, kBPW each, written as 16 kBPW columns (two 16-bit weights per
+    // column, slot order) of the stage's A columns
+    const int wc = warp - kEpiWarps;                 // 0 .. kProdWarps - 1
+    const int grp = wc >> 2;                         // block group of this warp
     const int r = 32 * (warp & 3) + lane;
-    const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(a_col0(NT) + 32 * half);
+    const uint32_t a_lane =
+        tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(a_col0(NT) + 16 * kBPW * grp);
     uint32_t g = 0, gr = 0;   // operand chunks, raw stages
     bool ok = true;
     for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
@@ -462,11 +488,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         for (int c = cs; c < ce; ++c, ++g) {
           const int cc = c - cs;
           const int nb = min(kChunk, p.K - c * kChunk) / 32;   // 32-column blocks in this chunk: 4, or 2 at the end
-          uint4 code[2];
-          float d[2];
+          uint4 code[kBPW];
+          float d[kBPW];
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int bb = 2 * half + i;
+          for (int i = 0; i < kBPW; ++i) {
+            const int bb = kBPW * grp + i;
             if (bb < nb) {
               // the codes tile arrives in the 128-byte swizzle: 16-byte group
               // j of row r sits at group j ^ (r % 8), so the 32 rows read by a
@@ -489,11 +515,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           }
           tc_fence_after();   // the MMAs that read this A stage have completed
           if (wc == 0 && lane == 0) stamp(g, 2);
-          if (2 * half < nb) {   // warp-uniform: a last chunk of 64 columns has no blocks 2, 3
-            uint32_t v[32];
+          if (kBPW * grp < nb) {   // warp-uniform: a last chunk of 64 columns has no blocks 2, 3
+            uint32_t v[16 * kBPW];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int bb = 2 * half + i;
+            for (int i = 0; i < kBPW; ++i) {
+              const int bb = kBPW * grp + i;
               const uint32_t w4[4] = {code[i].x, code[i].y, code[i].z, code[i].w};
               uint4 o[4];
               if (bb < nb) {
@@ -518,7 +544,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
                 v[16 * i + 4 * j + 3] = o[j].w;
               }
             }
-            tmem_st32(a_lane + (uint32_t)(kACols * s), v);
+            tmem_st_cols<16 * kBPW>(a_lane + (uint32_t)(kACols * s), v);
           }
           tc_fence_before();   // this warp's TMEM stores, before the MMA issuer reads them
           __syncwarp();
@@ -603,7 +629,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
       int tile, c0, c1;
       item_range(p, item, tile, c0, c1);
       const int a = it & 1;
-      if (!mbar_wait(accfull0 + 8 * a, (it >> 1) & 1, p.wait_limit, abort_flag, 256)) break;
+      if (!mbar_wait(accfull0 + 8 * a, (it >> 1) & 1, p.wait_limit, abort_flag)) break;
       if (threadIdx.x == 0) stamp(ge, 6);
       tc_fence_after();
       const int n = tile * kTileM + row;   // output row (vocabulary index for the head)

@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     const int r64 = row & 63;
     const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
     const bool has = ns > 0;                   // without K work the partial sums are zero
-    if (ok && has) ok = tc::mbar_wait(accfull, 0, p.wait_limit, abort_flag, p.dev_err, 128);
+    if (ok && has) ok = tc::mbar_wait(accfull, 0, p.wait_limit, abort_flag, p.dev_err);
     ok = __all_sync(0xffffffffu, ok);          // the TMEM loads below are warp-wide
     tc::fence_after();
     if (ct == 0) stamp(kTraceRows - 1, 5);

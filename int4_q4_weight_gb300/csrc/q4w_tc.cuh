@@ -54,13 +54,32 @@ __device__ __forceinline__ bool mbar_probe(uint32_t a, uint32_t parity) {   // n
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps (issuing nothing)
+// until the phase completes or about `ns` nanoseconds have passed.
+__device__ __forceinline__ bool mbar_test_for(uint32_t a, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Suspend hint of the bounded waits: long enough that a waiting warp costs
+// no issue slots (a plain try_wait returns after a short time and a spinning
+// warp takes issue slots from the warps on its scheduler), short enough that
+// the abort flag and the budget are still seen within a fraction of a
+// millisecond.
+constexpr uint32_t kSuspendNs = 200000;
+
 // Bounded wait on phase `parity` of an mbarrier.  False when the budget ran
 // out (the CTA's abort flag and bit 0 of *err are then set) or when another
 // role of the CTA is aborting.  The first check does not suspend and the
 // budget is checked before every suspending retry, so a zero budget gives up
 // at once on a phase that is not complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, long long limit, volatile int* abort_flag,
-                                          unsigned* err, unsigned sleep_ns = 0) {
+                                          unsigned* err) {
   if (mbar_probe(a, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
@@ -70,8 +89,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, long long
       atomicOr(err, 1u);
       return false;
     }
-    if (mbar_test(a, parity)) return true;
-    if (sleep_ns) __nanosleep(sleep_ns);
+    if (mbar_test_for(a, parity, kSuspendNs)) return true;
   }
 }
 
