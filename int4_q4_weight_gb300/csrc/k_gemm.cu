@@ -74,7 +74,7 @@ unsigned* device_error_word() {
 
 namespace gemm {
 
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kRawStages = 8;
 constexpr int kRawChunks = 2;          // operand chunks per raw stage (256 K columns)
 constexpr int kTileM = 128;            // weight rows per tile (MMA M)
@@ -96,7 +96,10 @@ constexpr int kRawCodeBytes = kTileM * kChunk * kRawChunks / 2;   // 16 KB: [128
 constexpr int kRawScaleBytes = kTileM * 16;                         // 2 KB: [128 rows][8 fp16]
 constexpr int kRawBytes = kRawCodeBytes + kRawScaleBytes;
 constexpr int kEpiWarps = 4, kProdWarps = 16;
-constexpr int kBPW = 16 / kProdWarps;   // 32-column blocks of a chunk per converter warp
+// The converter warps form kRawChunks groups; group k converts chunk k of
+// every raw stage, so consecutive chunks are converted concurrently.
+constexpr int kGroupWarps = kProdWarps / kRawChunks;   // 8: two per lane quarter
+constexpr int kBPW = 16 / kGroupWarps;                 // 32-column blocks of a chunk per converter warp
 constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 20
 constexpr int kTmaWarp = kMmaWarp + 1;             // 21
 constexpr int kBWarp = kTmaWarp + 1;               // 22
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     abort_sh = 0;
     t0_sh = tc::clock_ordered();
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, kProdWarps + 1);   // one arrival per converter warp + the B loader's, with its bytes
+      mbar_init(full0 + 8 * s, kGroupWarps + 1);   // one arrival per warp of the chunk's group + the B loader's
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -460,17 +463,19 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     __syncwarp();
   } else if (warp >= kEpiWarps && warp < kMmaWarp) {
     // ----------------------------------------------------------- converters
+    // Group k (warps 4 + 8k .. 11 + 8k) converts chunk k of every raw stage.
     // thread = tile row r (TMEM lane r): warp w writes TMEM lanes
-    // 32 (w % 4) .. + 31 (the lane quarter its scheduler may access); the
-    // kProdWarps / 4 warps of a quarter split the chunk's four 32-column
-    // blocks, kBPW each, written as 16 kBPW columns (two 16-bit weights per
-    // column, slot order) of the stage's A columns
+    // 32 (w % 4) .. + 31 (the lane quarter its scheduler may access); the two
+    // warps of a quarter in a group split the chunk's four 32-column blocks,
+    // kBPW each, written as 16 kBPW columns (two 16-bit weights per column,
+    // slot order) of the stage's A columns
     const int wc = warp - kEpiWarps;                 // 0 .. kProdWarps - 1
-    const int grp = wc >> 2;                         // block group of this warp
+    const int cg = wc / kGroupWarps;                 // chunk group
+    const int grp = (wc % kGroupWarps) >> 2;         // block group of this warp
     const int r = 32 * (warp & 3) + lane;
     const uint32_t a_lane =
         tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(a_col0(NT) + 16 * kBPW * grp);
-    uint32_t g = 0, gr = 0;   // operand chunks, raw stages
+    uint32_t g0 = 0, gr = 0;   // first operand chunk of the raw stage, raw stages
     bool ok = true;
     for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
       int tile, c0, c1;
@@ -482,75 +487,74 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           ok = false;
           break;
         }
-        if (wc == 0 && lane == 0) stamp(g, 1);
         const uint8_t* raw = raw_base + (size_t)rs * kRawBytes;
-        const int ce = min(cs + kRawChunks, c1);
-        for (int c = cs; c < ce; ++c, ++g) {
-          const int cc = c - cs;
-          const int nb = min(kChunk, p.K - c * kChunk) / 32;   // 32-column blocks in this chunk: 4, or 2 at the end
-          uint4 code[kBPW];
-          float d[kBPW];
+        const int c = cs + cg;                 // this group's chunk
+        const uint32_t g = g0 + (uint32_t)cg;
+        g0 += (uint32_t)(min(cs + kRawChunks, c1) - cs);
+        const bool mine = c < c1;              // an item's last raw stage may hold one chunk
+        if (wc == 0 && lane == 0) stamp(g, 1);
+        const int nb = mine ? min(kChunk, p.K - c * kChunk) / 32 : 0;   // 32-column blocks: 4, or 2 at the end
+        uint4 code[kBPW];
+        float d[kBPW];
+#pragma unroll
+        for (int i = 0; i < kBPW; ++i) {
+          const int bb = kBPW * grp + i;
+          if (bb < nb) {
+            // the codes tile arrives in the 128-byte swizzle: 16-byte group
+            // j of row r sits at group j ^ (r % 8), so the 32 rows read by a
+            // warp spread over the banks
+            code[i] = *reinterpret_cast<const uint4*>(raw + r * 128 + (((cg * 4 + bb) ^ (r & 7)) << 4));
+            d[i] = p.sc_tma ? __half2float(*reinterpret_cast<const __half*>(raw + kRawCodeBytes + r * 16 +
+                                                                              (cg * 4 + bb) * 2))
+                            : ld_scale(p.scales + ((size_t)tile * kTileM + r) * (p.K >> 5) + c * 4 + bb);
+          }
+        }
+        __syncwarp();   // this warp has read its part of the raw stage
+        if (lane == 0) mbar_arrive(rawempty0 + 8 * rs);
+        if (!mine) continue;
+        const uint32_t s = g % kStages, round = g / kStages;
+        const bool free_ = mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag);
+        if (!__all_sync(0xffffffffu, free_)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();   // the MMAs that read this A stage have completed
+        if (wc == 0 && lane == 0) stamp(g, 2);
+        if (kBPW * grp < nb) {   // warp-uniform: a last chunk of 64 columns has no blocks 2, 3
+          uint32_t v[16 * kBPW];
 #pragma unroll
           for (int i = 0; i < kBPW; ++i) {
             const int bb = kBPW * grp + i;
+            const uint32_t w4[4] = {code[i].x, code[i].y, code[i].z, code[i].w};
+            uint4 o[4];
             if (bb < nb) {
-              // the codes tile arrives in the 128-byte swizzle: 16-byte group
-              // j of row r sits at group j ^ (r % 8), so the 32 rows read by a
-              // warp spread over the banks
-              code[i] = *reinterpret_cast<const uint4*>(raw + r * 128 + (((cc * 4 + bb) ^ (r & 7)) << 4));
-              d[i] = p.sc_tma ? __half2float(*reinterpret_cast<const __half*>(raw + kRawCodeBytes + r * 16 +
-                                                                                (cc * 4 + bb) * 2))
-                              : ld_scale(p.scales + ((size_t)tile * kTileM + r) * (p.K >> 5) + c * 4 + bb);
-            }
-          }
-          if (c == ce - 1) {   // the raw stage has been read
-            __syncwarp();
-            if (lane == 0) mbar_arrive(rawempty0 + 8 * rs);
-          }
-          const uint32_t s = g % kStages, round = g / kStages;
-          const bool free_ = mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag);
-          if (!__all_sync(0xffffffffu, free_)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();   // the MMAs that read this A stage have completed
-          if (wc == 0 && lane == 0) stamp(g, 2);
-          if (kBPW * grp < nb) {   // warp-uniform: a last chunk of 64 columns has no blocks 2, 3
-            uint32_t v[16 * kBPW];
+              if (F16) {
+                const __half2 dd = __float2half2_rn(d[i]);   // d is an fp16 value: exact
 #pragma unroll
-            for (int i = 0; i < kBPW; ++i) {
-              const int bb = kBPW * grp + i;
-              const uint32_t w4[4] = {code[i].x, code[i].y, code[i].z, code[i].w};
-              uint4 o[4];
-              if (bb < nb) {
-                if (F16) {
-                  const __half2 dd = __float2half2_rn(d[i]);   // d is an fp16 value: exact
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) o[j] = dequant_word_f16(w4[j], dd);
-                } else {
-                  const ScalePieces sp = scale_pieces(d[i]);
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) o[j] = dequant_word(w4[j], sp);
-                }
+                for (int j = 0; j < 4; ++j) o[j] = dequant_word_f16(w4[j], dd);
               } else {
+                const ScalePieces sp = scale_pieces(d[i]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
+                for (int j = 0; j < 4; ++j) o[j] = dequant_word(w4[j], sp);
               }
+            } else {
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                v[16 * i + 4 * j] = o[j].x;
-                v[16 * i + 4 * j + 1] = o[j].y;
-                v[16 * i + 4 * j + 2] = o[j].z;
-                v[16 * i + 4 * j + 3] = o[j].w;
-              }
+              for (int j = 0; j < 4; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
             }
-            tmem_st_cols<16 * kBPW>(a_lane + (uint32_t)(kACols * s), v);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              v[16 * i + 4 * j] = o[j].x;
+              v[16 * i + 4 * j + 1] = o[j].y;
+              v[16 * i + 4 * j + 2] = o[j].z;
+              v[16 * i + 4 * j + 3] = o[j].w;
+            }
           }
-          tc_fence_before();   // this warp's TMEM stores, before the MMA issuer reads them
-          __syncwarp();
-          if (lane == 0) mbar_arrive(full0 + 8 * s);
-          if (wc == 0 && lane == 0) stamp(g, 3);
+          tmem_st_cols<16 * kBPW>(a_lane + (uint32_t)(kACols * s), v);
         }
+        tc_fence_before();   // this warp's TMEM stores, before the MMA issuer reads them
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full0 + 8 * s);
+        if (wc == 0 && lane == 0) stamp(g, 3);
       }
     }
   } else if (warp == kMmaWarp) {
