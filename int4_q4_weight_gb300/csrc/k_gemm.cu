@@ -74,7 +74,7 @@ unsigned* device_error_word() {
 
 namespace gemm {
 
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kRawStages = 8;
 constexpr int kRawChunks = 2;          // operand chunks per raw stage (256 K columns)
 constexpr int kTileM = 128;            // weight rows per tile (MMA M)
@@ -96,18 +96,26 @@ constexpr int kRawCodeBytes = kTileM * kChunk * kRawChunks / 2;   // 16 KB: [128
 constexpr int kRawScaleBytes = kTileM * 16;                         // 2 KB: [128 rows][8 fp16]
 constexpr int kRawBytes = kRawCodeBytes + kRawScaleBytes;
 constexpr int kEpiWarps = 4, kProdWarps = 16;
-// The converter warps form kRawChunks groups; group k converts chunk k of
-// every raw stage, so consecutive chunks are converted concurrently.
-constexpr int kGroupWarps = kProdWarps / kRawChunks;   // 8: two per lane quarter
-constexpr int kBPW = 16 / kGroupWarps;                 // 32-column blocks of a chunk per converter warp
+// The converter warps form kGroups groups of one warp per lane quarter;
+// consecutive chunks go to consecutive groups (chunk j of raw stage gr to
+// group kRawChunks (gr % kStageSets) + j), so kGroups chunks are converted
+// concurrently.
+constexpr int kGroups = 4;
+constexpr int kStageSets = kGroups / kRawChunks;       // raw stages per round of the groups
+constexpr int kGroupWarps = kProdWarps / kGroups;      // 4: one per lane quarter
+constexpr int kBPW = 16 / kGroupWarps;                 // 32-column blocks of a chunk per converter warp: 4
+static_assert(kGroups % kRawChunks == 0 && kGroupWarps == 4, "one warp per lane quarter in a group");
 constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 20
 constexpr int kTmaWarp = kMmaWarp + 1;             // 21
 constexpr int kBWarp = kTmaWarp + 1;               // 22
 constexpr int kThreadsG = (kBWarp + 1) * 32;       // 736
 constexpr int kBars = 2 * kStages + 2 * kRawStages + 5;
-__host__ __device__ constexpr size_t smem_bytes(int n) {
+__host__ __device__ constexpr size_t smem_bytes(int n) {   // dynamic shared memory
   return 1024 + (size_t)kStages * stage_bytes(n) + (size_t)kRawStages * kRawBytes + kBars * 8;
 }
+// dynamic plus static shared memory (the LM-head records) within the 227 KB
+// a CTA may hold
+static_assert(smem_bytes(kTok) + 1024 <= 232448 && smem_bytes(16) + 40960 <= 232448, "shared memory");
 constexpr long long kDrainCycles = 2000000000LL;
 constexpr long long kShortDrainCycles = 4000000LL;   // aborting: copies in flight land well within this
 
@@ -359,7 +367,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     mbar_init(drain, 1);
     for (int s = 0; s < kRawStages; ++s) {
       mbar_init(rawfull0 + 8 * s, 1);
-      mbar_init(rawempty0 + 8 * s, kProdWarps);
+      mbar_init(rawempty0 + 8 * s, kRawChunks * kGroupWarps);   // the warps of the groups that read it
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -463,24 +471,26 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     __syncwarp();
   } else if (warp >= kEpiWarps && warp < kMmaWarp) {
     // ----------------------------------------------------------- converters
-    // Group k (warps 4 + 8k .. 11 + 8k) converts chunk k of every raw stage.
-    // thread = tile row r (TMEM lane r): warp w writes TMEM lanes
-    // 32 (w % 4) .. + 31 (the lane quarter its scheduler may access); the two
-    // warps of a quarter in a group split the chunk's four 32-column blocks,
-    // kBPW each, written as 16 kBPW columns (two 16-bit weights per column,
-    // slot order) of the stage's A columns
+    // Group cg (warps 4 + 4 cg .. 7 + 4 cg) converts chunk j of the raw stages
+    // gr with kRawChunks (gr % kStageSets) + j == cg.  thread = tile row r
+    // (TMEM lane r): warp w writes TMEM lanes 32 (w % 4) .. + 31 (the lane
+    // quarter its scheduler may access), all four 32-column blocks of the
+    // chunk for its rows, as two stores of 32 columns (two 16-bit weights per
+    // column, slot order) into the stage's A columns
     const int wc = warp - kEpiWarps;                 // 0 .. kProdWarps - 1
     const int cg = wc / kGroupWarps;                 // chunk group
-    const int grp = (wc % kGroupWarps) >> 2;         // block group of this warp
     const int r = 32 * (warp & 3) + lane;
-    const uint32_t a_lane =
-        tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(a_col0(NT) + 16 * kBPW * grp);
+    const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)a_col0(NT);
     uint32_t g0 = 0, gr = 0;   // first operand chunk of the raw stage, raw stages
     bool ok = true;
     for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
       int tile, c0, c1;
       item_range(p, item, tile, c0, c1);
       for (int cs = c0; cs < c1 && ok; cs += kRawChunks, ++gr) {
+        const int j = cg - kRawChunks * (int)(gr % kStageSets);   // this group's chunk in the raw stage
+        const uint32_t gs = g0;
+        g0 += (uint32_t)(min(cs + kRawChunks, c1) - cs);
+        if (j < 0 || j >= kRawChunks) continue;   // a raw stage of the other groups
         const uint32_t rs = gr % kRawStages, rround = gr / kRawStages;
         const bool landed = mbar_wait(rawfull0 + 8 * rs, rround & 1, p.wait_limit, abort_flag);
         if (!__all_sync(0xffffffffu, landed)) {
@@ -488,25 +498,23 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           break;
         }
         const uint8_t* raw = raw_base + (size_t)rs * kRawBytes;
-        const int c = cs + cg;                 // this group's chunk
-        const uint32_t g = g0 + (uint32_t)cg;
-        g0 += (uint32_t)(min(cs + kRawChunks, c1) - cs);
+        const int c = cs + j;                  // this group's chunk
+        const uint32_t g = gs + (uint32_t)j;
         const bool mine = c < c1;              // an item's last raw stage may hold one chunk
         if (wc == 0 && lane == 0) stamp(g, 1);
         const int nb = mine ? min(kChunk, p.K - c * kChunk) / 32 : 0;   // 32-column blocks: 4, or 2 at the end
         uint4 code[kBPW];
         float d[kBPW];
 #pragma unroll
-        for (int i = 0; i < kBPW; ++i) {
-          const int bb = kBPW * grp + i;
+        for (int bb = 0; bb < kBPW; ++bb) {
           if (bb < nb) {
             // the codes tile arrives in the 128-byte swizzle: 16-byte group
-            // j of row r sits at group j ^ (r % 8), so the 32 rows read by a
+            // i of row r sits at group i ^ (r % 8), so the 32 rows read by a
             // warp spread over the banks
-            code[i] = *reinterpret_cast<const uint4*>(raw + r * 128 + (((cg * 4 + bb) ^ (r & 7)) << 4));
-            d[i] = p.sc_tma ? __half2float(*reinterpret_cast<const __half*>(raw + kRawCodeBytes + r * 16 +
-                                                                              (cg * 4 + bb) * 2))
-                            : ld_scale(p.scales + ((size_t)tile * kTileM + r) * (p.K >> 5) + c * 4 + bb);
+            code[bb] = *reinterpret_cast<const uint4*>(raw + r * 128 + (((j * 4 + bb) ^ (r & 7)) << 4));
+            d[bb] = p.sc_tma ? __half2float(*reinterpret_cast<const __half*>(raw + kRawCodeBytes + r * 16 +
+                                                                              (j * 4 + bb) * 2))
+                             : ld_scale(p.scales + ((size_t)tile * kTileM + r) * (p.K >> 5) + c * 4 + bb);
           }
         }
         __syncwarp();   // this warp has read its part of the raw stage
@@ -520,36 +528,33 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         }
         tc_fence_after();   // the MMAs that read this A stage have completed
         if (wc == 0 && lane == 0) stamp(g, 2);
-        if (kBPW * grp < nb) {   // warp-uniform: a last chunk of 64 columns has no blocks 2, 3
-          uint32_t v[16 * kBPW];
 #pragma unroll
-          for (int i = 0; i < kBPW; ++i) {
-            const int bb = kBPW * grp + i;
-            const uint32_t w4[4] = {code[i].x, code[i].y, code[i].z, code[i].w};
+        for (int pp = 0; pp < kBPW / 2; ++pp) {
+          if (2 * pp >= nb) break;   // warp-uniform: a last chunk of 64 columns has no blocks 2, 3
+          uint32_t v[32];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int bb = 2 * pp + i;
+            const uint32_t w4[4] = {code[bb].x, code[bb].y, code[bb].z, code[bb].w};
             uint4 o[4];
-            if (bb < nb) {
-              if (F16) {
-                const __half2 dd = __float2half2_rn(d[i]);   // d is an fp16 value: exact
+            if (F16) {
+              const __half2 dd = __float2half2_rn(d[bb]);   // d is an fp16 value: exact
 #pragma unroll
-                for (int j = 0; j < 4; ++j) o[j] = dequant_word_f16(w4[j], dd);
-              } else {
-                const ScalePieces sp = scale_pieces(d[i]);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) o[j] = dequant_word(w4[j], sp);
-              }
+              for (int q = 0; q < 4; ++q) o[q] = dequant_word_f16(w4[q], dd);
             } else {
+              const ScalePieces sp = scale_pieces(d[bb]);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
+              for (int q = 0; q < 4; ++q) o[q] = dequant_word(w4[q], sp);
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              v[16 * i + 4 * j] = o[j].x;
-              v[16 * i + 4 * j + 1] = o[j].y;
-              v[16 * i + 4 * j + 2] = o[j].z;
-              v[16 * i + 4 * j + 3] = o[j].w;
+            for (int q = 0; q < 4; ++q) {
+              v[16 * i + 4 * q] = o[q].x;
+              v[16 * i + 4 * q + 1] = o[q].y;
+              v[16 * i + 4 * q + 2] = o[q].z;
+              v[16 * i + 4 * q + 3] = o[q].w;
             }
           }
-          tmem_st_cols<16 * kBPW>(a_lane + (uint32_t)(kACols * s), v);
+          tmem_st32(a_lane + (uint32_t)(kACols * s + 32 * pp), v);
         }
         tc_fence_before();   // this warp's TMEM stores, before the MMA issuer reads them
         __syncwarp();
