@@ -110,6 +110,7 @@ constexpr int kTmaWarp = kMmaWarp + 1;             // 21
 constexpr int kBWarp = kTmaWarp + 1;               // 22
 constexpr int kThreadsG = (kBWarp + 1) * 32;       // 736
 constexpr int kBars = 2 * kStages + 2 * kRawStages + 5;
+static_assert(kBars <= 32, "one barrier per lane of warp 0");
 __host__ __device__ constexpr size_t smem_bytes(int n) {   // dynamic shared memory
   return 1024 + (size_t)kStages * stage_bytes(n) + (size_t)kRawStages * kRawBytes + kBars * 8;
 }
@@ -353,23 +354,25 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   const uint32_t rawfull0 = smem_u32(bars + 2 * kStages + 5), rawempty0 = rawfull0 + 8 * kRawStages;
   volatile int* abort_flag = &abort_sh;
 
-  if (threadIdx.x == 0) {
-    abort_sh = 0;
-    t0_sh = tc::clock_ordered();
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, kGroupWarps + 1);   // one arrival per warp of the chunk's group + the B loader's
-      mbar_init(empty0 + 8 * s, 1);
+  if (warp == 0) {
+    // lane i initialises barrier i (in the order of the layout above)
+    if (lane == 0) {
+      abort_sh = 0;
+      t0_sh = tc::clock_ordered();
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(accfull0 + 8 * a, 1);
-      mbar_init(accempty0 + 8 * a, kEpiWarps);
+    if (lane < kBars) {
+      const int i = lane;
+      unsigned count = 1;                                              // empty, accfull, drain, rawfull
+      if (i < kStages) count = kGroupWarps + 1;                        // full: the chunk's group + the B loader
+      else if (i >= 2 * kStages + 2 && i < 2 * kStages + 4) count = kEpiWarps;   // accempty
+      else if (i >= 2 * kStages + 5 + kRawStages) count = kRawChunks * kGroupWarps;   // rawempty: its readers
+      mbar_init(smem_u32(bars + i), count);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    mbar_init(drain, 1);
-    for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(rawfull0 + 8 * s, 1);
-      mbar_init(rawempty0 + 8 * s, kRawChunks * kGroupWarps);   // the warps of the groups that read it
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  } else if (warp == kTmaWarp && lane == 0) {
+    // the tensor maps' descriptors, fetched while the CTA sets up
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_codes)) : "memory");
+    if (p.sc_tma) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_sc)) : "memory");
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_sh)),
@@ -625,6 +628,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   } else {
     // ------------------------------------------------------------ epilogue
     const int row = warp * 32 + lane;          // TMEM lane = tile row
+    if (p.splits > 1) pdl_wait();              // Y is cleared by the kernel launched just before
     // LM head: the best two (z, row) per token over the rows this thread
     // reads, kept in shared memory (token-major: a warp's records of one token
     // are 512 contiguous bytes)
@@ -709,8 +713,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
 // (group, token).
 template <int NT, bool F16>
 __global__ void __launch_bounds__(256) x_layout_kernel(const __half* __restrict__ X, uint8_t* __restrict__ xb,
-                                                       int K, int ntok) {
+                                                       int K, int ntok, float4* __restrict__ yclear, int n4) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;   // = group * NT + token
+  // the output the split-K GEMM adds into, cleared (n4 float4s; 0 if none)
+  for (int k = i; k < n4; k += gridDim.x * blockDim.x) yclear[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (i < (K >> 3) * NT) {
     const int grp = i / NT, tok = i - grp * NT;
     uint4 o = make_uint4(0u, 0u, 0u, 0u);
@@ -814,10 +820,6 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
                 ? static_cast<unsigned long long*>(tb)
                 : nullptr;
   cudaError_t e;
-  if (p.splits > 1) {
-    e = cudaMemsetAsync(Y, 0, (size_t)ntok * N * sizeof(float), s);
-    if (e != cudaSuccess) return cuda_fail(e, "gemm output clear");
-  }
   static PerDevice attr_set;   // one per instantiation and device
   if (!attr_set.get(dev.ordinal)) {
     e = cudaFuncSetAttribute(gemm::gemm_kernel<NT, F16, HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -826,7 +828,11 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
     attr_set.set(dev.ordinal);
   }
   const int nx = (K >> 3) * NT;
-  gemm::x_layout_kernel<NT, F16><<<(nx + 255) / 256, 256, 0, s>>>(X, static_cast<uint8_t*>(ws), K, ntok);
+  // split K: the token-layout kernel also clears Y, which the GEMM's
+  // epilogue adds into only after waiting for that kernel
+  const int n4 = p.splits > 1 ? (int)((size_t)ntok * N / 4) : 0;
+  gemm::x_layout_kernel<NT, F16><<<(nx + 255) / 256, 256, 0, s>>>(X, static_cast<uint8_t*>(ws), K, ntok,
+                                                                  reinterpret_cast<float4*>(Y), n4);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "gemm token layout launch");
   // the GEMM starts while the token layout is written; only its B loader waits for it
