@@ -12,38 +12,39 @@
 // items (a 128-row tile and a range of 64-column K chunks; K is split across
 // CTAs when there are fewer tiles than SMs, the splits then add into Y).
 //
-// Warp roles (736 threads):
-//   warps 0-3   epilogue: tcgen05.ld of their TMEM lane quarter, store to Y;
-//               in the LM-head form (16 tokens, fp16 tiles) no Y: each thread
-//               keeps the best two (z, row) per token over its rows, the
-//               warps merge them at the end, and the CTA that finishes last
-//               merges every CTA's record (tanh(z/cap)*cap written only when
-//               the caller asks for the logits)
-//   warps 4-19  converters: raw codes + scales from the raw ring, nibble ->
-//               bf16 d*(q-8) rounded once (or fp16 for the head form); a
-//               thread owns a tile row (TMEM lane) and one 32-column block
-//               of the chunk, written with one tcgen05.st of 16 columns
-//               (warps w, w + 4, w + 8, w + 12 share TMEM lane quarter w % 4,
-//               the only lanes their scheduler may access); 16 warps rather
-//               than 8 so that each scheduler has four to switch between
-//               while one waits on its loads, stores or barriers
-//   warp 20     TMEM allocator and MMA issuer: the warp walks the pipeline
-//               and waits together, one elected lane issues the 8 MMAs of a
-//               128-column stage (A from tensor memory) and the commits
-//   warp 21     raw-ring TMA loads (one elected lane issues)
-//   warp 22     token tile (B) of each operand stage: one bulk copy from the
+// Warp roles (768 threads):
+//   warps 0-3   epilogue: tcgen05.ld of their TMEM lane quarter (both
+//               issuers' accumulators, added), store to Y; in the LM-head
+//               form (16 tokens, fp16 tiles) no Y: each thread keeps the best
+//               two (z, row) per token over its rows, the warps merge them at
+//               the end, and the CTA that finishes last merges every CTA's
+//               record (tanh(z/cap)*cap written only when the caller asks for
+//               the logits)
+//   warps 4-19  converters, four groups of one warp per TMEM lane quarter
+//               (the only lanes a warp's scheduler may access); consecutive
+//               chunks go to consecutive groups.  Raw codes + scales from the
+//               raw ring, nibble -> bf16 d*(q-8) rounded once (or fp16 for the
+//               head form); a thread owns a tile row (TMEM lane) and writes
+//               the chunk's 128 columns of it as two tcgen05.st of 32 columns
+//   warps 20-21 MMA issuers (20 also allocates TMEM): one elected lane each
+//               issues half of every chunk's 8 MMAs (A from tensor memory)
+//               into its own accumulator, and commits.  An MMA takes ~65
+//               cycles of its issuing thread, so one issuer alone capped the
+//               kernel at ~0.5 us per chunk
+//   warp 22     raw-ring TMA loads (one elected lane issues)
+//   warp 23     token tile (B) of each operand stage: one bulk copy from the
 //               bf16 copy of X, completing on the stage's full barrier
 // X is rounded to bf16 once per call by a small kernel ahead of the GEMM (in
 // the caller's workspace) instead of once per tile and chunk.  The raw ring
 // (kRawStages x 256 K columns: codes 16 KB + scales 2 KB) keeps weight bytes
 // in flight; the operand stages (kStages x (A: 64 TMEM columns, B: 16 KB of
 // shared memory), 128 K columns each) feed the tensor cores.  full counts the
-// converter warps and the B loader (with its bytes), so the MMA issuer waits
-// on one barrier per stage.
-// Two TMEM accumulators (2 x N columns) let the epilogue of one item
-// overlap the MMAs of the next.  Every mbarrier wait is bounded in
+// chunk's converter group and the B loader (with its bytes), so an MMA issuer
+// waits on one barrier per stage.
+// Two items' accumulators (2 issuers x 2 x N columns) let the epilogue of
+// one item overlap the MMAs of the next.  Every mbarrier wait is bounded in
 // clock cycles; on expiry the CTA raises an abort flag, every role leaves its
-// loop, the MMA issuer drains its own tcgen05 work (bounded again), TMEM is
+// loop, each MMA issuer drains its own tcgen05 work (bounded again), TMEM is
 // freed and the kernel returns with the device error word set.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -74,7 +75,7 @@ unsigned* device_error_word() {
 
 namespace gemm {
 
-constexpr int kStages = 5;
+constexpr int kStages = 4;
 constexpr int kRawStages = 8;
 constexpr int kRawChunks = 2;          // operand chunks per raw stage (256 K columns)
 constexpr int kTileM = 128;            // weight rows per tile (MMA M)
@@ -84,11 +85,12 @@ constexpr int kChunk = 128;            // K columns per operand stage (8 MMAs of
 // 16-bit weights of a chunk, two per 32-bit column, K order)
 constexpr int kACols = kChunk / 2;
 // per token count N (the MMA N): token tile bytes per stage (the only operand
-// in shared memory), the first TMEM column of the A stages (after the two
-// accumulators) and the TMEM columns allocated (a power of two)
+// in shared memory), the first TMEM column of the A stages (after two items'
+// accumulators, one per MMA issuer) and the TMEM columns allocated (a power
+// of two)
 __host__ __device__ constexpr int b_bytes(int n) { return n * kChunk * 2; }
 __host__ __device__ constexpr int stage_bytes(int n) { return b_bytes(n); }
-__host__ __device__ constexpr int a_col0(int n) { return 2 * n < 32 ? 32 : 2 * n; }
+__host__ __device__ constexpr int a_col0(int n) { return 4 * n < 32 ? 32 : 4 * n; }
 __host__ __device__ constexpr int tmem_cols(int n) {
   return a_col0(n) + kStages * kACols <= 256 ? 256 : 512;
 }
@@ -105,10 +107,11 @@ constexpr int kStageSets = kGroups / kRawChunks;       // raw stages per round o
 constexpr int kGroupWarps = kProdWarps / kGroups;      // 4: one per lane quarter
 constexpr int kBPW = 16 / kGroupWarps;                 // 32-column blocks of a chunk per converter warp: 4
 static_assert(kGroups % kRawChunks == 0 && kGroupWarps == 4, "one warp per lane quarter in a group");
-constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 20
-constexpr int kTmaWarp = kMmaWarp + 1;             // 21
-constexpr int kBWarp = kTmaWarp + 1;               // 22
-constexpr int kThreadsG = (kBWarp + 1) * 32;       // 736
+constexpr int kIssuers = 2;                        // MMA-issuing warps, one accumulator each
+constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 20, 21 (20 also allocates TMEM)
+constexpr int kTmaWarp = kMmaWarp + kIssuers;      // 22
+constexpr int kBWarp = kTmaWarp + 1;               // 23
+constexpr int kThreadsG = (kBWarp + 1) * 32;       // 768
 constexpr int kBars = 2 * kStages + 2 * kRawStages + 5;
 static_assert(kBars <= 32, "one barrier per lane of warp 0");
 __host__ __device__ constexpr size_t smem_bytes(int n) {   // dynamic shared memory
@@ -329,6 +332,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   constexpr int kStageBytes = stage_bytes(NT);
   constexpr int kBBytes = b_bytes(NT);
   constexpr int kTmemCols = tmem_cols(NT);
+  static_assert(a_col0(NT) + kStages * kACols <= 512, "tensor memory");
+  static_assert(kIssuers == 2, "two accumulators per item");
   constexpr uint32_t kId = idesc(NT, F16);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -362,9 +367,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     }
     if (lane < kBars) {
       const int i = lane;
-      unsigned count = 1;                                              // empty, accfull, drain, rawfull
+      unsigned count = 1;                                              // rawfull
       if (i < kStages) count = kGroupWarps + 1;                        // full: the chunk's group + the B loader
-      else if (i >= 2 * kStages + 2 && i < 2 * kStages + 4) count = kEpiWarps;   // accempty
+      else if (i < 2 * kStages + 2) count = 2;                         // empty, accfull: one commit per issuer
+      else if (i < 2 * kStages + 4) count = kEpiWarps;                 // accempty
+      else if (i == 2 * kStages + 4) count = 2;                        // drain: one commit per issuer
       else if (i >= 2 * kStages + 5 + kRawStages) count = kRawChunks * kGroupWarps;   // rawempty: its readers
       mbar_init(smem_u32(bars + i), count);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -565,9 +572,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         if (wc == 0 && lane == 0) stamp(g, 3);
       }
     }
-  } else if (warp == kMmaWarp) {
-    // --------------------------------------------------------- MMA issuer
-    // (the whole warp walks the loop and waits, one elected lane issues)
+  } else if (warp >= kMmaWarp && warp < kMmaWarp + kIssuers) {
+    // -------------------------------------------------------- MMA issuers
+    // Issuer m takes the second or first half of each chunk's K steps into
+    // its own accumulator (each accumulator's MMAs come from one thread, in
+    // order); both commit to the stage's empty barrier.  (Each warp walks
+    // the loop and waits together, one elected lane issues.)
+    const int m = warp - kMmaWarp;
     uint32_t g = 0;
     int it = 0;
     bool ok = true;
@@ -582,7 +593,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem + (uint32_t)(a * NT);
+      const uint32_t d_tmem = tmem + (uint32_t)((kIssuers * a + m) * NT);
       for (int c = c0; c < c1; ++c, ++g) {
         const uint32_t s = g % kStages, round = g / kStages;
         // full: the converter warps' A tile and the B loader's token tile
@@ -593,20 +604,20 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
         }
         tc_fence_after();
         if (elect_one()) {
-          stamp(g, 4);
-          const uint32_t B = stage0 + s * kStageBytes;
-          const uint32_t A = tmem + (uint32_t)(a_col0(NT) + kACols * s);   // lane 0, the stage's A columns
-          const int nks = min(kChunk, p.K - c * kChunk) / 16;
+          if (m == 0) stamp(g, 4);
+          const int half = min(kChunk, p.K - c * kChunk) / 32;   // K steps per issuer: 4, or 2 at the end
+          const int ks0 = m * half;
+          // B: [16 column groups][NT tokens][8]: groups NT * 16 B apart;
+          // K step ks starts NT * 32 bytes further (2 NT in the descriptor's
+          // address field, which no step carries out of)
+          const uint64_t bd0 = smem_desc(stage0 + s * kStageBytes + ks0 * NT * 32, NT * 16, 128);
+          const uint32_t A = tmem + (uint32_t)(a_col0(NT) + kACols * s + 8 * ks0);   // lane 0
 #pragma unroll
-          for (int ks = 0; ks < kChunk / 16; ++ks) {
-            if (ks < nks) {
-              // B: [16 column groups][NT tokens][8]: groups NT * 16 B apart
-              const uint64_t bd = smem_desc(B + ks * NT * 32, NT * 16, 128);
-              tc_mma_ta(d_tmem, A + 8 * ks, bd, kId, (c > c0 || ks > 0) ? 1u : 0u);
-            }
+          for (int kk = 0; kk < kChunk / 32; ++kk) {
+            if (kk < half) tc_mma_ta(d_tmem, A + 8 * kk, bd0 + (uint64_t)(kk * NT * 2), kId, (c > c0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(empty0 + 8 * s);
-          stamp(g, 5);
+          if (m == 0) stamp(g, 5);
         }
         __syncwarp();
       }
@@ -649,7 +660,14 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
 #pragma unroll
       for (int cb = 0; cb < NT / 16; ++cb) {
         float v[16];
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(a * NT + cb * 16), v);
+        const uint32_t t_acc = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(kIssuers * a * NT + cb * 16);
+        tmem_ld16(t_acc, v);
+        {   // the second issuer's accumulator, added in a fixed order
+          float u[16];
+          tmem_ld16(t_acc + (uint32_t)NT, u);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] += u[j];
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int t = cb * 16 + j;
