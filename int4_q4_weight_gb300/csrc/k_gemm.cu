@@ -112,14 +112,23 @@ constexpr int kMmaWarp = kEpiWarps + kProdWarps;   // 20, 21 (20 also allocates 
 constexpr int kTmaWarp = kMmaWarp + kIssuers;      // 22
 constexpr int kBWarp = kTmaWarp + 1;               // 23
 constexpr int kThreadsG = (kBWarp + 1) * 32;       // 768
-constexpr int kBars = 2 * kStages + 2 * kRawStages + 5;
+constexpr int kBars = 2 * kStages + 2 * kRawStages + 6;
 static_assert(kBars <= 32, "one barrier per lane of warp 0");
-__host__ __device__ constexpr size_t smem_bytes(int n) {   // dynamic shared memory
-  return 1024 + (size_t)kStages * stage_bytes(n) + (size_t)kRawStages * kRawBytes + kBars * 8;
+// The LM-head form keeps the whole token operand (K / 8 column groups x 16
+// tokens x 16 B = 32 K bytes) resident in shared memory, loaded once, instead
+// of a ring of token tiles: no token-tile fetch sits between one chunk's MMAs
+// and the next.
+__host__ __device__ constexpr size_t xres_bytes(int K) { return ((size_t)K * 32 + 1023) & ~(size_t)1023; }
+__host__ __device__ constexpr size_t operand_bytes(int n, bool head, int K) {
+  return head ? xres_bytes(K) : (size_t)kStages * stage_bytes(n);
+}
+__host__ __device__ constexpr size_t smem_bytes(int n, bool head, int K) {   // dynamic shared memory
+  return 1024 + operand_bytes(n, head, K) + (size_t)kRawStages * kRawBytes + kBars * 8;
 }
 // dynamic plus static shared memory (the LM-head records) within the 227 KB
 // a CTA may hold
-static_assert(smem_bytes(kTok) + 1024 <= 232448 && smem_bytes(16) + 40960 <= 232448, "shared memory");
+static_assert(smem_bytes(kTok, false, 0) + 1024 <= 232448, "shared memory");
+constexpr size_t kSmemMax = 232448;   // dynamic plus static shared memory of a CTA
 constexpr long long kDrainCycles = 2000000000LL;
 constexpr long long kShortDrainCycles = 4000000LL;   // aborting: copies in flight land well within this
 
@@ -338,15 +347,15 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* stage_base = smem;
-  uint8_t* raw_base = smem + (size_t)kStages * kStageBytes;
+  uint8_t* raw_base = smem + operand_bytes(NT, HEAD, p.K);
   uint64_t* bars = reinterpret_cast<uint64_t*>(raw_base + (size_t)kRawStages * kRawBytes);
   // bars: full[kStages], empty[kStages], accfull[2], accempty[2], drain,
-  //       rawfull[kRawStages], rawempty[kRawStages]
+  //       rawfull[kRawStages], rawempty[kRawStages], xfull (resident token operand)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ long long t0_sh;
   __shared__ Top2 head_st[kEpiWarps][HEAD ? NT : 1];   // LM head: per epilogue warp and token
-  __shared__ Top2 head_run[HEAD ? NT : 1][HEAD ? kEpiWarps * 32 : 1];   // LM head: per token and row
+  __shared__ Top2 head_run[HEAD ? kMaxBatch : 1][HEAD ? kEpiWarps * 32 : 1];   // LM head: per token and row
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned long long* const tr = (p.trace && blockIdx.x == 0) ? p.trace : nullptr;
@@ -357,6 +366,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
   const uint32_t accfull0 = smem_u32(bars + 2 * kStages), accempty0 = smem_u32(bars + 2 * kStages + 2);
   const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
   const uint32_t rawfull0 = smem_u32(bars + 2 * kStages + 5), rawempty0 = rawfull0 + 8 * kRawStages;
+  const uint32_t xfull = rawempty0 + 8 * kRawStages;
   volatile int* abort_flag = &abort_sh;
 
   if (warp == 0) {
@@ -368,11 +378,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     if (lane < kBars) {
       const int i = lane;
       unsigned count = 1;                                              // rawfull
-      if (i < kStages) count = kGroupWarps + 1;                        // full: the chunk's group + the B loader
+      if (i < kStages) count = HEAD ? kGroupWarps : kGroupWarps + 1;   // full: the chunk's group (+ the B loader)
       else if (i < 2 * kStages + 2) count = 2;                         // empty, accfull: one commit per issuer
       else if (i < 2 * kStages + 4) count = kEpiWarps;                 // accempty
       else if (i == 2 * kStages + 4) count = 2;                        // drain: one commit per issuer
-      else if (i >= 2 * kStages + 5 + kRawStages) count = kRawChunks * kGroupWarps;   // rawempty: its readers
+      else if (i >= 2 * kStages + 5 + kRawStages && i < kBars - 1)
+        count = kRawChunks * kGroupWarps;                                  // rawempty: its readers
+      // xfull (the last): the loader's bytes
       mbar_init(smem_u32(bars + i), count);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -442,9 +454,27 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
     pdl_wait();   // the bf16 copy of X is written by the kernel launched just before
     const uint32_t stage0 = smem_u32(stage_base);
+    if constexpr (HEAD) {
+      // the whole token operand, once: K * 32 bytes in pieces of at most 16 KB
+      const uint32_t total = (uint32_t)p.K * 32u;
+      if (elect_one()) {
+        mbar_expect_tx(xfull, total);
+        for (uint32_t off = 0; off < total; off += 16384u)
+          bulk_load(stage0 + off, p.xb + off, min(16384u, total - off), xfull, pol_keep);
+      }
+      __syncwarp();
+      const long long t0 = clock64();   // it lands before the CTA may exit
+      while (!mbar_test(xfull, 0)) {
+        if (clock64() - t0 > kDrainCycles) {
+          atomicOr(&g_device_error, 1u);
+          break;
+        }
+      }
+      __syncwarp();
+    }
     uint32_t g = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
+    for (int item = blockIdx.x; item < p.items && ok && !HEAD; item += gridDim.x) {
       int tile, c0, c1;
       item_range(p, item, tile, c0, c1);
       for (int c = c0; c < c1; ++c, ++g) {
@@ -466,7 +496,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     }
     // every issued copy lands before the CTA may exit (full also waits for
     // the converters, which an aborting CTA may never bring, hence the
-    // short bound then)
+    // short bound then); none in the LM-head form
     const uint32_t first = g > (uint32_t)kStages ? g - kStages : 0u;
     for (uint32_t q = first; q < g; ++q) {
       const long long lim = *abort_flag ? kShortDrainCycles : kDrainCycles;
@@ -583,6 +613,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     int it = 0;
     bool ok = true;
     const uint32_t stage0 = smem_u32(stage_base);
+    if constexpr (HEAD) ok = __all_sync(0xffffffffu, mbar_wait(xfull, 0, p.wait_limit, abort_flag));
     for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
       int tile, c0, c1;
       item_range(p, item, tile, c0, c1);
@@ -610,7 +641,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
           // B: [16 column groups][NT tokens][8]: groups NT * 16 B apart;
           // K step ks starts NT * 32 bytes further (2 NT in the descriptor's
           // address field, which no step carries out of)
-          const uint64_t bd0 = smem_desc(stage0 + s * kStageBytes + ks0 * NT * 32, NT * 16, 128);
+          const uint32_t bbase = HEAD ? stage0 + (uint32_t)c * kBBytes : stage0 + s * kStageBytes;
+          const uint64_t bd0 = smem_desc(bbase + ks0 * NT * 32, NT * 16, 128);
           const uint32_t A = tmem + (uint32_t)(a_col0(NT) + kACols * s + 8 * ks0);   // lane 0
 #pragma unroll
           for (int kk = 0; kk < kChunk / 32; ++kk) {
@@ -645,7 +677,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
     // are 512 contiguous bytes)
     if constexpr (HEAD) {
 #pragma unroll
-      for (int t = 0; t < NT; ++t) top2_init(head_run[t][row]);
+      for (int t = 0; t < kMaxBatch; ++t) top2_init(head_run[t][row]);
     }
     int it = 0;
     uint32_t ge = 0;   // this item's first chunk in the CTA's sequence (trace only)
@@ -838,13 +870,22 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
                 ? static_cast<unsigned long long*>(tb)
                 : nullptr;
   cudaError_t e;
-  static PerDevice attr_set;   // one per instantiation and device
+  // dynamic shared memory up to what the CTA's static part leaves (set once
+  // per instantiation and device)
+  static PerDevice attr_set;
+  static size_t dyn_max[64] = {0};
   if (!attr_set.get(dev.ordinal)) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<NT, F16, HEAD>);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm attributes");
+    dyn_max[dev.ordinal] = gemm::kSmemMax - fa.sharedSizeBytes;
     e = cudaFuncSetAttribute(gemm::gemm_kernel<NT, F16, HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)gemm::smem_bytes(NT));
+                             (int)dyn_max[dev.ordinal]);
     if (e != cudaSuccess) return cuda_fail(e, "gemm smem attribute");
     attr_set.set(dev.ordinal);
   }
+  const size_t dyn = gemm::smem_bytes(NT, HEAD, K);
+  if (dyn > dyn_max[dev.ordinal]) return fail(Q4_ERR_SHAPE, "K=%d: the token operand does not fit", K);
   const int nx = (K >> 3) * NT;
   // split K: the token-layout kernel also clears Y, which the GEMM's
   // epilogue adds into only after waiting for that kernel
@@ -858,7 +899,7 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(gemm::kThreadsG);
-  cfg.dynamicSmemBytes = gemm::smem_bytes(NT);
+  cfg.dynamicSmemBytes = dyn;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -875,9 +916,15 @@ int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* 
   return launch_mma<gemm::kTok, false, false>(codes, scales, X, gemm::kTok, Y, N, K, ws, true, nullptr, dev, s);
 }
 
+bool head_mma_fits(int K) {
+  // the resident token operand, the raw ring and the barriers, next to the
+  // head form's static records (per-token top-two records: under 18 KB)
+  return K >= 64 && gemm::smem_bytes(16, true, K) + 18 * 1024 <= gemm::kSmemMax;
+}
+
 int launch_head_mma(const uint8_t* codes, const __half* scales, const __half* X, int ntok, int N, int K, void* ws,
                     const HeadOutputs& head, const DeviceInfo& dev, cudaStream_t s) {
-  if (ntok < 1 || ntok > 16) return fail(Q4_ERR_SHAPE, "token count %d must be in [1, 16]", ntok);
+  if (ntok < 1 || ntok > kMaxBatch) return fail(Q4_ERR_SHAPE, "token count %d must be in [1, %d]", ntok, kMaxBatch);
   return launch_mma<16, true, true>(codes, scales, X, ntok, nullptr, N, K, ws, false, &head, dev, s);
 }
 

@@ -124,7 +124,7 @@ static int head_grid(const DeviceInfo& dev) { return 2 * dev.sms; }   // >= the 
 // CTA per 128-row tile, the selection in its epilogue) when the vocabulary
 // fills every SM with tiles.
 static bool head_tc_eligible(int b, int V, int K, const DeviceInfo& dev) {
-  return b >= 2 && V % 128 == 0 && V >= 128 * dev.sms && K % 64 == 0;
+  return b >= 2 && V % 128 == 0 && V >= 128 * dev.sms && K % 64 == 0 && head_mma_fits(K);
 }
 
 static size_t up256(size_t n) { return (n + 255) & ~(size_t)255; }

@@ -122,14 +122,16 @@ int encode_tensor_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type
 size_t gemm_ws_bytes(int K);   // the bf16 copy of X [64][K]
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s);
-// The LM head of ntok <= 16 vectors on the tensor cores: z[t][n] through the
+// The LM head of ntok <= 8 vectors on the tensor cores: z[t][n] through the
 // GEMM kernel with fp16 tiles (weights rounded once to fp16, tokens exact),
 // one CTA per 128-row tile (no split of K, so every row is summed in one fixed
-// order); z never reaches memory: the epilogue softcaps it into head.logits
-// (when set) and keeps a running top two per token, and the CTA that finishes
-// last merges the per-CTA records into idx/top1/top2.  N % 128 == 0,
-// K % 64 == 0; ws: mma16_ws_bytes(K) bytes for the token operand;
-// head.partials: one record per SM and kMaxBatch tokens; head.ticket zero.
+// order), the token operand resident in shared memory; z never reaches
+// memory: the epilogue softcaps it into head.logits (when set) and keeps a
+// running top two per token, and the CTA that finishes last merges the per-CTA
+// records into idx/top1/top2.  N % 128 == 0, K % 64 == 0, head_mma_fits(K);
+// ws: mma16_ws_bytes(K) bytes for the token operand; head.partials: one
+// record per SM and kMaxBatch tokens; head.ticket zero.
+bool head_mma_fits(int K);
 struct Top2;
 struct HeadOutputs {
   float cap;
