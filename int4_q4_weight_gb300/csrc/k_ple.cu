@@ -25,7 +25,7 @@
 // gathered bytes) from shared memory with tensor stores.  The table bytes of
 // those columns are fetched at the start by one 64-byte bulk copy per token.
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0     TMA loads (one elected lane): per stage of 64 K columns the
 //              raw projection tile as two boxes [128 rows][32 fp32]
 //              (128-byte swizzle) and the hidden tile [64 tokens][64 fp16]
@@ -33,10 +33,12 @@
 //   warp 1     TMEM allocation; the warp runs the MMA loop together and one
 //              elected lane issues the MMAs (8 per stage: 4 per piece) and
 //              the commits
-//   warps 2-5  issue the table copies, split the raw tile in place into the
-//              pieces P1 and P2 (thread = projection row: its two 128-byte
-//              raw rows become its P1 and P2 rows, in the 128-byte swizzle
-//              of a K-major fp16 operand), then run the epilogue on their
+//   warps 2-9  converters: split the raw tile in place into the pieces P1
+//              and P2 (thread = projection row and raw box: the box's
+//              128-byte row becomes 64 bytes of P1 and 64 of P2, in the
+//              128-byte swizzle of a K-major fp16 operand); eight warps so
+//              that each scheduler has two to switch between
+//   warps 2-5  also issue the table copies and run the epilogue on their
 //              TMEM lane quarters (warp w reads lanes 32 (w % 4) .. + 31)
 // A ring of kFStages stages (raw / pieces 32 KB + hidden 8 KB) is guarded by
 // full (TMA bytes), bready (converter warps, which arrive only after seeing
@@ -46,7 +48,7 @@
 // is int8 per block of 32) keeps the clusters, roles and epilogue.  A stage is
 // 128 K columns: the code tile [128 rows][128 int8] and two hidden tiles
 // [64 tokens][64 fp16] (128-byte swizzle, the B operand as loaded) come from
-// TMA; warps 2-5 widen the codes to fp16(scale * code) into two swizzled A
+// TMA; warps 2-9 widen the codes to fp16(scale * code) into two swizzled A
 // halves, and 8 MMAs of kind::f16 follow (3 stages of 64 KB: A 32 KB, B 16 KB,
 // codes 16 KB; the block scales of the CTA's rows sit in shared memory).  The
 // K halves of a cluster take alternate 128-column units.
@@ -80,8 +82,10 @@ constexpr int kFHBytes = kTok * kFC * 2;            // 8 KB: hidden tile [64 tok
 constexpr int kFStageBytes = kFRawBytes + kFHBytes;   // 40 KB, a multiple of 1024
 constexpr int kRecvBytes = kTok * 64 * 4;           // partner's partial sums of 64 rows
 constexpr int kGtabBytes = kTok * 64;               // table bytes of the 64 finished rows per token
-constexpr int kThreads = 192;
 constexpr int kEpi0 = 2;                            // first converter / epilogue warp
+constexpr int kConvWarps = 8;                       // converter warps: 2-5 (also the epilogue) and 6-9
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kThreads = (kEpi0 + kConvWarps) * 32;   // 320
 constexpr int kCluster = 4;
 constexpr long long kDrainCycles = 2000000000LL;
 
@@ -271,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     if (trc) trc[0] = tc::globaltimer();
     for (int s = 0; s < kSt; ++s) {
       tc::mbar_init(full0 + 8 * s, 1);
-      tc::mbar_init(bready0 + 8 * s, 4);
+      tc::mbar_init(bready0 + 8 * s, kConvWarps);
       tc::mbar_init(empty0 + 8 * s, 1);
     }
     tc::mbar_init(accfull, 1);
@@ -356,14 +360,16 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
               mma_f16(tmem, tc::desc_sw128(A + h * kQAHalf + 32 * k), tc::desc_sw128(B + h * kQBHalf + 32 * k), idesc,
                       (st | h | k) ? 1u : 0u);
         } else {
-          // D1 (columns 0-63) += P1 . h, D2 (columns 64-127) += P2 . h
+          // D1 (columns 0-63) += P1 . h, D2 (columns 64-127) += P2 . h; K
+          // step k (16 columns) of piece h sits in box k / 2 at byte
+          // 64 h + 32 (k % 2) of each 128-byte row
           const uint32_t A = st0 + s * kStB, H = A + kFRawBytes;
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int k = 0; k < 4; ++k)   // K = 16 fp16 (32 bytes) per MMA
-              mma_f16(tmem + 64 * h, tc::desc_sw128(A + h * kFBox + 32 * k), tc::desc_sw128(H + 32 * k), idesc,
-                      (st | k) ? 1u : 0u);
+              mma_f16(tmem + 64 * h, tc::desc_sw128(A + (k >> 1) * kFBox + 64 * h + 32 * (k & 1)),
+                      tc::desc_sw128(H + 32 * k), idesc, (st | k) ? 1u : 0u);
         }
         tc::commit(empty0 + 8 * s);
         stamp(st, 4);
@@ -378,8 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     __syncwarp();
     tc::mbar_drain(drain, 0, kDrainCycles, p.dev_err);
   } else {
-    // ------------------------------------- B operand: fp16 hidden -> fp32 tile
-    const int ct = threadIdx.x - kEpi0 * 32;   // 0..127
+    // ------------------------------------- converters (warps 2-9), epilogue (2-5)
+    const int cv = threadIdx.x - kEpi0 * 32;   // converter thread 0..255
+    const int ct = cv;                         // epilogue thread 0..127 (warps 2-5)
+    const bool epi = cv < 128;
     // token ct's id; the table bytes of the finished rows: one 64-byte copy
     // per valid token, issued by that token's thread (column row0 + 64 kh and
     // the row width L * 256 are multiples of 16 bytes); thread 0 posts the
@@ -387,14 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     // its load stays in flight through the stage loop.
     int my_id = -1;
     float my_sc = 0.f;
-    if (ct < ntok) {
+    if (epi && ct < ntok) {
       const int v = p.ids[t0 + ct];
       if (v >= 0 && v < p.V)
         my_id = v;
       else if (p.err)
         atomicExch(p.err, 1);
     }
-    if (ct < kTok) {
+    if (epi && ct < kTok) {
       tid_sh[ct] = my_id;
       if (my_id >= 0) {
         tc::bulk_load(tc::smem_u32(gtab + ct * 64), p.table + (size_t)my_id * PLD + (size_t)row0 + 64 * kh, 64,
@@ -407,15 +415,18 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     if constexpr (Q8) {
       // the block scales of this CTA's rows over its stages (row stride D/128
       // quads), all loads in flight together
-      const uint2* src = p.proj_sc + (size_t)(row0 + ct) * (p.D / kQC) + kh;
-      uint2 v[kQMaxStages];
+      if (epi) {
+        const uint2* src = p.proj_sc + (size_t)(row0 + ct) * (p.D / kQC) + kh;
+        uint2 v[kQMaxStages];
 #pragma unroll
-      for (int u = 0; u < kQMaxStages; ++u) v[u] = u < ns ? __ldg(src + 2 * u) : make_uint2(0u, 0u);
+        for (int u = 0; u < kQMaxStages; ++u) v[u] = u < ns ? __ldg(src + 2 * u) : make_uint2(0u, 0u);
 #pragma unroll
-      for (int u = 0; u < kQMaxStages; ++u)
-        if (u < ns) scs[u * kRows + ct] = v[u];
+        for (int u = 0; u < kQMaxStages; ++u)
+          if (u < ns) scs[u * kRows + ct] = v[u];
+      }
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");   // every id (and block scale) is in shared memory
+    // every id (and block scale) is in shared memory
+    asm volatile("bar.sync 2, %0;" ::"n"(kConvThreads) : "memory");
     if (ct == 0) {
       uint32_t nb = 0;
       for (int t = 0; t < ntok; ++t) nb += tid_sh[t] >= 0 ? 64u : 0u;
@@ -434,12 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
         if (ct == 0) stamp(st, 1);
         uint8_t* A = smem + (size_t)s * kStB;
         const uint8_t* raw = A + kQABytes + kQBBytes;
-        // (row r, 8-column group j of its 128 columns): j = ct % 16 is fixed
+        // (row r, 8-column group j of its 128 columns): j = cv % 16 is fixed
         // per thread, so is its block (j / 4) and operand half (j / 8)
-        const int j = ct & 15, jj = j & 7, h = j >> 3, blk = j >> 2;
+        const int j = cv & 15, jj = j & 7, h = j >> 3, blk = j >> 2;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = (ct >> 4) + 8 * i;
+        for (int i = 0; i < 128 / (kConvThreads / 16); ++i) {
+          const int r = (cv >> 4) + (kConvThreads / 16) * i;
           const uint2 c = *reinterpret_cast<const uint2*>(raw + r * kQC + j * 8);
           const uint2 s4 = scs[st * kRows + r];   // scales of columns 0-31, 32-63 (x), 64-95, 96-127 (y)
           const uint32_t sw = blk < 2 ? s4.x : s4.y;
@@ -455,12 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
       }
     } else {
       // ------------------------- A operands: raw f32 tile -> pieces P1, P2
-      // thread ct = projection row r: its 128-byte rows of the two raw boxes
-      // (box b holds columns 32 b .. 32 b + 31) become its P1 row (64 fp16,
-      // first box's slot) and its P2 row (second box's slot); both layouts
-      // put 16-byte group g of row r at group g ^ (r % 8) of its row, so a
-      // quarter-warp (eight consecutive rows) touches eight distinct banks
-      const int r = ct, r8 = r & 7;
+      // thread cv = (projection row r, box hc): its 128-byte row of raw box
+      // hc (columns 32 hc .. 32 hc + 31) becomes, in place, 64 bytes of P1
+      // (16-byte groups 0-3: those columns of P1) followed by 64 bytes of P2
+      // (groups 4-7), so a thread overwrites only what it read itself.  Both
+      // layouts put 16-byte group g of row r at group g ^ (r % 8) of its row,
+      // so a quarter-warp (eight consecutive rows) touches eight distinct banks
+      const int r = cv & 127, hc = cv >> 7, r8 = r & 7;
       for (int st = 0; st < ns; ++st) {
         const int s = st % kSt, round = st / kSt;
         const bool landed = tc::mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
@@ -470,26 +482,24 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
         }
         if (ct == 0) stamp(st, 1);
         uint8_t* row_p = smem + (size_t)s * kFStageBytes + (r >> 3) * 1024 + r8 * 128;
-        float w[64];
+        float w[32];
 #pragma unroll
-        for (int b = 0; b < 2; ++b)
+        for (int c = 0; c < 8; ++c) {   // floats 4c .. 4c+3 of box hc
+          const float4 f = *reinterpret_cast<const float4*>(row_p + hc * kFBox + ((c ^ r8) << 4));
+          w[4 * c] = f.x;
+          w[4 * c + 1] = f.y;
+          w[4 * c + 2] = f.z;
+          w[4 * c + 3] = f.w;
+        }
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {   // floats 4c .. 4c+3 of box b
-            const float4 f = *reinterpret_cast<const float4*>(row_p + b * kFBox + ((c ^ r8) << 4));
-            w[32 * b + 4 * c] = f.x;
-            w[32 * b + 4 * c + 1] = f.y;
-            w[32 * b + 4 * c + 2] = f.z;
-            w[32 * b + 4 * c + 3] = f.w;
-          }
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {     // fp16 columns 8g .. 8g+7
+        for (int g = 0; g < 4; ++g) {     // columns 32 hc + 8 g .. + 7
           float v[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) v[e] = w[8 * g + e];
           uint4 p1, p2;
           split_f32_f16(v, p1, p2);
-          *reinterpret_cast<uint4*>(row_p + ((g ^ r8) << 4)) = p1;
-          *reinterpret_cast<uint4*>(row_p + kFBox + ((g ^ r8) << 4)) = p2;
+          *reinterpret_cast<uint4*>(row_p + hc * kFBox + ((g ^ r8) << 4)) = p1;
+          *reinterpret_cast<uint4*>(row_p + hc * kFBox + (((4 + g) ^ r8) << 4)) = p2;
         }
         tc::fence_proxy_async();
         __syncwarp();
@@ -497,145 +507,155 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
         if (ct == 0) stamp(st, 2);
       }
     }
-    // ------------------------------------------------------------- epilogue
-    if (ct < kTok) tsc[ct] = my_sc;            // read after the barriers below
-    const int q = warp & 3;                    // TMEM lane quarter
-    const int row = 32 * q + lane;             // row of this CTA's tile
-    const bool mine = (q >> 1) == kh;          // rows 64 kh .. 64 kh + 63 are finished here
-    const int r64 = row & 63;
-    const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
-    const bool has = ns > 0;                   // without K work the partial sums are zero
-    if (ok && has) ok = tc::mbar_wait(accfull, 0, p.wait_limit, abort_flag, p.dev_err);
-    ok = __all_sync(0xffffffffu, ok);          // the TMEM loads below are warp-wide
-    tc::fence_after();
-    if (ct == 0) stamp(kTraceRows - 1, 5);
-    // this row's accumulator columns (one per token): one load and one wait
-    float acc[kTok];
-    if (ok && has) {
-      tc::tmem_ld64(taddr, acc);
-      if constexpr (!Q8) {   // p = D1 + D2 * 2^-11 (the scaling is exact: one rounding)
-        float acc2[kTok];
-        tc::tmem_ld64(taddr + 64, acc2);
-#pragma unroll
-        for (int u = 0; u < kTok; ++u) acc[u] = fmaf(acc2[u], 0x1p-11f, acc[u]);
-      }
+    if (!epi) {
+      // conversion-only warps take part in every cluster phase, like the
+      // TMA and MMA warps
+      tc::cluster_wait();
+      tc::cluster_arrive_release();
+      tc::cluster_wait();
+      tc::cluster_arrive_release();
+      tc::cluster_wait();
     } else {
-#pragma unroll
-      for (int u = 0; u < kTok; ++u) acc[u] = 0.f;
-    }
-    tc::cluster_wait();                        // phase 1: every peer is running
-    if (ct == 0) stamp(kTraceRows - 2, 0);
-    if (!mine) {                               // the partner finishes these rows
-      const uint32_t peer = tc::cluster_addr(recv, (uint32_t)(rank ^ 2));
-#pragma unroll
-      for (int cb = 0; cb < kTok / 16; ++cb) {
-        if (cb < npad / 16) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {   // tokens 16 cb + 4 g .. + 3 of this row
-            const int u = 16 * cb + 4 * g;
-            tc::st_cluster_v4(peer + (uint32_t)((((cb * 4 + g) * 64) + r64) * 16), acc[u], acc[u + 1], acc[u + 2],
-                              acc[u + 3]);
-          }
-        }
-      }
-    }
-    tc::cluster_arrive_release();
-    tc::cluster_wait();                        // phase 2: the partner's partial sums are here
-    if (ct == 0) stamp(kTraceRows - 2, 1);
-    // p = (K half 0) + (K half 1), the same order in both CTAs; the four token
-    // groups' reductions are independent of one another
-    float pv[kTok];   // this row's projection sums, kept for the output pass
-#pragma unroll
-    for (int cb = 0; cb < kTok / 16; ++cb) {
-      if (mine && cb < npad / 16) {   // warp-uniform
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const float4 o4 = *reinterpret_cast<const float4*>(recv + (((cb * 4 + g) * 64) + r64) * 4);
-          const float other[4] = {o4.x, o4.y, o4.z, o4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int u = 16 * cb + 4 * g + e;
-            pv[u] = kh == 0 ? acc[u] + other[e] : other[e] + acc[u];
-          }
+      // ----------------------------------------------------------- epilogue
+      if (ct < kTok) tsc[ct] = my_sc;            // read after the barriers below
+      const int q = warp & 3;                    // TMEM lane quarter
+      const int row = 32 * q + lane;             // row of this CTA's tile
+      const bool mine = (q >> 1) == kh;          // rows 64 kh .. 64 kh + 63 are finished here
+      const int r64 = row & 63;
+      const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
+      const bool has = ns > 0;                   // without K work the partial sums are zero
+      if (ok && has) ok = tc::mbar_wait(accfull, 0, p.wait_limit, abort_flag, p.dev_err);
+      ok = __all_sync(0xffffffffu, ok);          // the TMEM loads below are warp-wide
+      tc::fence_after();
+      if (ct == 0) stamp(kTraceRows - 1, 5);
+      // this row's accumulator columns (one per token): one load and one wait
+      float acc[kTok];
+      if (ok && has) {
+        tc::tmem_ld64(taddr, acc);
+        if constexpr (!Q8) {   // p = D1 + D2 * 2^-11 (the scaling is exact: one rounding)
+          float acc2[kTok];
+          tc::tmem_ld64(taddr + 64, acc2);
+  #pragma unroll
+          for (int u = 0; u < kTok; ++u) acc[u] = fmaf(acc2[u], 0x1p-11f, acc[u]);
         }
       } else {
-#pragma unroll
-        for (int u = 0; u < 16; ++u) pv[cb * 16 + u] = 0.f;
+  #pragma unroll
+        for (int u = 0; u < kTok; ++u) acc[u] = 0.f;
       }
-    }
-#pragma unroll
-    for (int cb = 0; cb < kTok / 16; ++cb) {
-      if (mine && cb < npad / 16) {
-        float v[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) v[u] = pv[cb * 16 + u] * pv[cb * 16 + u];
-        const float s2 = lane_token_sums16(v, lane);
-        if ((lane & 1) == 0) red[q & 1][cb * 16 + (lane >> 1)] = s2;
+      tc::cluster_wait();                        // phase 1: every peer is running
+      if (ct == 0) stamp(kTraceRows - 2, 0);
+      if (!mine) {                               // the partner finishes these rows
+        const uint32_t peer = tc::cluster_addr(recv, (uint32_t)(rank ^ 2));
+  #pragma unroll
+        for (int cb = 0; cb < kTok / 16; ++cb) {
+          if (cb < npad / 16) {
+  #pragma unroll
+            for (int g = 0; g < 4; ++g) {   // tokens 16 cb + 4 g .. + 3 of this row
+              const int u = 16 * cb + 4 * g;
+              tc::st_cluster_v4(peer + (uint32_t)((((cb * 4 + g) * 64) + r64) * 16), acc[u], acc[u + 1], acc[u + 2],
+                                acc[u + 3]);
+            }
+          }
+        }
       }
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (ct < kTok) {
-      const float own = red[0][ct] + red[1][ct];   // rows in order within this CTA's 64
-#pragma unroll
-      for (int r = 0; r < kCluster; ++r) tc::st_cluster_f32(tc::cluster_addr(&ssq_in[rank][ct], (uint32_t)r), own);
-    }
-    tc::cluster_arrive_release();
-    tc::cluster_wait();                        // phase 3: all four row quarters' sums are here
-    if (ct == 0) stamp(kTraceRows - 2, 2);
-    if (ct < kTok) rfac[ct] = 1.f / sqrtf((((ssq_in[0][ct] + ssq_in[1][ct]) + ssq_in[2][ct]) + ssq_in[3][ct]) /
-                                                (float)kLd +
-                                            p.eps);
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (ct == 0) stamp(kTraceRows - 1, 6);
-    if (mine) {   // warp-uniform: the TMEM loads below are warp-wide
-      const bool g = ok && tc::mbar_wait(gbar, 0, p.wait_limit, abort_flag, p.dev_err);
-      ok = __all_sync(0xffffffffu, g);
-    }
-    if (ok && mine) {
-      // the output tile [64 tokens][64 columns] in shared memory (the partner's
-      // partial sums are no longer needed), then one tensor store; padding
-      // tokens are outside the tensor and not written
-      float* tile = recv;
-      const float nw = p.norm_w[m * kRows + row];
-      const float es = p.embed_scale;
-      // 16 tokens at a time: every shared-memory read of the group is issued
-      // before its stores (the compiler cannot move reads across the stores)
-#pragma unroll
+      tc::cluster_arrive_release();
+      tc::cluster_wait();                        // phase 2: the partner's partial sums are here
+      if (ct == 0) stamp(kTraceRows - 2, 1);
+      // p = (K half 0) + (K half 1), the same order in both CTAs; the four token
+      // groups' reductions are independent of one another
+      float pv[kTok];   // this row's projection sums, kept for the output pass
+  #pragma unroll
       for (int cb = 0; cb < kTok / 16; ++cb) {
-        float sc[16], rf[16], val[16];
-        int id[16];
-        int8_t tq[16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 a = *reinterpret_cast<const float4*>(tsc + cb * 16 + 4 * i);
-          const float4 b = *reinterpret_cast<const float4*>(rfac + cb * 16 + 4 * i);
-          const int4 c = *reinterpret_cast<const int4*>(tid_sh + cb * 16 + 4 * i);
-          sc[4 * i] = a.x, sc[4 * i + 1] = a.y, sc[4 * i + 2] = a.z, sc[4 * i + 3] = a.w;
-          rf[4 * i] = b.x, rf[4 * i + 1] = b.y, rf[4 * i + 2] = b.z, rf[4 * i + 3] = b.w;
-          id[4 * i] = c.x, id[4 * i + 1] = c.y, id[4 * i + 2] = c.z, id[4 * i + 3] = c.w;
+        if (mine && cb < npad / 16) {   // warp-uniform
+  #pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const float4 o4 = *reinterpret_cast<const float4*>(recv + (((cb * 4 + g) * 64) + r64) * 4);
+            const float other[4] = {o4.x, o4.y, o4.z, o4.w};
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int u = 16 * cb + 4 * g + e;
+              pv[u] = kh == 0 ? acc[u] + other[e] : other[e] + acc[u];
+            }
+          }
+        } else {
+  #pragma unroll
+          for (int u = 0; u < 16; ++u) pv[cb * 16 + u] = 0.f;
         }
-#pragma unroll
-        for (int u = 0; u < 16; ++u) tq[u] = gtab[(cb * 16 + u) * 64 + r64];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float g = __fmul_rn(__fmul_rn((float)tq[u], sc[u]), es);
-          val[u] = id[u] >= 0 ? pv[cb * 16 + u] * rf[u] * nw + g : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 16; ++u) tile[(cb * 16 + u) * 64 + r64] = val[u];
       }
+  #pragma unroll
+      for (int cb = 0; cb < kTok / 16; ++cb) {
+        if (mine && cb < npad / 16) {
+          float v[16];
+  #pragma unroll
+          for (int u = 0; u < 16; ++u) v[u] = pv[cb * 16 + u] * pv[cb * 16 + u];
+          const float s2 = lane_token_sums16(v, lane);
+          if ((lane & 1) == 0) red[q & 1][cb * 16 + (lane >> 1)] = s2;
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (ct < kTok) {
+        const float own = red[0][ct] + red[1][ct];   // rows in order within this CTA's 64
+  #pragma unroll
+        for (int r = 0; r < kCluster; ++r) tc::st_cluster_f32(tc::cluster_addr(&ssq_in[rank][ct], (uint32_t)r), own);
+      }
+      tc::cluster_arrive_release();
+      tc::cluster_wait();                        // phase 3: all four row quarters' sums are here
+      if (ct == 0) stamp(kTraceRows - 2, 2);
+      if (ct < kTok) rfac[ct] = 1.f / sqrtf((((ssq_in[0][ct] + ssq_in[1][ct]) + ssq_in[2][ct]) + ssq_in[3][ct]) /
+                                                  (float)kLd +
+                                              p.eps);
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (ct == 0) stamp(kTraceRows - 1, 6);
+      if (mine) {   // warp-uniform: the TMEM loads below are warp-wide
+        const bool g = ok && tc::mbar_wait(gbar, 0, p.wait_limit, abort_flag, p.dev_err);
+        ok = __all_sync(0xffffffffu, g);
+      }
+      if (ok && mine) {
+        // the output tile [64 tokens][64 columns] in shared memory (the partner's
+        // partial sums are no longer needed), then one tensor store; padding
+        // tokens are outside the tensor and not written
+        float* tile = recv;
+        const float nw = p.norm_w[m * kRows + row];
+        const float es = p.embed_scale;
+        // 16 tokens at a time: every shared-memory read of the group is issued
+        // before its stores (the compiler cannot move reads across the stores)
+  #pragma unroll
+        for (int cb = 0; cb < kTok / 16; ++cb) {
+          float sc[16], rf[16], val[16];
+          int id[16];
+          int8_t tq[16];
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 a = *reinterpret_cast<const float4*>(tsc + cb * 16 + 4 * i);
+            const float4 b = *reinterpret_cast<const float4*>(rfac + cb * 16 + 4 * i);
+            const int4 c = *reinterpret_cast<const int4*>(tid_sh + cb * 16 + 4 * i);
+            sc[4 * i] = a.x, sc[4 * i + 1] = a.y, sc[4 * i + 2] = a.z, sc[4 * i + 3] = a.w;
+            rf[4 * i] = b.x, rf[4 * i + 1] = b.y, rf[4 * i + 2] = b.z, rf[4 * i + 3] = b.w;
+            id[4 * i] = c.x, id[4 * i + 1] = c.y, id[4 * i + 2] = c.z, id[4 * i + 3] = c.w;
+          }
+  #pragma unroll
+          for (int u = 0; u < 16; ++u) tq[u] = gtab[(cb * 16 + u) * 64 + r64];
+  #pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const float g = __fmul_rn(__fmul_rn((float)tq[u], sc[u]), es);
+            val[u] = id[u] >= 0 ? pv[cb * 16 + u] * rf[u] * nw + g : 0.f;
+          }
+  #pragma unroll
+          for (int u = 0; u < 16; ++u) tile[(cb * 16 + u) * 64 + r64] = val[u];
+        }
+      }
+      tc::fence_proxy_async();   // the tile (and the zeroed table rows) before the tensor stores read them
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (ct == 0 && ok) {
+        const int x = row0 + 64 * kh;   // 64 f32 = 256 bytes, 64 int8: 16-byte aligned
+        tc::tma_store_2d(&p.tm_out, x, t0, tc::smem_u32(recv));
+        if (p.gathered) tc::tma_store_2d(&p.tm_gat, x, t0, tc::smem_u32(gtab));
+        tc::bulk_commit();
+        tc::bulk_wait_read_all();   // the tile has been read; the writes complete with the grid
+      }
+      if (mine && (q & 1) == 0 && lane == 0) stamp(kTraceRows - 2, 3);
+      if (ct == 0) stamp(kTraceRows - 1, 7);
     }
-    tc::fence_proxy_async();   // the tile (and the zeroed table rows) before the tensor stores read them
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (ct == 0 && ok) {
-      const int x = row0 + 64 * kh;   // 64 f32 = 256 bytes, 64 int8: 16-byte aligned
-      tc::tma_store_2d(&p.tm_out, x, t0, tc::smem_u32(recv));
-      if (p.gathered) tc::tma_store_2d(&p.tm_gat, x, t0, tc::smem_u32(gtab));
-      tc::bulk_commit();
-      tc::bulk_wait_read_all();   // the tile has been read; the writes complete with the grid
-    }
-    if (mine && (q & 1) == 0 && lane == 0) stamp(kTraceRows - 2, 3);
-    if (ct == 0) stamp(kTraceRows - 1, 7);
   }
   if (warp < kEpi0) {   // the TMA and MMA warps take part in every cluster phase too
     tc::cluster_wait();
