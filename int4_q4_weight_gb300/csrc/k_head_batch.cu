@@ -75,32 +75,47 @@ __global__ void __launch_bounds__(kThr) head_batch_kernel(const uint8_t* __restr
   // giving the chunk's four pairs and its even / odd column sums; the four
   // chunks of a block sit in adjacent lanes and add by shuffles (the same
   // order as the single-vector engine).  Rows b >= B are zero.
+  // Up to kLB 16-byte loads of a thread are issued before any is used, so
+  // their L2 round trips overlap instead of following one another.
   const int nch = nb * 4;
-  for (int e0 = 0; e0 < NBP * nch; e0 += kThr) {   // uniform trip count: the shuffles use the full mask
-    const int e = e0 + threadIdx.x;
-    const bool in = e < NBP * nch;
-    const int i = e & 3, j = (e >> 2) % nb, b = (e >> 2) / nb;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (in && b < B) v = __ldg(reinterpret_cast<const uint4*>(h + (size_t)b * K + 32 * j + 8 * i));
-    float pe = 0.f, po = 0.f;
-    const uint32_t hv[4] = {v.x, v.y, v.z, v.w};   // hv[q] = (x[8i+2q], x[8i+2q+1])
+  constexpr int kLB = 4;
+  for (int e00 = 0; e00 < NBP * nch; e00 += kLB * kThr) {   // uniform trip counts: the shuffles use the full mask
+    uint4 vv[kLB];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hv[q]));
-      pe += f.x;
-      po += f.y;
+    for (int u = 0; u < kLB; ++u) {
+      const int e = e00 + u * kThr + threadIdx.x;
+      const int i = e & 3, j = (e >> 2) % nb, b = (e >> 2) / nb;
+      vv[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (e < NBP * nch && b < B) vv[u] = __ldg(reinterpret_cast<const uint4*>(h + (size_t)b * K + 32 * j + 8 * i));
     }
-    pe += __shfl_xor_sync(0xffffffffu, pe, 1);
-    po += __shfl_xor_sync(0xffffffffu, po, 1);
-    pe += __shfl_xor_sync(0xffffffffu, pe, 2);
-    po += __shfl_xor_sync(0xffffffffu, po, 2);
-    if (in) {
-      uint32_t* dst = xw + j * xstride + (4 * i) * NBP + b;
-      dst[0 * NBP] = __byte_perm(hv[0], hv[2], 0x5410);   // (x[8i], x[8i+4])
-      dst[1 * NBP] = __byte_perm(hv[0], hv[2], 0x7632);   // (x[8i+1], x[8i+5])
-      dst[2 * NBP] = __byte_perm(hv[1], hv[3], 0x5410);   // (x[8i+2], x[8i+6])
-      dst[3 * NBP] = __byte_perm(hv[1], hv[3], 0x7632);   // (x[8i+3], x[8i+7])
-      if (i == 0) xb[j * NBP + b] = kBiasEven * pe + kBiasOdd * po;
+#pragma unroll
+    for (int u = 0; u < kLB; ++u) {
+      const int e0 = e00 + u * kThr;
+      if (e0 >= NBP * nch) break;   // uniform
+      const int e = e0 + threadIdx.x;
+      const bool in = e < NBP * nch;
+      const int i = e & 3, j = (e >> 2) % nb, b = (e >> 2) / nb;
+      const uint4 v = vv[u];
+      float pe = 0.f, po = 0.f;
+      const uint32_t hv[4] = {v.x, v.y, v.z, v.w};   // hv[q] = (x[8i+2q], x[8i+2q+1])
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hv[q]));
+        pe += f.x;
+        po += f.y;
+      }
+      pe += __shfl_xor_sync(0xffffffffu, pe, 1);
+      po += __shfl_xor_sync(0xffffffffu, po, 1);
+      pe += __shfl_xor_sync(0xffffffffu, pe, 2);
+      po += __shfl_xor_sync(0xffffffffu, po, 2);
+      if (in) {
+        uint32_t* dst = xw + j * xstride + (4 * i) * NBP + b;
+        dst[0 * NBP] = __byte_perm(hv[0], hv[2], 0x5410);   // (x[8i], x[8i+4])
+        dst[1 * NBP] = __byte_perm(hv[0], hv[2], 0x7632);   // (x[8i+1], x[8i+5])
+        dst[2 * NBP] = __byte_perm(hv[1], hv[3], 0x5410);   // (x[8i+2], x[8i+6])
+        dst[3 * NBP] = __byte_perm(hv[1], hv[3], 0x7632);   // (x[8i+3], x[8i+7])
+        if (i == 0) xb[j * NBP + b] = kBiasEven * pe + kBiasOdd * po;
+      }
     }
   }
   __syncthreads();
@@ -277,8 +292,10 @@ int launch_gemv_batch_decoded(const uint8_t* codes, const __half* scales, const 
                               int batch, const DeviceInfo& dev, cudaStream_t s) {
   if (batch < 2 || batch > 8 || head_batch_smem(batch, K) > (size_t)220 * 1024)
     return fail(Q4_ERR_SHAPE, "batched GEMV: batch %d x K %d does not fit", batch, K);
+  // one CTA per (kThr / P) rows: CTAs past the last row would only stage x
   int grid = 2 * dev.sms;
-  const int need = (N + 7) / 8;
+  const int rows_per_cta = hb::kThr >> head_batch_lgp(K >> 5);
+  const int need = (N + rows_per_cta - 1) / rows_per_cta;
   if (grid > need) grid = need;
   return launch_head_batch(codes, scales, x, batch, N, K, 1.f, nullptr, nullptr, nullptr, nullptr, nullptr,
                            nullptr, grid, s, y);
