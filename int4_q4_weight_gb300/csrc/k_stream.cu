@@ -88,14 +88,17 @@ __device__ __forceinline__ bool aborting(const Ctl& c) {
 }
 
 // Bounded mbarrier wait; false on expiry (raises the abort) or when aborting.
-// The shared abort flag is read every iteration; the grid-wide flag (a
-// global load, about an L2 round trip) and the clock on the first retry and
-// then every 256 (so a zero budget gives up at once).
+// A retry suspends the thread in try_wait (up to kRetrySuspendNs, woken when
+// the phase completes), so waiting warps do not poll.  The shared abort flag
+// is read every iteration; the grid-wide flag (a global load, about an L2
+// round trip) and the clock on the first retry and then every 256 (so a zero
+// budget gives up at once).
+constexpr uint32_t kRetrySuspendNs = 20000;
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, const Ctl& c) {
   if (mbar_probe(a, parity)) return true;
   const long long t0 = clock64();
   for (unsigned it = 1;; ++it) {
-    if (mbar_test(a, parity)) return true;
+    if (tc::mbar_test_for(a, parity, kRetrySuspendNs)) return true;
     if (*c.abort_cta) return false;
     if ((it & 255u) == 1) {   // first failed retry, then every 256
       if (c.abort_grid && *(volatile int*)c.abort_grid) return false;
