@@ -337,6 +337,27 @@ __device__ __forceinline__ float xform(float v, int mode, float r, float r2) {
 // false when aborting (uniform over the consumers).  kDirect: an untagged
 // fp16 input with no normalisation may be read straight from global memory
 // (single-stage kernels; the persistent pass never has such an input).
+// One staged 8-byte group -- four fp16 values packed as two half pairs, or
+// two floats -- added into a sum of squares in one fixed order.  The tagged
+// and the untagged staging both stage 8-byte groups v = tid, tid + kCT, ...
+// per thread and add them here, so the persistent pass and the stage-by-stage
+// launches form the same sums while the input is read.
+__device__ __forceinline__ float group_sq(uint2 p, bool f16, float acc) {
+  if (f16) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&p.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&p.y));
+    acc = fmaf(a.x, a.x, acc);
+    acc = fmaf(a.y, a.y, acc);
+    acc = fmaf(b.x, b.x, acc);
+    acc = fmaf(b.y, b.y, acc);
+  } else {
+    const float a = __uint_as_float(p.x), b = __uint_as_float(p.y);
+    acc = fmaf(a, a, acc);
+    acc = fmaf(b, b, acc);
+  }
+  return acc;
+}
+
 template <bool kDirect>
 __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, float* red8, const Ctl& c) {
   const int tid = threadIdx.x, K = a.K, mode = a.in_mode;
@@ -350,16 +371,28 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, float* red8, cons
   // thread takes its 8-element chunks straight from global memory
   const bool direct = kDirect && a.in_tag == 0 && mode == Q4_IN_F16;
   float r = 1.f, r2 = 1.f;
+  float ssq = 0.f;   // this thread's share of the sum of squares, formed while staging
   if (staged) {
     bool ok = true;
     if (a.in_tag == 0) {
       if (!direct) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.in);
-        if (f16in) {
+        uint2* dst32 = reinterpret_cast<uint2*>(st32);
+        if (mode == Q4_IN_F16) {   // no sum of squares needed: 16-byte loads
+          const uint4* src = reinterpret_cast<const uint4*>(a.in);
           for (int v = tid; v < K / 8; v += kCT) *reinterpret_cast<uint4*>(home16(v)) = ldcg_v4(src + v);
         } else {
-          uint4* dst = reinterpret_cast<uint4*>(st32);
-          for (int v = tid; v < K / 4; v += kCT) dst[v] = ldcg_v4(src + v);
+          // 8-byte groups, as the tagged staging takes them
+          const uint2* src = reinterpret_cast<const uint2*>(a.in);
+          const int nv = f16in ? K / 4 : K / 2;
+          for (int v = tid; v < nv; v += kCT) {
+            uint2 g;
+            asm volatile("ld.global.cg.v2.u32 {%0,%1}, [%2];" : "=r"(g.x), "=r"(g.y) : "l"(src + v));
+            if (f16in)
+              *reinterpret_cast<uint2*>(home16(v >> 1) + 2 * (v & 1)) = g;
+            else
+              dst32[v] = g;
+            ssq = group_sq(g, f16in, ssq);
+          }
         }
       }
     } else {
@@ -382,11 +415,13 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, float* red8, cons
           if (v < nv && ok) {
             if (!tags_ready(u[i], f16in, tag)) ok = poll_tags(src + v, u[i], f16in, tag, c);
             // fp16: group v is half (v & 1) of chunk v >> 1
+            const uint2 g = f16in ? make_uint2(__byte_perm(u[i].x, u[i].y, 0x5410), __byte_perm(u[i].z, u[i].w, 0x5410))
+                                  : make_uint2(u[i].x, u[i].z);
             if (f16in)
-              *reinterpret_cast<uint2*>(home16(v >> 1) + 2 * (v & 1)) =
-                  make_uint2(__byte_perm(u[i].x, u[i].y, 0x5410), __byte_perm(u[i].z, u[i].w, 0x5410));
+              *reinterpret_cast<uint2*>(home16(v >> 1) + 2 * (v & 1)) = g;
             else
-              dst32[v] = make_uint2(u[i].x, u[i].z);
+              dst32[v] = g;
+            ssq = group_sq(g, f16in, ssq);
           }
         }
       }
@@ -423,14 +458,7 @@ __device__ bool eng_prologue(const StageArgs& a, uint32_t* xh, float* red8, cons
       }
     };
     if (mode != Q4_IN_F16) {
-      float ss = 0.f;
-      for (int ch = tid; ch < nch; ch += kCT) {
-        float v[8];
-        load8(ch, v);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss += v[e] * v[e];
-      }
-      ss = consumer_sum1(ss, red8);
+      const float ss = consumer_sum1(ssq, red8);
       r = 1.f / sqrtf(ss / (float)K + a.eps);
       if (mode == Q4_IN_RMS2_F32) {
         float ss2 = 0.f;
