@@ -231,11 +231,13 @@ int ple_gather_project_q8(const int32_t* ids, int S, const int8_t* table,
  *   ws: q4_workspace_bytes(Q4_OP_LMHEAD, V, K, b) bytes; its contents on
  *   entry do not matter.  Calls that share one ws must not overlap.
  * Arithmetic: b = 1 sums exact products (fp32 accumulation).  For b >= 2
- * with V % 128 == 0, V >= 128 x (SM count) and K % 64 == 0, z is computed on
- * the tensor cores with each weight rounded once to fp16, fp16(d*(q-8)), and
- * fp32 accumulation (the workspace then also holds z, b*V floats); other
- * shapes sum exact products on the CUDA cores.  Either way each row's sum
- * has a fixed order: repeated calls give the same bits.                    */
+ * with V % 128 == 0, V >= 128 x (SM count), K % 64 == 0 and K <= 1984, z is
+ * computed on the tensor cores with each weight rounded once to fp16,
+ * fp16(d*(q-8)), and fp32 accumulation, and selected in the same kernel (z
+ * is not written unless logits_opt is given; the workspace then also holds
+ * the fp16 copy of h, 32 K bytes); other shapes sum exact products on the
+ * CUDA cores.  Either way each row's sum has a fixed order: repeated calls
+ * give the same bits.                                                       */
 int lmhead_softcap_argmax(const uint8_t* codes, const uint16_t* scales,
                           const uint16_t* h_f16, int b, int V, int K, float cap,
                           int32_t* idx, float* top1, float* top2, float* logits_opt,
@@ -254,7 +256,7 @@ int lmhead_softcap_argmax(const uint8_t* codes, const uint16_t* scales,
  * b.  A device with more than 255 SMs gets Q4_ERR_WORKSPACE.  (The figure
  * q4_workspace_bytes(Q4_OP_LMHEAD, ...) reports is the workspace entry
  * point's need, which for b >= 2 on a large vocabulary includes the
- * tensor-core path's logits; it is not this limit.)  The first call on a
+ * tensor-core path's token operand; it is not this limit.)  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with
  * that device current, and caches it per device without a lock: host threads
  * whose first calls on one device coincide all store the same address.  Make
