@@ -45,13 +45,18 @@
 // full) and empty (MMA commit) mbarriers; the MMA warp waits on bready alone.
 // The int8 form (ple_tc_kernel<true>; "Gemma-4 E2B mobile mixed-bit QAT
 // weights", decode recipe and official-checkpoint notes: the model projection
-// is int8 per block of 32) keeps the clusters, roles and epilogue.  A stage is
-// 128 K columns: the code tile [128 rows][128 int8] and two hidden tiles
-// [64 tokens][64 fp16] (128-byte swizzle, the B operand as loaded) come from
-// TMA; warps 2-9 widen the codes to fp16(scale * code) into two swizzled A
-// halves, and 8 MMAs of kind::f16 follow (3 stages of 64 KB: A 32 KB, B 16 KB,
-// codes 16 KB; the block scales of the CTA's rows sit in shared memory).  The
-// K halves of a cluster take alternate 128-column units.
+// is int8 per block of 32) keeps the clusters and the epilogue.  A stage is
+// 128 K columns: the code tile [128 rows][128 int8] (128-byte swizzle) and two
+// hidden tiles [64 tokens][64 fp16] (128-byte swizzle, the B operand as
+// loaded) come from TMA into one of six 32 KB slots, so a K half of D = 1536
+// is in flight at once; two groups of four converter warps (2-5, 6-9) take
+// alternate stages and widen the codes to fp16(scale * code) straight into
+// one of four 64-column A stages in tensor memory (thread = projection row =
+// TMEM lane), and 8 MMAs of kind::f16 with A in tensor memory follow (the
+// block scales of the CTA's rows sit in shared memory).  A slot is free again
+// once its group has read the codes and the MMAs have read the hidden tile;
+// an A stage once its MMAs have completed.  The K halves of a cluster take
+// alternate 128-column units.
 //
 // In both forms the token ids, table copies and table scales are handled by
 // warps 2-5 while the first tiles load, and the epilogue reads each row's 64
@@ -84,7 +89,6 @@ constexpr int kRecvBytes = kTok * 64 * 4;           // partner's partial sums of
 constexpr int kGtabBytes = kTok * 64;               // table bytes of the 64 finished rows per token
 constexpr int kEpi0 = 2;                            // first converter / epilogue warp
 constexpr int kConvWarps = 8;                       // converter warps: 2-5 (also the epilogue) and 6-9
-constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kThreads = (kEpi0 + kConvWarps) * 32;   // 320
 constexpr int kCluster = 4;
 constexpr long long kDrainCycles = 2000000000LL;
@@ -94,24 +98,25 @@ constexpr long long kDrainCycles = 2000000000LL;
 // operands are two 64-column halves, each a 128-byte row of fp16 per operand
 // row in the 128-byte swizzle.
 constexpr int kQC = 128;                            // K columns per stage
-constexpr int kQStages = 3;
-constexpr int kQAHalf = kRows * 64 * 2;             // 16 KB: fp16 weights of 64 columns
+constexpr int kQR = 6;                              // raw slots (a K half of D = 1536 stays resident)
+constexpr int kQA = 4;                              // A stages in tensor memory
 constexpr int kQBHalf = kTok * 64 * 2;              // 8 KB: fp16 hidden of 64 columns (tensor load)
-constexpr int kQABytes = 2 * kQAHalf;
 constexpr int kQBBytes = 2 * kQBHalf;
-constexpr int kQRawBytes = kRows * kQC;             // 16 KB int8 codes [128 rows][128]
-constexpr int kQStageBytes = kQABytes + kQBBytes + kQRawBytes;   // 64 KB, a multiple of 1024
+constexpr int kQRawBytes = kRows * kQC;             // 16 KB int8 codes [128 rows][128], 128-byte swizzle
+constexpr int kQSlotBytes = kQBBytes + kQRawBytes;  // 32 KB, a multiple of 1024
+constexpr int kQACol0 = 64;                         // TMEM: the accumulator, then kQA A stages of 64 columns
 constexpr int kQMaxStages = 8;                      // stages per K half: D <= 2048
 constexpr int kQScBytes = kQMaxStages * kRows * 8;  // per (stage, row): the stage's four fp16 scales
 
 template <bool Q8>
 constexpr size_t ring_bytes() {
-  return Q8 ? (size_t)kQStages * kQStageBytes : (size_t)kFStages * kFStageBytes;
+  return Q8 ? (size_t)kQR * kQSlotBytes : (size_t)kFStages * kFStageBytes;
 }
-// TMEM columns: one 64-column accumulator (int8 form) or two (f32 pieces)
+// TMEM columns: two 64-column accumulators (f32 pieces), or one plus the A
+// stages (int8 form: 64 + 4 x 64)
 template <bool Q8>
 constexpr int tmem_cols() {
-  return Q8 ? 64 : 128;
+  return Q8 ? 512 : 128;
 }
 template <bool Q8>
 constexpr size_t smem_bytes() {
@@ -129,6 +134,16 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+// D (+)= A . B with A in tensor memory (128 lanes x 8 columns per K = 16).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accum)
       : "memory");
 }
 
@@ -177,7 +192,7 @@ __device__ __forceinline__ void split_f32_f16(const float (&w)[8], uint4& p1, ui
 
 struct Params {
   CUtensorMap tm_proj;   // f32 [L*ld][D], box [128 rows][32], 128-byte swizzle;
-                         // int8 form: codes [L*ld][D], box [128 rows][64], no swizzle
+                         // int8 form: codes [L*ld][D], box [128 rows][128], 128-byte swizzle
   CUtensorMap tm_hid;    // fp16 bits [S][D], box [64 rows][64], 128-byte swizzle; rows past S
                          // and columns past D read as zero
   CUtensorMap tm_out;    // f32 out [S][L*ld], box [64 tokens][64 columns]; rows past S not written
@@ -223,8 +238,8 @@ using tc::elect_one;
 // tile then goes to the tensor core straight from its tensor load).
 template <bool Q8>
 __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_constant__ Params p) {
-  constexpr int kSt = Q8 ? kQStages : kFStages;            // ring stages
-  constexpr int kStB = Q8 ? kQStageBytes : kFStageBytes;   // bytes per stage
+  constexpr int kSt = Q8 ? kQR : kFStages;                 // ring slots
+  constexpr int kStB = Q8 ? kQSlotBytes : kFStageBytes;    // bytes per slot
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   // partner's partial sums, [token / 4][64 rows][4 tokens]
@@ -233,7 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   int8_t* gtab = reinterpret_cast<int8_t*>(smem + ring_bytes<Q8>() + kRecvBytes);
   // Q8: per (stage, row) the stage's four block scales, [stage][128 rows]
   uint2* scs = reinterpret_cast<uint2*>(smem + ring_bytes<Q8>() + kRecvBytes + kGtabBytes);
-  __shared__ __align__(8) uint64_t bars[3 * kSt + 3];   // full, bready, empty, accfull, drain, gbar
+  // f32: full, bready, empty [kSt each]; int8: full, rempty [kQR each], aready,
+  // aempty [kQA each]; then accfull, drain, gbar
+  constexpr int kNB = Q8 ? 2 * kQR + 2 * kQA + 3 : 3 * kSt + 3;
+  __shared__ __align__(8) uint64_t bars[kNB];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
   __shared__ long long t0_sh;
@@ -259,7 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   const int ns = Q8 ? (nsub + 1 - kh) / 2 : se - sb;   // my stages (0 only when D has one unit)
   const int PLD = p.L * kLd;
   const uint32_t full0 = tc::smem_u32(bars), bready0 = full0 + 8 * kSt, empty0 = bready0 + 8 * kSt;
-  const uint32_t accfull = empty0 + 8 * kSt, drain = accfull + 8, gbar = drain + 8;
+  const uint32_t rempty0 = bready0;                       // int8: raw slot read (converters + MMA)
+  const uint32_t aready0 = full0 + 16 * kQR, aempty0 = aready0 + 8 * kQA;   // int8: A stages
+  const uint32_t accfull = full0 + 8 * (kNB - 3), drain = accfull + 8, gbar = drain + 8;
   volatile int* abort_flag = &abort_sh;
   unsigned long long* const tr = (p.trace && blockIdx.x == 0 && blockIdx.y == 0) ? p.trace : nullptr;
   // with a trace: every CTA's start and end (globaltimer ns) after the stage stamps
@@ -273,14 +293,25 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     abort_sh = 0;
     t0_sh = tc::clock_ordered();
     if (trc) trc[0] = tc::globaltimer();
-    for (int s = 0; s < kSt; ++s) {
-      tc::mbar_init(full0 + 8 * s, 1);
-      tc::mbar_init(bready0 + 8 * s, kConvWarps);
-      tc::mbar_init(empty0 + 8 * s, 1);
+    if constexpr (Q8) {
+      for (int s = 0; s < kQR; ++s) {
+        tc::mbar_init(full0 + 8 * s, 1);
+        tc::mbar_init(rempty0 + 8 * s, 4 + 1);   // the stage's converter group, then the MMA commit
+      }
+      for (int s = 0; s < kQA; ++s) {
+        tc::mbar_init(aready0 + 8 * s, 4);
+        tc::mbar_init(aempty0 + 8 * s, 1);
+      }
+    } else {
+      for (int s = 0; s < kSt; ++s) {
+        tc::mbar_init(full0 + 8 * s, 1);
+        tc::mbar_init(bready0 + 8 * s, kConvWarps);
+        tc::mbar_init(empty0 + 8 * s, 1);
+      }
     }
     tc::mbar_init(accfull, 1);
     tc::mbar_init(drain, 1);
-    tc::mbar_init(gbar, 1);
+    tc::mbar_init(gbar, kTok);   // one arrival per token slot
     tc::mbar_fence_init();
   }
   if (warp == 1) tc::tmem_alloc(tc::smem_u32(&tmem_sh), tmem_cols<Q8>());
@@ -304,18 +335,19 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     int st = 0;
     for (; st < ns; ++st) {
       const int s = st % kSt, round = st / kSt;
-      const bool free_ = tc::mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, p.dev_err);
+      const bool free_ =
+          tc::mbar_wait((Q8 ? rempty0 : empty0) + 8 * s, (round & 1) ^ 1, p.wait_limit, abort_flag, p.dev_err);
       if (!__all_sync(0xffffffffu, free_)) break;
       if constexpr (Q8) {
         if (elect_one()) {
-          const uint32_t A = st0 + s * kStB;
+          const uint32_t B = st0 + s * kStB;
           stamp(st, 0);
           tc::mbar_expect_tx(full0 + 8 * s, (uint32_t)(kQRawBytes + kQBBytes));
           // x = 128 (2 st + kh) int8 code bytes / fp16 hidden columns (+ 64): 16-byte aligned
           const int x = (2 * st + kh) * kQC;
-          tc::tma_load_2d(A + kQABytes + kQBBytes, &p.tm_proj, x, row0, full0 + 8 * s, pol_once);
-          tc::tma_load_2d(A + kQABytes, &p.tm_hid, x, t0, full0 + 8 * s, pol_keep);
-          tc::tma_load_2d(A + kQABytes + kQBHalf, &p.tm_hid, x + 64, t0, full0 + 8 * s, pol_keep);
+          tc::tma_load_2d(B + kQBBytes, &p.tm_proj, x, row0, full0 + 8 * s, pol_once);
+          tc::tma_load_2d(B, &p.tm_hid, x, t0, full0 + 8 * s, pol_keep);
+          tc::tma_load_2d(B + kQBHalf, &p.tm_hid, x + 64, t0, full0 + 8 * s, pol_keep);
         }
       } else if (elect_one()) {
         const uint32_t A = st0 + s * kFStageBytes;
@@ -341,9 +373,13 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     bool ok = true;
     for (int st = 0; st < ns; ++st) {
       const int s = st % kSt, round = st / kSt;
-      // bready completes only after the converter warps have seen this
-      // stage's TMA bytes land (full), so it orders the projection tile too
-      ok = tc::mbar_wait(bready0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
+      const int a = st % kQA;   // int8: the A stage in tensor memory
+      // bready (aready) completes only after the converter warps have seen
+      // this stage's TMA bytes land (full), so it orders the tiles too
+      if constexpr (Q8)
+        ok = tc::mbar_wait(aready0 + 8 * a, (st / kQA) & 1, p.wait_limit, abort_flag, p.dev_err);
+      else
+        ok = tc::mbar_wait(bready0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -352,13 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
       if (elect_one()) {
         stamp(st, 3);
         if constexpr (Q8) {
-          const uint32_t A = st0 + s * kStB, B = A + kQABytes;
+          // K step k (16 columns): A columns 8k .. 8k + 7 of stage a; B half
+          // k / 4 at byte 32 (k % 4) of each 128-byte row
+          const uint32_t B = st0 + s * kStB, A = tmem + kQACol0 + 64 * a;
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)   // K = 16 fp16 (32 bytes) per MMA
-              mma_f16(tmem, tc::desc_sw128(A + h * kQAHalf + 32 * k), tc::desc_sw128(B + h * kQBHalf + 32 * k), idesc,
-                      (st | h | k) ? 1u : 0u);
+          for (int k = 0; k < 8; ++k)
+            mma_f16_ta(tmem, A + 8 * k, tc::desc_sw128(B + (k >> 2) * kQBHalf + 32 * (k & 3)), idesc,
+                       (st | k) ? 1u : 0u);
+          tc::commit(aempty0 + 8 * a);
+          tc::commit(rempty0 + 8 * s);
         } else {
           // D1 (columns 0-63) += P1 . h, D2 (columns 64-127) += P2 . h; K
           // step k (16 columns) of piece h sits in box k / 2 at byte
@@ -370,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
             for (int k = 0; k < 4; ++k)   // K = 16 fp16 (32 bytes) per MMA
               mma_f16(tmem + 64 * h, tc::desc_sw128(A + (k >> 1) * kFBox + 64 * h + 32 * (k & 1)),
                       tc::desc_sw128(H + 32 * k), idesc, (st | k) ? 1u : 0u);
+          tc::commit(empty0 + 8 * s);
         }
-        tc::commit(empty0 + 8 * s);
         stamp(st, 4);
       }
       __syncwarp();
@@ -390,9 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     const bool epi = cv < 128;
     // token ct's id; the table bytes of the finished rows: one 64-byte copy
     // per valid token, issued by that token's thread (column row0 + 64 kh and
-    // the row width L * 256 are multiples of 16 bytes); thread 0 posts the
-    // byte count.  The token's table scale is only needed by the epilogue:
-    // its load stays in flight through the stage loop.
+    // the row width L * 256 are multiples of 16 bytes) after it has posted
+    // the 64 bytes on gbar; every token slot arrives once, so no thread has to
+    // count the valid ids.  The token's table scale is only needed by the
+    // epilogue: its load stays in flight through the stage loop.
     int my_id = -1;
     float my_sc = 0.f;
     if (epi && ct < ntok) {
@@ -405,63 +444,85 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     if (epi && ct < kTok) {
       tid_sh[ct] = my_id;
       if (my_id >= 0) {
+        tc::mbar_expect_tx(gbar, 64u);
         tc::bulk_load(tc::smem_u32(gtab + ct * 64), p.table + (size_t)my_id * PLD + (size_t)row0 + 64 * kh, 64,
                       gbar, tc::policy_evict_first());
         my_sc = p.row_scale[my_id];
       } else {   // no copy: the gathered bytes are zero
         for (int e = 0; e < 64; e += 16) *reinterpret_cast<uint4*>(gtab + ct * 64 + e) = make_uint4(0u, 0u, 0u, 0u);
+        tc::mbar_arrive(gbar);
       }
     }
     if constexpr (Q8) {
-      // the block scales of this CTA's rows over its stages (row stride D/128
-      // quads), all loads in flight together
-      if (epi) {
-        const uint2* src = p.proj_sc + (size_t)(row0 + ct) * (p.D / kQC) + kh;
-        uint2 v[kQMaxStages];
+      // the block scales of the row this thread converts, for the stages of
+      // its group (row stride D/128 quads), all loads in flight together;
+      // the thread reads back only what it wrote, so no barrier is needed
+      const int grp = (warp - kEpi0) >> 2, r = 32 * (warp & 3) + lane;
+      const uint2* src = p.proj_sc + (size_t)(row0 + r) * (p.D / kQC) + kh;
+      uint2 v[kQMaxStages / 2];
 #pragma unroll
-        for (int u = 0; u < kQMaxStages; ++u) v[u] = u < ns ? __ldg(src + 2 * u) : make_uint2(0u, 0u);
+      for (int u = 0; u < kQMaxStages / 2; ++u)
+        v[u] = grp + 2 * u < ns ? __ldg(src + 2 * (grp + 2 * u)) : make_uint2(0u, 0u);
 #pragma unroll
-        for (int u = 0; u < kQMaxStages; ++u)
-          if (u < ns) scs[u * kRows + ct] = v[u];
-      }
-    }
-    // every id (and block scale) is in shared memory
-    asm volatile("bar.sync 2, %0;" ::"n"(kConvThreads) : "memory");
-    if (ct == 0) {
-      uint32_t nb = 0;
-      for (int t = 0; t < ntok; ++t) nb += tid_sh[t] >= 0 ? 64u : 0u;
-      tc::mbar_expect_tx(gbar, nb);
+      for (int u = 0; u < kQMaxStages / 2; ++u)
+        if (grp + 2 * u < ns) scs[(grp + 2 * u) * kRows + r] = v[u];
     }
     bool ok = true;
     if constexpr (Q8) {
-      // ------------------------------- A operand: int8 codes -> fp16 tile
-      for (int st = 0; st < ns; ++st) {
-        const int s = st % kSt, round = st / kSt;
+      // ------------------------ A operand: int8 codes -> fp16 tensor memory
+      // two groups of four warps take alternate stages; thread = projection
+      // row r (its warp's TMEM lane quarter): it reads the row's 128 codes
+      // (8 swizzled 16-byte groups: a quarter-warp of eight consecutive rows
+      // hits eight distinct bank groups), releases the raw slot, and writes
+      // the 64 columns of fp16 pairs of its lane in the stage's A columns
+      const int grp = (warp - kEpi0) >> 2;
+      const int r = 32 * (warp & 3) + lane, r8 = r & 7;
+      const uint32_t a_lane = tmem + kQACol0 + ((uint32_t)(32 * (warp & 3)) << 16);
+      for (int st = grp; st < ns; st += 2) {
+        const int s = st % kSt, round = st / kSt, a = st % kQA;
         const bool landed = tc::mbar_wait(full0 + 8 * s, round & 1, p.wait_limit, abort_flag, p.dev_err);
         if (!__all_sync(0xffffffffu, landed)) {   // leave the loop as a whole warp
           ok = false;
           break;
         }
         if (ct == 0) stamp(st, 1);
-        uint8_t* A = smem + (size_t)s * kStB;
-        const uint8_t* raw = A + kQABytes + kQBBytes;
-        // (row r, 8-column group j of its 128 columns): j = cv % 16 is fixed
-        // per thread, so is its block (j / 4) and operand half (j / 8)
-        const int j = cv & 15, jj = j & 7, h = j >> 3, blk = j >> 2;
+        const uint8_t* raw = smem + (size_t)s * kStB + kQBBytes + r * kQC;
+        uint4 c[8];
 #pragma unroll
-        for (int i = 0; i < 128 / (kConvThreads / 16); ++i) {
-          const int r = (cv >> 4) + (kConvThreads / 16) * i;
-          const uint2 c = *reinterpret_cast<const uint2*>(raw + r * kQC + j * 8);
-          const uint2 s4 = scs[st * kRows + r];   // scales of columns 0-31, 32-63 (x), 64-95, 96-127 (y)
-          const uint32_t sw = blk < 2 ? s4.x : s4.y;
-          const __half2 dd = __half2half2(__ushort_as_half((uint16_t)((blk & 1) ? sw >> 16 : sw & 0xFFFFu)));
-          // 128-byte swizzle: group jj of row r sits at group jj ^ (r % 8) of its row
-          *reinterpret_cast<uint4*>(A + h * kQAHalf + (r >> 3) * 1024 + (r & 7) * 128 + ((jj ^ (r & 7)) << 4)) =
-              dequant_i8_f16(c, dd);
-        }
-        tc::fence_proxy_async();
+        for (int g = 0; g < 8; ++g) c[g] = *reinterpret_cast<const uint4*>(raw + ((g ^ r8) << 4));
+        const uint2 s4 = scs[st * kRows + r];   // scales of columns 0-31, 32-63 (x), 64-95, 96-127 (y)
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(bready0 + 8 * s);
+        if (lane == 0) tc::mbar_arrive(rempty0 + 8 * s);
+        const bool freed = tc::mbar_wait(aempty0 + 8 * a, ((st / kQA) & 1) ^ 1, p.wait_limit, abort_flag, p.dev_err);
+        if (!__all_sync(0xffffffffu, freed)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {   // columns 64 hh .. 64 hh + 63: blocks 2 hh, 2 hh + 1
+          const uint32_t sw = hh ? s4.y : s4.x;
+          uint32_t v[32];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const __half2 dd = __half2half2(__ushort_as_half((uint16_t)(g < 2 ? sw & 0xFFFFu : sw >> 16)));
+            const uint4 cc = c[4 * hh + g];
+            const uint4 lo = dequant_i8_f16(make_uint2(cc.x, cc.y), dd);
+            const uint4 hi = dequant_i8_f16(make_uint2(cc.z, cc.w), dd);
+            v[8 * g + 0] = lo.x;
+            v[8 * g + 1] = lo.y;
+            v[8 * g + 2] = lo.z;
+            v[8 * g + 3] = lo.w;
+            v[8 * g + 4] = hi.x;
+            v[8 * g + 5] = hi.y;
+            v[8 * g + 6] = hi.z;
+            v[8 * g + 7] = hi.w;
+          }
+          tc::tmem_st32(a_lane + 64 * a + 32 * hh, v);
+        }
+        tc::fence_before();   // this warp's TMEM stores, before the MMA issuer reads them
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(aready0 + 8 * a);
         if (ct == 0) stamp(st, 2);
       }
     } else {
@@ -688,7 +749,7 @@ static int launch_ple_t(const int32_t* ids, int S, const int8_t* table, const fl
   int st;
   if (Q8) {
     st = encode_tensor_2d(&p.tm_proj, proj, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)D, (uint64_t)L * ld, ple::kQC,
-                          ple::kRows, CU_TENSOR_MAP_SWIZZLE_NONE, "proj_codes");
+                          ple::kRows, CU_TENSOR_MAP_SWIZZLE_128B, "proj_codes");
     if (st != Q4_OK) return st;
     st = encode_tensor_2d(&p.tm_hid, hidden, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)D, (uint64_t)S, 64,
                           ple::kTok, CU_TENSOR_MAP_SWIZZLE_128B, "hidden");
