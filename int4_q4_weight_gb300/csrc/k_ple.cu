@@ -22,8 +22,12 @@
 // sends its per-token sum of squares over its 64 finished rows to all four,
 // so each finishes the chunk's RMSNorm for its own rows, adds the gathered
 // table term, and writes its [64 tokens][64 columns] output tile (and the
-// gathered bytes) from shared memory with tensor stores.  The table bytes of
-// those columns are fetched at the start by one 64-byte bulk copy per token.
+// gathered bytes) from shared memory with tensor stores.  Both exchanges are
+// stores into the peers' shared memory that count their bytes on an mbarrier
+// of the receiving CTA (st.async), so after the one cluster barrier at the
+// start (every peer running) a CTA waits only for the data it needs.  The
+// table bytes of those columns are fetched at the start by one 64-byte bulk
+// copy per token.
 //
 // Warp roles (320 threads):
 //   warp 0     TMA loads (one elected lane): per stage of 64 K columns the
@@ -65,8 +69,10 @@
 // overlaps the previous kernel, its first reads of inputs come after
 // griddepcontrol.wait.  Every mbarrier wait is bounded; on expiry the CTA
 // sets its abort flag and the device error word, every role leaves its loop,
-// work in flight is drained, and all four CTAs still meet at every cluster
-// barrier, so none waits for a partner that has given up.
+// work in flight is drained, and every CTA still sends its partial sums and
+// sums of squares, so each receiver's byte count is met; a CTA drains its
+// receive barriers before it leaves, so no peer stores into a CTA that has
+// gone.
 #include "q4w_device.cuh"
 #include "q4w_internal.cuh"
 #include "q4w_tc.cuh"
@@ -249,8 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   // Q8: per (stage, row) the stage's four block scales, [stage][128 rows]
   uint2* scs = reinterpret_cast<uint2*>(smem + ring_bytes<Q8>() + kRecvBytes + kGtabBytes);
   // f32: full, bready, empty [kSt each]; int8: full, rempty [kQR each], aready,
-  // aempty [kQA each]; then accfull, drain, gbar
-  constexpr int kNB = Q8 ? 2 * kQR + 2 * kQA + 3 : 3 * kSt + 3;
+  // aempty [kQA each]; then accfull, drain, gbar, xbar (the partner's partial
+  // sums), sbar (the four sums of squares)
+  constexpr int kNB = Q8 ? 2 * kQR + 2 * kQA + 5 : 3 * kSt + 5;
   __shared__ __align__(8) uint64_t bars[kNB];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
@@ -279,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   const uint32_t full0 = tc::smem_u32(bars), bready0 = full0 + 8 * kSt, empty0 = bready0 + 8 * kSt;
   const uint32_t rempty0 = bready0;                       // int8: raw slot read (converters + MMA)
   const uint32_t aready0 = full0 + 16 * kQR, aempty0 = aready0 + 8 * kQA;   // int8: A stages
-  const uint32_t accfull = full0 + 8 * (kNB - 3), drain = accfull + 8, gbar = drain + 8;
+  const uint32_t accfull = full0 + 8 * (kNB - 5), drain = accfull + 8, gbar = drain + 8;
+  const uint32_t xbar = gbar + 8, sbar = xbar + 8;
   volatile int* abort_flag = &abort_sh;
   unsigned long long* const tr = (p.trace && blockIdx.x == 0 && blockIdx.y == 0) ? p.trace : nullptr;
   // with a trace: every CTA's start and end (globaltimer ns) after the stage stamps
@@ -312,6 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     tc::mbar_init(accfull, 1);
     tc::mbar_init(drain, 1);
     tc::mbar_init(gbar, kTok);   // one arrival per token slot
+    tc::mbar_init(xbar, 1);
+    tc::mbar_init(sbar, 1);
+    // the bytes the peers will store here: the partner's partial sums of the
+    // 64 rows finished here (npad tokens), and 64 sums of squares from each
+    // of the three other CTAs
+    tc::mbar_expect_tx(xbar, (uint32_t)(64 * 4 * npad));
+    tc::mbar_expect_tx(sbar, (uint32_t)((kCluster - 1) * kTok * 4));
     tc::mbar_fence_init();
   }
   if (warp == 1) tc::tmem_alloc(tc::smem_u32(&tmem_sh), tmem_cols<Q8>());
@@ -569,13 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
       }
     }
     if (!epi) {
-      // conversion-only warps take part in every cluster phase, like the
-      // TMA and MMA warps
-      tc::cluster_wait();
-      tc::cluster_arrive_release();
-      tc::cluster_wait();
-      tc::cluster_arrive_release();
-      tc::cluster_wait();
+      tc::cluster_wait();   // conversion-only warps: the one cluster phase, like the TMA and MMA warps
     } else {
       // ----------------------------------------------------------- epilogue
       if (ct < kTok) tsc[ct] = my_sc;            // read after the barriers below
@@ -603,24 +612,30 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
   #pragma unroll
         for (int u = 0; u < kTok; ++u) acc[u] = 0.f;
       }
-      tc::cluster_wait();                        // phase 1: every peer is running
+      tc::cluster_wait();                        // every peer is running (its barriers initialised)
       if (ct == 0) stamp(kTraceRows - 2, 0);
+      // Partial sums and sums of squares go to the peers as stores that count
+      // their bytes on the receiver's xbar / sbar; they are sent even after a
+      // failed wait (with whatever values), so every receiver's byte count is
+      // met and no CTA leaves while a peer may still store into it.
       if (!mine) {                               // the partner finishes these rows
         const uint32_t peer = tc::cluster_addr(recv, (uint32_t)(rank ^ 2));
+        const uint32_t peer_bar = tc::cluster_addr(&bars[kNB - 2], (uint32_t)(rank ^ 2));
   #pragma unroll
         for (int cb = 0; cb < kTok / 16; ++cb) {
           if (cb < npad / 16) {
   #pragma unroll
             for (int g = 0; g < 4; ++g) {   // tokens 16 cb + 4 g .. + 3 of this row
               const int u = 16 * cb + 4 * g;
-              tc::st_cluster_v4(peer + (uint32_t)((((cb * 4 + g) * 64) + r64) * 16), acc[u], acc[u + 1], acc[u + 2],
-                                acc[u + 3]);
+              tc::st_async_v4(peer + (uint32_t)((((cb * 4 + g) * 64) + r64) * 16), acc[u], acc[u + 1], acc[u + 2],
+                              acc[u + 3], peer_bar);
             }
           }
         }
+      } else {                                   // the partner's partial sums of these rows
+        const bool g = tc::mbar_wait(xbar, 0, p.wait_limit, abort_flag, p.dev_err);
+        ok = __all_sync(0xffffffffu, ok && g);
       }
-      tc::cluster_arrive_release();
-      tc::cluster_wait();                        // phase 2: the partner's partial sums are here
       if (ct == 0) stamp(kTraceRows - 2, 1);
       // p = (K half 0) + (K half 1), the same order in both CTAs; the four token
       // groups' reductions are independent of one another
@@ -654,18 +669,23 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
         }
       }
       asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (ct < kTok) {
+      if (ct < kTok) {   // warps 2 and 3
         const float own = red[0][ct] + red[1][ct];   // rows in order within this CTA's 64
+        ssq_in[rank][ct] = own;   // read back by this thread only
   #pragma unroll
-        for (int r = 0; r < kCluster; ++r) tc::st_cluster_f32(tc::cluster_addr(&ssq_in[rank][ct], (uint32_t)r), own);
+        for (int d = 1; d < kCluster; ++d) {
+          const uint32_t r = (uint32_t)((rank + d) & (kCluster - 1));
+          tc::st_async_f32(tc::cluster_addr(&ssq_in[rank][ct], r), own, tc::cluster_addr(&bars[kNB - 1], r));
+        }
+        // all four row quarters' sums are here
+        const bool g = tc::mbar_wait(sbar, 0, p.wait_limit, abort_flag, p.dev_err);
+        if (!__all_sync(0xffffffffu, g)) ok = false;
+        if (ct == 0) stamp(kTraceRows - 2, 2);
+        rfac[ct] = 1.f / sqrtf((((ssq_in[0][ct] + ssq_in[1][ct]) + ssq_in[2][ct]) + ssq_in[3][ct]) / (float)kLd +
+                               p.eps);
       }
-      tc::cluster_arrive_release();
-      tc::cluster_wait();                        // phase 3: all four row quarters' sums are here
-      if (ct == 0) stamp(kTraceRows - 2, 2);
-      if (ct < kTok) rfac[ct] = 1.f / sqrtf((((ssq_in[0][ct] + ssq_in[1][ct]) + ssq_in[2][ct]) + ssq_in[3][ct]) /
-                                                  (float)kLd +
-                                              p.eps);
       asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (*abort_flag) ok = false;   // a wait of another epilogue warp gave up
       if (ct == 0) stamp(kTraceRows - 1, 6);
       if (mine) {   // warp-uniform: the TMEM loads below are warp-wide
         const bool g = ok && tc::mbar_wait(gbar, 0, p.wait_limit, abort_flag, p.dev_err);
@@ -718,12 +738,12 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
       if (ct == 0) stamp(kTraceRows - 1, 7);
     }
   }
-  if (warp < kEpi0) {   // the TMA and MMA warps take part in every cluster phase too
-    tc::cluster_wait();
-    tc::cluster_arrive_release();
-    tc::cluster_wait();
-    tc::cluster_arrive_release();
-    tc::cluster_wait();
+  if (warp < kEpi0) tc::cluster_wait();   // the TMA and MMA warps take part in the cluster phase too
+  if (warp == kEpi0) {
+    // every store a peer makes into this CTA has landed before it leaves
+    // (already so unless a wait above gave up)
+    tc::mbar_drain(xbar, 0, kDrainCycles, p.dev_err);
+    tc::mbar_drain(sbar, 0, kDrainCycles, p.dev_err);
   }
   tc::fence_before();
   __syncthreads();

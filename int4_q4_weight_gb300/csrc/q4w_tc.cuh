@@ -279,6 +279,21 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t remote, float a, float b,
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
+// Stores into the shared memory of a CTA of the cluster whose bytes are
+// counted on an mbarrier of that CTA (both addresses from cluster_addr): the
+// receiver learns from its own barrier that the data is there, with no
+// cluster-wide barrier and no release fence on the sending side.
+__device__ __forceinline__ void st_async_v4(uint32_t remote, float a, float b, float c, float d, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t remote, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote), "f"(v),
+               "r"(remote_bar)
+               : "memory");
+}
 
 }  // namespace tc
 }  // namespace q4w
