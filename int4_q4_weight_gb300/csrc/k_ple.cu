@@ -449,6 +449,14 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
     // epilogue: its load stays in flight through the stage loop.
     int my_id = -1;
     float my_sc = 0.f;
+    // the norm weights of the four output columns this epilogue thread
+    // finishes (4 (ct % 16) .. + 3 of the 64 finished here), in flight
+    // through the stage loop
+    float my_nw[4] = {0.f, 0.f, 0.f, 0.f};
+    if (epi) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) my_nw[j] = p.norm_w[m * kRows + 64 * kh + 4 * (ct & 15) + j];
+    }
     if (epi && ct < ntok) {
       const int v = p.ids[t0 + ct];
       if (v >= 0 && v < p.V)
@@ -639,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
       if (ct == 0) stamp(kTraceRows - 2, 1);
       // p = (K half 0) + (K half 1), the same order in both CTAs; the four token
       // groups' reductions are independent of one another
-      float pv[kTok];   // this row's projection sums, kept for the output pass
+      float pv[kTok];   // this row's projection sums
   #pragma unroll
       for (int cb = 0; cb < kTok / 16; ++cb) {
         if (mine && cb < npad / 16) {   // warp-uniform
@@ -668,8 +676,11 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
           if ((lane & 1) == 0) red[q & 1][cb * 16 + (lane >> 1)] = s2;
         }
       }
+      // every read of the partner's partial sums is done (recv becomes the
+      // output tile), and the per-warp sums of squares are in red
       asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (ct < kTok) {   // warps 2 and 3
+      float* tile = recv;   // [64 tokens][64 columns] f32
+      if (ct < kTok) {   // warps 2 and 3: this CTA's sums to the three peers
         const float own = red[0][ct] + red[1][ct];   // rows in order within this CTA's 64
         ssq_in[rank][ct] = own;   // read back by this thread only
   #pragma unroll
@@ -677,6 +688,16 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
           const uint32_t r = (uint32_t)((rank + d) & (kCluster - 1));
           tc::st_async_f32(tc::cluster_addr(&ssq_in[rank][ct], r), own, tc::cluster_addr(&bars[kNB - 1], r));
         }
+      }
+      if (mine) {   // the finished sums into the tile while the peers' sums travel
+  #pragma unroll
+        for (int cb = 0; cb < kTok / 16; ++cb)
+          if (cb < npad / 16) {
+  #pragma unroll
+            for (int u = 0; u < 16; ++u) tile[(cb * 16 + u) * 64 + r64] = pv[cb * 16 + u];
+          }
+      }
+      if (ct < kTok) {
         // all four row quarters' sums are here
         const bool g = tc::mbar_wait(sbar, 0, p.wait_limit, abort_flag, p.dev_err);
         if (!__all_sync(0xffffffffu, g)) ok = false;
@@ -684,45 +705,33 @@ __global__ void __launch_bounds__(kThreads, 1) ple_tc_kernel(const __grid_consta
         rfac[ct] = 1.f / sqrtf((((ssq_in[0][ct] + ssq_in[1][ct]) + ssq_in[2][ct]) + ssq_in[3][ct]) / (float)kLd +
                                p.eps);
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (*abort_flag) ok = false;   // a wait of another epilogue warp gave up
-      if (ct == 0) stamp(kTraceRows - 1, 6);
-      if (mine) {   // warp-uniform: the TMEM loads below are warp-wide
+      {   // the gathered table bytes
         const bool g = ok && tc::mbar_wait(gbar, 0, p.wait_limit, abort_flag, p.dev_err);
         ok = __all_sync(0xffffffffu, g);
       }
-      if (ok && mine) {
-        // the output tile [64 tokens][64 columns] in shared memory (the partner's
-        // partial sums are no longer needed), then one tensor store; padding
-        // tokens are outside the tensor and not written
-        float* tile = recv;
-        const float nw = p.norm_w[m * kRows + row];
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (*abort_flag) ok = false;   // a wait of another epilogue warp gave up
+      if (ct == 0) stamp(kTraceRows - 1, 6);
+      if (ok) {
+        // out = p * rfac * norm_w + (q * s) * 16 in place, thread = (token
+        // t = ct / 16 + 8 k, columns 4 (ct % 16) .. + 3); padding tokens are
+        // outside the tensor and not written; a bad id gives zeros
+        const int cg = ct & 15;
         const float es = p.embed_scale;
-        // 16 tokens at a time: every shared-memory read of the group is issued
-        // before its stores (the compiler cannot move reads across the stores)
   #pragma unroll
-        for (int cb = 0; cb < kTok / 16; ++cb) {
-          float sc[16], rf[16], val[16];
-          int id[16];
-          int8_t tq[16];
+        for (int k = 0; k < kTok / 8; ++k) {
+          const int t = (ct >> 4) + 8 * k;
+          float4 v = *reinterpret_cast<const float4*>(tile + t * 64 + 4 * cg);
+          const uint32_t tq = *reinterpret_cast<const uint32_t*>(gtab + t * 64 + 4 * cg);
+          const float rf = rfac[t], sc = tsc[t];
+          const bool good = tid_sh[t] >= 0;
+          float* e = &v.x;
   #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 a = *reinterpret_cast<const float4*>(tsc + cb * 16 + 4 * i);
-            const float4 b = *reinterpret_cast<const float4*>(rfac + cb * 16 + 4 * i);
-            const int4 c = *reinterpret_cast<const int4*>(tid_sh + cb * 16 + 4 * i);
-            sc[4 * i] = a.x, sc[4 * i + 1] = a.y, sc[4 * i + 2] = a.z, sc[4 * i + 3] = a.w;
-            rf[4 * i] = b.x, rf[4 * i + 1] = b.y, rf[4 * i + 2] = b.z, rf[4 * i + 3] = b.w;
-            id[4 * i] = c.x, id[4 * i + 1] = c.y, id[4 * i + 2] = c.z, id[4 * i + 3] = c.w;
+          for (int j = 0; j < 4; ++j) {
+            const float g = __fmul_rn(__fmul_rn((float)(int8_t)(tq >> (8 * j)), sc), es);
+            e[j] = good ? e[j] * rf * my_nw[j] + g : 0.f;
           }
-  #pragma unroll
-          for (int u = 0; u < 16; ++u) tq[u] = gtab[(cb * 16 + u) * 64 + r64];
-  #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const float g = __fmul_rn(__fmul_rn((float)tq[u], sc[u]), es);
-            val[u] = id[u] >= 0 ? pv[cb * 16 + u] * rf[u] * nw + g : 0.f;
-          }
-  #pragma unroll
-          for (int u = 0; u < 16; ++u) tile[(cb * 16 + u) * 64 + r64] = val[u];
+          *reinterpret_cast<float4*>(tile + t * 64 + 4 * cg) = v;
         }
       }
       tc::fence_proxy_async();   // the tile (and the zeroed table rows) before the tensor stores read them
