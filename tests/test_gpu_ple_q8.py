@@ -66,7 +66,8 @@ def _ple_q8_check(q4w, p, L, proj_zero=False):
 
 
 @pytest.mark.parametrize("S,V,L,D", [(5, 1000, 3, 128), (17, 333, 2, 1536), (64, 4096, 35, 1536),
-                                     (1, 50, 1, 128), (9, 77, 2, 384), (33, 120, 1, 2048)])
+                                     (1, 50, 1, 128), (9, 77, 2, 384), (33, 120, 1, 2048),
+                                     (12, 200, 2, 1920)])   # K halves of 8 and 7 stages
 def test_ple_q8_small(cuda_lib, S, V, L, D):
     p = synth.ple_inputs(seed=95, device="cuda", S=S, V=V, L=L, D=D)
     _ple_q8_check(cuda_lib, p, L)
