@@ -391,10 +391,13 @@ long long q4_set_wait_limit(long long cycles);
  * for their layout (else they write nothing):
  *   ple_gather_project / _q8: CTA 0 writes row r < 256 of 8 words (SM
  *   cycles since its start) per stage r: 0 tile loads issued, 1 tiles seen
- *   by the converter warps, 2 operand converted, 3 MMAs started, 4 MMAs
- *   committed; row 255 words 5-7 and row 254 words 0-4 mark the epilogue
- *   (accumulator ready, cluster phases 1-3, RMS factors, output written,
- *   exit); then every CTA writes its start and end globaltimer (ns) as two
+ *   by the converter warps, 2 operand converted (words 1-2: even stages
+ *   only in the int8 form, whose two converter groups alternate), 3 MMAs
+ *   started, 4 MMAs committed; the epilogue: row 255 word 5 accumulator
+ *   ready, row 254 word 0 the cluster barrier passed, word 1 the partial
+ *   sums sent or received, word 2 the sums of squares received, row 255
+ *   word 6 RMS factors, word 7 and row 254 word 3 output written, row 254
+ *   word 4 exit; then every CTA writes its start and end globaltimer (ns) as two
  *   words at 2048 + 2 * (blockIdx.y * gridDim.x + blockIdx.x).  Needs
  *   (2048 + 2 * 4 * L * ceil(S / 64)) * 8 bytes.
  *   q4_gemm_chunk and the batched LM head: CTA 0 writes 8 words (SM cycles)

@@ -19,8 +19,8 @@
 // K half kh of the hidden width.  The two K halves of a row half swap the
 // partial sums of the rows the other one finishes (64 rows each) through
 // distributed shared memory and add them in a fixed order; then every CTA
-// sends its per-token sum of squares over its 64 finished rows to all four,
-// so each finishes the chunk's RMSNorm for its own rows, adds the gathered
+// sends its per-token sum of squares over its 64 finished rows to the three
+// others, so each finishes the chunk's RMSNorm for its own rows, adds the gathered
 // table term, and writes its [64 tokens][64 columns] output tile (and the
 // gathered bytes) from shared memory with tensor stores.  Both exchanges are
 // stores into the peers' shared memory that count their bytes on an mbarrier
@@ -42,8 +42,11 @@
 //              128-byte row becomes 64 bytes of P1 and 64 of P2, in the
 //              128-byte swizzle of a K-major fp16 operand); eight warps so
 //              that each scheduler has two to switch between
-//   warps 2-5  also issue the table copies and run the epilogue on their
-//              TMEM lane quarters (warp w reads lanes 32 (w % 4) .. + 31)
+//   warps 2-5  also issue the table copies and run the epilogue: each
+//              reads the accumulator rows of its TMEM lane quarter (warp w
+//              reads lanes 32 (w % 4) .. + 31) for the exchanges, and the
+//              four then form the output tile in place (one token and four
+//              columns per thread)
 // A ring of kFStages stages (raw / pieces 32 KB + hidden 8 KB) is guarded by
 // full (TMA bytes), bready (converter warps, which arrive only after seeing
 // full) and empty (MMA commit) mbarriers; the MMA warp waits on bready alone.
@@ -56,8 +59,9 @@
 // is in flight at once; two groups of four converter warps (2-5, 6-9) take
 // alternate stages and widen the codes to fp16(scale * code) straight into
 // one of four 64-column A stages in tensor memory (thread = projection row =
-// TMEM lane), and 8 MMAs of kind::f16 with A in tensor memory follow (the
-// block scales of the CTA's rows sit in shared memory).  A slot is free again
+// TMEM lane), and 8 MMAs of kind::f16 with A in tensor memory follow (each
+// converter thread loads the block scales of its row for its group's stages
+// at the start and reads them back from shared memory itself).  A slot is free again
 // once its group has read the codes and the MMAs have read the hidden tile;
 // an A stage once its MMAs have completed.  The K halves of a cluster take
 // alternate 128-column units.
