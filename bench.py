@@ -481,6 +481,51 @@ def row_gemm(q4w, synth, dev, hbm, bf16_peak, N, K, reps=10):
             "us": round(t * 1e6, 2), "bytes": b, "flops": flops, "copies": copies}
 
 
+def _a8_scale(q4w, synth, dev, K):
+    """w4a8 activation scale, min-max calibrated on 128 synthetic samples [128, K]."""
+    cal = synth.normal_f16((128, K), synth.sub_seed(1007, K), dev)
+    return float(q4w.q4_act_calibrate_a8(cal).cpu()[0])
+
+
+def row_gemv_a8(q4w, synth, dev, hbm, reps=10):
+    """w4a8 [2048, 1536] GEMV (activation codes under a calibrated scale),
+    streamed over distinct weight copies totalling >= 4x L2."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    W, x = synth.gemv_inputs(seed=1001, device=dev)
+    c, s = q4w.q4_quantize(W)
+    act = _a8_scale(q4w, synth, dev, 1536)
+    per = c.numel() + s.numel() * 2
+    copies = max(8, math.ceil(4 * l2 / per))
+    cs = [(c.clone(), s.clone()) for _ in range(copies)]
+    y = torch.empty(2048, dtype=torch.float32, device=dev)
+    xv = x[0].contiguous()
+    t = _time_graph(lambda: [q4w.q4_gemv_a8(ci, si, xv, act, y) for ci, si in cs], reps) / copies
+    b = per + 2 * 1536 + 4 * 2048
+    return {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4), "us": round(t * 1e6, 3),
+            "act_scale": act, "bytes": b, "copies": copies}
+
+
+def row_gemm_a8(q4w, synth, dev, hbm, bf16_peak, N, K, reps=10):
+    """w4a8 S=64 prefill GEMM (the token operand as activation codes)."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    W, X = synth.gemm_inputs(seed=1005, device=dev, N=N, K=K)
+    c, s = q4w.q4_quantize(W)
+    del W
+    act = _a8_scale(q4w, synth, dev, K)
+    per = c.numel() + s.numel() * 2
+    copies = max(1, math.ceil(2 * l2 / per)) if per < l2 else 1
+    cs = [(c, s)] + [(c.clone(), s.clone()) for _ in range(copies - 1)]
+    Y = torch.empty((64, N), dtype=torch.float32, device=dev)
+    t = _time_graph(lambda: [q4w.q4_gemm_chunk_a8(ci, si, X, act, Y) for ci, si in cs], reps) / copies
+    b = per + 64 * K * 2 + 64 * N * 4
+    flops = 2 * 64 * N * K
+    return {"GB/s": round(b / t / 1e9, 1), "TFLOP/s": round(flops / t / 1e12, 2),
+            "frac_hbm": round(b / t / 1e9 / hbm, 4), "frac_bf16": round(flops / t / 1e12 / bf16_peak, 4),
+            "us": round(t * 1e6, 2), "act_scale": act, "bytes": b, "flops": flops, "copies": copies}
+
+
 def row_q2(q4w, synth, dev, hbm, which, reps=10):
     """INT2 GEMV of the mixed-bit recipe: the FFN gate/up shape streamed over
     distinct weight copies totalling >= 4x L2, or the tied head (> L2 alone)."""
@@ -515,11 +560,13 @@ def measure_rows(q4w, synth, dev, hbm, clocks, bf16_peak):
         rows[name] = row_gemm(q4w, synth, dev, hbm, bf16_peak, N, K)
     rows["q2_gemv_12288x1536"] = row_q2(q4w, synth, dev, hbm, "gate")
     rows["q2_gemv_head_262144x1536"] = row_q2(q4w, synth, dev, hbm, "head")
+    rows["gemv_a8_2048x1536"] = row_gemv_a8(q4w, synth, dev, hbm)
+    rows["gemm_a8_s64_up"] = row_gemm_a8(q4w, synth, dev, hbm, bf16_peak, 6144, 1536)
     return rows
 
 
 CASES = ("gemv", "gemv_b4", "head_b1", "head_b8", "ple", "ple_q8", "gemm_up", "gemm_down", "gemm_head", "q2_gate",
-         "q2_head", "pass_trace")
+         "q2_head", "gemv_a8", "gemm_a8_up", "pass_trace")
 
 
 def pass_trace(q4w, synth, dev, reps):
@@ -625,6 +672,10 @@ def run_case(args):
         r = row_q2(q4w, synth, dev, hbm, args.case[3:], reps)
     elif args.case == "pass_trace":
         r = pass_trace(q4w, synth, dev, reps)
+    elif args.case == "gemv_a8":
+        r = row_gemv_a8(q4w, synth, dev, hbm, reps)
+    elif args.case == "gemm_a8_up":
+        r = row_gemm_a8(q4w, synth, dev, hbm, bf16, 6144, 1536, reps)
     else:
         N, K = {"gemm_up": (6144, 1536), "gemm_down": (1536, 6144), "gemm_head": (262144, 1536)}[args.case]
         r = row_gemm(q4w, synth, dev, hbm, bf16, N, K, reps)

@@ -164,6 +164,44 @@ int q4_gemm_chunk(const uint8_t* codes, const uint16_t* scales, const uint16_t* 
                   q4_stream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* w4a8: int8 quantize/dequantize on the activations of a q4_0 linear.     */
+/* ---------------------------------------------------------------------- */
+/* The w4a8 bundle ("visible-cx/gemma-4-E2B-CoreAI", About the w4a8 bundle)
+ * keeps the int4 per-block-32 weights and puts an int8 quantize/dequantize
+ * pair, calibrated on 128 samples, on the input of every linear layer.
+ * Readings (the pages name the pair, not its grid): per-tensor symmetric,
+ * zero point 0, one fp32 scale s per linear input;
+ *   q = clamp(rint(x / s), -128, 127)  (IEEE fp32 quotient, ties to even),
+ *   x' = s * q,
+ * and calibration by min-max: s = max |x| / 127 over the samples (fp32), 1
+ * when every sample is zero.  The layer sees x'; since q is exact in fp16 and
+ * bf16 the kernels multiply the weights by q and scale each output by s.
+ * x must be finite (a NaN or infinity gives an undefined code).           */
+
+/* q4_gemv_a8: y[n] = act_scale * sum_k scale[n][k/32] * (code[n][k] - 8) * q[k],
+ * q the codes of x_f16 [K] under act_scale; fp32 accumulation (each block's
+ * dot with integer q is exact in fp32).  codes/scales: q4_0 matrix [N][K];
+ * y: f32 [N].  N >= 1; K % 32 == 0, 32 <= K <= 32768; act_scale finite and
+ * > 0 (else Q4_ERR_SHAPE).  Deterministic.                                 */
+int q4_gemv_a8(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16,
+               float act_scale, float* y, int N, int K, q4_stream_t stream);
+
+/* q4_gemm_chunk_a8: q4_gemm_chunk on the activation codes:
+ * Y[t][n] = act_scale * sum_k bf16(scale*(code-8))[n][k] * q[t][k], q the
+ * codes of X_f16 under act_scale (exact in bf16).  Shapes, workspace and
+ * errors as q4_gemm_chunk; act_scale finite and > 0 (else Q4_ERR_SHAPE).  */
+int q4_gemm_chunk_a8(const uint8_t* codes, const uint16_t* scales, const uint16_t* X_f16,
+                     float act_scale, float* Y, int M, int N, int K, void* ws,
+                     size_t ws_bytes, q4_stream_t stream);
+
+/* q4_act_calibrate_a8: *scale_out (device f32) = max |x| / 127 over the n fp16
+ * values of x_f16 (all calibration samples, concatenated), or 1 when every
+ * value is zero.  n >= 1.  One CTA reduces the values (a calibration step,
+ * not a per-token one).                                                    */
+int q4_act_calibrate_a8(const uint16_t* x_f16, long long n, float* scale_out,
+                        q4_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* Per-Layer-Embedding gather + projection.                                */
 /* ---------------------------------------------------------------------- */
 /* ple_gather_project: for each of S tokens t with id v = ids[t]:

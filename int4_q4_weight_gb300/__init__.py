@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "load", "build", "Q4Error", "q4_quantize", "q4_gemv", "q4_gemv_weights_ro", "q4_gemv_stage", "q4_rmsnorm_f16",
     "q4_decode_pass", "q4_decode_pass_launches", "q2_gemv", "lmhead_softcap_argmax", "ple_gather_project", "q4_gemm_chunk",
-    "q8_quantize", "ple_gather_project_q8",
+    "q8_quantize", "ple_gather_project_q8", "q4_gemv_a8", "q4_gemm_chunk_a8", "q4_act_calibrate_a8",
     "q4_workspace_bytes", "q4_version", "Q4_IN_F16", "Q4_IN_RMS_F16", "Q4_IN_RMS_F32",
     "Q4_IN_RMS2_F32", "Q4_OP_GEMV", "Q4_OP_GEMM_CHUNK", "Q4_OP_PLE", "Q4_OP_LMHEAD",
     "Q4_OP_DECODE_PASS", "q4_layer", "q4_matrix",
@@ -52,6 +52,9 @@ _SIGS = {
     "q4_gemv": (ci, [vp, vp, vp, vp, ci, ci, ci, vp, csz, vp]),
     "q4_gemv_weights_ro": (ci, [vp, vp, vp, vp, ci, ci, ci, vp, csz, vp]),
     "q4_gemm_chunk": (ci, [vp, vp, vp, vp, ci, ci, ci, vp, csz, vp]),
+    "q4_gemv_a8": (ci, [vp, vp, vp, cf, vp, ci, ci, vp]),
+    "q4_gemm_chunk_a8": (ci, [vp, vp, vp, cf, vp, ci, ci, ci, vp, csz, vp]),
+    "q4_act_calibrate_a8": (ci, [vp, ctypes.c_longlong, vp, vp]),
     "ple_gather_project": (ci, [vp, ci, vp, vp, ci, ci, ci, cf, vp, vp, ci, vp, cf, vp, vp, vp, vp]),
     "q8_quantize": (ci, [vp, ci, ci, vp, vp, vp, vp]),
     "ple_gather_project_q8": (ci, [vp, ci, vp, vp, ci, ci, ci, cf, vp, vp, vp, ci, vp, cf, vp, vp, vp, vp]),
@@ -466,6 +469,64 @@ def q4_gemm_chunk(codes, scales, X, Y=None):
     _check(lib.q4_gemm_chunk(_ptr(codes), _ptr(scales), _ptr(X), _ptr(Y), M, N, K, _ptr(ws), nws,
                              _stream()), "q4_gemm_chunk")
     return Y
+
+
+def q4_gemv_a8(codes, scales, x, act_scale, y=None):
+    """w4a8 GEMV: y [N] f32 = act_scale * dequant(codes, scales) @ q, q the int8
+    codes clamp(rint(x / act_scale), -128, 127) of x (fp16 [K])."""
+    lib = load()
+    _dev(codes, torch.uint8, "codes")
+    _dev(scales, torch.float16, "scales")
+    _dev(x, torch.float16, "x")
+    N, K = codes.shape[0], codes.shape[1] * 2
+    if y is None:
+        y = torch.empty(N, dtype=torch.float32, device=x.device)
+    _dev(y, torch.float32, "y")
+    _numel(scales, N * K // 32, "scales")
+    _numel(x, K, "x")
+    _numel(y, N, "y")
+    _check(lib.q4_gemv_a8(_ptr(codes), _ptr(scales), _ptr(x), float(act_scale), _ptr(y), N, K, _stream()),
+           "q4_gemv_a8")
+    return y
+
+
+def q4_gemm_chunk_a8(codes, scales, X, act_scale, Y=None):
+    """w4a8 S=64 chunk: Y [64, N] f32 = act_scale * (bf16 tiles of dequant(codes, scales)) @ Q.T,
+    Q the int8 codes of X [64, K] under act_scale."""
+    lib = load()
+    _dev(codes, torch.uint8, "codes")
+    _dev(scales, torch.float16, "scales")
+    _dev(X, torch.float16, "X")
+    N, K = codes.shape[0], codes.shape[1] * 2
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    _dev(Y, torch.float32, "Y")
+    _numel(scales, N * K // 32, "scales")
+    _numel(X, M * K, "X")
+    _numel(Y, M * N, "Y")
+    nws = lib.q4_workspace_bytes(Q4_OP_GEMM_CHUNK, N, K, M)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=X.device)
+    _check(lib.q4_gemm_chunk_a8(_ptr(codes), _ptr(scales), _ptr(X), float(act_scale), _ptr(Y), M, N, K,
+                                _ptr(ws), nws, _stream()), "q4_gemm_chunk_a8")
+    return Y
+
+
+def q4_act_calibrate_a8(samples, out=None):
+    """Min-max calibration of a w4a8 activation scale: a one-element f32 CUDA
+    tensor holding max |x| / 127 over every value of ``samples`` (fp16, any
+    shape, e.g. [128, K]), or 1 when all are zero."""
+    lib = load()
+    _dev(samples, torch.float16, "samples")
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=samples.device)
+    _dev(out, torch.float32, "out")
+    _numel(out, 1, "out")
+    if samples.numel() < 1:
+        raise Q4Error("samples must hold at least one value")
+    _check(lib.q4_act_calibrate_a8(_ptr(samples), samples.numel(), _ptr(out), _stream()),
+           "q4_act_calibrate_a8")
+    return out
 
 
 def q2_gemv(codes, scales, x, y=None):

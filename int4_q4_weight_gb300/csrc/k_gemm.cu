@@ -273,6 +273,7 @@ struct Params {
   const __half* scales;   // read directly when K % 256 != 0 (row stride not a multiple of 16 B)
   int sc_tma;
   float* Y;
+  float out_scale;        // Y = out_scale * (the product): 1, or the w4a8 activation scale
   int N, K;
   int ntok;               // tokens written to Y (the rows of Y; the MMA N may be padded beyond)
   int tiles, splits, cps, nchunks, items;
@@ -679,10 +680,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
             if (p.logits) p.logits[(size_t)t * p.N + n] = p.cap * tanhf(v[j] / p.cap);
           } else {
             float* dst = p.Y + (size_t)t * p.N + n;
+            const float o = v[j] * p.out_scale;   // exact when out_scale is 1
             if (p.splits == 1)
-              *dst = v[j];
+              *dst = o;
             else
-              atomicAdd(dst, v[j]);
+              atomicAdd(dst, o);
           }
         }
       }
@@ -731,7 +733,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
 // (group, token).
 template <int NT, bool F16>
 __global__ void __launch_bounds__(256) x_layout_kernel(const __half* __restrict__ X, uint8_t* __restrict__ xb,
-                                                       int K, int ntok, float4* __restrict__ yclear, int n4) {
+                                                       int K, int ntok, float4* __restrict__ yclear, int n4,
+                                                       float act_s) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;   // = group * NT + token
   // the output the split-K GEMM adds into, cleared (n4 float4s; 0 if none)
   for (int k = i; k < n4; k += gridDim.x * blockDim.x) yclear[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -739,7 +742,16 @@ __global__ void __launch_bounds__(256) x_layout_kernel(const __half* __restrict_
     const int grp = i / NT, tok = i - grp * NT;
     uint4 o = make_uint4(0u, 0u, 0u, 0u);
     if (tok < ntok) {
-      const uint4 v = *reinterpret_cast<const uint4*>(X + (size_t)tok * K + grp * 8);
+      uint4 v = *reinterpret_cast<const uint4*>(X + (size_t)tok * K + grp * 8);
+      if (act_s > 0.f) {   // w4a8: the token operand is the activation codes q (the GEMM scales Y by s)
+        uint32_t* w = &v.x;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+          const __half2 h = __floats2half2_rn(a8_code(f.x, act_s), a8_code(f.y, act_s));
+          w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+      }
       // slot order 0 4 1 5 2 6 3 7 (the weights' decoded pairs)
       const uint4 q = make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
                                  __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
@@ -794,7 +806,7 @@ size_t mma16_ws_bytes(int K) { return ((size_t)16 * K * 2 + 255) & ~(size_t)255;
 template <int NT, bool F16, bool HEAD>
 static int launch_mma(const uint8_t* codes, const __half* scales, const __half* X, int ntok, float* Y, int N,
                       int K, void* ws, bool allow_split, const HeadOutputs* head, const DeviceInfo& dev,
-                      cudaStream_t s) {
+                      cudaStream_t s, float act_scale = 0.f) {
   if (HEAD && (head == nullptr || allow_split)) return fail(Q4_ERR_SHAPE, "head GEMM: outputs missing or split K");
   gemm::Params p;
   memset(&p, 0, sizeof(p));
@@ -819,6 +831,7 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
     if (st != Q4_OK) return st;
   }
   p.Y = Y;
+  p.out_scale = act_scale > 0.f ? act_scale : 1.f;
   p.N = N;
   p.K = K;
   p.ntok = ntok;
@@ -859,7 +872,7 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
   // epilogue adds into only after waiting for that kernel
   const int n4 = p.splits > 1 ? (int)((size_t)ntok * N / 4) : 0;
   gemm::x_layout_kernel<NT, F16><<<(nx + 255) / 256, 256, 0, s>>>(X, static_cast<uint8_t*>(ws), K, ntok,
-                                                                  reinterpret_cast<float4*>(Y), n4);
+                                                                  reinterpret_cast<float4*>(Y), n4, act_scale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "gemm token layout launch");
   // the GEMM starts while the token layout is written; only its B loader waits for it
@@ -879,9 +892,10 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
 }
 
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
-                      int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s) {
+                      int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s, float act_scale) {
   (void)M;
-  return launch_mma<gemm::kTok, false, false>(codes, scales, X, gemm::kTok, Y, N, K, ws, true, nullptr, dev, s);
+  return launch_mma<gemm::kTok, false, false>(codes, scales, X, gemm::kTok, Y, N, K, ws, true, nullptr, dev, s,
+                                              act_scale);
 }
 
 bool head_mma_fits(int K) {

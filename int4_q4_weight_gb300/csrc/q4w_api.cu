@@ -511,8 +511,8 @@ int ple_gather_project_q8(const int32_t* ids, int S, const int8_t* table, const 
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
-int q4_gemm_chunk(const uint8_t* codes, const uint16_t* scales, const uint16_t* X_f16, float* Y, int M,
-                  int N, int K, void* ws, size_t ws_bytes, q4_stream_t stream) {
+static int gemm_chunk_impl(const uint8_t* codes, const uint16_t* scales, const uint16_t* X_f16, float* Y, int M,
+                           int N, int K, void* ws, size_t ws_bytes, q4_stream_t stream, float act_scale) {
   clear_error();
   CHECK_NULL(codes);
   CHECK_NULL(scales);
@@ -531,7 +531,54 @@ int q4_gemm_chunk(const uint8_t* codes, const uint16_t* scales, const uint16_t* 
   DEVICE_OR_RETURN(dev);
   return launch_gemm_chunk(codes, reinterpret_cast<const __half*>(scales),
                            reinterpret_cast<const __half*>(X_f16), Y, M, N, K, ws, dev,
-                           reinterpret_cast<cudaStream_t>(stream));
+                           reinterpret_cast<cudaStream_t>(stream), act_scale);
+}
+
+int q4_gemm_chunk(const uint8_t* codes, const uint16_t* scales, const uint16_t* X_f16, float* Y, int M,
+                  int N, int K, void* ws, size_t ws_bytes, q4_stream_t stream) {
+  return gemm_chunk_impl(codes, scales, X_f16, Y, M, N, K, ws, ws_bytes, stream, 0.f);
+}
+
+static bool act_scale_ok(float s) { return s > 0.f && s <= 3.4e38f; }   // finite and positive (false for NaN)
+
+int q4_gemm_chunk_a8(const uint8_t* codes, const uint16_t* scales, const uint16_t* X_f16, float act_scale,
+                     float* Y, int M, int N, int K, void* ws, size_t ws_bytes, q4_stream_t stream) {
+  if (!act_scale_ok(act_scale)) {
+    clear_error();
+    return fail(Q4_ERR_SHAPE, "act_scale=%g must be finite and > 0", (double)act_scale);
+  }
+  return gemm_chunk_impl(codes, scales, X_f16, Y, M, N, K, ws, ws_bytes, stream, act_scale);
+}
+
+int q4_gemv_a8(const uint8_t* codes, const uint16_t* scales, const uint16_t* x_f16, float act_scale, float* y,
+               int N, int K, q4_stream_t stream) {
+  clear_error();
+  CHECK_NULL(codes);
+  CHECK_NULL(scales);
+  CHECK_NULL(x_f16);
+  CHECK_NULL(y);
+  CHECK_ALIGN(codes);
+  CHECK_ALIGN(scales);
+  CHECK_ALIGN(x_f16);
+  CHECK_ALIGN(y);
+  CHECK(N >= 1, "N=%d must be >= 1", N);
+  CHECK(K >= 32 && K % 32 == 0 && K <= kMaxK, "K=%d must be a multiple of 32 in [32, %d]", K, kMaxK);
+  CHECK(act_scale_ok(act_scale), "act_scale=%g must be finite and > 0", (double)act_scale);
+  DEVICE_OR_RETURN(dev);
+  return launch_gemv_a8(codes, reinterpret_cast<const __half*>(scales), reinterpret_cast<const __half*>(x_f16),
+                        act_scale, y, N, K, dev, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int q4_act_calibrate_a8(const uint16_t* x_f16, long long n, float* scale_out, q4_stream_t stream) {
+  clear_error();
+  CHECK_NULL(x_f16);
+  CHECK_NULL(scale_out);
+  CHECK_ALIGN(x_f16);
+  CHECK(n >= 1, "n=%lld must be >= 1", n);
+  DEVICE_OR_RETURN(dev);
+  (void)dev;
+  return launch_a8_calibrate(reinterpret_cast<const __half*>(x_f16), n, scale_out,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

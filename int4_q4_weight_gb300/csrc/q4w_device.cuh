@@ -190,6 +190,15 @@ __device__ __forceinline__ float block_sum(float v, float* red /* kWarps floats 
 
 __device__ __forceinline__ float f16_round(float v) { return __half2float(__float2half_rn(v)); }
 
+// w4a8 activation code ("visible-cx/gemma-4-E2B-CoreAI", About the w4a8
+// bundle: an int8 quantize/dequantize pair on every linear input):
+// q = clamp(rint(x / s), -128, 127), the quotient an IEEE fp32 division and
+// rint rounding half to even; an integer of at most 8 bits, exact in fp16
+// and bf16.  x must be finite.
+__device__ __forceinline__ float a8_code(float x, float s) {
+  return fminf(fmaxf(rintf(__fdiv_rn(x, s)), -128.f), 127.f);
+}
+
 // x into the padded shared layout, then the per-block biases.
 __device__ __forceinline__ void xs_store(float* xs, int k, float v) {
   xs[(k >> 5) * kXStride + (k & 31)] = v;

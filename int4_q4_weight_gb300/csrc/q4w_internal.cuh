@@ -120,8 +120,16 @@ int encode_tensor_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType type
                      uint64_t rows, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle,
                      const char* what);
 size_t gemm_ws_bytes(int K);   // the bf16 copy of X [64][K]
+// act_scale > 0: the w4a8 form -- the token operand is the activation codes
+// q = clamp(rint(x / act_scale), -128, 127) and Y is scaled by act_scale.
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
-                      int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s);
+                      int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s, float act_scale = 0.f);
+// w4a8 (k_a8.cu): the single-vector q4_0 GEMV on the activation codes, y =
+// act_scale * (W q); and the min-max calibration s = max |x| / 127 (1 when
+// every x is zero) over n fp16 values into *s_out (device).
+int launch_gemv_a8(const uint8_t* codes, const __half* scales, const __half* x, float act_scale, float* y, int N,
+                   int K, const DeviceInfo& dev, cudaStream_t s);
+int launch_a8_calibrate(const __half* x, long long n, float* s_out, cudaStream_t s);
 // The LM head of ntok <= 8 vectors on the tensor cores: z[t][n] through the
 // GEMM kernel with fp16 tiles (weights rounded once to fp16, tokens exact),
 // one CTA per 128-row tile (no split of K, so every row is summed in one fixed

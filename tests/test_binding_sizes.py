@@ -56,6 +56,9 @@ def test_correct_sizes_reach_the_library(lib):
     q4w.q4_gemv(codes, scales, _z((4, K), torch.float16), _z((4, N), torch.float32))
     q4w.lmhead_softcap_argmax(codes, scales, _z((2, K), torch.float16), logits=_z((2, N), torch.float32))
     q4w.q4_gemm_chunk(codes, scales, _z((64, K), torch.float16))
+    q4w.q4_gemv_a8(codes, scales, _z(K, torch.float16), 0.01)
+    q4w.q4_gemm_chunk_a8(codes, scales, _z((64, K), torch.float16), 0.01)
+    q4w.q4_act_calibrate_a8(_z((128, K), torch.float16))
     q4w.q2_gemv(_z((N, K // 4), torch.uint8), _z(N, torch.float32), _z(K, torch.float16))
     a = _ple_args()
     q4w.ple_gather_project(a["ids"], a["table"], a["row_scale"], a["proj"], a["hidden"], a["norm_w"], L=2,
@@ -65,7 +68,8 @@ def test_correct_sizes_reach_the_library(lib):
                               b["hidden"], b["norm_w"], L=2)
     assert lib.calls.count("q4_gemv") == 2
     for name in ("q4_quantize", "q8_quantize", "lmhead_softcap_argmax", "q4_gemm_chunk", "q2_gemv",
-                 "ple_gather_project", "ple_gather_project_q8"):
+                 "ple_gather_project", "ple_gather_project_q8", "q4_gemv_a8", "q4_gemm_chunk_a8",
+                 "q4_act_calibrate_a8"):
         assert name in lib.calls, name
 
 
@@ -85,6 +89,10 @@ def test_mis_sized_arrays_are_refused(lib):
                                                      logits=_z((1, N), torch.float32)), "logits")
     _rejects(lib, lambda: q4w.q4_gemm_chunk(codes, scales, _z((64, K), torch.float16),
                                             _z((64, N // 2), torch.float32)), "Y")
+    _rejects(lib, lambda: q4w.q4_gemv_a8(codes, scales, _z(K - 32, torch.float16), 0.01), "x")
+    _rejects(lib, lambda: q4w.q4_gemv_a8(codes, scales, _z(K, torch.float16), 0.01, _z(N + 1, torch.float32)), "y")
+    _rejects(lib, lambda: q4w.q4_gemm_chunk_a8(codes, scales[:-1], _z((64, K), torch.float16), 0.01), "scales")
+    _rejects(lib, lambda: q4w.q4_act_calibrate_a8(_z(8, torch.float16), out=_z(2, torch.float32)), "out")
     _rejects(lib, lambda: q4w.q2_gemv(_z((N, K // 4), torch.uint8), _z(N, torch.float32),
                                       _z(K // 2, torch.float16)), "x")
     _rejects(lib, lambda: q4w.q4_quantize(_z((N, K), torch.float32), codes=_z((N, K // 4), torch.uint8)), "codes")
