@@ -304,8 +304,10 @@ __device__ __forceinline__ void item_range(const Params& p, int item, int& tile,
 }
 
 // NT: the MMA N (token tile), F16: fp16 tiles (else bf16), HEAD: the LM-head
-// epilogue (softcap and top two per token, no Y).
-template <int NT, bool F16, bool HEAD>
+// epilogue (softcap and top two per token, no Y), A8: the w4a8 form (the
+// token operand holds activation codes, Y is scaled by p.out_scale), its own
+// instantiation so that the plain GEMM's epilogue carries no scaling.
+template <int NT, bool F16, bool HEAD, bool A8 = false>
 __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constant__ Params p) {
   constexpr int kStageBytes = stage_bytes(NT);
   constexpr int kBBytes = b_bytes(NT);
@@ -669,6 +671,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] += u[j];
         }
+        if constexpr (A8) {   // w4a8: Y = s * (W q)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] *= p.out_scale;
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int t = cb * 16 + j;
@@ -680,11 +686,10 @@ __global__ void __launch_bounds__(kThreadsG, 1) gemm_kernel(const __grid_constan
             if (p.logits) p.logits[(size_t)t * p.N + n] = p.cap * tanhf(v[j] / p.cap);
           } else {
             float* dst = p.Y + (size_t)t * p.N + n;
-            const float o = v[j] * p.out_scale;   // exact when out_scale is 1
             if (p.splits == 1)
-              *dst = o;
+              *dst = v[j];
             else
-              atomicAdd(dst, o);
+              atomicAdd(dst, v[j]);
           }
         }
       }
@@ -803,7 +808,7 @@ size_t mma16_ws_bytes(int K) { return ((size_t)16 * K * 2 + 255) & ~(size_t)255;
 // atomics, so the summation order is not fixed); else one CTA per tile.
 // HEAD: Y is not written; head->* receive the softcapped top two per token
 // (and the softcapped logits when head->logits is set).
-template <int NT, bool F16, bool HEAD>
+template <int NT, bool F16, bool HEAD, bool A8 = false>
 static int launch_mma(const uint8_t* codes, const __half* scales, const __half* X, int ntok, float* Y, int N,
                       int K, void* ws, bool allow_split, const HeadOutputs* head, const DeviceInfo& dev,
                       cudaStream_t s, float act_scale = 0.f) {
@@ -857,10 +862,10 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
   static size_t dyn_max[64] = {0};
   if (!attr_set.get(dev.ordinal)) {
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<NT, F16, HEAD>);
+    e = cudaFuncGetAttributes(&fa, gemm::gemm_kernel<NT, F16, HEAD, A8>);
     if (e != cudaSuccess) return cuda_fail(e, "gemm attributes");
     dyn_max[dev.ordinal] = gemm::kSmemMax - fa.sharedSizeBytes;
-    e = cudaFuncSetAttribute(gemm::gemm_kernel<NT, F16, HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gemm::gemm_kernel<NT, F16, HEAD, A8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)dyn_max[dev.ordinal]);
     if (e != cudaSuccess) return cuda_fail(e, "gemm smem attribute");
     attr_set.set(dev.ordinal);
@@ -887,15 +892,17 @@ static int launch_mma(const uint8_t* codes, const __half* scales, const __half* 
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<NT, F16, HEAD>, p);
+  e = cudaLaunchKernelEx(&cfg, gemm::gemm_kernel<NT, F16, HEAD, A8>, p);
   return e == cudaSuccess ? Q4_OK : cuda_fail(e, "gemm launch");
 }
 
 int launch_gemm_chunk(const uint8_t* codes, const __half* scales, const __half* X, float* Y, int M,
                       int N, int K, void* ws, const DeviceInfo& dev, cudaStream_t s, float act_scale) {
   (void)M;
-  return launch_mma<gemm::kTok, false, false>(codes, scales, X, gemm::kTok, Y, N, K, ws, true, nullptr, dev, s,
-                                              act_scale);
+  if (act_scale > 0.f)
+    return launch_mma<gemm::kTok, false, false, true>(codes, scales, X, gemm::kTok, Y, N, K, ws, true, nullptr, dev,
+                                                      s, act_scale);
+  return launch_mma<gemm::kTok, false, false>(codes, scales, X, gemm::kTok, Y, N, K, ws, true, nullptr, dev, s);
 }
 
 bool head_mma_fits(int K) {
