@@ -274,7 +274,8 @@ int ple_gather_project_q8(const int32_t* ids, int S, const int8_t* table,
  * fp16(d*(q-8)), and fp32 accumulation, and selected in the same kernel (z
  * is not written unless logits_opt is given; the workspace then also holds
  * the fp16 copy of h, 32 K bytes); other shapes sum exact products on the
- * CUDA cores.  Either way each row's sum has a fixed order: repeated calls
+ * CUDA cores, where every batch row's h is staged in shared memory: K <=
+ * 25024 for b = 2..4 and K <= 12864 for b = 5..8 (larger: Q4_ERR_SHAPE).  Either way each row's sum has a fixed order: repeated calls
  * give the same bits.                                                       */
 int lmhead_softcap_argmax(const uint8_t* codes, const uint16_t* scales,
                           const uint16_t* h_f16, int b, int V, int K, float cap,

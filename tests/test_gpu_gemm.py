@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("N,K", [(128, 64), (256, 1536), (384, 320), (6144, 1536), (1536, 6144),
-                                 (1280, 12288)])
+                                 (1280, 12288), (128, 32768)])
 def test_gemm_parity(cuda_lib, N, K):
     W, X = synth.gemm_inputs(seed=100, device="cuda", N=N, K=K)
     codes, scales = cuda_lib.q4_quantize(W)

@@ -32,7 +32,8 @@ def _head_check(q4w, codes, scales, h, oc, os_, want_logits=True):
 
 
 @pytest.mark.parametrize("V,K,b", [(1000, 1536, 1), (4099, 256, 1), (77, 96, 1), (3000, 1536, 8),
-                                   (513, 160, 3), (2, 32, 1), (5000, 2048, 2)])
+                                   (513, 160, 3), (2, 32, 1), (5000, 2048, 2), (300, 32768, 1),
+                                   (40, 25024, 4), (33, 12864, 8)])
 def test_head_small(cuda_lib, V, K, b):
     W, h = synth.head_inputs(seed=80, device="cuda", batch=b, V=V, K=K)
     codes, scales = cuda_lib.q4_quantize(W)
@@ -40,6 +41,17 @@ def test_head_small(cuda_lib, V, K, b):
     torch.cuda.synchronize()
     assert np.array_equal(codes.cpu().numpy(), oc)
     _head_check(cuda_lib, codes, scales, h, oc, os_)
+
+
+@pytest.mark.parametrize("K,b", [(25056, 2), (12896, 5)])
+def test_head_batch_beyond_shared_memory_is_refused(cuda_lib, K, b):
+    """b >= 2 off the tensor-core path stages every batch row's x in shared
+    memory: one block more than fits (K 25024 for b <= 4, 12864 for b <= 8)
+    is a shape error, not a launch."""
+    W, h = synth.head_inputs(seed=82, device="cuda", batch=b, V=64, K=K)
+    codes, scales = cuda_lib.q4_quantize(W)
+    with pytest.raises(cuda_lib.Q4Error, match="does not fit"):
+        cuda_lib.lmhead_softcap_argmax(codes, scales, h)
 
 
 def test_head_ties_lowest_index(cuda_lib):
@@ -146,7 +158,7 @@ def _ple_check(q4w, p, L, proj_zero=False, tol=None):
 
 
 @pytest.mark.parametrize("S,V,L,D", [(5, 1000, 3, 64), (17, 333, 2, 1536), (64, 4096, 35, 1536),
-                                     (1, 50, 1, 32)])
+                                     (1, 50, 1, 32), (3, 50, 1, 32768)])
 def test_ple_small(cuda_lib, S, V, L, D):
     p = synth.ple_inputs(seed=90, device="cuda", S=S, V=V, L=L, D=D)
     _ple_check(cuda_lib, p, L)

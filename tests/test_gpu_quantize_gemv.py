@@ -10,7 +10,7 @@ from parity import assert_close
 pytestmark = pytest.mark.gpu
 
 SHAPES = [(2048, 1536), (1000, 1536), (37, 96), (1, 32), (513, 160), (300, 2048), (129, 6144),
-          (64, 12288), (7, 4096), (3, 224)]
+          (64, 12288), (7, 4096), (3, 224), (5, 32768)]
 
 
 def _quant_both(q4w, W):
@@ -73,7 +73,7 @@ def test_quantize_head_rows_sampled(cuda_lib):
 
 
 GEMV_CASES = SHAPES + [(2048, 1536, 2), (300, 1536, 8), (37, 96, 3), (100, 6144, 8), (5, 32, 5),
-                       (70, 12288, 4), (33, 160, 7)]
+                       (70, 12288, 4), (33, 160, 7), (9, 32768, 3)]
 
 
 @pytest.mark.parametrize("case", GEMV_CASES)
