@@ -164,7 +164,8 @@ def test_ple_small(cuda_lib, S, V, L, D):
     _ple_check(cuda_lib, p, L)
 
 
-@pytest.mark.parametrize("S,V,L,D", [(130, 900, 2, 96), (65, 300, 3, 1536)])
+@pytest.mark.parametrize("S,V,L,D", [(130, 900, 2, 96), (65, 300, 3, 1536), (4096, 100, 1, 64),
+                                     (2, 50, 256, 64)])
 def test_ple_token_groups(cuda_lib, S, V, L, D):
     # several 64-token groups with a ragged last group
     p = synth.ple_inputs(seed=94, device="cuda", S=S, V=V, L=L, D=D)

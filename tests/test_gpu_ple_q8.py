@@ -73,7 +73,8 @@ def test_ple_q8_small(cuda_lib, S, V, L, D):
     _ple_q8_check(cuda_lib, p, L)
 
 
-@pytest.mark.parametrize("S,V,L,D", [(130, 900, 2, 128), (65, 300, 3, 1536)])
+@pytest.mark.parametrize("S,V,L,D", [(130, 900, 2, 128), (65, 300, 3, 1536), (4096, 100, 1, 128),
+                                     (2, 50, 256, 128)])
 def test_ple_q8_token_groups(cuda_lib, S, V, L, D):
     # several 64-token groups with a ragged last group
     p = synth.ple_inputs(seed=96, device="cuda", S=S, V=V, L=L, D=D)
