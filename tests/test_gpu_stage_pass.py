@@ -217,6 +217,19 @@ def test_pass_is_stage_composition_small(cuda_lib):
     assert torch.equal(_pass(cuda_lib, gl, h0, H), _composed(cuda_lib, gl, h0, H))
 
 
+@pytest.mark.parametrize("n", [48, 49])
+def test_layer_count_across_the_persistent_limit(cuda_lib, n):
+    """48 layers still run as one persistent launch, 49 as one launch per
+    stage (4 n + 1 kernels); both equal the stage-by-stage composition bit
+    for bit."""
+    H = 256
+    dims = [{"q": 256, "kv": 0 if i % 2 else 256, "mlp": 512} for i in range(n)]
+    gl, _ = _layers(cuda_lib, dims, H, 74)
+    assert cuda_lib.q4_decode_pass_launches(cuda_lib.make_layers(gl, H), H) == (1 if n <= 48 else 4 * n + 1)
+    h0 = synth.normal_f16((H,), 75, "cuda")
+    assert torch.equal(_pass(cuda_lib, gl, h0, H), _composed(cuda_lib, gl, h0, H))
+
+
 def test_full_e2b_pass(cuda_lib):
     """35 E2B layers: deterministic, finite, RMS-normalised, and bitwise equal to
     the stage-by-stage composition whose stages are oracle-checked above."""
