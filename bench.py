@@ -458,7 +458,7 @@ def row_ple_q8(q4w, synth, dev, hbm, bf16_peak, reps=10, V=None):
     # fp16 operands: the measured bf16 peak (the same nominal dense rate)
     return {"GB/s": round(b / t / 1e9, 1), "frac": round(b / t / 1e9 / hbm, 4),
             "TFLOP/s": round(flops / t / 1e12, 2), "frac_f16": round(flops / t / 1e12 / bf16_peak, 4),
-            "bound": "hbm (int8 projection widened to fp16 tiles, kind::f16)", "us": round(t * 1e6, 2), "bytes": b,
+            "bound": "hbm (int8 projection widened to fp16 in tensor memory, kind::f16)", "us": round(t * 1e6, 2), "bytes": b,
             "copies": ncp}
 
 
