@@ -90,16 +90,42 @@ def e2b_step_bytes(layer_dims, H=1536):
     return wbytes, abytes
 
 
+def parse_clock_lines(lines, t_begin=None, t_end=None):
+    """Median SM clock, max clock and throttle reasons from nvidia-smi lines of
+    ClockSampler.FIELDS.  Only samples stamped within [t_begin, t_end]
+    (datetimes, local time) count; when none falls inside (a region shorter
+    than the sampling interval) every sample counts.  None when no line parses."""
+    import datetime
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    rows = []
+    for line in lines:
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+            rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
+        except ValueError:
+            continue
+    inside = [r for r in rows if (t_begin is None or r[0] >= t_begin) and (t_end is None or r[0] <= t_end)]
+    use = inside or rows
+    if not use:
+        return None
+    reasons = {n for r in use for n, v in zip(names, r[3]) if v.lower().startswith("active")}
+    return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+            "reasons": sorted(reasons), "samples": len(use)}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples every 200 ms (read-only)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index):
         self.proc = None
-        self.lines = []
+        self.t_begin = self.t_end = None
         try:
             import torch
             pr = torch.cuda.get_device_properties(device_index)
@@ -114,6 +140,15 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def begin(self):
+        """The timed region starts (samples before it are not counted)."""
+        import datetime
+        self.t_begin = datetime.datetime.now()
+
+    def end(self):
+        import datetime
+        self.t_end = datetime.datetime.now()
+
     def stop(self):
         if self.proc is None:
             return None
@@ -124,24 +159,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return parse_clock_lines(out.splitlines(), self.t_begin, self.t_end)
 
 
 def dist_setup():
@@ -235,14 +253,20 @@ def run_ours(args, world, rank, local):
             torch.distributed.barrier()
 
     sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)   # nvidia-smi starts before the timed region, not inside it
     barrier()
     torch.cuda.synchronize()
+    if sampler:
+        sampler.begin()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
         plan.step_device()
     ev1.record(stream)
     torch.cuda.synchronize()
+    if sampler:
+        sampler.end()
     barrier()
     clocks = sampler.stop() if sampler else None
     elapsed = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
