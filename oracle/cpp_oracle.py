@@ -57,6 +57,14 @@ _SIGS = {
     "q4o_e2b_layer_dims": (None, [_i, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "q4o_e2b_layer": (None, [_p, _i, ctypes.POINTER(_Mat), _i, _i, _i, _d] + [_p] * 11 + [_i]),
     "q4o_e2b_pass": (None, [_p, _i, ctypes.POINTER(_Mat), _p, _i, _d, _p, _i]),
+    "q4o_q2_gemv": (None, [_p, _p, _p, _i, _i, _i, _p, _i]),
+    "q4o_q8_quantize": (_i, [_p, _i, _i, _p, _p]),
+    "q4o_q8_dequantize": (None, [_p, _p, _i, _i, _p]),
+    "q4o_ple_q8": (_i, [_p, _i, _p, _p, _i, _i, _i, _f, _p, _p, _p, _i, _p, _d, _p, _p, _i]),
+    "q4o_a8_calibrate": (_f, [_p, _ll]),
+    "q4o_a8_quantize": (None, [_p, _ll, _f, _p]),
+    "q4o_gemv_a8": (None, [_p, _p, _p, _i, _i, _f, _p, _i]),
+    "q4o_gemm_chunk_a8": (None, [_p, _p, _p, _i, _i, _i, _f, _p, _i]),
 }
 
 
@@ -253,6 +261,118 @@ class Oracle:
                            eps=1e-6, threads=1):
         out, gathered = self.ple64(ids, table, row_scale, proj, hidden_f16, norm_w, L, ld, embed_scale, eps, threads)
         return out.astype(np.float32), gathered
+
+    # NEXT-2: INT2 per-row symmetric GEMV (oracle.q2_oracle's API)
+    def q2_gemv(self, codes, scales, x_f16, threads=1):
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        scales = np.ascontiguousarray(scales, dtype=np.float32)
+        x = np.ascontiguousarray(x_f16, dtype=np.float16)
+        N, K = codes.shape[0], codes.shape[1] * 4
+        B = 1 if x.ndim == 1 else x.shape[0]
+        if x.size != B * K or scales.size != N:
+            raise ValueError("INT2 operand shapes disagree")
+        y = np.empty((B, N), dtype=np.float64)
+        self.lib.q4o_q2_gemv(_ptr(codes), _ptr(scales), _ptr(x.view(np.uint16)), N, K, B, _ptr(y), _threads(threads))
+        return y[0] if x.ndim == 1 else y
+
+    # NEXT-4: int8 per-block-32 weights (oracle.q8_oracle's API)
+    def quantize_q8_0(self, W):
+        W = np.ascontiguousarray(W, dtype=np.float32)
+        if W.ndim != 2 or W.shape[1] % 32:
+            raise ValueError("W must be [N, K] with K a multiple of 32")
+        N, K = W.shape
+        codes = np.empty((N, K), dtype=np.int8)
+        scales = np.empty((N, K // 32), dtype=np.uint16)
+        st = self.lib.q4o_q8_quantize(_ptr(W), N, K, _ptr(codes), _ptr(scales))
+        if st == 2:
+            raise ValueError("non-finite weight")
+        if st == 3:
+            raise ValueError("block scale overflows fp16")
+        if st != 0:
+            raise ValueError(f"quantize failed ({st})")
+        return codes, scales
+
+    def dequantize_q8_0(self, codes, scales):
+        codes = np.ascontiguousarray(codes, dtype=np.int8)
+        scales = np.ascontiguousarray(scales, dtype=np.uint16)
+        N, K = codes.shape
+        out = np.empty((N, K), dtype=np.float64)
+        self.lib.q4o_q8_dequantize(_ptr(codes), _ptr(scales), N, K, _ptr(out))
+        return out
+
+    def ple_gather_project_q8(self, ids, table, row_scale, codes, scales, hidden_f16, norm_w, L=35, ld=256,
+                              embed_scale=None, eps=1e-6, threads=1):
+        ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+        table = np.ascontiguousarray(table, dtype=np.int8)
+        V, PLD = table.shape
+        codes = np.ascontiguousarray(codes, dtype=np.int8)
+        scales = np.ascontiguousarray(scales, dtype=np.uint16)
+        row_scale = np.ascontiguousarray(row_scale, dtype=np.float32)
+        hidden = np.ascontiguousarray(np.atleast_2d(hidden_f16), dtype=np.float16)
+        norm_w = np.ascontiguousarray(norm_w, dtype=np.float32)
+        S, D = ids.size, codes.shape[1]
+        if (PLD != L * ld or codes.shape[0] != L * ld or scales.size != L * ld * D // 32 or hidden.shape != (S, D)
+                or norm_w.size != ld or row_scale.size != V):
+            raise ValueError("PLE operand shapes disagree")
+        out = np.empty((S, L * ld), dtype=np.float64)
+        gathered = np.empty((S, L * ld), dtype=np.int8)
+        es = self.PLE_EMBED_SCALE if embed_scale is None else float(embed_scale)
+        st = self.lib.q4o_ple_q8(_ptr(ids), S, _ptr(table), _ptr(row_scale), V, L, ld, es, _ptr(codes),
+                                 _ptr(scales), _ptr(hidden.view(np.uint16)), D, _ptr(norm_w), float(eps), _ptr(out),
+                                 _ptr(gathered), _threads(threads))
+        if st != 0:
+            raise ValueError("token id out of range")
+        return out.astype(np.float32), gathered
+
+    # NEXT-4: w4a8 activation quantize/dequantize (oracle.a8_oracle's API)
+    def a8_calibrate(self, samples):
+        x = np.ascontiguousarray(np.asarray(samples, dtype=np.float16)).reshape(-1)
+        if not np.all(np.isfinite(x.astype(np.float32))):
+            raise ValueError("non-finite calibration sample")
+        return np.float32(self.lib.q4o_a8_calibrate(_ptr(x.view(np.uint16)), x.size))
+
+    @staticmethod
+    def _scale(s):
+        s32 = np.float32(s)
+        if not (np.isfinite(s32) and s32 > 0):
+            raise ValueError("the activation scale must be finite and > 0")
+        return float(s32)
+
+    def a8_quantize(self, x_f16, s):
+        x = np.ascontiguousarray(np.asarray(x_f16, dtype=np.float16))
+        if not np.all(np.isfinite(x.astype(np.float32))):
+            raise ValueError("non-finite activation")
+        q = np.empty(x.shape, dtype=np.int32)
+        self.lib.q4o_a8_quantize(_ptr(x.view(np.uint16)), x.size, self._scale(s), _ptr(q))
+        return q.astype(np.int64)
+
+    def a8_qdq(self, x_f16, s):
+        return self.a8_quantize(x_f16, s).astype(np.float64) * float(np.float32(s))
+
+    def q4_gemv_a8(self, codes, scales, x_f16, s, threads=1):
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        scales = np.ascontiguousarray(scales, dtype=np.uint16)
+        x = np.ascontiguousarray(x_f16, dtype=np.float16).reshape(-1)
+        N, K = codes.shape[0], codes.shape[1] * 2
+        if x.size != K:
+            raise ValueError("x must hold K values")
+        y = np.empty(N, dtype=np.float64)
+        self.lib.q4o_gemv_a8(_ptr(codes), _ptr(scales), _ptr(x.view(np.uint16)), N, K, self._scale(s), _ptr(y),
+                             _threads(threads))
+        return y.astype(np.float32)
+
+    def q4_gemm_chunk_a8(self, codes, scales, X_f16, s, threads=1):
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        scales = np.ascontiguousarray(scales, dtype=np.uint16)
+        X = np.ascontiguousarray(X_f16, dtype=np.float16)
+        N, K = codes.shape[0], codes.shape[1] * 2
+        M = X.shape[0]
+        if X.shape != (M, K):
+            raise ValueError("X must be [M, K]")
+        Y = np.empty((M, N), dtype=np.float64)
+        self.lib.q4o_gemm_chunk_a8(_ptr(codes), _ptr(scales), _ptr(X.view(np.uint16)), M, N, K, self._scale(s),
+                                   _ptr(Y), _threads(threads))
+        return Y.astype(np.float32)
 
     # a3
     def e2b_layer_dims(self, layer):

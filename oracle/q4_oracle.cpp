@@ -34,6 +34,19 @@
 //   R8 per layer: a = f16(RMSNorm(h)); q,k,v = W a; o = W_o f16(q);
 //      b = f16(RMSNorm(o)); g,u = W b; m = f16(gelu_tanh(g) * u);
 //      h' = f16(RMSNorm(W_d m)); k, v produced and not consumed.
+// The "next" rows, with the numpy oracles' readings:
+//   Q2 ("Gemma-4 E2B mobile mixed-bit QAT weights", decode recipe, P3, P6):
+//      4 codes per byte, the first in bits [1:0], value code - 2, one f32
+//      scale per row applied to the finished row sum;
+//   Q8 (same page, decode recipe and official-checkpoint notes): per block
+//      of 32, d = max |w| / 127 (fp32), code = clamp(round(w / d), -127,
+//      127) from the fp32 quotient, half away from zero, scale fp16(d); a
+//      zero block stores +0 and codes 0; the PLE on it is the f32 PLE on
+//      w' = fp16(d) * code;
+//   A8 ("visible-cx/gemma-4-E2B-CoreAI", About the w4a8 bundle): per-tensor
+//      symmetric, zero point 0, fp32 scale s; q = clamp(rint(x / s), -128,
+//      127) from the fp32 quotient, ties to even; x' = s q; min-max
+//      calibration s = max |x| / 127 (fp32), 1 when every x is zero.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -393,6 +406,139 @@ void q4o_e2b_pass(const uint16_t* h0, int H, const q4o_matrix* mats, const int* 
     h = hn;
   }
   std::memcpy(h_out, h.data(), sizeof(uint16_t) * H);
+}
+
+// --------------------------------------------------- NEXT-2 INT2 GEMV ---
+// codes [N][K/4], scales f32 [N], x fp16 bits [B][K]:
+// y[b][n] = scale[n] * sum_k (code - 2) * x[b][k], the sum in fp64, k order.
+void q4o_q2_gemv(const uint8_t* codes, const float* scales, const uint16_t* x, int N, int K, int B, double* y,
+                 int threads) {
+  std::vector<double> xv((size_t)B * K);
+  for (size_t i = 0; i < xv.size(); ++i) xv[i] = f16_value(x[i]);
+  parallel_rows(N, threads, [&](int lo, int hi) {
+    for (int n = lo; n < hi; ++n)
+      for (int b = 0; b < B; ++b) {
+        double acc = 0.0;
+        for (int k = 0; k < K; ++k) {
+          const int c = (codes[(size_t)n * (K / 4) + k / 4] >> (2 * (k % 4))) & 3;
+          acc += (double)(c - 2) * xv[(size_t)b * K + k];
+        }
+        y[(size_t)b * N + n] = (double)scales[n] * acc;
+      }
+  });
+}
+
+// ---------------------------------------- NEXT-4 int8 per-block-32 weights ---
+// W fp32 [N][K] -> codes int8 [N][K], fp16 scale bits [N][K/32].
+// 0 ok; 1 K not a multiple of 32; 2 a non-finite weight; 3 a scale beyond fp16.
+int q4o_q8_quantize(const float* W, int N, int K, int8_t* codes, uint16_t* scales) {
+  if (N < 0 || K <= 0 || K % 32) return 1;
+  for (long long i = 0; i < (long long)N * K; ++i)
+    if (!std::isfinite(W[i])) return 2;
+  const int nb = K / 32;
+  for (long long i = 0; i < (long long)N * nb; ++i) {
+    float a = 0.0f;
+    for (int t = 0; t < 32; ++t) a = std::fmax(a, std::fabs(W[i * 32 + t]));
+    if (a / 127.0f > 65504.0f) return 3;
+  }
+  for (int n = 0; n < N; ++n)
+    for (int j = 0; j < nb; ++j) {
+      const float* blk = W + (size_t)n * K + 32 * j;
+      float a = 0.0f;
+      for (int i = 0; i < 32; ++i) a = std::fmax(a, std::fabs(blk[i]));
+      const float d32 = a / 127.0f;                     // IEEE fp32 quotient
+      scales[(size_t)n * nb + j] = f16_bits((double)d32);
+      for (int i = 0; i < 32; ++i) {
+        double c = 0.0;
+        if (d32 != 0.0f) {
+          const float ratio = blk[i] / d32;             // IEEE fp32 quotient
+          c = std::round((double)ratio);                // half away from zero
+          if (c < -127.0) c = -127.0;
+          if (c > 127.0) c = 127.0;
+        }
+        codes[(size_t)n * K + 32 * j + i] = (int8_t)c;
+      }
+    }
+  return 0;
+}
+
+// w' = fp16(d) * code, exact in double.
+void q4o_q8_dequantize(const int8_t* codes, const uint16_t* scales, int N, int K, double* Wd) {
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < K; ++k)
+      Wd[(size_t)n * K + k] = f16_value(scales[(size_t)n * (K / 32) + k / 32]) * (double)codes[(size_t)n * K + k];
+}
+
+// The PLE with the int8 projection: the f32 PLE on w' (exact in fp32: an
+// 11-bit scale times an 8-bit code).
+int q4o_ple_q8(const int32_t* ids, int S, const int8_t* table, const float* row_scale, int V, int L, int ld,
+               float embed_scale, const int8_t* codes, const uint16_t* scales, const uint16_t* hidden, int D,
+               const float* norm_w, double eps, double* out, int8_t* gathered, int threads) {
+  const int R = L * ld;
+  std::vector<double> wd((size_t)R * D);
+  q4o_q8_dequantize(codes, scales, R, D, wd.data());
+  std::vector<float> proj(wd.size());
+  for (size_t i = 0; i < wd.size(); ++i) proj[i] = (float)wd[i];
+  return q4o_ple(ids, S, table, row_scale, V, L, ld, embed_scale, proj.data(), hidden, D, norm_w, eps, out, gathered,
+                 threads);
+}
+
+// ------------------------------------------------ NEXT-4 w4a8 activations ---
+// Min-max calibration over n fp16 values.
+float q4o_a8_calibrate(const uint16_t* x, long long n) {
+  float amax = 0.0f;
+  for (long long i = 0; i < n; ++i) amax = std::fmax(amax, (float)std::fabs(f16_value(x[i])));
+  return amax > 0.0f ? amax / 127.0f : 1.0f;
+}
+
+// q[i] = clamp(rint(x[i] / s), -128, 127), the quotient in fp32, ties to even.
+void q4o_a8_quantize(const uint16_t* x, long long n, float s, int32_t* q) {
+  for (long long i = 0; i < n; ++i) {
+    const float r = (float)f16_value(x[i]) / s;
+    double c = std::nearbyint((double)r);               // round to nearest, ties to even
+    if (c < -128.0) c = -128.0;
+    if (c > 127.0) c = 127.0;
+    q[i] = (int32_t)c;
+  }
+}
+
+// y[n] = sum_k w'[n][k] * x'[k], x' = s q, fp64 in k order.
+void q4o_gemv_a8(const uint8_t* codes, const uint16_t* scales, const uint16_t* x, int N, int K, float s, double* y,
+                 int threads) {
+  std::vector<int32_t> q(K);
+  q4o_a8_quantize(x, K, s, q.data());
+  std::vector<double> xd(K);
+  for (int k = 0; k < K; ++k) xd[k] = (double)q[k] * (double)s;
+  parallel_rows(N, threads, [&](int lo, int hi) {
+    for (int n = lo; n < hi; ++n) {
+      double acc = 0.0;
+      for (int k = 0; k < K; ++k) acc += weight_at(codes, scales, K, n, k) * xd[k];
+      y[n] = acc;
+    }
+  });
+}
+
+// Y[t][n] = sum_k bf16(w'[n][k]) * x'[t][k], x' = s q, fp64 in k order.
+void q4o_gemm_chunk_a8(const uint8_t* codes, const uint16_t* scales, const uint16_t* X, int M, int N, int K, float s,
+                       double* Y, int threads) {
+  std::vector<int32_t> q((size_t)M * K);
+  q4o_a8_quantize(X, (long long)M * K, s, q.data());
+  std::vector<double> xd(q.size());
+  for (size_t i = 0; i < q.size(); ++i) xd[i] = (double)q[i] * (double)s;
+  parallel_rows(N, threads, [&](int lo, int hi) {
+    std::vector<double> wt(K);
+    for (int n = lo; n < hi; ++n) {
+      for (int k = 0; k < K; ++k) {
+        const float w32 = (float)weight_at(codes, scales, K, n, k);   // exact: 11 by 4 bits
+        wt[k] = (double)bf16_round(w32);
+      }
+      for (int t = 0; t < M; ++t) {
+        double acc = 0.0;
+        for (int k = 0; k < K; ++k) acc += wt[k] * xd[(size_t)t * K + k];
+        Y[(size_t)t * N + n] = acc;
+      }
+    }
+  });
 }
 
 }  // extern "C"
