@@ -88,6 +88,51 @@ def test_a8_codes_calibration_and_products(C):
     _same_fp32(C.q4_gemm_chunk_a8(codes, scales, X, s, threads=3), A8.q4_gemm_chunk_a8(codes, scales, X, s))
 
 
+# INT2 GEMV pins over any oracle object with q2_gemv (fixtures packed with
+# the numpy oracle's pack_q2): what the pages fix about the format.
+def pin_q2_bit_order_and_midpoint(M):
+    """Byte 0b11100100 holds codes 0, 1, 2, 3 for columns 0..3 (the first code
+    in bits [1:0]); column j alone gives scale * (code_j - 2)."""
+    c = np.full((1, 1), 0xE4, dtype=np.uint8)
+    s = np.array([0.5], dtype=np.float32)
+    for j in range(4):
+        x = np.zeros(4, np.float16)
+        x[j] = 1.0
+        assert float(M.q2_gemv(c, s, x)[0]) == 0.5 * (j - 2)
+
+
+def pin_q2_constant_codes(M):
+    """Codes all 2 give 0, all 3 give scale * sum(x), all 0 give -2 scale * sum(x)."""
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((2, 64)).astype(np.float16)
+    s = np.array([0.5, 3.0, 0.01], dtype=np.float32)
+    sx = x.astype(np.float64).sum(axis=1)
+    for code, factor in ((2, 0.0), (3, 1.0), (0, -2.0)):
+        y = M.q2_gemv(Q2.pack_q2(np.full((3, 64), code, dtype=np.uint8)), s, x)
+        assert np.allclose(y, factor * sx[:, None] * s.astype(np.float64)[None, :], rtol=0, atol=1e-12)
+
+
+def pin_q2_row_scale_bruteforce(M):
+    """One scale per row, on that row's sum only."""
+    rng = np.random.default_rng(9)
+    q = rng.integers(0, 4, size=(3, 8), dtype=np.uint8)
+    s = np.array([2.0, -0.5, 0.25], dtype=np.float32)
+    x = rng.standard_normal(8).astype(np.float16)
+    y = M.q2_gemv(Q2.pack_q2(q), s, x)
+    for n in range(3):
+        acc = sum((int(q[n, k]) - 2) * float(x[k]) for k in range(8))
+        assert abs(float(y[n]) - float(s[n]) * acc) <= 1e-12 * max(1.0, abs(acc))
+
+
+Q2_PINS = [pin_q2_bit_order_and_midpoint, pin_q2_constant_codes, pin_q2_row_scale_bruteforce]
+
+
+@pytest.mark.parametrize("pin", Q2_PINS, ids=[p.__name__ for p in Q2_PINS])
+def test_q2_pins_on_both(C, pin):
+    pin(Q2)
+    pin(C)
+
+
 @pytest.mark.parametrize("pin", TQ8.PINS, ids=[p.__name__ for p in TQ8.PINS])
 def test_q8_pins_on_cpp(C, pin):
     pin(C)
@@ -101,6 +146,10 @@ def test_a8_pins_on_cpp(C, pin):
 # Planted mistakes in the C++ oracle's "next" rows (textual edits of a copy,
 # compiled with the oracle's flags): some int8 or w4a8 pin must reject each.
 NEXT_MUTANTS = [
+    ("q2 last code in bits [1:0]", "(codes[(size_t)n * (K / 4) + k / 4] >> (2 * (k % 4))) & 3",
+     "(codes[(size_t)n * (K / 4) + k / 4] >> (2 * (3 - k % 4))) & 3"),
+    ("q2 midpoint 1", "acc += (double)(c - 2) * xv[(size_t)b * K + k];",
+     "acc += (double)(c - 1) * xv[(size_t)b * K + k];"),
     ("q8 ties to even", "c = std::round((double)ratio);                // half away from zero",
      "c = std::nearbyint((double)ratio);"),
     ("q8 step max/128", "const float d32 = a / 127.0f;                     // IEEE fp32 quotient",
@@ -127,7 +176,7 @@ def test_some_pin_rejects_next_row_cpp_mutant(mutant, tmp_path):
         f.write(src.replace(old, new))
     lib_path = cpp_oracle.build(force=True, src=mut_src, out=os.path.join(tmp_path, "libmutant.so"))
     mod = cpp_oracle.Oracle(cpp_oracle.load(lib_path))
-    for pin in TQ8.PINS + TA8.PINS:
+    for pin in TQ8.PINS + TA8.PINS + Q2_PINS:
         try:
             pin(mod)
         except Exception:   # any failure or crash counts as the pin biting
